@@ -1,0 +1,257 @@
+"""Seeded synthetic inputs for softmax-threshold block-skipping attention.
+
+This module only draws numbers: it holds none of the attention arithmetic, so
+both the CUDA path and the fp64 oracle may read what it produces.
+
+Planted-salience recipe (one draw per KV head, independent across heads):
+
+* ``u`` is a seeded random unit vector scaled to length ``sqrt(d)``;
+* keys ``K_j = N(0, I) + a_j * u`` with ``a_0 = sink_a`` (an attention sink),
+  ``a_j = salient_a`` on a seeded fraction of the positions ``1..T-1`` drawn
+  without replacement, ``a_j = 0`` elsewhere;
+* queries ``Q_i = N(0, I) + u`` (every query head of the group uses its KV
+  head's ``u``), values ``V ~ N(0, 1)``;
+* optional local band (long prefill): query tile ``t`` adds ``w_t`` and key
+  block ``b`` adds ``band_a * (w_b + w_{b+1})``, so tile ``t`` sees about
+  ``+band_a * sqrt(d)`` on the scores of blocks ``t-1`` and ``t`` (its 256
+  nearest keys at 128-wide blocks).  The ``w`` are seeded ``N(0, I)`` draws
+  made orthogonal to ``u``;
+* bf16 configurations round every element to bf16 (round to nearest even).
+
+Heavy-tailed score distributions of this kind stand in for the long-context
+benchmarks the BLASST page evaluates on (RULER, LongBench), which are not
+available here.  Each (tensor, batch, head) slice has its own generator keyed
+by (seed, tensor tag, batch, head), so any head can be regenerated alone and
+slices can be drawn in parallel.
+"""
+from __future__ import annotations
+
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+from dataclasses import dataclass, replace
+
+import torch
+
+_TAGS = {"u": 1, "sal": 2, "k": 3, "v": 4, "q": 5, "w": 6}
+
+
+def _gen(seed: int, tag: str, b: int, h: int) -> torch.Generator:
+    # A fixed mixing of the key into one 63-bit seed (splitmix64 finaliser).
+    x = (seed * 0x9E3779B97F4A7C15 + _TAGS[tag] * 0xBF58476D1CE4E5B9
+         + b * 0x94D049BB133111EB + h * 0xD6E8FEB86659FD93 + 0x632BE59BD9B4E019)
+    x &= (1 << 64) - 1
+    x ^= x >> 30
+    x = (x * 0xBF58476D1CE4E5B9) & ((1 << 64) - 1)
+    x ^= x >> 27
+    x = (x * 0x94D049BB133111EB) & ((1 << 64) - 1)
+    x ^= x >> 31
+    return torch.Generator().manual_seed(x & ((1 << 63) - 1))
+
+
+def _threads() -> int:
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+@dataclass(frozen=True)
+class PrefillConfig:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    T: int
+    d: int
+    dtype: str  # "bf16" or "f32"
+    Br: int = 128
+    Bc: int = 128
+    causal: bool = True
+    salient_frac: float = 0.02
+    sink_a: float = 6.0
+    salient_a: float = 3.0
+    band_a: float = 0.0
+    seed: int = 1234
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def n_t(self) -> int:
+        return -(-self.T // self.Br)
+
+    @property
+    def n_b(self) -> int:
+        return -(-self.T // self.Bc)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def with_(self, **kw) -> "PrefillConfig":
+        return replace(self, **kw)
+
+
+@dataclass(frozen=True)
+class DecodeConfig:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    L: int
+    dk: int
+    dv: int
+    dtype: str
+    Bc: int = 128
+    n_splits: int = 8
+    latent: bool = False  # V is the first dv columns of K (absorbed MLA)
+    salient_frac: float = 0.02
+    sink_a: float = 6.0
+    salient_a: float = 3.0
+    seed: int = 1234
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def n_b(self) -> int:
+        return -(-self.L // self.Bc)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.dk)
+
+    def with_(self, **kw) -> "DecodeConfig":
+        return replace(self, **kw)
+
+
+# The five workloads: shapes follow the attention layers of the models the
+# BLASST page evaluates (Llama-3.1-8B GQA 32/8 heads, d=128; DeepSeek-style
+# absorbed MLA with a 512+64 latent).
+TINY_PREFILL = PrefillConfig("tiny_prefill_f32_T1024", 1, 1, 1, 1024, 64, "f32", seed=1234)
+GQA_PREFILL_16K = PrefillConfig("gqa_prefill_bf16_T16384", 1, 32, 8, 16384, 128, "bf16", seed=1235)
+GQA_DECODE_32K = DecodeConfig("gqa_decode_bf16_B16_L32768", 16, 32, 8, 32768, 128, 128, "bf16",
+                              Bc=128, n_splits=8, seed=1236)
+GQA_PREFILL_64K = PrefillConfig("gqa_prefill_bf16_T65536_band", 1, 32, 8, 65536, 128, "bf16",
+                                salient_frac=0.01, band_a=2.0, seed=1237)
+MLA_DECODE_16K = DecodeConfig("mla_decode_bf16_B32_L16384", 32, 128, 1, 16384, 576, 512, "bf16",
+                              Bc=64, n_splits=16, latent=True, seed=1238)
+
+CONFIGS = {c.name: c for c in (TINY_PREFILL, GQA_PREFILL_16K, GQA_DECODE_32K, GQA_PREFILL_64K,
+                                MLA_DECODE_16K)}
+
+
+def _unit_u(seed: int, b: int, hk: int, d: int) -> torch.Tensor:
+    u = torch.randn(d, generator=_gen(seed, "u", b, hk), dtype=torch.float64)
+    return (u / u.norm() * math.sqrt(d)).to(torch.float32)
+
+
+def _salience(seed: int, b: int, hk: int, T: int, frac: float, sink_a: float,
+              salient_a: float) -> torch.Tensor:
+    a = torch.zeros(T, dtype=torch.float32)
+    if T > 0:
+        a[0] = sink_a
+    n_sal = int(round(frac * max(T - 1, 0)))
+    if n_sal > 0:
+        perm = torch.randperm(T - 1, generator=_gen(seed, "sal", b, hk))[:n_sal] + 1
+        a[perm] = salient_a
+    return a
+
+
+def _band_vectors(seed: int, b: int, hk: int, n: int, d: int, u: torch.Tensor) -> torch.Tensor:
+    w = torch.randn(n, d, generator=_gen(seed, "w", b, hk), dtype=torch.float32)
+    un = u / u.norm()
+    return w - (w @ un)[:, None] * un[None, :]
+
+
+def _finish(x: torch.Tensor, dtype: str) -> torch.Tensor:
+    return x.to(torch.bfloat16) if dtype == "bf16" else x.contiguous()
+
+
+def prefill_inputs(cfg: PrefillConfig, heads=None):
+    """Return ``(q, k, v)`` as CPU tensors in ``[B, H, T, d]`` layout.
+
+    ``heads`` optionally restricts generation to a list of KV-head indices
+    (the other heads are left as zeros); a restricted draw reproduces exactly
+    the slices of a full draw.
+    """
+    B, Hq, Hkv, T, d, G = cfg.B, cfg.Hq, cfg.Hkv, cfg.T, cfg.d, cfg.G
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    q = torch.zeros(B, Hq, T, d, dtype=tdt)
+    k = torch.zeros(B, Hkv, T, d, dtype=tdt)
+    v = torch.zeros(B, Hkv, T, d, dtype=tdt)
+    hks = range(Hkv) if heads is None else heads
+
+    def one(job):
+        b, hk = job
+        u = _unit_u(cfg.seed, b, hk, d)
+        a = _salience(cfg.seed, b, hk, T, cfg.salient_frac, cfg.sink_a, cfg.salient_a)
+        kk = torch.randn(T, d, generator=_gen(cfg.seed, "k", b, hk)) + a[:, None] * u[None, :]
+        band_q = None
+        if cfg.band_a != 0.0:
+            nb = cfg.n_b
+            w = _band_vectors(cfg.seed, b, hk, nb + 1, d, u)
+            wk = cfg.band_a * (w[:-1] + w[1:])  # [n_b, d]
+            kk += wk.repeat_interleave(cfg.Bc, dim=0)[:T]
+            band_q = w[: cfg.n_t].repeat_interleave(cfg.Br, dim=0)[:T]
+        k[b, hk] = _finish(kk, cfg.dtype)
+        v[b, hk] = _finish(torch.randn(T, d, generator=_gen(cfg.seed, "v", b, hk)), cfg.dtype)
+        for g in range(G):
+            h = hk * G + g
+            qq = torch.randn(T, d, generator=_gen(cfg.seed, "q", b, h)) + u[None, :]
+            if band_q is not None:
+                qq += band_q
+            q[b, h] = _finish(qq, cfg.dtype)
+
+    jobs = [(b, hk) for b in range(B) for hk in hks]
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(one, jobs))
+    return q, k, v
+
+
+def decode_inputs(cfg: DecodeConfig, batches=None):
+    """Return ``(q, k, v)``: q ``[B, Hq, dk]``, k ``[B, Hkv, L, dk]``.
+
+    For a latent (MLA) configuration ``v`` is ``None``: the values are the
+    first ``dv`` columns of ``k``.  ``batches`` restricts generation to a list
+    of batch indices (others stay zero).
+    """
+    B, Hq, Hkv, L, dk, dv, G = cfg.B, cfg.Hq, cfg.Hkv, cfg.L, cfg.dk, cfg.dv, cfg.G
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    q = torch.zeros(B, Hq, dk, dtype=tdt)
+    k = torch.zeros(B, Hkv, L, dk, dtype=tdt)
+    v = None if cfg.latent else torch.zeros(B, Hkv, L, dv, dtype=tdt)
+    bs = range(B) if batches is None else batches
+
+    def one(job):
+        b, hk = job
+        u = _unit_u(cfg.seed, b, hk, dk)
+        a = _salience(cfg.seed, b, hk, L, cfg.salient_frac, cfg.sink_a, cfg.salient_a)
+        kk = torch.randn(L, dk, generator=_gen(cfg.seed, "k", b, hk)) + a[:, None] * u[None, :]
+        k[b, hk] = _finish(kk, cfg.dtype)
+        if v is not None:
+            v[b, hk] = _finish(torch.randn(L, dv, generator=_gen(cfg.seed, "v", b, hk)), cfg.dtype)
+        for g in range(G):
+            h = hk * G + g
+            qq = torch.randn(dk, generator=_gen(cfg.seed, "q", b, h)) + u
+            q[b, h] = _finish(qq, cfg.dtype)
+
+    jobs = [(b, hk) for b in bs for hk in range(Hkv)]
+    with ThreadPoolExecutor(_threads()) as ex:
+        list(ex.map(one, jobs))
+    return q, k, v
+
+
+def temperate(cfg):
+    """The same recipe with half-strength sink and salience (3 and 1.5), so
+    outputs are true mixtures of many value rows and thresholds from 1e-3 to
+    0.3 give intermediate block sparsity (a test-only variant)."""
+    kw = dict(sink_a=3.0, salient_a=1.5)
+    if isinstance(cfg, PrefillConfig) and cfg.band_a:
+        kw["band_a"] = 1.0
+    return cfg.with_(**kw)
+
+
+def as_f32(x: torch.Tensor) -> torch.Tensor:
+    """Exact fp32 copy of a bf16/f32 tensor (bf16 values are fp32-representable)."""
+    return x.to(torch.float32).contiguous()

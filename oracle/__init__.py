@@ -1,0 +1,207 @@
+"""fp64 CPU oracle for softmax-threshold block-skipping attention.
+
+TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / reference leg of ``bench.py`` may import this package.  The
+library under ``block_sparse_attention_online_gb300`` never does.
+
+The arithmetic lives in ``oracle.c`` (plain C, fp64, OpenMP over independent
+query tiles or decode splits); this module only marshals numpy arrays.  It
+follows the BLASST page ("BLASST：一个标量阈值实现的动态块稀疏注意力", sections
+"铺垫：FlashAttention 的在线 softmax" and "BLASST 的判定准则") step by step.
+
+Parity status of each function (what pins it, in ``tests/test_oracle.py``):
+
+* ``dense_prefill`` / ``dense_decode``: brute-force numpy softmax on tiny
+  inputs, and torch's fp64 ``scaled_dot_product_attention`` on CPU.
+* ``prefill`` / ``decode``: lambda = 0 equals dense attention; the closed form
+  "softmax restricted to the kept tokens"; the champion rule (the block holding
+  a row's maximum is never skipped); every skipped token has softmax weight
+  below lambda; the output error bound; hand-worked fixtures under
+  ``tests/golden/``; brute-force recomputation of each skip bit.
+* ``combine``: lambda = 0 merged decode equals dense single-pass attention;
+  one split is the identity.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libbsa_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` with gcc (fp64, no fast-math, no FMA contraction)."""
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-ffp-contract=off",
+           "-fno-fast-math", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        i, d, i64 = ctypes.c_int, ctypes.c_double, ctypes.c_int64
+        lib.bsa_oracle_dense_prefill.argtypes = [P, P, P, i, i, i, i, i, i, d, i, P, i64, P, P]
+        lib.bsa_oracle_dense_decode.argtypes = [P, P, P, i, i, i, i, i, i, i64, i64, d, P, P]
+        lib.bsa_oracle_prefill.argtypes = [P, P, P, i, i, i, i, i, i, d, d, i, i, i, P, i64,
+                                           P, P, P, P]
+        lib.bsa_oracle_decode.argtypes = [P, P, P, i, i, i, i, i, i, i64, i64, d, d, i, i, P,
+                                          i64, P, P, P, P]
+        lib.bsa_oracle_combine.argtypes = [P, P, i, i, i, i, P, P]
+        for f in ("bsa_oracle_dense_prefill", "bsa_oracle_dense_decode", "bsa_oracle_prefill",
+                  "bsa_oracle_decode", "bsa_oracle_combine", "bsa_oracle_num_threads"):
+            getattr(lib, f).restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    return _load().bsa_oracle_num_threads()
+
+
+def _f32(x) -> np.ndarray:
+    """Exact fp32 numpy copy of a torch tensor (bf16 widens exactly) or array."""
+    if hasattr(x, "detach"):
+        import torch
+        x = x.detach().to("cpu", torch.float32).numpy()
+    return np.ascontiguousarray(x, dtype=np.float32)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _units(units):
+    if units is None:
+        return None, 0
+    u = np.ascontiguousarray(np.asarray(units, dtype=np.int64).ravel())
+    return u, u.size
+
+
+def dense_prefill(q, k, v, scale, causal=True, rows=None):
+    """Exact softmax attention; q [B,Hq,T,dk], k [B,Hkv,T,dk], v [B,Hkv,T,dv].
+
+    Returns ``(y [B,Hq,T,dv], lse [B,Hq,T])`` in fp64 (only ``rows`` — flat
+    indices into [B,Hq,T] — are filled when given)."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, Hq, T, dk = q.shape
+    Hkv, dv = k.shape[1], v.shape[3]
+    y = np.zeros((B, Hq, T, dv))
+    lse = np.full((B, Hq, T), np.nan)
+    r, nr = _units(rows)
+    rc = _load().bsa_oracle_dense_prefill(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, T, dk, dv,
+                                          float(scale), int(bool(causal)),
+                                          None if r is None else _ptr(r), nr, _ptr(y), _ptr(lse))
+    if rc:
+        raise ValueError("bsa_oracle_dense_prefill: invalid arguments")
+    return y, lse
+
+
+def dense_decode(q, k, v, scale, dv=None):
+    """Exact softmax attention for one query token per sequence.
+
+    q [B,Hq,dk]; k [B,Hkv,L,dk]; v [B,Hkv,L,dv] or ``None`` for a latent cache
+    whose values are the first ``dv`` columns of k."""
+    q, k = _f32(q), _f32(k)
+    B, Hq, dk = q.shape
+    _, Hkv, L, kstride = k.shape
+    if v is None:
+        vv, vstride = k, kstride
+    else:
+        vv = _f32(v)
+        dv, vstride = vv.shape[3], vv.shape[3]
+    y = np.zeros((B, Hq, dv))
+    lse = np.zeros((B, Hq))
+    rc = _load().bsa_oracle_dense_decode(_ptr(q), _ptr(k), _ptr(vv), B, Hq, Hkv, L, dk, dv,
+                                         kstride, vstride, float(scale), _ptr(y), _ptr(lse))
+    if rc:
+        raise ValueError("bsa_oracle_dense_decode: invalid arguments")
+    return y, lse
+
+
+def prefill(q, k, v, scale, lam, Br=128, Bc=128, causal=True, units=None):
+    """Thresholded online-softmax prefill in fp64.
+
+    Returns a dict with ``o`` [B,Hq,T,dv], ``lse`` [B,Hq,T], ``skip``
+    [B,Hq,n_t,n_b] (uint8, 1 = skipped) and ``margin`` [B,Hq,n_t,n_b] (the tile
+    statistic max_r(rowmax - m_new); NaN where not traversed).  ``units`` are
+    flat indices into [B,Hq,n_t]; only those tiles are computed."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, Hq, T, dk = q.shape
+    Hkv, dv = k.shape[1], v.shape[3]
+    n_t, n_b = -(-T // Br), -(-T // Bc)
+    o = np.zeros((B, Hq, T, dv))
+    lse = np.full((B, Hq, T), np.nan)
+    skip = np.zeros((B, Hq, n_t, n_b), dtype=np.uint8)
+    margin = np.full((B, Hq, n_t, n_b), np.nan)
+    u, nu = _units(units)
+    rc = _load().bsa_oracle_prefill(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, T, dk, dv,
+                                    float(scale), float(lam), Br, Bc, int(bool(causal)),
+                                    None if u is None else _ptr(u), nu, _ptr(o), _ptr(lse),
+                                    _ptr(skip), _ptr(margin))
+    if rc:
+        raise ValueError("bsa_oracle_prefill: invalid arguments")
+    return {"o": o, "lse": lse, "skip": skip, "margin": margin}
+
+
+def decode(q, k, v, scale, lam, Bc, n_splits, dv=None, units=None):
+    """Split-KV thresholded decode in fp64 (partials, before the merge).
+
+    Returns ``o_part`` [B,Hq,S,dv], ``lse_part`` [B,Hq,S], ``skip`` and
+    ``margin`` [B,Hkv,S,bps] with bps = ceil(n_b / S).  ``units`` are flat
+    indices into [B,Hkv,S]."""
+    q, k = _f32(q), _f32(k)
+    B, Hq, dk = q.shape
+    _, Hkv, L, kstride = k.shape
+    if v is None:
+        vv, vstride = k, kstride
+    else:
+        vv = _f32(v)
+        dv, vstride = vv.shape[3], vv.shape[3]
+    n_b = -(-L // Bc)
+    bps = -(-n_b // n_splits)
+    o_part = np.zeros((B, Hq, n_splits, dv))
+    lse_part = np.full((B, Hq, n_splits), np.nan)
+    skip = np.zeros((B, Hkv, n_splits, bps), dtype=np.uint8)
+    margin = np.full((B, Hkv, n_splits, bps), np.nan)
+    u, nu = _units(units)
+    rc = _load().bsa_oracle_decode(_ptr(q), _ptr(k), _ptr(vv), B, Hq, Hkv, L, dk, dv, kstride,
+                                   vstride, float(scale), float(lam), Bc, n_splits,
+                                   None if u is None else _ptr(u), nu, _ptr(o_part),
+                                   _ptr(lse_part), _ptr(skip), _ptr(margin))
+    if rc:
+        raise ValueError("bsa_oracle_decode: invalid arguments")
+    return {"o_part": o_part, "lse_part": lse_part, "skip": skip, "margin": margin}
+
+
+def combine(o_part, lse_part):
+    """LSE merge of split partials: returns ``(o [B,Hq,dv], lse [B,Hq])``."""
+    o_part = np.ascontiguousarray(o_part, dtype=np.float64)
+    lse_part = np.ascontiguousarray(lse_part, dtype=np.float64)
+    B, Hq, S, dv = o_part.shape
+    o = np.zeros((B, Hq, dv))
+    lse = np.zeros((B, Hq))
+    rc = _load().bsa_oracle_combine(_ptr(o_part), _ptr(lse_part), B, Hq, S, dv, _ptr(o), _ptr(lse))
+    if rc:
+        raise ValueError("bsa_oracle_combine: invalid arguments")
+    return o, lse
+
+
+def ln_lambda(lam: float) -> float:
+    return math.log(lam) if lam > 0 else -math.inf
