@@ -1,0 +1,190 @@
+"""ctypes binding of ``libattn_skip.so`` (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of its own: it checks tensor placement, allocates the outputs with
+torch (device memory is plumbing), passes raw pointers and the current CUDA
+stream, and raises :class:`AttnSkipError` on a non-OK status.  There is no CPU
+fallback: without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build",
+                         "libattn_skip.so")
+_lib = None
+
+ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT = range(5)
+ATTN_BF16, ATTN_F32 = 0, 1
+
+#: Every symbol include/attn_skip.h declares.
+EXPORTED = ("attn_skip_prefill", "attn_skip_decode", "attn_skip_decode_combine",
+            "attn_skip_last_device_error", "attn_skip_status_string")
+
+
+class AttnSkipError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load the library (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"{_LIB_PATH} is missing: build it with "
+                           "`python -m block_sparse_attention_online_gb300.build`")
+    lib = ctypes.CDLL(_LIB_PATH)
+    P, i, f, d, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_int64
+    lib.attn_skip_prefill.argtypes = [P, P, P, i, i, i, i, i, i, i, f, d, i, i, i, P, P, P, P]
+    lib.attn_skip_decode.argtypes = [P, P, P, i, i, i, i, i, i, i, i64, i64, f, d, i, i, P, P, P,
+                                     P]
+    lib.attn_skip_decode_combine.argtypes = [P, P, i, i, i, i, i, P, P, P]
+    lib.attn_skip_last_device_error.argtypes = [P]
+    lib.attn_skip_status_string.argtypes = [i]
+    lib.attn_skip_status_string.restype = ctypes.c_char_p
+    for fn in ("attn_skip_prefill", "attn_skip_decode", "attn_skip_decode_combine",
+               "attn_skip_last_device_error"):
+        getattr(lib, fn).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().attn_skip_status_string(int(status)).decode()
+
+
+attn_skip_status_string = status_string
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float32:
+        return ATTN_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check(fn: str, status: int):
+    if status != ATTN_OK:
+        raise AttnSkipError(fn, status)
+
+
+def _cuda_contig(*ts):
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def prefill_bitmap_shape(B, Hq, T, Br, Bc):
+    n_t, n_b = -(-T // Br), -(-T // Bc)
+    return (B, Hq, n_t, -(-n_b // 32))
+
+
+def decode_bitmap_shape(B, Hkv, L, Bc, n_splits):
+    n_b = -(-L // Bc)
+    bps = -(-n_b // n_splits)
+    return (B, Hkv, n_splits, -(-bps // 32))
+
+
+def attn_skip_prefill(q, k, v, lam, Br=128, Bc=128, causal=True, scale=0.0, out=None,
+                      stream=None):
+    """q [B,Hq,T,dk], k [B,Hkv,T,dk], v [B,Hkv,T,dv] on one CUDA device.
+
+    Returns ``(o, lse, skip_bits)``; ``out`` may pass preallocated
+    ``(o, lse, skip_bits)`` tensors."""
+    _cuda_contig(q, k, v)
+    B, Hq, T, dk = q.shape
+    Hkv, dv = k.shape[1], v.shape[3]
+    if out is None:
+        o = torch.empty(B, Hq, T, dv, dtype=q.dtype, device=q.device)
+        lse = torch.empty(B, Hq, T, dtype=torch.float32, device=q.device)
+        bits = torch.empty(prefill_bitmap_shape(B, Hq, T, Br, Bc), dtype=torch.int32,
+                           device=q.device)
+    else:
+        o, lse, bits = out
+    st = load().attn_skip_prefill(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, Hq, Hkv, T, dk,
+                                  dv, float(scale), float(lam), Br, Bc, int(bool(causal)),
+                                  _ptr(o), _ptr(lse), _ptr(bits), _stream(stream, q.device))
+    _check("attn_skip_prefill", st)
+    return o, lse, bits
+
+
+def attn_skip_decode(q, k, v, lam, Bc=128, n_splits=8, dv=None, scale=0.0, out=None,
+                     stream=None):
+    """q [B,Hq,dk], k [B,Hkv,L,dk], v [B,Hkv,L,dv] or ``None`` (values are the
+    first ``dv`` columns of each key row).  Returns fp32 ``(o_part, lse_part,
+    skip_bits)``."""
+    _cuda_contig(q, k)
+    B, Hq, dk = q.shape
+    _, Hkv, L, kstride = k.shape
+    if v is None:
+        vv, vstride = k, kstride
+        if dv is None:
+            raise ValueError("dv is required when values alias the keys")
+    else:
+        _cuda_contig(v)
+        vv, dv, vstride = v, v.shape[3], v.shape[3]
+    if out is None:
+        o_part = torch.empty(B, Hq, n_splits, dv, dtype=torch.float32, device=q.device)
+        lse_part = torch.empty(B, Hq, n_splits, dtype=torch.float32, device=q.device)
+        bits = torch.empty(decode_bitmap_shape(B, Hkv, L, Bc, n_splits), dtype=torch.int32,
+                           device=q.device)
+    else:
+        o_part, lse_part, bits = out
+    st = load().attn_skip_decode(_ptr(q), _ptr(k), _ptr(vv), _dtype_code(q), B, Hq, Hkv, L, dk,
+                                 dv, kstride, vstride, float(scale), float(lam), Bc, n_splits,
+                                 _ptr(o_part), _ptr(lse_part), _ptr(bits),
+                                 _stream(stream, q.device))
+    _check("attn_skip_decode", st)
+    return o_part, lse_part, bits
+
+
+def attn_skip_decode_combine(o_part, lse_part, out_dtype=torch.bfloat16, out=None, stream=None):
+    """Merge ``o_part`` [B,Hq,S,dv] / ``lse_part`` [B,Hq,S] into ``(o, lse)``."""
+    _cuda_contig(o_part, lse_part)
+    B, Hq, S, dv = o_part.shape
+    if out is None:
+        o = torch.empty(B, Hq, dv, dtype=out_dtype, device=o_part.device)
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=o_part.device)
+    else:
+        o, lse = out
+    st = load().attn_skip_decode_combine(_ptr(o_part), _ptr(lse_part), B, Hq, S, dv,
+                                         _dtype_code(o), _ptr(o), _ptr(lse),
+                                         _stream(stream, o_part.device))
+    _check("attn_skip_decode_combine", st)
+    return o, lse
+
+
+def attn_skip_last_device_error(stream=None, device=None):
+    st = load().attn_skip_last_device_error(_stream(stream, device))
+    _check("attn_skip_last_device_error", st)
+
+
+def unpack_bits(bits: torch.Tensor, n: int) -> torch.Tensor:
+    """Expand uint32 bitmap words [..., W] into a bool tensor [..., n] (CPU)."""
+    w = bits.to("cpu").to(torch.int64) & 0xFFFFFFFF
+    shifts = torch.arange(32, dtype=torch.int64)
+    b = ((w[..., :, None] >> shifts) & 1).reshape(*w.shape[:-1], w.shape[-1] * 32)
+    return b[..., :n].bool()

@@ -1,0 +1,51 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+// Not part of the public ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn_skip {
+
+// Bits of the device error word.
+enum : unsigned {
+  kErrTimeout = 1u,  // a bounded mbarrier / flag wait gave up
+};
+
+struct PrefillArgs {
+  const void *q, *k, *v;
+  void *o;
+  float *lse;
+  uint32_t *bits;
+  int B, Hq, Hkv, T, dk, dv, Br, Bc, causal;
+  int n_t, n_b, words;  // tiles, blocks, bitmap words per tile
+  float scale;          // natural-log scale applied to q.k
+  float ln_lambda;      // -inf when lambda == 0
+  unsigned *err;        // device error word
+};
+
+struct DecodeArgs {
+  const void *q, *k, *v;
+  float *o_part, *lse_part;
+  uint32_t *bits;
+  int B, Hq, Hkv, L, dk, dv, Bc, n_splits;
+  int64_t k_row_stride, v_row_stride;
+  int n_b, bps, words;  // blocks, blocks per split (max), bitmap words per split
+  float scale;
+  float ln_lambda;
+  unsigned *err;
+};
+
+struct CombineArgs {
+  const float *o_part, *lse_part;
+  void *o;
+  float *lse;
+  int B, Hq, n_splits, dv;
+  int out_bf16;
+};
+
+cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t s);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
+cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
+
+}  // namespace attn_skip

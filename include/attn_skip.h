@@ -1,0 +1,143 @@
+/*
+ * attn_skip -- softmax-threshold block skipping inside a FlashAttention-style
+ * online-softmax tile loop, for one NVIDIA GB300 (sm_103a).
+ *
+ * Method: the web page "BLASST：一个标量阈值实现的动态块稀疏注意力（MLSys 2026）"
+ * (BLASST, arXiv 2512.12087).  For query tile i and KV block j, after the
+ * running max is updated to m_i^(j), the block is skipped when
+ *
+ *        rowmax(S_ij) - m_i^(j) < ln(lambda)          (section "BLASST 的判定准则", Eq. 5)
+ *
+ * holds for every row of the tile (section "判定本身：几乎零成本的秘密"); a
+ * skipped block costs no exponentials, no P.V product and -- in decode -- no
+ * value load (sections "Prefill 内核：砍计算", "Decode 内核：砍带宽").  Q.K^T
+ * is always computed: it is the only source of the block max.
+ *
+ * Conventions shared by every call
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    allocates no device memory and keeps no state between calls except one
+ *    device error word per GPU.  Layouts are dense row-major (C order).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Arguments are validated on the host before any launch;
+ *    on a validation error nothing is launched and no output is written.
+ *  - Scores are s = scale * <q, k>; scale <= 0 selects 1/sqrt(dk).  LSE outputs
+ *    are natural-log log-sum-exp of the scaled scores of the kept keys.
+ *  - lambda in [0, 1).  lambda = 0 disables skipping (dense attention).
+ *    The library evaluates ln(lambda) once on the host in double precision and
+ *    compares in the log domain in fp32 (section "BLASST 的判定准则": one
+ *    subtraction and one compare per element, no exponential).
+ *  - Skip bitmaps are uint32 words; bit (j % 32) of word (j / 32) of a unit's
+ *    row is 1 when block j was skipped.  Blocks a unit does not traverse (causal
+ *    blocks above the diagonal, positions past the end of a split) read 0.
+ *    Every word of every unit is written, so the buffer needs no clearing.
+ *  - Pointers must be 16-byte aligned.
+ *
+ * Status codes: ATTN_EINVAL for a null pointer, a non-positive size, Hq not a
+ * multiple of Hkv, lambda outside [0,1) or NaN, or a misaligned pointer;
+ * ATTN_EUNSUPPORTED for a valid combination this build has no kernel for;
+ * ATTN_ECUDA for a launch or CUDA runtime error (the CUDA error is cleared);
+ * ATTN_ETIMEOUT when a device-side bounded wait gave up (reported by
+ * attn_skip_last_device_error).
+ */
+#ifndef ATTN_SKIP_H
+#define ATTN_SKIP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_EINVAL = 1,
+  ATTN_EUNSUPPORTED = 2,
+  ATTN_ECUDA = 3,
+  ATTN_ETIMEOUT = 4
+} attn_status;
+
+typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
+
+/*
+ * Causal (or full) GQA prefill with block skipping.
+ *
+ * Defines: the online-softmax loop of section "铺垫：FlashAttention 的在线 softmax"
+ * (Eqs. 2-4) with the skip test of Eq. 5, KV blocks visited in ascending
+ * order; a query tile of Br rows skips block j only if all its valid rows
+ * vote skip.  Causal masking is top-left with equal query and key length:
+ * key c is visible to row r iff c <= r.
+ *
+ *  q          [B, Hq,  T, dk]  (dt)
+ *  k          [B, Hkv, T, dk]  (dt)   query head h reads KV head h / (Hq/Hkv)
+ *  v          [B, Hkv, T, dv]  (dt)
+ *  o          [B, Hq,  T, dv]  (dt)   written: softmax over the kept keys times V
+ *  lse        [B, Hq,  T]      fp32   written
+ *  skip_bits  [B, Hq, ceil(T/Br), ceil(ceil(T/Bc)/32)] uint32, written
+ *
+ * Kernels built: dt = ATTN_BF16 with dk = dv = 128, Br = Bc = 128 (tcgen05
+ * tensor-core path, fp32 accumulation, P rounded to bf16 for the P.V product);
+ * dt = ATTN_F32 with dk = dv in {32, 64}, Br, Bc in {64, 128} (CUDA-core path).
+ * Anything else returns ATTN_EUNSUPPORTED.
+ */
+attn_status attn_skip_prefill(const void *q, const void *k, const void *v, attn_dtype dt, int B,
+                              int Hq, int Hkv, int T, int dk, int dv, float scale, double lambda,
+                              int Br, int Bc, int causal, void *o, float *lse,
+                              uint32_t *skip_bits, void *stream);
+
+/*
+ * Split-KV decode, one query token per sequence, with block skipping.
+ *
+ * Defines: section "Decode 内核：砍带宽" -- scores of a batch of KV blocks are
+ * computed first, the skip decisions are taken for the batch in block order,
+ * and values are loaded only for the kept blocks.  The G = Hq/Hkv query heads
+ * that share a KV head form one group and skip a block only if all of them
+ * vote skip.  The cache of each (b, KV head) is split into n_splits ranges of
+ * whole blocks, split s owning blocks [floor(s*nb/n), floor((s+1)*nb/n)) with
+ * nb = ceil(L/Bc); each split restarts its running max (FlashDecoding).
+ *
+ *  q          [B, Hq, dk]                      (dt)
+ *  k          key c of (b, hk) at k + ((b*Hkv + hk)*L + c) * k_row_stride   (dt)
+ *  v          value c at v + ((b*Hkv + hk)*L + c) * v_row_stride            (dt)
+ *             (an absorbed-MLA latent cache passes v == k: values are the
+ *             first dv columns of each key row)
+ *  o_part     [B, Hq, n_splits, dv]  fp32, written (0 for an empty split)
+ *  lse_part   [B, Hq, n_splits]      fp32, written (-inf for an empty split)
+ *  skip_bits  [B, Hkv, n_splits, ceil(bps/32)] uint32 with bps = ceil(nb/n_splits);
+ *             bit p of split s is block floor(s*nb/n_splits) + p
+ *
+ * Kernels built: dt = ATTN_BF16, dk = dv = 128, Bc = 128, G in {1, 2, 4, 8},
+ * k_row_stride = v_row_stride = 128 (CUDA-core memory-bound path).
+ */
+attn_status attn_skip_decode(const void *q, const void *k, const void *v, attn_dtype dt, int B,
+                             int Hq, int Hkv, int L, int dk, int dv, int64_t k_row_stride,
+                             int64_t v_row_stride, float scale, double lambda, int Bc,
+                             int n_splits, float *o_part, float *lse_part, uint32_t *skip_bits,
+                             void *stream);
+
+/*
+ * Merge of decode split partials by log-sum-exp (FlashDecoding):
+ * LSE = ln sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) * O_s.
+ * Splits with LSE_s = -inf weigh zero.
+ *
+ *  o_part [B, Hq, n_splits, dv] fp32,  lse_part [B, Hq, n_splits] fp32
+ *  o      [B, Hq, dv] (out_dt),       lse      [B, Hq] fp32
+ */
+attn_status attn_skip_decode_combine(const float *o_part, const float *lse_part, int B, int Hq,
+                                     int n_splits, int dv, attn_dtype out_dt, void *o,
+                                     float *lse, void *stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word: ATTN_ETIMEOUT if a kernel gave up a bounded wait since the last read,
+ * ATTN_ECUDA on a CUDA error, else ATTN_OK.
+ */
+attn_status attn_skip_last_device_error(void *stream);
+
+/* Static, human-readable name of a status code. */
+const char *attn_skip_status_string(attn_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_SKIP_H */

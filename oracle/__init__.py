@@ -60,9 +60,9 @@ def _load():
         lib.bsa_oracle_dense_prefill.argtypes = [P, P, P, i, i, i, i, i, i, d, i, P, i64, P, P]
         lib.bsa_oracle_dense_decode.argtypes = [P, P, P, i, i, i, i, i, i, i64, i64, d, P, P]
         lib.bsa_oracle_prefill.argtypes = [P, P, P, i, i, i, i, i, i, d, d, i, i, i, P, i64,
-                                           P, P, P, P]
+                                           P, P, P, P, P]
         lib.bsa_oracle_decode.argtypes = [P, P, P, i, i, i, i, i, i, i64, i64, d, d, i, i, P,
-                                          i64, P, P, P, P]
+                                          i64, P, P, P, P, P]
         lib.bsa_oracle_combine.argtypes = [P, P, i, i, i, i, P, P]
         for f in ("bsa_oracle_dense_prefill", "bsa_oracle_dense_decode", "bsa_oracle_prefill",
                   "bsa_oracle_decode", "bsa_oracle_combine", "bsa_oracle_num_threads"):
@@ -135,13 +135,24 @@ def dense_decode(q, k, v, scale, dv=None):
     return y, lse
 
 
-def prefill(q, k, v, scale, lam, Br=128, Bc=128, causal=True, units=None):
+def _forced(force_skip, shape):
+    if force_skip is None:
+        return None
+    f = np.ascontiguousarray(np.asarray(force_skip, dtype=np.uint8))
+    if f.shape != shape:
+        raise ValueError(f"force_skip has shape {f.shape}, expected {shape}")
+    return f
+
+
+def prefill(q, k, v, scale, lam, Br=128, Bc=128, causal=True, units=None, force_skip=None):
     """Thresholded online-softmax prefill in fp64.
 
     Returns a dict with ``o`` [B,Hq,T,dv], ``lse`` [B,Hq,T], ``skip``
     [B,Hq,n_t,n_b] (uint8, 1 = skipped) and ``margin`` [B,Hq,n_t,n_b] (the tile
     statistic max_r(rowmax - m_new); NaN where not traversed).  ``units`` are
-    flat indices into [B,Hq,n_t]; only those tiles are computed."""
+    flat indices into [B,Hq,n_t]; only those tiles are computed.
+    ``force_skip`` ([B,Hq,n_t,n_b]) replaces the skip decisions by given ones
+    (the loop's arithmetic is unchanged)."""
     q, k, v = _f32(q), _f32(k), _f32(v)
     B, Hq, T, dk = q.shape
     Hkv, dv = k.shape[1], v.shape[3]
@@ -151,21 +162,24 @@ def prefill(q, k, v, scale, lam, Br=128, Bc=128, causal=True, units=None):
     skip = np.zeros((B, Hq, n_t, n_b), dtype=np.uint8)
     margin = np.full((B, Hq, n_t, n_b), np.nan)
     u, nu = _units(units)
+    f = _forced(force_skip, skip.shape)
     rc = _load().bsa_oracle_prefill(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, T, dk, dv,
                                     float(scale), float(lam), Br, Bc, int(bool(causal)),
-                                    None if u is None else _ptr(u), nu, _ptr(o), _ptr(lse),
+                                    None if u is None else _ptr(u), nu,
+                                    None if f is None else _ptr(f), _ptr(o), _ptr(lse),
                                     _ptr(skip), _ptr(margin))
     if rc:
         raise ValueError("bsa_oracle_prefill: invalid arguments")
     return {"o": o, "lse": lse, "skip": skip, "margin": margin}
 
 
-def decode(q, k, v, scale, lam, Bc, n_splits, dv=None, units=None):
+def decode(q, k, v, scale, lam, Bc, n_splits, dv=None, units=None, force_skip=None):
     """Split-KV thresholded decode in fp64 (partials, before the merge).
 
     Returns ``o_part`` [B,Hq,S,dv], ``lse_part`` [B,Hq,S], ``skip`` and
     ``margin`` [B,Hkv,S,bps] with bps = ceil(n_b / S).  ``units`` are flat
-    indices into [B,Hkv,S]."""
+    indices into [B,Hkv,S]; ``force_skip`` ([B,Hkv,S,bps]) replaces the skip
+    decisions by given ones."""
     q, k = _f32(q), _f32(k)
     B, Hq, dk = q.shape
     _, Hkv, L, kstride = k.shape
@@ -181,9 +195,11 @@ def decode(q, k, v, scale, lam, Bc, n_splits, dv=None, units=None):
     skip = np.zeros((B, Hkv, n_splits, bps), dtype=np.uint8)
     margin = np.full((B, Hkv, n_splits, bps), np.nan)
     u, nu = _units(units)
+    f = _forced(force_skip, skip.shape)
     rc = _load().bsa_oracle_decode(_ptr(q), _ptr(k), _ptr(vv), B, Hq, Hkv, L, dk, dv, kstride,
                                    vstride, float(scale), float(lam), Bc, n_splits,
-                                   None if u is None else _ptr(u), nu, _ptr(o_part),
+                                   None if u is None else _ptr(u), nu,
+                                   None if f is None else _ptr(f), _ptr(o_part),
                                    _ptr(lse_part), _ptr(skip), _ptr(margin))
     if rc:
         raise ValueError("bsa_oracle_decode: invalid arguments")

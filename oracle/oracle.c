@@ -171,9 +171,10 @@ static void state_free(loop_state *st) {
 /* One step j of the loop, once st->s holds S_ij for the block's nc keys (masked
  * scores are -inf).  Returns 1 if the block is skipped.  *margin receives the
  * tile statistic max_r (rowmax_r - m_new_r): the block is skipped iff that
- * statistic is below ln(lambda) (and lambda > 0). */
+ * statistic is below ln(lambda) (and lambda > 0).  forced >= 0 replaces the
+ * decision by the caller's (0 keep, 1 skip); the arithmetic is unchanged. */
 static int loop_step(loop_state *st, int nc, int Bc, const float *vblk, int64_t v_row_stride,
-                     double lambda, double ln_lambda, double *margin) {
+                     double lambda, double ln_lambda, int forced, double *margin) {
   const int nr = st->nr, dv = st->dv;
   double mu = NEG_INF;
   int all_vote_skip = 1;
@@ -191,6 +192,7 @@ static int loop_step(loop_state *st, int nc, int Bc, const float *vblk, int64_t 
     if (!vote) all_vote_skip = 0;
   }
   *margin = mu;
+  if (forced >= 0) all_vote_skip = forced;
   if (!all_vote_skip) {
     /* Eqs. (2)-(4): rescale the history to the new max, add this block. */
     for (int r = 0; r < nr; ++r) {
@@ -219,11 +221,14 @@ static int loop_step(loop_state *st, int nc, int Bc, const float *vblk, int64_t 
  * KV head h / (Hq/Hkv).  units: flat indices into [B,Hq,n_t] (NULL = all).
  * Outputs (only the chosen units' entries are written):
  *   o:[B,Hq,T,dv], lse:[B,Hq,T]   final O = acc / l and LSE = m + ln l;
- *   skip:[B,Hq,n_t,n_b] (1 = skipped), margin:[B,Hq,n_t,n_b] (NaN = not traversed). */
+ *   skip:[B,Hq,n_t,n_b] (1 = skipped), margin:[B,Hq,n_t,n_b] (NaN = not traversed).
+ * force_skip (NULL = none), same layout as skip: the decisions to take instead of
+ * the test's, for evaluating the loop under another valid set of decisions. */
 int bsa_oracle_prefill(const float *q, const float *k, const float *v, int B, int Hq, int Hkv,
                        int T, int dk, int dv, double scale, double lambda, int Br, int Bc,
-                       int causal, const int64_t *units, int64_t n_units, double *o,
-                       double *lse, uint8_t *skip, double *margin) {
+                       int causal, const int64_t *units, int64_t n_units,
+                       const uint8_t *force_skip, double *o, double *lse, uint8_t *skip,
+                       double *margin) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || dk <= 0 || dv <= 0 || Br <= 0 || Bc <= 0 ||
       Hq % Hkv || !(lambda >= 0.0 && lambda < 1.0))
     return -1;
@@ -259,8 +264,9 @@ int bsa_oracle_prefill(const float *q, const float *k, const float *v, int B, in
               : scale * dot_f32(qb + (int64_t)row * dk, kb + (int64_t)col * dk, dk);
         }
       }
+      const int forced = force_skip ? (int)force_skip[u * n_b + j] : -1;
       sk[j] = (uint8_t)loop_step(&st, nc, Bc, vb + (int64_t)c0 * dv, dv, lambda, ln_lambda,
-                                 &mg[j]);
+                                 forced, &mg[j]);
     }
     for (int r = 0; r < nr; ++r) {
       const int64_t orow = ((int64_t)b * Hq + h) * T + r0 + r;
@@ -278,12 +284,13 @@ int bsa_oracle_prefill(const float *q, const float *k, const float *v, int B, in
  * units: flat indices into [B,Hkv,n_splits] (NULL = all).  Outputs:
  *   o_part:[B,Hq,n_splits,dv], lse_part:[B,Hq,n_splits] (-inf for an empty split);
  *   skip, margin:[B,Hkv,n_splits,bps] with bps = ceil(n_b/n_splits), block j of split s
- *   at position j - floor(s*n_b/n_splits). */
+ *   at position j - floor(s*n_b/n_splits).
+ * force_skip (NULL = none), same layout as skip: decisions to take instead of the test's. */
 int bsa_oracle_decode(const float *q, const float *k, const float *v, int B, int Hq, int Hkv,
                       int L, int dk, int dv, int64_t k_row_stride, int64_t v_row_stride,
                       double scale, double lambda, int Bc, int n_splits, const int64_t *units,
-                      int64_t n_units, double *o_part, double *lse_part, uint8_t *skip,
-                      double *margin) {
+                      int64_t n_units, const uint8_t *force_skip, double *o_part,
+                      double *lse_part, uint8_t *skip, double *margin) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || L <= 0 || dk <= 0 || dv <= 0 || Bc <= 0 ||
       n_splits <= 0 || Hq % Hkv || !(lambda >= 0.0 && lambda < 1.0))
     return -1;
@@ -313,8 +320,9 @@ int bsa_oracle_decode(const float *q, const float *k, const float *v, int B, int
         for (int c = 0; c < nc; ++c)
           st.s[(size_t)g * Bc + c] = scale * dot_f32(qr, k + (base + c0 + c) * k_row_stride, dk);
       }
+      const int forced = force_skip ? (int)force_skip[u * bps + (j - j0)] : -1;
       sk[j - j0] = (uint8_t)loop_step(&st, nc, Bc, v + (base + c0) * v_row_stride,
-                                      v_row_stride, lambda, ln_lambda, &mg[j - j0]);
+                                      v_row_stride, lambda, ln_lambda, forced, &mg[j - j0]);
     }
     for (int g = 0; g < G; ++g) {
       const int64_t row = ((int64_t)b * Hq + hk * G + g) * n_splits + sp;

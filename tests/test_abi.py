@@ -1,0 +1,93 @@
+"""The C-ABI library loads, exports every declared symbol, and validates its
+arguments on the host (CPU only: no call here reaches a kernel launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_sparse_attention_online_gb300 import binding as bs
+from block_sparse_attention_online_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return bs.load()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "attn_skip.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_skip_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    syms = declared_symbols()
+    assert "attn_skip_prefill" in syms and "attn_skip_decode_combine" in syms
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert set(syms) == set(bs.EXPORTED)
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert bs.status_string(code)
+    assert "invalid" in bs.status_string(bs.ATTN_EINVAL)
+
+
+FAKE = ctypes.c_void_p(0x10000)  # aligned, never dereferenced: validation fails first
+
+
+def _prefill(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, dt=0, B=1, Hq=4, Hkv=2, T=256, dk=128, dv=128, scale=0.0,
+             lam=0.01, Br=128, Bc=128, causal=1, o=FAKE, lse=FAKE, bits=FAKE, stream=None)
+    a.update(kw)
+    return lib.attn_skip_prefill(*a.values())
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=None), dict(o=None), dict(bits=None), dict(B=0), dict(T=-1), dict(Hq=3),
+    dict(lam=-0.1), dict(lam=1.0), dict(lam=float("nan")), dict(scale=float("nan")),
+    dict(dt=7), dict(q=ctypes.c_void_p(0x10004)), dict(Br=0),
+])
+def test_prefill_rejects_invalid_arguments(lib, kw):
+    assert _prefill(lib, **kw) == bs.ATTN_EINVAL
+
+
+def _decode(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, dt=0, B=2, Hq=8, Hkv=2, L=1024, dk=128, dv=128, ks=128,
+             vs=128, scale=0.0, lam=0.01, Bc=128, n=4, op=FAKE, lp=FAKE, bits=FAKE, stream=None)
+    a.update(kw)
+    return lib.attn_skip_decode(*a.values())
+
+
+@pytest.mark.parametrize("kw", [
+    dict(k=None), dict(lp=None), dict(n=0), dict(L=0), dict(Hq=6, Hkv=4), dict(lam=1.5),
+    dict(ks=64), dict(bits=None), dict(v=ctypes.c_void_p(0x10002)),
+])
+def test_decode_rejects_invalid_arguments(lib, kw):
+    assert _decode(lib, **kw) == bs.ATTN_EINVAL
+
+
+def test_combine_rejects_invalid_arguments(lib):
+    f = lib.attn_skip_decode_combine
+    assert f(None, FAKE, 1, 1, 1, 128, 0, FAKE, FAKE, None) == bs.ATTN_EINVAL
+    assert f(FAKE, FAKE, 1, 1, 0, 128, 0, FAKE, FAKE, None) == bs.ATTN_EINVAL
+    assert f(FAKE, FAKE, 1, 1, 4, 128, 5, FAKE, FAKE, None) == bs.ATTN_EINVAL
+
+
+def test_bitmap_shapes():
+    assert bs.prefill_bitmap_shape(1, 32, 16384, 128, 128) == (1, 32, 128, 4)
+    assert bs.decode_bitmap_shape(16, 8, 32768, 128, 8) == (16, 8, 8, 1)
+    assert bs.decode_bitmap_shape(32, 1, 16384, 64, 16) == (32, 1, 16, 1)
+
+
+def test_unpack_bits_roundtrip():
+    import torch
+    w = torch.tensor([[0b1011, -1]], dtype=torch.int32)
+    u = bs.unpack_bits(w, 40)
+    assert u[0, :4].tolist() == [True, True, False, True]
+    assert u[0, 4:32].sum() == 0 and u[0, 32:40].all()
