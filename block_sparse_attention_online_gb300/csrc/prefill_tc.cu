@@ -1,6 +1,463 @@
-// bf16 tensor-core prefill (tcgen05 / TMEM / TMA) -- under construction.
+// bf16 tensor-core prefill with softmax-threshold block skipping (d = 128,
+// Br = Bc = 128), tcgen05 MMAs accumulating in TMEM, operands staged by TMA.
+//
+// Method: the BLASST page, sections "铺垫：FlashAttention 的在线 softmax"
+// (Eqs. 2-4), "BLASST 的判定准则" (Eq. 5), "判定本身：几乎零成本的秘密" (the
+// per-row predicate, a warp vote and a tile-wide AND) and "Prefill 内核：砍计算"
+// (a skipped block costs no exponentials, no row sum and no P.V product).  The
+// value tile of a block is loaded only once the block is known to be kept.
+//
+// One CTA per (batch, query head, query tile), longest causal tiles first.
+// Warp roles (192 threads):
+//   warps 0-3  softmax: thread i owns query row i (TMEM lane i).  Per block it
+//              reads the S row from TMEM, masks, takes the row max, votes,
+//              and for kept blocks writes P (bf16) to shared memory, keeps the
+//              row sum and rescales O in TMEM when the exp reference moves
+//              by more than 2^8; then the epilogue O / l and LSE;
+//   warp 4     TMA producer: Q once, K_j for every block, V_j for kept blocks;
+//   warp 5     MMA issuer: S_j = Q K_j^T into one of two TMEM S buffers, and
+//              O += P_j V_j for kept blocks, QK of block j+1 issued before the
+//              PV of block j so the softmax of one block overlaps the MMAs.
+// TMEM columns: S buffers [0,128) and [128,256), O [256,384).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <math.h>
+
 #include "internal.h"
+#include "tc_common.cuh"
 
 namespace attn_skip {
-cudaError_t launch_prefill_tc(const PrefillArgs &, cudaStream_t) { return cudaErrorNotYetImplemented; }
+namespace {
+
+using namespace tc;
+
+constexpr int D = 128;       // head size of keys and values
+constexpr int BM = 128;      // query rows per tile
+constexpr int BN = 128;      // keys per block
+constexpr int NK = 2;        // K stages
+constexpr int NV = 2;        // V stages
+constexpr int NDEC = 4;      // decision ring
+constexpr int NTHREADS = 192;
+constexpr uint32_t TILE_BYTES = BM * D * 2;    // 32 KB: one 128 x 128 bf16 tile
+constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;  // one 64-column swizzled box
+constexpr uint32_t SMEM_Q = 0;
+constexpr uint32_t SMEM_K = SMEM_Q + TILE_BYTES;
+constexpr uint32_t SMEM_V = SMEM_K + NK * TILE_BYTES;
+constexpr uint32_t SMEM_P = SMEM_V + NV * TILE_BYTES;
+constexpr uint32_t SMEM_BYTES = SMEM_P + 2 * TILE_BYTES;  // 224 KB
+constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;       // + alignment slack
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_O = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;  // exp reference may lag the max by 2^8
+constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);  // K: K-major
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 1);   // V: MN-major
+
+struct Shared {
+  uint64_t q_full;
+  uint64_t k_full[NK], k_empty[NK];
+  uint64_t v_full[NV], v_empty[NV];
+  uint64_t s_full[2], s_free[2];
+  uint64_t p_full[2], pv_done[2];
+  uint64_t dec_full[NDEC];
+  uint64_t vote_full[2];
+  int dec[NDEC];
+  int vote[2][4];
+  uint32_t tmem_base;
+  int abort;
+};
+
+
+// Descriptor of k-step kk (16 columns) of a K-major 128 x 128 bf16 tile held as
+// two 128-byte-swizzled boxes of 64 columns: box kk/4, 32-byte step kk%4,
+// 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
+  return smem_desc_sw128(tile + (uint32_t)(kk >> 2) * HALF_BYTES + (uint32_t)(kk & 3) * 32u, 16u,
+                         1024u);
+}
+
+// Descriptor of k-step kk (16 keys) of the MN-major value tile: rows are keys
+// (128 bytes = 64 values per swizzled row), 8-key groups 1024 bytes apart
+// (SBO), the second 64-value half 16 KB further (LBO).
+__device__ __forceinline__ uint64_t vmajor_desc(uint32_t tile, int kk) {
+  return smem_desc_sw128(tile + (uint32_t)kk * 2048u, HALF_BYTES, 1024u);
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Shared sh;
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-byte aligned for the swizzle
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  // Longest causal tiles first: blocks are ordered by decreasing tile index.
+  const int BH = a.B * a.Hq;
+  const int t = a.n_t - 1 - (int)(blockIdx.x / BH);
+  const int bh = (int)(blockIdx.x % BH);
+  const int h = bh % a.Hq, b = bh / a.Hq;
+  const int hk = h / (a.Hq / a.Hkv);
+  const int row0 = t * BM;
+  const int last_row = min(a.T, row0 + BM) - 1;
+  const int nblk = a.causal ? last_row / BN + 1 : a.n_b;
+  volatile int *abort = &sh.abort;
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&sh.q_full), 1);
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(smem_u32(&sh.k_full[i]), 1);
+      mbar_init(smem_u32(&sh.k_empty[i]), 1);
+    }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(smem_u32(&sh.v_full[i]), 1);
+      mbar_init(smem_u32(&sh.v_empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sh.s_full[i]), 1);
+      mbar_init(smem_u32(&sh.s_free[i]), 4);
+      mbar_init(smem_u32(&sh.p_full[i]), 4);
+      mbar_init(smem_u32(&sh.pv_done[i]), 1);
+    }
+    for (int i = 0; i < NDEC; ++i) mbar_init(smem_u32(&sh.dec_full[i]), 1);
+    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&sh.vote_full[i]), 4);
+    sh.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) tmem_alloc(smem_u32(&sh.tmem_base), TMEM_COLS);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer --
+    if (lane == 0) {
+      prefetch_tmap(&tm_q);
+      prefetch_tmap(&tm_k);
+      prefetch_tmap(&tm_v);
+      const uint64_t keep_l2 = policy_evict_last();   // K/V are re-read by other tiles/heads
+      const uint64_t stream_l2 = policy_evict_first(); // Q is read once
+      const int zq = b * a.Hq + h, zkv = b * a.Hkv + hk;
+      mbar_expect_tx(smem_u32(&sh.q_full), TILE_BYTES);
+      tma_load_3d(base + SMEM_Q, &tm_q, smem_u32(&sh.q_full), 0, row0, zq, stream_l2);
+      tma_load_3d(base + SMEM_Q + HALF_BYTES, &tm_q, smem_u32(&sh.q_full), 64, row0, zq,
+                  stream_l2);
+      int vi = 0, ki = 0;
+      for (int j = 0; j <= nblk && !*abort; ++j) {
+        if (j < nblk) {  // K_j
+          const int s = j % NK;
+          if (j >= NK &&
+              !mbar_wait(smem_u32(&sh.k_empty[s]), ((j / NK) - 1) & 1, abort, a.err, kErrTimeout))
+            break;
+          const uint32_t dst = base + SMEM_K + s * TILE_BYTES;
+          mbar_expect_tx(smem_u32(&sh.k_full[s]), TILE_BYTES);
+          tma_load_3d(dst, &tm_k, smem_u32(&sh.k_full[s]), 0, j * BN, zkv, keep_l2);
+          tma_load_3d(dst + HALF_BYTES, &tm_k, smem_u32(&sh.k_full[s]), 64, j * BN, zkv, keep_l2);
+          ++ki;
+        }
+        if (j >= 1) {  // V_{j-1}, only if block j-1 is kept
+          const int jd = j - 1;
+          if (!mbar_wait(smem_u32(&sh.dec_full[jd % NDEC]), (jd / NDEC) & 1, abort, a.err,
+                         kErrTimeout))
+            break;
+          if (sh.dec[jd % NDEC]) {
+            const int s = vi % NV;
+            if (vi >= NV && !mbar_wait(smem_u32(&sh.v_empty[s]), ((vi / NV) - 1) & 1, abort,
+                                       a.err, kErrTimeout))
+              break;
+            const uint32_t dst = base + SMEM_V + s * TILE_BYTES;
+            mbar_expect_tx(smem_u32(&sh.v_full[s]), TILE_BYTES);
+            tma_load_3d(dst, &tm_v, smem_u32(&sh.v_full[s]), 0, jd * BN, zkv, keep_l2);
+            tma_load_3d(dst + HALF_BYTES, &tm_v, smem_u32(&sh.v_full[s]), 64, jd * BN, zkv,
+                        keep_l2);
+            ++vi;
+          }
+        }
+      }
+      // Drain: the last load issued into each slot has landed before the CTA
+      // may exit (earlier loads of a slot were consumed before it was reused).
+      mbar_wait_drain(smem_u32(&sh.q_full), 0);
+      for (int s = 0; s < NK && s < ki; ++s) {
+        const int last = s + ((ki - 1 - s) / NK) * NK;
+        mbar_wait_drain(smem_u32(&sh.k_full[s]), (last / NK) & 1);
+      }
+      for (int s = 0; s < NV && s < vi; ++s) {
+        const int last = s + ((vi - 1 - s) / NV) * NV;
+        mbar_wait_drain(smem_u32(&sh.v_full[s]), (last / NV) & 1);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA --
+    if (lane == 0) {
+      bool ok = mbar_wait(smem_u32(&sh.q_full), 0, abort, a.err, kErrTimeout);
+      fence_after_sync();
+      int kc = 0, vi = 0;
+      for (int j = 0; ok && j <= nblk; ++j) {
+        if (j < nblk) {  // S_j = Q K_j^T
+          const int s = j % NK, sb = j & 1;
+          ok = mbar_wait(smem_u32(&sh.k_full[s]), (j / NK) & 1, abort, a.err, kErrTimeout);
+          if (ok && j >= 2)
+            ok = mbar_wait(smem_u32(&sh.s_free[sb]), ((j >> 1) - 1) & 1, abort, a.err,
+                           kErrTimeout);
+          if (!ok) break;
+          fence_after_sync();
+          const uint32_t ktile = base + SMEM_K + s * TILE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ss(tmem + sb * BN, kmajor_desc(base + SMEM_Q, kk), kmajor_desc(ktile, kk),
+                        IDESC_QK, kk > 0);
+          mma_commit(smem_u32(&sh.s_full[sb]));
+          mma_commit(smem_u32(&sh.k_empty[s]));
+        }
+        if (j >= 1) {  // O += P_{j-1} V_{j-1} if kept
+          const int jd = j - 1;
+          ok = mbar_wait(smem_u32(&sh.dec_full[jd % NDEC]), (jd / NDEC) & 1, abort, a.err,
+                         kErrTimeout);
+          if (!ok) break;
+          if (sh.dec[jd % NDEC]) {
+            const int pb = kc & 1, vs = vi % NV;
+            ok = mbar_wait(smem_u32(&sh.p_full[pb]), (kc >> 1) & 1, abort, a.err, kErrTimeout);
+            if (ok) ok = mbar_wait(smem_u32(&sh.v_full[vs]), (vi / NV) & 1, abort, a.err,
+                                   kErrTimeout);
+            if (!ok) break;
+            fence_after_sync();
+            const uint32_t ptile = base + SMEM_P + pb * TILE_BYTES;
+            const uint32_t vtile = base + SMEM_V + vs * TILE_BYTES;
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_bf16_ss(tmem + TMEM_O, kmajor_desc(ptile, kk), vmajor_desc(vtile, kk),
+                          IDESC_PV, (kc > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(smem_u32(&sh.v_empty[vs]));
+            mma_commit(smem_u32(&sh.pv_done[pb]));
+            ++kc;
+            ++vi;
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax --
+    const int r = tid;  // row within the tile == TMEM lane
+    const int row = row0 + r;
+    const bool valid = row < a.T;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const float sl2 = a.scale * kLog2e;        // raw score -> log2 units
+    const float c2 = a.ln_lambda * kLog2e;     // ln(lambda) in log2 units
+    float m2 = -INFINITY;                      // running max (log2 units)
+    float mref = -INFINITY;                    // exp reference (log2 units)
+    float l = 0.f;
+    int kc = 0;
+    uint32_t word = 0;
+    uint32_t *bits = a.bits + ((size_t)bh * a.n_t + t) * a.words;
+    bool ok = true;
+
+    for (int j = 0; j < nblk; ++j) {
+      const int sb = j & 1;
+      ok = mbar_wait(smem_u32(&sh.s_full[sb]), (j >> 1) & 1, abort, a.err, kErrTimeout);
+      if (!ok) break;
+      fence_after_sync();
+      uint32_t sr[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + sb * BN + c * 32, sr[c]);
+      tmem_wait_ld();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.s_free[sb]));
+
+      // Mask: causal (key > row) on the diagonal block; keys past T.
+      const int key0 = j * BN;
+      const bool diag = a.causal ? (key0 + BN - 1 > row0) : (key0 + BN > a.T);
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int key = key0 + c * 32 + i;
+          float s = __uint_as_float(sr[c][i]);
+          if (diag && (a.causal ? key > row : key >= a.T)) s = -INFINITY;
+          sr[c][i] = __float_as_uint(s);
+          mt = fmaxf(mt, s);
+        }
+      }
+      const float mt2 = mt * sl2;
+      const float mnew = fmaxf(m2, mt2);
+      const float diff = (mt == -INFINITY) ? -INFINITY : mt2 - mnew;
+      // Eq. 5 against the updated running max; rows past T are neutral.
+      const bool vote = !valid || (diff < c2);
+      const unsigned all = __all_sync(0xffffffffu, vote);
+      if (lane == 0) {
+        sh.vote[sb][warp] = (int)all;
+        mbar_arrive(smem_u32(&sh.vote_full[sb]));
+      }
+      ok = mbar_wait(smem_u32(&sh.vote_full[sb]), (j >> 1) & 1, abort, a.err, kErrTimeout);
+      if (!ok) break;
+      const bool skip = sh.vote[sb][0] && sh.vote[sb][1] && sh.vote[sb][2] && sh.vote[sb][3];
+      if (tid == 0) {
+        sh.dec[j % NDEC] = skip ? 0 : 1;
+        mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
+        if (skip) word |= 1u << (j & 31);
+        if ((j & 31) == 31 || j == nblk - 1) {
+          bits[j >> 5] = word;
+          word = 0;
+        }
+      }
+      m2 = mnew;
+      if (skip) continue;
+
+      // ---- kept block: exp reference, P, row sum --------------------------
+      bool rescale = false;
+      float alpha = 1.f;
+      if (mref == -INFINITY) {
+        mref = mnew;
+      } else if (mnew > mref + kRescaleLog2) {
+        alpha = ex2(mref - mnew);
+        mref = mnew;
+        rescale = true;
+      }
+      const float neg_ref = -mref;
+      float rowsum = 0.f;
+      const int pb = kc & 1;
+      // P buffer pb was last read by the PV of kept block kc-2.
+      if (kc >= 2) {
+        ok = mbar_wait(smem_u32(&sh.pv_done[pb]), ((kc - 2) >> 1) & 1, abort, a.err,
+                       kErrTimeout);
+        if (!ok) break;
+      }
+      const uint32_t prow = base + SMEM_P + pb * TILE_BYTES + (uint32_t)r * 128u;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * i]), sl2, neg_ref));
+          const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * i + 1]), sl2, neg_ref));
+          rowsum += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        // 32 keys = four 16-byte chunks; chunk ch of the row lives in box ch/8,
+        // 16-byte slot (ch%8) XOR (row%8) (128-byte swizzle).
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const int ch = c * 4 + q4;
+          const uint32_t addr = prow + (uint32_t)(ch >> 3) * HALF_BYTES +
+                                ((uint32_t)((ch & 7) ^ (r & 7)) << 4);
+          st_shared_v4(addr, pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      l = l * alpha + rowsum;
+      // O rescale (warp-wide if any row needs it), after the previous PV landed.
+      if (__any_sync(0xffffffffu, rescale) && kc >= 1) {
+        ok = mbar_wait(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort, a.err,
+                       kErrTimeout);
+        if (!ok) break;
+        fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + TMEM_O + c * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(lane_base + TMEM_O + c * 32, o);
+        }
+        tmem_wait_st();
+      }
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[pb]));
+      ++kc;
+    }
+
+    // ---- epilogue ----------------------------------------------------------
+    if (tid == 0) {
+      for (int w = ((nblk - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
+    }
+    if (ok && kc > 0) {
+      ok = mbar_wait(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort, a.err,
+                     kErrTimeout);
+    }
+    if (ok) {
+      fence_after_sync();
+      const float inv = 1.f / l;
+      __nv_bfloat16 *orow = (__nv_bfloat16 *)a.o + ((size_t)bh * a.T + row) * D;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + TMEM_O + c * 32, o);
+        tmem_wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * q4 + 0]) * inv, __uint_as_float(o[8 * q4 + 1]) * inv);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * q4 + 2]) * inv, __uint_as_float(o[8 * q4 + 3]) * inv);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * q4 + 4]) * inv, __uint_as_float(o[8 * q4 + 5]) * inv);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * q4 + 6]) * inv, __uint_as_float(o[8 * q4 + 7]) * inv);
+            *reinterpret_cast<uint4 *>(orow + c * 32 + q4 * 8) = v;
+          }
+        }
+      }
+      if (valid) a.lse[(size_t)bh * a.T + row] = mref * kLn2 + logf(l);
+    }
+  }
+
+  fence_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    fence_after_sync();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (EncodeTiledFn)p;
+  }
+  return fn;
+}
+
+// 3-D map over a [heads, T, 128] bf16 tensor, box 64 x 128 x 1, 128-byte swizzle;
+// rows past T read as zero.
+bool make_map(CUtensorMap *m, const void *ptr, int heads, int T) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)heads};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, a.q, a.B * a.Hq, a.T) || !make_map(&mk, a.k, a.B * a.Hkv, a.T) ||
+      !make_map(&mv, a.v, a.B * a.Hkv, a.T))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  const long units = (long)a.B * a.Hq * a.n_t;
+  prefill_tc_kernel<<<(unsigned)units, NTHREADS, SMEM_ALLOC, s>>>(mq, mk, mv, a);
+  return cudaGetLastError();
+}
+
 }  // namespace attn_skip

@@ -1,0 +1,114 @@
+"""bf16 tcgen05 prefill on the GPU against the fp64 oracle."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_attention_online_gb300 import binding as bs
+from block_sparse_attention_online_gb300 import workloads as W
+from tests.parity import check_outputs, compare_bits
+
+pytestmark = pytest.mark.gpu
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _lambda(cfg_name, target):
+    with open(os.path.join(GOLDEN, "lambdas.json")) as f:
+        return json.load(f)[cfg_name][str(target)]["lambda"]
+
+
+def run_prefill(q, k, v, lam, causal=True):
+    dev = torch.device("cuda")
+    o, lse, bits = bs.attn_skip_prefill(q.to(dev), k.to(dev), v.to(dev), lam, 128, 128, causal)
+    bs.attn_skip_last_device_error()
+    return o.float().cpu().numpy(), lse.cpu().numpy(), bits
+
+
+def check_prefill(cfg, q, k, v, lam, units=None, causal=True):
+    """Compare all tiles (units=None) or the given (b,h,t) units."""
+    o, lse, bits = run_prefill(q, k, v, lam, causal)
+    skip = bs.unpack_bits(bits, cfg.n_b).numpy()
+    r = oracle.prefill(q, k, v, cfg.scale, lam, 128, 128, causal, units=units)
+    sel = np.zeros((cfg.B, cfg.Hq, cfg.n_t), dtype=bool)
+    if units is None:
+        sel[:] = True
+    else:
+        sel.reshape(-1)[np.asarray(units)] = True
+    n_bad, flips = compare_bits(skip[sel], r["skip"][sel], r["margin"][sel], lam)
+    assert n_bad == 0, f"{n_bad} skip bits differ outside the margin band"
+    if flips.any():
+        forced = np.zeros_like(r["skip"])
+        forced[sel] = skip[sel]
+        r = oracle.prefill(q, k, v, cfg.scale, lam, 128, 128, causal, units=units,
+                           force_skip=forced)
+    rows = np.repeat(sel, 128, axis=2)[:, :, :cfg.T]
+    check_outputs(o[rows], r["o"][rows], lse[rows], r["lse"][rows], "bf16", "prefill")
+    trav = np.isfinite(r["margin"][sel])
+    return float(skip[sel][trav].mean()), int(flips.sum())
+
+
+@pytest.mark.parametrize("T", [128, 640, 1000])
+def test_prefill_tc_planted(T):
+    cfg = W.GQA_PREFILL_16K.with_(T=T, Hq=4, Hkv=2, B=2, seed=51)
+    q, k, v = W.prefill_inputs(cfg)
+    for lam in (0.0, 1e-12, 1e-8, 1e-4):
+        check_prefill(cfg, q, k, v, lam)
+
+
+@pytest.mark.parametrize("lam", [0.0, 1e-3, 3e-2, 0.3])
+def test_prefill_tc_temperate_mixtures(lam):
+    cfg = W.temperate(W.GQA_PREFILL_16K.with_(T=1536, Hq=8, Hkv=2, seed=52))
+    q, k, v = W.prefill_inputs(cfg)
+    check_prefill(cfg, q, k, v, lam)
+
+
+def test_prefill_tc_rescale_path():
+    """Scores whose running max keeps rising (keys drift along the query
+    direction), so the exp reference moves by more than 2^8 many times."""
+    g = torch.Generator().manual_seed(53)
+    T, d = 1280, 128
+    u = torch.randn(d, generator=g)
+    u = u / u.norm()
+    ramp = torch.linspace(0, 60, T)[:, None] * u[None, :] * (d ** 0.5) / 8
+    q = (torch.randn(1, 2, T, d, generator=g) + 4 * u).to(torch.bfloat16)
+    k = (torch.randn(1, 1, T, d, generator=g) + ramp).to(torch.bfloat16)
+    v = torch.randn(1, 1, T, d, generator=g).to(torch.bfloat16)
+    cfg = W.GQA_PREFILL_16K.with_(T=T, Hq=2, Hkv=1)
+    for lam in (0.0, 1e-6):
+        check_prefill(cfg, q, k, v, lam)
+
+
+def test_prefill_tc_noncausal_ragged():
+    cfg = W.temperate(W.GQA_PREFILL_16K.with_(T=700, Hq=4, Hkv=1, causal=False, seed=54))
+    q, k, v = W.prefill_inputs(cfg)
+    for lam in (0.0, 1e-2):
+        check_prefill(cfg, q, k, v, lam, causal=False)
+
+
+def _sample_units(cfg, n_heads, seed):
+    rng = np.random.default_rng(seed)
+    heads = rng.choice(cfg.Hq, n_heads, replace=False)
+    tiles = [0, 1, cfg.n_t // 2, cfg.n_t - 2, cfg.n_t - 1]
+    return sorted({int(h) * cfg.n_t + t for h in heads for t in tiles})
+
+
+@pytest.mark.parametrize("target", ["0.0", "0.7"])
+def test_prefill_tc_full_size_16k(target):
+    """B=1, 32/8 heads, T=16384 (the benchmark's launch), sampled tiles."""
+    cfg = W.GQA_PREFILL_16K
+    q, k, v = W.prefill_inputs(cfg)
+    lam = 0.0 if target == "0.0" else _lambda(cfg.name, target)
+    sparsity, flips = check_prefill(cfg, q, k, v, lam, units=_sample_units(cfg, 3, 7))
+    if target == "0.7":
+        assert 0.5 <= sparsity <= 0.9, sparsity
+
+
+def test_prefill_tc_full_size_64k_sampled():
+    cfg = W.GQA_PREFILL_64K
+    q, k, v = W.prefill_inputs(cfg)
+    lam = _lambda(cfg.name, "0.7")
+    units = [cfg.n_t - 1, cfg.n_t // 2, 5 * cfg.n_t + cfg.n_t - 1]
+    check_prefill(cfg, q, k, v, lam, units=units)
