@@ -1,0 +1,482 @@
+"""Benchmark of softmax-threshold block-skipping attention on one GB300.
+
+One step is one pass of the hot path over resident synthetic inputs:
+  * causal GQA prefill, B=1, Hq=32, Hkv=8, d=128, T=16384, bf16, Br=Bc=128;
+  * split-KV decode, B=16, Hq=32, Hkv=8, d=128, L=32768, bf16, Bc=128,
+    8 splits, then the LSE merge;
+both at the threshold that gives ~70 % block sparsity (stored in
+tests/golden/lambdas.json, computed by the fp64 oracle alone).
+
+The JSON line's ``value`` is prefill dense-equivalent TFLOP/s
+(4 * d * Hq * T(T+1)/2 per call, i.e. the causal work of dense attention);
+decode tokens/s and GB/s are in ``decode``.  Kernel durations come from CUDA
+events on the launching stream; L2 is flushed (a 512 MB write) before every
+timed launch.  ``--impl reference`` times the fp64 CPU oracle on a bounded
+sample of the same prefill workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+import torch.distributed as dist  # noqa: E402
+
+from block_sparse_attention_online_gb300 import workloads as W  # noqa: E402
+
+METRIC = "skip-softmax attn: prefill dense-equiv TFLOP/s, decode tok/s & GB/s @~70% skip"
+PREFILL = W.GQA_PREFILL_16K
+DECODE = W.GQA_DECODE_32K
+TARGET = "0.7"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def lambdas():
+    with open(os.path.join(ROOT, "tests", "golden", "lambdas.json")) as f:
+        return json.load(f)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- work model --
+def prefill_flops(cfg):
+    """Dense-equivalent FLOPs of one causal prefill call, and executed FLOPs of
+    the tile loop: every traversed (tile, block) pair runs QK^T (2*Br*Bc*d);
+    kept pairs also run P.V (2*Br*Bc*d)."""
+    dense = 4.0 * cfg.d * cfg.Hq * cfg.B * cfg.T * (cfg.T + 1) / 2
+    per_pair = 2.0 * cfg.Br * cfg.Bc * cfg.d
+    return dense, per_pair
+
+
+def traversed_pairs(cfg):
+    n_t = cfg.n_t
+    per_head = sum(min(cfg.n_b, (min(cfg.T, (t + 1) * cfg.Br) - 1) // cfg.Bc + 1)
+                   for t in range(n_t))
+    return per_head * cfg.B * cfg.Hq
+
+
+def decode_bytes(cfg, kept_blocks, total_blocks):
+    """HBM bytes of one decode call: every K block, the V blocks of kept
+    (b, KV head, split, block) units, the queries and the fp32 partials."""
+    elt = 2
+    kv_block = cfg.Bc * cfg.dk * elt
+    v_block = cfg.Bc * cfg.dv * elt
+    q = cfg.B * cfg.Hq * cfg.dk * elt
+    part = cfg.B * cfg.Hq * cfg.n_splits * (cfg.dv + 1) * 4
+    return total_blocks * kv_block + kept_blocks * v_block + q + part
+
+
+# ------------------------------------------------------------------ clocks --
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), float(f[3]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v == "Active"})
+        loaded = [r for r in rows if r[2] > 300] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": rows[0][1],
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------- GPU arm --
+def timed_launches(fn, n_warm, n_timed, flush, stream):
+    """Durations (ms) of n_timed launches of fn, L2 flushed before each."""
+    for _ in range(n_warm):
+        fn()
+    durs = []
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n_timed)]
+    for i in range(n_timed):
+        flush.zero_()
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        durs.append(a.elapsed_time(b))
+    return durs
+
+
+def run_gpu(args, rank, world):
+    from block_sparse_attention_online_gb300 import binding as bs
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    lam = lambdas()
+    pk, pk_kind = peaks()
+    lp = {t: lam[PREFILL.name][t]["lambda"] for t in ("0.0", "0.5", "0.7", "0.85")
+          if t in lam[PREFILL.name]}
+    ld = {t: lam[DECODE.name][t]["lambda"] for t in ("0.0", "0.7")}
+
+    # inputs resident in HBM
+    q, k, v = W.prefill_inputs(PREFILL)
+    dq, dk_, dv_ = (x.to(dev) for x in (q, k, v))
+    qd, kd, vd = W.decode_inputs(DECODE)
+    dqd, dkd, dvd = (x.to(dev) for x in (qd, kd, vd))
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    P = PREFILL
+    po = torch.empty(P.B, P.Hq, P.T, P.d, dtype=torch.bfloat16, device=dev)
+    plse = torch.empty(P.B, P.Hq, P.T, dtype=torch.float32, device=dev)
+    pbits = torch.empty(bs.prefill_bitmap_shape(P.B, P.Hq, P.T, P.Br, P.Bc), dtype=torch.int32,
+                        device=dev)
+    D = DECODE
+    op = torch.empty(D.B, D.Hq, D.n_splits, D.dv, dtype=torch.float32, device=dev)
+    lpart = torch.empty(D.B, D.Hq, D.n_splits, dtype=torch.float32, device=dev)
+    dbits = torch.empty(bs.decode_bitmap_shape(D.B, D.Hkv, D.L, D.Bc, D.n_splits),
+                        dtype=torch.int32, device=dev)
+    do = torch.empty(D.B, D.Hq, D.dv, dtype=torch.bfloat16, device=dev)
+    dlse = torch.empty(D.B, D.Hq, dtype=torch.float32, device=dev)
+
+    def prefill(lmb):
+        return lambda: bs.attn_skip_prefill(dq, dk_, dv_, lmb, P.Br, P.Bc, True,
+                                            out=(po, plse, pbits))
+
+    def decode(lmb):
+        return lambda: bs.attn_skip_decode(dqd, dkd, dvd, lmb, D.Bc, D.n_splits,
+                                           out=(op, lpart, dbits))
+
+    def combine():
+        bs.attn_skip_decode_combine(op, lpart, out=(do, dlse))
+
+    pairs = traversed_pairs(P)
+    dense, per_pair = prefill_flops(P)
+    n_b = -(-D.L // D.Bc)
+    d_blocks = D.B * D.Hkv * n_b
+
+    # prefill sweep: lambda = 0 and the 50/70/85 % thresholds
+    sweep = {}
+    for t, lmb in lp.items():
+        durs = timed_launches(prefill(lmb), args.warmup, args.steps, flush, stream)
+        bits = bs.unpack_bits(pbits, P.n_b)
+        skipped = int(bits.sum())
+        kept = pairs - skipped
+        executed = per_pair * (pairs + kept)
+        ms = statistics.mean(durs)
+        sweep[t] = {"lambda": lmb, "sparsity": skipped / pairs, "ms": ms,
+                    "dense_equiv_tflops": dense / ms / 1e9,
+                    "executed_tflops": executed / ms / 1e9, "executed_flops": executed}
+    for t in sweep:
+        sweep[t]["speedup_vs_lambda0"] = sweep["0.0"]["ms"] / sweep[t]["ms"]
+    dsweep = {}
+    for t, lmb in ld.items():
+        durs = timed_launches(decode(lmb), args.warmup, args.steps, flush, stream)
+        cdurs = timed_launches(combine, args.warmup, args.steps, flush, stream)
+        bits = bs.unpack_bits(dbits, -(-n_b // D.n_splits))
+        skipped = int(bits.sum())
+        kept = d_blocks - skipped
+        byts = decode_bytes(D, kept, d_blocks)
+        ms, cms = statistics.mean(durs), statistics.mean(cdurs)
+        dsweep[t] = {"lambda": lmb, "sparsity": skipped / d_blocks, "ms_decode": ms,
+                     "ms_combine": cms, "tok_per_s": D.B / ((ms + cms) / 1e3),
+                     "gbs": byts / ms / 1e6, "bytes": byts}
+    for t in dsweep:
+        dsweep[t]["speedup_vs_lambda0"] = ((dsweep["0.0"]["ms_decode"] + dsweep["0.0"]["ms_combine"])
+                                          / (dsweep[t]["ms_decode"] + dsweep[t]["ms_combine"]))
+
+    # ---- the timed region: K steps of the whole hot path at ~70 % ---------
+    fp, fd = prefill(lp[TARGET]), decode(ld[TARGET])
+    for _ in range(args.warmup):
+        fp(); fd(); combine()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            fp()
+            ev[i][1].record(stream)
+            fd()
+            ev[i][2].record(stream)
+            combine()
+            ev[i][3].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    p_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    d_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    c_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    step_ms = statistics.mean(a + b + c for a, b, c in zip(p_ms, d_ms, c_ms))
+    p_avg, d_avg, c_avg = statistics.mean(p_ms), statistics.mean(d_ms), statistics.mean(c_ms)
+    p_avg, d_avg, c_avg, step_ms = (max_over_ranks(x, world) for x in (p_avg, d_avg, c_avg,
+                                                                         step_ms))
+    s70 = sweep[TARGET]
+    value = world * dense / p_avg / 1e9
+    executed_tflops = s70["executed_flops"] / p_avg / 1e9
+    dec = dsweep[TARGET]
+    dec_gbs = dec["bytes"] / d_avg / 1e6
+
+    # ---- end to end: pinned host buffers, copies inside the timed region --
+    e2e = end_to_end(args, bs, dev, stream, q, k, v, lp[TARGET])
+
+    peak_tf = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    peak_hbm = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": f"{P.name}+{D.name}", "prefill": f"B{P.B} Hq{P.Hq} Hkv{P.Hkv} "
+                   f"d{P.d} T{P.T} causal Br{P.Br} Bc{P.Bc}",
+                   "decode": f"B{D.B} Hq{D.Hq} Hkv{D.Hkv} d{D.dk} L{D.L} Bc{D.Bc} "
+                   f"splits{D.n_splits}", "target_sparsity": float(TARGET),
+                   "l2": "flushed before every timed step (512 MB write)",
+                   "parallelism": f"replicas x{world}"},
+        "prefill": {"ms": round(p_avg, 4), "lambda": lp[TARGET],
+                    "sparsity": round(s70["sparsity"], 4),
+                    "dense_equiv_tflops": round(value / world, 2),
+                    "executed_tflops": round(executed_tflops, 2),
+                    "sweep": {t: {kk: (round(vv, 5) if isinstance(vv, float) else vv)
+                                  for kk, vv in s.items()} for t, s in sweep.items()}},
+        "decode": {"ms": round(d_avg, 4), "ms_combine": round(c_avg, 4),
+                   "lambda": ld[TARGET], "sparsity": round(dec["sparsity"], 4),
+                   "tok_per_s": round(world * D.B / ((d_avg + c_avg) / 1e3), 1),
+                   "gbs": round(dec_gbs, 1), "hbm_frac": round(dec_gbs / peak_hbm, 4),
+                   "sweep": {t: {kk: (round(vv, 5) if isinstance(vv, float) else vv)
+                                 for kk, vv in s.items()} for t, s in dsweep.items()}},
+        "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel",
+                     "achieved": round(executed_tflops, 2), "peak": peak_tf,
+                     "peak_kind": f"bf16 dense burst ({pk_kind})", "unit": "TFLOP/s",
+                     "frac": round(executed_tflops / peak_tf, 4),
+                     "frac_sustained": round(executed_tflops / pk.get(
+                         "bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]), 4),
+                     "traffic": None},
+        "decode_roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel",
+                            "achieved": round(dec_gbs, 1), "peak": peak_hbm, "unit": "GB/s",
+                            "frac": round(dec_gbs / peak_hbm, 4), "traffic": None},
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    return line
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def end_to_end(args, bs, dev, stream, q, k, v, lmb):
+    """Prefill through the C ABI from pinned host buffers: the host->device
+    copies of Q, K, V and the device->host copy of O and LSE are inside the
+    timed region of every step."""
+    P = PREFILL
+    hq, hk, hv = (x.pin_memory() for x in (q, k, v))
+    ho = torch.empty(P.B, P.Hq, P.T, P.d, dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty(P.B, P.Hq, P.T, dtype=torch.float32).pin_memory()
+    dq, dk_, dv_ = (torch.empty_like(x, device=dev) for x in (q, k, v))
+
+    def step():
+        dq.copy_(hq, non_blocking=True)
+        dk_.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        o, lse, _ = bs.attn_skip_prefill(dq, dk_, dv_, lmb, P.Br, P.Bc, True)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / args.steps
+    dense, _ = prefill_flops(P)
+    h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv))
+    d2h = ho.numel() * ho.element_size() + hl.numel() * hl.element_size()
+    return {"value": round(dense / ms / 1e9, 2), "unit": "TFLOP/s", "ms": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------ oracle (CPU) --
+def oracle_sample_units(n_tiles):
+    """The n_tiles longest causal tiles of query head 0 (a bounded sample of
+    the prefill workload)."""
+    P = PREFILL
+    return list(range(P.n_t - n_tiles, P.n_t))
+
+
+def oracle_prefill_rate(n_tiles, q=None, k=None, v=None):
+    import oracle
+    P = PREFILL
+    lam = lambdas()[P.name][TARGET]["lambda"]
+    if q is None:
+        q, k, v = W.prefill_inputs(P.with_(Hq=P.G, Hkv=1))  # KV head 0 and its query heads
+    units = oracle_sample_units(n_tiles)
+    t0 = time.perf_counter()
+    oracle.prefill(q[:, :1], k, v, P.scale, lam, P.Br, P.Bc, True, units=units)
+    dt = time.perf_counter() - t0
+    dense = sum(4.0 * P.d * tile_visible_pairs(P, t) for t in units)
+    return dense / dt / 1e12, dt, min(oracle.num_threads(), len(units)), (q, k, v)
+
+
+def tile_visible_pairs(P, t):
+    """(row, key) pairs a causal tile attends to: sum of (r + 1) over its rows."""
+    r0, r1 = t * P.Br, min(P.T, (t + 1) * P.Br)
+    return (r1 * (r1 + 1) - r0 * (r0 + 1)) / 2
+
+
+def cpu_baseline(n_tiles=128):
+    rate, dt, cores, _ = oracle_prefill_rate(n_tiles)
+    return {"value": round(rate, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle, prefill query head 0, the {n_tiles} longest causal tiles "
+                      f"of T={PREFILL.T} (1/{PREFILL.Hq * PREFILL.n_t // n_tiles} of the "
+                      f"workload) at the ~70% threshold, {dt:.1f} s"}
+
+
+def run_reference(args):
+    """The reference arm: the fp64 CPU oracle as it stands, each step a bounded
+    sample (the 4 longest tiles of one query head) of the prefill workload."""
+    n_tiles = 16
+    rate, dt, cores, cache = oracle_prefill_rate(n_tiles)
+    for _ in range(max(0, args.warmup - 1)):
+        oracle_prefill_rate(n_tiles, *cache)
+    rates, times = [], []
+    for _ in range(args.steps):
+        r, t, _, _ = oracle_prefill_rate(n_tiles, *cache)
+        rates.append(r)
+        times.append(t)
+    value = statistics.mean(rates)
+    sample = (f"fp64 oracle, prefill query head 0, the {n_tiles} longest causal tiles of "
+              f"T={PREFILL.T} per step")
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * statistics.mean(times), 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{PREFILL.name} (sampled tiles)",
+                       "target_sparsity": float(TARGET)},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": cores,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def run_profile_case(args):
+    """Warm-up launches then one launch of a single kernel at the ~70 %
+    threshold, for an ncu capture (prefill: the T=16384 workload, inputs 201 MB;
+    decode: the B=16, L=32768 workload, 2.1 GB)."""
+    from block_sparse_attention_online_gb300 import binding as bs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    lam = lambdas()
+    if args.profile == "prefill":
+        q, k, v = (x.to(dev) for x in W.prefill_inputs(PREFILL))
+        lmb = lam[PREFILL.name][TARGET]["lambda"]
+        fn = lambda: bs.attn_skip_prefill(q, k, v, lmb, PREFILL.Br, PREFILL.Bc, True)  # noqa: E731
+    else:
+        q, k, v = (x.to(dev) for x in W.decode_inputs(DECODE))
+        lmb = lam[DECODE.name][TARGET]["lambda"]
+
+        def fn():
+            op, lp, _ = bs.attn_skip_decode(q, k, v, lmb, DECODE.Bc, DECODE.n_splits)
+            bs.attn_skip_decode_combine(op, lp)
+    for _ in range(args.warmup + 1):
+        fn()
+    torch.cuda.synchronize()
+    bs.attn_skip_last_device_error()
+    print(json.dumps({"profile": args.profile, "launches": args.warmup + 1}))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=("prefill", "decode"),
+                    help="only warm up and launch one kernel (for ncu captures)")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    try:
+        if args.profile:
+            run_profile_case(args)
+            return
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps(run_reference(args)), flush=True)
+            return
+        line = run_gpu(args, rank, world)
+        if rank == 0:
+            if not args.no_cpu_baseline:
+                line["cpu_baseline"] = cpu_baseline()
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
