@@ -2,23 +2,26 @@
 // Br = Bc = 128), tcgen05 MMAs accumulating in TMEM, operands staged by TMA.
 //
 // Method: the BLASST page, sections "铺垫：FlashAttention 的在线 softmax"
-// (Eqs. 2-4), "BLASST 的判定准则" (Eq. 5), "判定本身：几乎零成本的秘密" (the
-// per-row predicate, a warp vote and a tile-wide AND) and "Prefill 内核：砍计算"
-// (a skipped block costs no exponentials, no row sum and no P.V product).  The
-// value tile of a block is loaded only once the block is known to be kept.
+// (Eqs. 2-4), "BLASST 的判定准则" (Eq. 5), "判定本身：几乎零成本的秘密" (a per-row
+// predicate, a warp vote and a tile-wide AND) and "Prefill 内核：砍计算" (a
+// skipped block costs no exponentials, no row sum and no P.V product).  Unlike
+// the page's prefill kernel, the value tile of a block is loaded only once the
+// block is known to be kept; the decision of block j+1 is taken before the
+// exponentials of block j so that load has time to land.
 //
 // One CTA per (batch, query head, query tile), longest causal tiles first.
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread i owns query row i (TMEM lane i).  Per block it
-//              reads the S row from TMEM, masks, takes the row max, votes,
-//              and for kept blocks writes P (bf16) to shared memory, keeps the
-//              row sum and rescales O in TMEM when the exp reference moves
-//              by more than 2^8; then the epilogue O / l and LSE;
-//   warp 4     TMA producer: Q once, K_j for every block, V_j for kept blocks;
-//   warp 5     MMA issuer: S_j = Q K_j^T into one of two TMEM S buffers, and
-//              O += P_j V_j for kept blocks, QK of block j+1 issued before the
-//              PV of block j so the softmax of one block overlaps the MMAs.
-// TMEM columns: S buffers [0,128) and [128,256), O [256,384).
+// Warp roles (224 threads):
+//   warps 0-3  softmax: thread i owns query row i (TMEM lane i).  Per block:
+//              decide(j+1) = row max of S_{j+1} (read from TMEM in 32-column
+//              chunks), the vote and the tile AND; then, if block j is kept,
+//              P_j = exp2(S_j - ref) to shared memory (bf16), the row sum, and
+//              an O rescale in TMEM when the exp reference moves by > 2^8;
+//   warp 4     TMA producer of Q (once) and K_j (every block);
+//   warp 5     MMA issuer: S_j = Q K_j^T two blocks ahead of the softmax, and
+//              O += P_j V_j for kept blocks;
+//   warp 6     TMA producer of V_j, for kept blocks only, as soon as the
+//              block's decision is known.
+// TMEM columns: three S buffers [0,384), O [384,512).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -31,14 +34,16 @@ namespace {
 
 using namespace tc;
 
-constexpr int D = 128;       // head size of keys and values
-constexpr int BM = 128;      // query rows per tile
-constexpr int BN = 128;      // keys per block
-constexpr int NK = 2;        // K stages
-constexpr int NV = 2;        // V stages
-constexpr int NDEC = 4;      // decision ring
-constexpr int NTHREADS = 192;
-constexpr uint32_t TILE_BYTES = BM * D * 2;    // 32 KB: one 128 x 128 bf16 tile
+constexpr int D = 128;        // head size of keys and values
+constexpr int BM = 128;       // query rows per tile
+constexpr int BN = 128;       // keys per block
+constexpr int NK = 2;         // K stages
+constexpr int NV = 2;         // V stages
+constexpr int NS = 3;         // TMEM S buffers
+constexpr int NDEC = 4;       // decision ring
+constexpr int NTHREADS = 224;
+constexpr int WARP_K = 4, WARP_MMA = 5, WARP_V = 6;
+constexpr uint32_t TILE_BYTES = BM * D * 2;      // 32 KB: one 128 x 128 bf16 tile
 constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;  // one 64-column swizzled box
 constexpr uint32_t SMEM_Q = 0;
 constexpr uint32_t SMEM_K = SMEM_Q + TILE_BYTES;
@@ -47,18 +52,19 @@ constexpr uint32_t SMEM_P = SMEM_V + NV * TILE_BYTES;
 constexpr uint32_t SMEM_BYTES = SMEM_P + 2 * TILE_BYTES;  // 224 KB
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;       // + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_O = 256;
+constexpr uint32_t TMEM_O = NS * BN;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // exp reference may lag the max by 2^8
 constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);  // K: K-major
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 1);   // V: MN-major
+constexpr uint32_t NEG_INF_BITS = 0xff800000u;
 
 struct Shared {
   uint64_t q_full;
   uint64_t k_full[NK], k_empty[NK];
   uint64_t v_full[NV], v_empty[NV];
-  uint64_t s_full[2], s_free[2];
+  uint64_t s_full[NS], s_free[NS];
   uint64_t p_full[2], pv_done[2];
   uint64_t dec_full[NDEC];
   uint64_t vote_full[2];
@@ -67,7 +73,6 @@ struct Shared {
   uint32_t tmem_base;
   int abort;
 };
-
 
 // Descriptor of k-step kk (16 columns) of a K-major 128 x 128 bf16 tile held as
 // two 128-byte-swizzled boxes of 64 columns: box kk/4, 32-byte step kk%4,
@@ -82,6 +87,52 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
 // (SBO), the second 64-value half 16 KB further (LBO).
 __device__ __forceinline__ uint64_t vmajor_desc(uint32_t tile, int kk) {
   return smem_desc_sw128(tile + (uint32_t)kk * 2048u, HALF_BYTES, 1024u);
+}
+
+// Mask the 32 scores of a chunk whose first key is kbase: causal (key > row)
+// or, without causality, keys past T.
+__device__ __forceinline__ void mask_chunk(uint32_t (&s)[32], int kbase, int row, int causal,
+                                           int T) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const int key = kbase + i;
+    if (causal ? key > row : key >= T) s[i] = NEG_INF_BITS;
+  }
+}
+
+__device__ __forceinline__ float chunk_max(const uint32_t (&s)[32]) {
+  float m[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i)
+    m[i] = fmax3(__uint_as_float(s[3 * i]), __uint_as_float(s[3 * i + 1]),
+                 __uint_as_float(s[3 * i + 2]));
+  m[10] = fmaxf(__uint_as_float(s[30]), __uint_as_float(s[31]));
+  const float a = fmax3(m[0], m[1], m[2]), b = fmax3(m[3], m[4], m[5]);
+  const float c = fmax3(m[6], m[7], m[8]), d = fmaxf(m[9], m[10]);
+  return fmaxf(fmax3(a, b, c), d);
+}
+
+// P = exp2(s * sl2 - ref) for one 32-key chunk: accumulate the row sum and
+// store the bf16 values into the 128-byte-swizzled P tile (chunk c holds
+// 16-byte pieces 4c..4c+3 of the row; piece ch lives in box ch/8, slot
+// (ch%8) XOR (row%8)).
+__device__ __forceinline__ void chunk_exp_store(const uint32_t (&s)[32], float sl2, float neg_ref,
+                                                float (&acc)[4], uint32_t prow, int c, int r) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float p0 = ex2(fmaf(__uint_as_float(s[2 * i]), sl2, neg_ref));
+    const float p1 = ex2(fmaf(__uint_as_float(s[2 * i + 1]), sl2, neg_ref));
+    acc[i & 3] += p0 + p1;
+    pk[i] = pack_bf16x2(p0, p1);
+  }
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    const int ch = c * 4 + q4;
+    const uint32_t addr =
+        prow + (uint32_t)(ch >> 3) * HALF_BYTES + ((uint32_t)((ch & 7) ^ (r & 7)) << 4);
+    st_shared_v4(addr, pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+  }
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1)
@@ -104,6 +155,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int last_row = min(a.T, row0 + BM) - 1;
   const int nblk = a.causal ? last_row / BN + 1 : a.n_b;
   volatile int *abort = &sh.abort;
+  const int zq = b * a.Hq + h, zkv = b * a.Hkv + hk;
 
   if (tid == 0) {
     mbar_init(smem_u32(&sh.q_full), 1);
@@ -115,127 +167,130 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(smem_u32(&sh.v_full[i]), 1);
       mbar_init(smem_u32(&sh.v_empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&sh.s_full[i]), 1);
       mbar_init(smem_u32(&sh.s_free[i]), 4);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh.p_full[i]), 4);
       mbar_init(smem_u32(&sh.pv_done[i]), 1);
+      mbar_init(smem_u32(&sh.vote_full[i]), 4);
     }
     for (int i = 0; i < NDEC; ++i) mbar_init(smem_u32(&sh.dec_full[i]), 1);
-    for (int i = 0; i < 2; ++i) mbar_init(smem_u32(&sh.vote_full[i]), 4);
     sh.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) tmem_alloc(smem_u32(&sh.tmem_base), TMEM_COLS);
+  if (warp == WARP_MMA) tmem_alloc(smem_u32(&sh.tmem_base), TMEM_COLS);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = sh.tmem_base;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer --
+  if (warp == WARP_K) {
+    // -------------------------------------------------------- Q/K producer --
     if (lane == 0) {
       prefetch_tmap(&tm_q);
       prefetch_tmap(&tm_k);
-      prefetch_tmap(&tm_v);
-      const uint64_t keep_l2 = policy_evict_last();   // K/V are re-read by other tiles/heads
-      const uint64_t stream_l2 = policy_evict_first(); // Q is read once
-      const int zq = b * a.Hq + h, zkv = b * a.Hkv + hk;
+      const uint64_t keep_l2 = policy_evict_last();    // K is re-read by other tiles/heads
+      const uint64_t stream_l2 = policy_evict_first();  // Q is read once
       mbar_expect_tx(smem_u32(&sh.q_full), TILE_BYTES);
       tma_load_3d(base + SMEM_Q, &tm_q, smem_u32(&sh.q_full), 0, row0, zq, stream_l2);
       tma_load_3d(base + SMEM_Q + HALF_BYTES, &tm_q, smem_u32(&sh.q_full), 64, row0, zq,
                   stream_l2);
-      int vi = 0, ki = 0;
-      for (int j = 0; j <= nblk && !*abort; ++j) {
-        if (j < nblk) {  // K_j
-          const int s = j % NK;
-          if (j >= NK &&
-              !mbar_wait(smem_u32(&sh.k_empty[s]), ((j / NK) - 1) & 1, abort, a.err, kErrTimeout))
-            break;
-          const uint32_t dst = base + SMEM_K + s * TILE_BYTES;
-          mbar_expect_tx(smem_u32(&sh.k_full[s]), TILE_BYTES);
-          tma_load_3d(dst, &tm_k, smem_u32(&sh.k_full[s]), 0, j * BN, zkv, keep_l2);
-          tma_load_3d(dst + HALF_BYTES, &tm_k, smem_u32(&sh.k_full[s]), 64, j * BN, zkv, keep_l2);
-          ++ki;
-        }
-        if (j >= 1) {  // V_{j-1}, only if block j-1 is kept
-          const int jd = j - 1;
-          if (!mbar_wait(smem_u32(&sh.dec_full[jd % NDEC]), (jd / NDEC) & 1, abort, a.err,
-                         kErrTimeout))
-            break;
-          if (sh.dec[jd % NDEC]) {
-            const int s = vi % NV;
-            if (vi >= NV && !mbar_wait(smem_u32(&sh.v_empty[s]), ((vi / NV) - 1) & 1, abort,
-                                       a.err, kErrTimeout))
-              break;
-            const uint32_t dst = base + SMEM_V + s * TILE_BYTES;
-            mbar_expect_tx(smem_u32(&sh.v_full[s]), TILE_BYTES);
-            tma_load_3d(dst, &tm_v, smem_u32(&sh.v_full[s]), 0, jd * BN, zkv, keep_l2);
-            tma_load_3d(dst + HALF_BYTES, &tm_v, smem_u32(&sh.v_full[s]), 64, jd * BN, zkv,
-                        keep_l2);
-            ++vi;
-          }
-        }
+      int ki = 0;
+      for (int j = 0; j < nblk && !*abort; ++j) {
+        const int s = j % NK;
+        if (j >= NK &&
+            !mbar_wait(smem_u32(&sh.k_empty[s]), ((j / NK) - 1) & 1, abort, a.err, kErrTimeout))
+          break;
+        const uint32_t dst = base + SMEM_K + s * TILE_BYTES;
+        mbar_expect_tx(smem_u32(&sh.k_full[s]), TILE_BYTES);
+        tma_load_3d(dst, &tm_k, smem_u32(&sh.k_full[s]), 0, j * BN, zkv, keep_l2);
+        tma_load_3d(dst + HALF_BYTES, &tm_k, smem_u32(&sh.k_full[s]), 64, j * BN, zkv, keep_l2);
+        ++ki;
       }
-      // Drain: the last load issued into each slot has landed before the CTA
-      // may exit (earlier loads of a slot were consumed before it was reused).
+      // Drain: the last load issued into each slot has landed before exit
+      // (earlier loads of a slot were consumed before the slot was reused).
       mbar_wait_drain(smem_u32(&sh.q_full), 0);
       for (int s = 0; s < NK && s < ki; ++s) {
         const int last = s + ((ki - 1 - s) / NK) * NK;
         mbar_wait_drain(smem_u32(&sh.k_full[s]), (last / NK) & 1);
+      }
+    }
+  } else if (warp == WARP_V) {
+    // ---------------------------------------------------------- V producer --
+    if (lane == 0) {
+      prefetch_tmap(&tm_v);
+      const uint64_t keep_l2 = policy_evict_last();
+      int vi = 0;
+      for (int j = 0; j < nblk && !*abort; ++j) {
+        if (!mbar_wait(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
+                       kErrTimeout))
+          break;
+        if (!sh.dec[j % NDEC]) continue;
+        const int s = vi % NV;
+        if (vi >= NV &&
+            !mbar_wait(smem_u32(&sh.v_empty[s]), ((vi / NV) - 1) & 1, abort, a.err, kErrTimeout))
+          break;
+        const uint32_t dst = base + SMEM_V + s * TILE_BYTES;
+        mbar_expect_tx(smem_u32(&sh.v_full[s]), TILE_BYTES);
+        tma_load_3d(dst, &tm_v, smem_u32(&sh.v_full[s]), 0, j * BN, zkv, keep_l2);
+        tma_load_3d(dst + HALF_BYTES, &tm_v, smem_u32(&sh.v_full[s]), 64, j * BN, zkv, keep_l2);
+        ++vi;
       }
       for (int s = 0; s < NV && s < vi; ++s) {
         const int last = s + ((vi - 1 - s) / NV) * NV;
         mbar_wait_drain(smem_u32(&sh.v_full[s]), (last / NV) & 1);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == WARP_MMA) {
     // ---------------------------------------------------------------- MMA --
     if (lane == 0) {
       bool ok = mbar_wait(smem_u32(&sh.q_full), 0, abort, a.err, kErrTimeout);
       fence_after_sync();
       int kc = 0, vi = 0;
-      for (int j = 0; ok && j <= nblk; ++j) {
-        if (j < nblk) {  // S_j = Q K_j^T
-          const int s = j % NK, sb = j & 1;
-          ok = mbar_wait(smem_u32(&sh.k_full[s]), (j / NK) & 1, abort, a.err, kErrTimeout);
-          if (ok && j >= 2)
-            ok = mbar_wait(smem_u32(&sh.s_free[sb]), ((j >> 1) - 1) & 1, abort, a.err,
-                           kErrTimeout);
-          if (!ok) break;
-          fence_after_sync();
-          const uint32_t ktile = base + SMEM_K + s * TILE_BYTES;
+      // S_j = Q K_j^T into S buffer j % NS.
+      auto issue_qk = [&](int j) -> bool {
+        const int s = j % NK, sb = j % NS;
+        if (!mbar_wait(smem_u32(&sh.k_full[s]), (j / NK) & 1, abort, a.err, kErrTimeout))
+          return false;
+        if (j >= NS && !mbar_wait(smem_u32(&sh.s_free[sb]), ((j / NS) - 1) & 1, abort, a.err,
+                                  kErrTimeout))
+          return false;
+        fence_after_sync();
+        const uint32_t ktile = base + SMEM_K + s * TILE_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_bf16_ss(tmem + sb * BN, kmajor_desc(base + SMEM_Q, kk), kmajor_desc(ktile, kk),
-                        IDESC_QK, kk > 0);
-          mma_commit(smem_u32(&sh.s_full[sb]));
-          mma_commit(smem_u32(&sh.k_empty[s]));
-        }
-        if (j >= 1) {  // O += P_{j-1} V_{j-1} if kept
-          const int jd = j - 1;
-          ok = mbar_wait(smem_u32(&sh.dec_full[jd % NDEC]), (jd / NDEC) & 1, abort, a.err,
-                         kErrTimeout);
-          if (!ok) break;
-          if (sh.dec[jd % NDEC]) {
-            const int pb = kc & 1, vs = vi % NV;
-            ok = mbar_wait(smem_u32(&sh.p_full[pb]), (kc >> 1) & 1, abort, a.err, kErrTimeout);
-            if (ok) ok = mbar_wait(smem_u32(&sh.v_full[vs]), (vi / NV) & 1, abort, a.err,
-                                   kErrTimeout);
-            if (!ok) break;
-            fence_after_sync();
-            const uint32_t ptile = base + SMEM_P + pb * TILE_BYTES;
-            const uint32_t vtile = base + SMEM_V + vs * TILE_BYTES;
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(tmem + sb * BN, kmajor_desc(base + SMEM_Q, kk), kmajor_desc(ktile, kk),
+                      IDESC_QK, kk > 0);
+        mma_commit(smem_u32(&sh.s_full[sb]));
+        mma_commit(smem_u32(&sh.k_empty[s]));
+        return true;
+      };
+      for (int j = 0; ok && j < 2 && j < nblk; ++j) ok = issue_qk(j);
+      for (int i = 0; ok && i < nblk; ++i) {
+        if (i + 2 < nblk && !issue_qk(i + 2)) break;
+        // O += P_i V_i if block i is kept
+        if (!mbar_wait(smem_u32(&sh.dec_full[i % NDEC]), (i / NDEC) & 1, abort, a.err,
+                       kErrTimeout))
+          break;
+        if (!sh.dec[i % NDEC]) continue;
+        const int pb = kc & 1, vs = vi % NV;
+        if (!mbar_wait(smem_u32(&sh.p_full[pb]), (kc >> 1) & 1, abort, a.err, kErrTimeout))
+          break;
+        if (!mbar_wait(smem_u32(&sh.v_full[vs]), (vi / NV) & 1, abort, a.err, kErrTimeout))
+          break;
+        fence_after_sync();
+        const uint32_t ptile = base + SMEM_P + pb * TILE_BYTES;
+        const uint32_t vtile = base + SMEM_V + vs * TILE_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk)
-              mma_bf16_ss(tmem + TMEM_O, kmajor_desc(ptile, kk), vmajor_desc(vtile, kk),
-                          IDESC_PV, (kc > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(smem_u32(&sh.v_empty[vs]));
-            mma_commit(smem_u32(&sh.pv_done[pb]));
-            ++kc;
-            ++vi;
-          }
-        }
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_bf16_ss(tmem + TMEM_O, kmajor_desc(ptile, kk), vmajor_desc(vtile, kk), IDESC_PV,
+                      (kc > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&sh.v_empty[vs]));
+        mma_commit(smem_u32(&sh.pv_done[pb]));
+        ++kc;
+        ++vi;
       }
     }
   } else {
@@ -244,57 +299,67 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int row = row0 + r;
     const bool valid = row < a.T;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const float sl2 = a.scale * kLog2e;        // raw score -> log2 units
-    const float c2 = a.ln_lambda * kLog2e;     // ln(lambda) in log2 units
-    float m2 = -INFINITY;                      // running max (log2 units)
-    float mref = -INFINITY;                    // exp reference (log2 units)
+    const float sl2 = a.scale * kLog2e;     // raw score -> log2 units
+    const float c2 = a.ln_lambda * kLog2e;  // ln(lambda) in log2 units
+    float m2 = -INFINITY;                   // running max (log2 units)
+    float mref = -INFINITY;                 // exp reference (log2 units)
     float l = 0.f;
     int kc = 0;
     uint32_t word = 0;
     uint32_t *bits = a.bits + ((size_t)bh * a.n_t + t) * a.words;
     bool ok = true;
 
-    for (int j = 0; j < nblk; ++j) {
-      const int sb = j & 1;
-      ok = mbar_wait(smem_u32(&sh.s_full[sb]), (j >> 1) & 1, abort, a.err, kErrTimeout);
-      if (!ok) break;
-      fence_after_sync();
-      uint32_t sr[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + sb * BN + c * 32, sr[c]);
-      tmem_wait_ld();
+    auto needs_mask = [&](int j) {
+      const int key0 = j * BN;
+      return a.causal ? (key0 + BN - 1 > row0) : (key0 + BN > a.T);
+    };
+    auto release_s = [&](int j) {
       fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.s_free[sb]));
+      if (lane == 0) mbar_arrive(smem_u32(&sh.s_free[j % NS]));
+    };
 
-      // Mask: causal (key > row) on the diagonal block; keys past T.
-      const int key0 = j * BN;
-      const bool diag = a.causal ? (key0 + BN - 1 > row0) : (key0 + BN > a.T);
-      float mt = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = key0 + c * 32 + i;
-          float s = __uint_as_float(sr[c][i]);
-          if (diag && (a.causal ? key > row : key >= a.T)) s = -INFINITY;
-          sr[c][i] = __float_as_uint(s);
-          mt = fmaxf(mt, s);
-        }
-      }
+    // decide(j): row max of S_j, the vote, the tile AND; returns keep (or -1 on
+    // abort) and this row's updated running max in *mnew_out.
+    auto decide = [&](int j, float *mnew_out) -> int {
+      const int sb = j % NS;
+      if (!mbar_wait(smem_u32(&sh.s_full[sb]), (j / NS) & 1, abort, a.err, kErrTimeout))
+        return -1;
+      fence_after_sync();
+      const bool msk = needs_mask(j);
+      const uint32_t sa = lane_base + sb * BN;
+      uint32_t x[32], y[32];
+      float mt;
+      tmem_ld32(sa, x);
+      tmem_wait_ld_regs(x);
+      tmem_ld32(sa + 32, y);
+      if (msk) mask_chunk(x, j * BN, row, a.causal, a.T);
+      mt = chunk_max(x);
+      tmem_wait_ld_regs(y);
+      tmem_ld32(sa + 64, x);
+      if (msk) mask_chunk(y, j * BN + 32, row, a.causal, a.T);
+      mt = fmaxf(mt, chunk_max(y));
+      tmem_wait_ld_regs(x);
+      tmem_ld32(sa + 96, y);
+      if (msk) mask_chunk(x, j * BN + 64, row, a.causal, a.T);
+      mt = fmaxf(mt, chunk_max(x));
+      tmem_wait_ld_regs(y);
+      if (msk) mask_chunk(y, j * BN + 96, row, a.causal, a.T);
+      mt = fmaxf(mt, chunk_max(y));
       const float mt2 = mt * sl2;
       const float mnew = fmaxf(m2, mt2);
       const float diff = (mt == -INFINITY) ? -INFINITY : mt2 - mnew;
       // Eq. 5 against the updated running max; rows past T are neutral.
       const bool vote = !valid || (diff < c2);
       const unsigned all = __all_sync(0xffffffffu, vote);
+      const int vb = j & 1;
       if (lane == 0) {
-        sh.vote[sb][warp] = (int)all;
-        mbar_arrive(smem_u32(&sh.vote_full[sb]));
+        sh.vote[vb][warp] = (int)all;
+        mbar_arrive(smem_u32(&sh.vote_full[vb]));
       }
-      ok = mbar_wait(smem_u32(&sh.vote_full[sb]), (j >> 1) & 1, abort, a.err, kErrTimeout);
-      if (!ok) break;
-      const bool skip = sh.vote[sb][0] && sh.vote[sb][1] && sh.vote[sb][2] && sh.vote[sb][3];
+      if (!mbar_wait(smem_u32(&sh.vote_full[vb]), (j >> 1) & 1, abort, a.err, kErrTimeout))
+        return -1;
+      const bool skip = sh.vote[vb][0] && sh.vote[vb][1] && sh.vote[vb][2] && sh.vote[vb][3];
       if (tid == 0) {
         sh.dec[j % NDEC] = skip ? 0 : 1;
         mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
@@ -305,9 +370,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       m2 = mnew;
-      if (skip) continue;
+      *mnew_out = mnew;
+      if (skip) release_s(j);  // a skipped block's scores are no longer needed
+      return skip ? 0 : 1;
+    };
 
-      // ---- kept block: exp reference, P, row sum --------------------------
+    // exponentiate(j) for a kept block whose running max after it is mnew.
+    auto exponentiate = [&](int j, float mnew) -> bool {
       bool rescale = false;
       float alpha = 1.f;
       if (mref == -INFINITY) {
@@ -317,49 +386,47 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mref = mnew;
         rescale = true;
       }
-      const float neg_ref = -mref;
-      float rowsum = 0.f;
       const int pb = kc & 1;
       // P buffer pb was last read by the PV of kept block kc-2.
-      if (kc >= 2) {
-        ok = mbar_wait(smem_u32(&sh.pv_done[pb]), ((kc - 2) >> 1) & 1, abort, a.err,
-                       kErrTimeout);
-        if (!ok) break;
-      }
+      if (kc >= 2 && !mbar_wait(smem_u32(&sh.pv_done[pb]), ((kc - 2) >> 1) & 1, abort, a.err,
+                                kErrTimeout))
+        return false;
+      const bool msk = needs_mask(j);
+      const uint32_t sa = lane_base + (j % NS) * BN;
       const uint32_t prow = base + SMEM_P + pb * TILE_BYTES + (uint32_t)r * 128u;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * i]), sl2, neg_ref));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * i + 1]), sl2, neg_ref));
-          rowsum += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        // 32 keys = four 16-byte chunks; chunk ch of the row lives in box ch/8,
-        // 16-byte slot (ch%8) XOR (row%8) (128-byte swizzle).
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          const int ch = c * 4 + q4;
-          const uint32_t addr = prow + (uint32_t)(ch >> 3) * HALF_BYTES +
-                                ((uint32_t)((ch & 7) ^ (r & 7)) << 4);
-          st_shared_v4(addr, pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
-        }
-      }
+      const float neg_ref = -mref;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t x[32], y[32];
+      tmem_ld32(sa, x);
+      tmem_wait_ld_regs(x);
+      tmem_ld32(sa + 32, y);
+      if (msk) mask_chunk(x, j * BN, row, a.causal, a.T);
+      chunk_exp_store(x, sl2, neg_ref, acc, prow, 0, r);
+      tmem_wait_ld_regs(y);
+      tmem_ld32(sa + 64, x);
+      if (msk) mask_chunk(y, j * BN + 32, row, a.causal, a.T);
+      chunk_exp_store(y, sl2, neg_ref, acc, prow, 1, r);
+      tmem_wait_ld_regs(x);
+      tmem_ld32(sa + 96, y);
+      if (msk) mask_chunk(x, j * BN + 64, row, a.causal, a.T);
+      chunk_exp_store(x, sl2, neg_ref, acc, prow, 2, r);
+      tmem_wait_ld_regs(y);
+      release_s(j);  // all of S_j is in registers now
+      if (msk) mask_chunk(y, j * BN + 96, row, a.causal, a.T);
+      chunk_exp_store(y, sl2, neg_ref, acc, prow, 3, r);
       fence_proxy_async_smem();
-      l = l * alpha + rowsum;
+      l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
       // O rescale (warp-wide if any row needs it), after the previous PV landed.
       if (__any_sync(0xffffffffu, rescale) && kc >= 1) {
-        ok = mbar_wait(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort, a.err,
-                       kErrTimeout);
-        if (!ok) break;
+        if (!mbar_wait(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort, a.err,
+                       kErrTimeout))
+          return false;
         fence_after_sync();
-#pragma unroll
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
           tmem_ld32(lane_base + TMEM_O + c * 32, o);
-          tmem_wait_ld();
+          tmem_wait_ld_regs(o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           tmem_st32(lane_base + TMEM_O + c * 32, o);
@@ -370,6 +437,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[pb]));
       ++kc;
+      return true;
+    };
+
+    float mnew_cur = -INFINITY, mnew_next = -INFINITY;
+    int keep_cur = decide(0, &mnew_cur);
+    ok = keep_cur >= 0;
+    for (int j = 0; ok && j < nblk; ++j) {
+      int keep_next = 0;
+      if (j + 1 < nblk) {
+        keep_next = decide(j + 1, &mnew_next);
+        if (keep_next < 0) {
+          ok = false;
+          break;
+        }
+      }
+      if (keep_cur && !exponentiate(j, mnew_cur)) {
+        ok = false;
+        break;
+      }
+      keep_cur = keep_next;
+      mnew_cur = mnew_next;
     }
 
     // ---- epilogue ----------------------------------------------------------
@@ -384,11 +472,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       fence_after_sync();
       const float inv = 1.f / l;
       __nv_bfloat16 *orow = (__nv_bfloat16 *)a.o + ((size_t)bh * a.T + row) * D;
-#pragma unroll
+#pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
         tmem_ld32(lane_base + TMEM_O + c * 32, o);
-        tmem_wait_ld();
+        tmem_wait_ld_regs(o);
         if (valid) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
@@ -407,7 +495,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
   fence_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == WARP_MMA) {
     fence_after_sync();
     tmem_dealloc(tmem, TMEM_COLS);
   }
