@@ -10,18 +10,26 @@
 // exponentials of block j so that load has time to land.
 //
 // One CTA per (batch, query head, query tile), longest causal tiles first.
-// Warp roles (224 threads):
-//   warps 0-3  softmax: thread i owns query row i (TMEM lane i).  Per block:
-//              decide(j+1) = row max of S_{j+1} (read from TMEM in 32-column
-//              chunks), the vote and the tile AND; then, if block j is kept,
-//              P_j = exp2(S_j - ref) to shared memory (bf16), the row sum, and
-//              an O rescale in TMEM when the exp reference moves by > 2^8;
-//   warp 4     TMA producer of Q (once) and K_j (every block);
-//   warp 5     MMA issuer: S_j = Q K_j^T two blocks ahead of the softmax, and
+// Warp roles (352 threads):
+//   warps 0-7  softmax: warps w and w+4 share query rows 32(w%4)..+31 (TMEM
+//              lanes) and own key columns [0,64) and [64,128) of each block.
+//              Per block: decide(j+1) = partial row max of S_{j+1} over the
+//              warp's 64 columns and the half-row vote against the running
+//              max before the block, one barrier round to AND all votes and
+//              exchange the partial maxima; then, if block j is kept,
+//              P_j = exp2(S_j - ref) (bf16) to shared memory, a partial row
+//              sum, and an O rescale of the warp's 64 output columns in TMEM
+//              when the exp reference moves by > 2^8;
+//   warp 8     TMA producer of Q (once) and K_j (every block);
+//   warp 9     MMA issuer: S_j = Q K_j^T two blocks ahead of the softmax, and
 //              O += P_j V_j for kept blocks;
-//   warp 6     TMA producer of V_j, for kept blocks only, as soon as the
+//   warp 10    TMA producer of V_j, for kept blocks only, as soon as the
 //              block's decision is known.
 // TMEM columns: three S buffers [0,384), O [384,512).
+//
+// Half-row votes: with c = ln(lambda) < 0, "rowmax(S_ij) - m_new < c" holds
+// iff "rowmax(S_ij) - m_old < c" (if the block raises the max both sides are
+// false), and the latter is the AND of the same test on each half row.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -41,16 +49,16 @@ constexpr int NK = 2;         // K stages
 constexpr int NV = 2;         // V stages
 constexpr int NS = 3;         // TMEM S buffers
 constexpr int NDEC = 4;       // decision ring
-constexpr int NTHREADS = 224;
-constexpr int WARP_K = 4, WARP_MMA = 5, WARP_V = 6;
+constexpr int NSOFT = 8;  // softmax warps
+constexpr int NTHREADS = (NSOFT + 3) * 32;
+constexpr int WARP_K = NSOFT, WARP_MMA = NSOFT + 1, WARP_V = NSOFT + 2;
 constexpr uint32_t TILE_BYTES = BM * D * 2;      // 32 KB: one 128 x 128 bf16 tile
 constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;  // one 64-column swizzled box
 constexpr uint32_t SMEM_Q = 0;
 constexpr uint32_t SMEM_K = SMEM_Q + TILE_BYTES;
 constexpr uint32_t SMEM_V = SMEM_K + NK * TILE_BYTES;
 constexpr uint32_t SMEM_P = SMEM_V + NV * TILE_BYTES;
-constexpr uint32_t SMEM_BYTES = SMEM_P + 2 * TILE_BYTES;  // 224 KB
-constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;       // + alignment slack
+constexpr uint32_t SMEM_TILES = SMEM_P + 2 * TILE_BYTES;  // 224 KB
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_O = NS * BN;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -68,11 +76,19 @@ struct Shared {
   uint64_t p_full[2], pv_done[2];
   uint64_t dec_full[NDEC];
   uint64_t vote_full[2];
+  uint64_t l_full;
   int dec[NDEC];
-  int vote[2][4];
+  int vote[2][NSOFT];
+  // [block parity][column half][row] partial row max (log2 units); after the
+  // loop, parity nblk%2 (unused by the last block) carries the partial row sums.
+  float pmax[2][2][128];
   uint32_t tmem_base;
   int abort;
 };
+// Dynamic shared memory: the tiles at a 1024-byte aligned base (the 128-byte
+// swizzle repeats every 1024 bytes), then the control block.
+constexpr uint32_t SMEM_ALLOC = SMEM_TILES + ((sizeof(Shared) + 127) / 128) * 128;
+static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
 // Descriptor of k-step kk (16 columns) of a K-major 128 x 128 bf16 tile held as
 // two 128-byte-swizzled boxes of 64 columns: box kk/4, 32-byte step kk%4,
@@ -139,11 +155,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ Shared sh;
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;  // 1024-byte aligned for the swizzle
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Shared &sh = *reinterpret_cast<Shared *>(smem_raw + SMEM_TILES);
+  const uint32_t base = smem_u32(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (base & 1023u) {  // the swizzled layouts need a 1024-byte aligned base
+    if (tid == 0) atomicOr(a.err, kErrTimeout);
+    return;
+  }
 
   // Longest causal tiles first: blocks are ordered by decreasing tile index.
   const int BH = a.B * a.Hq;
@@ -169,13 +188,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&sh.s_full[i]), 1);
-      mbar_init(smem_u32(&sh.s_free[i]), 4);
+      mbar_init(smem_u32(&sh.s_free[i]), NSOFT);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&sh.p_full[i]), 4);
+      mbar_init(smem_u32(&sh.p_full[i]), NSOFT);
       mbar_init(smem_u32(&sh.pv_done[i]), 1);
-      mbar_init(smem_u32(&sh.vote_full[i]), 4);
+      mbar_init(smem_u32(&sh.vote_full[i]), NSOFT);
     }
+    mbar_init(smem_u32(&sh.l_full), NSOFT);
     for (int i = 0; i < NDEC; ++i) mbar_init(smem_u32(&sh.dec_full[i]), 1);
     sh.abort = 0;
     fence_mbar_init();
@@ -295,15 +315,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax --
-    const int r = tid;  // row within the tile == TMEM lane
+    const int quarter = warp & 3, half = warp >> 2;  // TMEM lane quarter, column half
+    const int r = quarter * 32 + lane;                // row within the tile == TMEM lane
     const int row = row0 + r;
     const bool valid = row < a.T;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const float sl2 = a.scale * kLog2e;     // raw score -> log2 units
-    const float c2 = a.ln_lambda * kLog2e;  // ln(lambda) in log2 units
-    float m2 = -INFINITY;                   // running max (log2 units)
-    float mref = -INFINITY;                 // exp reference (log2 units)
-    float l = 0.f;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    const int col0 = half * 64;                       // first key column of this warp
+    const float sl2 = a.scale * kLog2e;               // raw score -> log2 units
+    const float c2 = a.ln_lambda * kLog2e;            // ln(lambda) in log2 units
+    float m2 = -INFINITY;                             // running max (log2 units)
+    float mref = -INFINITY;                           // exp reference (log2 units)
+    float l = 0.f;                                    // partial row sum over own columns
     int kc = 0;
     uint32_t word = 0;
     uint32_t *bits = a.bits + ((size_t)bh * a.n_t + t) * a.words;
@@ -319,47 +341,43 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (lane == 0) mbar_arrive(smem_u32(&sh.s_free[j % NS]));
     };
 
-    // decide(j): row max of S_j, the vote, the tile AND; returns keep (or -1 on
-    // abort) and this row's updated running max in *mnew_out.
+    // decide(j): partial row max of S_j over this warp's 64 columns, the
+    // half-row vote against the running max before the block, then one
+    // barrier round: AND of all votes, and the partner's partial max for the
+    // running-max update.  Returns keep (or -1 on abort); *mnew_out receives
+    // this row's updated running max.
     auto decide = [&](int j, float *mnew_out) -> int {
       const int sb = j % NS;
       if (!mbar_wait(smem_u32(&sh.s_full[sb]), (j / NS) & 1, abort, a.err, kErrTimeout))
         return -1;
       fence_after_sync();
       const bool msk = needs_mask(j);
-      const uint32_t sa = lane_base + sb * BN;
+      const uint32_t sa = lane_base + sb * BN + col0;
+      const int kbase = j * BN + col0;
       uint32_t x[32], y[32];
-      float mt;
       tmem_ld32(sa, x);
-      tmem_wait_ld_regs(x);
       tmem_ld32(sa + 32, y);
-      if (msk) mask_chunk(x, j * BN, row, a.causal, a.T);
-      mt = chunk_max(x);
-      tmem_wait_ld_regs(y);
-      tmem_ld32(sa + 64, x);
-      if (msk) mask_chunk(y, j * BN + 32, row, a.causal, a.T);
-      mt = fmaxf(mt, chunk_max(y));
       tmem_wait_ld_regs(x);
-      tmem_ld32(sa + 96, y);
-      if (msk) mask_chunk(x, j * BN + 64, row, a.causal, a.T);
-      mt = fmaxf(mt, chunk_max(x));
+      if (msk) mask_chunk(x, kbase, row, a.causal, a.T);
+      float mt = chunk_max(x);
       tmem_wait_ld_regs(y);
-      if (msk) mask_chunk(y, j * BN + 96, row, a.causal, a.T);
+      if (msk) mask_chunk(y, kbase + 32, row, a.causal, a.T);
       mt = fmaxf(mt, chunk_max(y));
-      const float mt2 = mt * sl2;
-      const float mnew = fmaxf(m2, mt2);
-      const float diff = (mt == -INFINITY) ? -INFINITY : mt2 - mnew;
-      // Eq. 5 against the updated running max; rows past T are neutral.
+      const float pm2 = mt * sl2;
+      const float diff = (mt == -INFINITY) ? -INFINITY : pm2 - m2;
       const bool vote = !valid || (diff < c2);
       const unsigned all = __all_sync(0xffffffffu, vote);
       const int vb = j & 1;
-      if (lane == 0) {
-        sh.vote[vb][warp] = (int)all;
-        mbar_arrive(smem_u32(&sh.vote_full[vb]));
-      }
+      sh.pmax[vb][half][r] = pm2;
+      if (lane == 0) sh.vote[vb][warp] = (int)all;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.vote_full[vb]));
       if (!mbar_wait(smem_u32(&sh.vote_full[vb]), (j >> 1) & 1, abort, a.err, kErrTimeout))
         return -1;
-      const bool skip = sh.vote[vb][0] && sh.vote[vb][1] && sh.vote[vb][2] && sh.vote[vb][3];
+      bool skip = true;
+#pragma unroll
+      for (int w = 0; w < NSOFT; ++w) skip = skip && sh.vote[vb][w];
+      const float mnew = fmax3(m2, pm2, sh.pmax[vb][half ^ 1][r]);
       if (tid == 0) {
         sh.dec[j % NDEC] = skip ? 0 : 1;
         mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
@@ -375,7 +393,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       return skip ? 0 : 1;
     };
 
-    // exponentiate(j) for a kept block whose running max after it is mnew.
+    // exponentiate(j) for a kept block whose running max after it is mnew:
+    // this warp's 64 columns of P_j, its partial row sum, its half of O.
     auto exponentiate = [&](int j, float mnew) -> bool {
       bool rescale = false;
       float alpha = 1.f;
@@ -392,44 +411,39 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                 kErrTimeout))
         return false;
       const bool msk = needs_mask(j);
-      const uint32_t sa = lane_base + (j % NS) * BN;
+      const uint32_t sa = lane_base + (j % NS) * BN + col0;
+      const int kbase = j * BN + col0;
       const uint32_t prow = base + SMEM_P + pb * TILE_BYTES + (uint32_t)r * 128u;
       const float neg_ref = -mref;
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t x[32], y[32];
       tmem_ld32(sa, x);
-      tmem_wait_ld_regs(x);
       tmem_ld32(sa + 32, y);
-      if (msk) mask_chunk(x, j * BN, row, a.causal, a.T);
-      chunk_exp_store(x, sl2, neg_ref, acc, prow, 0, r);
-      tmem_wait_ld_regs(y);
-      tmem_ld32(sa + 64, x);
-      if (msk) mask_chunk(y, j * BN + 32, row, a.causal, a.T);
-      chunk_exp_store(y, sl2, neg_ref, acc, prow, 1, r);
       tmem_wait_ld_regs(x);
-      tmem_ld32(sa + 96, y);
-      if (msk) mask_chunk(x, j * BN + 64, row, a.causal, a.T);
-      chunk_exp_store(x, sl2, neg_ref, acc, prow, 2, r);
       tmem_wait_ld_regs(y);
-      release_s(j);  // all of S_j is in registers now
-      if (msk) mask_chunk(y, j * BN + 96, row, a.causal, a.T);
-      chunk_exp_store(y, sl2, neg_ref, acc, prow, 3, r);
+      release_s(j);  // this warp's part of S_j is in registers
+      if (msk) mask_chunk(x, kbase, row, a.causal, a.T);
+      chunk_exp_store(x, sl2, neg_ref, acc, prow, 2 * half, r);
+      if (msk) mask_chunk(y, kbase + 32, row, a.causal, a.T);
+      chunk_exp_store(y, sl2, neg_ref, acc, prow, 2 * half + 1, r);
       fence_proxy_async_smem();
       l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
-      // O rescale (warp-wide if any row needs it), after the previous PV landed.
+      // O rescale of this warp's 64 columns (warp-wide if any row needs it),
+      // after the previous PV landed.
       if (__any_sync(0xffffffffu, rescale) && kc >= 1) {
         if (!mbar_wait(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort, a.err,
                        kErrTimeout))
           return false;
         fence_after_sync();
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t o[32];
-          tmem_ld32(lane_base + TMEM_O + c * 32, o);
+          const uint32_t oa = lane_base + TMEM_O + col0 + c * 32;
+          tmem_ld32(oa, o);
           tmem_wait_ld_regs(o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(lane_base + TMEM_O + c * 32, o);
+          tmem_st32(oa, o);
         }
         tmem_wait_st();
       }
@@ -468,14 +482,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       ok = mbar_wait(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort, a.err,
                      kErrTimeout);
     }
+    // Row sum = the two column halves' partial sums.
+    float (*lhalf)[128] = sh.pmax[nblk & 1];
+    lhalf[half][r] = l;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sh.l_full));
+    if (ok) ok = mbar_wait(smem_u32(&sh.l_full), 0, abort, a.err, kErrTimeout);
     if (ok) {
       fence_after_sync();
-      const float inv = 1.f / l;
-      __nv_bfloat16 *orow = (__nv_bfloat16 *)a.o + ((size_t)bh * a.T + row) * D;
+      const float lrow = lhalf[0][r] + lhalf[1][r];
+      const float inv = 1.f / lrow;
+      __nv_bfloat16 *orow = (__nv_bfloat16 *)a.o + ((size_t)bh * a.T + row) * D + col0;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
-        tmem_ld32(lane_base + TMEM_O + c * 32, o);
+        tmem_ld32(lane_base + TMEM_O + col0 + c * 32, o);
         tmem_wait_ld_regs(o);
         if (valid) {
 #pragma unroll
@@ -489,7 +510,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
       }
-      if (valid) a.lse[(size_t)bh * a.T + row] = mref * kLn2 + logf(l);
+      if (valid && half == 0) a.lse[(size_t)bh * a.T + row] = mref * kLn2 + logf(lrow);
     }
   }
 
