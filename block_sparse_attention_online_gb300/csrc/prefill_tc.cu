@@ -7,7 +7,9 @@
 // skipped block costs no exponentials, no row sum and no P.V product).  Unlike
 // the page's prefill kernel, the value tile of a block is loaded only once the
 // block is known to be kept; the decision of block j+1 is taken before the
-// exponentials of block j so that load has time to land.
+// exponentials of block j so that load has time to land.  P_j (bf16) is
+// written back into the TMEM columns of S_j and read from there by the P.V
+// MMA, so it never touches shared memory.
 //
 // One CTA per (batch, query head, query tile), longest causal tiles first.
 // Warp roles (352 threads):
@@ -17,12 +19,14 @@
 //              warp's 64 columns and the half-row vote against the running
 //              max before the block, one barrier round to AND all votes and
 //              exchange the partial maxima; then, if block j is kept,
-//              P_j = exp2(S_j - ref) (bf16) to shared memory, a partial row
-//              sum, and an O rescale of the warp's 64 output columns in TMEM
-//              when the exp reference moves by > 2^8;
+//              P_j = exp2(S_j - ref) (bf16, into the first 32 TMEM columns of
+//              the warp's own 64 S columns), a partial row sum, and an O
+//              rescale of the warp's 64 output columns in TMEM when the exp
+//              reference moves by > 2^8;
 //   warp 8     TMA producer of Q (once) and K_j (every block);
 //   warp 9     MMA issuer: S_j = Q K_j^T two blocks ahead of the softmax, and
-//              O += P_j V_j for kept blocks;
+//              O += P_j V_j (P from TMEM) for kept blocks; the commit of that
+//              product frees the S buffer of a kept block;
 //   warp 10    TMA producer of V_j, for kept blocks only, as soon as the
 //              block's decision is known.
 // TMEM columns: three S buffers [0,384), O [384,512).
@@ -45,8 +49,8 @@ using namespace tc;
 constexpr int D = 128;        // head size of keys and values
 constexpr int BM = 128;       // query rows per tile
 constexpr int BN = 128;       // keys per block
-constexpr int NK = 2;         // K stages
-constexpr int NV = 2;         // V stages
+constexpr int NK = 3;         // K stages
+constexpr int NV = 3;         // V stages
 constexpr int NS = 3;         // TMEM S buffers
 constexpr int NDEC = 4;       // decision ring
 constexpr int NSOFT = 8;  // softmax warps
@@ -57,8 +61,7 @@ constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;  // one 64-column swizzled box
 constexpr uint32_t SMEM_Q = 0;
 constexpr uint32_t SMEM_K = SMEM_Q + TILE_BYTES;
 constexpr uint32_t SMEM_V = SMEM_K + NK * TILE_BYTES;
-constexpr uint32_t SMEM_P = SMEM_V + NV * TILE_BYTES;
-constexpr uint32_t SMEM_TILES = SMEM_P + 2 * TILE_BYTES;  // 224 KB
+constexpr uint32_t SMEM_TILES = SMEM_V + NV * TILE_BYTES;  // 224 KB
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_O = NS * BN;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -128,26 +131,20 @@ __device__ __forceinline__ float chunk_max(const uint32_t (&s)[32]) {
   return fmaxf(fmax3(a, b, c), d);
 }
 
-// P = exp2(s * sl2 - ref) for one 32-key chunk: accumulate the row sum and
-// store the bf16 values into the 128-byte-swizzled P tile (chunk c holds
-// 16-byte pieces 4c..4c+3 of the row; piece ch lives in box ch/8, slot
-// (ch%8) XOR (row%8)).
-__device__ __forceinline__ void chunk_exp_store(const uint32_t (&s)[32], float sl2, float neg_ref,
-                                                float (&acc)[4], uint32_t prow, int c, int r) {
-  uint32_t pk[16];
+// P = exp2(s * sl2 - ref) for one 32-key chunk, as 16 packed bf16 pairs, with
+// the row sum accumulated in two packed fp32 pairs.
+__device__ __forceinline__ void chunk_exp(const uint32_t (&s)[32], uint64_t sl2x2,
+                                          uint64_t negref2, uint64_t (&acc)[2],
+                                          uint32_t *pk) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const float p0 = ex2(fmaf(__uint_as_float(s[2 * i]), sl2, neg_ref));
-    const float p1 = ex2(fmaf(__uint_as_float(s[2 * i + 1]), sl2, neg_ref));
-    acc[i & 3] += p0 + p1;
+    float x0, x1;
+    f2_split(f2_fma(f2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), sl2x2,
+                    negref2),
+             x0, x1);
+    const float p0 = ex2(x0), p1 = ex2(x1);
+    acc[i & 1] = f2_add(acc[i & 1], f2(p0, p1));
     pk[i] = pack_bf16x2(p0, p1);
-  }
-#pragma unroll
-  for (int q4 = 0; q4 < 4; ++q4) {
-    const int ch = c * 4 + q4;
-    const uint32_t addr =
-        prow + (uint32_t)(ch >> 3) * HALF_BYTES + ((uint32_t)((ch & 7) ^ (r & 7)) << 4);
-    st_shared_v4(addr, pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
   }
 }
 
@@ -188,7 +185,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&sh.s_full[i]), 1);
-      mbar_init(smem_u32(&sh.s_free[i]), NSOFT);
+      mbar_init(smem_u32(&sh.s_free[i]), 1);  // PV commit (kept) or one softmax thread (skipped)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh.p_full[i]), NSOFT);
@@ -301,13 +298,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!mbar_wait(smem_u32(&sh.v_full[vs]), (vi / NV) & 1, abort, a.err, kErrTimeout))
           break;
         fence_after_sync();
-        const uint32_t ptile = base + SMEM_P + pb * TILE_BYTES;
+        // P_i: keys [0,64) in columns [0,32) and keys [64,128) in [64,96) of S buffer i % NS.
+        const uint32_t pt = tmem + (i % NS) * BN;
         const uint32_t vtile = base + SMEM_V + vs * TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ss(tmem + TMEM_O, kmajor_desc(ptile, kk), vmajor_desc(vtile, kk), IDESC_PV,
-                      (kc > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(tmem + TMEM_O, pt + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+                      vmajor_desc(vtile, kk), IDESC_PV, (kc > 0 || kk > 0) ? 1u : 0u);
         mma_commit(smem_u32(&sh.v_empty[vs]));
+        mma_commit(smem_u32(&sh.s_free[i % NS]));
         mma_commit(smem_u32(&sh.pv_done[pb]));
         ++kc;
         ++vi;
@@ -334,11 +333,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto needs_mask = [&](int j) {
       const int key0 = j * BN;
       return a.causal ? (key0 + BN - 1 > row0) : (key0 + BN > a.T);
-    };
-    auto release_s = [&](int j) {
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.s_free[j % NS]));
     };
 
     // decide(j): partial row max of S_j over this warp's 64 columns, the
@@ -370,6 +364,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const int vb = j & 1;
       sh.pmax[vb][half][r] = pm2;
       if (lane == 0) sh.vote[vb][warp] = (int)all;
+      fence_before_sync();  // this warp's reads of S_j are complete
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.vote_full[vb]));
       if (!mbar_wait(smem_u32(&sh.vote_full[vb]), (j >> 1) & 1, abort, a.err, kErrTimeout))
@@ -379,6 +374,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int w = 0; w < NSOFT; ++w) skip = skip && sh.vote[vb][w];
       const float mnew = fmax3(m2, pm2, sh.pmax[vb][half ^ 1][r]);
       if (tid == 0) {
+        if (skip) {  // every warp has read its part of S_j: the buffer is free
+          fence_after_sync();
+          fence_before_sync();
+          mbar_arrive(smem_u32(&sh.s_free[sb]));
+        }
         sh.dec[j % NDEC] = skip ? 0 : 1;
         mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
         if (skip) word |= 1u << (j & 31);
@@ -389,7 +389,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       m2 = mnew;
       *mnew_out = mnew;
-      if (skip) release_s(j);  // a skipped block's scores are no longer needed
       return skip ? 0 : 1;
     };
 
@@ -406,27 +405,29 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         rescale = true;
       }
       const int pb = kc & 1;
-      // P buffer pb was last read by the PV of kept block kc-2.
-      if (kc >= 2 && !mbar_wait(smem_u32(&sh.pv_done[pb]), ((kc - 2) >> 1) & 1, abort, a.err,
-                                kErrTimeout))
-        return false;
       const bool msk = needs_mask(j);
       const uint32_t sa = lane_base + (j % NS) * BN + col0;
       const int kbase = j * BN + col0;
-      const uint32_t prow = base + SMEM_P + pb * TILE_BYTES + (uint32_t)r * 128u;
-      const float neg_ref = -mref;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t x[32], y[32];
       tmem_ld32(sa, x);
       tmem_ld32(sa + 32, y);
       tmem_wait_ld_regs(x);
       tmem_wait_ld_regs(y);
-      release_s(j);  // this warp's part of S_j is in registers
-      if (msk) mask_chunk(x, kbase, row, a.causal, a.T);
-      chunk_exp_store(x, sl2, neg_ref, acc, prow, 2 * half, r);
-      if (msk) mask_chunk(y, kbase + 32, row, a.causal, a.T);
-      chunk_exp_store(y, sl2, neg_ref, acc, prow, 2 * half + 1, r);
-      fence_proxy_async_smem();
+      if (msk) {
+        mask_chunk(x, kbase, row, a.causal, a.T);
+        mask_chunk(y, kbase + 32, row, a.causal, a.T);
+      }
+      const uint64_t sl2x2 = f2(sl2, sl2), negref2 = f2(-mref, -mref);
+      uint64_t acc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+      uint32_t pk[32];
+      chunk_exp(x, sl2x2, negref2, acc2, pk);
+      chunk_exp(y, sl2x2, negref2, acc2, pk + 16);
+      // P over this warp's 64 keys -> the first 32 columns of its own S columns.
+      tmem_st32(sa, pk);
+      tmem_wait_st();
+      float acc[4];
+      f2_split(acc2[0], acc[0], acc[1]);
+      f2_split(acc2[1], acc[2], acc[3]);
       l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
       // O rescale of this warp's 64 columns (warp-wide if any row needs it),
       // after the previous PV landed.
