@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // this row's updated running max.
     auto decide = [&](int j, float *mnew_out) -> int {
       const int sb = j % NS;
-      if (!mbar_wait(smem_u32(&sh.s_full[sb]), (j / NS) & 1, abort, a.err, kErrTimeout))
+      if (!mbar_wait_warp(smem_u32(&sh.s_full[sb]), (j / NS) & 1, abort, a.err, kErrTimeout))
         return -1;
       fence_after_sync();
       const bool msk = needs_mask(j);
@@ -367,7 +367,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       fence_before_sync();  // this warp's reads of S_j are complete
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.vote_full[vb]));
-      if (!mbar_wait(smem_u32(&sh.vote_full[vb]), (j >> 1) & 1, abort, a.err, kErrTimeout))
+      if (!mbar_wait_warp(smem_u32(&sh.vote_full[vb]), (j >> 1) & 1, abort, a.err, kErrTimeout))
         return -1;
       bool skip = true;
 #pragma unroll
@@ -432,8 +432,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // O rescale of this warp's 64 columns (warp-wide if any row needs it),
       // after the previous PV landed.
       if (__any_sync(0xffffffffu, rescale) && kc >= 1) {
-        if (!mbar_wait(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort, a.err,
-                       kErrTimeout))
+        if (!mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort,
+                            a.err, kErrTimeout))
           return false;
         fence_after_sync();
 #pragma unroll 1
@@ -480,15 +480,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int w = ((nblk - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
     }
     if (ok && kc > 0) {
-      ok = mbar_wait(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort, a.err,
-                     kErrTimeout);
+      ok = mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort, a.err,
+                          kErrTimeout);
     }
     // Row sum = the two column halves' partial sums.
     float (*lhalf)[128] = sh.pmax[nblk & 1];
     lhalf[half][r] = l;
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&sh.l_full));
-    if (ok) ok = mbar_wait(smem_u32(&sh.l_full), 0, abort, a.err, kErrTimeout);
+    if (ok) ok = mbar_wait_warp(smem_u32(&sh.l_full), 0, abort, a.err, kErrTimeout);
     if (ok) {
       fence_after_sync();
       const float lrow = lhalf[0][r] + lhalf[1][r];
