@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(NT, 1) decode_bf16_kernel(const DecodeArgs a) 
   // QK layout: 8 lanes per key, lane p holds dims [8p, 8p+8) and [64+8p, 64+8p+8);
   // a warp step covers 4 keys.
   const int kq = lane >> 3, p = lane & 7;
-  float qf[G][16];
+  uint64_t qp[G][8];  // packed fp32 pairs of the thread's 16 query dims, per head
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     const __nv_bfloat16 *qh = (const __nv_bfloat16 *)a.q + (size_t)(b * a.Hq + hk * G + g) * D;
@@ -188,21 +188,19 @@ __global__ void __launch_bounds__(NT, 1) decode_bf16_kernel(const DecodeArgs a) 
     const uint4 hi = *reinterpret_cast<const uint4 *>(qh + 64 + 8 * p);
     const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      qf[g][2 * i] = bf_lo(w[i]);
-      qf[g][2 * i + 1] = bf_hi(w[i]);
-    }
+    for (int i = 0; i < 8; ++i) qp[g][i] = f2(bf_lo(w[i]), bf_hi(w[i]));
   }
   // PV layout: chunk c = tid % 16 owns value dims [8c, 8c+8); key slot ks = tid / 16.
   const int c = tid & 15, ks = tid >> 4;
-  float acc[G][8], lsum[G], ref[G], m[G];
+  uint64_t acc2[G][4];  // packed output pairs (dims 8c+2e, 8c+2e+1)
+  float lsum[G], ref[G], m[G];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     m[g] = -INFINITY;
     ref[g] = -INFINITY;
     lsum[g] = 0.f;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[g][e] = 0.f;
+    for (int e = 0; e < 4; ++e) acc2[g][e] = f2(0.f, 0.f);
   }
   uint32_t hist = 0;  // bit d: block (j - d) kept
   uint32_t word = 0;
@@ -223,11 +221,10 @@ __global__ void __launch_bounds__(NT, 1) decode_bf16_kernel(const DecodeArgs a) 
       }
       const int keys = block_keys(j);
       const uint32_t kt = kring + s * BLK_BYTES;
-      float bm[G];
+      constexpr int NSTEP = BC / (4 * NCW);  // warp steps of 4 keys (= 4)
+      float val[NSTEP * G];                    // partial dots, index step * G + g
 #pragma unroll
-      for (int g = 0; g < G; ++g) bm[g] = -INFINITY;
-#pragma unroll
-      for (int step = 0; step < BC / (4 * NCW); ++step) {
+      for (int step = 0; step < NSTEP; ++step) {
         const int kl = (step * NCW + warp) * 4 + kq;
         uint4 k0 = make_uint4(0, 0, 0, 0), k1 = make_uint4(0, 0, 0, 0);
         if (kl < keys) {
@@ -235,36 +232,82 @@ __global__ void __launch_bounds__(NT, 1) decode_bf16_kernel(const DecodeArgs a) 
           k1 = lds128(kt + kl * (D * 2) + 128 + p * 16);
         }
         const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-        float dot[G];
+        uint64_t d2[G];
 #pragma unroll
-        for (int g = 0; g < G; ++g) dot[g] = 0.f;
+        for (int g = 0; g < G; ++g) d2[g] = f2(0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float x0 = bf_lo(w[i]), x1 = bf_hi(w[i]);
+          const uint64_t x = f2(bf_lo(w[i]), bf_hi(w[i]));
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            dot[g] = fmaf(qf[g][2 * i], x0, dot[g]);
-            dot[g] = fmaf(qf[g][2 * i + 1], x1, dot[g]);
-          }
+          for (int g = 0; g < G; ++g) d2[g] = f2_fma(qp[g][i], x, d2[g]);
         }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 1);
-          dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 2);
-          dot[g] += __shfl_xor_sync(0xffffffffu, dot[g], 4);
-          const float sv = kl < keys ? dot[g] * sl2 : -INFINITY;
-          bm[g] = fmaxf(bm[g], sv);
-          if (p == (g & 7)) sh.S[rs][kl][g] = sv;
+          float lo, hi;
+          f2_split(d2[g], lo, hi);
+          val[step * G + g] = lo + hi;
         }
       }
+      // Sum over the 8 lanes of a key group.  Transposed butterfly: each level
+      // exchanges half of the values, so after three levels lane p holds the
+      // full dots v = p*G/2 + r (r < G/2) of step p/2, heads (p%2)*G/2 + r.
+      float bm[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        bm[g] = fmaxf(bm[g], __shfl_xor_sync(0xffffffffu, bm[g], 8));
-        bm[g] = fmaxf(bm[g], __shfl_xor_sync(0xffffffffu, bm[g], 16));
-      }
-      if (lane == 0) {
+      for (int g = 0; g < G; ++g) bm[g] = -INFINITY;
+      if constexpr (G >= 2) {
+        float v1[2 * G], v2[G], v3[G / 2];
+        const bool u1 = lane & 4, u2 = lane & 2, u3 = lane & 1;
 #pragma unroll
-        for (int g = 0; g < G; ++g) sh.wmax[pb][warp][g] = bm[g];
+        for (int i = 0; i < 2 * G; ++i) {
+          const float x = val[i], y = val[i + 2 * G];
+          v1[i] = (u1 ? y : x) + __shfl_xor_sync(0xffffffffu, u1 ? x : y, 4);
+        }
+#pragma unroll
+        for (int i = 0; i < G; ++i) {
+          const float x = v1[i], y = v1[i + G];
+          v2[i] = (u2 ? y : x) + __shfl_xor_sync(0xffffffffu, u2 ? x : y, 2);
+        }
+#pragma unroll
+        for (int i = 0; i < G / 2; ++i) {
+          const float x = v2[i], y = v2[i + G / 2];
+          v3[i] = (u3 ? y : x) + __shfl_xor_sync(0xffffffffu, u3 ? x : y, 1);
+        }
+        const int step = p >> 1, g0 = (p & 1) * (G / 2);
+        const int kl = (step * NCW + warp) * 4 + kq;
+        float hm[G / 2];
+#pragma unroll
+        for (int r = 0; r < G / 2; ++r) {
+          const float sv = kl < keys ? v3[r] * sl2 : -INFINITY;
+          sh.S[rs][kl][g0 + r] = sv;
+          hm[r] = sv;
+        }
+        // block max per head: lanes with the same p%2 hold the same heads
+#pragma unroll
+        for (int r = 0; r < G / 2; ++r) {
+          hm[r] = fmaxf(hm[r], __shfl_xor_sync(0xffffffffu, hm[r], 2));
+          hm[r] = fmaxf(hm[r], __shfl_xor_sync(0xffffffffu, hm[r], 4));
+          hm[r] = fmaxf(hm[r], __shfl_xor_sync(0xffffffffu, hm[r], 8));
+          hm[r] = fmaxf(hm[r], __shfl_xor_sync(0xffffffffu, hm[r], 16));
+        }
+        if (lane < 2) {
+#pragma unroll
+          for (int r = 0; r < G / 2; ++r) sh.wmax[pb][warp][lane * (G / 2) + r] = hm[r];
+        }
+      } else {  // one head: plain butterfly over the 8 lanes
+#pragma unroll
+        for (int step = 0; step < NSTEP; ++step) {
+          float x = val[step];
+          x += __shfl_xor_sync(0xffffffffu, x, 1);
+          x += __shfl_xor_sync(0xffffffffu, x, 2);
+          x += __shfl_xor_sync(0xffffffffu, x, 4);
+          const int kl = (step * NCW + warp) * 4 + kq;
+          const float sv = kl < keys ? x * sl2 : -INFINITY;
+          if (p == 0) sh.S[rs][kl][0] = sv;
+          bm[0] = fmaxf(bm[0], sv);
+        }
+        bm[0] = fmaxf(bm[0], __shfl_xor_sync(0xffffffffu, bm[0], 8));
+        bm[0] = fmaxf(bm[0], __shfl_xor_sync(0xffffffffu, bm[0], 16));
+        if (lane == 0) sh.wmax[pb][warp][0] = bm[0];
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.k_empty[s]));
@@ -323,8 +366,9 @@ __global__ void __launch_bounds__(NT, 1) decode_bf16_kernel(const DecodeArgs a) 
         const float alpha = (ref[g] == -INFINITY) ? 0.f : ex2(ref[g] - nr);
         ref[g] = nr;
         lsum[g] *= alpha;
+        const uint64_t a2 = f2(alpha, alpha);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[g][e] *= alpha;
+        for (int e = 0; e < 4; ++e) acc2[g][e] = f2_fma(acc2[g][e], a2, f2(0.f, 0.f));
       }
       const int keys = block_keys(i1);
       const uint32_t vt = vring + vs * BLK_BYTES;
@@ -343,14 +387,15 @@ __global__ void __launch_bounds__(NT, 1) decode_bf16_kernel(const DecodeArgs a) 
 #pragma unroll
           for (int g = 0; g < G; ++g) pg[g] = sh.S[i1 % R][kk][g];
         }
+        uint64_t vx[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) vx[e] = f2(bf_lo(w[e]), bf_hi(w[e]));
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           lsum[g] += pg[g];
+          const uint64_t pp = f2(pg[g], pg[g]);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            acc[g][2 * e] = fmaf(pg[g], bf_lo(w[e]), acc[g][2 * e]);
-            acc[g][2 * e + 1] = fmaf(pg[g], bf_hi(w[e]), acc[g][2 * e + 1]);
-          }
+          for (int e = 0; e < 4; ++e) acc2[g][e] = f2_fma(pp, vx[e], acc2[g][e]);
         }
       }
       __syncwarp();
@@ -383,9 +428,15 @@ __global__ void __launch_bounds__(NT, 1) decode_bf16_kernel(const DecodeArgs a) 
   for (int g = 0; g < G; ++g) {
     lsum[g] += __shfl_xor_sync(0xffffffffu, lsum[g], 16);
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      acc[g][e] += __shfl_xor_sync(0xffffffffu, acc[g][e], 16);
-      if (lane < 16) red[warp][g][8 * c + e] = acc[g][e];
+    for (int e = 0; e < 4; ++e) {
+      float lo, hi;
+      f2_split(acc2[g][e], lo, hi);
+      lo += __shfl_xor_sync(0xffffffffu, lo, 16);
+      hi += __shfl_xor_sync(0xffffffffu, hi, 16);
+      if (lane < 16) {
+        red[warp][g][8 * c + 2 * e] = lo;
+        red[warp][g][8 * c + 2 * e + 1] = hi;
+      }
     }
     if (lane == 0) lred[warp][g] = lsum[g];
   }
