@@ -123,6 +123,10 @@ extern "C" attn_status attn_skip_decode(const void *q, const void *k, const void
   if (dt == ATTN_BF16 && dk == 128 && dv == 128 && Bc == 128 && k_row_stride == 128 &&
       v_row_stride == 128 && (G == 1 || G == 2 || G == 4 || G == 8))
     return from_cuda(launch_decode_bf16(a, s));
+  // Absorbed MLA: one latent head of 576 columns, values = its first 512 columns.
+  if (dt == ATTN_BF16 && dk == 576 && dv == 512 && v == k && k_row_stride == 576 &&
+      v_row_stride == 576 && Bc == 64 && Hkv == 1 && Hq == 128)
+    return from_cuda(launch_mla_decode(a, s));
   return ATTN_EUNSUPPORTED;
 }
 

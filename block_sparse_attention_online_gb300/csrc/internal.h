@@ -46,6 +46,7 @@ struct CombineArgs {
 cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 
 }  // namespace attn_skip

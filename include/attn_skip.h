@@ -106,7 +106,11 @@ attn_status attn_skip_prefill(const void *q, const void *k, const void *v, attn_
  *             bit p of split s is block floor(s*nb/n_splits) + p
  *
  * Kernels built: dt = ATTN_BF16, dk = dv = 128, Bc = 128, G in {1, 2, 4, 8},
- * k_row_stride = v_row_stride = 128 (CUDA-core memory-bound path).
+ * k_row_stride = v_row_stride = 128 (CUDA-core memory-bound path); and the
+ * absorbed-MLA shape dt = ATTN_BF16, Hkv = 1, Hq = 128, dk = 576, dv = 512,
+ * v == k, k_row_stride = v_row_stride = 576, Bc = 64 (tcgen05 path, the 128
+ * heads as one M = 128 tile; a skipped block saves its exponentials and its
+ * P.V product, its value bytes being the key bytes already read).
  */
 attn_status attn_skip_decode(const void *q, const void *k, const void *v, attn_dtype dt, int B,
                              int Hq, int Hkv, int L, int dk, int dv, int64_t k_row_stride,

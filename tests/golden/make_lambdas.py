@@ -65,11 +65,19 @@ def main(names):
             k = int(round(s * m.size))
             k = min(max(k, 1), m.size - 1)
             ln_lam = 0.5 * (m[k - 1] + m[k])
-            if not ln_lam < 0:  # cannot reach the target (first blocks are never skipped)
+            if not ln_lam < 0:  # unreachable: too many blocks raise some row's max
                 continue
             entry[str(s)] = {"lambda": math.exp(ln_lam), "ln_lambda": float(ln_lam),
                              "sparsity": float((m < ln_lam).mean()),
                              "gap": float(m[k] - m[k - 1])}
+        # The largest reachable sparsity: ln(lambda) halfway between the largest
+        # negative statistic and 0 (blocks with statistic 0 raise a row's max and
+        # are never skipped, whatever lambda < 1).
+        neg = m[m < 0]
+        if neg.size:
+            ln_lam = 0.5 * neg.max()
+            entry["max"] = {"lambda": math.exp(ln_lam), "ln_lambda": float(ln_lam),
+                            "sparsity": float((m < ln_lam).mean())}
         entry["seconds"] = round(time.time() - t0, 1)
         data[name] = entry
         print(name, json.dumps(entry))
