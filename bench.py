@@ -36,8 +36,32 @@ from block_sparse_attention_online_gb300 import workloads as W  # noqa: E402
 METRIC = "skip-softmax attn: prefill dense-equiv TFLOP/s, decode tok/s & GB/s @~70% skip"
 PREFILL = W.GQA_PREFILL_16K
 DECODE = W.GQA_DECODE_32K
+MLA = W.MLA_DECODE_16K
 TARGET = "0.7"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+CSRC = os.path.join(ROOT, "block_sparse_attention_online_gb300", "csrc")
+# DRAM bytes (read + write) per launch from one ncu capture of the kernel at
+# the bench's workload and threshold (summaries under profiles/).  Reported
+# only while the kernel's source is the captured one.
+NCU_TRAFFIC = {
+    "prefill_tc_kernel": {
+        "file": "prefill_tc.cu",
+        "sha256": "46858a035abb485a12c62e4b099cfd65c1b18fa6c5fb1512d2b6a20e0942950d",
+        "bytes": 232137216 + 82776320},
+    "decode_bf16_kernel": {
+        "file": "decode.cu",
+        "sha256": "8d56116c44ad809818b6a8816f9efa1d0dfadd4071b9e7a1e967acc49574fee0",
+        "bytes": 1396073000 + 8058624},
+}
+
+
+def ncu_traffic(kernel):
+    import hashlib
+    t = NCU_TRAFFIC[kernel]
+    with open(os.path.join(CSRC, t["file"]), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != t["sha256"]:
+            return None
+    return t["bytes"]
 
 
 def lambdas():
@@ -228,6 +252,8 @@ def run_gpu(args, rank, world):
         dsweep[t]["speedup_vs_lambda0"] = ((dsweep["0.0"]["ms_decode"] + dsweep["0.0"]["ms_combine"])
                                           / (dsweep[t]["ms_decode"] + dsweep[t]["ms_combine"]))
 
+    msweep = mla_sweep(args, bs, dev, stream, flush, lam)
+
     # ---- the timed region: K steps of the whole hot path at ~70 % ---------
     fp, fd = prefill(lp[TARGET]), decode(ld[TARGET])
     for _ in range(args.warmup):
@@ -300,15 +326,61 @@ def run_gpu(args, rank, world):
                      "frac": round(executed_tflops / peak_tf, 4),
                      "frac_sustained": round(executed_tflops / pk.get(
                          "bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]), 4),
-                     "traffic": None},
+                     "traffic": ncu_traffic("prefill_tc_kernel"),
+                     "algorithmic_bytes": int(P.B * P.Hq * P.T * P.d * 2 * 2
+                                              + 2 * P.B * P.Hkv * P.T * P.d * 2)},
         "decode_roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel",
                             "achieved": round(dec_gbs, 1), "peak": peak_hbm, "unit": "GB/s",
-                            "frac": round(dec_gbs / peak_hbm, 4), "traffic": None},
+                            "frac": round(dec_gbs / peak_hbm, 4),
+                            "traffic": ncu_traffic("decode_bf16_kernel"),
+                            "algorithmic_bytes": dec["bytes"]},
+        "mla_decode": msweep,
         "e2e": e2e,
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 3 * args.steps,  # prefill, decode, merge per timed step
         "clocks": clk.summary(),
     }
     return line
+
+
+def mla_sweep(args, bs, dev, stream, flush, lam):
+    """Absorbed-MLA decode (B=32, 128 heads, 576/512 latent, L=16384, Bc=64, 16
+    splits) + merge at lambda = 0 and at the largest reachable sparsity."""
+    M = MLA
+    q, k, _ = W.decode_inputs(M)
+    dq, dk_ = q.to(dev), k.to(dev)
+    del q, k
+    n_b = -(-M.L // M.Bc)
+    units = M.B * n_b
+    op = torch.empty(M.B, M.Hq, M.n_splits, M.dv, dtype=torch.float32, device=dev)
+    lp = torch.empty(M.B, M.Hq, M.n_splits, dtype=torch.float32, device=dev)
+    bits = torch.empty(bs.decode_bitmap_shape(M.B, 1, M.L, M.Bc, M.n_splits), dtype=torch.int32,
+                       device=dev)
+    o = torch.empty(M.B, M.Hq, M.dv, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(M.B, M.Hq, dtype=torch.float32, device=dev)
+    out = {}
+    for t in ("0.0", "max"):
+        lmb = lam[M.name][t]["lambda"]
+
+        def step():
+            bs.attn_skip_decode(dq, dk_, None, lmb, M.Bc, M.n_splits, dv=M.dv,
+                                out=(op, lp, bits))
+            bs.attn_skip_decode_combine(op, lp, out=(o, lse))
+
+        durs = timed_launches(step, args.warmup, args.steps, flush, stream)
+        skipped = int(bs.unpack_bits(bits, -(-n_b // M.n_splits)).sum())
+        kept = units - skipped
+        ms = statistics.mean(durs)
+        qk = 2.0 * M.Hq * M.Bc * M.dk * units          # every block
+        pv = 2.0 * M.Hq * M.Bc * M.dv * kept           # kept blocks
+        byts = M.B * M.L * M.dk * 2 + M.B * M.Hq * M.dk * 2 + op.numel() * 4 + lp.numel() * 4
+        out[t] = {"lambda": lmb, "sparsity": round(skipped / units, 4), "ms": round(ms, 4),
+                  "tok_per_s": round(M.B / (ms / 1e3), 1), "gbs": round(byts / ms / 1e6, 1),
+                  "algorithmic_tflops": round((qk + pv) / ms / 1e9, 2),
+                  "tensor_tflops_executed": round((2 * qk + pv) / ms / 1e9, 2)}
+    out["max"]["speedup_vs_lambda0"] = round(out["0.0"]["ms"] / out["max"]["ms"], 4)
+    out["workload"] = (f"B{M.B} Hq{M.Hq} latent dk{M.dk} dv{M.dv} L{M.L} Bc{M.Bc} "
+                       f"splits{M.n_splits}; 'max' = largest sparsity any lambda < 1 reaches")
+    return out
 
 
 def max_over_ranks(x, world):
@@ -363,17 +435,21 @@ def oracle_sample_units(n_tiles):
     return list(range(P.n_t - n_tiles, P.n_t))
 
 
-def oracle_prefill_rate(n_tiles, q=None, k=None, v=None):
+def oracle_prefill_rate(n_tiles, n_heads=1, q=None, k=None, v=None):
+    """The fp64 oracle on the n_tiles longest causal tiles of the first n_heads
+    query heads (KV heads 0 .. n_heads/G - 1) of the prefill workload."""
     import oracle
     P = PREFILL
     lam = lambdas()[P.name][TARGET]["lambda"]
+    n_kv = max(1, -(-n_heads // P.G))
     if q is None:
-        q, k, v = W.prefill_inputs(P.with_(Hq=P.G, Hkv=1))  # KV head 0 and its query heads
-    units = oracle_sample_units(n_tiles)
+        q, k, v = W.prefill_inputs(P.with_(Hq=n_kv * P.G, Hkv=n_kv))
+    tiles = oracle_sample_units(n_tiles)
+    units = [h * P.n_t + t for h in range(n_heads) for t in tiles]
     t0 = time.perf_counter()
-    oracle.prefill(q[:, :1], k, v, P.scale, lam, P.Br, P.Bc, True, units=units)
+    oracle.prefill(q, k, v, P.scale, lam, P.Br, P.Bc, True, units=units)
     dt = time.perf_counter() - t0
-    dense = sum(4.0 * P.d * tile_visible_pairs(P, t) for t in units)
+    dense = n_heads * sum(4.0 * P.d * tile_visible_pairs(P, t) for t in tiles)
     return dense / dt / 1e12, dt, min(oracle.num_threads(), len(units)), (q, k, v)
 
 
@@ -383,12 +459,15 @@ def tile_visible_pairs(P, t):
     return (r1 * (r1 + 1) - r0 * (r0 + 1)) / 2
 
 
-def cpu_baseline(n_tiles=128):
-    rate, dt, cores, _ = oracle_prefill_rate(n_tiles)
+def cpu_baseline(n_heads=16):
+    """The oracle on all tiles of the first n_heads query heads (about 15 s on
+    16 cores)."""
+    P = PREFILL
+    rate, dt, cores, _ = oracle_prefill_rate(P.n_t, n_heads)
     return {"value": round(rate, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"fp64 oracle, prefill query head 0, the {n_tiles} longest causal tiles "
-                      f"of T={PREFILL.T} (1/{PREFILL.Hq * PREFILL.n_t // n_tiles} of the "
-                      f"workload) at the ~70% threshold, {dt:.1f} s"}
+            "sample": f"fp64 oracle, prefill query heads 0-{n_heads - 1}, all {P.n_t} causal "
+                      f"tiles of T={P.T} ({n_heads}/{P.Hq} of the workload) at the ~70% "
+                      f"threshold, {dt:.1f} s"}
 
 
 def run_reference(args):
@@ -397,10 +476,10 @@ def run_reference(args):
     n_tiles = 16
     rate, dt, cores, cache = oracle_prefill_rate(n_tiles)
     for _ in range(max(0, args.warmup - 1)):
-        oracle_prefill_rate(n_tiles, *cache)
+        oracle_prefill_rate(n_tiles, 1, *cache)
     rates, times = [], []
     for _ in range(args.steps):
-        r, t, _, _ = oracle_prefill_rate(n_tiles, *cache)
+        r, t, _, _ = oracle_prefill_rate(n_tiles, 1, *cache)
         rates.append(r)
         times.append(t)
     value = statistics.mean(rates)

@@ -78,6 +78,7 @@ struct Shared {
   uint64_t s_full[NS], s_free[NS];
   uint64_t p_full[2], pv_done[2];
   uint64_t dec_full[NDEC];
+  uint64_t dec_read[NDEC];  // the V producer has read decision slot j % NDEC
   uint64_t vote_full[2];
   uint64_t l_full;
   int dec[NDEC];
@@ -193,7 +194,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(smem_u32(&sh.vote_full[i]), NSOFT);
     }
     mbar_init(smem_u32(&sh.l_full), NSOFT);
-    for (int i = 0; i < NDEC; ++i) mbar_init(smem_u32(&sh.dec_full[i]), 1);
+    for (int i = 0; i < NDEC; ++i) {
+      mbar_init(smem_u32(&sh.dec_full[i]), 1);
+      mbar_init(smem_u32(&sh.dec_read[i]), 1);
+    }
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -244,7 +248,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!mbar_wait(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
                        kErrTimeout))
           break;
-        if (!sh.dec[j % NDEC]) continue;
+        const int keep = sh.dec[j % NDEC];
+        mbar_arrive(smem_u32(&sh.dec_read[j % NDEC]));
+        if (!keep) continue;
         const int s = vi % NV;
         if (vi >= NV &&
             !mbar_wait(smem_u32(&sh.v_empty[s]), ((vi / NV) - 1) & 1, abort, a.err, kErrTimeout))
@@ -379,8 +385,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           fence_before_sync();
           mbar_arrive(smem_u32(&sh.s_free[sb]));
         }
-        sh.dec[j % NDEC] = skip ? 0 : 1;
-        mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
+        // The slot's previous decision (block j - NDEC) must have been read by
+        // the V producer (the MMA reads it before this block's scores exist).
+        // On a timeout the abort flag is raised and every later wait fails.
+        if (j < NDEC || mbar_wait(smem_u32(&sh.dec_read[j % NDEC]), ((j / NDEC) - 1) & 1, abort,
+                                  a.err, kErrTimeout)) {
+          sh.dec[j % NDEC] = skip ? 0 : 1;
+          mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
+        }
         if (skip) word |= 1u << (j & 31);
         if ((j & 31) == 31 || j == nblk - 1) {
           bits[j >> 5] = word;
