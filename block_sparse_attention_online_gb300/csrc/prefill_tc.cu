@@ -24,11 +24,15 @@
 //              rescale of the warp's 64 output columns in TMEM when the exp
 //              reference moves by > 2^8;
 //   warp 8     TMA producer of Q (once) and K_j (every block);
-//   warp 9     MMA issuer: S_j = Q K_j^T two blocks ahead of the softmax, and
-//              O += P_j V_j (P from TMEM) for kept blocks; the commit of that
-//              product frees the S buffer of a kept block;
+//   warp 9     Q.K^T issuer: S_j = Q K_j^T two blocks ahead of the softmax
+//              (also allocates TMEM);
 //   warp 10    TMA producer of V_j, for kept blocks only, as soon as the
-//              block's decision is known.
+//              block's decision is known;
+//   warp 11    P.V issuer: O += P_j V_j (P from TMEM) for kept blocks; the
+//              commit of that product frees the S buffer of a kept block.
+// Two issuing threads keep one product chain from waiting on the other's
+// barriers: a tcgen05.mma issue is accepted at about the rate the tensor core
+// retires it, so a single issuer serialises every wait with every product.
 // TMEM columns: three S buffers [0,384), O [384,512).
 //
 // Half-row votes: with c = ln(lambda) < 0, "rowmax(S_ij) - m_new < c" holds
@@ -54,8 +58,8 @@ constexpr int NV = 3;         // V stages
 constexpr int NS = 3;         // TMEM S buffers
 constexpr int NDEC = 4;       // decision ring
 constexpr int NSOFT = 8;  // softmax warps
-constexpr int NTHREADS = (NSOFT + 3) * 32;
-constexpr int WARP_K = NSOFT, WARP_MMA = NSOFT + 1, WARP_V = NSOFT + 2;
+constexpr int NTHREADS = (NSOFT + 4) * 32;
+constexpr int WARP_K = NSOFT, WARP_MMA = NSOFT + 1, WARP_V = NSOFT + 2, WARP_PV = NSOFT + 3;
 constexpr uint32_t TILE_BYTES = BM * D * 2;      // 32 KB: one 128 x 128 bf16 tile
 constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;  // one 64-column swizzled box
 constexpr uint32_t SMEM_Q = 0;
@@ -78,7 +82,7 @@ struct Shared {
   uint64_t s_full[NS], s_free[NS];
   uint64_t p_full[2], pv_done[2];
   uint64_t dec_full[NDEC];
-  uint64_t dec_read[NDEC];  // the V producer has read decision slot j % NDEC
+  uint64_t dec_read[NDEC];  // the V producer and the P.V issuer have read slot j % NDEC
   uint64_t vote_full[2];
   uint64_t l_full;
   int dec[NDEC];
@@ -94,19 +98,28 @@ struct Shared {
 constexpr uint32_t SMEM_ALLOC = SMEM_TILES + ((sizeof(Shared) + 127) / 128) * 128;
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
-// Descriptor of k-step kk (16 columns) of a K-major 128 x 128 bf16 tile held as
-// two 128-byte-swizzled boxes of 64 columns: box kk/4, 32-byte step kk%4,
-// 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
-  return smem_desc_sw128(tile + (uint32_t)(kk >> 2) * HALF_BYTES + (uint32_t)(kk & 3) * 32u, 16u,
-                         1024u);
+// Descriptors are built once per tile and advanced per k-step by adding the
+// byte offset >> 4 to the start-address field (shared addresses stay below
+// 2^18, so the 14-bit field never carries).
+//
+// K-major 128 x 128 bf16 tile held as two 128-byte-swizzled boxes of 64
+// columns: k-step kk (16 columns) is box kk/4 at 32-byte step kk%4; 8-row
+// groups are 1024 bytes apart.
+__device__ __forceinline__ uint64_t kmajor_base(uint32_t tile) {
+  return smem_desc_sw128(tile, 16u, 1024u);
+}
+__device__ __forceinline__ constexpr uint64_t kmajor_step(int kk) {
+  return (uint64_t)(((uint32_t)(kk >> 2) * HALF_BYTES + (uint32_t)(kk & 3) * 32u) >> 4);
 }
 
-// Descriptor of k-step kk (16 keys) of the MN-major value tile: rows are keys
-// (128 bytes = 64 values per swizzled row), 8-key groups 1024 bytes apart
-// (SBO), the second 64-value half 16 KB further (LBO).
-__device__ __forceinline__ uint64_t vmajor_desc(uint32_t tile, int kk) {
-  return smem_desc_sw128(tile + (uint32_t)kk * 2048u, HALF_BYTES, 1024u);
+// MN-major value tile: rows are keys (128 bytes = 64 values per swizzled row),
+// 8-key groups 1024 bytes apart (SBO), the second 64-value half 16 KB further
+// (LBO); k-step kk (16 keys) starts 2048 bytes further.
+__device__ __forceinline__ uint64_t vmajor_base(uint32_t tile) {
+  return smem_desc_sw128(tile, HALF_BYTES, 1024u);
+}
+__device__ __forceinline__ constexpr uint64_t vmajor_step(int kk) {
+  return (uint64_t)(((uint32_t)kk * 2048u) >> 4);
 }
 
 // Mask the 32 scores of a chunk whose first key is kbase: causal (key > row)
@@ -186,7 +199,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&sh.s_full[i]), 1);
-      mbar_init(smem_u32(&sh.s_free[i]), 1);  // PV commit (kept) or one softmax thread (skipped)
+      mbar_init(smem_u32(&sh.s_free[i]), 1);  // the P.V commit of a kept block
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh.p_full[i]), NSOFT);
@@ -196,7 +209,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(smem_u32(&sh.l_full), NSOFT);
     for (int i = 0; i < NDEC; ++i) {
       mbar_init(smem_u32(&sh.dec_full[i]), 1);
-      mbar_init(smem_u32(&sh.dec_read[i]), 1);
+      mbar_init(smem_u32(&sh.dec_read[i]), 2);
     }
     sh.abort = 0;
     fence_mbar_init();
@@ -267,37 +280,50 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
   } else if (warp == WARP_MMA) {
-    // ---------------------------------------------------------------- MMA --
+    // -------------------------------------------------------- Q.K^T issuer --
     if (lane == 0) {
       bool ok = mbar_wait(smem_u32(&sh.q_full), 0, abort, a.err, kErrTimeout);
       fence_after_sync();
-      int kc = 0, vi = 0;
-      // S_j = Q K_j^T into S buffer j % NS.
-      auto issue_qk = [&](int j) -> bool {
+      const uint64_t qdesc = kmajor_base(base + SMEM_Q);
+      int pv_into[NS] = {0, 0, 0};  // P.V products issued into each S buffer
+      for (int j = 0; ok && j < nblk; ++j) {
         const int s = j % NK, sb = j % NS;
-        if (!mbar_wait(smem_u32(&sh.k_full[s]), (j / NK) & 1, abort, a.err, kErrTimeout))
-          return false;
-        if (j >= NS && !mbar_wait(smem_u32(&sh.s_free[sb]), ((j / NS) - 1) & 1, abort, a.err,
-                                  kErrTimeout))
-          return false;
+        if (!mbar_wait(smem_u32(&sh.k_full[s]), (j / NK) & 1, abort, a.err, kErrTimeout)) break;
+        if (j >= NS) {
+          // S buffer sb last held block j - NS: free once its scores were read
+          // (a skipped block: its decision exists) or its P.V completed (kept).
+          const int jp = j - NS;
+          if (!mbar_wait(smem_u32(&sh.dec_full[jp % NDEC]), (jp / NDEC) & 1, abort, a.err,
+                         kErrTimeout))
+            break;
+          if (sh.dec[jp % NDEC]) {
+            ++pv_into[sb];
+            if (!mbar_wait(smem_u32(&sh.s_free[sb]), (pv_into[sb] - 1) & 1, abort, a.err,
+                           kErrTimeout))
+              break;
+          }
+        }
         fence_after_sync();
-        const uint32_t ktile = base + SMEM_K + s * TILE_BYTES;
+        const uint64_t kd = kmajor_base(base + SMEM_K + s * TILE_BYTES);
+        const uint32_t d_s = tmem + sb * BN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(tmem + sb * BN, kmajor_desc(base + SMEM_Q, kk), kmajor_desc(ktile, kk),
-                      IDESC_QK, kk > 0);
+          mma_bf16_ss(d_s, qdesc + kmajor_step(kk), kd + kmajor_step(kk), IDESC_QK, kk > 0);
         mma_commit(smem_u32(&sh.s_full[sb]));
         mma_commit(smem_u32(&sh.k_empty[s]));
-        return true;
-      };
-      for (int j = 0; ok && j < 2 && j < nblk; ++j) ok = issue_qk(j);
-      for (int i = 0; ok && i < nblk; ++i) {
-        if (i + 2 < nblk && !issue_qk(i + 2)) break;
-        // O += P_i V_i if block i is kept
+      }
+    }
+  } else if (warp == WARP_PV) {
+    // ---------------------------------------------------------- P.V issuer --
+    if (lane == 0) {
+      int kc = 0, vi = 0;
+      for (int i = 0; i < nblk && !*abort; ++i) {
         if (!mbar_wait(smem_u32(&sh.dec_full[i % NDEC]), (i / NDEC) & 1, abort, a.err,
                        kErrTimeout))
           break;
-        if (!sh.dec[i % NDEC]) continue;
+        const int keep = sh.dec[i % NDEC];
+        mbar_arrive(smem_u32(&sh.dec_read[i % NDEC]));
+        if (!keep) continue;
         const int pb = kc & 1, vs = vi % NV;
         if (!mbar_wait(smem_u32(&sh.p_full[pb]), (kc >> 1) & 1, abort, a.err, kErrTimeout))
           break;
@@ -306,11 +332,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         fence_after_sync();
         // P_i: keys [0,64) in columns [0,32) and keys [64,128) in [64,96) of S buffer i % NS.
         const uint32_t pt = tmem + (i % NS) * BN;
-        const uint32_t vtile = base + SMEM_V + vs * TILE_BYTES;
+        const uint64_t vd = vmajor_base(base + SMEM_V + vs * TILE_BYTES);
+        const uint32_t d_o = tmem + TMEM_O;
+        const uint32_t acc0 = kc > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ts(tmem + TMEM_O, pt + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
-                      vmajor_desc(vtile, kk), IDESC_PV, (kc > 0 || kk > 0) ? 1u : 0u);
+          mma_bf16_ts(d_o, pt + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), vd + vmajor_step(kk),
+                      IDESC_PV, kk > 0 ? 1u : acc0);
         mma_commit(smem_u32(&sh.v_empty[vs]));
         mma_commit(smem_u32(&sh.s_free[i % NS]));
         mma_commit(smem_u32(&sh.pv_done[pb]));
@@ -380,11 +408,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       for (int w = 0; w < NSOFT; ++w) skip = skip && sh.vote[vb][w];
       const float mnew = fmax3(m2, pm2, sh.pmax[vb][half ^ 1][r]);
       if (tid == 0) {
-        if (skip) {  // every warp has read its part of S_j: the buffer is free
-          fence_after_sync();
-          fence_before_sync();
-          mbar_arrive(smem_u32(&sh.s_free[sb]));
-        }
+        // (A skipped block's S buffer is reused by the Q.K^T issuer as soon as
+        // it reads this decision: every warp has read S_j before the vote.)
         // The slot's previous decision (block j - NDEC) must have been read by
         // the V producer (the MMA reads it before this block's scores exist).
         // On a timeout the abort flag is raised and every later wait fails.
