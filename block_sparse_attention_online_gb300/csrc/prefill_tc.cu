@@ -86,7 +86,7 @@ struct Shared {
   uint64_t vote_full[2];
   uint64_t l_full;
   int dec[NDEC];
-  int vote[2][NSOFT];
+  unsigned keepw[3];  // ring: bit w set when softmax warp w votes "keep" for the block
   // [block parity][column half][row] partial row max (log2 units); after the
   // loop, parity nblk%2 (unused by the last block) carries the partial row sums.
   float pmax[2][2][128];
@@ -207,6 +207,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(smem_u32(&sh.vote_full[i]), NSOFT);
     }
     mbar_init(smem_u32(&sh.l_full), NSOFT);
+    sh.keepw[0] = sh.keepw[1] = sh.keepw[2] = 0u;
     for (int i = 0; i < NDEC; ++i) {
       mbar_init(smem_u32(&sh.dec_full[i]), 1);
       mbar_init(smem_u32(&sh.dec_read[i]), 2);
@@ -374,8 +375,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // barrier round: AND of all votes, and the partner's partial max for the
     // running-max update.  Returns keep (or -1 on abort); *mnew_out receives
     // this row's updated running max.
-    auto decide = [&](int j, float *mnew_out) -> int {
-      const int sb = j % NS;
+    auto decide = [&](int j, int sb, float *mnew_out) -> int {
+      // Slot (j+1)%3 was last read after the barrier of block j-2, before
+      // every warp arrived at the barrier of block j-1; it is next written
+      // after the barrier of block j, which waits for this warp.
+      if (tid == 0) sh.keepw[(sb + 1) % 3] = 0u;
       if (!mbar_wait_warp(smem_u32(&sh.s_full[sb]), (j / NS) & 1, abort, a.err, kErrTimeout))
         return -1;
       fence_after_sync();
@@ -397,15 +401,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const unsigned all = __all_sync(0xffffffffu, vote);
       const int vb = j & 1;
       sh.pmax[vb][half][r] = pm2;
-      if (lane == 0) sh.vote[vb][warp] = (int)all;
+      if (lane == 0 && !all) atomicOr(&sh.keepw[sb], 1u << warp);
       fence_before_sync();  // this warp's reads of S_j are complete
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.vote_full[vb]));
       if (!mbar_wait_warp(smem_u32(&sh.vote_full[vb]), (j >> 1) & 1, abort, a.err, kErrTimeout))
         return -1;
-      bool skip = true;
-#pragma unroll
-      for (int w = 0; w < NSOFT; ++w) skip = skip && sh.vote[vb][w];
+      const bool skip = sh.keepw[sb] == 0u;
       const float mnew = fmax3(m2, pm2, sh.pmax[vb][half ^ 1][r]);
       if (tid == 0) {
         // (A skipped block's S buffer is reused by the Q.K^T issuer as soon as
@@ -431,7 +433,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // exponentiate(j) for a kept block whose running max after it is mnew:
     // this warp's 64 columns of P_j, its partial row sum, its half of O.
-    auto exponentiate = [&](int j, float mnew) -> bool {
+    auto exponentiate = [&](int j, int sb, float mnew) -> bool {
       bool rescale = false;
       float alpha = 1.f;
       if (mref == -INFINITY) {
@@ -443,7 +445,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
       const int pb = kc & 1;
       const bool msk = needs_mask(j);
-      const uint32_t sa = lane_base + (j % NS) * BN + col0;
+      const uint32_t sa = lane_base + sb * BN + col0;
       const int kbase = j * BN + col0;
       uint32_t x[32], y[32];
       tmem_ld32(sa, x);
@@ -493,23 +495,26 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
 
     float mnew_cur = -INFINITY, mnew_next = -INFINITY;
-    int keep_cur = decide(0, &mnew_cur);
+    int sb_cur = 0;  // S buffer (and vote slot) of block j: j % NS
+    int keep_cur = decide(0, 0, &mnew_cur);
     ok = keep_cur >= 0;
     for (int j = 0; ok && j < nblk; ++j) {
+      const int sb_next = sb_cur == NS - 1 ? 0 : sb_cur + 1;
       int keep_next = 0;
       if (j + 1 < nblk) {
-        keep_next = decide(j + 1, &mnew_next);
+        keep_next = decide(j + 1, sb_next, &mnew_next);
         if (keep_next < 0) {
           ok = false;
           break;
         }
       }
-      if (keep_cur && !exponentiate(j, mnew_cur)) {
+      if (keep_cur && !exponentiate(j, sb_cur, mnew_cur)) {
         ok = false;
         break;
       }
       keep_cur = keep_next;
       mnew_cur = mnew_next;
+      sb_cur = sb_next;
     }
 
     // ---- epilogue ----------------------------------------------------------
