@@ -6,26 +6,28 @@
 // predicate, a warp vote and a tile-wide AND) and "Prefill 内核：砍计算" (a
 // skipped block costs no exponentials, no row sum and no P.V product).  Unlike
 // the page's prefill kernel, the value tile of a block is loaded only once the
-// block is known to be kept; the decision of block j+1 is taken before the
-// exponentials of block j so that load has time to land.  P_j (bf16) is
+// block is known to be kept; decisions are taken by their own warps ahead of
+// the exponentials, so that load has time to land.  P_j (bf16) is
 // written back into the TMEM columns of S_j and read from there by the P.V
 // MMA, so it never touches shared memory.
 //
 // One CTA per (batch, query head, query tile), longest causal tiles first.
-// Warp roles (352 threads):
-//   warps 0-7  softmax: warps w and w+4 share query rows 32(w%4)..+31 (TMEM
-//              lanes) and own key columns [0,64) and [64,128) of each block.
-//              Per block: decide(j+1) = partial row max of S_{j+1} over the
-//              warp's 64 columns and the half-row vote against the running
-//              max before the block, one barrier round to AND all votes and
-//              exchange the partial maxima; then, if block j is kept,
-//              P_j = exp2(S_j - ref) (bf16, into the first 32 TMEM columns of
-//              the warp's own 64 S columns), a partial row sum, and an O
-//              rescale of the warp's 64 output columns in TMEM when the exp
-//              reference moves by > 2^8;
+// Warp roles (384 threads):
+//   warps 0-3  deciders: warp w owns query rows 32w..32w+31 (TMEM lane
+//              quarter w) over all 128 key columns.  Per block: the row max
+//              of S_j, the row vote against the running max before the
+//              block, one barrier round of the four deciders to AND the
+//              votes; thread 0 publishes the decision and the bitmap.  The
+//              deciders run ahead of the exponentials as far as the three S
+//              buffers allow, so in a run of skipped blocks nothing else
+//              waits for them;
+//   warps 4-7  exponentials: warp 4+w owns the same rows; for each kept block
+//              P_j = exp2(S_j - ref) (bf16 pairs into TMEM columns [0,64) of
+//              the block's S buffer), the row sum, and an O rescale in TMEM
+//              when the exp reference moves by > 2^8;
 //   warp 8     TMA producer of Q (once) and K_j (every block);
-//   warp 9     Q.K^T issuer: S_j = Q K_j^T two blocks ahead of the softmax
-//              (also allocates TMEM);
+//   warp 9     Q.K^T issuer: S_j = Q K_j^T up to three blocks ahead (also
+//              allocates TMEM);
 //   warp 10    TMA producer of V_j, for kept blocks only, as soon as the
 //              block's decision is known;
 //   warp 11    P.V issuer: O += P_j V_j (P from TMEM) for kept blocks; the
@@ -35,9 +37,9 @@
 // retires it, so a single issuer serialises every wait with every product.
 // TMEM columns: three S buffers [0,384), O [384,512).
 //
-// Half-row votes: with c = ln(lambda) < 0, "rowmax(S_ij) - m_new < c" holds
-// iff "rowmax(S_ij) - m_old < c" (if the block raises the max both sides are
-// false), and the latter is the AND of the same test on each half row.
+// Votes: with c = ln(lambda) < 0, "rowmax(S_ij) - m_new < c" holds iff
+// "rowmax(S_ij) - m_old < c" (if the block raises the max both sides are
+// false).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
@@ -57,7 +59,8 @@ constexpr int NK = 3;         // K stages
 constexpr int NV = 3;         // V stages
 constexpr int NS = 3;         // TMEM S buffers
 constexpr int NDEC = 4;       // decision ring
-constexpr int NSOFT = 8;  // softmax warps
+constexpr int NQ = 4;     // decider warps (0-3) and exponential warps (4-7): one per TMEM lane quarter
+constexpr int NSOFT = 2 * NQ;
 constexpr int NTHREADS = (NSOFT + 4) * 32;
 constexpr int WARP_K = NSOFT, WARP_MMA = NSOFT + 1, WARP_V = NSOFT + 2, WARP_PV = NSOFT + 3;
 constexpr uint32_t TILE_BYTES = BM * D * 2;      // 32 KB: one 128 x 128 bf16 tile
@@ -82,14 +85,15 @@ struct Shared {
   uint64_t s_full[NS], s_free[NS];
   uint64_t p_full[2], pv_done[2];
   uint64_t dec_full[NDEC];
-  uint64_t dec_read[NDEC];  // the V producer and the P.V issuer have read slot j % NDEC
+  uint64_t dec_read[NDEC];  // the V producer, the P.V issuer and the exponential warps read slot j % NDEC
   uint64_t vote_full[2];
   uint64_t l_full;
   int dec[NDEC];
-  unsigned keepw[3];  // ring: bit w set when softmax warp w votes "keep" for the block
-  // [block parity][column half][row] partial row max (log2 units); after the
-  // loop, parity nblk%2 (unused by the last block) carries the partial row sums.
-  float pmax[2][2][128];
+  unsigned keepw[3];  // ring: bit w set when decider warp w votes "keep" for the block
+  // [S buffer][row] running max after the buffer's block (log2 units), from
+  // the deciders to the exponential warps.
+  float mdec[NS][128];
+  float lfin[128], mfin[128];  // row sum and exp reference for the epilogue
   uint32_t tmem_base;
   int abort;
 };
@@ -202,15 +206,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(smem_u32(&sh.s_free[i]), 1);  // the P.V commit of a kept block
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&sh.p_full[i]), NSOFT);
+      mbar_init(smem_u32(&sh.p_full[i]), NQ);
       mbar_init(smem_u32(&sh.pv_done[i]), 1);
-      mbar_init(smem_u32(&sh.vote_full[i]), NSOFT);
+      mbar_init(smem_u32(&sh.vote_full[i]), NQ);
     }
-    mbar_init(smem_u32(&sh.l_full), NSOFT);
+    mbar_init(smem_u32(&sh.l_full), NQ);
     sh.keepw[0] = sh.keepw[1] = sh.keepw[2] = 0u;
     for (int i = 0; i < NDEC; ++i) {
       mbar_init(smem_u32(&sh.dec_full[i]), 1);
-      mbar_init(smem_u32(&sh.dec_read[i]), 2);
+      mbar_init(smem_u32(&sh.dec_read[i]), 2 + NQ);
     }
     sh.abort = 0;
     fence_mbar_init();
@@ -331,15 +335,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (!mbar_wait(smem_u32(&sh.v_full[vs]), (vi / NV) & 1, abort, a.err, kErrTimeout))
           break;
         fence_after_sync();
-        // P_i: keys [0,64) in columns [0,32) and keys [64,128) in [64,96) of S buffer i % NS.
+        // P_i (bf16 pairs): keys [0,128) in columns [0,64) of S buffer i % NS.
         const uint32_t pt = tmem + (i % NS) * BN;
         const uint64_t vd = vmajor_base(base + SMEM_V + vs * TILE_BYTES);
         const uint32_t d_o = tmem + TMEM_O;
         const uint32_t acc0 = kc > 0 ? 1u : 0u;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_bf16_ts(d_o, pt + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8), vd + vmajor_step(kk),
-                      IDESC_PV, kk > 0 ? 1u : acc0);
+          mma_bf16_ts(d_o, pt + kk * 8, vd + vmajor_step(kk), IDESC_PV, kk > 0 ? 1u : acc0);
         mma_commit(smem_u32(&sh.v_empty[vs]));
         mma_commit(smem_u32(&sh.s_free[i % NS]));
         mma_commit(smem_u32(&sh.pv_done[pb]));
@@ -348,193 +351,198 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
   } else {
-    // ------------------------------------------------------------ softmax --
-    const int quarter = warp & 3, half = warp >> 2;  // TMEM lane quarter, column half
-    const int r = quarter * 32 + lane;                // row within the tile == TMEM lane
+    // ------------------------------------------------- deciders / exponentials --
+    const bool decider = warp < NQ;
+    const int quarter = warp & 3;                 // TMEM lane quarter
+    const int r = quarter * 32 + lane;            // row within the tile == TMEM lane
     const int row = row0 + r;
     const bool valid = row < a.T;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    const int col0 = half * 64;                       // first key column of this warp
-    const float sl2 = a.scale * kLog2e;               // raw score -> log2 units
-    const float c2 = a.ln_lambda * kLog2e;            // ln(lambda) in log2 units
-    float m2 = -INFINITY;                             // running max (log2 units)
-    float mref = -INFINITY;                           // exp reference (log2 units)
-    float l = 0.f;                                    // partial row sum over own columns
-    int kc = 0;
-    uint32_t word = 0;
-    uint32_t *bits = a.bits + ((size_t)bh * a.n_t + t) * a.words;
+    const float sl2 = a.scale * kLog2e;           // raw score -> log2 units
+    float mref = -INFINITY;                       // exp reference (log2 units)
+    float l = 0.f;                                // row sum relative to mref
+    int kc = 0;                                   // kept blocks exponentiated
     bool ok = true;
-
     auto needs_mask = [&](int j) {
       const int key0 = j * BN;
       return a.causal ? (key0 + BN - 1 > row0) : (key0 + BN > a.T);
     };
 
-    // decide(j): partial row max of S_j over this warp's 64 columns, the
-    // half-row vote against the running max before the block, then one
-    // barrier round: AND of all votes, and the partner's partial max for the
-    // running-max update.  Returns keep (or -1 on abort); *mnew_out receives
-    // this row's updated running max.
-    auto decide = [&](int j, int sb, float *mnew_out) -> int {
-      // Slot (j+1)%3 was last read after the barrier of block j-2, before
-      // every warp arrived at the barrier of block j-1; it is next written
-      // after the barrier of block j, which waits for this warp.
-      if (tid == 0) sh.keepw[(sb + 1) % 3] = 0u;
-      if (!mbar_wait_warp(smem_u32(&sh.s_full[sb]), (j / NS) & 1, abort, a.err, kErrTimeout))
-        return -1;
-      fence_after_sync();
-      const bool msk = needs_mask(j);
-      const uint32_t sa = lane_base + sb * BN + col0;
-      const int kbase = j * BN + col0;
-      uint32_t x[32], y[32];
-      tmem_ld32(sa, x);
-      tmem_ld32(sa + 32, y);
-      tmem_wait_ld_regs(x);
-      if (msk) mask_chunk(x, kbase, row, a.causal, a.T);
-      float mt = chunk_max(x);
-      tmem_wait_ld_regs(y);
-      if (msk) mask_chunk(y, kbase + 32, row, a.causal, a.T);
-      mt = fmaxf(mt, chunk_max(y));
-      const float pm2 = mt * sl2;
-      const float diff = (mt == -INFINITY) ? -INFINITY : pm2 - m2;
-      const bool vote = !valid || (diff < c2);
-      const unsigned all = __all_sync(0xffffffffu, vote);
-      const int vb = j & 1;
-      sh.pmax[vb][half][r] = pm2;
-      if (lane == 0 && !all) atomicOr(&sh.keepw[sb], 1u << warp);
-      fence_before_sync();  // this warp's reads of S_j are complete
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.vote_full[vb]));
-      if (!mbar_wait_warp(smem_u32(&sh.vote_full[vb]), (j >> 1) & 1, abort, a.err, kErrTimeout))
-        return -1;
-      const bool skip = sh.keepw[sb] == 0u;
-      const float mnew = fmax3(m2, pm2, sh.pmax[vb][half ^ 1][r]);
-      if (tid == 0) {
-        // (A skipped block's S buffer is reused by the Q.K^T issuer as soon as
-        // it reads this decision: every warp has read S_j before the vote.)
-        // The slot's previous decision (block j - NDEC) must have been read by
-        // the V producer (the MMA reads it before this block's scores exist).
-        // On a timeout the abort flag is raised and every later wait fails.
-        if (j < NDEC || mbar_wait(smem_u32(&sh.dec_read[j % NDEC]), ((j / NDEC) - 1) & 1, abort,
-                                  a.err, kErrTimeout)) {
-          sh.dec[j % NDEC] = skip ? 0 : 1;
-          mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
-        }
-        if (skip) word |= 1u << (j & 31);
-        if ((j & 31) == 31 || j == nblk - 1) {
-          bits[j >> 5] = word;
-          word = 0;
-        }
-      }
-      m2 = mnew;
-      *mnew_out = mnew;
-      return skip ? 0 : 1;
-    };
-
-    // exponentiate(j) for a kept block whose running max after it is mnew:
-    // this warp's 64 columns of P_j, its partial row sum, its half of O.
-    auto exponentiate = [&](int j, int sb, float mnew) -> bool {
-      bool rescale = false;
-      float alpha = 1.f;
-      if (mref == -INFINITY) {
-        mref = mnew;
-      } else if (mnew > mref + kRescaleLog2) {
-        alpha = ex2(mref - mnew);
-        mref = mnew;
-        rescale = true;
-      }
-      const int pb = kc & 1;
-      const bool msk = needs_mask(j);
-      const uint32_t sa = lane_base + sb * BN + col0;
-      const int kbase = j * BN + col0;
-      uint32_t x[32], y[32];
-      tmem_ld32(sa, x);
-      tmem_ld32(sa + 32, y);
-      tmem_wait_ld_regs(x);
-      tmem_wait_ld_regs(y);
-      if (msk) {
-        mask_chunk(x, kbase, row, a.causal, a.T);
-        mask_chunk(y, kbase + 32, row, a.causal, a.T);
-      }
-      const uint64_t sl2x2 = f2(sl2, sl2), negref2 = f2(-mref, -mref);
-      uint64_t acc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
-      uint32_t pk[32];
-      chunk_exp(x, sl2x2, negref2, acc2, pk);
-      chunk_exp(y, sl2x2, negref2, acc2, pk + 16);
-      // P over this warp's 64 keys -> the first 32 columns of its own S columns.
-      tmem_st32(sa, pk);
-      tmem_wait_st();
-      float acc[4];
-      f2_split(acc2[0], acc[0], acc[1]);
-      f2_split(acc2[1], acc[2], acc[3]);
-      l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
-      // O rescale of this warp's 64 columns (warp-wide if any row needs it),
-      // after the previous PV landed.
-      if (__any_sync(0xffffffffu, rescale) && kc >= 1) {
-        if (!mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort,
-                            a.err, kErrTimeout))
-          return false;
-        fence_after_sync();
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          uint32_t o[32];
-          const uint32_t oa = lane_base + TMEM_O + col0 + c * 32;
-          tmem_ld32(oa, o);
-          tmem_wait_ld_regs(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(oa, o);
-        }
-        tmem_wait_st();
-      }
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[pb]));
-      ++kc;
-      return true;
-    };
-
-    float mnew_cur = -INFINITY, mnew_next = -INFINITY;
-    int sb_cur = 0;  // S buffer (and vote slot) of block j: j % NS
-    int keep_cur = decide(0, 0, &mnew_cur);
-    ok = keep_cur >= 0;
-    for (int j = 0; ok && j < nblk; ++j) {
-      const int sb_next = sb_cur == NS - 1 ? 0 : sb_cur + 1;
-      int keep_next = 0;
-      if (j + 1 < nblk) {
-        keep_next = decide(j + 1, sb_next, &mnew_next);
-        if (keep_next < 0) {
+    if (decider) {
+      // Per block: the full row max of S_j, the row vote against the running
+      // max before the block, then one barrier round of the four deciders to
+      // AND the votes.  Thread 0 publishes the decision and the bitmap.
+      const float c2 = a.ln_lambda * kLog2e;      // ln(lambda) in log2 units
+      float m2 = -INFINITY;                       // running max (log2 units)
+      uint32_t word = 0;
+      uint32_t *bits = a.bits + ((size_t)bh * a.n_t + t) * a.words;
+      int sb = 0;
+      for (int j = 0; j < nblk; ++j) {
+        const int sbn = sb == NS - 1 ? 0 : sb + 1;
+        // Slot sbn was last read after the barrier of block j-2, before every
+        // decider arrived at the barrier of block j-1.
+        if (tid == 0) sh.keepw[sbn] = 0u;
+        if (!mbar_wait_warp(smem_u32(&sh.s_full[sb]), (j / NS) & 1, abort, a.err, kErrTimeout)) {
           ok = false;
           break;
         }
+        fence_after_sync();
+        const uint32_t sa = lane_base + sb * BN;
+        uint32_t x0[32], x1[32], x2[32], x3[32];
+        tmem_ld32(sa, x0);
+        tmem_ld32(sa + 32, x1);
+        tmem_ld32(sa + 64, x2);
+        tmem_ld32(sa + 96, x3);
+        tmem_wait_ld_regs(x0);
+        tmem_wait_ld_regs(x1);
+        tmem_wait_ld_regs(x2);
+        tmem_wait_ld_regs(x3);
+        if (needs_mask(j)) {
+          const int kb = j * BN;
+          mask_chunk(x0, kb, row, a.causal, a.T);
+          mask_chunk(x1, kb + 32, row, a.causal, a.T);
+          mask_chunk(x2, kb + 64, row, a.causal, a.T);
+          mask_chunk(x3, kb + 96, row, a.causal, a.T);
+        }
+        const float mt =
+            fmaxf(fmaxf(chunk_max(x0), chunk_max(x1)), fmaxf(chunk_max(x2), chunk_max(x3)));
+        const float pm2 = mt * sl2;
+        // With c < 0, "rowmax - m_new < c" is "rowmax - m_old < c" (a block
+        // that raises the max fails both).
+        const float diff = (mt == -INFINITY) ? -INFINITY : pm2 - m2;
+        const unsigned all = __all_sync(0xffffffffu, !valid || (diff < c2));
+        const float mnew = fmaxf(m2, pm2);
+        sh.mdec[sb][r] = mnew;
+        if (lane == 0 && !all) atomicOr(&sh.keepw[sb], 1u << warp);
+        fence_before_sync();  // this warp's reads of S_j are complete
+        __syncwarp();
+        const int vb = j & 1;
+        if (lane == 0) mbar_arrive(smem_u32(&sh.vote_full[vb]));
+        if (!mbar_wait_warp(smem_u32(&sh.vote_full[vb]), (j >> 1) & 1, abort, a.err,
+                            kErrTimeout)) {
+          ok = false;
+          break;
+        }
+        const bool skip = sh.keepw[sb] == 0u;
+        m2 = mnew;
+        if (tid == 0) {
+          // (A skipped block's S buffer is reused by the Q.K^T issuer as soon
+          // as it reads this decision.)  The slot's previous decision (block
+          // j - NDEC) must have been read by all its readers; on a timeout the
+          // abort flag is raised and every later wait fails.
+          if (j < NDEC || mbar_wait(smem_u32(&sh.dec_read[j % NDEC]), ((j / NDEC) - 1) & 1,
+                                    abort, a.err, kErrTimeout)) {
+            sh.dec[j % NDEC] = skip ? 0 : 1;
+            mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
+          }
+          if (skip) word |= 1u << (j & 31);
+          if ((j & 31) == 31 || j == nblk - 1) {
+            bits[j >> 5] = word;
+            word = 0;
+          }
+        }
+        sb = sbn;
       }
-      if (keep_cur && !exponentiate(j, sb_cur, mnew_cur)) {
-        ok = false;
-        break;
+      if (tid == 0) {
+        for (int w = ((nblk - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
       }
-      keep_cur = keep_next;
-      mnew_cur = mnew_next;
-      sb_cur = sb_next;
+    } else {
+      // Per kept block: P_j = exp2(S_j - ref) as bf16 pairs into columns
+      // [0,64) of the block's S buffer, the row sum, and an O rescale when
+      // the exp reference moves by more than 2^8.
+      int sb = 0;
+      for (int j = 0; ok && j < nblk; ++j, sb = (sb == NS - 1 ? 0 : sb + 1)) {
+        if (!mbar_wait_warp(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
+                            kErrTimeout)) {
+          ok = false;
+          break;
+        }
+        const int keep = sh.dec[j % NDEC];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.dec_read[j % NDEC]));
+        if (!keep) continue;
+        const float mnew = sh.mdec[sb][r];
+        bool rescale = false;
+        float alpha = 1.f;
+        if (mref == -INFINITY) {
+          mref = mnew;
+        } else if (mnew > mref + kRescaleLog2) {
+          alpha = ex2(mref - mnew);
+          mref = mnew;
+          rescale = true;
+        }
+        fence_after_sync();
+        const bool msk = needs_mask(j);
+        const uint32_t sa = lane_base + sb * BN;
+        const uint64_t sl2x2 = f2(sl2, sl2), negref2 = f2(-mref, -mref);
+        uint64_t acc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          // Keys [64hh, 64hh+64): their P pairs land in columns [32hh, 32hh+32),
+          // whose scores were loaded by this or the previous half.
+          uint32_t x[32], y[32];
+          tmem_ld32(sa + 64 * hh, x);
+          tmem_ld32(sa + 64 * hh + 32, y);
+          tmem_wait_ld_regs(x);
+          tmem_wait_ld_regs(y);
+          if (msk) {
+            mask_chunk(x, j * BN + 64 * hh, row, a.causal, a.T);
+            mask_chunk(y, j * BN + 64 * hh + 32, row, a.causal, a.T);
+          }
+          uint32_t pk[32];
+          chunk_exp(x, sl2x2, negref2, acc2, pk);
+          chunk_exp(y, sl2x2, negref2, acc2, pk + 16);
+          tmem_st32(sa + 32 * hh, pk);
+        }
+        tmem_wait_st();
+        float acc[4];
+        f2_split(acc2[0], acc[0], acc[1]);
+        f2_split(acc2[1], acc[2], acc[3]);
+        l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+        // O rescale of this warp's rows (warp-wide if any row needs it), after
+        // the previous P.V landed.
+        if (__any_sync(0xffffffffu, rescale) && kc >= 1) {
+          if (!mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort,
+                              a.err, kErrTimeout)) {
+            ok = false;
+            break;
+          }
+          fence_after_sync();
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            const uint32_t oa = lane_base + TMEM_O + c * 32;
+            tmem_ld32(oa, o);
+            tmem_wait_ld_regs(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(oa, o);
+          }
+          tmem_wait_st();
+        }
+        fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[kc & 1]));
+        ++kc;
+      }
+      if (ok && kc > 0) {
+        ok = mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort,
+                            a.err, kErrTimeout);
+      }
+      sh.lfin[r] = l;
+      sh.mfin[r] = mref;
+      fence_before_sync();  // the final P.V is complete (observed above)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.l_full));
     }
 
-    // ---- epilogue ----------------------------------------------------------
-    if (tid == 0) {
-      for (int w = ((nblk - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
-    }
-    if (ok && kc > 0) {
-      ok = mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort, a.err,
-                          kErrTimeout);
-    }
-    // Row sum = the two column halves' partial sums.
-    float (*lhalf)[128] = sh.pmax[nblk & 1];
-    lhalf[half][r] = l;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&sh.l_full));
+    // ---- epilogue: deciders take O columns [0,64), exponential warps [64,128)
     if (ok) ok = mbar_wait_warp(smem_u32(&sh.l_full), 0, abort, a.err, kErrTimeout);
     if (ok) {
       fence_after_sync();
-      const float lrow = lhalf[0][r] + lhalf[1][r];
+      const float lrow = sh.lfin[r];
       const float inv = 1.f / lrow;
+      const int col0 = decider ? 0 : 64;
       __nv_bfloat16 *orow = (__nv_bfloat16 *)a.o + ((size_t)bh * a.T + row) * D + col0;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
@@ -553,7 +561,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
       }
-      if (valid && half == 0) a.lse[(size_t)bh * a.T + row] = mref * kLn2 + logf(lrow);
+      if (valid && !decider) a.lse[(size_t)bh * a.T + row] = sh.mfin[r] * kLn2 + logf(lrow);
     }
   }
 
