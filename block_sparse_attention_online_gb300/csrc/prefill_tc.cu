@@ -126,15 +126,33 @@ __device__ __forceinline__ constexpr uint64_t vmajor_step(int kk) {
   return (uint64_t)(((uint32_t)kk * 2048u) >> 4);
 }
 
-// Mask the 32 scores of a chunk whose first key is kbase: causal (key > row)
-// or, without causality, keys past T.
-__device__ __forceinline__ void mask_chunk(uint32_t (&s)[32], int kbase, int row, int causal,
-                                           int T) {
+// Write -inf over the invisible scores of block j in this warp's TMEM lanes
+// (causal: key > row; otherwise key >= T), 32 keys at a time: chunks with no
+// visible key get a constant store, a partial chunk is loaded, masked and
+// stored back.  Only a tile's last blocks need it; the code is kept short
+// because it runs from a cold instruction cache.  Every later reader of the
+// buffer (this warp after tcgen05.wait::st, the exponential warps after the
+// decision is published) sees the masked scores through the normal path.
+__device__ __noinline__ void mask_block_tmem(uint32_t sa, int kbase, int row, int causal, int T) {
+  uint32_t ninf[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const int key = kbase + i;
-    if (causal ? key > row : key >= T) s[i] = NEG_INF_BITS;
+  for (int i = 0; i < 32; ++i) ninf[i] = NEG_INF_BITS;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    const int lim = causal ? row - (kbase + 32 * c) + 1 : T - (kbase + 32 * c);
+    if (__all_sync(0xffffffffu, lim >= 32)) continue;
+    if (__all_sync(0xffffffffu, lim <= 0)) {
+      tmem_st32(sa + 32 * c, ninf);
+      continue;
+    }
+    uint32_t x[32];
+    tmem_ld32(sa + 32 * c, x);
+    tmem_wait_ld_regs(x);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = i < lim ? x[i] : NEG_INF_BITS;
+    tmem_st32(sa + 32 * c, x);
   }
+  tmem_wait_st();
 }
 
 __device__ __forceinline__ float chunk_max(const uint32_t (&s)[32]) {
@@ -388,6 +406,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         fence_after_sync();
         const uint32_t sa = lane_base + sb * BN;
+        if (needs_mask(j)) mask_block_tmem(sa, j * BN, row, a.causal, a.T);
         uint32_t x0[32], x1[32], x2[32], x3[32];
         tmem_ld32(sa, x0);
         tmem_ld32(sa + 32, x1);
@@ -397,13 +416,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tmem_wait_ld_regs(x1);
         tmem_wait_ld_regs(x2);
         tmem_wait_ld_regs(x3);
-        if (needs_mask(j)) {
-          const int kb = j * BN;
-          mask_chunk(x0, kb, row, a.causal, a.T);
-          mask_chunk(x1, kb + 32, row, a.causal, a.T);
-          mask_chunk(x2, kb + 64, row, a.causal, a.T);
-          mask_chunk(x3, kb + 96, row, a.causal, a.T);
-        }
         const float mt =
             fmaxf(fmaxf(chunk_max(x0), chunk_max(x1)), fmaxf(chunk_max(x2), chunk_max(x3)));
         const float pm2 = mt * sl2;
@@ -472,8 +484,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           rescale = true;
         }
         fence_after_sync();
-        const bool msk = needs_mask(j);
-        const uint32_t sa = lane_base + sb * BN;
+        const uint32_t sa = lane_base + sb * BN;  // scores already masked by the deciders
         const uint64_t sl2x2 = f2(sl2, sl2), negref2 = f2(-mref, -mref);
         uint64_t acc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll 1
@@ -485,10 +496,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           tmem_ld32(sa + 64 * hh + 32, y);
           tmem_wait_ld_regs(x);
           tmem_wait_ld_regs(y);
-          if (msk) {
-            mask_chunk(x, j * BN + 64 * hh, row, a.causal, a.T);
-            mask_chunk(y, j * BN + 64 * hh + 32, row, a.causal, a.T);
-          }
           uint32_t pk[32];
           chunk_exp(x, sl2x2, negref2, acc2, pk);
           chunk_exp(y, sl2x2, negref2, acc2, pk + 16);
