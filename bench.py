@@ -46,8 +46,8 @@ CSRC = os.path.join(ROOT, "block_sparse_attention_online_gb300", "csrc")
 NCU_TRAFFIC = {
     "prefill_tc_kernel": {
         "file": "prefill_tc.cu",
-        "sha256": "46858a035abb485a12c62e4b099cfd65c1b18fa6c5fb1512d2b6a20e0942950d",
-        "bytes": 232137216 + 82776320},
+        "sha256": "511769a136493c9b2aecee9272ec007e392c2d115d79b0ad6b3b8aa5e73e767c",
+        "bytes": 240706304 + 83190272},
     "decode_bf16_kernel": {
         "file": "decode.cu",
         "sha256": "8d56116c44ad809818b6a8816f9efa1d0dfadd4071b9e7a1e967acc49574fee0",
