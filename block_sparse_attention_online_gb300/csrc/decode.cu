@@ -1,21 +1,35 @@
-// Split-KV decode with softmax-threshold block skipping (bf16 cache, d = 128).
+// Split-KV decode with softmax-threshold block skipping (bf16 cache, d = 128,
+// Bc = 128), on the tensor cores.
 //
-// One CTA per (sequence, KV head, split).  The G query heads sharing the KV
-// head are packed into the CTA, so each key byte is read once for all of them.
-// The BLASST page's decode kernel (section "Decode 内核：砍带宽") skips the value
-// load of a skipped block and avoids a decide-then-load bubble by computing
-// the scores of a batch of blocks before issuing the value loads of the
-// survivors.  Here that batch is a sliding window:
-//   * a K-producer warp streams whole 32 KB key blocks into a 4-stage shared
-//     memory ring with bulk copies (every block: Q.K^T is never skipped);
-//   * eight consumer warps compute the scores of block j from shared memory
-//     (16-byte vector reads, fp32 FMA), reduce the block maxima and take the
-//     decision of block j in order (Eq. 5 against the running max; all G
-//     heads must vote skip);
-//   * a V-producer warp loads the value block of each kept block as soon as
-//     its decision is published;
-//   * the consumers exponentiate block j-2 and accumulate P.V of block j-3,
-//     so a kept block's value load has the score work of two blocks to land.
+// Method: the BLASST page, sections "BLASST 的判定准则" (Eq. 5) and "Decode 内核：
+// 砍带宽" (in decode the skipped block's value load is the saving; the scores
+// of a block decide whether its values are read at all).  One CTA per
+// (sequence, KV head, split); the G query heads sharing the KV head are the
+// rows of the products, so each key byte is read once for all of them and the
+// decision of a block is the AND of the G heads' votes.
+//
+// The G heads are padded to the 128 rows of a tcgen05 MMA: the tensor core
+// idles in decode anyway, and a full-width row per head puts each head's 128
+// scores in one thread, so a block's row maxima, votes and decision need no
+// reduction across warps.  Per block:
+//   S_j   = Q K_j^T        (M 128 padded heads, N 128 keys, K 128; TMEM)
+//   P_j   = exp2(S_j - ref) (bf16 pairs into a TMEM P buffer, kept blocks)
+//   O    += P_j V_j        (A = P from TMEM, B = V_j from shared memory)
+// Warp roles (160 threads):
+//   warp 0  softmax: lane g < G owns head g.  Row max of S_j, vote, decision
+//           (published to the producers and the P.V issuer), then for a kept
+//           block P_j, its row sum and a lazy O rescale; epilogue;
+//   warp 1  TMA producer of K_j (every block, 4-stage ring);
+//   warp 2  Q.K^T issuer (two TMEM S buffers; also allocates TMEM);
+//   warp 3  TMA producer of V_j for kept blocks only, issued as soon as the
+//           block's decision is published (2-stage ring);
+//   warp 4  P.V issuer.
+// The softmax warp frees a block's S buffer as soon as the scores are in its
+// registers (P lives in its own TMEM buffers), so the Q.K^T products of the
+// next blocks, and with them the next decisions and value loads, run ahead
+// while a kept block's value load is still in flight.
+// TMEM columns: S buffers [0,256), P buffers [256,384), O [384,512).
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -27,56 +41,131 @@ namespace {
 
 using namespace tc;
 
-constexpr int D = 128;         // head size (keys and values)
-constexpr int BC = 128;        // keys per block
-constexpr int NKS = 4;         // key stages
-constexpr int NVS = 2;         // value stages
-constexpr int LAG = 2;         // exponentials of block j - LAG, P.V of block j - LAG - 1
-constexpr int R = LAG + 3;     // score ring (see the reuse argument at the loop)
-constexpr int NDEC = 8;        // decision ring
-constexpr int NCW = 8;         // consumer warps
-constexpr int NT = (NCW + 2) * 32;
-constexpr int WARP_K = NCW, WARP_V = NCW + 1;
-constexpr uint32_t BLK_BYTES = BC * D * 2;  // 32 KB
+constexpr int D = 128;   // head size (keys and values)
+constexpr int BC = 128;  // keys per block
+constexpr int MR = 128;  // MMA rows (heads padded)
+constexpr int NK = 4;    // key stages
+constexpr int NV = 2;    // value stages
+constexpr int NS = 2;    // TMEM S buffers
+constexpr int NP = 2;    // TMEM P buffers
+constexpr int NDEC = 8;  // decision ring
+constexpr int NT = 5 * 32;
+constexpr int WARP_K = 1, WARP_QK = 2, WARP_V = 3, WARP_PV = 4;  // warp 0: softmax
+constexpr uint32_t TILE_BYTES = BC * D * 2;      // 32 KB: 128 rows x 128 bf16
+constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;  // one 64-column swizzled box
+constexpr uint32_t SMEM_K = 0;
+constexpr uint32_t SMEM_V = SMEM_K + NK * TILE_BYTES;
+constexpr uint32_t SMEM_Q = SMEM_V + NV * TILE_BYTES;
+constexpr uint32_t SMEM_TILES = SMEM_Q + TILE_BYTES;  // 224 KB
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_P = NS * BC;
+constexpr uint32_t TMEM_O = TMEM_P + NP * (BC / 2);
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;  // exp reference may lag the max by 2^8
+constexpr uint32_t IDESC_QK = idesc_bf16_f32(MR, BC, 0);  // K_j: K-major
+constexpr uint32_t IDESC_PV = idesc_bf16_f32(MR, D, 1);   // V_j: MN-major
+constexpr uint32_t NEG_INF_BITS = 0xff800000u;
 
-template <int G>
-struct DecShared {
-  uint64_t k_full[NKS], k_empty[NKS];
-  uint64_t v_full[NVS], v_empty[NVS];
+struct Shared {
+  uint64_t k_full[NK], k_empty[NK];
+  uint64_t v_full[NV], v_empty[NV];
+  uint64_t s_full[NS], s_free[NS];
+  uint64_t p_full[NP], p_free[NP];
+  uint64_t pv_done[2];
   uint64_t dec_full[NDEC], dec_empty[NDEC];
-  uint64_t bar[2], fin;
   int dec[NDEC];
-  float wmax[2][NCW][G];
-  float mrow[R][G];               // running max after block (log2 units), slot block % R
-  alignas(16) float S[R][BC][G];  // scores (log2 units), then P in place
+  uint32_t tmem_base;
   int abort;
 };
+constexpr uint32_t SMEM_ALLOC = SMEM_TILES + ((sizeof(Shared) + 127) / 128) * 128;
+static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
-template <int G>
-constexpr uint32_t smem_bytes() {
-  return (NKS + NVS) * BLK_BYTES + (uint32_t)sizeof(DecShared<G>);
+// K-major 128 x 128 bf16 tile held as two 128-byte-swizzled boxes of 64
+// columns: k-step kk (16 columns) is box kk/4 at 32-byte step kk%4; 8-row
+// groups are 1024 bytes apart.
+__device__ __forceinline__ uint64_t kmajor_base(uint32_t tile) {
+  return smem_desc_sw128(tile, 16u, 1024u);
+}
+__device__ __forceinline__ constexpr uint64_t kmajor_step(int kk) {
+  return (uint64_t)(((uint32_t)(kk >> 2) * HALF_BYTES + (uint32_t)(kk & 3) * 32u) >> 4);
+}
+// MN-major value tile: rows are keys (64 values per swizzled 128-byte row),
+// 8-key groups 1024 bytes apart, the second 64-value half 16 KB further;
+// k-step kk (16 keys) starts 2048 bytes further.
+__device__ __forceinline__ uint64_t vmajor_base(uint32_t tile) {
+  return smem_desc_sw128(tile, HALF_BYTES, 1024u);
+}
+__device__ __forceinline__ constexpr uint64_t vmajor_step(int kk) {
+  return (uint64_t)(((uint32_t)kk * 2048u) >> 4);
 }
 
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 r;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "r"(addr));
-  return r;
+__device__ __forceinline__ float chunk_max(const uint32_t (&s)[32]) {
+  float m[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i)
+    m[i] = fmax3(__uint_as_float(s[3 * i]), __uint_as_float(s[3 * i + 1]),
+                 __uint_as_float(s[3 * i + 2]));
+  m[10] = fmaxf(__uint_as_float(s[30]), __uint_as_float(s[31]));
+  const float a = fmax3(m[0], m[1], m[2]), b = fmax3(m[3], m[4], m[5]);
+  const float c = fmax3(m[6], m[7], m[8]), d = fmaxf(m[9], m[10]);
+  return fmaxf(fmax3(a, b, c), d);
 }
 
-template <int G>
-__global__ void __launch_bounds__(NT, 1) decode_bf16_kernel(const DecodeArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  DecShared<G> &sh = *reinterpret_cast<DecShared<G> *>(smem + (NKS + NVS) * BLK_BYTES);
-  const uint32_t kring = smem_u32(smem), vring = kring + NKS * BLK_BYTES;
-  volatile int *abort = &sh.abort;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// P = exp2(s * sl2 - ref) for one 32-key chunk as 16 packed bf16 pairs, with
+// the row sum accumulated in two packed fp32 pairs.
+__device__ __forceinline__ void chunk_exp(const uint32_t (&s)[32], uint64_t sl2x2,
+                                          uint64_t negref2, uint64_t (&acc)[2],
+                                          uint32_t *pk) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float x0, x1;
+    f2_split(f2_fma(f2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), sl2x2,
+                    negref2),
+             x0, x1);
+    const float p0 = ex2(x0), p1 = ex2(x1);
+    acc[i & 1] = f2_add(acc[i & 1], f2(p0, p1));
+    pk[i] = pack_bf16x2(p0, p1);
+  }
+}
+
+// Scores of keys at or past the cache end (the zero-filled tail of the last
+// block) become -inf in TMEM before anything reads them.  Short and out of
+// line: it runs once per sequence from a cold instruction cache.
+__device__ __noinline__ void mask_tail_tmem(uint32_t sa, int lim) {
+  uint32_t ninf[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) ninf[i] = NEG_INF_BITS;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    const int l = lim - 32 * c;
+    if (l >= 32) continue;
+    if (l <= 0) {
+      tmem_st32(sa + 32 * c, ninf);
+      continue;
+    }
+    uint32_t x[32];
+    tmem_ld32(sa + 32 * c, x);
+    tmem_wait_ld_regs(x);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = i < l ? x[i] : NEG_INF_BITS;
+    tmem_st32(sa + 32 * c, x);
+  }
+  tmem_wait_st();
+}
+
+__global__ void __launch_bounds__(NT, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Shared &sh = *reinterpret_cast<Shared *>(smem_raw + SMEM_TILES);
+  const uint32_t base = smem_u32(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (base & 1023u) {  // the swizzled layouts need a 1024-byte aligned base
+    if (tid == 0) atomicOr(a.err, kErrTimeout);
+    return;
+  }
+  const int G = a.Hq / a.Hkv;
   const int unit = blockIdx.x;
   const int sp = unit % a.n_splits;
   const int hk = (unit / a.n_splits) % a.Hkv;
@@ -84,11 +173,9 @@ __global__ void __launch_bounds__(NT, 1) decode_bf16_kernel(const DecodeArgs a) 
   const int j0 = (int)((long)sp * a.n_b / a.n_splits);
   const int j1 = (int)((long)(sp + 1) * a.n_b / a.n_splits);
   const int nb = j1 - j0;
-  const float sl2 = a.scale * kLog2e;      // raw score -> log2 units
-  const float c2 = a.ln_lambda * kLog2e;   // ln(lambda) in log2 units (-inf if lambda = 0)
-  const __nv_bfloat16 *kg = (const __nv_bfloat16 *)a.k + ((size_t)(b * a.Hkv + hk) * a.L) * D;
-  const __nv_bfloat16 *vg = (const __nv_bfloat16 *)a.v + ((size_t)(b * a.Hkv + hk) * a.L) * D;
+  const int zkv = b * a.Hkv + hk;
   uint32_t *bits = a.bits + (size_t)unit * a.words;
+  volatile int *abort = &sh.abort;
 
   if (nb == 0) {  // empty split: no key, zero weight in the merge
     for (int idx = tid; idx < G * D; idx += NT) {
@@ -100,55 +187,81 @@ __global__ void __launch_bounds__(NT, 1) decode_bf16_kernel(const DecodeArgs a) 
     return;
   }
 
+  // Q tile (A operand of Q.K^T): row g < G = query head hk*G + g, other rows
+  // zero; K-major, two 128-byte-swizzled boxes of 64 columns (16-byte chunk c
+  // of row r sits at chunk position c ^ (r % 8)).
+  {
+    const __nv_bfloat16 *qg = (const __nv_bfloat16 *)a.q + (size_t)(b * a.Hq + hk * G) * D;
+    for (int idx = tid; idx < MR * (D / 8); idx += NT) {  // one 16-byte chunk each
+      const int r = idx / (D / 8), cc = idx % (D / 8);
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < G) v = *reinterpret_cast<const uint4 *>(qg + (size_t)r * D + cc * 8);
+      const int box = cc >> 3, c = cc & 7;
+      st_shared_v4(base + SMEM_Q + box * HALF_BYTES + r * 128 + ((c ^ (r & 7)) * 16), v.x, v.y,
+                   v.z, v.w);
+    }
+    fence_proxy_async_smem();  // visible to the tensor core
+  }
   if (tid == 0) {
-    for (int i = 0; i < NKS; ++i) {
+    for (int i = 0; i < NK; ++i) {
       mbar_init(smem_u32(&sh.k_full[i]), 1);
-      mbar_init(smem_u32(&sh.k_empty[i]), NCW);
+      mbar_init(smem_u32(&sh.k_empty[i]), 1);
     }
-    for (int i = 0; i < NVS; ++i) {
+    for (int i = 0; i < NV; ++i) {
       mbar_init(smem_u32(&sh.v_full[i]), 1);
-      mbar_init(smem_u32(&sh.v_empty[i]), NCW);
+      mbar_init(smem_u32(&sh.v_empty[i]), 1);
     }
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(&sh.s_full[i]), 1);
+      mbar_init(smem_u32(&sh.s_free[i]), 1);
+    }
+    for (int i = 0; i < NP; ++i) {
+      mbar_init(smem_u32(&sh.p_full[i]), 1);
+      mbar_init(smem_u32(&sh.p_free[i]), 1);
+    }
+    mbar_init(smem_u32(&sh.pv_done[0]), 1);
+    mbar_init(smem_u32(&sh.pv_done[1]), 1);
     for (int i = 0; i < NDEC; ++i) {
       mbar_init(smem_u32(&sh.dec_full[i]), 1);
-      mbar_init(smem_u32(&sh.dec_empty[i]), 1);
+      mbar_init(smem_u32(&sh.dec_empty[i]), 2);  // V producer and P.V issuer
     }
-    mbar_init(smem_u32(&sh.bar[0]), NCW);
-    mbar_init(smem_u32(&sh.bar[1]), NCW);
-    mbar_init(smem_u32(&sh.fin), NCW);
     sh.abort = 0;
     fence_mbar_init();
   }
+  if (warp == WARP_QK) tmem_alloc(smem_u32(&sh.tmem_base), TMEM_COLS);
+  fence_before_sync();
   __syncthreads();
-
-  auto block_keys = [&](int j) { return min(BC, a.L - (j0 + j) * BC); };
+  fence_after_sync();
+  const uint32_t tmem = sh.tmem_base;
 
   if (warp == WARP_K) {
     // ---------------------------------------------------------- K producer --
     if (lane == 0) {
+      prefetch_tmap(&tm_k);
       const uint64_t pol = policy_evict_first();  // the cache is streamed once
       int issued = 0;
       for (int j = 0; j < nb && !*abort; ++j) {
-        const int s = j % NKS;
-        if (j >= NKS &&
-            !mbar_wait(smem_u32(&sh.k_empty[s]), ((j / NKS) - 1) & 1, abort, a.err, kErrTimeout))
+        const int s = j % NK;
+        if (j >= NK &&
+            !mbar_wait(smem_u32(&sh.k_empty[s]), ((j / NK) - 1) & 1, abort, a.err, kErrTimeout))
           break;
-        const uint32_t bytes = (uint32_t)block_keys(j) * D * 2;
-        mbar_expect_tx(smem_u32(&sh.k_full[s]), bytes);
-        bulk_load(kring + s * BLK_BYTES, kg + (size_t)(j0 + j) * BC * D, bytes,
-                  smem_u32(&sh.k_full[s]), pol);
+        const uint32_t dst = base + SMEM_K + s * TILE_BYTES;
+        const int key0 = (j0 + j) * BC;
+        mbar_expect_tx(smem_u32(&sh.k_full[s]), TILE_BYTES);
+        tma_load_3d(dst, &tm_k, smem_u32(&sh.k_full[s]), 0, key0, zkv, pol);
+        tma_load_3d(dst + HALF_BYTES, &tm_k, smem_u32(&sh.k_full[s]), 64, key0, zkv, pol);
         ++issued;
       }
-      for (int s = 0; s < NKS && s < issued; ++s) {
-        const int last = s + ((issued - 1 - s) / NKS) * NKS;
-        mbar_wait_drain(smem_u32(&sh.k_full[s]), (last / NKS) & 1);
+      // Drain: the last load issued into each slot has landed before exit.
+      for (int s = 0; s < NK && s < issued; ++s) {
+        const int last = s + ((issued - 1 - s) / NK) * NK;
+        mbar_wait_drain(smem_u32(&sh.k_full[s]), (last / NK) & 1);
       }
     }
-    return;
-  }
-  if (warp == WARP_V) {
+  } else if (warp == WARP_V) {
     // ---------------------------------------------------------- V producer --
     if (lane == 0) {
+      prefetch_tmap(&tm_v);
       const uint64_t pol = policy_evict_first();
       int vi = 0;
       for (int j = 0; j < nb && !*abort; ++j) {
@@ -158,326 +271,245 @@ __global__ void __launch_bounds__(NT, 1) decode_bf16_kernel(const DecodeArgs a) 
         const int keep = sh.dec[j % NDEC];
         mbar_arrive(smem_u32(&sh.dec_empty[j % NDEC]));
         if (!keep) continue;
-        const int s = vi % NVS;
-        if (vi >= NVS &&
-            !mbar_wait(smem_u32(&sh.v_empty[s]), ((vi / NVS) - 1) & 1, abort, a.err, kErrTimeout))
+        const int s = vi % NV;
+        if (vi >= NV &&
+            !mbar_wait(smem_u32(&sh.v_empty[s]), ((vi / NV) - 1) & 1, abort, a.err, kErrTimeout))
           break;
-        const uint32_t bytes = (uint32_t)block_keys(j) * D * 2;
-        mbar_expect_tx(smem_u32(&sh.v_full[s]), bytes);
-        bulk_load(vring + s * BLK_BYTES, vg + (size_t)(j0 + j) * BC * D, bytes,
-                  smem_u32(&sh.v_full[s]), pol);
+        const uint32_t dst = base + SMEM_V + s * TILE_BYTES;
+        const int key0 = (j0 + j) * BC;
+        mbar_expect_tx(smem_u32(&sh.v_full[s]), TILE_BYTES);
+        tma_load_3d(dst, &tm_v, smem_u32(&sh.v_full[s]), 0, key0, zkv, pol);
+        tma_load_3d(dst + HALF_BYTES, &tm_v, smem_u32(&sh.v_full[s]), 64, key0, zkv, pol);
         ++vi;
       }
-      for (int s = 0; s < NVS && s < vi; ++s) {
-        const int last = s + ((vi - 1 - s) / NVS) * NVS;
-        mbar_wait_drain(smem_u32(&sh.v_full[s]), (last / NVS) & 1);
+      for (int s = 0; s < NV && s < vi; ++s) {
+        const int last = s + ((vi - 1 - s) / NV) * NV;
+        mbar_wait_drain(smem_u32(&sh.v_full[s]), (last / NV) & 1);
       }
     }
-    return;
-  }
-
-  // -------------------------------------------------------------- consumers --
-  // QK layout: 8 lanes per key, lane p holds dims [8p, 8p+8) and [64+8p, 64+8p+8);
-  // a warp step covers 4 keys.
-  const int kq = lane >> 3, p = lane & 7;
-  uint64_t qp[G][8];  // packed fp32 pairs of the thread's 16 query dims, per head
+  } else if (warp == WARP_QK) {
+    // -------------------------------------------------------- Q.K^T issuer --
+    if (lane == 0) {
+      const uint64_t qdesc = kmajor_base(base + SMEM_Q);
+      for (int j = 0; j < nb; ++j) {
+        const int s = j % NK, sb = j % NS;
+        if (!mbar_wait(smem_u32(&sh.k_full[s]), (j / NK) & 1, abort, a.err, kErrTimeout)) break;
+        // S buffer sb is free once the softmax warp has read block j - NS.
+        if (j >= NS && !mbar_wait(smem_u32(&sh.s_free[sb]), ((j / NS) - 1) & 1, abort, a.err,
+                                  kErrTimeout))
+          break;
+        fence_after_sync();
+        const uint64_t kd = kmajor_base(base + SMEM_K + s * TILE_BYTES);
+        const uint32_t d_s = tmem + sb * BC;
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const __nv_bfloat16 *qh = (const __nv_bfloat16 *)a.q + (size_t)(b * a.Hq + hk * G + g) * D;
-    const uint4 lo = *reinterpret_cast<const uint4 *>(qh + 8 * p);
-    const uint4 hi = *reinterpret_cast<const uint4 *>(qh + 64 + 8 * p);
-    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ss(d_s, qdesc + kmajor_step(kk), kd + kmajor_step(kk), IDESC_QK, kk > 0);
+        mma_commit(smem_u32(&sh.s_full[sb]));
+        mma_commit(smem_u32(&sh.k_empty[s]));
+      }
+    }
+  } else if (warp == WARP_PV) {
+    // ---------------------------------------------------------- P.V issuer --
+    if (lane == 0) {
+      int kc = 0, vi = 0;
+      for (int j = 0; j < nb && !*abort; ++j) {
+        if (!mbar_wait(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
+                       kErrTimeout))
+          break;
+        const int keep = sh.dec[j % NDEC];
+        mbar_arrive(smem_u32(&sh.dec_empty[j % NDEC]));
+        if (!keep) continue;
+        const int pb = kc % NP, vs = vi % NV;
+        if (!mbar_wait(smem_u32(&sh.p_full[pb]), (kc / NP) & 1, abort, a.err, kErrTimeout) ||
+            !mbar_wait(smem_u32(&sh.v_full[vs]), (vi / NV) & 1, abort, a.err, kErrTimeout))
+          break;
+        fence_after_sync();
+        // P (bf16 pairs): keys [0,128) in the 64 columns of P buffer pb.
+        const uint32_t pt = tmem + TMEM_P + pb * (BC / 2);
+        const uint64_t vd = vmajor_base(base + SMEM_V + vs * TILE_BYTES);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) qp[g][i] = f2(bf_lo(w[i]), bf_hi(w[i]));
-  }
-  // PV layout: chunk c = tid % 16 owns value dims [8c, 8c+8); key slot ks = tid / 16.
-  const int c = tid & 15, ks = tid >> 4;
-  uint64_t acc2[G][4];  // packed output pairs (dims 8c+2e, 8c+2e+1)
-  float lsum[G], ref[G], m[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m[g] = -INFINITY;
-    ref[g] = -INFINITY;
-    lsum[g] = 0.f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc2[g][e] = f2(0.f, 0.f);
-  }
-  uint32_t hist = 0;  // bit d: block (j - d) kept
-  uint32_t word = 0;
-  int vi = 0;
-  bool ok = true;
-
-  // Ring reuse: the score slot of block j (written before the barrier of
-  // iteration j) last served the P.V of block j - R = j - LAG - 3 in iteration
-  // j - 2, which every warp finished before the barrier of iteration j - 1.
-  for (int j = 0; ok && j < nb + LAG + 1; ++j) {
-    const int pb = j & 1;
-    if (j < nb) {
-      // ---- scores of block j ---------------------------------------------
-      const int s = j % NKS, rs = j % R;
-      if (!mbar_wait_warp(smem_u32(&sh.k_full[s]), (j / NKS) & 1, abort, a.err, kErrTimeout)) {
+        for (int kk = 0; kk < BC / 16; ++kk)
+          mma_bf16_ts(tmem + TMEM_O, pt + kk * 8, vd + vmajor_step(kk), IDESC_PV,
+                      (kc > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&sh.v_empty[vs]));
+        mma_commit(smem_u32(&sh.p_free[pb]));
+        mma_commit(smem_u32(&sh.pv_done[kc & 1]));
+        ++kc;
+        ++vi;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- softmax --
+    // Lane g < G: head g's row (TMEM lane g) over the block's 128 keys.
+    const bool head = lane < G;
+    const float sl2 = a.scale * kLog2e;   // raw score -> log2 units
+    const float c2 = a.ln_lambda * kLog2e;  // ln(lambda) in log2 units
+    float m2 = -INFINITY;                 // running max of the split (log2 units)
+    float mref = -INFINITY;               // exp reference (log2 units)
+    float l = 0.f;                        // row sum relative to mref
+    int kc = 0;                           // kept blocks
+    uint32_t word = 0;
+    bool ok = true;
+    for (int j = 0; j < nb; ++j) {
+      const int sb = j % NS;
+      if (!mbar_wait_warp(smem_u32(&sh.s_full[sb]), (j / NS) & 1, abort, a.err, kErrTimeout)) {
         ok = false;
         break;
       }
-      const int keys = block_keys(j);
-      const uint32_t kt = kring + s * BLK_BYTES;
-      constexpr int NSTEP = BC / (4 * NCW);  // warp steps of 4 keys (= 4)
-      float val[NSTEP * G];                    // partial dots, index step * G + g
-#pragma unroll
-      for (int step = 0; step < NSTEP; ++step) {
-        const int kl = (step * NCW + warp) * 4 + kq;
-        uint4 k0 = make_uint4(0, 0, 0, 0), k1 = make_uint4(0, 0, 0, 0);
-        if (kl < keys) {
-          k0 = lds128(kt + kl * (D * 2) + p * 16);
-          k1 = lds128(kt + kl * (D * 2) + 128 + p * 16);
-        }
-        const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-        uint64_t d2[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) d2[g] = f2(0.f, 0.f);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint64_t x = f2(bf_lo(w[i]), bf_hi(w[i]));
-#pragma unroll
-          for (int g = 0; g < G; ++g) d2[g] = f2_fma(qp[g][i], x, d2[g]);
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float lo, hi;
-          f2_split(d2[g], lo, hi);
-          val[step * G + g] = lo + hi;
-        }
-      }
-      // Sum over the 8 lanes of a key group.  Transposed butterfly: each level
-      // exchanges half of the values, so after three levels lane p holds the
-      // full dots v = p*G/2 + r (r < G/2) of step p/2, heads (p%2)*G/2 + r.
-      float bm[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) bm[g] = -INFINITY;
-      if constexpr (G >= 2) {
-        float v1[2 * G], v2[G], v3[G / 2];
-        const bool u1 = lane & 4, u2 = lane & 2, u3 = lane & 1;
-#pragma unroll
-        for (int i = 0; i < 2 * G; ++i) {
-          const float x = val[i], y = val[i + 2 * G];
-          v1[i] = (u1 ? y : x) + __shfl_xor_sync(0xffffffffu, u1 ? x : y, 4);
-        }
-#pragma unroll
-        for (int i = 0; i < G; ++i) {
-          const float x = v1[i], y = v1[i + G];
-          v2[i] = (u2 ? y : x) + __shfl_xor_sync(0xffffffffu, u2 ? x : y, 2);
-        }
-#pragma unroll
-        for (int i = 0; i < G / 2; ++i) {
-          const float x = v2[i], y = v2[i + G / 2];
-          v3[i] = (u3 ? y : x) + __shfl_xor_sync(0xffffffffu, u3 ? x : y, 1);
-        }
-        const int step = p >> 1, g0 = (p & 1) * (G / 2);
-        const int kl = (step * NCW + warp) * 4 + kq;
-        float hm[G / 2];
-#pragma unroll
-        for (int r = 0; r < G / 2; ++r) {
-          const float sv = kl < keys ? v3[r] * sl2 : -INFINITY;
-          sh.S[rs][kl][g0 + r] = sv;
-          hm[r] = sv;
-        }
-        // block max per head: lanes with the same p%2 hold the same heads
-#pragma unroll
-        for (int r = 0; r < G / 2; ++r) {
-          hm[r] = fmaxf(hm[r], __shfl_xor_sync(0xffffffffu, hm[r], 2));
-          hm[r] = fmaxf(hm[r], __shfl_xor_sync(0xffffffffu, hm[r], 4));
-          hm[r] = fmaxf(hm[r], __shfl_xor_sync(0xffffffffu, hm[r], 8));
-          hm[r] = fmaxf(hm[r], __shfl_xor_sync(0xffffffffu, hm[r], 16));
-        }
-        if (lane < 2) {
-#pragma unroll
-          for (int r = 0; r < G / 2; ++r) sh.wmax[pb][warp][lane * (G / 2) + r] = hm[r];
-        }
-      } else {  // one head: plain butterfly over the 8 lanes
-#pragma unroll
-        for (int step = 0; step < NSTEP; ++step) {
-          float x = val[step];
-          x += __shfl_xor_sync(0xffffffffu, x, 1);
-          x += __shfl_xor_sync(0xffffffffu, x, 2);
-          x += __shfl_xor_sync(0xffffffffu, x, 4);
-          const int kl = (step * NCW + warp) * 4 + kq;
-          const float sv = kl < keys ? x * sl2 : -INFINITY;
-          if (p == 0) sh.S[rs][kl][0] = sv;
-          bm[0] = fmaxf(bm[0], sv);
-        }
-        bm[0] = fmaxf(bm[0], __shfl_xor_sync(0xffffffffu, bm[0], 8));
-        bm[0] = fmaxf(bm[0], __shfl_xor_sync(0xffffffffu, bm[0], 16));
-        if (lane == 0) sh.wmax[pb][warp][0] = bm[0];
-      }
+      fence_after_sync();
+      const uint32_t sa = tmem + sb * BC;  // lanes 0-31: this warp's TMEM quarter
+      const int lim = a.L - (j0 + j) * BC;
+      if (lim < BC) mask_tail_tmem(sa, lim);
+      uint32_t x0[32], x1[32], x2[32], x3[32];
+      tmem_ld32(sa, x0);
+      tmem_ld32(sa + 32, x1);
+      tmem_ld32(sa + 64, x2);
+      tmem_ld32(sa + 96, x3);
+      tmem_wait_ld_regs(x0);
+      tmem_wait_ld_regs(x1);
+      tmem_wait_ld_regs(x2);
+      tmem_wait_ld_regs(x3);
+      // The scores are in registers: the S buffer can take block j + NS.
+      fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.k_empty[s]));
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&sh.bar[pb]));
-    if (!mbar_wait_warp(smem_u32(&sh.bar[pb]), (j >> 1) & 1, abort, a.err, kErrTimeout)) {
-      ok = false;
-      break;
-    }
-
-    // ---- decision of block j (every thread takes it identically) -----------
-    if (j < nb) {
-      bool all_skip = true;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float mt = sh.wmax[pb][0][g];
-#pragma unroll
-        for (int w = 1; w < NCW; ++w) mt = fmaxf(mt, sh.wmax[pb][w][g]);
-        const float mn = fmaxf(m[g], mt);
-        const float diff = (mt == -INFINITY) ? -INFINITY : mt - mn;
-        all_skip = all_skip && (diff < c2);
-        m[g] = mn;
-      }
-      hist = (hist << 1) | (all_skip ? 0u : 1u);
-      if (tid == 0) {
+      if (lane == 0) mbar_arrive(smem_u32(&sh.s_free[sb]));
+      const float mt =
+          fmaxf(fmaxf(chunk_max(x0), chunk_max(x1)), fmaxf(chunk_max(x2), chunk_max(x3)));
+      const float pm2 = mt * sl2;
+      // With c < 0, "rowmax - m_new < c" is "rowmax - m_old < c" (a block
+      // that raises the max fails both).  Every head must vote skip.
+      const float diff = (mt == -INFINITY) ? -INFINITY : pm2 - m2;
+      const bool skip = __all_sync(0xffffffffu, !head || diff < c2);
+      if (lane == 0) {
         // On a timeout the abort flag is raised and every later wait fails.
-        if (j < NDEC || mbar_wait(smem_u32(&sh.dec_empty[j % NDEC]), ((j / NDEC) - 1) & 1, abort,
-                                  a.err, kErrTimeout)) {
-          sh.dec[j % NDEC] = all_skip ? 0 : 1;
+        if (j < NDEC || mbar_wait(smem_u32(&sh.dec_empty[j % NDEC]), ((j / NDEC) - 1) & 1,
+                                  abort, a.err, kErrTimeout)) {
+          sh.dec[j % NDEC] = skip ? 0 : 1;
           mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
         }
-#pragma unroll
-        for (int g = 0; g < G; ++g) sh.mrow[j % R][g] = m[g];
-        if (all_skip) word |= 1u << (j & 31);
+        if (skip) word |= 1u << (j & 31);
         if ((j & 31) == 31 || j == nb - 1) {
           bits[j >> 5] = word;
           word = 0;
         }
       }
-    } else {
-      hist <<= 1;  // past the end: nothing to keep
-    }
-
-    // ---- P.V of block j - LAG - 1 (its P was written in the last iteration) -
-    const int i1 = j - LAG - 1;
-    if (i1 >= 0 && ((hist >> (LAG + 1)) & 1u)) {
-      const int vs = vi % NVS;
-      if (!mbar_wait_warp(smem_u32(&sh.v_full[vs]), (vi / NVS) & 1, abort, a.err, kErrTimeout)) {
+      if (skip) continue;
+      const float mnew = fmaxf(m2, pm2);
+      m2 = mnew;
+      bool rescale = false;
+      float alpha = 1.f;
+      if (mref == -INFINITY) {
+        mref = mnew;
+      } else if (mnew > mref + kRescaleLog2) {
+        alpha = ex2(mref - mnew);
+        mref = mnew;
+        rescale = true;
+      }
+      const int pb = kc % NP;
+      // P buffer pb last fed the P.V of kept block kc - NP.
+      if (kc >= NP && !mbar_wait_warp(smem_u32(&sh.p_free[pb]), ((kc / NP) - 1) & 1, abort,
+                                      a.err, kErrTimeout)) {
         ok = false;
         break;
       }
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float nr = sh.mrow[i1 % R][g];
-        const float alpha = (ref[g] == -INFINITY) ? 0.f : ex2(ref[g] - nr);
-        ref[g] = nr;
-        lsum[g] *= alpha;
-        const uint64_t a2 = f2(alpha, alpha);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc2[g][e] = f2_fma(acc2[g][e], a2, f2(0.f, 0.f));
+      fence_after_sync();
+      const uint32_t pa = tmem + TMEM_P + pb * (BC / 2);
+      const uint64_t sl2x2 = f2(sl2, sl2), negref2 = f2(-mref, -mref);
+      uint64_t acc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+      {
+        uint32_t pk[32];
+        chunk_exp(x0, sl2x2, negref2, acc2, pk);
+        chunk_exp(x1, sl2x2, negref2, acc2, pk + 16);
+        tmem_st32(pa, pk);
+        chunk_exp(x2, sl2x2, negref2, acc2, pk);
+        chunk_exp(x3, sl2x2, negref2, acc2, pk + 16);
+        tmem_st32(pa + 32, pk);
       }
-      const int keys = block_keys(i1);
-      const uint32_t vt = vring + vs * BLK_BYTES;
-#pragma unroll 4
-      for (int kk = ks; kk < keys; kk += 16) {
-        const uint4 v = lds128(vt + kk * (D * 2) + c * 16);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        float pg[G];
-        if constexpr (G == 4) {
-          const float4 p4 = *reinterpret_cast<const float4 *>(&sh.S[i1 % R][kk][0]);
-          pg[0] = p4.x;
-          pg[1] = p4.y;
-          pg[2] = p4.z;
-          pg[3] = p4.w;
-        } else {
-#pragma unroll
-          for (int g = 0; g < G; ++g) pg[g] = sh.S[i1 % R][kk][g];
+      tmem_wait_st();
+      float acc[4];
+      f2_split(acc2[0], acc[0], acc[1]);
+      f2_split(acc2[1], acc[2], acc[3]);
+      l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+      // O rescale of the heads' rows once the previous P.V has landed.
+      if (__any_sync(0xffffffffu, rescale) && kc >= 1) {
+        if (!mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort,
+                            a.err, kErrTimeout)) {
+          ok = false;
+          break;
         }
-        uint64_t vx[4];
+        fence_after_sync();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          const uint32_t oa = tmem + TMEM_O + c * 32;
+          tmem_ld32(oa, o);
+          tmem_wait_ld_regs(o);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) vx[e] = f2(bf_lo(w[e]), bf_hi(w[e]));
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          lsum[g] += pg[g];
-          const uint64_t pp = f2(pg[g], pg[g]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc2[g][e] = f2_fma(pp, vx[e], acc2[g][e]);
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(oa, o);
         }
+        tmem_wait_st();
       }
+      fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.v_empty[vs]));
-      ++vi;
+      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[pb]));
+      ++kc;
     }
 
-    // ---- exponentials of block j - LAG (in place; read after the next barrier)
-    const int i2 = j - LAG;
-    if (i2 >= 0 && ((hist >> LAG) & 1u)) {
-      float nr[G];
+    // ---- epilogue: O_s = O / l and LSE_s = ref + ln l per head ---------------
+    if (lane == 0) {
+      for (int w = ((nb - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
+    }
+    if (ok && kc > 0)
+      ok = mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort, a.err,
+                          kErrTimeout);
+    if (ok) {
+      fence_after_sync();
+      const float inv = 1.f / l;
+      const size_t row = (size_t)(b * a.Hq + hk * G + lane) * a.n_splits + sp;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + TMEM_O + c * 32, o);
+        tmem_wait_ld_regs(o);
+        if (head) {
+          float4 *dst = reinterpret_cast<float4 *>(a.o_part + row * D + c * 32);
 #pragma unroll
-      for (int g = 0; g < G; ++g) nr[g] = sh.mrow[i2 % R][g];
-      float *Sv = &sh.S[i2 % R][0][0];
-      for (int idx = tid; idx < BC * G; idx += NCW * 32) {
-        const float sv = Sv[idx];
-        Sv[idx] = (sv == -INFINITY) ? 0.f : ex2(sv - nr[idx % G]);
+          for (int q4 = 0; q4 < 8; ++q4)
+            dst[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv,
+                                  __uint_as_float(o[4 * q4 + 1]) * inv,
+                                  __uint_as_float(o[4 * q4 + 2]) * inv,
+                                  __uint_as_float(o[4 * q4 + 3]) * inv);
+        }
       }
+      if (head) a.lse_part[row] = mref * kLn2 + logf(l);
     }
   }
 
-  // ---- epilogue: reduce the 16 key slots ------------------------------------
-  if (tid == 0) {
-    for (int w = ((nb - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
-  }
-  // Every key block was consumed, so the key ring is free for the reduction.
-  float(*red)[G][D] = reinterpret_cast<float(*)[G][D]>(smem);
-  float(*lred)[G] = reinterpret_cast<float(*)[G]>(smem + NCW * G * D * sizeof(float));
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    lsum[g] += __shfl_xor_sync(0xffffffffu, lsum[g], 16);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float lo, hi;
-      f2_split(acc2[g][e], lo, hi);
-      lo += __shfl_xor_sync(0xffffffffu, lo, 16);
-      hi += __shfl_xor_sync(0xffffffffu, hi, 16);
-      if (lane < 16) {
-        red[warp][g][8 * c + 2 * e] = lo;
-        red[warp][g][8 * c + 2 * e + 1] = hi;
-      }
-    }
-    if (lane == 0) lred[warp][g] = lsum[g];
-  }
   __syncwarp();
-  if (lane == 0) mbar_arrive(smem_u32(&sh.fin));
-  if (!mbar_wait_warp(smem_u32(&sh.fin), 0, abort, a.err, kErrTimeout) || !ok) return;
-  for (int idx = tid; idx < G * D; idx += NCW * 32) {
-    const int g = idx / D, e = idx % D;
-    float o = 0.f, l = 0.f;
-#pragma unroll
-    for (int w = 0; w < NCW; ++w) {
-      o += red[w][g][e];
-      l += lred[w][g];
-    }
-    const size_t row = (size_t)(b * a.Hq + hk * G + g) * a.n_splits + sp;
-    a.o_part[row * D + e] = o / l;
-    if (e == 0) a.lse_part[row] = ref[g] * kLn2 + logf(l);
+  fence_before_sync();
+  __syncthreads();
+  if (warp == WARP_QK) {
+    fence_after_sync();
+    tmem_dealloc(tmem, TMEM_COLS);
   }
-}
-
-template <int G>
-cudaError_t launch(const DecodeArgs &a, cudaStream_t s) {
-  constexpr uint32_t bytes = smem_bytes<G>();
-  static_assert(bytes <= 227 * 1024, "shared memory budget");
-  cudaError_t e = cudaFuncSetAttribute(decode_bf16_kernel<G>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e != cudaSuccess) return e;
-  const long units = (long)a.B * a.Hkv * a.n_splits;
-  decode_bf16_kernel<G><<<(unsigned)units, NT, bytes, s>>>(a);
-  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
-  switch (a.Hq / a.Hkv) {
-    case 1: return launch<1>(a, s);
-    case 2: return launch<2>(a, s);
-    case 4: return launch<4>(a, s);
-    default: return launch<8>(a, s);
-  }
+  CUtensorMap mk, mv;
+  // [B*Hkv, L, 128] bf16 with the caller's row stride; boxes of 64 columns x
+  // 128 keys; keys past L read as zero (and are masked).
+  if (!make_map_bf16_3d(&mk, a.k, D, a.k_row_stride, a.L, a.B * a.Hkv, BC) ||
+      !make_map_bf16_3d(&mv, a.v, D, a.v_row_stride, a.L, a.B * a.Hkv, BC))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  const long units = (long)a.B * a.Hkv * a.n_splits;
+  decode_tc_kernel<<<(unsigned)units, NT, SMEM_ALLOC, s>>>(mk, mv, a);
+  return cudaGetLastError();
 }
 
 }  // namespace attn_skip

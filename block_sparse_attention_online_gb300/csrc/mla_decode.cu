@@ -438,42 +438,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (EncodeTiledFn)p;
-  }
-  return fn;
-}
-
-// 3-D map over [outer, rows, 576] bf16 with a 64-column x box_rows box, 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *ptr, int outer, int rows, int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)DK, (cuuint64_t)rows, (cuuint64_t)outer};
-  const cuuint64_t strides[2] = {(cuuint64_t)DK * 2, (cuuint64_t)rows * DK * 2};
-  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s) {
   CUtensorMap mq, mkv;
-  if (!make_map(&mq, a.q, a.B, H, H) || !make_map(&mkv, a.k, a.B, a.L, BN))
+  // [B, rows, 576] bf16, boxes of 64 columns x (H or BN) rows, 128-byte swizzle.
+  if (!make_map_bf16_3d(&mq, a.q, DK, DK, H, a.B, H) ||
+      !make_map_bf16_3d(&mkv, a.k, DK, DK, a.L, a.B, BN))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);

@@ -580,44 +580,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = (EncodeTiledFn)p;
-  }
-  return fn;
-}
-
-// 3-D map over a [heads, T, 128] bf16 tensor, box 64 x 128 x 1, 128-byte swizzle;
-// rows past T read as zero.
-bool make_map(CUtensorMap *m, const void *ptr, int heads, int T) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)T, (cuuint64_t)heads};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)T * D * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, a.q, a.B * a.Hq, a.T) || !make_map(&mk, a.k, a.B * a.Hkv, a.T) ||
-      !make_map(&mv, a.v, a.B * a.Hkv, a.T))
+  // [heads, T, 128] bf16, boxes of 64 columns x 128 rows; rows past T read as zero.
+  if (!make_map_bf16_3d(&mq, a.q, D, D, a.T, a.B * a.Hq, BM) ||
+      !make_map_bf16_3d(&mk, a.k, D, D, a.T, a.B * a.Hkv, BN) ||
+      !make_map_bf16_3d(&mv, a.v, D, D, a.T, a.B * a.Hkv, BN))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
