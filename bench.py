@@ -48,10 +48,10 @@ NCU_TRAFFIC = {
         "file": "prefill_tc.cu",
         "sha256": "511769a136493c9b2aecee9272ec007e392c2d115d79b0ad6b3b8aa5e73e767c",
         "bytes": 240706304 + 83190272},
-    "decode_bf16_kernel": {
+    "decode_tc_kernel": {
         "file": "decode.cu",
-        "sha256": "8d56116c44ad809818b6a8816f9efa1d0dfadd4071b9e7a1e967acc49574fee0",
-        "bytes": 1396073000 + 8058624},
+        "sha256": "cbb3176da71abf2933cdd66f55ea77b4f11eacaa284e5e8338e00b63878345ef",
+        "bytes": 1396064256 + 3992064},
 }
 
 
@@ -329,10 +329,10 @@ def run_gpu(args, rank, world):
                      "traffic": ncu_traffic("prefill_tc_kernel"),
                      "algorithmic_bytes": int(P.B * P.Hq * P.T * P.d * 2 * 2
                                               + 2 * P.B * P.Hkv * P.T * P.d * 2)},
-        "decode_roofline": {"bound": "hbm", "kernel": "decode_bf16_kernel",
+        "decode_roofline": {"bound": "hbm", "kernel": "decode_tc_kernel",
                             "achieved": round(dec_gbs, 1), "peak": peak_hbm, "unit": "GB/s",
                             "frac": round(dec_gbs / peak_hbm, 4),
-                            "traffic": ncu_traffic("decode_bf16_kernel"),
+                            "traffic": ncu_traffic("decode_tc_kernel"),
                             "algorithmic_bytes": dec["bytes"]},
         "mla_decode": msweep,
         "e2e": e2e,
