@@ -19,8 +19,11 @@
 // scores, decisions, running maxima and row sums are bit-identical; the CTA
 // of half 0 writes the skip bits and the LSE.
 //
-// Per CTA (192 threads): warps 0-3 softmax (thread i owns head i = TMEM lane
-// i), warp 4 TMA producer, warp 5 MMA issuer.
+// Per CTA (224 threads): warps 0-3 softmax (thread i owns head i = TMEM lane
+// i), warp 4 TMA producer, warp 5 Q.K^T issuer, warp 6 P.V issuer.  With
+// separate issuing threads a kept block's P.V, and with it the release of its
+// latent slot, never waits behind the next block's Q.K^T (which waits for
+// that block's load).
 // Shared memory: Q dims [0,320) as five 128-byte-swizzled 64-column boxes
 // (80 KB); a two-slot ring of latent blocks, each nine 64 x 64 boxes (72 KB).
 // TMEM: Q dims [320,576) [0,128) (two bf16 per column, the MMA A operand),
@@ -44,8 +47,8 @@ constexpr int BN = 64;            // keys per block
 constexpr int NCH = DK / 64;      // 64-column chunks of a latent row
 constexpr int NCH_S = 5;          // chunks of Q kept in shared memory
 constexpr int NCH_T = NCH - NCH_S;  // chunks of Q kept in TMEM
-constexpr int NTHREADS = 192;
-constexpr int WARP_TMA = 4, WARP_MMA = 5;
+constexpr int NTHREADS = 224;
+constexpr int WARP_TMA = 4, WARP_MMA = 5, WARP_PV = 6;
 constexpr uint32_t QCH_BYTES = H * 64 * 2;   // 16 KB
 constexpr uint32_t KCH_BYTES = BN * 64 * 2;  // 8 KB
 constexpr uint32_t KBLK_BYTES = NCH * KCH_BYTES;  // 72 KB
@@ -114,7 +117,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     mbar_init(smem_u32(&sh.qt_ready), 4);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh.k_full[i]), 1);
-      mbar_init(smem_u32(&sh.k_empty[i]), 1);
+      mbar_init(smem_u32(&sh.k_empty[i]), 2);  // Q.K^T commit + P.V commit (or skip)
       mbar_init(smem_u32(&sh.s_full[i]), 1);
       mbar_init(smem_u32(&sh.s_free[i]), 1);
       mbar_init(smem_u32(&sh.p_full[i]), 4);
@@ -167,19 +170,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       }
     }
   } else if (warp == WARP_MMA) {
-    // ---------------------------------------------------------------- MMA --
+    // -------------------------------------------------------- Q.K^T issuer --
     if (lane == 0) {
       bool ok = mbar_wait(smem_u32(&sh.q_full), 0, abort, a.err, kErrTimeout) &&
                 mbar_wait(smem_u32(&sh.qt_ready), 0, abort, a.err, kErrTimeout);
       fence_after_sync();
-      int kc = 0;
-      auto issue_qk = [&](int j) -> bool {
+      for (int j = 0; ok && j < nb; ++j) {
         const int s = j & 1;
-        if (!mbar_wait(smem_u32(&sh.k_full[s]), (j >> 1) & 1, abort, a.err, kErrTimeout))
-          return false;
+        if (!mbar_wait(smem_u32(&sh.k_full[s]), (j >> 1) & 1, abort, a.err, kErrTimeout)) break;
         if (j >= 2 && !mbar_wait(smem_u32(&sh.s_free[s]), ((j >> 1) - 1) & 1, abort, a.err,
                                  kErrTimeout))
-          return false;
+          break;
         fence_after_sync();
         const uint32_t kt = base + SMEM_K + s * KBLK_BYTES;
         const uint32_t d = tmem + TMEM_S + s * BN;
@@ -198,32 +199,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
         mma_commit(smem_u32(&sh.s_full[s]));
-        return true;
-      };
-      if (ok) ok = issue_qk(0);
-      for (int i = 0; ok && i < nb; ++i) {
-        if (i + 1 < nb && !issue_qk(i + 1)) break;
+        mma_commit(smem_u32(&sh.k_empty[s]));  // this block's Q.K^T has read the slot
+      }
+    }
+  } else if (warp == WARP_PV) {
+    // ---------------------------------------------------------- P.V issuer --
+    if (lane == 0) {
+      int kc = 0;
+      for (int i = 0; i < nb && !*abort; ++i) {
         if (!mbar_wait(smem_u32(&sh.dec_full[i % NDEC]), (i / NDEC) & 1, abort, a.err,
                        kErrTimeout))
           break;
         const int s = i & 1;
-        if (sh.dec[i % NDEC]) {
-          if (!mbar_wait(smem_u32(&sh.p_full[kc & 1]), (kc >> 1) & 1, abort, a.err, kErrTimeout))
-            break;
-          fence_after_sync();
-          // O_half += P (TMEM, 64 keys = 32 columns) x V_half (MN-major: keys are the
-          // 128-byte rows of chunks 4*half..4*half+3, 8 KB apart).
-          const uint32_t vt = base + SMEM_K + s * KBLK_BYTES + half * 4 * KCH_BYTES;
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_bf16_ts(tmem + TMEM_O, tmem + TMEM_S + s * BN + kk * 8,
-                        smem_desc_sw128(vt + kk * 2048, KCH_BYTES, 1024), IDESC_PV,
-                        (kc > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(smem_u32(&sh.s_free[s]));
-          mma_commit(smem_u32(&sh.pv_done[kc & 1]));
-          ++kc;
+        if (!sh.dec[i % NDEC]) {
+          mbar_arrive(smem_u32(&sh.k_empty[s]));  // skipped: no value read
+          continue;
         }
-        mma_commit(smem_u32(&sh.k_empty[s]));  // Q.K^T (and P.V) of block i read the slot
+        if (!mbar_wait(smem_u32(&sh.p_full[kc & 1]), (kc >> 1) & 1, abort, a.err, kErrTimeout))
+          break;
+        fence_after_sync();
+        // O_half += P (TMEM, 64 keys = 32 columns) x V_half (MN-major: keys are the
+        // 128-byte rows of chunks 4*half..4*half+3, 8 KB apart).
+        const uint32_t vt = base + SMEM_K + s * KBLK_BYTES + half * 4 * KCH_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_bf16_ts(tmem + TMEM_O, tmem + TMEM_S + s * BN + kk * 8,
+                      smem_desc_sw128(vt + kk * 2048, KCH_BYTES, 1024), IDESC_PV,
+                      (kc > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&sh.s_free[s]));
+        mma_commit(smem_u32(&sh.pv_done[kc & 1]));
+        mma_commit(smem_u32(&sh.k_empty[s]));
+        ++kc;
       }
     }
   } else {
@@ -430,6 +436,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
   }
 
+  __syncwarp();
   fence_before_sync();
   __syncthreads();
   if (warp == WARP_MMA) {
