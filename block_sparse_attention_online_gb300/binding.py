@@ -11,6 +11,7 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
 import torch
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build",
@@ -22,7 +23,10 @@ ATTN_BF16, ATTN_F32 = 0, 1
 
 #: Every symbol include/attn_skip.h declares.
 EXPORTED = ("attn_skip_prefill", "attn_skip_decode", "attn_skip_decode_combine",
-            "attn_skip_last_device_error", "attn_skip_status_string")
+            "attn_skip_prefill_margins", "attn_skip_decode_margins", "attn_skip_sparsity_at",
+            "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
+            "attn_skip_lambda_for_target", "attn_skip_last_device_error",
+            "attn_skip_status_string")
 
 
 class AttnSkipError(RuntimeError):
@@ -49,10 +53,20 @@ def load() -> ctypes.CDLL:
     lib.attn_skip_decode.argtypes = [P, P, P, i, i, i, i, i, i, i, i64, i64, f, d, i, i, P, P, P,
                                      P]
     lib.attn_skip_decode_combine.argtypes = [P, P, i, i, i, i, i, P, P, P]
+    lib.attn_skip_prefill_margins.argtypes = [P, P, i, i, i, i, i, i, f, i, i, i, P, P]
+    lib.attn_skip_decode_margins.argtypes = [P, P, i, i, i, i, i, i, i64, f, i, i, P, P]
+    lib.attn_skip_sparsity_at.argtypes = [P, i64, d]
+    lib.attn_skip_sparsity_at.restype = d
+    lib.attn_skip_lambda_for_sparsity.argtypes = [P, i64, d, P]
+    lib.attn_skip_fit_lambda_model.argtypes = [P, P, P, i, P, P]
+    lib.attn_skip_lambda_for_target.argtypes = [d, d, d, d]
+    lib.attn_skip_lambda_for_target.restype = d
     lib.attn_skip_last_device_error.argtypes = [P]
     lib.attn_skip_status_string.argtypes = [i]
     lib.attn_skip_status_string.restype = ctypes.c_char_p
     for fn in ("attn_skip_prefill", "attn_skip_decode", "attn_skip_decode_combine",
+               "attn_skip_prefill_margins", "attn_skip_decode_margins",
+               "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
                "attn_skip_last_device_error"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
@@ -175,6 +189,94 @@ def attn_skip_decode_combine(o_part, lse_part, out_dtype=torch.bfloat16, out=Non
                                          _stream(stream, o_part.device))
     _check("attn_skip_decode_combine", st)
     return o, lse
+
+
+def prefill_margin_shape(B, Hq, T, Br, Bc):
+    return (B, Hq, -(-T // Br), -(-T // Bc))
+
+
+def decode_margin_shape(B, Hkv, L, Bc, n_splits):
+    n_b = -(-L // Bc)
+    return (B, Hkv, n_splits, -(-n_b // n_splits))
+
+
+def attn_skip_prefill_margins(q, k, Br=128, Bc=128, causal=True, scale=0.0, out=None,
+                              stream=None):
+    """Statistics pass of the prefill kernel: fp32 ``margin`` [B,Hq,n_t,n_b]
+    (NaN = not traversed) on the inputs' device."""
+    _cuda_contig(q, k)
+    B, Hq, T, dk = q.shape
+    Hkv = k.shape[1]
+    margin = out if out is not None else torch.empty(
+        prefill_margin_shape(B, Hq, T, Br, Bc), dtype=torch.float32, device=q.device)
+    st = load().attn_skip_prefill_margins(_ptr(q), _ptr(k), _dtype_code(q), B, Hq, Hkv, T, dk,
+                                          float(scale), Br, Bc, int(bool(causal)), _ptr(margin),
+                                          _stream(stream, q.device))
+    _check("attn_skip_prefill_margins", st)
+    return margin
+
+
+def attn_skip_decode_margins(q, k, Bc=128, n_splits=8, scale=0.0, out=None, stream=None):
+    """Statistics pass of the decode kernels: fp32 ``margin``
+    [B,Hkv,n_splits,bps] (NaN past a split's last block)."""
+    _cuda_contig(q, k)
+    B, Hq, dk = q.shape
+    _, Hkv, L, kstride = k.shape
+    margin = out if out is not None else torch.empty(
+        decode_margin_shape(B, Hkv, L, Bc, n_splits), dtype=torch.float32, device=q.device)
+    st = load().attn_skip_decode_margins(_ptr(q), _ptr(k), _dtype_code(q), B, Hq, Hkv, L, dk,
+                                         kstride, float(scale), Bc, n_splits, _ptr(margin),
+                                         _stream(stream, q.device))
+    _check("attn_skip_decode_margins", st)
+    return margin
+
+
+def _host_f32(margin):
+    """A contiguous host fp32 copy of ``margin`` (torch tensor or numpy array)."""
+    if isinstance(margin, torch.Tensor):
+        m = margin.detach().to("cpu", torch.float32).contiguous()
+    else:
+        m = torch.from_numpy(np.ascontiguousarray(margin, dtype=np.float32))
+    return m, ctypes.c_void_p(m.data_ptr()), m.numel()
+
+
+def attn_skip_sparsity_at(margin, lam):
+    """Fraction of the traversed blocks that ``lam`` skips (host computation)."""
+    m, p, n = _host_f32(margin)
+    r = load().attn_skip_sparsity_at(p, n, float(lam))
+    if r < 0:
+        raise AttnSkipError("attn_skip_sparsity_at", ATTN_EINVAL)
+    return r
+
+
+def attn_skip_lambda_for_sparsity(margin, target):
+    """A lambda in [0, 1) that skips the fraction ``target`` of the traversed
+    blocks of ``margin`` (host computation)."""
+    m, p, n = _host_f32(margin)
+    out = ctypes.c_double()
+    st = load().attn_skip_lambda_for_sparsity(p, n, float(target), ctypes.byref(out))
+    _check("attn_skip_lambda_for_sparsity", st)
+    return out.value
+
+
+def attn_skip_fit_lambda_model(lengths, sparsities, lambdas):
+    """Least-squares ``(alpha, beta)`` of lambda * L = alpha * exp(beta * s)."""
+    n = len(lengths)
+    if len(sparsities) != n or len(lambdas) != n:
+        raise ValueError("lengths, sparsities and lambdas must have equal length")
+    arr = ctypes.c_double * n
+    a_, b_ = ctypes.c_double(), ctypes.c_double()
+    st = load().attn_skip_fit_lambda_model(arr(*map(float, lengths)), arr(*map(float, sparsities)),
+                                           arr(*map(float, lambdas)), n, ctypes.byref(a_),
+                                           ctypes.byref(b_))
+    _check("attn_skip_fit_lambda_model", st)
+    return a_.value, b_.value
+
+
+def attn_skip_lambda_for_target(alpha, beta, sparsity, L):
+    """lambda = alpha * exp(beta * S) / L, capped below 1."""
+    return load().attn_skip_lambda_for_target(float(alpha), float(beta), float(sparsity),
+                                              float(L))
 
 
 def attn_skip_last_device_error(stream=None, device=None):

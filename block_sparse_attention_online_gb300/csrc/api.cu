@@ -1,8 +1,9 @@
 // C-ABI entry points: host-side validation, the log-domain threshold, the
-// device error word, and dispatch to the kernels.  No entry point allocates
-// device memory.
+// device error word, dispatch to the kernels, and the host-side threshold
+// calibration helpers.  No entry point allocates device memory.
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "../../include/attn_skip.h"
 #include "internal.h"
@@ -50,24 +51,26 @@ attn_status from_cuda(cudaError_t e) {
 
 using namespace attn_skip;
 
-extern "C" attn_status attn_skip_prefill(const void *q, const void *k, const void *v,
-                                         attn_dtype dt, int B, int Hq, int Hkv, int T, int dk,
-                                         int dv, float scale, double lambda, int Br, int Bc,
-                                         int causal, void *o, float *lse, uint32_t *skip_bits,
-                                         void *stream) {
-  if (!q || !k || !v || !o || !lse || !skip_bits) return ATTN_EINVAL;
+namespace attn_skip {
+namespace {
+
+// Shared by attn_skip_prefill and attn_skip_prefill_margins: validation of
+// the common arguments, the argument block, and dispatch.  `o`, `lse`,
+// `bits` are null in statistics mode.
+attn_status prefill_common(PrefillArgs &a, const void *q, const void *k, const void *v,
+                           attn_dtype dt, int B, int Hq, int Hkv, int T, int dk, int dv,
+                           float scale, double lambda, int Br, int Bc, int causal,
+                           cudaStream_t s) {
+  if (!q || !k || !v) return ATTN_EINVAL;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || dk <= 0 || dv <= 0 || Br <= 0 || Bc <= 0)
     return ATTN_EINVAL;
   if (Hq % Hkv != 0 || !lambda_ok(lambda) || !(scale == scale)) return ATTN_EINVAL;
   if (dt != ATTN_BF16 && dt != ATTN_F32) return ATTN_EINVAL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
-      !aligned16(skip_bits))
-    return ATTN_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return ATTN_EINVAL;
   const long n_t = (T + (long)Br - 1) / Br, n_b = (T + (long)Bc - 1) / Bc;
-  if ((long)B * Hq * n_t > 0x7fffffffL) return ATTN_EUNSUPPORTED;
-
-  PrefillArgs a{};
-  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse; a.bits = skip_bits;
+  if ((long)B * Hq * n_t > 0x7fffffffL || (long)B * Hq * n_t * n_b > 0x7fffffffffffL)
+    return ATTN_EUNSUPPORTED;
+  a.q = q; a.k = k; a.v = v;
   a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.T = T; a.dk = dk; a.dv = dv; a.Br = Br; a.Bc = Bc;
   a.causal = causal ? 1 : 0;
   a.n_t = (int)n_t; a.n_b = (int)n_b; a.words = (int)((n_b + 31) / 32);
@@ -75,8 +78,6 @@ extern "C" attn_status attn_skip_prefill(const void *q, const void *k, const voi
   a.ln_lambda = ln_lambda(lambda);
   cudaError_t e = error_word(&a.err);
   if (e != cudaSuccess) return from_cuda(e);
-  cudaStream_t s = (cudaStream_t)stream;
-
   if (dt == ATTN_F32) {
     if (dk != dv || (dk != 32 && dk != 64) || (Br != 64 && Br != 128) || (Bc != 64 && Bc != 128))
       return ATTN_EUNSUPPORTED;
@@ -88,27 +89,22 @@ extern "C" attn_status attn_skip_prefill(const void *q, const void *k, const voi
   return from_cuda(e);
 }
 
-extern "C" attn_status attn_skip_decode(const void *q, const void *k, const void *v,
-                                        attn_dtype dt, int B, int Hq, int Hkv, int L, int dk,
-                                        int dv, int64_t k_row_stride, int64_t v_row_stride,
-                                        float scale, double lambda, int Bc, int n_splits,
-                                        float *o_part, float *lse_part, uint32_t *skip_bits,
-                                        void *stream) {
-  if (!q || !k || !v || !o_part || !lse_part || !skip_bits) return ATTN_EINVAL;
+// Shared by attn_skip_decode and attn_skip_decode_margins.
+attn_status decode_common(DecodeArgs &a, const void *q, const void *k, const void *v,
+                          attn_dtype dt, int B, int Hq, int Hkv, int L, int dk, int dv,
+                          int64_t k_row_stride, int64_t v_row_stride, float scale,
+                          double lambda, int Bc, int n_splits, cudaStream_t s) {
+  if (!q || !k || !v) return ATTN_EINVAL;
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || L <= 0 || dk <= 0 || dv <= 0 || Bc <= 0 || n_splits <= 0)
     return ATTN_EINVAL;
   if (Hq % Hkv != 0 || !lambda_ok(lambda) || !(scale == scale)) return ATTN_EINVAL;
   if (k_row_stride < dk || v_row_stride < dv) return ATTN_EINVAL;
   if (dt != ATTN_BF16 && dt != ATTN_F32) return ATTN_EINVAL;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o_part) ||
-      !aligned16(lse_part) || !aligned16(skip_bits))
-    return ATTN_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v)) return ATTN_EINVAL;
   const int G = Hq / Hkv;
   const long n_b = (L + (long)Bc - 1) / Bc;
   if ((long)B * Hkv * n_splits > 0x7fffffffL) return ATTN_EUNSUPPORTED;
-
-  DecodeArgs a{};
-  a.q = q; a.k = k; a.v = v; a.o_part = o_part; a.lse_part = lse_part; a.bits = skip_bits;
+  a.q = q; a.k = k; a.v = v;
   a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.L = L; a.dk = dk; a.dv = dv; a.Bc = Bc;
   a.n_splits = n_splits; a.k_row_stride = k_row_stride; a.v_row_stride = v_row_stride;
   a.n_b = (int)n_b;
@@ -118,8 +114,6 @@ extern "C" attn_status attn_skip_decode(const void *q, const void *k, const void
   a.ln_lambda = ln_lambda(lambda);
   cudaError_t e = error_word(&a.err);
   if (e != cudaSuccess) return from_cuda(e);
-  cudaStream_t s = (cudaStream_t)stream;
-
   if (dt == ATTN_BF16 && dk == 128 && dv == 128 && Bc == 128 && k_row_stride == 128 &&
       v_row_stride == 128 && (G == 1 || G == 2 || G == 4 || G == 8))
     return from_cuda(launch_decode_bf16(a, s));
@@ -128,6 +122,64 @@ extern "C" attn_status attn_skip_decode(const void *q, const void *k, const void
       v_row_stride == 576 && Bc == 64 && Hkv == 1 && Hq == 128)
     return from_cuda(launch_mla_decode(a, s));
   return ATTN_EUNSUPPORTED;
+}
+
+}  // namespace
+}  // namespace attn_skip
+
+extern "C" attn_status attn_skip_prefill(const void *q, const void *k, const void *v,
+                                         attn_dtype dt, int B, int Hq, int Hkv, int T, int dk,
+                                         int dv, float scale, double lambda, int Br, int Bc,
+                                         int causal, void *o, float *lse, uint32_t *skip_bits,
+                                         void *stream) {
+  if (!o || !lse || !skip_bits) return ATTN_EINVAL;
+  if (!aligned16(o) || !aligned16(lse) || !aligned16(skip_bits)) return ATTN_EINVAL;
+  PrefillArgs a{};
+  a.o = o; a.lse = lse; a.bits = skip_bits;
+  return prefill_common(a, q, k, v, dt, B, Hq, Hkv, T, dk, dv, scale, lambda, Br, Bc, causal,
+                        (cudaStream_t)stream);
+}
+
+extern "C" attn_status attn_skip_prefill_margins(const void *q, const void *k, attn_dtype dt,
+                                                 int B, int Hq, int Hkv, int T, int dk,
+                                                 float scale, int Br, int Bc, int causal,
+                                                 float *margin, void *stream) {
+  if (!margin || !aligned16(margin)) return ATTN_EINVAL;
+  PrefillArgs a{};
+  a.margin = margin;
+  a.stats_only = 1;
+  // No value is read in statistics mode; the key tensor stands in for it.
+  return prefill_common(a, q, k, k, dt, B, Hq, Hkv, T, dk, dk, scale, 0.0, Br, Bc, causal,
+                        (cudaStream_t)stream);
+}
+
+extern "C" attn_status attn_skip_decode(const void *q, const void *k, const void *v,
+                                        attn_dtype dt, int B, int Hq, int Hkv, int L, int dk,
+                                        int dv, int64_t k_row_stride, int64_t v_row_stride,
+                                        float scale, double lambda, int Bc, int n_splits,
+                                        float *o_part, float *lse_part, uint32_t *skip_bits,
+                                        void *stream) {
+  if (!o_part || !lse_part || !skip_bits) return ATTN_EINVAL;
+  if (!aligned16(o_part) || !aligned16(lse_part) || !aligned16(skip_bits)) return ATTN_EINVAL;
+  DecodeArgs a{};
+  a.o_part = o_part; a.lse_part = lse_part; a.bits = skip_bits;
+  return decode_common(a, q, k, v, dt, B, Hq, Hkv, L, dk, dv, k_row_stride, v_row_stride, scale,
+                       lambda, Bc, n_splits, (cudaStream_t)stream);
+}
+
+extern "C" attn_status attn_skip_decode_margins(const void *q, const void *k, attn_dtype dt,
+                                                int B, int Hq, int Hkv, int L, int dk,
+                                                int64_t k_row_stride, float scale, int Bc,
+                                                int n_splits, float *margin, void *stream) {
+  if (!margin || !aligned16(margin)) return ATTN_EINVAL;
+  DecodeArgs a{};
+  a.margin = margin;
+  a.stats_only = 1;
+  // The value view is never read in statistics mode: the MLA layout (values =
+  // the first 512 latent columns) or the key tensor itself.
+  const int dv = dk == 576 ? 512 : dk;
+  return decode_common(a, q, k, k, dt, B, Hq, Hkv, L, dk, dv, k_row_stride, k_row_stride, scale,
+                       0.0, Bc, n_splits, (cudaStream_t)stream);
 }
 
 extern "C" attn_status attn_skip_decode_combine(const float *o_part, const float *lse_part, int B,
@@ -157,6 +209,89 @@ extern "C" attn_status attn_skip_last_device_error(void *stream) {
     if (e != cudaSuccess) return from_cuda(e);
     return (word & kErrTimeout) ? ATTN_ETIMEOUT : ATTN_ECUDA;
   }
+  return ATTN_OK;
+}
+
+namespace attn_skip {
+namespace {
+int cmp_float(const void *x, const void *y) {
+  const float a = *(const float *)x, b = *(const float *)y;
+  return (a > b) - (a < b);
+}
+}  // namespace
+}  // namespace attn_skip
+
+extern "C" double attn_skip_sparsity_at(const float *margin, int64_t n, double lambda) {
+  if (!margin || n < 0 || !(lambda >= 0.0 && lambda < 1.0)) return -1.0;
+  const double ln_l = lambda > 0.0 ? log(lambda) : -INFINITY;
+  int64_t trav = 0, skipped = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const float x = margin[i];
+    if (x != x) continue;
+    ++trav;
+    if (lambda > 0.0 && (double)x < ln_l) ++skipped;
+  }
+  return trav ? (double)skipped / (double)trav : 0.0;
+}
+
+extern "C" attn_status attn_skip_lambda_for_sparsity(const float *margin, int64_t n,
+                                                     double target, double *lambda) {
+  if (!margin || !lambda || n <= 0 || !(target >= 0.0 && target <= 1.0)) return ATTN_EINVAL;
+  // Traversed entries (NaN = not traversed), ascending; -inf sorts first.
+  float *v = (float *)malloc(sizeof(float) * (size_t)n);
+  if (!v) return ATTN_EINVAL;
+  int64_t m = 0, neg = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    const float x = margin[i];
+    if (x != x) continue;
+    v[m++] = x;
+    if (x < 0.f) ++neg;  // a statistic of 0 (a row found a new max) is never skipped
+  }
+  if (m == 0) {
+    free(v);
+    return ATTN_EINVAL;
+  }
+  qsort(v, (size_t)m, sizeof(float), cmp_float);
+  int64_t k = (int64_t)llround(target * (double)m);  // entries to skip
+  if (k > neg) k = neg;                               // the most any lambda < 1 skips
+  double ln_l;
+  if (k == 0) {
+    *lambda = 0.0;
+    free(v);
+    return ATTN_OK;
+  }
+  const double lo = v[k - 1];                   // largest skipped statistic
+  const double hi = k < m ? (double)v[k] : 0.0;  // smallest kept one
+  if (lo == -INFINITY) ln_l = hi == -INFINITY ? -1e30 : hi - 1.0;
+  else ln_l = 0.5 * (lo + (hi < 0.0 ? hi : 0.0));
+  free(v);
+  *lambda = exp(ln_l);
+  if (!(*lambda < 1.0)) *lambda = nextafter(1.0, 0.0);
+  return ATTN_OK;
+}
+
+extern "C" double attn_skip_lambda_for_target(double alpha, double beta, double sparsity,
+                                              double L) {
+  if (!(alpha > 0.0) || !(L > 0.0) || !(sparsity == sparsity) || !(beta == beta)) return 0.0;
+  const double lambda = alpha * exp(beta * sparsity) / L;
+  return lambda < 1.0 ? lambda : nextafter(1.0, 0.0);
+}
+
+extern "C" attn_status attn_skip_fit_lambda_model(const double *L, const double *sparsity,
+                                                  const double *lambda, int n, double *alpha,
+                                                  double *beta) {
+  if (!L || !sparsity || !lambda || !alpha || !beta || n < 2) return ATTN_EINVAL;
+  // Least squares on ln(lambda * L) = ln(alpha) + beta * sparsity.
+  double sx = 0, sy = 0, sxx = 0, sxy = 0;
+  for (int i = 0; i < n; ++i) {
+    if (!(L[i] > 0.0) || !(lambda[i] > 0.0) || !(sparsity[i] == sparsity[i])) return ATTN_EINVAL;
+    const double x = sparsity[i], y = log(lambda[i] * L[i]);
+    sx += x; sy += y; sxx += x * x; sxy += x * y;
+  }
+  const double den = n * sxx - sx * sx;
+  if (!(fabs(den) > 1e-300)) return ATTN_EINVAL;  // all sparsities equal
+  *beta = (n * sxy - sx * sy) / den;
+  *alpha = exp((sy - *beta * sx) / n);
   return ATTN_OK;
 }
 

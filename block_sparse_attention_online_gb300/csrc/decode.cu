@@ -174,10 +174,13 @@ __global__ void __launch_bounds__(NT, 1)
   const int j1 = (int)((long)(sp + 1) * a.n_b / a.n_splits);
   const int nb = j1 - j0;
   const int zkv = b * a.Hkv + hk;
-  uint32_t *bits = a.bits + (size_t)unit * a.words;
+  uint32_t *bits = a.bits ? a.bits + (size_t)unit * a.words : nullptr;
   volatile int *abort = &sh.abort;
 
   if (nb == 0) {  // empty split: no key, zero weight in the merge
+    if (a.margin)
+      for (int j = tid; j < a.bps; j += NT) a.margin[(size_t)unit * a.bps + j] = NAN;
+    if (a.stats_only) return;
     for (int idx = tid; idx < G * D; idx += NT) {
       const size_t row = (size_t)(b * a.Hq + hk * G + idx / D) * a.n_splits + sp;
       a.o_part[row * D + idx % D] = 0.f;
@@ -379,7 +382,15 @@ __global__ void __launch_bounds__(NT, 1)
       // With c < 0, "rowmax - m_new < c" is "rowmax - m_old < c" (a block
       // that raises the max fails both).  Every head must vote skip.
       const float diff = (mt == -INFINITY) ? -INFINITY : pm2 - m2;
-      const bool skip = __all_sync(0xffffffffu, !head || diff < c2);
+      const bool skip = a.stats_only || __all_sync(0xffffffffu, !head || diff < c2);
+      if (a.margin) {
+        // The block statistic: max over the heads of rowmax - m_new, where
+        // rowmax - m_new = min(rowmax - m_old, 0) (log2 units).
+        float st = (head && mt != -INFINITY) ? fminf(diff, 0.f) : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) st = fmaxf(st, __shfl_xor_sync(0xffffffffu, st, o));
+        if (lane == 0) a.margin[(size_t)unit * a.bps + j] = st * kLn2;
+      }
       if (lane == 0) {
         // On a timeout the abort flag is raised and every later wait fails.
         if (j < NDEC || mbar_wait(smem_u32(&sh.dec_empty[j % NDEC]), ((j / NDEC) - 1) & 1,
@@ -388,14 +399,16 @@ __global__ void __launch_bounds__(NT, 1)
           mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
         }
         if (skip) word |= 1u << (j & 31);
-        if ((j & 31) == 31 || j == nb - 1) {
+        if (!a.stats_only && ((j & 31) == 31 || j == nb - 1)) {
           bits[j >> 5] = word;
           word = 0;
         }
       }
-      if (skip) continue;
+      // The running max advances on every block (a skipped block leaves it
+      // unchanged unless the statistics mode forced the skip).
       const float mnew = fmaxf(m2, pm2);
       m2 = mnew;
+      if (skip) continue;
       bool rescale = false;
       float alpha = 1.f;
       if (mref == -INFINITY) {
@@ -458,12 +471,16 @@ __global__ void __launch_bounds__(NT, 1)
 
     // ---- epilogue: O_s = O / l and LSE_s = ref + ln l per head ---------------
     if (lane == 0) {
-      for (int w = ((nb - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
+      if (!a.stats_only)
+        for (int w = ((nb - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
+      if (a.margin)
+        for (int j = nb; j < a.bps; ++j) a.margin[(size_t)unit * a.bps + j] = NAN;
     }
+    // (Statistics mode: every block was treated as skipped, kc == 0, no output.)
     if (ok && kc > 0)
       ok = mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort, a.err,
                           kErrTimeout);
-    if (ok) {
+    if (ok && !a.stats_only) {
       fence_after_sync();
       const float inv = 1.f / l;
       const size_t row = (size_t)(b * a.Hq + hk * G + lane) * a.n_splits + sp;

@@ -21,6 +21,11 @@ struct PrefillArgs {
   float scale;          // natural-log scale applied to q.k
   float ln_lambda;      // -inf when lambda == 0
   unsigned *err;        // device error word
+  // Statistics mode: margin [B,Hq,n_t,n_b] receives each traversed block's
+  // statistic max_r(rowmax_r - m_new_r) (natural log; NaN = not traversed),
+  // every block is treated as skipped, and o, lse, bits are not written.
+  float *margin;
+  int stats_only;
 };
 
 struct DecodeArgs {
@@ -33,6 +38,11 @@ struct DecodeArgs {
   float scale;
   float ln_lambda;
   unsigned *err;
+  // Statistics mode: margin [B,Hkv,n_splits,bps] receives each block's
+  // statistic over the query heads of the KV head (NaN past a split's last
+  // block); every block is treated as skipped; o_part, lse_part, bits unused.
+  float *margin;
+  int stats_only;
 };
 
 struct CombineArgs {

@@ -74,6 +74,7 @@ struct Shared {
   uint64_t vote_full[2];
   int dec[NDEC];
   int vote[2][4];
+  float wstat[2][4];  // statistics mode: per warp, max over its heads of rowmax - m_new
   uint32_t tmem_base;
   int abort;
 };
@@ -97,10 +98,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int j0 = (int)((long)sp * a.n_b / a.n_splits);
   const int j1 = (int)((long)(sp + 1) * a.n_b / a.n_splits);
   const int nb = j1 - j0;
-  uint32_t *bits = a.bits + (size_t)us * a.words;
+  uint32_t *bits = a.bits ? a.bits + (size_t)us * a.words : nullptr;
   volatile int *abort = &sh.abort;
 
+  // Statistics mode: the half-0 CTA computes the statistics alone.
+  if (a.stats_only && half == 1) return;
   if (nb == 0) {  // empty split
+    if (a.margin)
+      for (int j = tid; j < a.bps; j += NTHREADS) a.margin[(size_t)us * a.bps + j] = NAN;
+    if (a.stats_only) return;
     for (int idx = tid; idx < H * DVH; idx += NTHREADS) {
       const int hh = idx / DVH, e = idx % DVH;
       const size_t row = (size_t)(b * a.Hq + hh) * a.n_splits + sp;
@@ -300,6 +306,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const unsigned all = __all_sync(0xffffffffu, vote);
       const int vb = j & 1;
       if (lane == 0) sh.vote[vb][warp] = (int)all;
+      if (a.margin) {  // the block statistic: max over the heads of rowmax - m_new
+        float st = diff;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) st = fmaxf(st, __shfl_xor_sync(0xffffffffu, st, o));
+        if (lane == 0) sh.wstat[vb][warp] = st;
+      }
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.vote_full[vb]));
@@ -308,7 +320,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ok = false;
         break;
       }
-      const bool skip = sh.vote[vb][0] && sh.vote[vb][1] && sh.vote[vb][2] && sh.vote[vb][3];
+      const bool skip =
+          a.stats_only || (sh.vote[vb][0] && sh.vote[vb][1] && sh.vote[vb][2] && sh.vote[vb][3]);
+      if (a.margin && tid == 0 && half == 0)
+        a.margin[(size_t)us * a.bps + j] =
+            fmaxf(fmaxf(sh.wstat[vb][0], sh.wstat[vb][1]), fmaxf(sh.wstat[vb][2], sh.wstat[vb][3])) *
+            kLn2;
       if (tid == 0) {
         if (skip) {
           fence_after_sync();
@@ -317,7 +334,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         sh.dec[j % NDEC] = skip ? 0 : 1;
         mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
-        if (half == 0) {
+        if (half == 0 && !a.stats_only) {
           if (skip) word |= 1u << (j & 31);
           if ((j & 31) == 31 || j == nb - 1) {
             bits[j >> 5] = word;
@@ -407,12 +424,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // ---- epilogue ------------------------------------------------------------
     if (tid == 0 && half == 0) {
-      for (int w = ((nb - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
+      if (!a.stats_only)
+        for (int w = ((nb - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
+      if (a.margin)
+        for (int j = nb; j < a.bps; ++j) a.margin[(size_t)us * a.bps + j] = NAN;
     }
+    // (Statistics mode: every block was treated as skipped, kc == 0, no output.)
     if (ok && kc > 0)
       ok = mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort,
                           a.err, kErrTimeout);
-    if (ok) {
+    if (ok && !a.stats_only) {
       fence_after_sync();
       const float inv = 1.f / l;
       const size_t row = (size_t)(b * a.Hq + r) * a.n_splits + sp;

@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(BR) prefill_f32_kernel(const PrefillArgs a) {
   float *Vs = Ks + BC * D;        // [BC][D]
   float *Ss = Vs + BC * D;        // [BR][BC + 1], one private row per thread
   __shared__ int warp_vote[BR / 32];
+  __shared__ float warp_stat[BR / 32];
 
   const int unit = blockIdx.x;
   const int t = unit % a.n_t;
@@ -44,7 +45,7 @@ __global__ void __launch_bounds__(BR) prefill_f32_kernel(const PrefillArgs a) {
   float m = -INFINITY, l = 0.f;
   const int last_row = min(a.T, (t + 1) * BR) - 1;
   const int jmax = a.causal ? last_row / BC : a.n_b - 1;
-  uint32_t *bits = a.bits + (size_t)unit * a.words;
+  uint32_t *bits = a.bits ? a.bits + (size_t)unit * a.words : nullptr;
   uint32_t word = 0;
   float *Sr = Ss + r * (BC + 1);
 
@@ -83,12 +84,25 @@ __global__ void __launch_bounds__(BR) prefill_f32_kernel(const PrefillArgs a) {
     const bool vote = !valid || (diff < a.ln_lambda);
     const unsigned all = __all_sync(0xffffffffu, vote);
     if (lane == 0) warp_vote[warp] = (int)all;
+    if (a.margin) {  // the block statistic: max over the tile's rows of rowmax - m_new
+      float st = valid ? diff : -INFINITY;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) st = fmaxf(st, __shfl_xor_sync(0xffffffffu, st, o));
+      if (lane == 0) warp_stat[warp] = st;
+    }
     __syncthreads();
     bool skip = true;
 #pragma unroll
     for (int w = 0; w < BR / 32; ++w) skip = skip && warp_vote[w];
+    if (a.margin && r == 0) {
+      float st = warp_stat[0];
+#pragma unroll
+      for (int w = 1; w < BR / 32; ++w) st = fmaxf(st, warp_stat[w]);
+      a.margin[(size_t)unit * a.n_b + j] = st;
+    }
+    if (a.stats_only) skip = true;
     if (skip) word |= 1u << (j & 31);
-    if (r == 0 && ((j & 31) == 31 || j == jmax)) {
+    if (!a.stats_only && r == 0 && ((j & 31) == 31 || j == jmax)) {
       bits[j >> 5] = word;
     }
     if ((j & 31) == 31) word = 0;
@@ -122,9 +136,16 @@ __global__ void __launch_bounds__(BR) prefill_f32_kernel(const PrefillArgs a) {
     }
     m = mnew;  // unchanged on a skipped block (its row max is below m)
   }
+  if (a.stats_only) {
+    if (r == 0)
+      for (int j = jmax + 1; j < a.n_b; ++j) a.margin[(size_t)unit * a.n_b + j] = NAN;
+    return;
+  }
   if (r == 0) {
     for (int w = (jmax >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
   }
+  if (a.margin && r == 0)
+    for (int j = jmax + 1; j < a.n_b; ++j) a.margin[(size_t)unit * a.n_b + j] = NAN;
   if (valid) {
     float *og = (float *)a.o + ((size_t)(b * a.Hq + h) * a.T + row) * D;
     const float inv = 1.f / l;

@@ -90,6 +90,7 @@ struct Shared {
   uint64_t l_full;
   int dec[NDEC];
   unsigned keepw[3];  // ring: bit w set when decider warp w votes "keep" for the block
+  float wstat[2][NQ];  // statistics mode: per decider warp, max over its rows of rowmax - m_new
   // [S buffer][row] running max after the buffer's block (log2 units), from
   // the deciders to the exponential warps.
   float mdec[NS][128];
@@ -184,6 +185,9 @@ __device__ __forceinline__ void chunk_exp(const uint32_t (&s)[32], uint64_t sl2x
   }
 }
 
+// STATS: the statistics mode (compiled separately so that the ordinary
+// kernel's decision loop carries none of its code).
+template <bool STATS>
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -393,7 +397,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const float c2 = a.ln_lambda * kLog2e;      // ln(lambda) in log2 units
       float m2 = -INFINITY;                       // running max (log2 units)
       uint32_t word = 0;
-      uint32_t *bits = a.bits + ((size_t)bh * a.n_t + t) * a.words;
+      uint32_t *bits = a.bits ? a.bits + ((size_t)bh * a.n_t + t) * a.words : nullptr;
       int sb = 0;
       for (int j = 0; j < nblk; ++j) {
         const int sbn = sb == NS - 1 ? 0 : sb + 1;
@@ -426,6 +430,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const float mnew = fmaxf(m2, pm2);
         sh.mdec[sb][r] = mnew;
         if (lane == 0 && !all) atomicOr(&sh.keepw[sb], 1u << warp);
+        if constexpr (STATS) {
+          // rowmax - m_new = min(rowmax - m_old, 0) (log2 units) over valid rows.
+          float st = (valid && mt != -INFINITY) ? fminf(diff, 0.f) : -INFINITY;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) st = fmaxf(st, __shfl_xor_sync(0xffffffffu, st, o));
+          if (lane == 0) sh.wstat[j & 1][warp] = st;
+        }
         fence_before_sync();  // this warp's reads of S_j are complete
         __syncwarp();
         const int vb = j & 1;
@@ -435,8 +446,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           ok = false;
           break;
         }
-        const bool skip = sh.keepw[sb] == 0u;
+        const bool skip = STATS || sh.keepw[sb] == 0u;
         m2 = mnew;
+        if (STATS && tid == 0) {
+          const float st = fmaxf(fmaxf(sh.wstat[j & 1][0], sh.wstat[j & 1][1]),
+                                 fmaxf(sh.wstat[j & 1][2], sh.wstat[j & 1][3]));
+          a.margin[((size_t)bh * a.n_t + t) * a.n_b + j] = st * kLn2;
+        }
         if (tid == 0) {
           // (A skipped block's S buffer is reused by the Q.K^T issuer as soon
           // as it reads this decision.)  The slot's previous decision (block
@@ -448,7 +464,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
           }
           if (skip) word |= 1u << (j & 31);
-          if ((j & 31) == 31 || j == nblk - 1) {
+          if (!STATS && ((j & 31) == 31 || j == nblk - 1)) {
             bits[j >> 5] = word;
             word = 0;
           }
@@ -456,7 +472,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         sb = sbn;
       }
       if (tid == 0) {
-        for (int w = ((nblk - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
+        if (!STATS)
+          for (int w = ((nblk - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
+        if (STATS)
+          for (int j = nblk; j < a.n_b; ++j) a.margin[((size_t)bh * a.n_t + t) * a.n_b + j] = NAN;
       }
     } else {
       // Per kept block: P_j = exp2(S_j - ref) as bf16 pairs into columns
@@ -545,7 +564,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     // ---- epilogue: deciders take O columns [0,64), exponential warps [64,128)
     if (ok) ok = mbar_wait_warp(smem_u32(&sh.l_full), 0, abort, a.err, kErrTimeout);
-    if (ok) {
+    if (ok && !STATS) {
       fence_after_sync();
       const float lrow = sh.lfin[r];
       const float inv = 1.f / lrow;
@@ -589,11 +608,12 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
       !make_map_bf16_3d(&mk, a.k, D, D, a.T, a.B * a.Hkv, BN) ||
       !make_map_bf16_3d(&mv, a.v, D, D, a.T, a.B * a.Hkv, BN))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  auto kernel = a.stats_only ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   const long units = (long)a.B * a.Hq * a.n_t;
-  prefill_tc_kernel<<<(unsigned)units, NTHREADS, SMEM_ALLOC, s>>>(mq, mk, mv, a);
+  kernel<<<(unsigned)units, NTHREADS, SMEM_ALLOC, s>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }
 

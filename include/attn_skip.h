@@ -106,7 +106,8 @@ attn_status attn_skip_prefill(const void *q, const void *k, const void *v, attn_
  *             bit p of split s is block floor(s*nb/n_splits) + p
  *
  * Kernels built: dt = ATTN_BF16, dk = dv = 128, Bc = 128, G in {1, 2, 4, 8},
- * k_row_stride = v_row_stride = 128 (CUDA-core memory-bound path); and the
+ * k_row_stride = v_row_stride = 128 (tcgen05 path with the G heads padded to
+ * the 128 MMA rows; memory bound; P rounded to bf16 for P.V); and the
  * absorbed-MLA shape dt = ATTN_BF16, Hkv = 1, Hq = 128, dk = 576, dv = 512,
  * v == k, k_row_stride = v_row_stride = 576, Bc = 64 (tcgen05 path, the 128
  * heads as one M = 128 tile; a skipped block saves its exponentials and its
@@ -129,6 +130,70 @@ attn_status attn_skip_decode(const void *q, const void *k, const void *v, attn_d
 attn_status attn_skip_decode_combine(const float *o_part, const float *lse_part, int B, int Hq,
                                      int n_splits, int dv, attn_dtype out_dt, void *o,
                                      float *lse, void *stream);
+
+/*
+ * Threshold calibration (section "校准算法：一次前向，一个指数模型", Algorithm 2):
+ * the block statistic that Eq. 5 compares with ln(lambda) does not depend on
+ * lambda (the running max advances on every traversed block, skipped or not),
+ * so one pass over the scores gives the sparsity for every candidate lambda.
+ *
+ * The two *_margins calls run the same kernels as attn_skip_prefill /
+ * attn_skip_decode in a statistics mode: every block is treated as skipped (no
+ * value load, no exponential, no P.V product) and, per traversed block,
+ *
+ *     margin = max over the unit's rows of (rowmax(S_ij) - m_new)   (natural log, <= 0)
+ *
+ * is written; the block is skipped at lambda iff margin < ln(lambda).  A unit
+ * is a prefill query tile (rows = its valid query rows) or a decode (b, KV
+ * head, split) (rows = its G query heads).  -inf: no row has a visible key in
+ * the block; NaN: block not traversed (causal blocks above the diagonal,
+ * positions past a split's last block).  No other output is written.
+ *
+ *  prefill: q, k as for attn_skip_prefill (no value tensor);
+ *           margin [B, Hq, ceil(T/Br), ceil(T/Bc)] fp32 (device)
+ *  decode:  q, k as for attn_skip_decode (no value tensor; dk = 576 selects
+ *           the absorbed-MLA shape with dv = 512);
+ *           margin [B, Hkv, n_splits, ceil(ceil(L/Bc)/n_splits)] fp32 (device)
+ *
+ * Same kernels built, same status codes as the corresponding calls.
+ */
+attn_status attn_skip_prefill_margins(const void *q, const void *k, attn_dtype dt, int B, int Hq,
+                                      int Hkv, int T, int dk, float scale, int Br, int Bc,
+                                      int causal, float *margin, void *stream);
+attn_status attn_skip_decode_margins(const void *q, const void *k, attn_dtype dt, int B, int Hq,
+                                     int Hkv, int L, int dk, int64_t k_row_stride, float scale,
+                                     int Bc, int n_splits, float *margin, void *stream);
+
+/*
+ * Host-side helpers (host memory, synchronous, no GPU work).
+ *
+ * attn_skip_sparsity_at: fraction of the n margins' traversed entries (NaN
+ * entries are ignored) that lambda skips, i.e. margin < ln(lambda); 0 for
+ * lambda = 0 and for an array with no traversed entry; -1 for invalid input.
+ *
+ * attn_skip_lambda_for_sparsity: a lambda in [0, 1) that skips the fraction
+ * `target` of the traversed entries: ln(lambda) is placed halfway between the
+ * largest skipped and the smallest kept statistic.  A statistic of 0 (some row
+ * found a new max in the block) is never skipped by any lambda < 1, so a target
+ * above the fraction of negative statistics returns the lambda that skips all
+ * of them.  ATTN_EINVAL for a null pointer, n <= 0, a target outside [0, 1]
+ * or no traversed entry.
+ *
+ * attn_skip_fit_lambda_model: least-squares fit of the section's exponential
+ * model lambda * L = alpha * exp(beta * s) to n >= 2 calibration points
+ * (L_i, s_i, lambda_i), on ln(lambda * L) = ln(alpha) + beta * s.  ATTN_EINVAL
+ * for null pointers, n < 2, a non-positive L or lambda, or all s equal.
+ *
+ * attn_skip_lambda_for_target: lambda = alpha * exp(beta * S) / L for a target
+ * sparsity S at context length L (the section's inference-time rule), capped
+ * below 1; 0 for alpha <= 0 or L <= 0.
+ */
+double attn_skip_sparsity_at(const float *margin, int64_t n, double lambda);
+attn_status attn_skip_lambda_for_sparsity(const float *margin, int64_t n, double target,
+                                          double *lambda);
+attn_status attn_skip_fit_lambda_model(const double *L, const double *sparsity,
+                                       const double *lambda, int n, double *alpha, double *beta);
+double attn_skip_lambda_for_target(double alpha, double beta, double sparsity, double L);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error

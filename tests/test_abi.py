@@ -72,6 +72,36 @@ def test_decode_rejects_invalid_arguments(lib, kw):
     assert _decode(lib, **kw) == bs.ATTN_EINVAL
 
 
+def _prefill_margins(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, dt=0, B=1, Hq=4, Hkv=2, T=256, dk=128, scale=0.0, Br=128, Bc=128,
+             causal=1, m=FAKE, stream=None)
+    a.update(kw)
+    return lib.attn_skip_prefill_margins(*a.values())
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=None), dict(k=None), dict(m=None), dict(m=ctypes.c_void_p(0x10008)), dict(B=0),
+    dict(Hq=3), dict(scale=float("nan")), dict(dt=5), dict(Bc=0),
+])
+def test_prefill_margins_rejects_invalid_arguments(lib, kw):
+    assert _prefill_margins(lib, **kw) == bs.ATTN_EINVAL
+
+
+def _decode_margins(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, dt=0, B=2, Hq=8, Hkv=2, L=1024, dk=128, ks=128, scale=0.0, Bc=128,
+             n=4, m=FAKE, stream=None)
+    a.update(kw)
+    return lib.attn_skip_decode_margins(*a.values())
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=None), dict(m=None), dict(n=0), dict(L=0), dict(Hq=6, Hkv=4), dict(ks=64),
+    dict(k=ctypes.c_void_p(0x10002)),
+])
+def test_decode_margins_rejects_invalid_arguments(lib, kw):
+    assert _decode_margins(lib, **kw) == bs.ATTN_EINVAL
+
+
 def test_combine_rejects_invalid_arguments(lib):
     f = lib.attn_skip_decode_combine
     assert f(None, FAKE, 1, 1, 1, 128, 0, FAKE, FAKE, None) == bs.ATTN_EINVAL
