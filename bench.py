@@ -28,6 +28,7 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
+import numpy as np  # noqa: E402
 import torch  # noqa: E402
 import torch.distributed as dist  # noqa: E402
 
@@ -253,6 +254,7 @@ def run_gpu(args, rank, world):
                                           / (dsweep[t]["ms_decode"] + dsweep[t]["ms_combine"]))
 
     msweep = mla_sweep(args, bs, dev, stream, flush, lam)
+    calib = calibration(args, bs, dev, stream, flush, dq, dk_, dv_, dqd, dkd, lp, ld, pbits)
 
     # ---- the timed region: K steps of the whole hot path at ~70 % ---------
     fp, fd = prefill(lp[TARGET]), decode(ld[TARGET])
@@ -335,6 +337,7 @@ def run_gpu(args, rank, world):
                             "traffic": ncu_traffic("decode_tc_kernel"),
                             "algorithmic_bytes": dec["bytes"]},
         "mla_decode": msweep,
+        "calibration": calib,
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,  # prefill, decode, merge per timed step
         "clocks": clk.summary(),
@@ -381,6 +384,65 @@ def mla_sweep(args, bs, dev, stream, flush, lam):
     out["workload"] = (f"B{M.B} Hq{M.Hq} latent dk{M.dk} dv{M.dv} L{M.L} Bc{M.Bc} "
                        f"splits{M.n_splits}; 'max' = largest sparsity any lambda < 1 reaches")
     return out
+
+
+def calibration(args, bs, dev, stream, flush, dq, dk_, dv_, dqd, dkd, lp, ld, pbits):
+    """One-pass threshold calibration on the bench's workloads: the statistics
+    pass of each kernel (no value load, exponential or P.V), the lambda it
+    gives for the ~70 % target, and the sparsity a prefill at that lambda
+    reaches; with --calibration-sweep, the exponential model
+    lambda * L = alpha * exp(beta * s) fitted over prefill lengths 4K-64K."""
+    P, D = PREFILL, DECODE
+    pm = torch.empty(bs.prefill_margin_shape(P.B, P.Hq, P.T, P.Br, P.Bc), dtype=torch.float32,
+                     device=dev)
+    dm = torch.empty(bs.decode_margin_shape(D.B, D.Hkv, D.L, D.Bc, D.n_splits),
+                     dtype=torch.float32, device=dev)
+    pms = statistics.mean(timed_launches(
+        lambda: bs.attn_skip_prefill_margins(dq, dk_, P.Br, P.Bc, True, out=pm),
+        args.warmup, args.steps, flush, stream))
+    dms = statistics.mean(timed_launches(
+        lambda: bs.attn_skip_decode_margins(dqd, dkd, D.Bc, D.n_splits, out=dm),
+        args.warmup, args.steps, flush, stream))
+    lam_p = bs.attn_skip_lambda_for_sparsity(pm, float(TARGET))
+    lam_d = bs.attn_skip_lambda_for_sparsity(dm, float(TARGET))
+    bits = bs.attn_skip_prefill(dq, dk_, dv_, lam_p, P.Br, P.Bc, True)[2]
+    trav = ~torch.isnan(pm.cpu())
+    got = float(bs.unpack_bits(bits, P.n_b)[trav].float().mean())
+    out = {"prefill_margins_ms": round(pms, 4), "decode_margins_ms": round(dms, 4),
+           "prefill": {"lambda_from_margins": lam_p, "lambda_oracle": lp[TARGET],
+                       "sparsity_reached": round(got, 4)},
+           "decode": {"lambda_from_margins": lam_d, "lambda_oracle": ld[TARGET],
+                      "sparsity_predicted": round(bs.attn_skip_sparsity_at(dm, lam_d), 4)}}
+    if args.calibration_sweep:
+        out["fit"] = calibration_fit(bs, dev)
+    return out
+
+
+def calibration_fit(bs, dev):
+    """Section "校准算法" on synthetic inputs: statistics at T = 4K..64K (the
+    16K prefill recipe at each length, 8/2 heads), points (lambda_j * L, s)
+    for a lambda grid, the least-squares alpha, beta, and the sparsity the
+    model's lambda = alpha * exp(beta * S) / L reaches at each length."""
+    lengths = [4096, 8192, 16384, 32768, 65536]
+    margins = {}
+    for T in lengths:
+        cfg = PREFILL.with_(T=T, Hq=8, Hkv=2, seed=4000 + T // 4096)
+        q, k, _ = W.prefill_inputs(cfg)
+        margins[T] = bs.attn_skip_prefill_margins(q.to(dev), k.to(dev), cfg.Br, cfg.Bc,
+                                                  True).cpu()
+    grid = [math.exp(x) for x in np.linspace(-30.0, -0.05, 60)]
+    Ls, ss, lams = [], [], []
+    for T in lengths:
+        for lam in grid:
+            s_ = bs.attn_skip_sparsity_at(margins[T], lam)
+            if 0.2 <= s_ <= 0.9:
+                Ls.append(T); ss.append(s_); lams.append(lam)
+    alpha, beta = bs.attn_skip_fit_lambda_model(Ls, ss, lams)
+    check = {}
+    for S in (0.5, 0.7):
+        check[str(S)] = {str(T): round(bs.attn_skip_sparsity_at(
+            margins[T], bs.attn_skip_lambda_for_target(alpha, beta, S, T)), 4) for T in lengths}
+    return {"alpha": alpha, "beta": beta, "points": len(Ls), "reached": check}
 
 
 def max_over_ranks(x, world):
@@ -530,6 +592,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--calibration-sweep", action="store_true",
+                    help="also fit the threshold model over prefill lengths 4K-64K")
     ap.add_argument("--profile", choices=("prefill", "decode"),
                     help="only warm up and launch one kernel (for ncu captures)")
     args = ap.parse_args(argv)
