@@ -25,8 +25,8 @@ ATTN_BF16, ATTN_F32 = 0, 1
 EXPORTED = ("attn_skip_prefill", "attn_skip_decode", "attn_skip_decode_combine",
             "attn_skip_prefill_margins", "attn_skip_decode_margins", "attn_skip_sparsity_at",
             "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
-            "attn_skip_lambda_for_target", "attn_skip_last_device_error",
-            "attn_skip_status_string")
+            "attn_skip_lambda_for_target", "attn_skip_selftest_wait_timeout",
+            "attn_skip_last_device_error", "attn_skip_status_string")
 
 
 class AttnSkipError(RuntimeError):
@@ -62,12 +62,13 @@ def load() -> ctypes.CDLL:
     lib.attn_skip_lambda_for_target.argtypes = [d, d, d, d]
     lib.attn_skip_lambda_for_target.restype = d
     lib.attn_skip_last_device_error.argtypes = [P]
+    lib.attn_skip_selftest_wait_timeout.argtypes = [P]
     lib.attn_skip_status_string.argtypes = [i]
     lib.attn_skip_status_string.restype = ctypes.c_char_p
     for fn in ("attn_skip_prefill", "attn_skip_decode", "attn_skip_decode_combine",
                "attn_skip_prefill_margins", "attn_skip_decode_margins",
                "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
-               "attn_skip_last_device_error"):
+               "attn_skip_selftest_wait_timeout", "attn_skip_last_device_error"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -277,6 +278,12 @@ def attn_skip_lambda_for_target(alpha, beta, sparsity, L):
     """lambda = alpha * exp(beta * S) / L, capped below 1."""
     return load().attn_skip_lambda_for_target(float(alpha), float(beta), float(sparsity),
                                               float(L))
+
+
+def attn_skip_selftest_wait_timeout(stream=None, device=None):
+    """Launch the diagnostic CTA whose bounded wait runs out (see the header)."""
+    st = load().attn_skip_selftest_wait_timeout(_stream(stream, device))
+    _check("attn_skip_selftest_wait_timeout", st)
 
 
 def attn_skip_last_device_error(stream=None, device=None):

@@ -197,6 +197,13 @@ extern "C" attn_status attn_skip_decode_combine(const float *o_part, const float
   return from_cuda(launch_combine(a, (cudaStream_t)stream));
 }
 
+extern "C" attn_status attn_skip_selftest_wait_timeout(void *stream) {
+  unsigned *err = nullptr;
+  cudaError_t e = error_word(&err);
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(launch_selftest_wait(err, (cudaStream_t)stream));
+}
+
 extern "C" attn_status attn_skip_last_device_error(void *stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return from_cuda(e);

@@ -58,5 +58,6 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
+cudaError_t launch_selftest_wait(unsigned *err, cudaStream_t s);
 
 }  // namespace attn_skip

@@ -196,6 +196,16 @@ attn_status attn_skip_fit_lambda_model(const double *L, const double *sparsity,
 double attn_skip_lambda_for_target(double alpha, double beta, double sparsity, double L);
 
 /*
+ * Diagnostic: launches one small CTA that allocates TMEM and then waits, with
+ * the same bounded wait as every kernel, on an mbarrier phase that nothing
+ * completes.  After the 1 s limit the wait gives up, the CTA raises its abort
+ * flag, frees its TMEM and exits, and the device error word records the
+ * timeout, so a following attn_skip_last_device_error returns ATTN_ETIMEOUT
+ * and the context stays usable.  Exercises the failure path without a fault.
+ */
+attn_status attn_skip_selftest_wait_timeout(void *stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's error
  * word: ATTN_ETIMEOUT if a kernel gave up a bounded wait since the last read,
  * ATTN_ECUDA on a CUDA error, else ATTN_OK.
