@@ -60,7 +60,7 @@ def _load():
         lib.bsa_oracle_dense_prefill.argtypes = [P, P, P, i, i, i, i, i, i, d, i, P, i64, P, P]
         lib.bsa_oracle_dense_decode.argtypes = [P, P, P, i, i, i, i, i, i, i64, i64, d, P, P]
         lib.bsa_oracle_prefill.argtypes = [P, P, P, i, i, i, i, i, i, d, d, i, i, i, P, i64,
-                                           P, P, P, P, P]
+                                           P, P, P, P, P, P]
         lib.bsa_oracle_decode.argtypes = [P, P, P, i, i, i, i, i, i, i64, i64, d, d, i, i, P,
                                           i64, P, P, P, P, P]
         lib.bsa_oracle_combine.argtypes = [P, P, i, i, i, i, P, P]
@@ -144,7 +144,8 @@ def _forced(force_skip, shape):
     return f
 
 
-def prefill(q, k, v, scale, lam, Br=128, Bc=128, causal=True, units=None, force_skip=None):
+def prefill(q, k, v, scale, lam, Br=128, Bc=128, causal=True, units=None, force_skip=None,
+            allow=None):
     """Thresholded online-softmax prefill in fp64.
 
     Returns a dict with ``o`` [B,Hq,T,dv], ``lse`` [B,Hq,T], ``skip``
@@ -152,7 +153,10 @@ def prefill(q, k, v, scale, lam, Br=128, Bc=128, causal=True, units=None, force_
     statistic max_r(rowmax - m_new); NaN where not traversed).  ``units`` are
     flat indices into [B,Hq,n_t]; only those tiles are computed.
     ``force_skip`` ([B,Hq,n_t,n_b]) replaces the skip decisions by given ones
-    (the loop's arithmetic is unchanged)."""
+    (the loop's arithmetic is unchanged).  ``allow`` ([B,Hq,n_t,n_b], nonzero =
+    in the set) restricts each tile to an explicit block set: blocks outside it
+    are not traversed; a row with no visible key in its set gets O = 0 and
+    LSE = -inf."""
     q, k, v = _f32(q), _f32(k), _f32(v)
     B, Hq, T, dk = q.shape
     Hkv, dv = k.shape[1], v.shape[3]
@@ -163,10 +167,12 @@ def prefill(q, k, v, scale, lam, Br=128, Bc=128, causal=True, units=None, force_
     margin = np.full((B, Hq, n_t, n_b), np.nan)
     u, nu = _units(units)
     f = _forced(force_skip, skip.shape)
+    al = None if allow is None else _forced(np.asarray(allow) != 0, skip.shape)
     rc = _load().bsa_oracle_prefill(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, T, dk, dv,
                                     float(scale), float(lam), Br, Bc, int(bool(causal)),
                                     None if u is None else _ptr(u), nu,
-                                    None if f is None else _ptr(f), _ptr(o), _ptr(lse),
+                                    None if f is None else _ptr(f),
+                                    None if al is None else _ptr(al), _ptr(o), _ptr(lse),
                                     _ptr(skip), _ptr(margin))
     if rc:
         raise ValueError("bsa_oracle_prefill: invalid arguments")

@@ -223,12 +223,18 @@ static int loop_step(loop_state *st, int nc, int Bc, const float *vblk, int64_t 
  *   o:[B,Hq,T,dv], lse:[B,Hq,T]   final O = acc / l and LSE = m + ln l;
  *   skip:[B,Hq,n_t,n_b] (1 = skipped), margin:[B,Hq,n_t,n_b] (NaN = not traversed).
  * force_skip (NULL = none), same layout as skip: the decisions to take instead of
- * the test's, for evaluating the loop under another valid set of decisions. */
+ * the test's, for evaluating the loop under another valid set of decisions.
+ * allow (NULL = every block), same layout as skip: an explicit block set per
+ * query tile (the SparDA page, section 2.1: an access set such as
+ * B_init u B_local u B_topk); blocks outside it are not traversed -- no scores,
+ * no running-max update, skip 0, margin NaN -- and the threshold test applies
+ * among the blocks inside it.  A row with no visible key in its tile's set gets
+ * O = 0 and LSE = -inf (no mass at all). */
 int bsa_oracle_prefill(const float *q, const float *k, const float *v, int B, int Hq, int Hkv,
                        int T, int dk, int dv, double scale, double lambda, int Br, int Bc,
                        int causal, const int64_t *units, int64_t n_units,
-                       const uint8_t *force_skip, double *o, double *lse, uint8_t *skip,
-                       double *margin) {
+                       const uint8_t *force_skip, const uint8_t *allow, double *o, double *lse,
+                       uint8_t *skip, double *margin) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || T <= 0 || dk <= 0 || dv <= 0 || Br <= 0 || Bc <= 0 ||
       Hq % Hkv || !(lambda >= 0.0 && lambda < 1.0))
     return -1;
@@ -254,6 +260,7 @@ int bsa_oracle_prefill(const float *q, const float *k, const float *v, int B, in
     loop_state st;
     state_init(&st, nr, Bc, dv);
     for (int j = 0; j <= jmax; ++j) { /* KV blocks in ascending order */
+      if (allow && !allow[u * n_b + j]) continue; /* outside the tile's block set */
       const int c0 = j * Bc, c1 = (c0 + Bc < T) ? c0 + Bc : T, nc = c1 - c0;
       for (int r = 0; r < nr; ++r) {
         const int row = r0 + r;
@@ -270,8 +277,9 @@ int bsa_oracle_prefill(const float *q, const float *k, const float *v, int B, in
     }
     for (int r = 0; r < nr; ++r) {
       const int64_t orow = ((int64_t)b * Hq + h) * T + r0 + r;
-      for (int e = 0; e < dv; ++e) o[orow * dv + e] = st.acc[(size_t)r * dv + e] / st.l[r];
-      lse[orow] = st.m[r] + log(st.l[r]);
+      const int empty = !(st.l[r] > 0.0); /* no visible key in the block set */
+      for (int e = 0; e < dv; ++e) o[orow * dv + e] = empty ? 0.0 : st.acc[(size_t)r * dv + e] / st.l[r];
+      lse[orow] = empty ? NEG_INF : st.m[r] + log(st.l[r]);
     }
     state_free(&st);
   }

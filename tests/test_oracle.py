@@ -518,3 +518,58 @@ def test_generator_plants_sink_and_salient_keys():
     assert proj[0] > 5 * math.sqrt(d)                        # sink, a_0 = 6
     n_sal = int(((proj > 2 * math.sqrt(d)) & (proj < 4 * math.sqrt(d))).sum())
     assert abs(n_sal - round(0.02 * (cfg.T - 1))) <= 3       # 2 % salient at a = 3
+
+
+# --------------------------------------------------------------------------
+# Explicit block sets (the SparDA page, section 2.1: an access set per query
+# tile, composed with the threshold test inside it)
+# --------------------------------------------------------------------------
+
+def _random_block_set(B, Hq, T, Br, Bc, density, seed, drop_diagonal=False):
+    g = np.random.default_rng(seed)
+    n_t, n_b = -(-T // Br), -(-T // Bc)
+    allow = g.random((B, Hq, n_t, n_b)) < density
+    allow[..., 0] = True  # an "init" block
+    if drop_diagonal:
+        allow[:, :, 1, :] = False  # tile 1 selects nothing at all
+    return allow.astype(np.uint8)
+
+
+def test_block_set_all_ones_is_the_plain_loop():
+    cfg, q, k, v = _planted_small(temperate=True, seed=21)
+    allow = np.ones((1, cfg.Hq, cfg.n_t, cfg.n_b), dtype=np.uint8)
+    for lam in (0.0, 1e-3):
+        a = oracle.prefill(q, k, v, cfg.scale, lam, cfg.Br, cfg.Bc, True)
+        b = oracle.prefill(q, k, v, cfg.scale, lam, cfg.Br, cfg.Bc, True, allow=allow)
+        for key in ("o", "lse", "skip", "margin"):
+            np.testing.assert_array_equal(a[key], b[key])
+
+
+@pytest.mark.parametrize("lam", [0.0, 1e-4, 2e-2])
+def test_block_set_output_is_softmax_over_selected_kept_tokens(lam):
+    """Closed form: O is the softmax over the visible tokens of the selected,
+    kept blocks; rows whose tile selected no visible key get O = 0, LSE = -inf;
+    blocks outside the set are untraversed (bit 0, statistic NaN)."""
+    cfg, q, k, v = _planted_small(temperate=True, seed=22)
+    allow = _random_block_set(1, cfg.Hq, cfg.T, cfg.Br, cfg.Bc, 0.5, seed=5, drop_diagonal=True)
+    r = oracle.prefill(q, k, v, cfg.scale, lam, cfg.Br, cfg.Bc, True, allow=allow)
+    out = ~allow.astype(bool)
+    assert (r["skip"][out] == 0).all() and np.isnan(r["margin"][out]).all()
+    s = scores_full(q, k, cfg.scale, True)
+    km = kept_token_mask(r["skip"], cfg.T, cfg.Br, cfg.Bc, True)
+    sel = allow.astype(bool)[:, :, np.arange(cfg.T) // cfg.Br][:, :, :, np.arange(cfg.T) // cfg.Bc]
+    km &= sel
+    empty = ~km.any(axis=-1)
+    assert empty[:, :, cfg.Br:2 * cfg.Br].all()  # the tile that selected nothing
+    sk = np.where(km, s, -np.inf)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        p, lse = softmax_rows(np.where(empty[..., None], 0.0, sk))
+    vv = np.repeat(v.astype(np.float64), cfg.G, axis=1)
+    want = np.einsum("bhrc,bhce->bhre", p, vv)
+    want[empty] = 0.0
+    lse[empty] = -np.inf
+    np.testing.assert_allclose(r["o"], want, rtol=1e-10, atol=1e-11)
+    np.testing.assert_allclose(r["lse"], lse, rtol=1e-12, atol=1e-11)
+    if lam > 0:  # every skipped selected block lies below ln(lambda)
+        sk_ = r["skip"].astype(bool)
+        assert (r["margin"][sk_] < np.log(lam)).all()
