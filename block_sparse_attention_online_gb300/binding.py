@@ -22,7 +22,8 @@ ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT = range(5)
 ATTN_BF16, ATTN_F32 = 0, 1
 
 #: Every symbol include/attn_skip.h declares.
-EXPORTED = ("attn_skip_prefill", "attn_skip_decode", "attn_skip_decode_combine",
+EXPORTED = ("attn_skip_prefill", "attn_skip_prefill_blocks", "attn_skip_decode",
+            "attn_skip_decode_combine",
             "attn_skip_prefill_margins", "attn_skip_decode_margins", "attn_skip_sparsity_at",
             "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
             "attn_skip_lambda_for_target", "attn_skip_selftest_wait_timeout",
@@ -50,6 +51,8 @@ def load() -> ctypes.CDLL:
     lib = ctypes.CDLL(_LIB_PATH)
     P, i, f, d, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_int64
     lib.attn_skip_prefill.argtypes = [P, P, P, i, i, i, i, i, i, i, f, d, i, i, i, P, P, P, P]
+    lib.attn_skip_prefill_blocks.argtypes = [P, P, P, i, i, i, i, i, i, i, f, d, i, i, i, P, P, P,
+                                             P, P]
     lib.attn_skip_decode.argtypes = [P, P, P, i, i, i, i, i, i, i, i64, i64, f, d, i, i, P, P, P,
                                      P]
     lib.attn_skip_decode_combine.argtypes = [P, P, i, i, i, i, i, P, P, P]
@@ -65,7 +68,8 @@ def load() -> ctypes.CDLL:
     lib.attn_skip_selftest_wait_timeout.argtypes = [P]
     lib.attn_skip_status_string.argtypes = [i]
     lib.attn_skip_status_string.restype = ctypes.c_char_p
-    for fn in ("attn_skip_prefill", "attn_skip_decode", "attn_skip_decode_combine",
+    for fn in ("attn_skip_prefill", "attn_skip_prefill_blocks", "attn_skip_decode",
+               "attn_skip_decode_combine",
                "attn_skip_prefill_margins", "attn_skip_decode_margins",
                "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
                "attn_skip_selftest_wait_timeout", "attn_skip_last_device_error"):
@@ -143,6 +147,44 @@ def attn_skip_prefill(q, k, v, lam, Br=128, Bc=128, causal=True, scale=0.0, out=
                                   dv, float(scale), float(lam), Br, Bc, int(bool(causal)),
                                   _ptr(o), _ptr(lse), _ptr(bits), _stream(stream, q.device))
     _check("attn_skip_prefill", st)
+    return o, lse, bits
+
+
+def pack_block_set(allow: torch.Tensor) -> torch.Tensor:
+    """Pack a bool tensor [..., n_b] (True = block in the set) into uint32 words
+    [..., ceil(n_b/32)], stored as int32, on the tensor's device."""
+    n = allow.shape[-1]
+    w = -(-n // 32)
+    a = torch.zeros(*allow.shape[:-1], w * 32, dtype=torch.int64, device=allow.device)
+    a[..., :n] = allow.to(torch.int64)
+    a = a.reshape(*allow.shape[:-1], w, 32)
+    words = (a << torch.arange(32, dtype=torch.int64, device=allow.device)).sum(-1)
+    return torch.where(words >= (1 << 31), words - (1 << 32), words).to(torch.int32)
+
+
+def attn_skip_prefill_blocks(q, k, v, lam, block_set, Br=128, Bc=128, causal=True, scale=0.0,
+                             out=None, stream=None):
+    """Prefill restricted to a block set: ``block_set`` is the packed uint32
+    mask [B,Hq,n_t,words] (see :func:`pack_block_set`) on the inputs' device.
+    Returns ``(o, lse, skip_bits)``."""
+    _cuda_contig(q, k, v, block_set)
+    B, Hq, T, dk = q.shape
+    Hkv, dv = k.shape[1], v.shape[3]
+    if tuple(block_set.shape) != prefill_bitmap_shape(B, Hq, T, Br, Bc):
+        raise ValueError(f"block_set has shape {tuple(block_set.shape)}, expected "
+                         f"{prefill_bitmap_shape(B, Hq, T, Br, Bc)}")
+    if out is None:
+        o = torch.empty(B, Hq, T, dv, dtype=q.dtype, device=q.device)
+        lse = torch.empty(B, Hq, T, dtype=torch.float32, device=q.device)
+        bits = torch.empty(prefill_bitmap_shape(B, Hq, T, Br, Bc), dtype=torch.int32,
+                           device=q.device)
+    else:
+        o, lse, bits = out
+    st = load().attn_skip_prefill_blocks(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, Hq, Hkv,
+                                         T, dk, dv, float(scale), float(lam), Br, Bc,
+                                         int(bool(causal)), _ptr(block_set), _ptr(o), _ptr(lse),
+                                         _ptr(bits), _stream(stream, q.device))
+    _check("attn_skip_prefill_blocks", st)
     return o, lse, bits
 
 

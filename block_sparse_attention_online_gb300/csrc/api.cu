@@ -140,6 +140,21 @@ extern "C" attn_status attn_skip_prefill(const void *q, const void *k, const voi
                         (cudaStream_t)stream);
 }
 
+extern "C" attn_status attn_skip_prefill_blocks(const void *q, const void *k, const void *v,
+                                                attn_dtype dt, int B, int Hq, int Hkv, int T,
+                                                int dk, int dv, float scale, double lambda,
+                                                int Br, int Bc, int causal,
+                                                const uint32_t *block_set, void *o, float *lse,
+                                                uint32_t *skip_bits, void *stream) {
+  if (!block_set || !o || !lse || !skip_bits) return ATTN_EINVAL;
+  if (!aligned16(block_set) || !aligned16(o) || !aligned16(lse) || !aligned16(skip_bits))
+    return ATTN_EINVAL;
+  PrefillArgs a{};
+  a.o = o; a.lse = lse; a.bits = skip_bits; a.block_set = block_set;
+  return prefill_common(a, q, k, v, dt, B, Hq, Hkv, T, dk, dv, scale, lambda, Br, Bc, causal,
+                        (cudaStream_t)stream);
+}
+
 extern "C" attn_status attn_skip_prefill_margins(const void *q, const void *k, attn_dtype dt,
                                                  int B, int Hq, int Hkv, int T, int dk,
                                                  float scale, int Br, int Bc, int causal,

@@ -26,6 +26,9 @@ struct PrefillArgs {
   // every block is treated as skipped, and o, lse, bits are not written.
   float *margin;
   int stats_only;
+  // Explicit block set: [B,Hq,n_t,words] bit masks, bit j = block j is
+  // traversed (within the causal range); null = every block.
+  const uint32_t *block_set;
 };
 
 struct DecodeArgs {

@@ -47,9 +47,16 @@ __global__ void __launch_bounds__(BR) prefill_f32_kernel(const PrefillArgs a) {
   const int jmax = a.causal ? last_row / BC : a.n_b - 1;
   uint32_t *bits = a.bits ? a.bits + (size_t)unit * a.words : nullptr;
   uint32_t word = 0;
+  int wcur = 0;  // next bitmap word to write
   float *Sr = Ss + r * (BC + 1);
+  // Explicit block set (null = every block): blocks outside it are not traversed.
+  const uint32_t *set = a.block_set ? a.block_set + (size_t)unit * a.words : nullptr;
 
   for (int j = 0; j <= jmax; ++j) {
+    if (set && !((set[j >> 5] >> (j & 31)) & 1u)) {
+      if (a.margin && r == 0) a.margin[(size_t)unit * a.n_b + j] = NAN;
+      continue;
+    }
     __syncthreads();  // the previous block's readers of Ks / Vs are done
     for (int i = r; i < BC * D / 4; i += BR) {
       const int c = (i * 4) / D, e = (i * 4) % D, key = j * BC + c;
@@ -101,11 +108,11 @@ __global__ void __launch_bounds__(BR) prefill_f32_kernel(const PrefillArgs a) {
       a.margin[(size_t)unit * a.n_b + j] = st;
     }
     if (a.stats_only) skip = true;
-    if (skip) word |= 1u << (j & 31);
-    if (!a.stats_only && r == 0 && ((j & 31) == 31 || j == jmax)) {
-      bits[j >> 5] = word;
+    for (; wcur < (j >> 5); ++wcur) {  // earlier words are complete
+      if (!a.stats_only && r == 0) bits[wcur] = word;
+      word = 0;
     }
-    if ((j & 31) == 31) word = 0;
+    if (skip) word |= 1u << (j & 31);
 
     if (!skip) {
       for (int i = r; i < BC * D / 4; i += BR) {
@@ -142,16 +149,21 @@ __global__ void __launch_bounds__(BR) prefill_f32_kernel(const PrefillArgs a) {
     return;
   }
   if (r == 0) {
-    for (int w = (jmax >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
+    for (; wcur < a.words; ++wcur) {
+      bits[wcur] = word;
+      word = 0;
+    }
   }
   if (a.margin && r == 0)
     for (int j = jmax + 1; j < a.n_b; ++j) a.margin[(size_t)unit * a.n_b + j] = NAN;
   if (valid) {
     float *og = (float *)a.o + ((size_t)(b * a.Hq + h) * a.T + row) * D;
-    const float inv = 1.f / l;
+    // (A row whose block set holds no visible key has no mass: O = 0, LSE = -inf.)
+    const bool empty = !(l > 0.f);
+    const float inv = empty ? 0.f : 1.f / l;
 #pragma unroll
-    for (int i = 0; i < D; ++i) og[i] = acc[i] * inv;
-    a.lse[(size_t)(b * a.Hq + h) * a.T + row] = m + logf(l);
+    for (int i = 0; i < D; ++i) og[i] = empty ? 0.f : acc[i] * inv;
+    a.lse[(size_t)(b * a.Hq + h) * a.T + row] = empty ? -INFINITY : m + logf(l);
   }
 }
 

@@ -83,7 +83,13 @@ struct Shared {
   uint64_t k_full[NK], k_empty[NK];
   uint64_t v_full[NV], v_empty[NV];
   uint64_t s_full[NS], s_free[NS];
-  uint64_t p_full[2], pv_done[2];
+  // P of kept block kc ready, slot kc % NS.  Kept blocks whose P exists but
+  // whose P.V has not completed each hold an S buffer, so at most NS are
+  // outstanding and a slot is never re-armed before its phase was consumed
+  // (with fewer slots than S buffers the exponential warps could complete a
+  // slot's next phase first when a value load is slow).
+  uint64_t p_full[NS];
+  uint64_t pv_done[2];
   uint64_t dec_full[NDEC];
   uint64_t dec_read[NDEC];  // the V producer, the P.V issuer and the exponential warps read slot j % NDEC
   uint64_t vote_full[2];
@@ -185,9 +191,11 @@ __device__ __forceinline__ void chunk_exp(const uint32_t (&s)[32], uint64_t sl2x
   }
 }
 
-// STATS: the statistics mode (compiled separately so that the ordinary
-// kernel's decision loop carries none of its code).
-template <bool STATS>
+// STATS: the statistics mode; SET: an explicit block set per tile (blocks
+// outside it are not traversed).  Each is compiled separately so that the
+// ordinary kernel's loops carry none of their code.  Ring positions count the
+// traversed blocks (c); addresses and bitmap positions use the block index (j).
+template <bool STATS, bool SET>
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -212,6 +220,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int nblk = a.causal ? last_row / BN + 1 : a.n_b;
   volatile int *abort = &sh.abort;
   const int zq = b * a.Hq + h, zkv = b * a.Hkv + hk;
+  const uint32_t *set_words = SET ? a.block_set + ((size_t)bh * a.n_t + t) * a.words : nullptr;
+  auto in_set = [&](int j) { return ((__ldg(set_words + (j >> 5)) >> (j & 31)) & 1u) != 0u; };
 
   if (tid == 0) {
     mbar_init(smem_u32(&sh.q_full), 1);
@@ -226,9 +236,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&sh.s_full[i]), 1);
       mbar_init(smem_u32(&sh.s_free[i]), 1);  // the P.V commit of a kept block
+      mbar_init(smem_u32(&sh.p_full[i]), NQ);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&sh.p_full[i]), NQ);
       mbar_init(smem_u32(&sh.pv_done[i]), 1);
       mbar_init(smem_u32(&sh.vote_full[i]), NQ);
     }
@@ -258,11 +268,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tma_load_3d(base + SMEM_Q, &tm_q, smem_u32(&sh.q_full), 0, row0, zq, stream_l2);
       tma_load_3d(base + SMEM_Q + HALF_BYTES, &tm_q, smem_u32(&sh.q_full), 64, row0, zq,
                   stream_l2);
-      int ki = 0;
+      int ki = 0, cc = 0;
       for (int j = 0; j < nblk && !*abort; ++j) {
-        const int s = j % NK;
-        if (j >= NK &&
-            !mbar_wait(smem_u32(&sh.k_empty[s]), ((j / NK) - 1) & 1, abort, a.err, kErrTimeout))
+        if constexpr (SET) {
+          if (!in_set(j)) continue;
+        }
+        const int c = SET ? cc++ : j;
+        const int s = c % NK;
+        if (c >= NK &&
+            !mbar_wait(smem_u32(&sh.k_empty[s]), ((c / NK) - 1) & 1, abort, a.err, kErrTimeout))
           break;
         const uint32_t dst = base + SMEM_K + s * TILE_BYTES;
         mbar_expect_tx(smem_u32(&sh.k_full[s]), TILE_BYTES);
@@ -283,13 +297,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (lane == 0) {
       prefetch_tmap(&tm_v);
       const uint64_t keep_l2 = policy_evict_last();
-      int vi = 0;
+      int vi = 0, cc = 0;
       for (int j = 0; j < nblk && !*abort; ++j) {
-        if (!mbar_wait(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
+        if constexpr (SET) {
+          if (!in_set(j)) continue;
+        }
+        const int c = SET ? cc++ : j;
+        if (!mbar_wait(smem_u32(&sh.dec_full[c % NDEC]), (c / NDEC) & 1, abort, a.err,
                        kErrTimeout))
           break;
-        const int keep = sh.dec[j % NDEC];
-        mbar_arrive(smem_u32(&sh.dec_read[j % NDEC]));
+        const int keep = sh.dec[c % NDEC];
+        mbar_arrive(smem_u32(&sh.dec_read[c % NDEC]));
         if (!keep) continue;
         const int s = vi % NV;
         if (vi >= NV &&
@@ -313,17 +331,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       fence_after_sync();
       const uint64_t qdesc = kmajor_base(base + SMEM_Q);
       int pv_into[NS] = {0, 0, 0};  // P.V products issued into each S buffer
+      int cc = 0;
       for (int j = 0; ok && j < nblk; ++j) {
-        const int s = j % NK, sb = j % NS;
-        if (!mbar_wait(smem_u32(&sh.k_full[s]), (j / NK) & 1, abort, a.err, kErrTimeout)) break;
-        if (j >= NS) {
+        if constexpr (SET) {
+          if (!in_set(j)) continue;
+        }
+        const int c = SET ? cc++ : j;
+        const int s = c % NK, sb = c % NS;
+        if (!mbar_wait(smem_u32(&sh.k_full[s]), (c / NK) & 1, abort, a.err, kErrTimeout)) break;
+        if (c >= NS) {
           // S buffer sb last held block j - NS: free once its scores were read
           // (a skipped block: its decision exists) or its P.V completed (kept).
-          const int jp = j - NS;
-          if (!mbar_wait(smem_u32(&sh.dec_full[jp % NDEC]), (jp / NDEC) & 1, abort, a.err,
+          const int cp = c - NS;
+          if (!mbar_wait(smem_u32(&sh.dec_full[cp % NDEC]), (cp / NDEC) & 1, abort, a.err,
                          kErrTimeout))
             break;
-          if (sh.dec[jp % NDEC]) {
+          if (sh.dec[cp % NDEC]) {
             ++pv_into[sb];
             if (!mbar_wait(smem_u32(&sh.s_free[sb]), (pv_into[sb] - 1) & 1, abort, a.err,
                            kErrTimeout))
@@ -343,8 +366,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == WARP_PV) {
     // ---------------------------------------------------------- P.V issuer --
     if (lane == 0) {
-      int kc = 0, vi = 0;
-      for (int i = 0; i < nblk && !*abort; ++i) {
+      int kc = 0, vi = 0, cc = 0;
+      for (int j = 0; j < nblk && !*abort; ++j) {
+        if constexpr (SET) {
+          if (!in_set(j)) continue;
+        }
+        const int i = SET ? cc++ : j;  // traversed-block position
         if (!mbar_wait(smem_u32(&sh.dec_full[i % NDEC]), (i / NDEC) & 1, abort, a.err,
                        kErrTimeout))
           break;
@@ -352,7 +379,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive(smem_u32(&sh.dec_read[i % NDEC]));
         if (!keep) continue;
         const int pb = kc & 1, vs = vi % NV;
-        if (!mbar_wait(smem_u32(&sh.p_full[pb]), (kc >> 1) & 1, abort, a.err, kErrTimeout))
+        if (!mbar_wait(smem_u32(&sh.p_full[kc % NS]), (kc / NS) & 1, abort, a.err, kErrTimeout))
           break;
         if (!mbar_wait(smem_u32(&sh.v_full[vs]), (vi / NV) & 1, abort, a.err, kErrTimeout))
           break;
@@ -398,13 +425,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       float m2 = -INFINITY;                       // running max (log2 units)
       uint32_t word = 0;
       uint32_t *bits = a.bits ? a.bits + ((size_t)bh * a.n_t + t) * a.words : nullptr;
-      int sb = 0;
+      int sb = 0, cc = 0;
+      int wcur = 0;  // block-set mode: next bitmap word to write
       for (int j = 0; j < nblk; ++j) {
+        if constexpr (SET) {
+          if (!in_set(j)) continue;
+        }
+        const int c = SET ? cc++ : j;
         const int sbn = sb == NS - 1 ? 0 : sb + 1;
         // Slot sbn was last read after the barrier of block j-2, before every
         // decider arrived at the barrier of block j-1.
         if (tid == 0) sh.keepw[sbn] = 0u;
-        if (!mbar_wait_warp(smem_u32(&sh.s_full[sb]), (j / NS) & 1, abort, a.err, kErrTimeout)) {
+        if (!mbar_wait_warp(smem_u32(&sh.s_full[sb]), (c / NS) & 1, abort, a.err, kErrTimeout)) {
           ok = false;
           break;
         }
@@ -435,13 +467,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           float st = (valid && mt != -INFINITY) ? fminf(diff, 0.f) : -INFINITY;
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) st = fmaxf(st, __shfl_xor_sync(0xffffffffu, st, o));
-          if (lane == 0) sh.wstat[j & 1][warp] = st;
+          if (lane == 0) sh.wstat[c & 1][warp] = st;
         }
         fence_before_sync();  // this warp's reads of S_j are complete
         __syncwarp();
-        const int vb = j & 1;
+        const int vb = c & 1;
         if (lane == 0) mbar_arrive(smem_u32(&sh.vote_full[vb]));
-        if (!mbar_wait_warp(smem_u32(&sh.vote_full[vb]), (j >> 1) & 1, abort, a.err,
+        if (!mbar_wait_warp(smem_u32(&sh.vote_full[vb]), (c >> 1) & 1, abort, a.err,
                             kErrTimeout)) {
           ok = false;
           break;
@@ -449,8 +481,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const bool skip = STATS || sh.keepw[sb] == 0u;
         m2 = mnew;
         if (STATS && tid == 0) {
-          const float st = fmaxf(fmaxf(sh.wstat[j & 1][0], sh.wstat[j & 1][1]),
-                                 fmaxf(sh.wstat[j & 1][2], sh.wstat[j & 1][3]));
+          const float st = fmaxf(fmaxf(sh.wstat[c & 1][0], sh.wstat[c & 1][1]),
+                                 fmaxf(sh.wstat[c & 1][2], sh.wstat[c & 1][3]));
           a.margin[((size_t)bh * a.n_t + t) * a.n_b + j] = st * kLn2;
         }
         if (tid == 0) {
@@ -458,13 +490,20 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // as it reads this decision.)  The slot's previous decision (block
           // j - NDEC) must have been read by all its readers; on a timeout the
           // abort flag is raised and every later wait fails.
-          if (j < NDEC || mbar_wait(smem_u32(&sh.dec_read[j % NDEC]), ((j / NDEC) - 1) & 1,
+          if (c < NDEC || mbar_wait(smem_u32(&sh.dec_read[c % NDEC]), ((c / NDEC) - 1) & 1,
                                     abort, a.err, kErrTimeout)) {
-            sh.dec[j % NDEC] = skip ? 0 : 1;
-            mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
+            sh.dec[c % NDEC] = skip ? 0 : 1;
+            mbar_arrive(smem_u32(&sh.dec_full[c % NDEC]));
+          }
+          if constexpr (SET) {
+            // Words before this block's are complete (untraversed blocks read 0).
+            for (; wcur < (j >> 5); ++wcur) {
+              if (!STATS) bits[wcur] = word;
+              word = 0;
+            }
           }
           if (skip) word |= 1u << (j & 31);
-          if (!STATS && ((j & 31) == 31 || j == nblk - 1)) {
+          if (!SET && !STATS && ((j & 31) == 31 || j == nblk - 1)) {
             bits[j >> 5] = word;
             word = 0;
           }
@@ -472,8 +511,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         sb = sbn;
       }
       if (tid == 0) {
-        if (!STATS)
+        if constexpr (SET) {
+          for (; wcur < a.words; ++wcur) {
+            if (!STATS) bits[wcur] = word;
+            word = 0;
+          }
+        } else if (!STATS) {
           for (int w = ((nblk - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
+        }
         if (STATS)
           for (int j = nblk; j < a.n_b; ++j) a.margin[((size_t)bh * a.n_t + t) * a.n_b + j] = NAN;
       }
@@ -481,16 +526,21 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // Per kept block: P_j = exp2(S_j - ref) as bf16 pairs into columns
       // [0,64) of the block's S buffer, the row sum, and an O rescale when
       // the exp reference moves by more than 2^8.
-      int sb = 0;
-      for (int j = 0; ok && j < nblk; ++j, sb = (sb == NS - 1 ? 0 : sb + 1)) {
-        if (!mbar_wait_warp(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
+      int sb = 0, cc = 0;  // sb = c % NS
+      for (int j = 0; ok && j < nblk; ++j) {
+        if constexpr (SET) {
+          if (!in_set(j)) continue;
+        }
+        const int c = SET ? cc++ : j;
+        if (c > 0) sb = sb == NS - 1 ? 0 : sb + 1;
+        if (!mbar_wait_warp(smem_u32(&sh.dec_full[c % NDEC]), (c / NDEC) & 1, abort, a.err,
                             kErrTimeout)) {
           ok = false;
           break;
         }
-        const int keep = sh.dec[j % NDEC];
+        const int keep = sh.dec[c % NDEC];
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.dec_read[j % NDEC]));
+        if (lane == 0) mbar_arrive(smem_u32(&sh.dec_read[c % NDEC]));
         if (!keep) continue;
         const float mnew = sh.mdec[sb][r];
         bool rescale = false;
@@ -548,7 +598,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[kc & 1]));
+        if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[kc % NS]));
         ++kc;
       }
       if (ok && kc > 0) {
@@ -567,7 +617,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (ok && !STATS) {
       fence_after_sync();
       const float lrow = sh.lfin[r];
-      const float inv = 1.f / lrow;
+      // Block-set mode: a tile that selected no block has no mass (O = 0,
+      // LSE = -inf); its O accumulator was never written.
+      const bool empty = SET && !(lrow > 0.f);
+      const float inv = empty ? 0.f : 1.f / lrow;
       const int col0 = decider ? 0 : 64;
       __nv_bfloat16 *orow = (__nv_bfloat16 *)a.o + ((size_t)bh * a.T + row) * D + col0;
 #pragma unroll 1
@@ -575,6 +628,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         uint32_t o[32];
         tmem_ld32(lane_base + TMEM_O + col0 + c * 32, o);
         tmem_wait_ld_regs(o);
+        if (empty) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
         if (valid) {
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
@@ -587,7 +644,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
         }
       }
-      if (valid && !decider) a.lse[(size_t)bh * a.T + row] = sh.mfin[r] * kLn2 + logf(lrow);
+      if (valid && !decider)
+        a.lse[(size_t)bh * a.T + row] = empty ? -INFINITY : sh.mfin[r] * kLn2 + logf(lrow);
     }
   }
 
@@ -608,7 +666,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
       !make_map_bf16_3d(&mk, a.k, D, D, a.T, a.B * a.Hkv, BN) ||
       !make_map_bf16_3d(&mv, a.v, D, D, a.T, a.B * a.Hkv, BN))
     return cudaErrorInvalidValue;
-  auto kernel = a.stats_only ? prefill_tc_kernel<true> : prefill_tc_kernel<false>;
+  auto kernel = a.stats_only  ? prefill_tc_kernel<true, false>
+                : a.block_set ? prefill_tc_kernel<false, true>
+                              : prefill_tc_kernel<false, false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_ALLOC);
   if (e != cudaSuccess) return e;

@@ -85,6 +85,26 @@ attn_status attn_skip_prefill(const void *q, const void *k, const void *v, attn_
                               uint32_t *skip_bits, void *stream);
 
 /*
+ * Prefill restricted to an explicit block set per query tile, composed with
+ * the threshold test: the consumer side of a block-selection stage such as the
+ * SparDA page's InfLLM-V2 access set B_init u B_local u B_topk (section 2.1).
+ * Blocks outside a tile's set are not traversed -- no Q.K^T, no running-max
+ * update, no value load -- and read 0 in skip_bits; inside the set the loop and
+ * the skip test are those of attn_skip_prefill, blocks visited in ascending
+ * order.  A row whose tile set holds no visible key gets O = 0, LSE = -inf.
+ *
+ *  block_set  [B, Hq, ceil(T/Br), ceil(ceil(T/Bc)/32)] uint32 (device): bit
+ *             (j % 32) of word (j / 32) = block j is in the tile's set; bits
+ *             of blocks a causal tile does not reach are ignored
+ *  other arguments and outputs as for attn_skip_prefill; same kernels built.
+ */
+attn_status attn_skip_prefill_blocks(const void *q, const void *k, const void *v, attn_dtype dt,
+                                     int B, int Hq, int Hkv, int T, int dk, int dv, float scale,
+                                     double lambda, int Br, int Bc, int causal,
+                                     const uint32_t *block_set, void *o, float *lse,
+                                     uint32_t *skip_bits, void *stream);
+
+/*
  * Split-KV decode, one query token per sequence, with block skipping.
  *
  * Defines: section "Decode 内核：砍带宽" -- scores of a batch of KV blocks are

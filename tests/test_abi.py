@@ -72,6 +72,22 @@ def test_decode_rejects_invalid_arguments(lib, kw):
     assert _decode(lib, **kw) == bs.ATTN_EINVAL
 
 
+def _prefill_blocks(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, dt=0, B=1, Hq=4, Hkv=2, T=256, dk=128, dv=128, scale=0.0,
+             lam=0.01, Br=128, Bc=128, causal=1, set=FAKE, o=FAKE, lse=FAKE, bits=FAKE,
+             stream=None)
+    a.update(kw)
+    return lib.attn_skip_prefill_blocks(*a.values())
+
+
+@pytest.mark.parametrize("kw", [
+    dict(set=None), dict(set=ctypes.c_void_p(0x10004)), dict(o=None), dict(q=None),
+    dict(lam=1.0), dict(Hq=3), dict(T=0),
+])
+def test_prefill_blocks_rejects_invalid_arguments(lib, kw):
+    assert _prefill_blocks(lib, **kw) == bs.ATTN_EINVAL
+
+
 def _prefill_margins(lib, **kw):
     a = dict(q=FAKE, k=FAKE, dt=0, B=1, Hq=4, Hkv=2, T=256, dk=128, scale=0.0, Br=128, Bc=128,
              causal=1, m=FAKE, stream=None)
