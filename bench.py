@@ -47,12 +47,12 @@ CSRC = os.path.join(ROOT, "block_sparse_attention_online_gb300", "csrc")
 NCU_TRAFFIC = {
     "prefill_tc_kernel": {
         "file": "prefill_tc.cu",
-        "sha256": "511769a136493c9b2aecee9272ec007e392c2d115d79b0ad6b3b8aa5e73e767c",
-        "bytes": 240706304 + 83190272},
+        "sha256": "de67a4dad17928c67bc3c2254eedb58c7682d897b6452eb16e8dee353e4ec812",
+        "bytes": 241140736 + 82635008},
     "decode_tc_kernel": {
         "file": "decode.cu",
-        "sha256": "cbb3176da71abf2933cdd66f55ea77b4f11eacaa284e5e8338e00b63878345ef",
-        "bytes": 1396064256 + 3992064},
+        "sha256": "ff34ba73cd4d7a696421321d8216e9dfb410f7de5c3dc96dfc0ac0f5ea45e540",
+        "bytes": 1396185600 + 3996928},
 }
 
 
@@ -255,6 +255,7 @@ def run_gpu(args, rank, world):
 
     msweep = mla_sweep(args, bs, dev, stream, flush, lam)
     calib = calibration(args, bs, dev, stream, flush, dq, dk_, dv_, dqd, dkd, lp, ld, pbits)
+    blocks = block_set_sweep(args, bs, dev, stream, flush, dq, dk_, dv_, lp, po, plse, pbits)
 
     # ---- the timed region: K steps of the whole hot path at ~70 % ---------
     fp, fd = prefill(lp[TARGET]), decode(ld[TARGET])
@@ -338,6 +339,7 @@ def run_gpu(args, rank, world):
                             "algorithmic_bytes": dec["bytes"]},
         "mla_decode": msweep,
         "calibration": calib,
+        "block_set": blocks,
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,  # prefill, decode, merge per timed step
         "clocks": clk.summary(),
@@ -383,6 +385,49 @@ def mla_sweep(args, bs, dev, stream, flush, lam):
     out["max"]["speedup_vs_lambda0"] = round(out["0.0"]["ms"] / out["max"]["ms"], 4)
     out["workload"] = (f"B{M.B} Hq{M.Hq} latent dk{M.dk} dv{M.dv} L{M.L} Bc{M.Bc} "
                        f"splits{M.n_splits}; 'max' = largest sparsity any lambda < 1 reaches")
+    return out
+
+
+def infllm_like_set(P, topk, seed):
+    """Per query tile: block 0 (init), the diagonal block and the one before
+    (local), and `topk` blocks drawn at random from the rest of the causal
+    range -- the shape of an InfLLM-V2 access set (SparDA page, section 2.1)."""
+    g = torch.Generator().manual_seed(seed)
+    allow = torch.zeros(P.B, P.Hq, P.n_t, P.n_b, dtype=torch.bool)
+    allow[..., 0] = True
+    for t in range(P.n_t):
+        allow[:, :, t, t] = True
+        if t > 0:
+            allow[:, :, t, t - 1] = True
+        if t > 2:
+            r = torch.rand(P.B, P.Hq, t - 2, generator=g).argsort(-1)[..., :topk] + 1
+            allow[:, :, t].scatter_(-1, r, True)
+    return allow
+
+
+def block_set_sweep(args, bs, dev, stream, flush, dq, dk_, dv_, lp, po, plse, pbits):
+    """Prefill over an InfLLM-like block set (init + local + 16 top-k blocks per
+    tile) alone (lambda = 0) and composed with the ~70 % threshold."""
+    P = PREFILL
+    allow = infllm_like_set(P, 16, seed=7)
+    words = bs.pack_block_set(allow).to(dev)
+    pairs_set = int(allow.sum())
+    dense, per_pair = prefill_flops(P)
+    out = {"set": "init + local + 16 top-k blocks per tile",
+           "set_fraction_of_causal_pairs": round(pairs_set / traversed_pairs(P), 4)}
+    for t in ("0.0", TARGET):
+        lmb = lp[t]
+        durs = timed_launches(
+            lambda: bs.attn_skip_prefill_blocks(dq, dk_, dv_, lmb, words, P.Br, P.Bc, True,
+                                                out=(po, plse, pbits)),
+            args.warmup, args.steps, flush, stream)
+        skipped = int(bs.unpack_bits(pbits, P.n_b).sum())
+        ms = statistics.mean(durs)
+        executed = per_pair * (2 * pairs_set - skipped)
+        out[t] = {"lambda": lmb, "ms": round(ms, 4),
+                  "threshold_sparsity_in_set": round(skipped / pairs_set, 4),
+                  "executed_tflops": round(executed / ms / 1e9, 1),
+                  "dense_equiv_tflops": round(dense / ms / 1e9, 1)}
     return out
 
 
