@@ -62,7 +62,7 @@ def _load():
         lib.bsa_oracle_prefill.argtypes = [P, P, P, i, i, i, i, i, i, d, d, i, i, i, P, i64,
                                            P, P, P, P, P, P]
         lib.bsa_oracle_decode.argtypes = [P, P, P, i, i, i, i, i, i, i64, i64, d, d, i, i, P,
-                                          i64, P, P, P, P, P]
+                                          i64, P, i, P, P, P, P]
         lib.bsa_oracle_combine.argtypes = [P, P, i, i, i, i, P, P]
         for f in ("bsa_oracle_dense_prefill", "bsa_oracle_dense_decode", "bsa_oracle_prefill",
                   "bsa_oracle_decode", "bsa_oracle_combine", "bsa_oracle_num_threads"):
@@ -179,13 +179,15 @@ def prefill(q, k, v, scale, lam, Br=128, Bc=128, causal=True, units=None, force_
     return {"o": o, "lse": lse, "skip": skip, "margin": margin}
 
 
-def decode(q, k, v, scale, lam, Bc, n_splits, dv=None, units=None, force_skip=None):
+def decode(q, k, v, scale, lam, Bc, n_splits, dv=None, units=None, force_skip=None,
+           per_head=False):
     """Split-KV thresholded decode in fp64 (partials, before the merge).
 
     Returns ``o_part`` [B,Hq,S,dv], ``lse_part`` [B,Hq,S], ``skip`` and
     ``margin`` [B,Hkv,S,bps] with bps = ceil(n_b / S).  ``units`` are flat
     indices into [B,Hkv,S]; ``force_skip`` ([B,Hkv,S,bps]) replaces the skip
-    decisions by given ones."""
+    decisions by given ones.  ``per_head``: each query head decides for
+    itself; ``skip``, ``margin`` and ``force_skip`` are then [B,Hq,S,bps]."""
     q, k = _f32(q), _f32(k)
     B, Hq, dk = q.shape
     _, Hkv, L, kstride = k.shape
@@ -198,15 +200,16 @@ def decode(q, k, v, scale, lam, Bc, n_splits, dv=None, units=None, force_skip=No
     bps = -(-n_b // n_splits)
     o_part = np.zeros((B, Hq, n_splits, dv))
     lse_part = np.full((B, Hq, n_splits), np.nan)
-    skip = np.zeros((B, Hkv, n_splits, bps), dtype=np.uint8)
-    margin = np.full((B, Hkv, n_splits, bps), np.nan)
+    rows = Hq if per_head else Hkv
+    skip = np.zeros((B, rows, n_splits, bps), dtype=np.uint8)
+    margin = np.full((B, rows, n_splits, bps), np.nan)
     u, nu = _units(units)
     f = _forced(force_skip, skip.shape)
     rc = _load().bsa_oracle_decode(_ptr(q), _ptr(k), _ptr(vv), B, Hq, Hkv, L, dk, dv, kstride,
                                    vstride, float(scale), float(lam), Bc, n_splits,
                                    None if u is None else _ptr(u), nu,
-                                   None if f is None else _ptr(f), _ptr(o_part),
-                                   _ptr(lse_part), _ptr(skip), _ptr(margin))
+                                   None if f is None else _ptr(f), int(bool(per_head)),
+                                   _ptr(o_part), _ptr(lse_part), _ptr(skip), _ptr(margin))
     if rc:
         raise ValueError("bsa_oracle_decode: invalid arguments")
     return {"o_part": o_part, "lse_part": lse_part, "skip": skip, "margin": margin}

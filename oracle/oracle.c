@@ -293,11 +293,14 @@ int bsa_oracle_prefill(const float *q, const float *k, const float *v, int B, in
  *   o_part:[B,Hq,n_splits,dv], lse_part:[B,Hq,n_splits] (-inf for an empty split);
  *   skip, margin:[B,Hkv,n_splits,bps] with bps = ceil(n_b/n_splits), block j of split s
  *   at position j - floor(s*n_b/n_splits).
- * force_skip (NULL = none), same layout as skip: decisions to take instead of the test's. */
+ * force_skip (NULL = none), same layout as skip: decisions to take instead of the test's.
+ * per_head != 0: each query head decides for itself instead of the G heads ANDing their
+ * votes (the per-head variant of the group reading); skip, margin and force_skip are then
+ * [B,Hq,n_splits,bps]. */
 int bsa_oracle_decode(const float *q, const float *k, const float *v, int B, int Hq, int Hkv,
                       int L, int dk, int dv, int64_t k_row_stride, int64_t v_row_stride,
                       double scale, double lambda, int Bc, int n_splits, const int64_t *units,
-                      int64_t n_units, const uint8_t *force_skip, double *o_part,
+                      int64_t n_units, const uint8_t *force_skip, int per_head, double *o_part,
                       double *lse_part, uint8_t *skip, double *margin) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || L <= 0 || dk <= 0 || dv <= 0 || Bc <= 0 ||
       n_splits <= 0 || Hq % Hkv || !(lambda >= 0.0 && lambda < 1.0))
@@ -316,6 +319,37 @@ int bsa_oracle_decode(const float *q, const float *k, const float *v, int B, int
     const int j0 = (int)((int64_t)sp * n_b / n_splits);
     const int j1 = (int)((int64_t)(sp + 1) * n_b / n_splits);
     const int64_t base = ((int64_t)b * Hkv + hk) * L;
+    if (per_head) {
+      /* Each query head is its own decision unit (one row): its own skip
+       * decisions, statistic and bits, rows of skip/margin [B,Hq,n_splits,bps]. */
+      for (int g = 0; g < G; ++g) {
+        const int64_t hrow = ((int64_t)b * Hq + hk * G + g) * n_splits + sp;
+        uint8_t *skh = skip + hrow * bps;
+        double *mgh = margin + hrow * bps;
+        for (int j = 0; j < bps; ++j) { skh[j] = 0; mgh[j] = NAN; }
+        loop_state st;
+        state_init(&st, 1, Bc, dv);
+        const float *qr = q + ((int64_t)b * Hq + hk * G + g) * dk;
+        for (int j = j0; j < j1; ++j) {
+          const int c0 = j * Bc, c1 = (c0 + Bc < L) ? c0 + Bc : L, nc = c1 - c0;
+          for (int c = 0; c < nc; ++c)
+            st.s[c] = scale * dot_f32(qr, k + (base + c0 + c) * k_row_stride, dk);
+          const int forced = force_skip ? (int)force_skip[hrow * bps + (j - j0)] : -1;
+          skh[j - j0] = (uint8_t)loop_step(&st, nc, Bc, v + (base + c0) * v_row_stride,
+                                           v_row_stride, lambda, ln_lambda, forced,
+                                           &mgh[j - j0]);
+        }
+        if (j1 == j0) { /* empty split */
+          for (int e = 0; e < dv; ++e) o_part[hrow * dv + e] = 0.0;
+          lse_part[hrow] = NEG_INF;
+        } else {
+          for (int e = 0; e < dv; ++e) o_part[hrow * dv + e] = st.acc[e] / st.l[0];
+          lse_part[hrow] = st.m[0] + log(st.l[0]);
+        }
+        state_free(&st);
+      }
+      continue;
+    }
     uint8_t *sk = skip + u * bps;
     double *mg = margin + u * bps;
     for (int j = 0; j < bps; ++j) { sk[j] = 0; mg[j] = NAN; }

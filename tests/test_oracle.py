@@ -573,3 +573,50 @@ def test_block_set_output_is_softmax_over_selected_kept_tokens(lam):
     if lam > 0:  # every skipped selected block lies below ln(lambda)
         sk_ = r["skip"].astype(bool)
         assert (r["margin"][sk_] < np.log(lam)).all()
+
+
+# --------------------------------------------------------------------------
+# Per-head decode decisions (each query head of a GQA group decides alone)
+# --------------------------------------------------------------------------
+
+def _decode_kept_mask_per_head(r, cfg, n_splits):
+    """[B,Hq,L] True for tokens of the blocks each head keeps."""
+    n_b = -(-cfg.L // cfg.Bc)
+    keep = np.ones((cfg.B, cfg.Hq, n_b), dtype=bool)
+    for s in range(n_splits):
+        j0, j1 = s * n_b // n_splits, (s + 1) * n_b // n_splits
+        keep[:, :, j0:j1] = ~r["skip"][:, :, s, :j1 - j0].astype(bool)
+    return np.repeat(keep, cfg.Bc, axis=-1)[..., :cfg.L]
+
+
+def test_per_head_decode_with_one_head_per_group_is_the_group_decode():
+    cfg, q, k, v = _small_decode(Hq=4, Hkv=4, temperate=True, seed=41)
+    for lam in (0.0, 1e-2, 0.3):
+        a = oracle.decode(q, k, v, cfg.scale, lam, cfg.Bc, 4)
+        b = oracle.decode(q, k, v, cfg.scale, lam, cfg.Bc, 4, per_head=True)
+        for key in ("o_part", "lse_part", "skip", "margin"):
+            np.testing.assert_array_equal(a[key], b[key])
+
+
+@pytest.mark.parametrize("lam", [1e-3, 5e-2, 0.3])
+def test_per_head_decode_closed_form_and_group_relation(lam):
+    """Merged output of each head = softmax over the tokens that head keeps;
+    the group statistic is the max of its heads' statistics, so the group
+    skips a block exactly when every head of it skips."""
+    cfg, q, k, v = _small_decode(temperate=True, seed=42)
+    n_splits = 4
+    r = oracle.decode(q, k, v, cfg.scale, lam, cfg.Bc, n_splits, per_head=True)
+    o, lse = oracle.combine(r["o_part"], r["lse_part"])
+    s = scores_full(q[:, :, None], k, cfg.scale, False)[:, :, 0]
+    km = _decode_kept_mask_per_head(r, cfg, n_splits)
+    p_kept, lse_kept = softmax_rows(np.where(km, s, -np.inf))
+    vrep = np.repeat(v.astype(np.float64), cfg.G, axis=1)
+    np.testing.assert_allclose(o, np.einsum("bhc,bhce->bhe", p_kept, vrep), rtol=1e-10,
+                               atol=1e-11)
+    np.testing.assert_allclose(lse, lse_kept, rtol=1e-12, atol=1e-11)
+    g = oracle.decode(q, k, v, cfg.scale, lam, cfg.Bc, n_splits)
+    hm = r["margin"].reshape(cfg.B, cfg.Hkv, cfg.G, n_splits, -1)
+    np.testing.assert_array_equal(np.nanmax(hm, axis=2), g["margin"])
+    hs = r["skip"].reshape(cfg.B, cfg.Hkv, cfg.G, n_splits, -1).astype(bool)
+    np.testing.assert_array_equal(hs.all(axis=2), g["skip"].astype(bool))
+    assert hs.any(axis=2).sum() > hs.all(axis=2).sum()  # heads do disagree here
