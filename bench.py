@@ -252,6 +252,17 @@ def run_gpu(args, rank, world):
     for t in dsweep:
         dsweep[t]["speedup_vs_lambda0"] = ((dsweep["0.0"]["ms_decode"] + dsweep["0.0"]["ms_combine"])
                                           / (dsweep[t]["ms_decode"] + dsweep[t]["ms_combine"]))
+    # per-head decisions at the group's ~70 % threshold: same value bytes
+    # (a block is read when any head keeps it), more blocks left out per head
+    hbits = torch.empty(bs.decode_bitmap_shape(D.B, D.Hq, D.L, D.Bc, D.n_splits),
+                        dtype=torch.int32, device=dev)
+    durs = timed_launches(
+        lambda: bs.attn_skip_decode_per_head(dqd, dkd, dvd, ld[TARGET], D.Bc, D.n_splits,
+                                             out=(op, lpart, hbits)),
+        args.warmup, args.steps, flush, stream)
+    dsweep["per_head_" + TARGET] = {
+        "lambda": ld[TARGET], "ms_decode": statistics.mean(durs),
+        "head_sparsity": float(bs.unpack_bits(hbits, -(-n_b // D.n_splits)).float().mean())}
 
     msweep = mla_sweep(args, bs, dev, stream, flush, lam)
     calib = calibration(args, bs, dev, stream, flush, dq, dk_, dv_, dqd, dkd, lp, ld, pbits)

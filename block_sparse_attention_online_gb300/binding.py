@@ -23,7 +23,7 @@ ATTN_BF16, ATTN_F32 = 0, 1
 
 #: Every symbol include/attn_skip.h declares.
 EXPORTED = ("attn_skip_prefill", "attn_skip_prefill_blocks", "attn_skip_decode",
-            "attn_skip_decode_combine",
+            "attn_skip_decode_per_head", "attn_skip_decode_combine",
             "attn_skip_prefill_margins", "attn_skip_decode_margins", "attn_skip_sparsity_at",
             "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
             "attn_skip_lambda_for_target", "attn_skip_selftest_wait_timeout",
@@ -56,6 +56,8 @@ def load() -> ctypes.CDLL:
     lib.attn_skip_decode.argtypes = [P, P, P, i, i, i, i, i, i, i, i64, i64, f, d, i, i, P, P, P,
                                      P]
     lib.attn_skip_decode_combine.argtypes = [P, P, i, i, i, i, i, P, P, P]
+    lib.attn_skip_decode_per_head.argtypes = [P, P, P, i, i, i, i, i, i, i, i64, i64, f, d, i,
+                                              i, P, P, P, P]
     lib.attn_skip_prefill_margins.argtypes = [P, P, i, i, i, i, i, i, f, i, i, i, P, P]
     lib.attn_skip_decode_margins.argtypes = [P, P, i, i, i, i, i, i, i64, f, i, i, P, P]
     lib.attn_skip_sparsity_at.argtypes = [P, i64, d]
@@ -69,7 +71,7 @@ def load() -> ctypes.CDLL:
     lib.attn_skip_status_string.argtypes = [i]
     lib.attn_skip_status_string.restype = ctypes.c_char_p
     for fn in ("attn_skip_prefill", "attn_skip_prefill_blocks", "attn_skip_decode",
-               "attn_skip_decode_combine",
+               "attn_skip_decode_per_head", "attn_skip_decode_combine",
                "attn_skip_prefill_margins", "attn_skip_decode_margins",
                "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
                "attn_skip_selftest_wait_timeout", "attn_skip_last_device_error"):
@@ -215,6 +217,29 @@ def attn_skip_decode(q, k, v, lam, Bc=128, n_splits=8, dv=None, scale=0.0, out=N
                                  _ptr(o_part), _ptr(lse_part), _ptr(bits),
                                  _stream(stream, q.device))
     _check("attn_skip_decode", st)
+    return o_part, lse_part, bits
+
+
+def attn_skip_decode_per_head(q, k, v, lam, Bc=128, n_splits=8, scale=0.0, out=None,
+                              stream=None):
+    """Decode with per-head decisions (GQA shape): returns fp32 ``(o_part,
+    lse_part, skip_bits)`` with bits per query head [B,Hq,S,words]."""
+    _cuda_contig(q, k, v)
+    B, Hq, dk = q.shape
+    _, Hkv, L, kstride = k.shape
+    dv, vstride = v.shape[3], v.shape[3]
+    if out is None:
+        o_part = torch.empty(B, Hq, n_splits, dv, dtype=torch.float32, device=q.device)
+        lse_part = torch.empty(B, Hq, n_splits, dtype=torch.float32, device=q.device)
+        bits = torch.empty(decode_bitmap_shape(B, Hq, L, Bc, n_splits), dtype=torch.int32,
+                           device=q.device)
+    else:
+        o_part, lse_part, bits = out
+    st = load().attn_skip_decode_per_head(_ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, Hq, Hkv,
+                                          L, dk, dv, kstride, vstride, float(scale), float(lam),
+                                          Bc, n_splits, _ptr(o_part), _ptr(lse_part),
+                                          _ptr(bits), _stream(stream, q.device))
+    _check("attn_skip_decode_per_head", st)
     return o_part, lse_part, bits
 
 

@@ -119,7 +119,7 @@ attn_status decode_common(DecodeArgs &a, const void *q, const void *k, const voi
     return from_cuda(launch_decode_bf16(a, s));
   // Absorbed MLA: one latent head of 576 columns, values = its first 512 columns.
   if (dt == ATTN_BF16 && dk == 576 && dv == 512 && v == k && k_row_stride == 576 &&
-      v_row_stride == 576 && Bc == 64 && Hkv == 1 && Hq == 128)
+      v_row_stride == 576 && Bc == 64 && Hkv == 1 && Hq == 128 && !a.per_head)
     return from_cuda(launch_mla_decode(a, s));
   return ATTN_EUNSUPPORTED;
 }
@@ -178,6 +178,21 @@ extern "C" attn_status attn_skip_decode(const void *q, const void *k, const void
   if (!aligned16(o_part) || !aligned16(lse_part) || !aligned16(skip_bits)) return ATTN_EINVAL;
   DecodeArgs a{};
   a.o_part = o_part; a.lse_part = lse_part; a.bits = skip_bits;
+  return decode_common(a, q, k, v, dt, B, Hq, Hkv, L, dk, dv, k_row_stride, v_row_stride, scale,
+                       lambda, Bc, n_splits, (cudaStream_t)stream);
+}
+
+extern "C" attn_status attn_skip_decode_per_head(const void *q, const void *k, const void *v,
+                                                 attn_dtype dt, int B, int Hq, int Hkv, int L,
+                                                 int dk, int dv, int64_t k_row_stride,
+                                                 int64_t v_row_stride, float scale,
+                                                 double lambda, int Bc, int n_splits,
+                                                 float *o_part, float *lse_part,
+                                                 uint32_t *skip_bits, void *stream) {
+  if (!o_part || !lse_part || !skip_bits) return ATTN_EINVAL;
+  if (!aligned16(o_part) || !aligned16(lse_part) || !aligned16(skip_bits)) return ATTN_EINVAL;
+  DecodeArgs a{};
+  a.o_part = o_part; a.lse_part = lse_part; a.bits = skip_bits; a.per_head = 1;
   return decode_common(a, q, k, v, dt, B, Hq, Hkv, L, dk, dv, k_row_stride, v_row_stride, scale,
                        lambda, Bc, n_splits, (cudaStream_t)stream);
 }

@@ -154,6 +154,10 @@ __device__ __noinline__ void mask_tail_tmem(uint32_t sa, int lim) {
   tmem_wait_st();
 }
 
+// PH: per-head decisions (each query head decides alone; the block's values
+// are read when any head keeps it), compiled separately from the group-AND
+// kernel.
+template <bool PH>
 __global__ void __launch_bounds__(NT, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
@@ -174,7 +178,12 @@ __global__ void __launch_bounds__(NT, 1)
   const int j1 = (int)((long)(sp + 1) * a.n_b / a.n_splits);
   const int nb = j1 - j0;
   const int zkv = b * a.Hkv + hk;
-  uint32_t *bits = a.bits ? a.bits + (size_t)unit * a.words : nullptr;
+  // Bitmap words of this unit (group mode) or of head lane g (per-head mode).
+  auto bits_of = [&](int g) -> uint32_t * {
+    if (!a.bits) return nullptr;
+    return PH ? a.bits + ((size_t)(b * a.Hq + hk * G + g) * a.n_splits + sp) * a.words
+              : a.bits + (size_t)unit * a.words;
+  };
   volatile int *abort = &sh.abort;
 
   if (nb == 0) {  // empty split: no key, zero weight in the merge
@@ -186,7 +195,8 @@ __global__ void __launch_bounds__(NT, 1)
       a.o_part[row * D + idx % D] = 0.f;
       if (idx % D == 0) a.lse_part[row] = -INFINITY;
     }
-    for (int w = tid; w < a.words; w += NT) bits[w] = 0u;
+    for (int idx = tid; idx < (PH ? G : 1) * a.words; idx += NT)
+      bits_of(idx / a.words)[idx % a.words] = 0u;
     return;
   }
 
@@ -345,6 +355,7 @@ __global__ void __launch_bounds__(NT, 1)
     // ------------------------------------------------------------- softmax --
     // Lane g < G: head g's row (TMEM lane g) over the block's 128 keys.
     const bool head = lane < G;
+    uint32_t *bits = bits_of(PH ? (head ? lane : 0) : 0);
     const float sl2 = a.scale * kLog2e;   // raw score -> log2 units
     const float c2 = a.ln_lambda * kLog2e;  // ln(lambda) in log2 units
     float m2 = -INFINITY;                 // running max of the split (log2 units)
@@ -382,7 +393,10 @@ __global__ void __launch_bounds__(NT, 1)
       // With c < 0, "rowmax - m_new < c" is "rowmax - m_old < c" (a block
       // that raises the max fails both).  Every head must vote skip.
       const float diff = (mt == -INFINITY) ? -INFINITY : pm2 - m2;
-      const bool skip = a.stats_only || __all_sync(0xffffffffu, !head || diff < c2);
+      // skip_h: this head leaves the block out; skip: nobody needs its values.
+      const bool vote = !head || diff < c2;
+      const bool skip_h = a.stats_only || (PH ? vote : __all_sync(0xffffffffu, vote));
+      const bool skip = PH ? __all_sync(0xffffffffu, skip_h) : skip_h;
       if (a.margin) {
         // The block statistic: max over the heads of rowmax - m_new, where
         // rowmax - m_new = min(rowmax - m_old, 0) (log2 units).
@@ -398,7 +412,9 @@ __global__ void __launch_bounds__(NT, 1)
           sh.dec[j % NDEC] = skip ? 0 : 1;
           mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
         }
-        if (skip) word |= 1u << (j & 31);
+      }
+      if (PH ? head : lane == 0) {
+        if (skip_h) word |= 1u << (j & 31);
         if (!a.stats_only && ((j & 31) == 31 || j == nb - 1)) {
           bits[j >> 5] = word;
           word = 0;
@@ -411,12 +427,14 @@ __global__ void __launch_bounds__(NT, 1)
       if (skip) continue;
       bool rescale = false;
       float alpha = 1.f;
-      if (mref == -INFINITY) {
-        mref = mnew;
-      } else if (mnew > mref + kRescaleLog2) {
-        alpha = ex2(mref - mnew);
-        mref = mnew;
-        rescale = true;
+      if (!skip_h) {  // (per-head mode: a head that leaves the block out keeps its state)
+        if (mref == -INFINITY) {
+          mref = mnew;
+        } else if (mnew > mref + kRescaleLog2) {
+          alpha = ex2(mref - mnew);
+          mref = mnew;
+          rescale = true;
+        }
       }
       const int pb = kc % NP;
       // P buffer pb last fed the P.V of kept block kc - NP.
@@ -427,7 +445,9 @@ __global__ void __launch_bounds__(NT, 1)
       }
       fence_after_sync();
       const uint32_t pa = tmem + TMEM_P + pb * (BC / 2);
-      const uint64_t sl2x2 = f2(sl2, sl2), negref2 = f2(-mref, -mref);
+      // A head that leaves the block out gets P = exp2(-inf) = 0 on its row.
+      const float nref = skip_h ? -INFINITY : -mref;
+      const uint64_t sl2x2 = f2(sl2, sl2), negref2 = f2(nref, nref);
       uint64_t acc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
       {
         uint32_t pk[32];
@@ -470,9 +490,11 @@ __global__ void __launch_bounds__(NT, 1)
     }
 
     // ---- epilogue: O_s = O / l and LSE_s = ref + ln l per head ---------------
-    if (lane == 0) {
+    if (PH ? head : lane == 0) {
       if (!a.stats_only)
         for (int w = ((nb - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
+    }
+    if (lane == 0) {
       if (a.margin)
         for (int j = nb; j < a.bps; ++j) a.margin[(size_t)unit * a.bps + j] = NAN;
     }
@@ -521,11 +543,12 @@ cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s) {
   if (!make_map_bf16_3d(&mk, a.k, D, a.k_row_stride, a.L, a.B * a.Hkv, BC) ||
       !make_map_bf16_3d(&mv, a.v, D, a.v_row_stride, a.L, a.B * a.Hkv, BC))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  auto kernel = a.per_head ? decode_tc_kernel<true> : decode_tc_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   const long units = (long)a.B * a.Hkv * a.n_splits;
-  decode_tc_kernel<<<(unsigned)units, NT, SMEM_ALLOC, s>>>(mk, mv, a);
+  kernel<<<(unsigned)units, NT, SMEM_ALLOC, s>>>(mk, mv, a);
   return cudaGetLastError();
 }
 

@@ -46,6 +46,9 @@ struct DecodeArgs {
   // block); every block is treated as skipped; o_part, lse_part, bits unused.
   float *margin;
   int stats_only;
+  // Per-head decisions: bits [B,Hq,n_splits,words], each query head decides
+  // for itself (the GQA kernel only).
+  int per_head;
 };
 
 struct CombineArgs {

@@ -140,6 +140,27 @@ attn_status attn_skip_decode(const void *q, const void *k, const void *v, attn_d
                              void *stream);
 
 /*
+ * Split-KV decode with per-head decisions: each of the G query heads sharing a
+ * KV head takes Eq. 5 for itself (a block it skips adds nothing to its
+ * output), instead of the group skipping a block only when all G agree.  A
+ * block's values are read when any head of the group keeps it, so the bytes
+ * read equal the group-AND call's; only each head's approximation changes.
+ * For G = 1 the two calls coincide.
+ *
+ *  skip_bits  [B, Hq, n_splits, ceil(bps/32)] uint32: per query head
+ *  other arguments and outputs as for attn_skip_decode.
+ *
+ * Kernels built: the GQA shape of attn_skip_decode (dt = ATTN_BF16, dk = dv =
+ * 128, Bc = 128, G in {1, 2, 4, 8}, row strides 128); anything else returns
+ * ATTN_EUNSUPPORTED.
+ */
+attn_status attn_skip_decode_per_head(const void *q, const void *k, const void *v, attn_dtype dt,
+                                      int B, int Hq, int Hkv, int L, int dk, int dv,
+                                      int64_t k_row_stride, int64_t v_row_stride, float scale,
+                                      double lambda, int Bc, int n_splits, float *o_part,
+                                      float *lse_part, uint32_t *skip_bits, void *stream);
+
+/*
  * Merge of decode split partials by log-sum-exp (FlashDecoding):
  * LSE = ln sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) * O_s.
  * Splits with LSE_s = -inf weigh zero.

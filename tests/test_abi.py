@@ -88,6 +88,16 @@ def test_prefill_blocks_rejects_invalid_arguments(lib, kw):
     assert _prefill_blocks(lib, **kw) == bs.ATTN_EINVAL
 
 
+def test_decode_per_head_rejects_invalid_arguments(lib):
+    f = lib.attn_skip_decode_per_head
+    base = [FAKE, FAKE, FAKE, 0, 2, 8, 2, 1024, 128, 128, 128, 128, 0.0, 0.01, 128, 4, FAKE, FAKE,
+            FAKE, None]
+    for i, bad in ((0, None), (16, None), (18, None), (4, 0), (13, 1.0), (15, 0)):
+        args = list(base)
+        args[i] = bad
+        assert f(*args) == bs.ATTN_EINVAL
+
+
 def _prefill_margins(lib, **kw):
     a = dict(q=FAKE, k=FAKE, dt=0, B=1, Hq=4, Hkv=2, T=256, dk=128, scale=0.0, Br=128, Bc=128,
              causal=1, m=FAKE, stream=None)
