@@ -33,7 +33,7 @@ from dataclasses import dataclass, replace
 
 import torch
 
-_TAGS = {"u": 1, "sal": 2, "k": 3, "v": 4, "q": 5, "w": 6}
+_TAGS = {"u": 1, "sal": 2, "k": 3, "v": 4, "q": 5, "w": 6, "santa": 7}
 
 
 def _gen(seed: int, tag: str, b: int, h: int) -> torch.Generator:
@@ -240,6 +240,21 @@ def decode_inputs(cfg: DecodeConfig, batches=None):
     with ThreadPoolExecutor(_threads()) as ex:
         list(ex.map(one, jobs))
     return q, k, v
+
+
+def santa_offsets(cfg: DecodeConfig, n_samples: int, mode: str, seed: int = 0) -> torch.Tensor:
+    """Uniform draws in [0, 1) for the sampled decode (fp32, one generator per
+    (sequence, query head)): ``[B, Hq]`` for the systematic sampler (one
+    offset per head), ``[B, Hq, n_samples]`` for the stratified and i.i.d.
+    samplers (one draw per sample).  ``seed`` selects another draw of the same
+    workload (a new decode step)."""
+    per = 1 if mode == "sys" else int(n_samples)
+    u = torch.empty(cfg.B, cfg.Hq, per, dtype=torch.float32)
+    for b in range(cfg.B):
+        for h in range(cfg.Hq):
+            u[b, h] = torch.rand(per, generator=_gen(cfg.seed + 7919 * seed, "santa", b, h),
+                                 dtype=torch.float32)
+    return u[:, :, 0].contiguous() if mode == "sys" else u
 
 
 def temperate(cfg):

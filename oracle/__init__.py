@@ -20,6 +20,13 @@ Parity status of each function (what pins it, in ``tests/test_oracle.py``):
   ``tests/golden/``; brute-force recomputation of each skip bit.
 * ``combine``: lambda = 0 merged decode equals dense single-pass attention;
   one split is the identity.
+* ``santa_decode`` (the page "Stochastic Sparse Attention for Memory-Bound
+  Inference", section "关键设计"): the closed form of equal scores (every
+  sample index and gap known exactly); a dominant key takes every sample; the
+  systematic sampler picks each key floor(S p_i) or ceil(S p_i) times and its
+  stratified form keeps sample m inside stratum m; the mean over a fine grid
+  of offsets, and the mean over many i.i.d. or stratified draws, equal dense
+  attention (unbiasedness).
 """
 from __future__ import annotations
 
@@ -64,8 +71,11 @@ def _load():
         lib.bsa_oracle_decode.argtypes = [P, P, P, i, i, i, i, i, i, i64, i64, d, d, i, i, P,
                                           i64, P, i, P, P, P, P]
         lib.bsa_oracle_combine.argtypes = [P, P, i, i, i, i, P, P]
+        lib.bsa_oracle_santa_decode.argtypes = [P, P, P, i, i, i, i, i, i, i64, i64, d, i, i, P,
+                                                P, P, P, P]
         for f in ("bsa_oracle_dense_prefill", "bsa_oracle_dense_decode", "bsa_oracle_prefill",
-                  "bsa_oracle_decode", "bsa_oracle_combine", "bsa_oracle_num_threads"):
+                  "bsa_oracle_decode", "bsa_oracle_combine", "bsa_oracle_num_threads",
+                  "bsa_oracle_santa_decode"):
             getattr(lib, f).restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -226,6 +236,45 @@ def combine(o_part, lse_part):
     if rc:
         raise ValueError("bsa_oracle_combine: invalid arguments")
     return o, lse
+
+
+SANTA_MODES = {"iid": 0, "sys": 1, "strat": 2}
+
+
+def santa_decode(q, k, v, scale, n_samples, mode, u, with_cdf=False):
+    """Sampled decode output (SANTA estimator) in fp64.
+
+    q [B,Hq,dk]; k [B,Hkv,L,dk]; v [B,Hkv,L,dv].  ``mode`` is ``"iid"``
+    (thresholds T_m = u[b,h,m]), ``"sys"`` (T_m = (m + u[b,h]) / S) or
+    ``"strat"`` (T_m = (m + u[b,h,m]) / S); every u lies in [0, 1).  Returns
+    ``y`` [B,Hq,dv] (mean of the sampled value rows), ``idx`` [B,Hq,S] (int32
+    sample indices), ``gap`` [B,Hq,S] (distance of each threshold from the
+    nearer end of its key's CDF interval) and, with ``with_cdf``, ``cdf``
+    [B,Hq,L]."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, Hq, dk = q.shape
+    _, Hkv, L, kstride = k.shape
+    dv, vstride = v.shape[3], v.shape[3]
+    S = int(n_samples)
+    md = SANTA_MODES[mode]
+    uu = _f32(u)
+    want = (B, Hq) if md == 1 else (B, Hq, S)
+    if uu.shape != want:
+        raise ValueError(f"u has shape {uu.shape}, expected {want}")
+    y = np.zeros((B, Hq, dv))
+    idx = np.zeros((B, Hq, S), dtype=np.int32)
+    gap = np.zeros((B, Hq, S))
+    cdf = np.zeros((B, Hq, L)) if with_cdf else None
+    rc = _load().bsa_oracle_santa_decode(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, L, dk, dv,
+                                         kstride, vstride, float(scale), S, md, _ptr(uu),
+                                         _ptr(y), _ptr(idx), _ptr(gap),
+                                         None if cdf is None else _ptr(cdf))
+    if rc:
+        raise ValueError("bsa_oracle_santa_decode: invalid arguments")
+    out = {"y": y, "idx": idx, "gap": gap}
+    if with_cdf:
+        out["cdf"] = cdf
+    return out
 
 
 def ln_lambda(lam: float) -> float:

@@ -12,6 +12,9 @@
  *   "判定本身：几乎零成本的秘密"            -- a tile skips only when all its rows agree;
  *   "Decode 内核：砍带宽"                   -- decode skips the value load of a skipped block;
  * and FlashDecoding's split-KV merge (the SANTA page, "FlashDecoding" baseline).
+ * The sampled decode output at the end of this file follows the web page
+ * "Stochastic Sparse Attention for Memory-Bound Inference" (SANTA), section
+ * "关键设计" (the unbiased estimator and its stratified / systematic forms).
  *
  * Arithmetic: every input is an fp32 array holding exactly the values the GPU
  * reads (bf16 inputs are widened exactly); all arithmetic is fp64, in the
@@ -403,6 +406,101 @@ int bsa_oracle_combine(const double *o_part, const double *lse_part, int B, int 
       for (int e = 0; e < dv; ++e) orow[e] += w * op[e];
     }
     lse[idx] = LSE;
+  }
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Sampled attention output for one decode token: the web page "Stochastic   */
+/* Sparse Attention for Memory-Bound Inference" (SANTA), section "关键设计",  */
+/* items "SANTA 无偏估计 + Stratified/Systematic 降方差" and "S²ANTA-prop"    */
+/* (the sampling that the kernel's second pass carries out).                */
+/*                                                                          */
+/* The attention weights of a query over its L keys form a categorical      */
+/* distribution p_i = exp(s_i - M) / Z.  With the cumulative weights         */
+/* W_i = sum_{j<=i} exp(s_j - M) (so W_{L-1} = Z), the inverse CDF of a      */
+/* threshold T in [0, 1) is the smallest i with W_i > T * Z.  The estimate   */
+/* of p V is the mean of the S value rows V_{J_m}, J_m the inverse CDF of   */
+/* threshold T_m:                                                           */
+/*   mode 0 (SANTA, i.i.d.):      T_m = u[b,h,m]                            */
+/*   mode 1 (S²ANTA-sys):         T_m = (m + u[b,h]) / S   (one offset; the  */
+/*                                page's U ~ Unif[0,1/S) is u / S)           */
+/*   mode 2 (S²ANTA-strat):       T_m = (m + u[b,h,m]) / S (one uniform     */
+/*                                draw inside each of the S equal-mass strata)*/
+/* with every u in [0, 1).  Outputs: y [B,Hq,dv] = (1/S) sum_m V_{J_m};      */
+/* idx [B,Hq,S] = J_m; gap [B,Hq,S] = the distance, in probability units,   */
+/* from T_m to the nearer end of J_m's interval [W_{J-1}, W_J) / Z; and,     */
+/* when cdf is not NULL, cdf [B,Hq,L] = W_i / Z.                             */
+/* A threshold that rounds to T*Z >= Z (possible only within rounding of 1) */
+/* takes the last key of positive weight.                                   */
+/* Returns -1 on invalid shapes, mode, or a u outside [0, 1).               */
+/* ------------------------------------------------------------------------ */
+static int64_t first_above(const double *W, int64_t n, double R, int strict) {
+  /* Bisection for the smallest i in [0, n) with W_i > R (strict) or W_i >= R;
+   * W is nondecreasing.  Returns n when no element qualifies. */
+  int64_t lo = 0, hi = n;
+  while (lo < hi) {
+    const int64_t mid = lo + (hi - lo) / 2;
+    const int ok = strict ? (W[mid] > R) : (W[mid] >= R);
+    if (ok) hi = mid; else lo = mid + 1;
+  }
+  return lo;
+}
+
+int bsa_oracle_santa_decode(const float *q, const float *k, const float *v, int B, int Hq,
+                            int Hkv, int L, int dk, int dv, int64_t k_row_stride,
+                            int64_t v_row_stride, double scale, int S, int mode,
+                            const float *u, double *y, int32_t *idx, double *gap, double *cdf) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || L <= 0 || dk <= 0 || dv <= 0 || Hq % Hkv || S <= 0)
+    return -1;
+  if (mode < 0 || mode > 2 || !u) return -1;
+  const int64_t n_u = (int64_t)B * Hq * (mode == 1 ? 1 : S);
+  for (int64_t i = 0; i < n_u; ++i)
+    if (!(u[i] >= 0.0f && u[i] < 1.0f)) return -1;
+  const int G = Hq / Hkv;
+#pragma omp parallel
+  {
+    double *W = (double *)malloc(sizeof(double) * (size_t)L);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t bh = 0; bh < (int64_t)B * Hq; ++bh) {
+      const int h = (int)(bh % Hq), b = (int)(bh / Hq), hk = h / G;
+      const float *qr = q + bh * dk;
+      const int64_t base = ((int64_t)b * Hkv + hk) * L;
+      /* Scores s_i, then W_i = running sum of exp(s_i - M) in key order. */
+      double M = NEG_INF;
+      for (int c = 0; c < L; ++c) {
+        W[c] = scale * dot_f32(qr, k + (base + c) * k_row_stride, dk);
+        if (W[c] > M) M = W[c];
+      }
+      double run = 0.0;
+      for (int c = 0; c < L; ++c) {
+        run += exp(W[c] - M);
+        W[c] = run;
+      }
+      const double Z = run;
+      if (cdf)
+        for (int c = 0; c < L; ++c) cdf[bh * L + c] = W[c] / Z;
+      double *yr = y + bh * dv;
+      for (int e = 0; e < dv; ++e) yr[e] = 0.0;
+      for (int m = 0; m < S; ++m) {
+        double T;
+        if (mode == 0) T = (double)u[bh * S + m];
+        else if (mode == 1) T = ((double)m + (double)u[bh]) / S;
+        else T = ((double)m + (double)u[bh * S + m]) / S;
+        const double R = T * Z;
+        int64_t J = first_above(W, L, R, 1);
+        if (J == L) J = first_above(W, L, Z, 0); /* R rounded up to Z */
+        const double lo = J > 0 ? W[J - 1] : 0.0, hi = W[J];
+        double g = fmin(hi - R, R - lo) / Z;
+        if (g < 0.0) g = 0.0;
+        idx[bh * S + m] = (int32_t)J;
+        gap[bh * S + m] = g;
+        const float *vr = v + (base + J) * v_row_stride;
+        for (int e = 0; e < dv; ++e) yr[e] += (double)vr[e];
+      }
+      for (int e = 0; e < dv; ++e) yr[e] /= S;
+    }
+    free(W);
   }
   return 0;
 }
