@@ -27,7 +27,11 @@ EXPORTED = ("attn_skip_prefill", "attn_skip_prefill_blocks", "attn_skip_decode",
             "attn_skip_prefill_margins", "attn_skip_decode_margins", "attn_skip_sparsity_at",
             "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
             "attn_skip_lambda_for_target", "attn_skip_selftest_wait_timeout",
-            "attn_skip_last_device_error", "attn_skip_status_string")
+            "attn_skip_last_device_error", "attn_skip_status_string",
+            "attn_skip_santa_workspace", "attn_skip_santa_decode")
+
+#: Samplers of attn_skip_santa_decode.
+SANTA_MODES = {"iid": 0, "sys": 1, "strat": 2}
 
 
 class AttnSkipError(RuntimeError):
@@ -68,13 +72,17 @@ def load() -> ctypes.CDLL:
     lib.attn_skip_lambda_for_target.restype = d
     lib.attn_skip_last_device_error.argtypes = [P]
     lib.attn_skip_selftest_wait_timeout.argtypes = [P]
+    lib.attn_skip_santa_workspace.argtypes = [i, i, i, i, P, P]
+    lib.attn_skip_santa_decode.argtypes = [P, P, P, i, i, i, i, i, i, i, i64, i64, f, i, i, P, i,
+                                           P, P, i, P, P, P]
     lib.attn_skip_status_string.argtypes = [i]
     lib.attn_skip_status_string.restype = ctypes.c_char_p
     for fn in ("attn_skip_prefill", "attn_skip_prefill_blocks", "attn_skip_decode",
                "attn_skip_decode_per_head", "attn_skip_decode_combine",
                "attn_skip_prefill_margins", "attn_skip_decode_margins",
                "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
-               "attn_skip_selftest_wait_timeout", "attn_skip_last_device_error"):
+               "attn_skip_selftest_wait_timeout", "attn_skip_last_device_error",
+               "attn_skip_santa_workspace", "attn_skip_santa_decode"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -345,6 +353,48 @@ def attn_skip_lambda_for_target(alpha, beta, sparsity, L):
     """lambda = alpha * exp(beta * S) / L, capped below 1."""
     return load().attn_skip_lambda_for_target(float(alpha), float(beta), float(sparsity),
                                               float(L))
+
+
+def attn_skip_santa_workspace(B, Hq, L, n_tiles):
+    """Sizes, in floats, of the score stash and the tile statistics."""
+    a, b = ctypes.c_size_t(), ctypes.c_size_t()
+    _check("attn_skip_santa_workspace",
+           load().attn_skip_santa_workspace(int(B), int(Hq), int(L), int(n_tiles),
+                                            ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def attn_skip_santa_decode(q, k, v, n_samples, mode, u, n_tiles=16, scale=0.0,
+                           out_dtype=torch.float32, with_idx=False, workspace=None, out=None,
+                           stream=None):
+    """Sampled decode output (SANTA estimator).  q [B,Hq,128], k/v
+    [B,Hkv,L,128] bf16; ``mode`` ``"sys"`` (u [B,Hq]) or ``"strat"`` (u
+    [B,Hq,S]), u fp32 in [0, 1) on the device.  Returns ``o`` [B,Hq,128] and,
+    with ``with_idx``, the int32 sample indices [B,Hq,S].  ``workspace`` is
+    an optional ``(scores, tile_stats)`` pair of fp32 device tensors of the
+    sizes attn_skip_santa_workspace gives."""
+    _cuda_contig(q, k, v, u)
+    B, Hq, dk = q.shape
+    _, Hkv, L, kstride = k.shape
+    dv, vstride = v.shape[3], v.shape[3]
+    if u.dtype != torch.float32:
+        raise TypeError("u must be float32")
+    if workspace is None:
+        ns, nt = attn_skip_santa_workspace(B, Hq, L, n_tiles)
+        workspace = (torch.empty(ns, dtype=torch.float32, device=q.device),
+                     torch.empty(nt, dtype=torch.float32, device=q.device))
+    scores, stats = workspace
+    _cuda_contig(scores, stats)
+    o = out if out is not None else torch.empty(B, Hq, dv, dtype=out_dtype, device=q.device)
+    idx = (torch.empty(B, Hq, int(n_samples), dtype=torch.int32, device=q.device)
+           if with_idx else None)
+    st = load().attn_skip_santa_decode(
+        _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, Hq, Hkv, L, dk, dv, kstride, vstride,
+        float(scale), int(n_samples), SANTA_MODES[mode], _ptr(u), int(n_tiles), _ptr(scores),
+        _ptr(stats), _dtype_code(o), _ptr(o), None if idx is None else _ptr(idx),
+        _stream(stream, q.device))
+    _check("attn_skip_santa_decode", st)
+    return (o, idx) if with_idx else o
 
 
 def attn_skip_selftest_wait_timeout(stream=None, device=None):

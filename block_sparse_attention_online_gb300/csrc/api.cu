@@ -227,6 +227,57 @@ extern "C" attn_status attn_skip_decode_combine(const float *o_part, const float
   return from_cuda(launch_combine(a, (cudaStream_t)stream));
 }
 
+extern "C" attn_status attn_skip_santa_workspace(int B, int Hq, int L, int n_tiles,
+                                                 size_t *scores_floats, size_t *stats_floats) {
+  if (B <= 0 || Hq <= 0 || L <= 0 || n_tiles <= 0 || !scores_floats || !stats_floats)
+    return ATTN_EINVAL;
+  const size_t n_b = ((size_t)L + 127) / 128;
+  *scores_floats = (size_t)B * Hq * n_b * 128;
+  *stats_floats = (size_t)B * Hq * n_tiles * 2;
+  return ATTN_OK;
+}
+
+extern "C" attn_status attn_skip_santa_decode(const void *q, const void *k, const void *v,
+                                              attn_dtype dt, int B, int Hq, int Hkv, int L, int dk,
+                                              int dv, int64_t k_row_stride, int64_t v_row_stride,
+                                              float scale, int n_samples, attn_santa_mode mode,
+                                              const float *u, int n_tiles, float *scores,
+                                              float *tile_stats, attn_dtype out_dt, void *o,
+                                              int32_t *idx, void *stream) {
+  if (!q || !k || !v || !u || !scores || !tile_stats || !o) return ATTN_EINVAL;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || L <= 0 || dk <= 0 || dv <= 0 || n_samples <= 0 ||
+      n_tiles <= 0)
+    return ATTN_EINVAL;
+  if (Hq % Hkv != 0 || !(scale == scale) || k_row_stride < dk || v_row_stride < dv)
+    return ATTN_EINVAL;
+  if (mode != ATTN_SANTA_IID && mode != ATTN_SANTA_SYS && mode != ATTN_SANTA_STRAT)
+    return ATTN_EINVAL;
+  if ((dt != ATTN_BF16 && dt != ATTN_F32) || (out_dt != ATTN_BF16 && out_dt != ATTN_F32))
+    return ATTN_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(u) || !aligned16(scores) ||
+      !aligned16(tile_stats) || !aligned16(o) || (idx && !aligned16(idx)))
+    return ATTN_EINVAL;
+  const int G = Hq / Hkv;
+  const long n_b = (L + 127L) / 128;
+  const long bps = (n_b + n_tiles - 1) / n_tiles;
+  if (dt != ATTN_BF16 || dk != 128 || dv != 128 || k_row_stride != 128 || v_row_stride != 128 ||
+      !(G == 1 || G == 2 || G == 4 || G == 8) || mode == ATTN_SANTA_IID)
+    return ATTN_EUNSUPPORTED;
+  if (n_samples > 2048 || n_tiles > 1024 || bps > 16 || (long)B * Hkv * n_tiles > 0x7fffffffL ||
+      (long)B * Hq > 0x7fffffffL)
+    return ATTN_EUNSUPPORTED;
+  if (santa_sample_smem_bytes(n_tiles, n_samples, (int)bps) > 200 * 1024) return ATTN_EUNSUPPORTED;
+  SantaArgs a{};
+  a.q = q; a.k = k; a.v = v; a.u = u; a.scores = scores; a.tile_stats = tile_stats;
+  a.o = o; a.idx = idx;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.L = L; a.n_b = (int)n_b; a.n_tiles = n_tiles;
+  a.bps = (int)bps; a.S = n_samples; a.mode = (int)mode; a.out_bf16 = out_dt == ATTN_BF16;
+  a.scale = scale > 0.f ? scale : (float)(1.0 / sqrt((double)dk));
+  cudaError_t e = error_word(&a.err);
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(launch_santa_decode(a, (cudaStream_t)stream));
+}
+
 extern "C" attn_status attn_skip_selftest_wait_timeout(void *stream) {
   unsigned *err = nullptr;
   cudaError_t e = error_word(&err);

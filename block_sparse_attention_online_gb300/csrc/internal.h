@@ -51,6 +51,21 @@ struct DecodeArgs {
   int per_head;
 };
 
+// Sampled decode output (SANTA estimator).
+enum : int { kSantaIid = 0, kSantaSys = 1, kSantaStrat = 2 };
+
+struct SantaArgs {
+  const void *q, *k, *v;     // bf16 [B,Hq,128], [B,Hkv,L,128], [B,Hkv,L,128]
+  const float *u;            // [B,Hq] (systematic) or [B,Hq,S] (stratified), in [0,1)
+  float *scores;             // [B,Hq,n_b*128] stash: log2-scaled scores, -inf past L
+  float *tile_stats;         // [B,Hq,n_tiles] (max, sum) pairs
+  void *o;                   // [B,Hq,128] fp32 or bf16
+  int32_t *idx;              // [B,Hq,S] sample indices, or null
+  int B, Hq, Hkv, L, n_b, n_tiles, bps, S, mode, out_bf16;
+  float scale;
+  unsigned *err;
+};
+
 struct CombineArgs {
   const float *o_part, *lse_part;
   void *o;
@@ -65,5 +80,7 @@ cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 cudaError_t launch_selftest_wait(unsigned *err, cudaStream_t s);
+cudaError_t launch_santa_decode(const SantaArgs &a, cudaStream_t s);
+size_t santa_sample_smem_bytes(int n_tiles, int S, int bps);
 
 }  // namespace attn_skip

@@ -140,6 +140,14 @@ MLA_DECODE_16K = DecodeConfig("mla_decode_bf16_B32_L16384", 32, 128, 1, 16384, 5
 CONFIGS = {c.name: c for c in (TINY_PREFILL, GQA_PREFILL_16K, GQA_DECODE_32K, GQA_PREFILL_64K,
                                 MLA_DECODE_16K)}
 
+# The same decode shape with weak salience (sink 1.2, salient keys 0.6): each
+# head's attention spreads over hundreds of keys (the top key holds 5-65 % of
+# the mass, 90 % of it sits on ~150-400 keys), the regime in which sampling
+# the value rows is worth doing.  With the default salience the sink holds all
+# but e^-30 of the mass and every sample lands on it.
+SANTA_DECODE_32K = GQA_DECODE_32K.with_(name="santa_decode_bf16_B16_L32768", sink_a=1.2,
+                                        salient_a=0.6, seed=1239)
+
 
 def _unit_u(seed: int, b: int, hk: int, d: int) -> torch.Tensor:
     u = torch.randn(d, generator=_gen(seed, "u", b, hk), dtype=torch.float64)

@@ -42,6 +42,7 @@
 #ifndef ATTN_SKIP_H
 #define ATTN_SKIP_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -57,6 +58,13 @@ typedef enum {
 } attn_status;
 
 typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
+
+/* Samplers of the sampled decode output (attn_skip_santa_decode). */
+typedef enum {
+  ATTN_SANTA_IID = 0,   /* S independent draws from the attention weights        */
+  ATTN_SANTA_SYS = 1,   /* one offset, S equally spaced thresholds (systematic)  */
+  ATTN_SANTA_STRAT = 2  /* one draw inside each of S equal-mass strata           */
+} attn_santa_mode;
 
 /*
  * Causal (or full) GQA prefill with block skipping.
@@ -235,6 +243,64 @@ attn_status attn_skip_lambda_for_sparsity(const float *margin, int64_t n, double
 attn_status attn_skip_fit_lambda_model(const double *L, const double *sparsity,
                                        const double *lambda, int n, double *alpha, double *beta);
 double attn_skip_lambda_for_target(double alpha, double beta, double sparsity, double L);
+
+/*
+ * Sampled decode output: the web page "Stochastic Sparse Attention for
+ * Memory-Bound Inference" (SANTA), section "关键设计".  The softmax weights
+ * p_i of a decode query over its L keys form a categorical distribution; with
+ * the cumulative weights F_i = p_0 + ... + p_i, the inverse CDF of a threshold
+ * T in [0, 1) is the smallest i with F_i > T, and
+ *
+ *     o = (1/S) * sum_{m<S} V[J_m],   J_m = inverse CDF of T_m,
+ *
+ * is an unbiased estimate of sum_i p_i V_i that reads S value rows instead of
+ * L.  Thresholds ("SANTA 无偏估计 + Stratified/Systematic 降方差"):
+ *   ATTN_SANTA_SYS:    T_m = (m + u[b,h]) / S     (the page's offset U ~
+ *                      Unif[0, 1/S) is u / S; one draw per head)
+ *   ATTN_SANTA_STRAT:  T_m = (m + u[b,h,m]) / S  (one draw per stratum)
+ *   ATTN_SANTA_IID:    T_m = u[b,h,m]            (declared for completeness;
+ *                      no kernel: ATTN_EUNSUPPORTED)
+ * The caller draws u (uniform in [0, 1)); a value outside [0, 1) still yields
+ * an in-range key index, but not the estimator.
+ *
+ * Schedule (item "S²ANTA-prop"): pass 1 streams the keys once per KV head and
+ * writes every key's score (log2-scaled, fp32) to the `scores` stash and one
+ * (max, sum of 2^(score - max)) pair per key tile and query head to
+ * `tile_stats`; pass 2, per query head, turns the tile sums into the CDF at
+ * the tile boundaries, gives each tile the thresholds that fall inside it,
+ * places them on keys with the tile's running sum, and gathers the sampled
+ * value rows.  A tile that receives no threshold costs no value read and no
+ * second read of its scores.  Tile t holds the 128-key blocks
+ * [floor(t*n_b/n_tiles), floor((t+1)*n_b/n_tiles)), n_b = ceil(L/128).
+ *
+ *  q           [B, Hq, dk]              bf16 (device)
+ *  k, v        [B, Hkv, L, 128]         bf16 (device), row strides 128
+ *  u           [B, Hq] (SYS) or [B, Hq, S] (STRAT) fp32 (device)
+ *  scores      [B, Hq, n_b * 128] fp32  (device, caller-owned workspace;
+ *              keys past L hold -inf)
+ *  tile_stats  [B, Hq, n_tiles, 2] fp32 (device, caller-owned workspace)
+ *  o           [B, Hq, 128]             out_dt (device)
+ *  idx         [B, Hq, S] int32         sample indices J_m (device) or NULL
+ * Index decisions are taken in fp32: a threshold within rounding of a CDF
+ * boundary may land on either neighbour.
+ *
+ * Kernels built: dt = ATTN_BF16, dk = dv = 128, row strides 128, G = Hq/Hkv
+ * in {1, 2, 4, 8}, S <= 2048, n_tiles <= 1024, at most 16 blocks (2048 keys)
+ * per tile; other valid combinations return ATTN_EUNSUPPORTED.  EINVAL for a
+ * null required pointer, a non-positive size or count, Hq % Hkv != 0, a
+ * stride below the head size, an unknown mode or dtype, or a misaligned
+ * pointer.  Both workspaces are fully written before they are read.
+ *
+ * attn_skip_santa_workspace: the two workspace sizes, in floats.
+ */
+attn_status attn_skip_santa_workspace(int B, int Hq, int L, int n_tiles, size_t *scores_floats,
+                                      size_t *stats_floats);
+attn_status attn_skip_santa_decode(const void *q, const void *k, const void *v, attn_dtype dt,
+                                   int B, int Hq, int Hkv, int L, int dk, int dv,
+                                   int64_t k_row_stride, int64_t v_row_stride, float scale,
+                                   int n_samples, attn_santa_mode mode, const float *u,
+                                   int n_tiles, float *scores, float *tile_stats,
+                                   attn_dtype out_dt, void *o, int32_t *idx, void *stream);
 
 /*
  * Diagnostic: launches one small CTA that allocates TMEM and then waits, with

@@ -147,3 +147,36 @@ def test_unpack_bits_roundtrip():
     u = bs.unpack_bits(w, 40)
     assert u[0, :4].tolist() == [True, True, False, True]
     assert u[0, 4:32].sum() == 0 and u[0, 32:40].all()
+
+
+def _santa(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, dt=0, B=2, Hq=8, Hkv=2, L=4096, dk=128, dv=128, ks=128,
+             vs=128, scale=0.0, S=128, mode=1, u=FAKE, T=4, scores=FAKE, stats=FAKE, odt=1,
+             o=FAKE, idx=None, stream=None)
+    a.update(kw)
+    return lib.attn_skip_santa_decode(*a.values())
+
+
+@pytest.mark.parametrize("kw", [
+    dict(q=None), dict(u=None), dict(scores=None), dict(stats=None), dict(o=None), dict(B=0),
+    dict(L=0), dict(S=0), dict(T=0), dict(Hq=6, Hkv=4), dict(mode=3), dict(mode=-1),
+    dict(odt=9), dict(dt=4), dict(ks=64), dict(scale=float("nan")),
+    dict(u=ctypes.c_void_p(0x10004)), dict(idx=ctypes.c_void_p(0x10008)),
+])
+def test_santa_rejects_invalid_arguments(lib, kw):
+    assert _santa(lib, **kw) == bs.ATTN_EINVAL
+
+
+@pytest.mark.parametrize("kw", [
+    dict(mode=0), dict(dk=64, ks=64), dict(dt=1), dict(S=4096), dict(L=32768, T=8),
+    dict(Hq=6, Hkv=2), dict(T=2000),
+])
+def test_santa_unsupported_shapes(lib, kw):
+    assert _santa(lib, **kw) == bs.ATTN_EUNSUPPORTED
+
+
+def test_santa_workspace_sizes(lib):
+    assert bs.attn_skip_santa_workspace(16, 32, 32768, 16) == (16 * 32 * 32768, 16 * 32 * 16 * 2)
+    assert bs.attn_skip_santa_workspace(1, 1, 1, 1) == (128, 2)
+    with pytest.raises(bs.AttnSkipError):
+        bs.attn_skip_santa_workspace(1, 0, 10, 1)
