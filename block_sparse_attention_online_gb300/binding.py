@@ -28,7 +28,8 @@ EXPORTED = ("attn_skip_prefill", "attn_skip_prefill_blocks", "attn_skip_decode",
             "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
             "attn_skip_lambda_for_target", "attn_skip_selftest_wait_timeout",
             "attn_skip_last_device_error", "attn_skip_status_string",
-            "attn_skip_santa_workspace", "attn_skip_santa_decode")
+            "attn_skip_santa_workspace", "attn_skip_santa_decode",
+            "attn_skip_santa_decode_noalloc")
 
 #: Samplers of attn_skip_santa_decode.
 SANTA_MODES = {"iid": 0, "sys": 1, "strat": 2}
@@ -75,6 +76,8 @@ def load() -> ctypes.CDLL:
     lib.attn_skip_santa_workspace.argtypes = [i, i, i, i, P, P]
     lib.attn_skip_santa_decode.argtypes = [P, P, P, i, i, i, i, i, i, i, i64, i64, f, i, i, P, i,
                                            P, P, i, P, P, P]
+    lib.attn_skip_santa_decode_noalloc.argtypes = [P, P, P, i, i, i, i, i, i, i, i64, i64, f, i,
+                                                   i, P, i, i, P, P, P]
     lib.attn_skip_status_string.argtypes = [i]
     lib.attn_skip_status_string.restype = ctypes.c_char_p
     for fn in ("attn_skip_prefill", "attn_skip_prefill_blocks", "attn_skip_decode",
@@ -82,7 +85,8 @@ def load() -> ctypes.CDLL:
                "attn_skip_prefill_margins", "attn_skip_decode_margins",
                "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
                "attn_skip_selftest_wait_timeout", "attn_skip_last_device_error",
-               "attn_skip_santa_workspace", "attn_skip_santa_decode"):
+               "attn_skip_santa_workspace", "attn_skip_santa_decode",
+               "attn_skip_santa_decode_noalloc"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -395,6 +399,36 @@ def attn_skip_santa_decode(q, k, v, n_samples, mode, u, n_tiles=16, scale=0.0,
         _stream(stream, q.device))
     _check("attn_skip_santa_decode", st)
     return (o, idx) if with_idx else o
+
+
+def attn_skip_santa_decode_noalloc(q, k, v, n_samples, mode, u, o, idx=None, n_tiles=16,
+                                   scale=0.0, stream=None):
+    """attn_skip_santa_decode with both workspaces in the library's own
+    device memory, for callers that cannot allocate when they decode.  The
+    caller passes the outputs: ``o`` [B,Hq,128] fp32 or bf16 and optionally
+    ``idx`` [B,Hq,S] int32; nothing is allocated here or in the library.
+    Sizes: B*Hq*ceil(L/128)*128 <= 4,194,304 and B*Hq*n_tiles*2 <= 65,536.
+    Calls that overlap on the GPU share the scratch and race."""
+    _cuda_contig(q, k, v, u, o)
+    if idx is not None:
+        _cuda_contig(idx)
+        if idx.dtype != torch.int32:
+            raise TypeError("idx must be int32")
+    B, Hq, dk = q.shape
+    _, Hkv, L, kstride = k.shape
+    dv, vstride = v.shape[3], v.shape[3]
+    if u.dtype != torch.float32:
+        raise TypeError("u must be float32")
+    st = load().attn_skip_santa_decode_noalloc(
+        _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, Hq, Hkv, L, dk, dv, kstride, vstride,
+        float(scale), int(n_samples), SANTA_MODES[mode], _ptr(u), int(n_tiles), _dtype_code(o),
+        _ptr(o), None if idx is None else _ptr(idx), _stream(stream, q.device))
+    if st == ATTN_EINVAL:
+        raise AttnSkipError("attn_skip_santa_decode_noalloc (the built-in scratch holds "
+                            "B*Hq*ceil(L/128)*128 <= 4194304 score floats and "
+                            "B*Hq*n_tiles*2 <= 65536 statistics floats)", st)
+    _check("attn_skip_santa_decode_noalloc", st)
+    return o
 
 
 def attn_skip_selftest_wait_timeout(stream=None, device=None):

@@ -303,6 +303,45 @@ attn_status attn_skip_santa_decode(const void *q, const void *k, const void *v, 
                                    attn_dtype out_dt, void *o, int32_t *idx, void *stream);
 
 /*
+ * attn_skip_santa_decode without caller workspaces.  The pages have no
+ * counterpart: this is a convenience of this library for callers that cannot
+ * allocate device memory when they decode (a host runtime whose plugin
+ * interface passes only input and output pointers, an engine that reserved
+ * all its device memory up front, a loop that cannot take the device-wide
+ * synchronisation of cudaMalloc / cudaFree).
+ *
+ * Same arguments, meaning and results as attn_skip_santa_decode, minus
+ * `scores` and `tile_stats`: both workspaces live in one fixed array in the
+ * library's device memory (16.25 MiB, held on every device that loads the
+ * library until the process exits).  The call allocates nothing: no
+ * cudaMalloc, cudaFree or allocating library routine.
+ *
+ * Limits: B * Hq * ceil(L / 128) * 128 <= 4,194,304 (e.g. B = 4, Hq = 32,
+ * L = 32768) and B * Hq * n_tiles * 2 <= 65,536; beyond either the call
+ * returns ATTN_EINVAL before any CUDA call.  The other checks are those of
+ * attn_skip_santa_decode.
+ *
+ * Set-up: the first call on a device (the device current on the calling
+ * thread; `stream` must belong to it) looks up the array's device address
+ * with cudaGetSymbolAddress, which can load the library's device code; make
+ * that first call before any stream capture.  ATTN_ECUDA if the look-up
+ * fails.
+ *
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents.  Nothing in it needs clearing (the score pass writes both
+ * parts in full before the sampling pass reads them), but two calls that
+ * overlap on the GPU (different streams, or concurrent host threads without
+ * ordering) race on it and both results are then undefined: order such calls
+ * on one stream or with events.
+ */
+attn_status attn_skip_santa_decode_noalloc(const void *q, const void *k, const void *v,
+                                           attn_dtype dt, int B, int Hq, int Hkv, int L, int dk,
+                                           int dv, int64_t k_row_stride, int64_t v_row_stride,
+                                           float scale, int n_samples, attn_santa_mode mode,
+                                           const float *u, int n_tiles, attn_dtype out_dt,
+                                           void *o, int32_t *idx, void *stream);
+
+/*
  * Diagnostic: launches one small CTA that allocates TMEM and then waits, with
  * the same bounded wait as every kernel, on an mbarrier phase that nothing
  * completes.  After the 1 s limit the wait gives up, the CTA raises its abort
