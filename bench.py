@@ -267,6 +267,7 @@ def run_gpu(args, rank, world):
     msweep = mla_sweep(args, bs, dev, stream, flush, lam)
     calib = calibration(args, bs, dev, stream, flush, dq, dk_, dv_, dqd, dkd, lp, ld, pbits)
     blocks = block_set_sweep(args, bs, dev, stream, flush, dq, dk_, dv_, lp, po, plse, pbits)
+    santa = santa_sweep(args, bs, dev, stream, flush)
 
     # ---- the timed region: K steps of the whole hot path at ~70 % ---------
     fp, fd = prefill(lp[TARGET]), decode(ld[TARGET])
@@ -351,6 +352,7 @@ def run_gpu(args, rank, world):
         "mla_decode": msweep,
         "calibration": calib,
         "block_set": blocks,
+        "santa_decode": santa,
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,  # prefill, decode, merge per timed step
         "clocks": clk.summary(),
@@ -396,6 +398,65 @@ def mla_sweep(args, bs, dev, stream, flush, lam):
     out["max"]["speedup_vs_lambda0"] = round(out["0.0"]["ms"] / out["max"]["ms"], 4)
     out["workload"] = (f"B{M.B} Hq{M.Hq} latent dk{M.dk} dv{M.dv} L{M.L} Bc{M.Bc} "
                        f"splits{M.n_splits}; 'max' = largest sparsity any lambda < 1 reaches")
+    return out
+
+
+def santa_sweep(args, bs, dev, stream, flush):
+    """Sampled decode output (SANTA estimator, S = 128 samples per head, 16 key
+    tiles) on the spread-attention decode inputs (B=16, 32/8 heads, L=32768),
+    both samplers, against the exact decode (lambda = 0) of the same inputs."""
+    C = W.SANTA_DECODE_32K
+    S, n_tiles = 128, 16
+    q, k, v = W.decode_inputs(C)
+    dq, dk_, dv_ = q.to(dev), k.to(dev), v.to(dev)
+    del q, k, v
+    n_b = -(-C.L // 128)
+    ns, nt = bs.attn_skip_santa_workspace(C.B, C.Hq, C.L, n_tiles)
+    ws = (torch.empty(ns, dtype=torch.float32, device=dev),
+          torch.empty(nt, dtype=torch.float32, device=dev))
+    o = torch.empty(C.B, C.Hq, C.dv, dtype=torch.float32, device=dev)
+    idx = torch.empty(C.B, C.Hq, S, dtype=torch.int32, device=dev)
+    k_bytes = C.B * C.Hkv * C.L * C.dk * 2
+    out = {"workload": f"{C.name}: B{C.B} Hq{C.Hq} Hkv{C.Hkv} d{C.dk} L{C.L}, sink 1.2, "
+                       f"salient 0.6; S={S} samples per head, {n_tiles} key tiles"}
+    for mode in ("sys", "strat"):
+        u = W.santa_offsets(C, S, mode).to(dev)
+
+        def step():
+            bs.attn_skip_santa_decode(dq, dk_, dv_, S, mode, u, n_tiles=n_tiles, workspace=ws,
+                                      out=o, idx_out=idx)
+
+        durs = timed_launches(step, args.warmup, args.steps, flush, stream)
+        ms = statistics.mean(durs)
+        ix = idx.to("cpu").to(torch.int64)
+        G = C.Hq // C.Hkv
+        tiles_hit = sum(len(torch.unique(ix[b, h] // (C.L // n_tiles)))
+                        for b in range(C.B) for h in range(C.Hq))
+        rows = sum(len(torch.unique(ix[b, hk * G:(hk + 1) * G]))
+                   for b in range(C.B) for hk in range(C.Hkv))
+        byts = (k_bytes + C.B * C.Hq * n_b * 128 * 4                 # keys, stash write
+                + tiles_hit * (n_b // n_tiles) * 128 * 4             # stash re-read
+                + rows * C.dv * 2 + C.B * C.Hq * (C.dk * 2 + C.dv * 4))
+        out[mode] = {"ms": round(ms, 4), "tok_per_s": round(C.B / (ms / 1e3), 1),
+                     "gbs": round(byts / ms / 1e6, 1), "bytes": byts,
+                     "value_rows_read": rows, "tiles_with_samples_frac":
+                         round(tiles_hit / (C.B * C.Hq * n_tiles), 4)}
+    # exact output of the same inputs: dense split-KV decode + merge
+    op = torch.empty(C.B, C.Hq, C.n_splits, C.dv, dtype=torch.float32, device=dev)
+    lpart = torch.empty(C.B, C.Hq, C.n_splits, dtype=torch.float32, device=dev)
+    bits = torch.empty(bs.decode_bitmap_shape(C.B, C.Hkv, C.L, C.Bc, C.n_splits),
+                       dtype=torch.int32, device=dev)
+    do = torch.empty(C.B, C.Hq, C.dv, dtype=torch.bfloat16, device=dev)
+    dlse = torch.empty(C.B, C.Hq, dtype=torch.float32, device=dev)
+
+    def exact():
+        bs.attn_skip_decode(dq, dk_, dv_, 0.0, C.Bc, C.n_splits, out=(op, lpart, bits))
+        bs.attn_skip_decode_combine(op, lpart, out=(do, dlse))
+
+    ms = statistics.mean(timed_launches(exact, args.warmup, args.steps, flush, stream))
+    out["exact_decode_ms"] = round(ms, 4)
+    for mode in ("sys", "strat"):
+        out[mode]["speedup_vs_exact"] = round(ms / out[mode]["ms"], 4)
     return out
 
 

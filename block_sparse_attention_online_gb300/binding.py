@@ -370,13 +370,14 @@ def attn_skip_santa_workspace(B, Hq, L, n_tiles):
 
 def attn_skip_santa_decode(q, k, v, n_samples, mode, u, n_tiles=16, scale=0.0,
                            out_dtype=torch.float32, with_idx=False, workspace=None, out=None,
-                           stream=None):
+                           idx_out=None, stream=None):
     """Sampled decode output (SANTA estimator).  q [B,Hq,128], k/v
     [B,Hkv,L,128] bf16; ``mode`` ``"sys"`` (u [B,Hq]) or ``"strat"`` (u
     [B,Hq,S]), u fp32 in [0, 1) on the device.  Returns ``o`` [B,Hq,128] and,
     with ``with_idx``, the int32 sample indices [B,Hq,S].  ``workspace`` is
     an optional ``(scores, tile_stats)`` pair of fp32 device tensors of the
-    sizes attn_skip_santa_workspace gives."""
+    sizes attn_skip_santa_workspace gives; ``out`` and ``idx_out`` optional
+    preallocated outputs."""
     _cuda_contig(q, k, v, u)
     B, Hq, dk = q.shape
     _, Hkv, L, kstride = k.shape
@@ -390,8 +391,9 @@ def attn_skip_santa_decode(q, k, v, n_samples, mode, u, n_tiles=16, scale=0.0,
     scores, stats = workspace
     _cuda_contig(scores, stats)
     o = out if out is not None else torch.empty(B, Hq, dv, dtype=out_dtype, device=q.device)
-    idx = (torch.empty(B, Hq, int(n_samples), dtype=torch.int32, device=q.device)
-           if with_idx else None)
+    idx = idx_out
+    if idx is None and with_idx:
+        idx = torch.empty(B, Hq, int(n_samples), dtype=torch.int32, device=q.device)
     st = load().attn_skip_santa_decode(
         _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, Hq, Hkv, L, dk, dv, kstride, vstride,
         float(scale), int(n_samples), SANTA_MODES[mode], _ptr(u), int(n_tiles), _ptr(scores),
