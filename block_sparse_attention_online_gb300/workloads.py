@@ -149,6 +149,71 @@ SANTA_DECODE_32K = GQA_DECODE_32K.with_(name="santa_decode_bf16_B16_L32768", sin
                                         salient_a=0.6, seed=1239)
 
 
+@dataclass(frozen=True)
+class VarlenConfig:
+    """A batch of independent causal prefills of different lengths, packed
+    token-major: q ``[total, Hq, d]``, k and v ``[total, Hkv, d]``, sequence
+    ``s`` at tokens ``[cu[s], cu[s+1])``.  Sequence ``s`` is drawn with the
+    planted-salience recipe of :class:`PrefillConfig` under its own seed."""
+    name: str
+    lengths: tuple
+    Hq: int
+    Hkv: int
+    d: int
+    dtype: str = "bf16"
+    Br: int = 128
+    Bc: int = 128
+    causal: bool = True
+    salient_frac: float = 0.02
+    sink_a: float = 6.0
+    salient_a: float = 3.0
+    seed: int = 1240
+
+    @property
+    def n_seq(self) -> int:
+        return len(self.lengths)
+
+    @property
+    def total(self) -> int:
+        return int(sum(self.lengths))
+
+    @property
+    def max_seqlen(self) -> int:
+        return int(max(self.lengths)) if self.lengths else 0
+
+    @property
+    def cu_seqlens(self) -> tuple:
+        out = [0]
+        for L in self.lengths:
+            out.append(out[-1] + int(L))
+        return tuple(out)
+
+    @property
+    def G(self) -> int:
+        return self.Hq // self.Hkv
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def sequence(self, s: int) -> PrefillConfig:
+        return PrefillConfig(f"{self.name}[{s}]", 1, self.Hq, self.Hkv, int(self.lengths[s]),
+                             self.d, self.dtype, self.Br, self.Bc, self.causal,
+                             self.salient_frac, self.sink_a, self.salient_a, 0.0,
+                             seed=self.seed + 101 * (s + 1))
+
+    def with_(self, **kw) -> "VarlenConfig":
+        return replace(self, **kw)
+
+
+# Sixteen sequences from 129 to 16384 tokens (ragged lengths included), the
+# Llama-3.1-8B attention shape; 65,536 tokens in all.
+VARLEN_PREFILL_64K = VarlenConfig(
+    "gqa_prefill_varlen_bf16_16seq_64k",
+    (16384, 12000, 8192, 6144, 5000, 4096, 3163, 2731, 2048, 1536, 1500, 1024, 777, 512, 300,
+     129), 32, 8, 128)
+
+
 def _unit_u(seed: int, b: int, hk: int, d: int) -> torch.Tensor:
     u = torch.randn(d, generator=_gen(seed, "u", b, hk), dtype=torch.float64)
     return (u / u.norm() * math.sqrt(d)).to(torch.float32)
@@ -215,6 +280,24 @@ def prefill_inputs(cfg: PrefillConfig, heads=None):
     with ThreadPoolExecutor(_threads()) as ex:
         list(ex.map(one, jobs))
     return q, k, v
+
+
+def varlen_inputs(cfg: VarlenConfig):
+    """Return ``(q, k, v, cu_seqlens)``: packed CPU tensors q ``[total, Hq, d]``,
+    k and v ``[total, Hkv, d]`` and int32 ``cu_seqlens`` ``[n_seq + 1]``."""
+    tdt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    q = torch.zeros(cfg.total, cfg.Hq, cfg.d, dtype=tdt)
+    k = torch.zeros(cfg.total, cfg.Hkv, cfg.d, dtype=tdt)
+    v = torch.zeros(cfg.total, cfg.Hkv, cfg.d, dtype=tdt)
+    cu = cfg.cu_seqlens
+    for s in range(cfg.n_seq):
+        if cfg.lengths[s] == 0:
+            continue
+        qs, ks, vs = prefill_inputs(cfg.sequence(s))
+        q[cu[s]:cu[s + 1]] = qs[0].transpose(0, 1)
+        k[cu[s]:cu[s + 1]] = ks[0].transpose(0, 1)
+        v[cu[s]:cu[s + 1]] = vs[0].transpose(0, 1)
+    return q, k, v, torch.tensor(cu, dtype=torch.int32)
 
 
 def decode_inputs(cfg: DecodeConfig, batches=None):

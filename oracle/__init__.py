@@ -20,6 +20,10 @@ Parity status of each function (what pins it, in ``tests/test_oracle.py``):
   ``tests/golden/``; brute-force recomputation of each skip bit.
 * ``combine``: lambda = 0 merged decode equals dense single-pass attention;
   one split is the identity.
+* ``prefill_varlen``: each packed sequence at lambda = 0 equals torch's fp64
+  SDPA on that sequence alone; with thresholds, each sequence's output is the
+  softmax over its own kept tokens, a larger lambda skips a superset of
+  blocks, and empty sequences leave their rows untouched.
 * ``santa_decode`` (the page "Stochastic Sparse Attention for Memory-Bound
   Inference", section "关键设计"): the closed form of equal scores (every
   sample index and gap known exactly); a dominant key takes every sample; the
@@ -236,6 +240,49 @@ def combine(o_part, lse_part):
     if rc:
         raise ValueError("bsa_oracle_combine: invalid arguments")
     return o, lse
+
+
+def prefill_varlen(q, k, v, cu_seqlens, scale, lambdas, Br=128, Bc=128, causal=True,
+                   max_seqlen=None):
+    """Batched variable-length prefill in fp64: every sequence is its own
+    thresholded prefill (the loop of :func:`prefill` with B = 1) with its own
+    threshold ``lambdas[s]`` (the BLASST page, section "λ = a/L：反比关系的直觉与
+    依据": the threshold of a sequence scales as a / L with its length).
+
+    q ``[total, Hq, dk]``, k ``[total, Hkv, dk]``, v ``[total, Hkv, dv]``
+    (token-major, sequence s at tokens ``[cu[s], cu[s+1])``).  Returns ``o``
+    ``[total, Hq, dv]``, ``lse`` ``[Hq, total]``, ``skip`` and ``margin``
+    ``[n_seq, Hq, n_t, n_t]`` with ``n_t = ceil(max_seqlen / Br)`` (blocks a
+    sequence does not have read 0 and NaN)."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    lam = np.asarray(lambdas, dtype=np.float64)
+    n_seq = len(cu) - 1
+    total, Hq, _ = q.shape
+    dv = v.shape[2]
+    lens = np.diff(cu)
+    mx = int(lens.max()) if max_seqlen is None else int(max_seqlen)
+    if Br != Bc:
+        raise ValueError("prefill_varlen: Br must equal Bc")
+    n_t = -(-mx // Br)
+    o = np.zeros((total, Hq, dv))
+    lse = np.full((Hq, total), np.nan)
+    skip = np.zeros((n_seq, Hq, n_t, n_t), dtype=np.uint8)
+    margin = np.full((n_seq, Hq, n_t, n_t), np.nan)
+    for s in range(n_seq):
+        c0, c1 = int(cu[s]), int(cu[s + 1])
+        if c1 == c0:
+            continue
+        qs = np.ascontiguousarray(q[c0:c1].transpose(1, 0, 2)[None])
+        ks = np.ascontiguousarray(k[c0:c1].transpose(1, 0, 2)[None])
+        vs = np.ascontiguousarray(v[c0:c1].transpose(1, 0, 2)[None])
+        r = prefill(qs, ks, vs, scale, float(lam[s]), Br, Bc, causal)
+        o[c0:c1] = r["o"][0].transpose(1, 0, 2)
+        lse[:, c0:c1] = r["lse"][0]
+        nt = r["skip"].shape[2]
+        skip[s, :, :nt, :nt] = r["skip"][0]
+        margin[s, :, :nt, :nt] = r["margin"][0]
+    return {"o": o, "lse": lse, "skip": skip, "margin": margin}
 
 
 SANTA_MODES = {"iid": 0, "sys": 1, "strat": 2}
