@@ -22,7 +22,8 @@ ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT = range(5)
 ATTN_BF16, ATTN_F32 = 0, 1
 
 #: Every symbol include/attn_skip.h declares.
-EXPORTED = ("attn_skip_prefill", "attn_skip_prefill_blocks", "attn_skip_decode",
+EXPORTED = ("attn_skip_prefill", "attn_skip_prefill_blocks", "attn_skip_prefill_varlen",
+            "attn_skip_decode",
             "attn_skip_decode_per_head", "attn_skip_decode_combine",
             "attn_skip_prefill_margins", "attn_skip_decode_margins", "attn_skip_sparsity_at",
             "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
@@ -58,6 +59,8 @@ def load() -> ctypes.CDLL:
     lib.attn_skip_prefill.argtypes = [P, P, P, i, i, i, i, i, i, i, f, d, i, i, i, P, P, P, P]
     lib.attn_skip_prefill_blocks.argtypes = [P, P, P, i, i, i, i, i, i, i, f, d, i, i, i, P, P, P,
                                              P, P]
+    lib.attn_skip_prefill_varlen.argtypes = [P, P, P, i, i, P, i, i, i, i, i, i, f, P, i, i, i,
+                                             P, P, P, P]
     lib.attn_skip_decode.argtypes = [P, P, P, i, i, i, i, i, i, i, i64, i64, f, d, i, i, P, P, P,
                                      P]
     lib.attn_skip_decode_combine.argtypes = [P, P, i, i, i, i, i, P, P, P]
@@ -80,7 +83,8 @@ def load() -> ctypes.CDLL:
                                                    i, P, i, i, P, P, P]
     lib.attn_skip_status_string.argtypes = [i]
     lib.attn_skip_status_string.restype = ctypes.c_char_p
-    for fn in ("attn_skip_prefill", "attn_skip_prefill_blocks", "attn_skip_decode",
+    for fn in ("attn_skip_prefill", "attn_skip_prefill_blocks", "attn_skip_prefill_varlen",
+               "attn_skip_decode",
                "attn_skip_decode_per_head", "attn_skip_decode_combine",
                "attn_skip_prefill_margins", "attn_skip_decode_margins",
                "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
@@ -114,7 +118,7 @@ def _stream(stream, device) -> ctypes.c_void_p:
 
 
 def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
-    return ctypes.c_void_p(t.data_ptr())
+    return ctypes.c_void_p(t.data_ptr() if t.numel() else None)
 
 
 def _check(fn: str, status: int):
@@ -199,6 +203,40 @@ def attn_skip_prefill_blocks(q, k, v, lam, block_set, Br=128, Bc=128, causal=Tru
                                          int(bool(causal)), _ptr(block_set), _ptr(o), _ptr(lse),
                                          _ptr(bits), _stream(stream, q.device))
     _check("attn_skip_prefill_blocks", st)
+    return o, lse, bits
+
+
+def varlen_bitmap_shape(n_seq, Hq, max_seqlen, Br=128):
+    n_t = -(-int(max_seqlen) // Br)
+    return (int(n_seq), int(Hq), n_t, -(-n_t // 32))
+
+
+def attn_skip_prefill_varlen(q, k, v, cu_seqlens, max_seqlen, lambdas, causal=True, scale=0.0,
+                             Br=128, Bc=128, out=None, stream=None):
+    """Batched variable-length prefill.  q [total,Hq,dk], k/v [total,Hkv,d]
+    token-major; ``cu_seqlens`` int32 [n_seq+1] and ``lambdas`` fp32 [n_seq]
+    on the inputs' device.  Returns ``(o [total,Hq,dv], lse [Hq,total],
+    skip_bits [n_seq,Hq,n_t,words])``."""
+    _cuda_contig(q, k, v, cu_seqlens, lambdas)
+    if cu_seqlens.dtype != torch.int32 or lambdas.dtype != torch.float32:
+        raise TypeError("cu_seqlens must be int32 and lambdas float32")
+    total, Hq, dk = q.shape
+    Hkv, dv = k.shape[1], v.shape[2]
+    n_seq = cu_seqlens.numel() - 1
+    if lambdas.numel() != n_seq:
+        raise ValueError(f"lambdas has {lambdas.numel()} entries, expected {n_seq}")
+    if out is None:
+        o = torch.empty(total, Hq, dv, dtype=q.dtype, device=q.device)
+        lse = torch.empty(Hq, total, dtype=torch.float32, device=q.device)
+        bits = torch.empty(varlen_bitmap_shape(n_seq, Hq, max_seqlen, Br), dtype=torch.int32,
+                           device=q.device)
+    else:
+        o, lse, bits = out
+    st = load().attn_skip_prefill_varlen(
+        _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), n_seq, _ptr(cu_seqlens), int(max_seqlen),
+        total, Hq, Hkv, dk, dv, float(scale), _ptr(lambdas), Br, Bc, int(bool(causal)), _ptr(o),
+        _ptr(lse), _ptr(bits), _stream(stream, q.device))
+    _check("attn_skip_prefill_varlen", st)
     return o, lse, bits
 
 

@@ -155,6 +155,48 @@ extern "C" attn_status attn_skip_prefill_blocks(const void *q, const void *k, co
                         (cudaStream_t)stream);
 }
 
+extern "C" attn_status attn_skip_prefill_varlen(const void *q, const void *k, const void *v,
+                                                attn_dtype dt, int n_seq,
+                                                const int32_t *cu_seqlens, int max_seqlen,
+                                                int total, int Hq, int Hkv, int dk, int dv,
+                                                float scale, const float *lambda, int Br, int Bc,
+                                                int causal, void *o, float *lse,
+                                                uint32_t *skip_bits, void *stream) {
+  if (!cu_seqlens || !lambda) return ATTN_EINVAL;
+  if (n_seq <= 0 || max_seqlen < 0 || total < 0 || Hq <= 0 || Hkv <= 0 || dk <= 0 || dv <= 0 ||
+      Br <= 0 || Bc <= 0)
+    return ATTN_EINVAL;
+  // With no token the tensors may be empty (null); the bitmap is needed
+  // whenever there is a tile row.
+  if (total > 0 && (!q || !k || !v || !o || !lse)) return ATTN_EINVAL;
+  if (max_seqlen > 0 && !skip_bits) return ATTN_EINVAL;
+  if (Hq % Hkv != 0 || !(scale == scale)) return ATTN_EINVAL;
+  if (dt != ATTN_BF16 && dt != ATTN_F32) return ATTN_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(skip_bits) || ((uintptr_t)cu_seqlens & 3u) || ((uintptr_t)lambda & 3u))
+    return ATTN_EINVAL;
+  if (dt != ATTN_BF16 || dk != 128 || dv != 128 || Br != 128 || Bc != 128)
+    return ATTN_EUNSUPPORTED;
+  const long n_t = (max_seqlen + 127L) / 128;
+  if ((long)n_seq * Hq * n_t > 0x7fffffffL) return ATTN_EUNSUPPORTED;
+  if (n_t == 0) return ATTN_OK;  // every sequence is empty: no tile, no bitmap word
+  if (total == 0)                 // every sequence is empty: only the bitmap to clear
+    return from_cuda(cudaMemsetAsync(skip_bits, 0,
+                                     (size_t)n_seq * Hq * n_t * ((n_t + 31) / 32) * 4,
+                                     (cudaStream_t)stream));
+  PrefillArgs a{};
+  a.q = q; a.k = k; a.v = v; a.o = o; a.lse = lse; a.bits = skip_bits;
+  a.B = n_seq; a.Hq = Hq; a.Hkv = Hkv; a.T = max_seqlen; a.dk = dk; a.dv = dv;
+  a.Br = Br; a.Bc = Bc; a.causal = causal ? 1 : 0;
+  a.n_t = (int)n_t; a.n_b = (int)n_t; a.words = (int)((n_t + 31) / 32);
+  a.scale = scale > 0.f ? scale : (float)(1.0 / sqrt((double)dk));
+  a.ln_lambda = -INFINITY;  // per sequence from lambda[]
+  a.cu_seqlens = cu_seqlens; a.lambda_seq = lambda; a.total = total;
+  cudaError_t e = error_word(&a.err);
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(launch_prefill_tc(a, (cudaStream_t)stream));
+}
+
 extern "C" attn_status attn_skip_prefill_margins(const void *q, const void *k, attn_dtype dt,
                                                  int B, int Hq, int Hkv, int T, int dk,
                                                  float scale, int Br, int Bc, int causal,
@@ -295,7 +337,9 @@ extern "C" attn_status attn_skip_last_device_error(void *stream) {
     const unsigned zero = 0;
     e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
     if (e != cudaSuccess) return from_cuda(e);
-    return (word & kErrTimeout) ? ATTN_ETIMEOUT : ATTN_ECUDA;
+    return (word & kErrTimeout)  ? ATTN_ETIMEOUT
+           : (word & kErrBadArg) ? ATTN_EINVAL
+                                 : ATTN_ECUDA;
   }
   return ATTN_OK;
 }

@@ -9,6 +9,7 @@ namespace attn_skip {
 // Bits of the device error word.
 enum : unsigned {
   kErrTimeout = 1u,  // a bounded mbarrier / flag wait gave up
+  kErrBadArg = 2u,   // a device-side argument (a varlen length or threshold) was out of range
 };
 
 struct PrefillArgs {
@@ -29,6 +30,13 @@ struct PrefillArgs {
   // Explicit block set: [B,Hq,n_t,words] bit masks, bit j = block j is
   // traversed (within the causal range); null = every block.
   const uint32_t *block_set;
+  // Variable-length batch: B sequences packed token-major, sequence b at
+  // tokens [cu_seqlens[b], cu_seqlens[b+1]) of q [total,Hq,128], k and v
+  // [total,Hkv,128] and o [total,Hq,128]; lse [Hq,total]; threshold
+  // lambda_seq[b]; T = the longest length.  Null cu_seqlens = fixed length.
+  const int32_t *cu_seqlens;
+  const float *lambda_seq;
+  int total;
 };
 
 struct DecodeArgs {

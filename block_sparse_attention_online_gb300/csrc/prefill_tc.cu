@@ -192,10 +192,12 @@ __device__ __forceinline__ void chunk_exp(const uint32_t (&s)[32], uint64_t sl2x
 }
 
 // STATS: the statistics mode; SET: an explicit block set per tile (blocks
-// outside it are not traversed).  Each is compiled separately so that the
-// ordinary kernel's loops carry none of their code.  Ring positions count the
-// traversed blocks (c); addresses and bitmap positions use the block index (j).
-template <bool STATS, bool SET>
+// outside it are not traversed); VARLEN: a batch of sequences of different
+// lengths packed token-major, each with its own threshold.  Each is compiled
+// separately so that the ordinary kernel's loops carry none of their code.
+// Ring positions count the traversed blocks (c); addresses and bitmap
+// positions use the block index (j).
+template <bool STATS, bool SET, bool VARLEN>
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                       const __grid_constant__ CUtensorMap tm_k,
@@ -215,11 +217,38 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int bh = (int)(blockIdx.x % BH);
   const int h = bh % a.Hq, b = bh / a.Hq;
   const int hk = h / (a.Hq / a.Hkv);
+  // Varlen: sequence b holds tokens [off, off + T) of the packed tensors; a
+  // tile past its end has no row, only bitmap words to clear.  A length or a
+  // threshold outside its range raises the bad-argument bit; the sequence is
+  // then treated as empty, the threshold as 0.
+  int T = a.T, off = 0;
+  float ln_lam = a.ln_lambda;
+  if constexpr (VARLEN) {
+    const int c0 = __ldg(a.cu_seqlens + b), c1 = __ldg(a.cu_seqlens + b + 1);
+    const float lam = __ldg(a.lambda_seq + b);
+    const bool bad_len = c0 < 0 || c1 < c0 || c1 - c0 > a.T || c1 > a.total;
+    const bool bad_lam = !(lam >= 0.f && lam < 1.f);
+    if ((bad_len || bad_lam) && tid == 0 && h == 0 && t == 0) atomicOr(a.err, kErrBadArg);
+    T = bad_len ? 0 : c1 - c0;
+    off = bad_len ? 0 : c0;
+    ln_lam = (bad_lam || !(lam > 0.f)) ? -INFINITY : logf(lam);
+    if (t * BM >= T) {
+      uint32_t *bw = a.bits + ((size_t)bh * a.n_t + t) * a.words;
+      for (int w = tid; w < a.words; w += NTHREADS) bw[w] = 0u;
+      return;
+    }
+  }
   const int row0 = t * BM;
-  const int last_row = min(a.T, row0 + BM) - 1;
-  const int nblk = a.causal ? last_row / BN + 1 : a.n_b;
+  const int last_row = min(T, row0 + BM) - 1;
+  const int nblk = a.causal ? last_row / BN + 1 : (VARLEN ? (T + BN - 1) / BN : a.n_b);
   volatile int *abort = &sh.abort;
   const int zq = b * a.Hq + h, zkv = b * a.Hkv + hk;
+  // TMA coordinates (column, y, z) of query rows / key block j: [heads, T, 128]
+  // maps take (row, head); the token-major varlen maps [total, heads, 128]
+  // take (head, token).
+  const int q_y = VARLEN ? h : row0, q_z = VARLEN ? off + row0 : zq;
+  auto kv_y = [&](int j) { return VARLEN ? hk : j * BN; };
+  auto kv_z = [&](int j) { return VARLEN ? off + j * BN : zkv; };
   const uint32_t *set_words = SET ? a.block_set + ((size_t)bh * a.n_t + t) * a.words : nullptr;
   auto in_set = [&](int j) { return ((__ldg(set_words + (j >> 5)) >> (j & 31)) & 1u) != 0u; };
 
@@ -265,8 +294,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint64_t keep_l2 = policy_evict_last();    // K is re-read by other tiles/heads
       const uint64_t stream_l2 = policy_evict_first();  // Q is read once
       mbar_expect_tx(smem_u32(&sh.q_full), TILE_BYTES);
-      tma_load_3d(base + SMEM_Q, &tm_q, smem_u32(&sh.q_full), 0, row0, zq, stream_l2);
-      tma_load_3d(base + SMEM_Q + HALF_BYTES, &tm_q, smem_u32(&sh.q_full), 64, row0, zq,
+      tma_load_3d(base + SMEM_Q, &tm_q, smem_u32(&sh.q_full), 0, q_y, q_z, stream_l2);
+      tma_load_3d(base + SMEM_Q + HALF_BYTES, &tm_q, smem_u32(&sh.q_full), 64, q_y, q_z,
                   stream_l2);
       int ki = 0, cc = 0;
       for (int j = 0; j < nblk && !*abort; ++j) {
@@ -280,8 +309,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           break;
         const uint32_t dst = base + SMEM_K + s * TILE_BYTES;
         mbar_expect_tx(smem_u32(&sh.k_full[s]), TILE_BYTES);
-        tma_load_3d(dst, &tm_k, smem_u32(&sh.k_full[s]), 0, j * BN, zkv, keep_l2);
-        tma_load_3d(dst + HALF_BYTES, &tm_k, smem_u32(&sh.k_full[s]), 64, j * BN, zkv, keep_l2);
+        tma_load_3d(dst, &tm_k, smem_u32(&sh.k_full[s]), 0, kv_y(j), kv_z(j), keep_l2);
+        tma_load_3d(dst + HALF_BYTES, &tm_k, smem_u32(&sh.k_full[s]), 64, kv_y(j), kv_z(j),
+                    keep_l2);
         ++ki;
       }
       // Drain: the last load issued into each slot has landed before exit
@@ -315,8 +345,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           break;
         const uint32_t dst = base + SMEM_V + s * TILE_BYTES;
         mbar_expect_tx(smem_u32(&sh.v_full[s]), TILE_BYTES);
-        tma_load_3d(dst, &tm_v, smem_u32(&sh.v_full[s]), 0, j * BN, zkv, keep_l2);
-        tma_load_3d(dst + HALF_BYTES, &tm_v, smem_u32(&sh.v_full[s]), 64, j * BN, zkv, keep_l2);
+        tma_load_3d(dst, &tm_v, smem_u32(&sh.v_full[s]), 0, kv_y(j), kv_z(j), keep_l2);
+        tma_load_3d(dst + HALF_BYTES, &tm_v, smem_u32(&sh.v_full[s]), 64, kv_y(j), kv_z(j),
+                    keep_l2);
         ++vi;
       }
       for (int s = 0; s < NV && s < vi; ++s) {
@@ -405,7 +436,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const int quarter = warp & 3;                 // TMEM lane quarter
     const int r = quarter * 32 + lane;            // row within the tile == TMEM lane
     const int row = row0 + r;
-    const bool valid = row < a.T;
+    const bool valid = row < T;
     const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
     const float sl2 = a.scale * kLog2e;           // raw score -> log2 units
     float mref = -INFINITY;                       // exp reference (log2 units)
@@ -414,14 +445,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     bool ok = true;
     auto needs_mask = [&](int j) {
       const int key0 = j * BN;
-      return a.causal ? (key0 + BN - 1 > row0) : (key0 + BN > a.T);
+      return a.causal ? (key0 + BN - 1 > row0) : (key0 + BN > T);
     };
 
     if (decider) {
       // Per block: the full row max of S_j, the row vote against the running
       // max before the block, then one barrier round of the four deciders to
       // AND the votes.  Thread 0 publishes the decision and the bitmap.
-      const float c2 = a.ln_lambda * kLog2e;      // ln(lambda) in log2 units
+      const float c2 = ln_lam * kLog2e;           // ln(lambda) in log2 units
       float m2 = -INFINITY;                       // running max (log2 units)
       uint32_t word = 0;
       uint32_t *bits = a.bits ? a.bits + ((size_t)bh * a.n_t + t) * a.words : nullptr;
@@ -442,7 +473,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         fence_after_sync();
         const uint32_t sa = lane_base + sb * BN;
-        if (needs_mask(j)) mask_block_tmem(sa, j * BN, row, a.causal, a.T);
+        if (needs_mask(j)) mask_block_tmem(sa, j * BN, row, a.causal, T);
         uint32_t x0[32], x1[32], x2[32], x3[32];
         tmem_ld32(sa, x0);
         tmem_ld32(sa + 32, x1);
@@ -622,7 +653,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const bool empty = SET && !(lrow > 0.f);
       const float inv = empty ? 0.f : 1.f / lrow;
       const int col0 = decider ? 0 : 64;
-      __nv_bfloat16 *orow = (__nv_bfloat16 *)a.o + ((size_t)bh * a.T + row) * D + col0;
+      // Output rows: [heads, T, 128], or token-major [total, Hq, 128] (varlen).
+      const size_t orow_idx =
+          VARLEN ? (size_t)(off + row) * a.Hq + h : (size_t)bh * a.T + row;
+      __nv_bfloat16 *orow = (__nv_bfloat16 *)a.o + orow_idx * D + col0;
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t o[32];
@@ -645,7 +679,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       if (valid && !decider)
-        a.lse[(size_t)bh * a.T + row] = empty ? -INFINITY : sh.mfin[r] * kLn2 + logf(lrow);
+        a.lse[VARLEN ? (size_t)h * a.total + off + row : (size_t)bh * a.T + row] =
+            empty ? -INFINITY : sh.mfin[r] * kLn2 + logf(lrow);
     }
   }
 
@@ -661,14 +696,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
   CUtensorMap mq, mk, mv;
-  // [heads, T, 128] bf16, boxes of 64 columns x 128 rows; rows past T read as zero.
-  if (!make_map_bf16_3d(&mq, a.q, D, D, a.T, a.B * a.Hq, BM) ||
-      !make_map_bf16_3d(&mk, a.k, D, D, a.T, a.B * a.Hkv, BN) ||
-      !make_map_bf16_3d(&mv, a.v, D, D, a.T, a.B * a.Hkv, BN))
-    return cudaErrorInvalidValue;
-  auto kernel = a.stats_only  ? prefill_tc_kernel<true, false>
-                : a.block_set ? prefill_tc_kernel<false, true>
-                              : prefill_tc_kernel<false, false>;
+  if (a.cu_seqlens) {
+    // Token-major [total, heads, 128] bf16, boxes of 64 columns x 1 head x
+    // 128 tokens (the same shared-memory image as below); tokens past the
+    // end read as zero.
+    const int tot = a.total > 0 ? a.total : 1;
+    if (!make_map_bf16_thd(&mq, a.q, a.Hq, tot, BM) || !make_map_bf16_thd(&mk, a.k, a.Hkv, tot, BN) ||
+        !make_map_bf16_thd(&mv, a.v, a.Hkv, tot, BN))
+      return cudaErrorInvalidValue;
+  } else {
+    // [heads, T, 128] bf16, boxes of 64 columns x 128 rows; rows past T read as zero.
+    if (!make_map_bf16_3d(&mq, a.q, D, D, a.T, a.B * a.Hq, BM) ||
+        !make_map_bf16_3d(&mk, a.k, D, D, a.T, a.B * a.Hkv, BN) ||
+        !make_map_bf16_3d(&mv, a.v, D, D, a.T, a.B * a.Hkv, BN))
+      return cudaErrorInvalidValue;
+  }
+  auto kernel = a.cu_seqlens  ? prefill_tc_kernel<false, false, true>
+                : a.stats_only ? prefill_tc_kernel<true, false, false>
+                : a.block_set  ? prefill_tc_kernel<false, true, false>
+                               : prefill_tc_kernel<false, false, false>;
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_ALLOC);
   if (e != cudaSuccess) return e;

@@ -359,5 +359,22 @@ inline bool make_map_bf16_3d(CUtensorMap *m, const void *ptr, int cols, int64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over a token-major bf16 tensor [tokens][heads][128]: dims (column,
+// head, token), box = 64 columns x 1 head x box_rows tokens, 128-byte
+// swizzle.  The box lands in shared memory as box_rows rows of 128 bytes,
+// the image of a [heads][tokens][128] box of 64 columns x box_rows rows.
+inline bool make_map_bf16_thd(CUtensorMap *m, const void *ptr, int heads, int tokens,
+                              int box_rows) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {128u, (cuuint64_t)heads, (cuuint64_t)tokens};
+  const cuuint64_t strides[2] = {256u, (cuuint64_t)heads * 256u};
+  const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace tc
 }  // namespace attn_skip

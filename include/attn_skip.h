@@ -113,6 +113,45 @@ attn_status attn_skip_prefill_blocks(const void *q, const void *k, const void *v
                                      uint32_t *skip_bits, void *stream);
 
 /*
+ * Batched variable-length causal (or full) prefill, one threshold per sequence.
+ *
+ * Defines: section "λ = a/L：反比关系的直觉与依据" -- the threshold that keeps
+ * a target sparsity falls as a / L with the context length L, so a batch of
+ * sequences of different lengths takes one lambda per sequence (e.g.
+ * lambda[s] = a / L_s, or alpha * exp(beta * S) / L_s from the calibration
+ * model); each sequence is the loop of attn_skip_prefill on its own tokens.
+ *
+ *  cu_seqlens [n_seq + 1] int32 (device): sequence s holds tokens
+ *             [cu_seqlens[s], cu_seqlens[s+1]); cu_seqlens[0] = 0,
+ *             nondecreasing, last = total; lengths <= max_seqlen; a length
+ *             of 0 is allowed
+ *  lambda     [n_seq] fp32 (device), each in [0, 1); 0 = dense; ln(lambda)
+ *             is taken on the device in fp32
+ *  q          [total, Hq, dk] token-major (device); k [total, Hkv, dk];
+ *             v [total, Hkv, dv]
+ *  o          [total, Hq, dv] (same dtype as q)
+ *  lse        [Hq, total] fp32, natural log
+ *  skip_bits  [n_seq, Hq, n_t, ceil(n_t / 32)] uint32, n_t =
+ *             ceil(max_seqlen / Br): tile t of sequence s in row (s, h, t);
+ *             rows of tiles a sequence does not have read 0
+ *  scale      as for attn_skip_prefill
+ *
+ * Host checks as for attn_skip_prefill (EINVAL also for a null cu_seqlens
+ * or lambda, n_seq <= 0, max_seqlen < 0 or total < 0; cu_seqlens and lambda
+ * need only 4-byte alignment).  Kernels built: bf16, dk = dv = 128,
+ * Br = Bc = 128 (else ATTN_EUNSUPPORTED).  The device arrays are checked by
+ * the kernel: a sequence whose bounds are out of range is treated as empty,
+ * a lambda outside [0, 1) as 0, and attn_skip_last_device_error then returns
+ * ATTN_EINVAL.  max_seqlen = 0 launches nothing; total = 0 (every sequence
+ * empty; q, k, v, o, lse may then be NULL) only zeroes skip_bits.
+ */
+attn_status attn_skip_prefill_varlen(const void *q, const void *k, const void *v, attn_dtype dt,
+                                     int n_seq, const int32_t *cu_seqlens, int max_seqlen,
+                                     int total, int Hq, int Hkv, int dk, int dv, float scale,
+                                     const float *lambda, int Br, int Bc, int causal, void *o,
+                                     float *lse, uint32_t *skip_bits, void *stream);
+
+/*
  * Split-KV decode, one query token per sequence, with block skipping.
  *
  * Defines: section "Decode 内核：砍带宽" -- scores of a batch of KV blocks are
@@ -354,7 +393,8 @@ attn_status attn_skip_selftest_wait_timeout(void *stream);
 /*
  * Synchronises `stream`, then reads and clears the current device's error
  * word: ATTN_ETIMEOUT if a kernel gave up a bounded wait since the last read,
- * ATTN_ECUDA on a CUDA error, else ATTN_OK.
+ * ATTN_EINVAL if a kernel found a device-side argument out of range (the
+ * varlen lengths and thresholds), ATTN_ECUDA on a CUDA error, else ATTN_OK.
  */
 attn_status attn_skip_last_device_error(void *stream);
 

@@ -180,3 +180,31 @@ def test_santa_workspace_sizes(lib):
     assert bs.attn_skip_santa_workspace(1, 1, 1, 1) == (128, 2)
     with pytest.raises(bs.AttnSkipError):
         bs.attn_skip_santa_workspace(1, 0, 10, 1)
+
+
+def _varlen(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, dt=0, n=3, cu=FAKE, mx=512, total=900, Hq=8, Hkv=2, dk=128,
+             dv=128, scale=0.0, lam=FAKE, Br=128, Bc=128, causal=1, o=FAKE, lse=FAKE, bits=FAKE,
+             stream=None)
+    a.update(kw)
+    return lib.attn_skip_prefill_varlen(*a.values())
+
+
+@pytest.mark.parametrize("kw", [
+    dict(cu=None), dict(lam=None), dict(q=None), dict(o=None), dict(lse=None), dict(bits=None),
+    dict(n=0), dict(mx=-1), dict(total=-5), dict(Hq=6, Hkv=4), dict(dt=3),
+    dict(scale=float("nan")), dict(q=ctypes.c_void_p(0x10008)), dict(cu=ctypes.c_void_p(0x10002)),
+])
+def test_varlen_rejects_invalid_arguments(lib, kw):
+    assert _varlen(lib, **kw) == bs.ATTN_EINVAL
+
+
+@pytest.mark.parametrize("kw", [dict(dt=1), dict(dk=64, dv=64), dict(Br=64), dict(Bc=64)])
+def test_varlen_unsupported_shapes(lib, kw):
+    assert _varlen(lib, **kw) == bs.ATTN_EUNSUPPORTED
+
+
+def test_varlen_nothing_to_do_without_tiles(lib):
+    # max_seqlen = 0: every sequence is empty, no tile row exists, nothing launches
+    assert _varlen(lib, mx=0, total=0, q=None, k=None, v=None, o=None, lse=None,
+                   bits=None) == bs.ATTN_OK
