@@ -268,6 +268,7 @@ def run_gpu(args, rank, world):
     calib = calibration(args, bs, dev, stream, flush, dq, dk_, dv_, dqd, dkd, lp, ld, pbits)
     blocks = block_set_sweep(args, bs, dev, stream, flush, dq, dk_, dv_, lp, po, plse, pbits)
     santa = santa_sweep(args, bs, dev, stream, flush)
+    varlen = varlen_sweep(args, bs, dev, stream, flush)
 
     # ---- the timed region: K steps of the whole hot path at ~70 % ---------
     fp, fd = prefill(lp[TARGET]), decode(ld[TARGET])
@@ -353,6 +354,7 @@ def run_gpu(args, rank, world):
         "calibration": calib,
         "block_set": blocks,
         "santa_decode": santa,
+        "varlen_prefill": varlen,
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,  # prefill, decode, merge per timed step
         "clocks": clk.summary(),
@@ -457,6 +459,72 @@ def santa_sweep(args, bs, dev, stream, flush):
     out["exact_decode_ms"] = round(ms, 4)
     for mode in ("sys", "strat"):
         out[mode]["speedup_vs_exact"] = round(ms / out[mode]["ms"], 4)
+    return out
+
+
+def varlen_sweep(args, bs, dev, stream, flush):
+    """Batched variable-length prefill (16 sequences, 129 to 16384 tokens,
+    65,536 in all) with lambda_s = a / L_s.  ``a`` is calibrated in one pass
+    for ~70 % sparsity of the whole batch: the statistics mode gives each
+    traversed block's statistic mu, a block of sequence s is skipped when
+    mu < ln(a) - ln(L_s), so ln(a) is placed between the shifted statistics
+    mu + ln(L_s) around the target quantile.  Timed: the packed call at a / L_s
+    and at lambda = 0, and the same work as one fixed-length call per sequence."""
+    C = W.VARLEN_PREFILL_64K
+    q, k, v, cu = W.varlen_inputs(C)
+    dq, dk_, dv_, dcu = (x.to(dev) for x in (q, k, v, cu))
+    cu_np = cu.numpy()
+    seqs = []
+    for s in range(C.n_seq):
+        c0, c1 = int(cu_np[s]), int(cu_np[s + 1])
+        seqs.append(tuple(x[c0:c1].transpose(0, 1)[None].contiguous().to(dev)
+                          for x in (q, k, v)))
+    del q, k, v
+    shifted, pairs = [], 0
+    for s, (qs, ks, _) in enumerate(seqs):
+        mu = bs.attn_skip_prefill_margins(qs, ks, 128, 128, True).cpu().numpy().ravel()
+        mu = mu[~np.isnan(mu)]
+        pairs += mu.size
+        shifted.append(mu[mu < 0] + math.log(C.lengths[s]))  # mu = 0 is never skipped
+    x = np.sort(np.concatenate(shifted))
+    kk = min(int(round(float(TARGET) * pairs)), x.size)
+    ln_a = 0.5 * (x[kk - 1] + x[kk]) if kk < x.size else x[-1] + 1e-3
+    a = math.exp(ln_a)
+    lam = [min(a / L, math.nextafter(1.0, 0.0)) for L in C.lengths]
+    dl = torch.tensor(lam, dtype=torch.float32, device=dev)
+    dl0 = torch.zeros(C.n_seq, dtype=torch.float32, device=dev)
+    o = torch.empty(C.total, C.Hq, C.d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(C.Hq, C.total, dtype=torch.float32, device=dev)
+    bits = torch.empty(bs.varlen_bitmap_shape(C.n_seq, C.Hq, C.max_seqlen), dtype=torch.int32,
+                       device=dev)
+    out = {"workload": f"{C.name}: {C.n_seq} sequences, lengths {list(C.lengths)}, "
+                       f"Hq{C.Hq} Hkv{C.Hkv} d{C.d} causal; lambda_s = a / L_s",
+           "a": a}
+    dense = sum(4.0 * C.d * C.Hq * L * (L + 1) / 2 for L in C.lengths)
+    per_pair = 2.0 * 128 * 128 * C.d
+    for name, lmb in (("0.0", dl0), ("a_over_L", dl)):
+        durs = timed_launches(
+            lambda: bs.attn_skip_prefill_varlen(dq, dk_, dv_, dcu, C.max_seqlen, lmb,
+                                                out=(o, lse, bits)),
+            args.warmup, args.steps, flush, stream)
+        ms = statistics.mean(durs)
+        skipped = int(bs.unpack_bits(bits, bits.shape[2]).sum())
+        executed = per_pair * (2 * pairs - skipped)
+        out[name] = {"ms": round(ms, 4), "sparsity": round(skipped / pairs, 4),
+                     "dense_equiv_tflops": round(dense / ms / 1e9, 2),
+                     "executed_tflops": round(executed / ms / 1e9, 2)}
+    out["a_over_L"]["speedup_vs_lambda0"] = round(out["0.0"]["ms"] / out["a_over_L"]["ms"], 4)
+    outs = [(torch.empty_like(qs), torch.empty(qs.shape[:3], dtype=torch.float32, device=dev),
+             torch.empty(bs.prefill_bitmap_shape(1, C.Hq, qs.shape[2], 128, 128),
+                         dtype=torch.int32, device=dev)) for qs, _, _ in seqs]
+
+    def per_sequence():
+        for (qs, ks, vs), ob, lm in zip(seqs, outs, lam):
+            bs.attn_skip_prefill(qs, ks, vs, lm, 128, 128, True, out=ob)
+
+    ms = statistics.mean(timed_launches(per_sequence, args.warmup, args.steps, flush, stream))
+    out["per_sequence_calls_ms"] = round(ms, 4)
+    out["a_over_L"]["speedup_vs_per_sequence_calls"] = round(ms / out["a_over_L"]["ms"], 4)
     return out
 
 

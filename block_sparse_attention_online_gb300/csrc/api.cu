@@ -178,7 +178,9 @@ extern "C" attn_status attn_skip_prefill_varlen(const void *q, const void *k, co
   if (dt != ATTN_BF16 || dk != 128 || dv != 128 || Br != 128 || Bc != 128)
     return ATTN_EUNSUPPORTED;
   const long n_t = (max_seqlen + 127L) / 128;
-  if ((long)n_seq * Hq * n_t > 0x7fffffffL) return ATTN_EUNSUPPORTED;
+  if ((long)n_seq * Hq * n_t > 0x7fffffffL ||
+      (long)Hq * ((total + 127L) / 128 + n_seq) > 0x7fffffffL)
+    return ATTN_EUNSUPPORTED;
   if (n_t == 0) return ATTN_OK;  // every sequence is empty: no tile, no bitmap word
   if (total == 0)                 // every sequence is empty: only the bitmap to clear
     return from_cuda(cudaMemsetAsync(skip_bits, 0,

@@ -78,6 +78,13 @@ constexpr uint32_t IDESC_QK = idesc_bf16_f32(BM, BN, 0);  // K: K-major
 constexpr uint32_t IDESC_PV = idesc_bf16_f32(BM, D, 1);   // V: MN-major
 constexpr uint32_t NEG_INF_BITS = 0xff800000u;
 
+// A tile of a variable-length batch: sequence s (-1: no tile for this CTA),
+// tile index t, the sequence's first token and length, ln(lambda_s).
+struct VarTile {
+  int s, t, c0, len;
+  float ln_lam;
+};
+
 struct Shared {
   uint64_t q_full;
   uint64_t k_full[NK], k_empty[NK];
@@ -101,6 +108,7 @@ struct Shared {
   // the deciders to the exponential warps.
   float mdec[NS][128];
   float lfin[128], mfin[128];  // row sum and exp reference for the epilogue
+  VarTile vt;                  // varlen: this CTA's tile
   uint32_t tmem_base;
   int abort;
 };
@@ -191,6 +199,171 @@ __device__ __forceinline__ void chunk_exp(const uint32_t (&s)[32], uint64_t sl2x
   }
 }
 
+// ---------------------------------------------------------- varlen schedule --
+// The tiles of a variable-length batch run in decreasing tile index t (the
+// longest causal tiles first, as in the fixed-length grid), then increasing
+// sequence index; CTA i * Hq + h runs the i-th tile of that order for query
+// head h.  The grid holds Hq * (ceil(total / Br) + n_seq) CTAs, at least one
+// per tile; a CTA past the last tile clears the bitmap rows of empty
+// sequences.  One warp locates its CTA's tile: with nt(s) the tile count of
+// sequence s, C(t) = sum_s max(0, nt(s) - t - 1) tiles lie at levels above t,
+// so the tile's level is the smallest t with C(t) <= i (bisection) and its
+// sequence the (i - C(t))-th one, in index order, with nt(s) > t.
+constexpr int kVarCache = 4;  // sequences 0..127 are served from registers
+
+// Length of sequence s, or -1 when its bounds are out of range.
+__device__ __forceinline__ int var_len(const PrefillArgs &a, int s) {
+  const int c0 = __ldg(a.cu_seqlens + s), c1 = __ldg(a.cu_seqlens + s + 1);
+  return (c0 < 0 || c1 < c0 || c1 - c0 > a.T || c1 > a.total) ? -1 : c1 - c0;
+}
+
+__device__ __forceinline__ int tiles_of(int len) { return len > 0 ? (len + BM - 1) / BM : 0; }
+
+// Batches of up to 32 sequences (one per lane): a short, branch-light path,
+// since this code runs once per CTA from a cold instruction cache.
+__device__ __forceinline__ bool varlen_locate_small(const PrefillArgs &a, int i, int h, int lane,
+                                                    VarTile *out) {
+  int c0 = 0, c1 = 0;
+  float lam = 0.f;
+  if (lane < a.B) {
+    c0 = __ldg(a.cu_seqlens + lane);
+    c1 = __ldg(a.cu_seqlens + lane + 1);
+    lam = __ldg(a.lambda_seq + lane);
+  }
+  const bool bad = c0 < 0 || c1 < c0 || c1 - c0 > a.T || c1 > a.total;
+  const int len = bad ? -1 : c1 - c0;
+  const int nt = tiles_of(len);
+  if (i >= (int)__reduce_add_sync(0xffffffffu, (unsigned)nt)) return false;
+  int lo = 0, hi = a.n_t - 1;  // smallest t with C(t) <= i
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if ((int)__reduce_add_sync(0xffffffffu, (unsigned)max(0, nt - mid - 1)) <= i) hi = mid;
+    else lo = mid + 1;
+  }
+  const int r = i - (int)__reduce_add_sync(0xffffffffu, (unsigned)max(0, nt - lo - 1));
+  const unsigned m = __ballot_sync(0xffffffffu, nt > lo);
+  const bool mine = nt > lo && __popc(m & ((2u << lane) - 1u)) == r + 1;
+  const int s = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+  const int sc0 = __shfl_sync(0xffffffffu, c0, s), slen = __shfl_sync(0xffffffffu, len, s);
+  const float slam = __shfl_sync(0xffffffffu, lam, s);
+  if (lane == 0)
+    *out = VarTile{s, lo, sc0, slen, (slam > 0.f && slam < 1.f) ? logf(slam) : -INFINITY};
+  if (lo == tiles_of(slen) - 1) {  // the sequence's last tile clears the rows past it
+    uint32_t *bw = a.bits + ((size_t)(s * a.Hq + h) * a.n_t + lo + 1) * a.words;
+    for (int w = lane; w < (a.n_t - lo - 1) * a.words; w += 32) bw[w] = 0u;
+  }
+  if (i == 0 && h == 0 &&
+      __any_sync(0xffffffffu, lane < a.B && (len < 0 || !(lam >= 0.f && lam < 1.f))) &&
+      lane == 0)
+    atomicOr(a.err, kErrBadArg);
+  return true;
+}
+
+// Everything the CTA needs is read in one round of loads at the start (the
+// first sequences' bounds and thresholds, kept in registers); the tile's own
+// values then come from the lane that holds them.
+__device__ __noinline__ void varlen_locate(const PrefillArgs &a, int i, int grid_tiles, int h,
+                                           int lane, VarTile *out) {
+  const int nch = (a.B + 31) / 32;
+  int c0c[kVarCache], lenc[kVarCache];
+  float lamc[kVarCache];
+#pragma unroll
+  for (int c = 0; c < kVarCache; ++c) {
+    const int s = c * 32 + lane;
+    int c0 = 0, c1 = 0;
+    float lam = 0.f;
+    if (s < a.B) {
+      c0 = __ldg(a.cu_seqlens + s);
+      c1 = __ldg(a.cu_seqlens + s + 1);
+      lam = __ldg(a.lambda_seq + s);
+    }
+    const bool bad = c0 < 0 || c1 < c0 || c1 - c0 > a.T || c1 > a.total;
+    c0c[c] = c0;
+    lenc[c] = bad ? -1 : c1 - c0;
+    lamc[c] = lam;
+  }
+  auto nt_chunk = [&](int c) {  // tile count of sequence 32 c + lane (0 past the batch)
+    if (c >= kVarCache) {
+      const int s = c * 32 + lane;
+      return s < a.B ? tiles_of(var_len(a, s)) : 0;
+    }
+    int v = 0;
+#pragma unroll
+    for (int k = 0; k < kVarCache; ++k) v = k == c ? lenc[k] : v;
+    return tiles_of(v);
+  };
+  auto above = [&](int t) {  // C(t)
+    int sum = 0;
+    for (int c = 0; c < nch; ++c)
+      sum += (int)__reduce_add_sync(0xffffffffu, (unsigned)max(0, nt_chunk(c) - t - 1));
+    return sum;
+  };
+  const int n_tiles = above(-1);
+  if (i >= n_tiles) {
+    // No tile: clear the rows of the empty sequences e, e + n_extra, ...
+    const int e = i - n_tiles, n_extra = grid_tiles - n_tiles;
+    for (int s = e; s < a.B; s += n_extra) {
+      if (var_len(a, s) > 0) continue;
+      uint32_t *bw = a.bits + (size_t)(s * a.Hq + h) * a.n_t * a.words;
+      for (int w = lane; w < a.n_t * a.words; w += 32) bw[w] = 0u;
+    }
+    if (lane == 0) *out = VarTile{-1, 0, 0, 0, -INFINITY};
+    return;
+  }
+  int lo = 0, hi = a.n_t - 1;  // smallest t with C(t) <= i
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (above(mid) <= i) hi = mid;
+    else lo = mid + 1;
+  }
+  const int t = lo;
+  int r = i - above(t), s = -1;
+  for (int c = 0; c < nch && s < 0; ++c) {
+    const unsigned m = __ballot_sync(0xffffffffu, nt_chunk(c) > t);
+    const int n = __popc(m);
+    if (r < n) {
+      const unsigned upto = (2u << lane) - 1u;  // bits 0..lane
+      const bool mine = ((m >> lane) & 1u) && __popc(m & upto) == r + 1;
+      s = c * 32 + __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+    } else {
+      r -= n;
+    }
+  }
+  int c0 = 0, len = 0;
+  float lam = 0.f;
+  if ((s >> 5) < kVarCache) {
+    int v0 = 0, v1 = 0;
+    float v2 = 0.f;
+#pragma unroll
+    for (int k = 0; k < kVarCache; ++k) {
+      v0 = k == (s >> 5) ? c0c[k] : v0;
+      v1 = k == (s >> 5) ? lenc[k] : v1;
+      v2 = k == (s >> 5) ? lamc[k] : v2;
+    }
+    c0 = __shfl_sync(0xffffffffu, v0, s & 31);
+    len = __shfl_sync(0xffffffffu, v1, s & 31);
+    lam = __shfl_sync(0xffffffffu, v2, s & 31);
+  } else {
+    c0 = __ldg(a.cu_seqlens + s);
+    len = var_len(a, s);
+    lam = __ldg(a.lambda_seq + s);
+  }
+  if (lane == 0)
+    *out = VarTile{s, t, c0, len, (lam > 0.f && lam < 1.f) ? logf(lam) : -INFINITY};
+  if (t == tiles_of(len) - 1) {  // the sequence's last tile clears the rows past it
+    uint32_t *bw = a.bits + ((size_t)(s * a.Hq + h) * a.n_t + t + 1) * a.words;
+    for (int w = lane; w < (a.n_t - t - 1) * a.words; w += 32) bw[w] = 0u;
+  }
+  if (i == 0 && h == 0) {  // one CTA reports out-of-range lengths or thresholds
+    bool bad = false;
+    for (int q = lane; q < a.B; q += 32) {
+      const float lq = __ldg(a.lambda_seq + q);
+      bad |= var_len(a, q) < 0 || !(lq >= 0.f && lq < 1.f);
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.err, kErrBadArg);
+  }
+}
+
 // STATS: the statistics mode; SET: an explicit block set per tile (blocks
 // outside it are not traversed); VARLEN: a batch of sequences of different
 // lengths packed token-major, each with its own threshold.  Each is compiled
@@ -210,47 +383,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (tid == 0) atomicOr(a.err, kErrTimeout);
     return;
   }
-
-  // Longest causal tiles first: blocks are ordered by decreasing tile index.
-  const int BH = a.B * a.Hq;
-  const int t = a.n_t - 1 - (int)(blockIdx.x / BH);
-  const int bh = (int)(blockIdx.x % BH);
-  const int h = bh % a.Hq, b = bh / a.Hq;
-  const int hk = h / (a.Hq / a.Hkv);
-  // Varlen: sequence b holds tokens [off, off + T) of the packed tensors; a
-  // tile past its end has no row, only bitmap words to clear.  A length or a
-  // threshold outside its range raises the bad-argument bit; the sequence is
-  // then treated as empty, the threshold as 0.
-  int T = a.T, off = 0;
-  float ln_lam = a.ln_lambda;
-  if constexpr (VARLEN) {
-    const int c0 = __ldg(a.cu_seqlens + b), c1 = __ldg(a.cu_seqlens + b + 1);
-    const float lam = __ldg(a.lambda_seq + b);
-    const bool bad_len = c0 < 0 || c1 < c0 || c1 - c0 > a.T || c1 > a.total;
-    const bool bad_lam = !(lam >= 0.f && lam < 1.f);
-    if ((bad_len || bad_lam) && tid == 0 && h == 0 && t == 0) atomicOr(a.err, kErrBadArg);
-    T = bad_len ? 0 : c1 - c0;
-    off = bad_len ? 0 : c0;
-    ln_lam = (bad_lam || !(lam > 0.f)) ? -INFINITY : logf(lam);
-    if (t * BM >= T) {
-      uint32_t *bw = a.bits + ((size_t)bh * a.n_t + t) * a.words;
-      for (int w = tid; w < a.words; w += NTHREADS) bw[w] = 0u;
-      return;
-    }
-  }
-  const int row0 = t * BM;
-  const int last_row = min(T, row0 + BM) - 1;
-  const int nblk = a.causal ? last_row / BN + 1 : (VARLEN ? (T + BN - 1) / BN : a.n_b);
-  volatile int *abort = &sh.abort;
-  const int zq = b * a.Hq + h, zkv = b * a.Hkv + hk;
-  // TMA coordinates (column, y, z) of query rows / key block j: [heads, T, 128]
-  // maps take (row, head); the token-major varlen maps [total, heads, 128]
-  // take (head, token).
-  const int q_y = VARLEN ? h : row0, q_z = VARLEN ? off + row0 : zq;
-  auto kv_y = [&](int j) { return VARLEN ? hk : j * BN; };
-  auto kv_z = [&](int j) { return VARLEN ? off + j * BN : zkv; };
-  const uint32_t *set_words = SET ? a.block_set + ((size_t)bh * a.n_t + t) * a.words : nullptr;
-  auto in_set = [&](int j) { return ((__ldg(set_words + (j >> 5)) >> (j & 31)) & 1u) != 0u; };
 
   if (tid == 0) {
     mbar_init(smem_u32(&sh.q_full), 1);
@@ -281,12 +413,54 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     fence_mbar_init();
   }
   if (warp == WARP_MMA) tmem_alloc(smem_u32(&sh.tmem_base), TMEM_COLS);
+  // Varlen: the V-producer warp locates this CTA's tile while the barriers and
+  // TMEM are set up.
+  if constexpr (VARLEN) {
+    if (warp == WARP_V) {
+      const int i = (int)(blockIdx.x / a.Hq), h = (int)(blockIdx.x % a.Hq);
+      if (a.B > 32 || !varlen_locate_small(a, i, h, lane, &sh.vt))
+        varlen_locate(a, i, (int)(gridDim.x / a.Hq), h, lane, &sh.vt);
+    }
+  }
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
   const uint32_t tmem = sh.tmem_base;
 
-  if (warp == WARP_K) {
+  // Varlen: sequence b holds tokens [off, off + T) of the packed tensors.  A
+  // length or a threshold outside its range raises the bad-argument bit; the
+  // sequence is then treated as empty, the threshold as 0.
+  VarTile vt{};
+  if constexpr (VARLEN) vt = sh.vt;
+  const bool has_tile = !VARLEN || vt.s >= 0;  // varlen: a CTA past the last tile has none
+  // Longest causal tiles first: blocks are ordered by decreasing tile index.
+  const int BH = a.B * a.Hq;
+  const int t = VARLEN ? vt.t : a.n_t - 1 - (int)(blockIdx.x / BH);
+  const int h = VARLEN ? (int)(blockIdx.x % a.Hq) : (int)(blockIdx.x % BH) % a.Hq;
+  const int b = VARLEN ? vt.s : (int)(blockIdx.x % BH) / a.Hq;
+  const int bh = b * a.Hq + h;
+  const int hk = h / (a.Hq / a.Hkv);
+  const int T = VARLEN ? vt.len : a.T;
+  const int off = VARLEN ? vt.c0 : 0;
+  const float ln_lam = VARLEN ? vt.ln_lam : a.ln_lambda;
+  const int row0 = t * BM;
+  const int last_row = min(T, row0 + BM) - 1;
+  const int nblk = a.causal ? last_row / BN + 1 : (VARLEN ? (T + BN - 1) / BN : a.n_b);
+  volatile int *abort = &sh.abort;
+  const int zq = b * a.Hq + h, zkv = b * a.Hkv + hk;
+  // TMA coordinates (column, y, z) of query rows / key block j: [heads, T, 128]
+  // maps take (row, head); the token-major varlen maps [total, heads, 128]
+  // take (head, token).
+  const int q_y = VARLEN ? h : row0, q_z = VARLEN ? off + row0 : zq;
+  auto kv_y = [&](int j) { return VARLEN ? hk : j * BN; };
+  auto kv_z = [&](int j) { return VARLEN ? off + j * BN : zkv; };
+  const uint32_t *set_words = SET ? a.block_set + ((size_t)bh * a.n_t + t) * a.words : nullptr;
+  auto in_set = [&](int j) { return ((__ldg(set_words + (j >> 5)) >> (j & 31)) & 1u) != 0u; };
+
+
+  if (!has_tile) {
+    // varlen: no tile for this CTA (its bitmap clearing is done)
+  } else if (warp == WARP_K) {
     // -------------------------------------------------------- Q/K producer --
     if (lane == 0) {
       prefetch_tmap(&tm_q);
@@ -718,7 +892,10 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_ALLOC);
   if (e != cudaSuccess) return e;
-  const long units = (long)a.B * a.Hq * a.n_t;
+  // Varlen: at least one CTA per tile (a sequence of L tokens has ceil(L/Br)
+  // tiles, so there are at most ceil(total/Br) + n_seq of them).
+  const long units = a.cu_seqlens ? (long)a.Hq * ((a.total + BM - 1) / BM + a.B)
+                                  : (long)a.B * a.Hq * a.n_t;
   kernel<<<(unsigned)units, NTHREADS, SMEM_ALLOC, s>>>(mq, mk, mv, a);
   return cudaGetLastError();
 }
