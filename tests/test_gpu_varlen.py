@@ -1,7 +1,6 @@
 """Batched variable-length prefill (one threshold per sequence) on the GPU
 against the fp64 oracle, and against the fixed-length kernel run on each
 sequence alone."""
-import math
 
 import numpy as np
 import pytest
@@ -150,3 +149,31 @@ def test_varlen_empty_batch_and_bad_device_arguments():
         bs.attn_skip_last_device_error()
     assert e.value.status == bs.ATTN_EINVAL
     bs.attn_skip_last_device_error()  # cleared
+
+
+@pytest.mark.parametrize("n_seq", [33, 150])
+def test_varlen_many_sequences(n_seq):
+    """More sequences than one warp holds (33) and than the registers cache
+    (150): the general tile locator; empty sequences among them."""
+    g = np.random.default_rng(n_seq)
+    lens = tuple(int(x) for x in g.choice([0, 1, 64, 128, 129, 200, 383, 700], size=n_seq))
+    cfg = W.VarlenConfig("t", lens, 4, 2, 128, sink_a=3.0, salient_a=1.5, seed=65)
+    q, k, v, cu = W.varlen_inputs(cfg)
+    lams = torch.tensor(g.choice([0.0, 1e-3, 3e-2], size=n_seq), dtype=torch.float32)
+    check_varlen(cfg, q, k, v, cu, lams, seqs=range(0, n_seq, 7))
+    dev = torch.device("cuda")
+    o, lse, bits = bs.attn_skip_prefill_varlen(q.to(dev), k.to(dev), v.to(dev), cu.to(dev),
+                                               cfg.max_seqlen, lams.to(dev))
+    bs.attn_skip_last_device_error()
+    cu_np = cu.numpy()
+    for s in range(n_seq):
+        c0, c1 = int(cu_np[s]), int(cu_np[s + 1])
+        if c1 == c0:
+            assert not bits[s].any()
+            continue
+        qs, ks, vs = (x[c0:c1].transpose(0, 1)[None].contiguous().to(dev) for x in (q, k, v))
+        o1, lse1, b1 = bs.attn_skip_prefill(qs, ks, vs, float(lams[s]), 128, 128, True)
+        assert torch.equal(o[c0:c1].transpose(0, 1), o1[0]), f"sequence {s}"
+        assert torch.equal(lse[:, c0:c1], lse1[0])
+        assert torch.equal(bits[s, :, :b1.shape[2], :b1.shape[3]], b1[0])
+        assert not bits[s, :, b1.shape[2]:].any()
