@@ -333,6 +333,34 @@ def decode_inputs(cfg: DecodeConfig, batches=None):
     return q, k, v
 
 
+def decode_inputs_fp8(cfg: DecodeConfig, pow2_scales: bool = True):
+    """The decode draws with an FP8 (E4M3) key/value cache: returns ``(q,
+    k8, v8, k_scale, v_scale)`` with q bf16 ``[B, Hq, dk]``, k8 and v8 uint8
+    E4M3 codes ``[B, Hkv, L, d]`` and fp32 scales ``[B, Hkv]``.  Each (sequence,
+    KV head) slice of the bf16 draws is quantised with scale = amax / 448
+    (rounded up to a power of two when ``pow2_scales``), codes = E4M3(x /
+    scale) rounded to nearest even (torch's conversion)."""
+    q, k, v = decode_inputs(cfg)
+
+    def quant(x):
+        xf = x.float()
+        amax = xf.abs().amax(dim=(2, 3)).clamp_min(1e-30)
+        sc = amax / 448.0
+        if pow2_scales:
+            sc = torch.exp2(torch.ceil(torch.log2(sc)))
+        codes = (xf / sc[:, :, None, None]).to(torch.float8_e4m3fn).view(torch.uint8)
+        return codes.contiguous(), sc.to(torch.float32).contiguous()
+
+    k8, ks = quant(k)
+    v8, vs = quant(v)
+    return q, k8, v8, ks, vs
+
+
+# The GQA decode shape with the key/value cache in FP8 (E4M3) and one scale
+# per (sequence, KV head) for keys and for values.
+GQA_DECODE_FP8_32K = GQA_DECODE_32K.with_(name="gqa_decode_fp8_B16_L32768", seed=1241)
+
+
 def santa_offsets(cfg: DecodeConfig, n_samples: int, mode: str, seed: int = 0) -> torch.Tensor:
     """Uniform draws in [0, 1) for the sampled decode (fp32, one generator per
     (sequence, query head)): ``[B, Hq]`` for the systematic sampler (one

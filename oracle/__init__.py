@@ -20,6 +20,10 @@ Parity status of each function (what pins it, in ``tests/test_oracle.py``):
   ``tests/golden/``; brute-force recomputation of each skip bit.
 * ``combine``: lambda = 0 merged decode equals dense single-pass attention;
   one split is the identity.
+* ``decode_fp8``: the E4M3 decoding it relies on equals an independent
+  bit-level decoder over all 256 codes; at lambda = 0 the merged output equals
+  a brute-force fp64 softmax over the scaled decoded rows (key scale in the
+  scores, value scale on the output), for scales that are not powers of two.
 * ``prefill_varlen``: each packed sequence at lambda = 0 equals torch's fp64
   SDPA on that sequence alone; with thresholds, each sequence's output is the
   softmax over its own kept tokens, a larger lambda skips a superset of
@@ -226,6 +230,52 @@ def decode(q, k, v, scale, lam, Bc, n_splits, dv=None, units=None, force_skip=No
                                    _ptr(o_part), _ptr(lse_part), _ptr(skip), _ptr(margin))
     if rc:
         raise ValueError("bsa_oracle_decode: invalid arguments")
+    return {"o_part": o_part, "lse_part": lse_part, "skip": skip, "margin": margin}
+
+
+def decode_fp8(q, k8, v8, k_scale, v_scale, scale, lam, Bc, n_splits, units=None,
+               force_skip=None):
+    """Split-KV thresholded decode over an FP8 (E4M3) key/value cache, fp64.
+
+    Reading (the pages name FP8/NVFP4 models but define no cache format): the
+    cache holds E4M3 codes ``k8``, ``v8`` ``[B,Hkv,L,d]`` (uint8 bit patterns)
+    and one fp32 scale per (sequence, KV head); the key and value rows are
+    ``k_scale[b,h] * decode(k8)`` and ``v_scale[b,h] * decode(v8)``.  The
+    scale of a key row multiplies its scores, so it is folded into the score
+    scale (``scale * k_scale``, exact in double); the value scale multiplies
+    the split outputs.  Each (b, h) slice then runs :func:`decode` on the
+    decoded codes, which are exact in fp32.  ``units`` / ``force_skip`` as for
+    :func:`decode`.  Returns the same dict."""
+    import torch
+    q = _f32(q)
+    B, Hq, dk = q.shape
+    k8 = torch.as_tensor(np.ascontiguousarray(k8, dtype=np.uint8))
+    v8 = torch.as_tensor(np.ascontiguousarray(v8, dtype=np.uint8))
+    kf = k8.view(torch.float8_e4m3fn).float().numpy()
+    vf = v8.view(torch.float8_e4m3fn).float().numpy()
+    _, Hkv, L, _ = kf.shape
+    dv = vf.shape[3]
+    ks = np.asarray(k_scale, dtype=np.float32).reshape(B, Hkv)
+    vs = np.asarray(v_scale, dtype=np.float32).reshape(B, Hkv)
+    G = Hq // Hkv
+    n_b = -(-L // Bc)
+    bps = -(-n_b // n_splits)
+    o_part = np.zeros((B, Hq, n_splits, dv))
+    lse_part = np.full((B, Hq, n_splits), np.nan)
+    skip = np.zeros((B, Hkv, n_splits, bps), dtype=np.uint8)
+    margin = np.full((B, Hkv, n_splits, bps), np.nan)
+    want = None if units is None else set(int(x) // n_splits for x in np.asarray(units).ravel())
+    for b in range(B):
+        for h in range(Hkv):
+            if want is not None and (b * Hkv + h) not in want:
+                continue
+            fs = None if force_skip is None else np.asarray(force_skip)[b:b + 1, h:h + 1]
+            r = decode(q[b:b + 1, h * G:(h + 1) * G], kf[b:b + 1, h:h + 1], vf[b:b + 1, h:h + 1],
+                       float(scale) * float(ks[b, h]), lam, Bc, n_splits, force_skip=fs)
+            o_part[b, h * G:(h + 1) * G] = r["o_part"][0] * float(vs[b, h])
+            lse_part[b, h * G:(h + 1) * G] = r["lse_part"][0]
+            skip[b, h] = r["skip"][0, 0]
+            margin[b, h] = r["margin"][0, 0]
     return {"o_part": o_part, "lse_part": lse_part, "skip": skip, "margin": margin}
 
 
