@@ -269,6 +269,7 @@ def run_gpu(args, rank, world):
     blocks = block_set_sweep(args, bs, dev, stream, flush, dq, dk_, dv_, lp, po, plse, pbits)
     santa = santa_sweep(args, bs, dev, stream, flush)
     varlen = varlen_sweep(args, bs, dev, stream, flush)
+    fp8 = fp8_decode_sweep(args, bs, dev, stream, flush, lam)
 
     # ---- the timed region: K steps of the whole hot path at ~70 % ---------
     fp, fd = prefill(lp[TARGET]), decode(ld[TARGET])
@@ -355,6 +356,7 @@ def run_gpu(args, rank, world):
         "block_set": blocks,
         "santa_decode": santa,
         "varlen_prefill": varlen,
+        "fp8_decode": fp8,
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,  # prefill, decode, merge per timed step
         "clocks": clk.summary(),
@@ -459,6 +461,46 @@ def santa_sweep(args, bs, dev, stream, flush):
     out["exact_decode_ms"] = round(ms, 4)
     for mode in ("sys", "strat"):
         out[mode]["speedup_vs_exact"] = round(ms / out[mode]["ms"], 4)
+    return out
+
+
+def fp8_decode_sweep(args, bs, dev, stream, flush, lam):
+    """Decode over an FP8 (E4M3) key/value cache, the GQA decode shape (B=16,
+    32/8 heads, L=32768, 8 splits), at lambda = 0 and the oracle's ~70 %
+    threshold, decode + merge; bytes = key codes + kept value codes + Q +
+    partials."""
+    C = W.GQA_DECODE_FP8_32K
+    q, k8, v8, ks, vs = W.decode_inputs_fp8(C)
+    dq, dk8, dv8, dks, dvs = (x.to(dev) for x in (q, k8, v8, ks, vs))
+    del q, k8, v8
+    n_b = -(-C.L // C.Bc)
+    blocks = C.B * C.Hkv * n_b
+    op = torch.empty(C.B, C.Hq, C.n_splits, C.dv, dtype=torch.float32, device=dev)
+    lpart = torch.empty(C.B, C.Hq, C.n_splits, dtype=torch.float32, device=dev)
+    bits = torch.empty(bs.decode_bitmap_shape(C.B, C.Hkv, C.L, C.Bc, C.n_splits),
+                       dtype=torch.int32, device=dev)
+    o = torch.empty(C.B, C.Hq, C.dv, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(C.B, C.Hq, dtype=torch.float32, device=dev)
+    out = {"workload": f"{C.name}: B{C.B} Hq{C.Hq} Hkv{C.Hkv} d{C.dk} L{C.L} Bc{C.Bc} "
+                       f"splits{C.n_splits}, E4M3 codes, one scale per (sequence, KV head)"}
+    for t in ("0.0", TARGET):
+        lmb = lam[C.name][t]["lambda"]
+        durs = timed_launches(
+            lambda: bs.attn_skip_decode_fp8(dq, dk8, dv8, dks, dvs, lmb, C.Bc, C.n_splits,
+                                            out=(op, lpart, bits)),
+            args.warmup, args.steps, flush, stream)
+        cdurs = timed_launches(lambda: bs.attn_skip_decode_combine(op, lpart, out=(o, lse)),
+                               args.warmup, args.steps, flush, stream)
+        skipped = int(bs.unpack_bits(bits, -(-n_b // C.n_splits)).sum())
+        kept = blocks - skipped
+        byts = (blocks + kept) * C.Bc * C.dk + C.B * C.Hq * C.dk * 2 + op.numel() * 4 * 2
+        ms, cms = statistics.mean(durs), statistics.mean(cdurs)
+        out[t] = {"lambda": lmb, "sparsity": round(skipped / blocks, 4), "ms_decode": round(ms, 4),
+                  "ms_combine": round(cms, 4), "tok_per_s": round(C.B / ((ms + cms) / 1e3), 1),
+                  "gbs": round(byts / ms / 1e6, 1), "bytes": byts}
+    out[TARGET]["speedup_vs_lambda0"] = round(
+        (out["0.0"]["ms_decode"] + out["0.0"]["ms_combine"])
+        / (out[TARGET]["ms_decode"] + out[TARGET]["ms_combine"]), 4)
     return out
 
 

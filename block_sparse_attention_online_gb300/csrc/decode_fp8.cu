@@ -1,0 +1,630 @@
+// Split-KV decode with softmax-threshold block skipping over an FP8 (E4M3)
+// key/value cache (d = 128, Bc = 128), on the tensor cores.
+//
+// Method: the BLASST page, sections "BLASST 的判定准则" (Eq. 5) and "Decode 内核：
+// 砍带宽": the scores of a block decide whether its values are read at all;
+// the cache format is E4M3 codes with one fp32 scale per (sequence, KV head)
+// for keys and for values (the page evaluates FP8/NVFP4 models and names no
+// cache format; this is the plainest one).  Decode is bound by the cache
+// bytes, so halving them halves the time of the same schedule.
+//
+// The structure is that of the bf16 decode kernel (the G query heads sharing
+// a KV head padded to the 128 rows of a tcgen05 MMA, one softmax warp holding
+// each head's 128 scores in one thread, the group-AND decision, values loaded
+// only for kept blocks), with two conversion stages: E4M3 tiles arrive by TMA
+// (16 KB per 128-key block) and converter warps widen them, exactly, to fp16
+// tiles in the 128-byte-swizzled layout the MMA reads.  fp16 because the
+// conversion is one instruction per pair of codes and every E4M3 value is an
+// fp16 value; Q (bf16, widened to fp16 once, in TMEM as the A operand) and P
+// (fp16) follow.  The key scale multiplies the scores (folded into the score
+// scale), the value scale the split outputs.
+//
+// Warp roles (288 threads):
+//   warp 0      softmax: lane g < G owns head g (TMEM lane g);
+//   warp 1      TMA producer of the E4M3 key tiles (every block, 4 stages);
+//   warp 2      Q.K^T issuer (A = Q from TMEM, B = fp16 K tile; allocates TMEM);
+//   warp 3      TMA producer of the E4M3 value tiles of kept blocks (2 stages);
+//   warp 4      P.V issuer (A = P from TMEM, B = fp16 V tile);
+//   warps 5-6   key converters (two key rows per thread);
+//   warps 7-8   value converters (follow the decisions; two key rows each).
+// Before the first block warps 5-8, one per TMEM lane quarter, write Q into
+// TMEM.
+// TMEM columns: S buffers [0,256), P [256,320), Q [320,384), O [384,512).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <math.h>
+
+#include "internal.h"
+#include "tc_common.cuh"
+
+namespace attn_skip {
+namespace {
+
+using namespace tc;
+
+constexpr int D = 128;    // head size (keys and values)
+constexpr int BC = 128;   // keys per block
+constexpr int MR = 128;   // MMA rows (heads padded)
+constexpr int NKF = 4;    // E4M3 key stages
+constexpr int NKH = 2;    // fp16 key stages
+constexpr int NVF = 2;    // E4M3 value stages
+constexpr int NVH = 2;    // fp16 value stages
+constexpr int NS = 2;     // TMEM S buffers
+constexpr int NDEC = 8;   // decision ring
+constexpr int NT = 9 * 32;
+constexpr int WARP_K = 1, WARP_QK = 2, WARP_V = 3, WARP_PV = 4;  // warp 0: softmax
+constexpr int WARP_KC = 5, WARP_VC = 7;                           // two warps each
+constexpr uint32_t F8_BYTES = BC * D;           // 16 KB: 128 keys x 128 codes
+constexpr uint32_t H_BYTES = BC * D * 2;        // 32 KB: 128 keys x 128 fp16
+constexpr uint32_t HALF_BYTES = H_BYTES / 2;    // one 64-column swizzled box
+constexpr uint32_t SMEM_KF = 0;
+constexpr uint32_t SMEM_KH = SMEM_KF + NKF * F8_BYTES;
+constexpr uint32_t SMEM_VF = SMEM_KH + NKH * H_BYTES;
+constexpr uint32_t SMEM_VH = SMEM_VF + NVF * F8_BYTES;
+constexpr uint32_t SMEM_TILES = SMEM_VH + NVH * H_BYTES;  // 224 KB
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_P = NS * BC;          // 256
+constexpr uint32_t TMEM_Q = TMEM_P + BC / 2;  // 320
+constexpr uint32_t TMEM_O = TMEM_Q + D / 2;   // 384
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.0f;  // exp reference may lag the max by 2^8
+constexpr uint32_t IDESC_QK = idesc_f16_f32(MR, BC, 0);  // K tile: K-major
+constexpr uint32_t IDESC_PV = idesc_f16_f32(MR, D, 1);   // V tile: MN-major
+constexpr uint32_t NEG_INF_BITS = 0xff800000u;
+static_assert(TMEM_O + D == TMEM_COLS, "TMEM budget");
+
+struct Shared {
+  uint64_t kf_full[NKF], kf_empty[NKF];
+  uint64_t kh_full[NKH], kh_empty[NKH];
+  uint64_t vf_full[NVF], vf_empty[NVF];
+  uint64_t vh_full[NVH], vh_empty[NVH];
+  uint64_t s_full[NS], s_free[NS];
+  uint64_t p_full, p_free;
+  uint64_t pv_done[2];
+  uint64_t dec_full[NDEC], dec_empty[NDEC];
+  uint64_t q_ready;
+  int dec[NDEC];
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr uint32_t SMEM_ALLOC = SMEM_TILES + ((sizeof(Shared) + 127) / 128) * 128;
+static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+
+// fp16 tiles: two 128-byte-swizzled boxes of 64 columns, 128 rows each.  As
+// the K-major B operand of Q.K^T: k-step kk (16 columns) is box kk/4 at
+// 32-byte step kk%4, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t kmajor_base(uint32_t tile) {
+  return smem_desc_sw128(tile, 16u, 1024u);
+}
+__device__ __forceinline__ constexpr uint64_t kmajor_step(int kk) {
+  return (uint64_t)(((uint32_t)(kk >> 2) * HALF_BYTES + (uint32_t)(kk & 3) * 32u) >> 4);
+}
+// As the MN-major B operand of P.V (rows are keys): 8-key groups 1024 bytes
+// apart, the second 64-value half 16 KB further; k-step kk (16 keys) starts
+// 2048 bytes further.
+__device__ __forceinline__ uint64_t vmajor_base(uint32_t tile) {
+  return smem_desc_sw128(tile, HALF_BYTES, 1024u);
+}
+__device__ __forceinline__ constexpr uint64_t vmajor_step(int kk) {
+  return (uint64_t)(((uint32_t)kk * 2048u) >> 4);
+}
+
+// Two E4M3 codes (low byte first) -> an fp16 pair (low half first); exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// Row r of an E4M3 tile (128 codes, 128-byte-swizzled: 16-byte chunk c at
+// chunk position c ^ (r % 8)) -> row r of an fp16 tile (columns 64b..64b+63
+// in box b, 16-byte chunk c' of a box row at position c' ^ (r % 8)).
+__device__ __forceinline__ void widen_row(uint32_t src_tile, uint32_t dst_tile, int r) {
+  const uint32_t srow = src_tile + (uint32_t)r * 128u;
+  const uint32_t drow = dst_tile + (uint32_t)r * 128u;
+  const uint32_t sw = (uint32_t)(r & 7);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {  // codes 16c .. 16c+15
+    uint32_t x[4];
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+                 : "r"(srow + (((uint32_t)c ^ sw) << 4)));
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      h[2 * i] = e4m3x2_to_f16x2(x[i] & 0xffffu);
+      h[2 * i + 1] = e4m3x2_to_f16x2(x[i] >> 16);
+    }
+    const uint32_t box = drow + (uint32_t)(c >> 2) * HALF_BYTES;
+    const uint32_t c0 = (uint32_t)(2 * (c & 3));
+    st_shared_v4(box + (((c0) ^ sw) << 4), h[0], h[1], h[2], h[3]);
+    st_shared_v4(box + (((c0 + 1) ^ sw) << 4), h[4], h[5], h[6], h[7]);
+  }
+}
+
+__device__ __forceinline__ float chunk_max(const uint32_t (&s)[32]) {
+  float m[11];
+#pragma unroll
+  for (int i = 0; i < 10; ++i)
+    m[i] = fmax3(__uint_as_float(s[3 * i]), __uint_as_float(s[3 * i + 1]),
+                 __uint_as_float(s[3 * i + 2]));
+  m[10] = fmaxf(__uint_as_float(s[30]), __uint_as_float(s[31]));
+  const float a = fmax3(m[0], m[1], m[2]), b = fmax3(m[3], m[4], m[5]);
+  const float c = fmax3(m[6], m[7], m[8]), d = fmaxf(m[9], m[10]);
+  return fmaxf(fmax3(a, b, c), d);
+}
+
+// P = exp2(s * sl2 - ref) for one 32-key chunk as 16 packed fp16 pairs, with
+// the row sum accumulated in two packed fp32 pairs.
+__device__ __forceinline__ void chunk_exp(const uint32_t (&s)[32], uint64_t sl2x2,
+                                          uint64_t negref2, uint64_t (&acc)[2],
+                                          uint32_t *pk) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    float x0, x1;
+    f2_split(f2_fma(f2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), sl2x2,
+                    negref2),
+             x0, x1);
+    const float p0 = ex2(x0), p1 = ex2(x1);
+    acc[i & 1] = f2_add(acc[i & 1], f2(p0, p1));
+    pk[i] = pack_f16x2(p0, p1);
+  }
+}
+
+// Scores of keys at or past the cache end (the zero-filled tail of the last
+// block) become -inf in TMEM before anything reads them.  Short and out of
+// line: it runs once per sequence from a cold instruction cache.
+__device__ __noinline__ void mask_tail_tmem(uint32_t sa, int lim) {
+  uint32_t ninf[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) ninf[i] = NEG_INF_BITS;
+#pragma unroll 1
+  for (int c = 0; c < 4; ++c) {
+    const int l = lim - 32 * c;
+    if (l >= 32) continue;
+    if (l <= 0) {
+      tmem_st32(sa + 32 * c, ninf);
+      continue;
+    }
+    uint32_t x[32];
+    tmem_ld32(sa + 32 * c, x);
+    tmem_wait_ld_regs(x);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) x[i] = i < l ? x[i] : NEG_INF_BITS;
+    tmem_st32(sa + 32 * c, x);
+  }
+  tmem_wait_st();
+}
+
+
+__global__ void __launch_bounds__(NT, 1)
+    decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Shared &sh = *reinterpret_cast<Shared *>(smem_raw + SMEM_TILES);
+  const uint32_t base = smem_u32(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (base & 1023u) {  // the swizzled layouts need a 1024-byte aligned base
+    if (tid == 0) atomicOr(a.err, kErrTimeout);
+    return;
+  }
+  const int G = a.Hq / a.Hkv;
+  const int unit = blockIdx.x;
+  const int sp = unit % a.n_splits;
+  const int hk = (unit / a.n_splits) % a.Hkv;
+  const int b = unit / (a.n_splits * a.Hkv);
+  const int j0 = (int)((long)sp * a.n_b / a.n_splits);
+  const int j1 = (int)((long)(sp + 1) * a.n_b / a.n_splits);
+  const int nb = j1 - j0;
+  const int zkv = b * a.Hkv + hk;
+  volatile int *abort = &sh.abort;
+
+  if (nb == 0) {  // empty split: no key, zero weight in the merge
+    for (int idx = tid; idx < G * D; idx += NT) {
+      const size_t row = (size_t)(b * a.Hq + hk * G + idx / D) * a.n_splits + sp;
+      a.o_part[row * D + idx % D] = 0.f;
+      if (idx % D == 0) a.lse_part[row] = -INFINITY;
+    }
+    for (int idx = tid; idx < a.words; idx += NT) a.bits[(size_t)unit * a.words + idx] = 0u;
+    return;
+  }
+
+  if (tid == 0) {
+    for (int i = 0; i < NKF; ++i) {
+      mbar_init(smem_u32(&sh.kf_full[i]), 1);
+      mbar_init(smem_u32(&sh.kf_empty[i]), 2);  // the two key converters
+    }
+    for (int i = 0; i < NKH; ++i) {
+      mbar_init(smem_u32(&sh.kh_full[i]), 2);
+      mbar_init(smem_u32(&sh.kh_empty[i]), 1);  // the Q.K^T commit
+    }
+    for (int i = 0; i < NVF; ++i) {
+      mbar_init(smem_u32(&sh.vf_full[i]), 1);
+      mbar_init(smem_u32(&sh.vf_empty[i]), 2);  // the two value converters
+    }
+    for (int i = 0; i < NVH; ++i) {
+      mbar_init(smem_u32(&sh.vh_full[i]), 2);
+      mbar_init(smem_u32(&sh.vh_empty[i]), 1);  // the P.V commit
+    }
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(smem_u32(&sh.s_full[i]), 1);
+      mbar_init(smem_u32(&sh.s_free[i]), 1);
+    }
+    mbar_init(smem_u32(&sh.p_full), 1);
+    mbar_init(smem_u32(&sh.p_free), 1);
+    mbar_init(smem_u32(&sh.pv_done[0]), 1);
+    mbar_init(smem_u32(&sh.pv_done[1]), 1);
+    for (int i = 0; i < NDEC; ++i) {
+      mbar_init(smem_u32(&sh.dec_full[i]), 1);
+      // readers: the value producer, the P.V issuer, the two value converters
+      mbar_init(smem_u32(&sh.dec_empty[i]), 4);
+    }
+    mbar_init(smem_u32(&sh.q_ready), 4);  // warps 5-8, one per lane quarter
+    sh.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == WARP_QK) tmem_alloc(smem_u32(&sh.tmem_base), TMEM_COLS);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == WARP_K) {
+    // ------------------------------------------------- E4M3 key producer --
+    if (lane == 0) {
+      prefetch_tmap(&tm_k);
+      const uint64_t pol = policy_evict_first();  // the cache is streamed once
+      int issued = 0;
+      for (int j = 0; j < nb && !*abort; ++j) {
+        const int f = j % NKF;
+        if (j >= NKF &&
+            !mbar_wait(smem_u32(&sh.kf_empty[f]), ((j / NKF) - 1) & 1, abort, a.err, kErrTimeout))
+          break;
+        mbar_expect_tx(smem_u32(&sh.kf_full[f]), F8_BYTES);
+        tma_load_3d(base + SMEM_KF + f * F8_BYTES, &tm_k, smem_u32(&sh.kf_full[f]), 0,
+                    (j0 + j) * BC, zkv, pol);
+        ++issued;
+      }
+      for (int f = 0; f < NKF && f < issued; ++f) {
+        const int last = f + ((issued - 1 - f) / NKF) * NKF;
+        mbar_wait_drain(smem_u32(&sh.kf_full[f]), (last / NKF) & 1);
+      }
+    }
+  } else if (warp == WARP_V) {
+    // ----------------------------------------------- E4M3 value producer --
+    if (lane == 0) {
+      prefetch_tmap(&tm_v);
+      const uint64_t pol = policy_evict_first();
+      int vi = 0;
+      for (int j = 0; j < nb && !*abort; ++j) {
+        if (!mbar_wait(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
+                       kErrTimeout))
+          break;
+        const int keep = sh.dec[j % NDEC];
+        mbar_arrive(smem_u32(&sh.dec_empty[j % NDEC]));
+        if (!keep) continue;
+        const int f = vi % NVF;
+        if (vi >= NVF &&
+            !mbar_wait(smem_u32(&sh.vf_empty[f]), ((vi / NVF) - 1) & 1, abort, a.err, kErrTimeout))
+          break;
+        mbar_expect_tx(smem_u32(&sh.vf_full[f]), F8_BYTES);
+        tma_load_3d(base + SMEM_VF + f * F8_BYTES, &tm_v, smem_u32(&sh.vf_full[f]), 0,
+                    (j0 + j) * BC, zkv, pol);
+        ++vi;
+      }
+      for (int f = 0; f < NVF && f < vi; ++f) {
+        const int last = f + ((vi - 1 - f) / NVF) * NVF;
+        mbar_wait_drain(smem_u32(&sh.vf_full[f]), (last / NVF) & 1);
+      }
+    }
+  } else if (warp >= WARP_KC) {
+    // ------------------------------------------------------- converters --
+    // First Q (bf16 -> fp16, exact for |q| in the fp16 range) into the TMEM
+    // rows of this warp's lane quarter: row r < G is query head hk*G + r, the
+    // other rows zero; rows past the softmax warp's quarter of the P buffer
+    // are zeroed too (the P.V product reads all 128 rows).
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+    {
+      const uint32_t *qg =
+          reinterpret_cast<const uint32_t *>((const __nv_bfloat16 *)a.q + (size_t)(b * a.Hq + hk * G) * D);
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          w[i] = r < G ? bf16x2_to_f16x2(__ldg(qg + (size_t)r * (D / 2) + c * 32 + i)) : 0u;
+        tmem_st32(lane_base + TMEM_Q + c * 32, w);
+      }
+      if (quarter != 0) {
+        uint32_t z[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) z[i] = 0u;
+        tmem_st32(lane_base + TMEM_P, z);
+        tmem_st32(lane_base + TMEM_P + 32, z);
+      }
+      tmem_wait_st();
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.q_ready));
+    }
+    if (warp < WARP_VC) {
+      // key converters: rows row and row + 32 of every key tile
+      const int row = (warp - WARP_KC) * 64 + lane;
+      for (int j = 0; j < nb; ++j) {
+        const int f = j % NKF, hs = j % NKH;
+        if (!mbar_wait_warp(smem_u32(&sh.kf_full[f]), (j / NKF) & 1, abort, a.err, kErrTimeout))
+          break;
+        if (j >= NKH && !mbar_wait_warp(smem_u32(&sh.kh_empty[hs]), ((j / NKH) - 1) & 1, abort,
+                                        a.err, kErrTimeout))
+          break;
+        widen_row(base + SMEM_KF + f * F8_BYTES, base + SMEM_KH + hs * H_BYTES, row);
+        widen_row(base + SMEM_KF + f * F8_BYTES, base + SMEM_KH + hs * H_BYTES, row + 32);
+        fence_proxy_async_smem();  // the fp16 rows are visible to the tensor core
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&sh.kf_empty[f]));
+          mbar_arrive(smem_u32(&sh.kh_full[hs]));
+        }
+      }
+    } else {
+      // value converters: follow the decisions; rows row and row + 32 of
+      // every kept value tile
+      const int row = (warp - WARP_VC) * 64 + lane;
+      int vi = 0;
+      for (int j = 0; j < nb; ++j) {
+        if (!mbar_wait_warp(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
+                            kErrTimeout))
+          break;
+        const int keep = sh.dec[j % NDEC];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.dec_empty[j % NDEC]));
+        if (!keep) continue;
+        const int f = vi % NVF, hs = vi % NVH;
+        if (!mbar_wait_warp(smem_u32(&sh.vf_full[f]), (vi / NVF) & 1, abort, a.err,
+                            kErrTimeout))
+          break;
+        if (vi >= NVH && !mbar_wait_warp(smem_u32(&sh.vh_empty[hs]), ((vi / NVH) - 1) & 1,
+                                         abort, a.err, kErrTimeout))
+          break;
+        widen_row(base + SMEM_VF + f * F8_BYTES, base + SMEM_VH + hs * H_BYTES, row);
+        widen_row(base + SMEM_VF + f * F8_BYTES, base + SMEM_VH + hs * H_BYTES, row + 32);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&sh.vf_empty[f]));
+          mbar_arrive(smem_u32(&sh.vh_full[hs]));
+        }
+        ++vi;
+      }
+    }
+  } else if (warp == WARP_QK) {
+    // -------------------------------------------------------- Q.K^T issuer --
+    if (lane == 0) {
+      bool ok = mbar_wait(smem_u32(&sh.q_ready), 0, abort, a.err, kErrTimeout);
+      for (int j = 0; ok && j < nb; ++j) {
+        const int hs = j % NKH, sb = j % NS;
+        if (!mbar_wait(smem_u32(&sh.kh_full[hs]), (j / NKH) & 1, abort, a.err, kErrTimeout))
+          break;
+        // S buffer sb is free once the softmax warp has read block j - NS.
+        if (j >= NS && !mbar_wait(smem_u32(&sh.s_free[sb]), ((j / NS) - 1) & 1, abort, a.err,
+                                  kErrTimeout))
+          break;
+        fence_after_sync();
+        const uint64_t kd = kmajor_base(base + SMEM_KH + hs * H_BYTES);
+        const uint32_t d_s = tmem + sb * BC;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_bf16_ts(d_s, tmem + TMEM_Q + kk * 8, kd + kmajor_step(kk), IDESC_QK, kk > 0);
+        mma_commit(smem_u32(&sh.s_full[sb]));
+        mma_commit(smem_u32(&sh.kh_empty[hs]));
+      }
+    }
+  } else if (warp == WARP_PV) {
+    // ---------------------------------------------------------- P.V issuer --
+    if (lane == 0) {
+      int kc = 0;
+      for (int j = 0; j < nb && !*abort; ++j) {
+        if (!mbar_wait(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
+                       kErrTimeout))
+          break;
+        const int keep = sh.dec[j % NDEC];
+        mbar_arrive(smem_u32(&sh.dec_empty[j % NDEC]));
+        if (!keep) continue;
+        const int hs = kc % NVH;
+        if (!mbar_wait(smem_u32(&sh.p_full), kc & 1, abort, a.err, kErrTimeout) ||
+            !mbar_wait(smem_u32(&sh.vh_full[hs]), (kc / NVH) & 1, abort, a.err, kErrTimeout))
+          break;
+        fence_after_sync();
+        // P (fp16 pairs): keys [0,128) in the 64 columns of the P buffer.
+        const uint64_t vd = vmajor_base(base + SMEM_VH + hs * H_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < BC / 16; ++kk)
+          mma_bf16_ts(tmem + TMEM_O, tmem + TMEM_P + kk * 8, vd + vmajor_step(kk), IDESC_PV,
+                      (kc > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(smem_u32(&sh.vh_empty[hs]));
+        mma_commit(smem_u32(&sh.p_free));
+        mma_commit(smem_u32(&sh.pv_done[kc & 1]));
+        ++kc;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- softmax --
+    // Lane g < G: head g's row (TMEM lane g) over the block's 128 keys.
+    const bool head = lane < G;
+    uint32_t *bits = a.bits + (size_t)unit * a.words;
+    // The key scale multiplies every score of the slice: fold it in.
+    const float sl2 = a.scale * __ldg(a.k_scale + zkv) * kLog2e;  // raw score -> log2 units
+    const float c2 = a.ln_lambda * kLog2e;                         // ln(lambda), log2 units
+    float m2 = -INFINITY;  // running max of the split (log2 units)
+    float mref = -INFINITY;  // exp reference (log2 units)
+    float l = 0.f;         // row sum relative to mref
+    int kc = 0;            // kept blocks
+    uint32_t word = 0;
+    bool ok = true;
+    for (int j = 0; j < nb; ++j) {
+      const int sb = j % NS;
+      if (!mbar_wait_warp(smem_u32(&sh.s_full[sb]), (j / NS) & 1, abort, a.err, kErrTimeout)) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      const uint32_t sa = tmem + sb * BC;  // lanes 0-31: this warp's TMEM quarter
+      const int lim = a.L - (j0 + j) * BC;
+      if (lim < BC) mask_tail_tmem(sa, lim);
+      uint32_t x0[32], x1[32], x2[32], x3[32];
+      tmem_ld32(sa, x0);
+      tmem_ld32(sa + 32, x1);
+      tmem_ld32(sa + 64, x2);
+      tmem_ld32(sa + 96, x3);
+      tmem_wait_ld_regs(x0);
+      tmem_wait_ld_regs(x1);
+      tmem_wait_ld_regs(x2);
+      tmem_wait_ld_regs(x3);
+      // The scores are in registers: the S buffer can take block j + NS.
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.s_free[sb]));
+      const float mt =
+          fmaxf(fmaxf(chunk_max(x0), chunk_max(x1)), fmaxf(chunk_max(x2), chunk_max(x3)));
+      const float pm2 = mt * sl2;
+      // With c < 0, "rowmax - m_new < c" is "rowmax - m_old < c" (a block
+      // that raises the max fails both).  Every head must vote skip.
+      const float diff = (mt == -INFINITY) ? -INFINITY : pm2 - m2;
+      const bool skip = __all_sync(0xffffffffu, !head || diff < c2);
+      if (lane == 0) {
+        // On a timeout the abort flag is raised and every later wait fails.
+        if (j < NDEC || mbar_wait(smem_u32(&sh.dec_empty[j % NDEC]), ((j / NDEC) - 1) & 1,
+                                  abort, a.err, kErrTimeout)) {
+          sh.dec[j % NDEC] = skip ? 0 : 1;
+          mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
+        }
+        if (skip) word |= 1u << (j & 31);
+        if ((j & 31) == 31 || j == nb - 1) {
+          bits[j >> 5] = word;
+          word = 0;
+        }
+      }
+      // The running max advances on every block (a skipped block leaves it unchanged).
+      const float mnew = fmaxf(m2, pm2);
+      m2 = mnew;
+      if (skip) continue;
+      bool rescale = false;
+      float alpha = 1.f;
+      if (mref == -INFINITY) {
+        mref = mnew;
+      } else if (mnew > mref + kRescaleLog2) {
+        alpha = ex2(mref - mnew);
+        mref = mnew;
+        rescale = true;
+      }
+      // The P buffer last fed the P.V of kept block kc - 1.
+      if (kc >= 1 && !mbar_wait_warp(smem_u32(&sh.p_free), (kc - 1) & 1, abort, a.err,
+                                     kErrTimeout)) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      const uint32_t pa = tmem + TMEM_P;
+      const uint64_t sl2x2 = f2(sl2, sl2), negref2 = f2(-mref, -mref);
+      uint64_t acc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+      {
+        uint32_t pk[32];
+        chunk_exp(x0, sl2x2, negref2, acc2, pk);
+        chunk_exp(x1, sl2x2, negref2, acc2, pk + 16);
+        tmem_st32(pa, pk);
+        chunk_exp(x2, sl2x2, negref2, acc2, pk);
+        chunk_exp(x3, sl2x2, negref2, acc2, pk + 16);
+        tmem_st32(pa + 32, pk);
+      }
+      tmem_wait_st();
+      float acc[4];
+      f2_split(acc2[0], acc[0], acc[1]);
+      f2_split(acc2[1], acc[2], acc[3]);
+      l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
+      // O rescale of the heads' rows once the previous P.V has landed (it has:
+      // the P buffer was free).
+      if (__any_sync(0xffffffffu, rescale) && kc >= 1) {
+        if (!mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort,
+                            a.err, kErrTimeout)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          const uint32_t oa = tmem + TMEM_O + c * 32;
+          tmem_ld32(oa, o);
+          tmem_wait_ld_regs(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(oa, o);
+        }
+        tmem_wait_st();
+      }
+      fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full));
+      ++kc;
+    }
+
+    // ---- epilogue: O_s = v_scale * O / l and LSE_s = ref + ln l per head ----
+    if (lane == 0)
+      for (int w = ((nb - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
+    if (ok && kc > 0)
+      ok = mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort, a.err,
+                          kErrTimeout);
+    if (ok) {
+      fence_after_sync();
+      const float inv = __ldg(a.v_scale + zkv) / l;
+      const size_t row = (size_t)(b * a.Hq + hk * G + lane) * a.n_splits + sp;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tmem + TMEM_O + c * 32, o);
+        tmem_wait_ld_regs(o);
+        if (head) {
+          float4 *dst = reinterpret_cast<float4 *>(a.o_part + row * D + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            dst[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv,
+                                  __uint_as_float(o[4 * q4 + 1]) * inv,
+                                  __uint_as_float(o[4 * q4 + 2]) * inv,
+                                  __uint_as_float(o[4 * q4 + 3]) * inv);
+        }
+      }
+      if (head) a.lse_part[row] = mref * kLn2 + logf(l);
+    }
+  }
+
+  __syncwarp();
+  fence_before_sync();
+  __syncthreads();
+  if (warp == WARP_QK) {
+    fence_after_sync();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_fp8(const DecodeArgs &a, cudaStream_t s) {
+  CUtensorMap mk, mv;
+  // [B*Hkv, L, 128] E4M3 codes with the caller's row stride (bytes); boxes of
+  // 128 codes x 128 keys; keys past L read as zero (and are masked).
+  if (!make_map_u8_3d(&mk, a.k, D, a.k_row_stride, a.L, a.B * a.Hkv, BC) ||
+      !make_map_u8_3d(&mv, a.v, D, a.v_row_stride, a.L, a.B * a.Hkv, BC))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(decode_fp8_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  if (e != cudaSuccess) return e;
+  const long units = (long)a.B * a.Hkv * a.n_splits;
+  decode_fp8_kernel<<<(unsigned)units, NT, SMEM_ALLOC, s>>>(mk, mv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace attn_skip

@@ -57,6 +57,9 @@ struct DecodeArgs {
   // Per-head decisions: bits [B,Hq,n_splits,words], each query head decides
   // for itself (the GQA kernel only).
   int per_head;
+  // FP8 (E4M3) cache: k and v hold codes; one fp32 scale per (b, KV head)
+  // for keys (multiplies the scores) and values (multiplies the outputs).
+  const float *k_scale, *v_scale;
 };
 
 // Sampled decode output (SANTA estimator).
@@ -86,6 +89,7 @@ cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_decode_fp8(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 cudaError_t launch_selftest_wait(unsigned *err, cudaStream_t s);
 cudaError_t launch_santa_decode(const SantaArgs &a, cudaStream_t s);

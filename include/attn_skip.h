@@ -215,6 +215,36 @@ attn_status attn_skip_decode_per_head(const void *q, const void *k, const void *
  *  o_part [B, Hq, n_splits, dv] fp32,  lse_part [B, Hq, n_splits] fp32
  *  o      [B, Hq, dv] (out_dt),       lse      [B, Hq] fp32
  */
+/*
+ * Split-KV decode with block skipping over an FP8 (E4M3) key/value cache.
+ *
+ * Defines: the loop of attn_skip_decode (section "Decode 内核：砍带宽": decide
+ * from the scores, read values only for kept blocks) over a cache of E4M3
+ * codes (OCP FP8 E4M3: bias 7, max 448, S.1111.111 = NaN) with one fp32
+ * scale per (sequence, KV head) for keys and for values:
+ * key row = k_scale[b,h] * E4M3(k), value row = v_scale[b,h] * E4M3(v).
+ * The BLASST page evaluates FP8/NVFP4-quantised models but fixes no cache
+ * format; halving the cache bytes halves the time of this bandwidth-bound
+ * loop.
+ *
+ *  q          [B, Hq, dk] bf16 (device); widened to fp16 for the products,
+ *             exact for |q| < 65504 (larger values overflow)
+ *  k, v       [B, Hkv, L, d] uint8 E4M3 codes (device), row strides in bytes
+ *             (multiples of 16); no NaN codes
+ *  k_scale, v_scale [B, Hkv] fp32 (device)
+ *  outputs, bitmap layout, merge, lambda, scale: as attn_skip_decode
+ *  (o_part already multiplied by v_scale; attn_skip_decode_combine merges)
+ *
+ * Kernels built: dk = dv = 128, Bc = 128, Hq/Hkv in {1, 2, 4, 8}; P is
+ * rounded to fp16 for the P.V product, accumulation in fp32.  EINVAL as for
+ * attn_skip_decode (also for a null or misaligned scale pointer).
+ */
+attn_status attn_skip_decode_fp8(const void *q, const void *k, const void *v, const float *k_scale,
+                                 const float *v_scale, int B, int Hq, int Hkv, int L, int dk,
+                                 int dv, int64_t k_row_stride, int64_t v_row_stride, float scale,
+                                 double lambda, int Bc, int n_splits, float *o_part,
+                                 float *lse_part, uint32_t *skip_bits, void *stream);
+
 attn_status attn_skip_decode_combine(const float *o_part, const float *lse_part, int B, int Hq,
                                      int n_splits, int dv, attn_dtype out_dt, void *o,
                                      float *lse, void *stream);
