@@ -798,6 +798,14 @@ def run_profile_case(args):
         q, k, v = (x.to(dev) for x in W.prefill_inputs(PREFILL))
         lmb = lam[PREFILL.name][TARGET]["lambda"]
         fn = lambda: bs.attn_skip_prefill(q, k, v, lmb, PREFILL.Br, PREFILL.Bc, True)  # noqa: E731
+    elif args.profile == "fp8":
+        C = W.GQA_DECODE_FP8_32K
+        q, k8, v8, ks, vs = (x.to(dev) for x in W.decode_inputs_fp8(C))
+        lmb = lam[C.name][TARGET]["lambda"]
+
+        def fn():
+            op, lp, _ = bs.attn_skip_decode_fp8(q, k8, v8, ks, vs, lmb, C.Bc, C.n_splits)
+            bs.attn_skip_decode_combine(op, lp)
     else:
         q, k, v = (x.to(dev) for x in W.decode_inputs(DECODE))
         lmb = lam[DECODE.name][TARGET]["lambda"]
@@ -821,7 +829,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--calibration-sweep", action="store_true",
                     help="also fit the threshold model over prefill lengths 4K-64K")
-    ap.add_argument("--profile", choices=("prefill", "decode"),
+    ap.add_argument("--profile", choices=("prefill", "decode", "fp8"),
                     help="only warm up and launch one kernel (for ncu captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

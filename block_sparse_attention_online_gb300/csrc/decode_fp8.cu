@@ -6,30 +6,38 @@
 // the cache format is E4M3 codes with one fp32 scale per (sequence, KV head)
 // for keys and for values (the page evaluates FP8/NVFP4 models and names no
 // cache format; this is the plainest one).  Decode is bound by the cache
-// bytes, so halving them halves the time of the same schedule.
+// bytes, so halving them halves the time of the same schedule -- provided
+// shared memory, which every byte crosses, keeps up.
 //
-// The structure is that of the bf16 decode kernel (the G query heads sharing
-// a KV head padded to the 128 rows of a tcgen05 MMA, one softmax warp holding
-// each head's 128 scores in one thread, the group-AND decision, values loaded
-// only for kept blocks), with two conversion stages: E4M3 tiles arrive by TMA
-// (16 KB per 128-key block) and converter warps widen them, exactly, to fp16
-// tiles in the 128-byte-swizzled layout the MMA reads.  fp16 because the
-// conversion is one instruction per pair of codes and every E4M3 value is an
-// fp16 value; Q (bf16, widened to fp16 once, in TMEM as the A operand) and P
-// (fp16) follow.  The key scale multiplies the scores (folded into the score
-// scale), the value scale the split outputs.
+// The schedule is that of the bf16 decode kernel: the G query heads sharing
+// a KV head are padded to the 128 rows of a tcgen05 MMA, one softmax warp
+// holds each head's 128 scores in one thread (row maxima, votes and the group
+// decision need no reduction across warps) and frees the S buffer as soon as
+// the scores are in registers, P has two TMEM buffers, and values are loaded
+// only for kept blocks, as soon as the decision exists.
 //
-// Warp roles (288 threads):
+// Keys stay E4M3 all the way: S = Q K^T is a kind::f8f6f4 product straight
+// from the TMA tile.  The query is written once, exactly, as an E4M3 pair: per
+// head, q 2^e (the largest power of two keeping the row within 256) = hi + lo
+// with hi = E4M3(q 2^e) and lo = E4M3(q 2^e - hi), which for a bf16 row is
+// exact except for elements below about 2^-10 of the row's largest; S = hi
+// K^T + lo K^T (eight k-steps of 32 codes, fp32 accumulation) and 2^-e goes
+// into the head's score scale.  Values are widened, exactly, to fp16 by
+// converter warps (P is no E4M3 quantity: its small weights would vanish) and
+// O += P V is a kind::f16 product with P in fp16.  Widening the keys as well
+// would move three times their bytes through shared memory.  The key scale
+// multiplies the scores (folded into the score scale), the value scale the
+// split outputs.
+//
+// Warp roles (224 threads):
 //   warp 0      softmax: lane g < G owns head g (TMEM lane g);
 //   warp 1      TMA producer of the E4M3 key tiles (every block, 4 stages);
-//   warp 2      Q.K^T issuer (A = Q from TMEM, B = fp16 K tile; allocates TMEM);
-//   warp 3      TMA producer of the E4M3 value tiles of kept blocks (2 stages);
+//   warp 2      Q.K^T issuer (A = the Q pair, B = the E4M3 key tile, both in
+//               shared memory; allocates TMEM);
+//   warp 3      TMA producer of the E4M3 value tiles of kept blocks (3 stages);
 //   warp 4      P.V issuer (A = P from TMEM, B = fp16 V tile);
-//   warps 5-6   key converters (two key rows per thread);
-//   warps 7-8   value converters (follow the decisions; two key rows each).
-// Before the first block warps 5-8, one per TMEM lane quarter, write Q into
-// TMEM.
-// TMEM columns: S buffers [0,256), P [256,320), Q [320,384), O [384,512).
+//   warps 5-6   value converters (follow the decisions; two key rows each).
+// TMEM columns: S buffers [0,256), P buffers [256,384), O [384,512).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -48,44 +56,41 @@ constexpr int D = 128;    // head size (keys and values)
 constexpr int BC = 128;   // keys per block
 constexpr int MR = 128;   // MMA rows (heads padded)
 constexpr int NKF = 4;    // E4M3 key stages
-constexpr int NKH = 2;    // fp16 key stages
-constexpr int NVF = 2;    // E4M3 value stages
+constexpr int NVF = 3;    // E4M3 value stages
 constexpr int NVH = 2;    // fp16 value stages
 constexpr int NS = 2;     // TMEM S buffers
+constexpr int NP = 2;     // TMEM P buffers
 constexpr int NDEC = 8;   // decision ring
-constexpr int NT = 9 * 32;
+constexpr int NT = 7 * 32;
 constexpr int WARP_K = 1, WARP_QK = 2, WARP_V = 3, WARP_PV = 4;  // warp 0: softmax
-constexpr int WARP_KC = 5, WARP_VC = 7;                           // two warps each
-constexpr uint32_t F8_BYTES = BC * D;           // 16 KB: 128 keys x 128 codes
+constexpr int WARP_VC = 5;                                        // two warps
+constexpr uint32_t F8_BYTES = BC * D;           // 16 KB: 128 rows x 128 codes
 constexpr uint32_t H_BYTES = BC * D * 2;        // 32 KB: 128 keys x 128 fp16
 constexpr uint32_t HALF_BYTES = H_BYTES / 2;    // one 64-column swizzled box
 constexpr uint32_t SMEM_KF = 0;
-constexpr uint32_t SMEM_KH = SMEM_KF + NKF * F8_BYTES;
-constexpr uint32_t SMEM_VF = SMEM_KH + NKH * H_BYTES;
+constexpr uint32_t SMEM_Q = SMEM_KF + NKF * F8_BYTES;  // Q hi, then Q lo
+constexpr uint32_t SMEM_VF = SMEM_Q + 2 * F8_BYTES;
 constexpr uint32_t SMEM_VH = SMEM_VF + NVF * F8_BYTES;
-constexpr uint32_t SMEM_TILES = SMEM_VH + NVH * H_BYTES;  // 224 KB
+constexpr uint32_t SMEM_TILES = SMEM_VH + NVH * H_BYTES;  // 208 KB
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_P = NS * BC;          // 256
-constexpr uint32_t TMEM_Q = TMEM_P + BC / 2;  // 320
-constexpr uint32_t TMEM_O = TMEM_Q + D / 2;   // 384
+constexpr uint32_t TMEM_P = NS * BC;             // 256
+constexpr uint32_t TMEM_O = TMEM_P + NP * (BC / 2);  // 384
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // exp reference may lag the max by 2^8
-constexpr uint32_t IDESC_QK = idesc_f16_f32(MR, BC, 0);  // K tile: K-major
+constexpr uint32_t IDESC_QK = idesc_e4m3_f32(MR, BC);    // E4M3 x E4M3, both K-major
 constexpr uint32_t IDESC_PV = idesc_f16_f32(MR, D, 1);   // V tile: MN-major
 constexpr uint32_t NEG_INF_BITS = 0xff800000u;
 static_assert(TMEM_O + D == TMEM_COLS, "TMEM budget");
 
 struct Shared {
   uint64_t kf_full[NKF], kf_empty[NKF];
-  uint64_t kh_full[NKH], kh_empty[NKH];
   uint64_t vf_full[NVF], vf_empty[NVF];
   uint64_t vh_full[NVH], vh_empty[NVH];
   uint64_t s_full[NS], s_free[NS];
-  uint64_t p_full, p_free;
+  uint64_t p_full[NP], p_free[NP];
   uint64_t pv_done[2];
   uint64_t dec_full[NDEC], dec_empty[NDEC];
-  uint64_t q_ready;
   int dec[NDEC];
   uint32_t tmem_base;
   int abort;
@@ -93,16 +98,17 @@ struct Shared {
 constexpr uint32_t SMEM_ALLOC = SMEM_TILES + ((sizeof(Shared) + 127) / 128) * 128;
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
-// fp16 tiles: two 128-byte-swizzled boxes of 64 columns, 128 rows each.  As
-// the K-major B operand of Q.K^T: k-step kk (16 columns) is box kk/4 at
-// 32-byte step kk%4, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t kmajor_base(uint32_t tile) {
+// E4M3 tiles (the key tile, the two query tiles) as K-major operands of
+// Q.K^T: one 128-byte-swizzled box of 128 codes x 128 rows; k-step kk (32
+// codes) starts 32 bytes further, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t kmajor8_base(uint32_t tile) {
   return smem_desc_sw128(tile, 16u, 1024u);
 }
-__device__ __forceinline__ constexpr uint64_t kmajor_step(int kk) {
-  return (uint64_t)(((uint32_t)(kk >> 2) * HALF_BYTES + (uint32_t)(kk & 3) * 32u) >> 4);
+__device__ __forceinline__ constexpr uint64_t kmajor8_step(int kk) {
+  return (uint64_t)(((uint32_t)kk * 32u) >> 4);
 }
-// As the MN-major B operand of P.V (rows are keys): 8-key groups 1024 bytes
+// fp16 value tiles: two 128-byte-swizzled boxes of 64 columns, 128 rows each,
+// as the MN-major B operand of P.V (rows are keys): 8-key groups 1024 bytes
 // apart, the second 64-value half 16 KB further; k-step kk (16 keys) starts
 // 2048 bytes further.
 __device__ __forceinline__ uint64_t vmajor_base(uint32_t tile) {
@@ -199,6 +205,64 @@ __device__ __noinline__ void mask_tail_tmem(uint32_t sa, int lim) {
 }
 
 
+// The query pair of head row r (r < G: query head hk*G + r) into the two
+// E4M3 query tiles (128-byte-swizzled rows of 128 codes); other rows zero.
+// Returns the row's exponent e (q 2^e = hi + lo, max |q| 2^e <= 256).
+__device__ __forceinline__ int write_query_pair(const DecodeArgs &a, int b, int hk, int G, int r,
+                                                uint32_t q_hi, uint32_t q_lo) {
+  uint32_t hi[32], lo[32];
+  int qexp = 0;
+  if (r < G) {
+    // The row in 16 independent 16-byte loads (bf16 pairs, low element first).
+    const uint4 *qr = reinterpret_cast<const uint4 *>((const __nv_bfloat16 *)a.q +
+                                                      (size_t)(b * a.Hq + hk * G + r) * D);
+    uint32_t w[64];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint4 v = __ldg(qr + i);
+      w[4 * i] = v.x;
+      w[4 * i + 1] = v.y;
+      w[4 * i + 2] = v.z;
+      w[4 * i + 3] = v.w;
+    }
+    uint32_t amax_bits = 0;  // |bf16| bit patterns order like their values
+#pragma unroll
+    for (int i = 0; i < 64; ++i)
+      amax_bits = max(amax_bits, max(w[i] & 0x7fffu, (w[i] >> 16) & 0x7fffu));
+    const float amax = __uint_as_float(amax_bits << 16);
+    int ex = 0;
+    const float fr = frexpf(amax > 0.f ? amax : 1.f, &ex);  // amax = fr * 2^ex
+    qexp = amax > 0.f ? 8 - (fr == 0.5f ? ex - 1 : ex) : 0;  // 8 - ceil(log2 amax)
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      uint32_t wh = 0, wl = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t pair = w[2 * c + (i >> 1)];
+        const float q = __uint_as_float((i & 1) ? (pair & 0xffff0000u) : (pair << 16));
+        const float x = ldexpf(q, qexp);      // exact
+        const __nv_fp8_e4m3 h(x);             // nearest even
+        const __nv_fp8_e4m3 l(x - (float)h);  // x - h is exact
+        wh |= (uint32_t)h.__x << (8 * i);
+        wl |= (uint32_t)l.__x << (8 * i);
+      }
+      hi[c] = wh;
+      lo[c] = wl;
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 32; ++c) hi[c] = lo[c] = 0u;
+  }
+  const uint32_t sw = (uint32_t)(r & 7);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {  // codes 16c .. 16c+15
+    const uint32_t off = (uint32_t)r * 128u + (((uint32_t)c ^ sw) << 4);
+    st_shared_v4(q_hi + off, hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+    st_shared_v4(q_lo + off, lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+  }
+  return qexp;
+}
+
 __global__ void __launch_bounds__(NT, 1)
     decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
@@ -231,14 +295,15 @@ __global__ void __launch_bounds__(NT, 1)
     return;
   }
 
+  // The query pair (threads 0-127, one row each); thread g < G keeps its
+  // head's exponent for the score scale.
+  int qexp = 0;
+  if (tid < MR) qexp = write_query_pair(a, b, hk, G, tid, base + SMEM_Q, base + SMEM_Q + F8_BYTES);
+  fence_proxy_async_smem();  // visible to the tensor core
   if (tid == 0) {
     for (int i = 0; i < NKF; ++i) {
       mbar_init(smem_u32(&sh.kf_full[i]), 1);
-      mbar_init(smem_u32(&sh.kf_empty[i]), 2);  // the two key converters
-    }
-    for (int i = 0; i < NKH; ++i) {
-      mbar_init(smem_u32(&sh.kh_full[i]), 2);
-      mbar_init(smem_u32(&sh.kh_empty[i]), 1);  // the Q.K^T commit
+      mbar_init(smem_u32(&sh.kf_empty[i]), 1);  // the Q.K^T commit
     }
     for (int i = 0; i < NVF; ++i) {
       mbar_init(smem_u32(&sh.vf_full[i]), 1);
@@ -252,8 +317,10 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(smem_u32(&sh.s_full[i]), 1);
       mbar_init(smem_u32(&sh.s_free[i]), 1);
     }
-    mbar_init(smem_u32(&sh.p_full), 1);
-    mbar_init(smem_u32(&sh.p_free), 1);
+    for (int i = 0; i < NP; ++i) {
+      mbar_init(smem_u32(&sh.p_full[i]), 1);
+      mbar_init(smem_u32(&sh.p_free[i]), 1);
+    }
     mbar_init(smem_u32(&sh.pv_done[0]), 1);
     mbar_init(smem_u32(&sh.pv_done[1]), 1);
     for (int i = 0; i < NDEC; ++i) {
@@ -261,7 +328,6 @@ __global__ void __launch_bounds__(NT, 1)
       // readers: the value producer, the P.V issuer, the two value converters
       mbar_init(smem_u32(&sh.dec_empty[i]), 4);
     }
-    mbar_init(smem_u32(&sh.q_ready), 4);  // warps 5-8, one per lane quarter
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -319,108 +385,57 @@ __global__ void __launch_bounds__(NT, 1)
         mbar_wait_drain(smem_u32(&sh.vf_full[f]), (last / NVF) & 1);
       }
     }
-  } else if (warp >= WARP_KC) {
-    // ------------------------------------------------------- converters --
-    // First Q (bf16 -> fp16, exact for |q| in the fp16 range) into the TMEM
-    // rows of this warp's lane quarter: row r < G is query head hk*G + r, the
-    // other rows zero; rows past the softmax warp's quarter of the P buffer
-    // are zeroed too (the P.V product reads all 128 rows).
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-    {
-      const uint32_t *qg =
-          reinterpret_cast<const uint32_t *>((const __nv_bfloat16 *)a.q + (size_t)(b * a.Hq + hk * G) * D);
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        uint32_t w[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          w[i] = r < G ? bf16x2_to_f16x2(__ldg(qg + (size_t)r * (D / 2) + c * 32 + i)) : 0u;
-        tmem_st32(lane_base + TMEM_Q + c * 32, w);
-      }
-      if (quarter != 0) {
-        uint32_t z[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) z[i] = 0u;
-        tmem_st32(lane_base + TMEM_P, z);
-        tmem_st32(lane_base + TMEM_P + 32, z);
-      }
-      tmem_wait_st();
-      fence_before_sync();
+  } else if (warp >= WARP_VC) {
+    // -------------------------------------------------- value converters --
+    // Follow the decisions; rows row and row + 32 of every kept value tile.
+    const int row = (warp - WARP_VC) * 64 + lane;
+    int vi = 0;
+    for (int j = 0; j < nb; ++j) {
+      if (!mbar_wait_warp(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
+                          kErrTimeout))
+        break;
+      const int keep = sh.dec[j % NDEC];
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.q_ready));
-    }
-    if (warp < WARP_VC) {
-      // key converters: rows row and row + 32 of every key tile
-      const int row = (warp - WARP_KC) * 64 + lane;
-      for (int j = 0; j < nb; ++j) {
-        const int f = j % NKF, hs = j % NKH;
-        if (!mbar_wait_warp(smem_u32(&sh.kf_full[f]), (j / NKF) & 1, abort, a.err, kErrTimeout))
-          break;
-        if (j >= NKH && !mbar_wait_warp(smem_u32(&sh.kh_empty[hs]), ((j / NKH) - 1) & 1, abort,
-                                        a.err, kErrTimeout))
-          break;
-        widen_row(base + SMEM_KF + f * F8_BYTES, base + SMEM_KH + hs * H_BYTES, row);
-        widen_row(base + SMEM_KF + f * F8_BYTES, base + SMEM_KH + hs * H_BYTES, row + 32);
-        fence_proxy_async_smem();  // the fp16 rows are visible to the tensor core
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&sh.kf_empty[f]));
-          mbar_arrive(smem_u32(&sh.kh_full[hs]));
-        }
+      if (lane == 0) mbar_arrive(smem_u32(&sh.dec_empty[j % NDEC]));
+      if (!keep) continue;
+      const int f = vi % NVF, hs = vi % NVH;
+      if (!mbar_wait_warp(smem_u32(&sh.vf_full[f]), (vi / NVF) & 1, abort, a.err, kErrTimeout))
+        break;
+      if (vi >= NVH && !mbar_wait_warp(smem_u32(&sh.vh_empty[hs]), ((vi / NVH) - 1) & 1, abort,
+                                       a.err, kErrTimeout))
+        break;
+      widen_row(base + SMEM_VF + f * F8_BYTES, base + SMEM_VH + hs * H_BYTES, row);
+      widen_row(base + SMEM_VF + f * F8_BYTES, base + SMEM_VH + hs * H_BYTES, row + 32);
+      fence_proxy_async_smem();  // the fp16 rows are visible to the tensor core
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&sh.vf_empty[f]));
+        mbar_arrive(smem_u32(&sh.vh_full[hs]));
       }
-    } else {
-      // value converters: follow the decisions; rows row and row + 32 of
-      // every kept value tile
-      const int row = (warp - WARP_VC) * 64 + lane;
-      int vi = 0;
-      for (int j = 0; j < nb; ++j) {
-        if (!mbar_wait_warp(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
-                            kErrTimeout))
-          break;
-        const int keep = sh.dec[j % NDEC];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh.dec_empty[j % NDEC]));
-        if (!keep) continue;
-        const int f = vi % NVF, hs = vi % NVH;
-        if (!mbar_wait_warp(smem_u32(&sh.vf_full[f]), (vi / NVF) & 1, abort, a.err,
-                            kErrTimeout))
-          break;
-        if (vi >= NVH && !mbar_wait_warp(smem_u32(&sh.vh_empty[hs]), ((vi / NVH) - 1) & 1,
-                                         abort, a.err, kErrTimeout))
-          break;
-        widen_row(base + SMEM_VF + f * F8_BYTES, base + SMEM_VH + hs * H_BYTES, row);
-        widen_row(base + SMEM_VF + f * F8_BYTES, base + SMEM_VH + hs * H_BYTES, row + 32);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&sh.vf_empty[f]));
-          mbar_arrive(smem_u32(&sh.vh_full[hs]));
-        }
-        ++vi;
-      }
+      ++vi;
     }
   } else if (warp == WARP_QK) {
     // -------------------------------------------------------- Q.K^T issuer --
     if (lane == 0) {
-      bool ok = mbar_wait(smem_u32(&sh.q_ready), 0, abort, a.err, kErrTimeout);
-      for (int j = 0; ok && j < nb; ++j) {
-        const int hs = j % NKH, sb = j % NS;
-        if (!mbar_wait(smem_u32(&sh.kh_full[hs]), (j / NKH) & 1, abort, a.err, kErrTimeout))
+      const uint64_t qhi = kmajor8_base(base + SMEM_Q), qlo = kmajor8_base(base + SMEM_Q + F8_BYTES);
+      for (int j = 0; j < nb; ++j) {
+        const int f = j % NKF, sb = j % NS;
+        if (!mbar_wait(smem_u32(&sh.kf_full[f]), (j / NKF) & 1, abort, a.err, kErrTimeout))
           break;
         // S buffer sb is free once the softmax warp has read block j - NS.
         if (j >= NS && !mbar_wait(smem_u32(&sh.s_free[sb]), ((j / NS) - 1) & 1, abort, a.err,
                                   kErrTimeout))
           break;
         fence_after_sync();
-        const uint64_t kd = kmajor_base(base + SMEM_KH + hs * H_BYTES);
+        const uint64_t kd = kmajor8_base(base + SMEM_KF + f * F8_BYTES);
         const uint32_t d_s = tmem + sb * BC;
+        // S = hi K^T + lo K^T: four k-steps of 32 codes for each part.
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ts(d_s, tmem + TMEM_Q + kk * 8, kd + kmajor_step(kk), IDESC_QK, kk > 0);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_f8f6f4_ss(d_s, (kk < 4 ? qhi : qlo) + kmajor8_step(kk & 3),
+                        kd + kmajor8_step(kk & 3), IDESC_QK, kk > 0);
         mma_commit(smem_u32(&sh.s_full[sb]));
-        mma_commit(smem_u32(&sh.kh_empty[hs]));
+        mma_commit(smem_u32(&sh.kf_empty[f]));
       }
     }
   } else if (warp == WARP_PV) {
@@ -434,19 +449,20 @@ __global__ void __launch_bounds__(NT, 1)
         const int keep = sh.dec[j % NDEC];
         mbar_arrive(smem_u32(&sh.dec_empty[j % NDEC]));
         if (!keep) continue;
-        const int hs = kc % NVH;
-        if (!mbar_wait(smem_u32(&sh.p_full), kc & 1, abort, a.err, kErrTimeout) ||
+        const int pb = kc % NP, hs = kc % NVH;
+        if (!mbar_wait(smem_u32(&sh.p_full[pb]), (kc / NP) & 1, abort, a.err, kErrTimeout) ||
             !mbar_wait(smem_u32(&sh.vh_full[hs]), (kc / NVH) & 1, abort, a.err, kErrTimeout))
           break;
         fence_after_sync();
-        // P (fp16 pairs): keys [0,128) in the 64 columns of the P buffer.
+        // P (fp16 pairs): keys [0,128) in the 64 columns of P buffer pb.
+        const uint32_t pt = tmem + TMEM_P + pb * (BC / 2);
         const uint64_t vd = vmajor_base(base + SMEM_VH + hs * H_BYTES);
 #pragma unroll
         for (int kk = 0; kk < BC / 16; ++kk)
-          mma_bf16_ts(tmem + TMEM_O, tmem + TMEM_P + kk * 8, vd + vmajor_step(kk), IDESC_PV,
+          mma_bf16_ts(tmem + TMEM_O, pt + kk * 8, vd + vmajor_step(kk), IDESC_PV,
                       (kc > 0 || kk > 0) ? 1u : 0u);
         mma_commit(smem_u32(&sh.vh_empty[hs]));
-        mma_commit(smem_u32(&sh.p_free));
+        mma_commit(smem_u32(&sh.p_free[pb]));
         mma_commit(smem_u32(&sh.pv_done[kc & 1]));
         ++kc;
       }
@@ -456,13 +472,14 @@ __global__ void __launch_bounds__(NT, 1)
     // Lane g < G: head g's row (TMEM lane g) over the block's 128 keys.
     const bool head = lane < G;
     uint32_t *bits = a.bits + (size_t)unit * a.words;
-    // The key scale multiplies every score of the slice: fold it in.
-    const float sl2 = a.scale * __ldg(a.k_scale + zkv) * kLog2e;  // raw score -> log2 units
-    const float c2 = a.ln_lambda * kLog2e;                         // ln(lambda), log2 units
-    float m2 = -INFINITY;  // running max of the split (log2 units)
+    // Raw score -> log2 units: the score scale, the key scale and 2^-e of the
+    // head's query pair.
+    const float sl2 = ldexpf(a.scale * __ldg(a.k_scale + zkv) * kLog2e, -qexp);
+    const float c2 = a.ln_lambda * kLog2e;  // ln(lambda), log2 units
+    float m2 = -INFINITY;    // running max of the split (log2 units)
     float mref = -INFINITY;  // exp reference (log2 units)
-    float l = 0.f;         // row sum relative to mref
-    int kc = 0;            // kept blocks
+    float l = 0.f;           // row sum relative to mref
+    int kc = 0;              // kept blocks
     uint32_t word = 0;
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
@@ -521,14 +538,15 @@ __global__ void __launch_bounds__(NT, 1)
         mref = mnew;
         rescale = true;
       }
-      // The P buffer last fed the P.V of kept block kc - 1.
-      if (kc >= 1 && !mbar_wait_warp(smem_u32(&sh.p_free), (kc - 1) & 1, abort, a.err,
-                                     kErrTimeout)) {
+      const int pb = kc % NP;
+      // P buffer pb last fed the P.V of kept block kc - NP.
+      if (kc >= NP && !mbar_wait_warp(smem_u32(&sh.p_free[pb]), ((kc / NP) - 1) & 1, abort,
+                                      a.err, kErrTimeout)) {
         ok = false;
         break;
       }
       fence_after_sync();
-      const uint32_t pa = tmem + TMEM_P;
+      const uint32_t pa = tmem + TMEM_P + pb * (BC / 2);
       const uint64_t sl2x2 = f2(sl2, sl2), negref2 = f2(-mref, -mref);
       uint64_t acc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
       {
@@ -545,8 +563,7 @@ __global__ void __launch_bounds__(NT, 1)
       f2_split(acc2[0], acc[0], acc[1]);
       f2_split(acc2[1], acc[2], acc[3]);
       l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
-      // O rescale of the heads' rows once the previous P.V has landed (it has:
-      // the P buffer was free).
+      // O rescale of the heads' rows once the previous P.V has landed.
       if (__any_sync(0xffffffffu, rescale) && kc >= 1) {
         if (!mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort,
                             a.err, kErrTimeout)) {
@@ -568,7 +585,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
       fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full));
+      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[pb]));
       ++kc;
     }
 
