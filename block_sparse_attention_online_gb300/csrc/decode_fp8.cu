@@ -29,14 +29,14 @@
 // multiplies the scores (folded into the score scale), the value scale the
 // split outputs.
 //
-// Warp roles (224 threads):
+// Warp roles (256 threads):
 //   warp 0      softmax: lane g < G owns head g (TMEM lane g);
-//   warp 1      TMA producer of the E4M3 key tiles (every block, 4 stages);
+//   warp 1      TMA producer of the E4M3 key tiles (every block, 6 stages);
 //   warp 2      Q.K^T issuer (A = the Q pair, B = the E4M3 key tile, both in
 //               shared memory; allocates TMEM);
-//   warp 3      TMA producer of the E4M3 value tiles of kept blocks (3 stages);
+//   warp 3      TMA producer of the E4M3 value tiles of kept blocks (2 stages);
 //   warp 4      P.V issuer (A = P from TMEM, B = fp16 V tile);
-//   warps 5-6   value converters (follow the decisions; two key rows each).
+//   warps 5-7   value converters (follow the decisions; a third of each tile).
 // TMEM columns: S buffers [0,256), P buffers [256,384), O [384,512).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -55,15 +55,16 @@ using namespace tc;
 constexpr int D = 128;    // head size (keys and values)
 constexpr int BC = 128;   // keys per block
 constexpr int MR = 128;   // MMA rows (heads padded)
-constexpr int NKF = 4;    // E4M3 key stages
-constexpr int NVF = 3;    // E4M3 value stages
+constexpr int NKF = 6;    // E4M3 key stages
+constexpr int NVF = 2;    // E4M3 value stages
 constexpr int NVH = 2;    // fp16 value stages
 constexpr int NS = 2;     // TMEM S buffers
 constexpr int NP = 2;     // TMEM P buffers
 constexpr int NDEC = 8;   // decision ring
-constexpr int NT = 7 * 32;
+constexpr int NT = 8 * 32;
 constexpr int WARP_K = 1, WARP_QK = 2, WARP_V = 3, WARP_PV = 4;  // warp 0: softmax
-constexpr int WARP_VC = 5;                                        // two warps
+constexpr int WARP_VC = 5;                                        // three warps
+constexpr int NVC = 3 * 32;                                       // converter threads
 constexpr uint32_t F8_BYTES = BC * D;           // 16 KB: 128 rows x 128 codes
 constexpr uint32_t H_BYTES = BC * D * 2;        // 32 KB: 128 keys x 128 fp16
 constexpr uint32_t HALF_BYTES = H_BYTES / 2;    // one 64-column swizzled box
@@ -71,7 +72,7 @@ constexpr uint32_t SMEM_KF = 0;
 constexpr uint32_t SMEM_Q = SMEM_KF + NKF * F8_BYTES;  // Q hi, then Q lo
 constexpr uint32_t SMEM_VF = SMEM_Q + 2 * F8_BYTES;
 constexpr uint32_t SMEM_VH = SMEM_VF + NVF * F8_BYTES;
-constexpr uint32_t SMEM_TILES = SMEM_VH + NVH * H_BYTES;  // 208 KB
+constexpr uint32_t SMEM_TILES = SMEM_VH + NVH * H_BYTES;  // 224 KB
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t TMEM_P = NS * BC;             // 256
 constexpr uint32_t TMEM_O = TMEM_P + NP * (BC / 2);  // 384
@@ -118,36 +119,36 @@ __device__ __forceinline__ constexpr uint64_t vmajor_step(int kk) {
   return (uint64_t)(((uint32_t)kk * 2048u) >> 4);
 }
 
-// Two E4M3 codes (low byte first) -> an fp16 pair (low half first); exact.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two, __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Two E4M3 codes -> an fp16 pair holding the code values times 2^-8, exactly
+// (the 2^8 goes into the value scale): with the code in the high byte of a
+// half word, the sign is already in place and the seven exponent / mantissa
+// bits, shifted right by one, land on the fp16 exponent / mantissa with the
+// exponent bias 7 read as 15 (subnormal codes become subnormal halves).
+// `w` holds the codes at bits 8-15 and 24-31.  NaN codes are not expected.
+__device__ __forceinline__ uint32_t e4m3_hi_bytes_to_f16x2(uint32_t w) {
+  return (w & 0x80008000u) | ((w >> 1) & 0x3f803f80u);
 }
 
-// Row r of an E4M3 tile (128 codes, 128-byte-swizzled: 16-byte chunk c at
-// chunk position c ^ (r % 8)) -> row r of an fp16 tile (columns 64b..64b+63
-// in box b, 16-byte chunk c' of a box row at position c' ^ (r % 8)).
-__device__ __forceinline__ void widen_row(uint32_t src_tile, uint32_t dst_tile, int r) {
-  const uint32_t srow = src_tile + (uint32_t)r * 128u;
-  const uint32_t drow = dst_tile + (uint32_t)r * 128u;
+// Chunk c (codes 16c..16c+15) of row r of an E4M3 tile (128 codes per row,
+// 128-byte-swizzled: chunk c at chunk position c ^ (r % 8)) -> the same
+// columns of row r of an fp16 tile of the values times 2^-8 (columns
+// 64b..64b+63 in box b, 16-byte chunk c' of a box row at position c' ^ (r % 8)).
+__device__ __forceinline__ void widen_chunk(uint32_t src_tile, uint32_t dst_tile, int r, int c) {
   const uint32_t sw = (uint32_t)(r & 7);
+  uint32_t x[4];
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+               : "r"(src_tile + (uint32_t)r * 128u + (((uint32_t)c ^ sw) << 4)));
+  uint32_t h[8];
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {  // codes 16c .. 16c+15
-    uint32_t x[4];
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
-                 : "r"(srow + (((uint32_t)c ^ sw) << 4)));
-    uint32_t h[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      h[2 * i] = e4m3x2_to_f16x2(x[i] & 0xffffu);
-      h[2 * i + 1] = e4m3x2_to_f16x2(x[i] >> 16);
-    }
-    const uint32_t box = drow + (uint32_t)(c >> 2) * HALF_BYTES;
-    const uint32_t c0 = (uint32_t)(2 * (c & 3));
-    st_shared_v4(box + (((c0) ^ sw) << 4), h[0], h[1], h[2], h[3]);
-    st_shared_v4(box + (((c0 + 1) ^ sw) << 4), h[4], h[5], h[6], h[7]);
+  for (int i = 0; i < 4; ++i) {
+    h[2 * i] = e4m3_hi_bytes_to_f16x2(__byte_perm(x[i], 0u, 0x1404));      // codes 0, 1
+    h[2 * i + 1] = e4m3_hi_bytes_to_f16x2(__byte_perm(x[i], 0u, 0x3424));  // codes 2, 3
   }
+  const uint32_t box = dst_tile + (uint32_t)r * 128u + (uint32_t)(c >> 2) * HALF_BYTES;
+  const uint32_t c0 = (uint32_t)(2 * (c & 3));
+  st_shared_v4(box + ((c0 ^ sw) << 4), h[0], h[1], h[2], h[3]);
+  st_shared_v4(box + (((c0 + 1) ^ sw) << 4), h[4], h[5], h[6], h[7]);
 }
 
 __device__ __forceinline__ float chunk_max(const uint32_t (&s)[32]) {
@@ -210,35 +211,43 @@ __device__ __noinline__ void mask_tail_tmem(uint32_t sa, int lim) {
 // Returns the row's exponent e (q 2^e = hi + lo, max |q| 2^e <= 256).
 __device__ __forceinline__ int write_query_pair(const DecodeArgs &a, int b, int hk, int G, int r,
                                                 uint32_t q_hi, uint32_t q_lo) {
-  uint32_t hi[32], lo[32];
-  int qexp = 0;
-  if (r < G) {
-    // The row in 16 independent 16-byte loads (bf16 pairs, low element first).
-    const uint4 *qr = reinterpret_cast<const uint4 *>((const __nv_bfloat16 *)a.q +
-                                                      (size_t)(b * a.Hq + hk * G + r) * D);
-    uint32_t w[64];
+  const uint32_t sw = (uint32_t)(r & 7);
+  if (r >= G) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint4 v = __ldg(qr + i);
-      w[4 * i] = v.x;
-      w[4 * i + 1] = v.y;
-      w[4 * i + 2] = v.z;
-      w[4 * i + 3] = v.w;
+    for (int c = 0; c < 8; ++c) {
+      const uint32_t off = (uint32_t)r * 128u + (((uint32_t)c ^ sw) << 4);
+      st_shared_v4(q_hi + off, 0u, 0u, 0u, 0u);
+      st_shared_v4(q_lo + off, 0u, 0u, 0u, 0u);
     }
-    uint32_t amax_bits = 0;  // |bf16| bit patterns order like their values
+    return 0;
+  }
+  // bf16 pairs of the row (low element first), 8 per 16-byte load.
+  const uint4 *qr = reinterpret_cast<const uint4 *>((const __nv_bfloat16 *)a.q +
+                                                    (size_t)(b * a.Hq + hk * G + r) * D);
+  uint32_t amax_bits = 0;  // |bf16| bit patterns order like their values
 #pragma unroll
-    for (int i = 0; i < 64; ++i)
-      amax_bits = max(amax_bits, max(w[i] & 0x7fffu, (w[i] >> 16) & 0x7fffu));
-    const float amax = __uint_as_float(amax_bits << 16);
-    int ex = 0;
-    const float fr = frexpf(amax > 0.f ? amax : 1.f, &ex);  // amax = fr * 2^ex
-    qexp = amax > 0.f ? 8 - (fr == 0.5f ? ex - 1 : ex) : 0;  // 8 - ceil(log2 amax)
+  for (int i = 0; i < 16; ++i) {
+    const uint4 v = __ldg(qr + i);
+    amax_bits = max(amax_bits, max(v.x & 0x7fffu, (v.x >> 16) & 0x7fffu));
+    amax_bits = max(amax_bits, max(v.y & 0x7fffu, (v.y >> 16) & 0x7fffu));
+    amax_bits = max(amax_bits, max(v.z & 0x7fffu, (v.z >> 16) & 0x7fffu));
+    amax_bits = max(amax_bits, max(v.w & 0x7fffu, (v.w >> 16) & 0x7fffu));
+  }
+  const float amax = __uint_as_float(amax_bits << 16);
+  int ex = 0;
+  const float fr = frexpf(amax > 0.f ? amax : 1.f, &ex);  // amax = fr * 2^ex
+  const int qexp = amax > 0.f ? 8 - (fr == 0.5f ? ex - 1 : ex) : 0;  // 8 - ceil(log2 amax)
+#pragma unroll 2
+  for (int c = 0; c < 8; ++c) {  // codes 16c .. 16c+15: two 16-byte loads of bf16
+    const uint4 v0 = __ldg(qr + 2 * c), v1 = __ldg(qr + 2 * c + 1);
+    const uint32_t pr[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t hi[4], lo[4];
 #pragma unroll
-    for (int c = 0; c < 32; ++c) {
+    for (int w = 0; w < 4; ++w) {
       uint32_t wh = 0, wl = 0;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint32_t pair = w[2 * c + (i >> 1)];
+        const uint32_t pair = pr[2 * w + (i >> 1)];
         const float q = __uint_as_float((i & 1) ? (pair & 0xffff0000u) : (pair << 16));
         const float x = ldexpf(q, qexp);      // exact
         const __nv_fp8_e4m3 h(x);             // nearest even
@@ -246,19 +255,12 @@ __device__ __forceinline__ int write_query_pair(const DecodeArgs &a, int b, int 
         wh |= (uint32_t)h.__x << (8 * i);
         wl |= (uint32_t)l.__x << (8 * i);
       }
-      hi[c] = wh;
-      lo[c] = wl;
+      hi[w] = wh;
+      lo[w] = wl;
     }
-  } else {
-#pragma unroll
-    for (int c = 0; c < 32; ++c) hi[c] = lo[c] = 0u;
-  }
-  const uint32_t sw = (uint32_t)(r & 7);
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {  // codes 16c .. 16c+15
     const uint32_t off = (uint32_t)r * 128u + (((uint32_t)c ^ sw) << 4);
-    st_shared_v4(q_hi + off, hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
-    st_shared_v4(q_lo + off, lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+    st_shared_v4(q_hi + off, hi[0], hi[1], hi[2], hi[3]);
+    st_shared_v4(q_lo + off, lo[0], lo[1], lo[2], lo[3]);
   }
   return qexp;
 }
@@ -307,10 +309,10 @@ __global__ void __launch_bounds__(NT, 1)
     }
     for (int i = 0; i < NVF; ++i) {
       mbar_init(smem_u32(&sh.vf_full[i]), 1);
-      mbar_init(smem_u32(&sh.vf_empty[i]), 2);  // the two value converters
+      mbar_init(smem_u32(&sh.vf_empty[i]), 3);  // the three value converters
     }
     for (int i = 0; i < NVH; ++i) {
-      mbar_init(smem_u32(&sh.vh_full[i]), 2);
+      mbar_init(smem_u32(&sh.vh_full[i]), 3);
       mbar_init(smem_u32(&sh.vh_empty[i]), 1);  // the P.V commit
     }
     for (int i = 0; i < NS; ++i) {
@@ -325,8 +327,8 @@ __global__ void __launch_bounds__(NT, 1)
     mbar_init(smem_u32(&sh.pv_done[1]), 1);
     for (int i = 0; i < NDEC; ++i) {
       mbar_init(smem_u32(&sh.dec_full[i]), 1);
-      // readers: the value producer, the P.V issuer, the two value converters
-      mbar_init(smem_u32(&sh.dec_empty[i]), 4);
+      // readers: the value producer, the P.V issuer, the three value converters
+      mbar_init(smem_u32(&sh.dec_empty[i]), 5);
     }
     sh.abort = 0;
     fence_mbar_init();
@@ -387,8 +389,9 @@ __global__ void __launch_bounds__(NT, 1)
     }
   } else if (warp >= WARP_VC) {
     // -------------------------------------------------- value converters --
-    // Follow the decisions; rows row and row + 32 of every kept value tile.
-    const int row = (warp - WARP_VC) * 64 + lane;
+    // Follow the decisions; chunks t, t + 96, ... (row = chunk / 8) of every
+    // kept value tile.
+    const int t0 = (warp - WARP_VC) * 32 + lane;
     int vi = 0;
     for (int j = 0; j < nb; ++j) {
       if (!mbar_wait_warp(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
@@ -404,8 +407,9 @@ __global__ void __launch_bounds__(NT, 1)
       if (vi >= NVH && !mbar_wait_warp(smem_u32(&sh.vh_empty[hs]), ((vi / NVH) - 1) & 1, abort,
                                        a.err, kErrTimeout))
         break;
-      widen_row(base + SMEM_VF + f * F8_BYTES, base + SMEM_VH + hs * H_BYTES, row);
-      widen_row(base + SMEM_VF + f * F8_BYTES, base + SMEM_VH + hs * H_BYTES, row + 32);
+#pragma unroll 4
+      for (int t = t0; t < BC * 8; t += NVC)
+        widen_chunk(base + SMEM_VF + f * F8_BYTES, base + SMEM_VH + hs * H_BYTES, t >> 3, t & 7);
       fence_proxy_async_smem();  // the fp16 rows are visible to the tensor core
       __syncwarp();
       if (lane == 0) {
@@ -597,7 +601,7 @@ __global__ void __launch_bounds__(NT, 1)
                           kErrTimeout);
     if (ok) {
       fence_after_sync();
-      const float inv = __ldg(a.v_scale + zkv) / l;
+      const float inv = __ldg(a.v_scale + zkv) * 256.f / l;  // values were widened times 2^-8
       const size_t row = (size_t)(b * a.Hq + hk * G + lane) * a.n_splits + sp;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
