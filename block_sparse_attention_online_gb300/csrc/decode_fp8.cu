@@ -6,38 +6,42 @@
 // the cache format is E4M3 codes with one fp32 scale per (sequence, KV head)
 // for keys and for values (the page evaluates FP8/NVFP4 models and names no
 // cache format; this is the plainest one).  Decode is bound by the cache
-// bytes, so halving them halves the time of the same schedule -- provided
-// shared memory, which every byte crosses, keeps up.
+// bytes, so halving them should halve the time -- provided the per-block work
+// on the chip keeps up with half the bytes.
 //
-// The schedule is that of the bf16 decode kernel: the G query heads sharing
-// a KV head are padded to the 128 rows of a tcgen05 MMA, one softmax warp
-// holds each head's 128 scores in one thread (row maxima, votes and the group
-// decision need no reduction across warps) and frees the S buffer as soon as
-// the scores are in registers, P has two TMEM buffers, and values are loaded
-// only for kept blocks, as soon as the decision exists.
+// Transposed products.  One CTA per (sequence, KV head, split).  The block's
+// 128 keys are the MMA rows and the G <= 8 query heads sharing the KV head
+// the columns (N = 16, padded):
+//   S^T = K_j Q^T   kind::f8f6f4, A = the E4M3 key tile straight from TMA,
+//                   B = the query as an exact E4M3 pair (below), 8 k-steps;
+//   O^T += V_j^T P^T  kind::f16, A = the fp16 value tile (MN-major: d is the
+//                   contiguous dimension), B = P^T (fp16, heads x keys).
+// So every thread of the four score warps owns one key of the block and its G
+// scores: a block costs G exponentials per thread for a kept block and one
+// cross-warp reduction of G maxima per block, spread over all four SMSPs,
+// and the tensor core computes 16 columns instead of 128 padded rows.
 //
-// Keys stay E4M3 all the way: S = Q K^T is a kind::f8f6f4 product straight
-// from the TMA tile.  The query is written once, exactly, as an E4M3 pair: per
-// head, q 2^e (the largest power of two keeping the row within 256) = hi + lo
-// with hi = E4M3(q 2^e) and lo = E4M3(q 2^e - hi), which for a bf16 row is
-// exact except for elements below about 2^-10 of the row's largest; S = hi
-// K^T + lo K^T (eight k-steps of 32 codes, fp32 accumulation) and 2^-e goes
-// into the head's score scale.  Values are widened, exactly, to fp16 by
-// converter warps (P is no E4M3 quantity: its small weights would vanish) and
-// O += P V is a kind::f16 product with P in fp16.  Widening the keys as well
-// would move three times their bytes through shared memory.  The key scale
-// multiplies the scores (folded into the score scale), the value scale the
-// split outputs.
+// The query: per head, q 2^e (the largest power of two keeping the row within
+// 256) = hi + lo with hi = E4M3(q 2^e) and lo = E4M3(q 2^e - hi), exact for a
+// bf16 row except for elements below about 2^-10 of its largest; S = hi K^T +
+// lo K^T and 2^-e goes into the head's score scale with the key scale.  P is
+// no E4M3 quantity (its small weights would vanish), so value tiles are
+// widened, exactly, to fp16 by converter warps (the fp16 pattern of code x
+// 2^-8; 2^8 goes into the value scale).
 //
-// Warp roles (256 threads):
-//   warp 0      softmax: lane g < G owns head g (TMEM lane g);
-//   warp 1      TMA producer of the E4M3 key tiles (every block, 6 stages);
-//   warp 2      Q.K^T issuer (A = the Q pair, B = the E4M3 key tile, both in
-//               shared memory; allocates TMEM);
-//   warp 3      TMA producer of the E4M3 value tiles of kept blocks (2 stages);
-//   warp 4      P.V issuer (A = P from TMEM, B = fp16 V tile);
-//   warps 5-7   value converters (follow the decisions; a third of each tile).
-// TMEM columns: S buffers [0,256), P buffers [256,384), O [384,512).
+// Warp roles (512 threads):
+//   warps 0-3   scores: thread = key 32w + lane of the block (TMEM lane);
+//               maxima, votes, decision, exponentials, P^T, row sums, O^T
+//               rescale, epilogue (thread = value dimension d);
+//   warp 4      TMA producer of the E4M3 key tiles (every block, 5 stages);
+//   warp 5      S^T issuer (allocates TMEM);
+//   warp 6      TMA producer of the E4M3 value tiles of kept blocks;
+//   warp 7      O^T issuer;
+//   warps 8-15  value converters (follow the decisions).
+// The decision ring holds 32 decisions and there are six P^T buffers, so the
+// score warps run ahead of the value loads and their widening by up to six
+// kept blocks; the value pipeline (load, widen, product) drains behind them.
+// TMEM columns: S^T buffers [0,64) (16 each), O^T [64,80).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -53,70 +57,105 @@ namespace {
 using namespace tc;
 
 constexpr int D = 128;    // head size (keys and values)
-constexpr int BC = 128;   // keys per block
-constexpr int MR = 128;   // MMA rows (heads padded)
-constexpr int NKF = 6;    // E4M3 key stages
-constexpr int NVF = 2;    // E4M3 value stages
+constexpr int BC = 128;   // keys per block (MMA rows of S^T)
+constexpr int NQ = 16;    // MMA columns: query heads, padded
+constexpr int NKF = 5;    // E4M3 key stages
+constexpr int NVF = 3;    // E4M3 value stages
 constexpr int NVH = 2;    // fp16 value stages
-constexpr int NS = 2;     // TMEM S buffers
-constexpr int NP = 2;     // TMEM P buffers
-constexpr int NDEC = 8;   // decision ring
-constexpr int NT = 8 * 32;
-constexpr int WARP_K = 1, WARP_QK = 2, WARP_V = 3, WARP_PV = 4;  // warp 0: softmax
-constexpr int WARP_VC = 5;                                        // three warps
-constexpr int NVC = 3 * 32;                                       // converter threads
-constexpr uint32_t F8_BYTES = BC * D;           // 16 KB: 128 rows x 128 codes
-constexpr uint32_t H_BYTES = BC * D * 2;        // 32 KB: 128 keys x 128 fp16
-constexpr uint32_t HALF_BYTES = H_BYTES / 2;    // one 64-column swizzled box
+constexpr int NS = 4;     // TMEM S^T buffers
+constexpr int NPT = 6;    // P^T buffers
+constexpr int NDEC = 32;  // decision ring
+constexpr int NT = 16 * 32;
+constexpr int WARP_K = 4, WARP_QK = 5, WARP_V = 6, WARP_PV = 7, WARP_VC = 8;  // 0-3: scores
+constexpr int NVC = 8 * 32;                                                 // converter threads
+constexpr uint32_t F8_BYTES = BC * D;         // 16 KB: 128 rows x 128 codes
+constexpr uint32_t H_BYTES = BC * D * 2;      // 32 KB: 128 keys x 128 fp16
+constexpr uint32_t HALF_BYTES = H_BYTES / 2;  // one 64-column swizzled box
+constexpr uint32_t QT_BYTES = NQ * 128;       // 2 KB: 16 rows x 128 codes
+constexpr uint32_t PT_BOX = NQ * 128;         // 2 KB: 16 heads x 64 fp16 keys
 constexpr uint32_t SMEM_KF = 0;
-constexpr uint32_t SMEM_Q = SMEM_KF + NKF * F8_BYTES;  // Q hi, then Q lo
-constexpr uint32_t SMEM_VF = SMEM_Q + 2 * F8_BYTES;
+constexpr uint32_t SMEM_VF = SMEM_KF + NKF * F8_BYTES;
 constexpr uint32_t SMEM_VH = SMEM_VF + NVF * F8_BYTES;
-constexpr uint32_t SMEM_TILES = SMEM_VH + NVH * H_BYTES;  // 224 KB
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_P = NS * BC;             // 256
-constexpr uint32_t TMEM_O = TMEM_P + NP * (BC / 2);  // 384
+constexpr uint32_t SMEM_Q = SMEM_VH + NVH * H_BYTES;  // Q hi, then Q lo
+constexpr uint32_t SMEM_PT = SMEM_Q + 2 * QT_BYTES;   // NPT x two 64-key boxes
+constexpr uint32_t SMEM_TILES = SMEM_PT + NPT * 2 * PT_BOX;  // 220 KB
+constexpr uint32_t TMEM_COLS = 128;
+constexpr uint32_t TMEM_O = NS * NQ;  // 64
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // exp reference may lag the max by 2^8
-constexpr uint32_t IDESC_QK = idesc_e4m3_f32(MR, BC);    // E4M3 x E4M3, both K-major
-constexpr uint32_t IDESC_PV = idesc_f16_f32(MR, D, 1);   // V tile: MN-major
-constexpr uint32_t NEG_INF_BITS = 0xff800000u;
-static_assert(TMEM_O + D == TMEM_COLS, "TMEM budget");
+// S^T: E4M3 x E4M3, both K-major.  O^T: fp16, A (V^T) MN-major, B (P^T) K-major.
+constexpr uint32_t IDESC_QK = idesc_e4m3_f32(BC, NQ);
+constexpr uint32_t IDESC_PV = idesc_f16_f32(D, NQ, 0) | (1u << 15);
+static_assert(TMEM_O + NQ <= TMEM_COLS, "TMEM budget");
 
 struct Shared {
   uint64_t kf_full[NKF], kf_empty[NKF];
   uint64_t vf_full[NVF], vf_empty[NVF];
   uint64_t vh_full[NVH], vh_empty[NVH];
   uint64_t s_full[NS], s_free[NS];
-  uint64_t p_full[NP], p_free[NP];
-  uint64_t pv_done[2];
+  uint64_t p_full[NPT], p_free[NPT];
   uint64_t dec_full[NDEC], dec_empty[NDEC];
+  uint64_t red_full[2];  // the four score warps' partial maxima of a block are in
+  uint64_t l_full;       // the four score warps' row sums are in
   int dec[NDEC];
+  float red[2][4][8];  // per block (double buffered): per score warp, per head max
+  float lsum[4][8];    // epilogue: per score warp, per head row sum
+  float sl2[NQ];       // per head: raw score -> log2 units
   uint32_t tmem_base;
   int abort;
 };
 constexpr uint32_t SMEM_ALLOC = SMEM_TILES + ((sizeof(Shared) + 127) / 128) * 128;
 static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
 
-// E4M3 tiles (the key tile, the two query tiles) as K-major operands of
-// Q.K^T: one 128-byte-swizzled box of 128 codes x 128 rows; k-step kk (32
-// codes) starts 32 bytes further, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t kmajor8_base(uint32_t tile) {
+// K-major E4M3 / fp16 operands with 128-byte rows: one 128-byte-swizzled box,
+// 8-row groups 1024 bytes apart; a k-step of 32 bytes (32 codes, 16 fp16).
+__device__ __forceinline__ uint64_t kmajor_base(uint32_t tile) {
   return smem_desc_sw128(tile, 16u, 1024u);
 }
-__device__ __forceinline__ constexpr uint64_t kmajor8_step(int kk) {
-  return (uint64_t)(((uint32_t)kk * 32u) >> 4);
+// P^T (16 heads x 128 fp16 keys) as K-major B: k-step kk (16 keys) is box kk/4
+// at 32-byte step kk%4.
+__device__ __forceinline__ constexpr uint64_t pt_step(int kk) {
+  return (uint64_t)(((uint32_t)(kk >> 2) * PT_BOX + (uint32_t)(kk & 3) * 32u) >> 4);
 }
-// fp16 value tiles: two 128-byte-swizzled boxes of 64 columns, 128 rows each,
-// as the MN-major B operand of P.V (rows are keys): 8-key groups 1024 bytes
-// apart, the second 64-value half 16 KB further; k-step kk (16 keys) starts
-// 2048 bytes further.
+// fp16 value tile (rows are keys, two 128-byte-swizzled boxes of 64 d values)
+// as the MN-major A operand V^T: the second 64-d half 16 KB further (LBO),
+// 8-key groups 1024 bytes apart (SBO); k-step kk (16 keys) 2048 bytes further.
 __device__ __forceinline__ uint64_t vmajor_base(uint32_t tile) {
   return smem_desc_sw128(tile, HALF_BYTES, 1024u);
 }
 __device__ __forceinline__ constexpr uint64_t vmajor_step(int kk) {
   return (uint64_t)(((uint32_t)kk * 2048u) >> 4);
+}
+
+// Maximum over the 32 lanes of the warp (one instruction on sm_100 family).
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// 32 lanes x 16 consecutive 32-bit columns (S^T or O^T rows of this warp's
+// lane quarter): thread i receives the 16 columns of its lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
 }
 
 // Two E4M3 codes -> an fp16 pair holding the code values times 2^-8, exactly
@@ -150,61 +189,6 @@ __device__ __forceinline__ void widen_chunk(uint32_t src_tile, uint32_t dst_tile
   st_shared_v4(box + ((c0 ^ sw) << 4), h[0], h[1], h[2], h[3]);
   st_shared_v4(box + (((c0 + 1) ^ sw) << 4), h[4], h[5], h[6], h[7]);
 }
-
-__device__ __forceinline__ float chunk_max(const uint32_t (&s)[32]) {
-  float m[11];
-#pragma unroll
-  for (int i = 0; i < 10; ++i)
-    m[i] = fmax3(__uint_as_float(s[3 * i]), __uint_as_float(s[3 * i + 1]),
-                 __uint_as_float(s[3 * i + 2]));
-  m[10] = fmaxf(__uint_as_float(s[30]), __uint_as_float(s[31]));
-  const float a = fmax3(m[0], m[1], m[2]), b = fmax3(m[3], m[4], m[5]);
-  const float c = fmax3(m[6], m[7], m[8]), d = fmaxf(m[9], m[10]);
-  return fmaxf(fmax3(a, b, c), d);
-}
-
-// P = exp2(s * sl2 - ref) for one 32-key chunk as 16 packed fp16 pairs, with
-// the row sum accumulated in two packed fp32 pairs.
-__device__ __forceinline__ void chunk_exp(const uint32_t (&s)[32], uint64_t sl2x2,
-                                          uint64_t negref2, uint64_t (&acc)[2],
-                                          uint32_t *pk) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    float x0, x1;
-    f2_split(f2_fma(f2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), sl2x2,
-                    negref2),
-             x0, x1);
-    const float p0 = ex2(x0), p1 = ex2(x1);
-    acc[i & 1] = f2_add(acc[i & 1], f2(p0, p1));
-    pk[i] = pack_f16x2(p0, p1);
-  }
-}
-
-// Scores of keys at or past the cache end (the zero-filled tail of the last
-// block) become -inf in TMEM before anything reads them.  Short and out of
-// line: it runs once per sequence from a cold instruction cache.
-__device__ __noinline__ void mask_tail_tmem(uint32_t sa, int lim) {
-  uint32_t ninf[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) ninf[i] = NEG_INF_BITS;
-#pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
-    const int l = lim - 32 * c;
-    if (l >= 32) continue;
-    if (l <= 0) {
-      tmem_st32(sa + 32 * c, ninf);
-      continue;
-    }
-    uint32_t x[32];
-    tmem_ld32(sa + 32 * c, x);
-    tmem_wait_ld_regs(x);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = i < l ? x[i] : NEG_INF_BITS;
-    tmem_st32(sa + 32 * c, x);
-  }
-  tmem_wait_st();
-}
-
 
 // The query pair of head row r (r < G: query head hk*G + r) into the two
 // E4M3 query tiles (128-byte-swizzled rows of 128 codes); other rows zero.
@@ -265,6 +249,7 @@ __device__ __forceinline__ int write_query_pair(const DecodeArgs &a, int b, int 
   return qexp;
 }
 
+template <int G>
 __global__ void __launch_bounds__(NT, 1)
     decode_fp8_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
@@ -276,7 +261,6 @@ __global__ void __launch_bounds__(NT, 1)
     if (tid == 0) atomicOr(a.err, kErrTimeout);
     return;
   }
-  const int G = a.Hq / a.Hkv;
   const int unit = blockIdx.x;
   const int sp = unit % a.n_splits;
   const int hk = (unit / a.n_splits) % a.Hkv;
@@ -297,39 +281,52 @@ __global__ void __launch_bounds__(NT, 1)
     return;
   }
 
-  // The query pair (threads 0-127, one row each); thread g < G keeps its
-  // head's exponent for the score scale.
-  int qexp = 0;
-  if (tid < MR) qexp = write_query_pair(a, b, hk, G, tid, base + SMEM_Q, base + SMEM_Q + F8_BYTES);
+  // The query pair (threads 0-15, one head row each, rows >= G zero) and each
+  // head's score scale; the P^T rows of the padding heads are zeroed once.
+  if (tid < NQ) {
+    const int e = write_query_pair(a, b, hk, G, tid, base + SMEM_Q, base + SMEM_Q + QT_BYTES);
+    sh.sl2[tid] = ldexpf(a.scale * __ldg(a.k_scale + zkv) * kLog2e, -e);
+  }
+  for (int idx = tid; idx < NPT * 2 * (NQ - 8) * 8; idx += NT) {  // rows 8..15, 16-byte chunks
+    const int c = idx & 7, r = 8 + ((idx >> 3) & 7), box = idx >> 6;
+    st_shared_v4(base + SMEM_PT + box * PT_BOX + r * 128 + c * 16, 0u, 0u, 0u, 0u);
+  }
+  if constexpr (G < 8) {
+    for (int idx = tid; idx < NPT * 2 * (8 - G) * 8; idx += NT) {  // rows G..7
+      const int c = idx & 7, r = G + (idx >> 3) % (8 - G), box = (idx >> 3) / (8 - G);
+      st_shared_v4(base + SMEM_PT + box * PT_BOX + r * 128 + c * 16, 0u, 0u, 0u, 0u);
+    }
+  }
   fence_proxy_async_smem();  // visible to the tensor core
   if (tid == 0) {
     for (int i = 0; i < NKF; ++i) {
       mbar_init(smem_u32(&sh.kf_full[i]), 1);
-      mbar_init(smem_u32(&sh.kf_empty[i]), 1);  // the Q.K^T commit
+      mbar_init(smem_u32(&sh.kf_empty[i]), 1);  // the S^T commit
     }
     for (int i = 0; i < NVF; ++i) {
       mbar_init(smem_u32(&sh.vf_full[i]), 1);
-      mbar_init(smem_u32(&sh.vf_empty[i]), 3);  // the three value converters
+      mbar_init(smem_u32(&sh.vf_empty[i]), 8);  // the eight value converters
     }
     for (int i = 0; i < NVH; ++i) {
-      mbar_init(smem_u32(&sh.vh_full[i]), 3);
-      mbar_init(smem_u32(&sh.vh_empty[i]), 1);  // the P.V commit
+      mbar_init(smem_u32(&sh.vh_full[i]), 8);
+      mbar_init(smem_u32(&sh.vh_empty[i]), 1);  // the O^T commit
     }
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&sh.s_full[i]), 1);
-      mbar_init(smem_u32(&sh.s_free[i]), 1);
+      mbar_init(smem_u32(&sh.s_free[i]), 4);  // the four score warps
     }
-    for (int i = 0; i < NP; ++i) {
-      mbar_init(smem_u32(&sh.p_full[i]), 1);
-      mbar_init(smem_u32(&sh.p_free[i]), 1);
+    for (int i = 0; i < NPT; ++i) {
+      mbar_init(smem_u32(&sh.p_full[i]), 4);  // the four score warps
+      mbar_init(smem_u32(&sh.p_free[i]), 1);  // the O^T commit
     }
-    mbar_init(smem_u32(&sh.pv_done[0]), 1);
-    mbar_init(smem_u32(&sh.pv_done[1]), 1);
     for (int i = 0; i < NDEC; ++i) {
       mbar_init(smem_u32(&sh.dec_full[i]), 1);
-      // readers: the value producer, the P.V issuer, the three value converters
-      mbar_init(smem_u32(&sh.dec_empty[i]), 5);
+      // readers: the value producer, the O^T issuer, the eight value converters
+      mbar_init(smem_u32(&sh.dec_empty[i]), 10);
     }
+    mbar_init(smem_u32(&sh.red_full[0]), 4);
+    mbar_init(smem_u32(&sh.red_full[1]), 4);
+    mbar_init(smem_u32(&sh.l_full), 4);
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -389,7 +386,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
   } else if (warp >= WARP_VC) {
     // -------------------------------------------------- value converters --
-    // Follow the decisions; chunks t, t + 96, ... (row = chunk / 8) of every
+    // Follow the decisions; chunks t, t + 256, ... (row = chunk / 8) of every
     // kept value tile.
     const int t0 = (warp - WARP_VC) * 32 + lane;
     int vi = 0;
@@ -419,31 +416,30 @@ __global__ void __launch_bounds__(NT, 1)
       ++vi;
     }
   } else if (warp == WARP_QK) {
-    // -------------------------------------------------------- Q.K^T issuer --
+    // --------------------------------------------------------- S^T issuer --
     if (lane == 0) {
-      const uint64_t qhi = kmajor8_base(base + SMEM_Q), qlo = kmajor8_base(base + SMEM_Q + F8_BYTES);
+      const uint64_t qhi = kmajor_base(base + SMEM_Q), qlo = kmajor_base(base + SMEM_Q + QT_BYTES);
       for (int j = 0; j < nb; ++j) {
         const int f = j % NKF, sb = j % NS;
         if (!mbar_wait(smem_u32(&sh.kf_full[f]), (j / NKF) & 1, abort, a.err, kErrTimeout))
           break;
-        // S buffer sb is free once the softmax warp has read block j - NS.
+        // S^T buffer sb is free once the score warps have read block j - NS.
         if (j >= NS && !mbar_wait(smem_u32(&sh.s_free[sb]), ((j / NS) - 1) & 1, abort, a.err,
                                   kErrTimeout))
           break;
         fence_after_sync();
-        const uint64_t kd = kmajor8_base(base + SMEM_KF + f * F8_BYTES);
-        const uint32_t d_s = tmem + sb * BC;
-        // S = hi K^T + lo K^T: four k-steps of 32 codes for each part.
+        const uint64_t kd = kmajor_base(base + SMEM_KF + f * F8_BYTES);
+        // S^T = K (hi)^T + K (lo)^T: four k-steps of 32 codes for each part.
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_f8f6f4_ss(d_s, (kk < 4 ? qhi : qlo) + kmajor8_step(kk & 3),
-                        kd + kmajor8_step(kk & 3), IDESC_QK, kk > 0);
+          mma_f8f6f4_ss(tmem + sb * NQ, kd + ((uint64_t)(kk & 3) * 2),
+                        (kk < 4 ? qhi : qlo) + ((uint64_t)(kk & 3) * 2), IDESC_QK, kk > 0);
         mma_commit(smem_u32(&sh.s_full[sb]));
         mma_commit(smem_u32(&sh.kf_empty[f]));
       }
     }
   } else if (warp == WARP_PV) {
-    // ---------------------------------------------------------- P.V issuer --
+    // --------------------------------------------------------- O^T issuer --
     if (lane == 0) {
       int kc = 0;
       for (int j = 0; j < nb && !*abort; ++j) {
@@ -453,37 +449,40 @@ __global__ void __launch_bounds__(NT, 1)
         const int keep = sh.dec[j % NDEC];
         mbar_arrive(smem_u32(&sh.dec_empty[j % NDEC]));
         if (!keep) continue;
-        const int pb = kc % NP, hs = kc % NVH;
-        if (!mbar_wait(smem_u32(&sh.p_full[pb]), (kc / NP) & 1, abort, a.err, kErrTimeout) ||
+        const int pb = kc % NPT, hs = kc % NVH;
+        if (!mbar_wait(smem_u32(&sh.p_full[pb]), (kc / NPT) & 1, abort, a.err, kErrTimeout) ||
             !mbar_wait(smem_u32(&sh.vh_full[hs]), (kc / NVH) & 1, abort, a.err, kErrTimeout))
           break;
         fence_after_sync();
-        // P (fp16 pairs): keys [0,128) in the 64 columns of P buffer pb.
-        const uint32_t pt = tmem + TMEM_P + pb * (BC / 2);
         const uint64_t vd = vmajor_base(base + SMEM_VH + hs * H_BYTES);
+        const uint64_t pd = kmajor_base(base + SMEM_PT + pb * 2 * PT_BOX);
 #pragma unroll
         for (int kk = 0; kk < BC / 16; ++kk)
-          mma_bf16_ts(tmem + TMEM_O, pt + kk * 8, vd + vmajor_step(kk), IDESC_PV,
+          mma_bf16_ss(tmem + TMEM_O, vd + vmajor_step(kk), pd + pt_step(kk), IDESC_PV,
                       (kc > 0 || kk > 0) ? 1u : 0u);
         mma_commit(smem_u32(&sh.vh_empty[hs]));
         mma_commit(smem_u32(&sh.p_free[pb]));
-        mma_commit(smem_u32(&sh.pv_done[kc & 1]));
         ++kc;
       }
     }
   } else {
-    // ------------------------------------------------------------- softmax --
-    // Lane g < G: head g's row (TMEM lane g) over the block's 128 keys.
-    const bool head = lane < G;
+    // ------------------------------------------------------------- scores --
+    // Thread = key kidx of the block (TMEM lane of S^T); G scores per thread.
+    // Every thread computes the same maxima, decisions and references from
+    // the four warps' partial maxima, so the warps stay in step.
+    const int kidx = warp * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     uint32_t *bits = a.bits + (size_t)unit * a.words;
-    // Raw score -> log2 units: the score scale, the key scale and 2^-e of the
-    // head's query pair.
-    const float sl2 = ldexpf(a.scale * __ldg(a.k_scale + zkv) * kLog2e, -qexp);
     const float c2 = a.ln_lambda * kLog2e;  // ln(lambda), log2 units
-    float m2 = -INFINITY;    // running max of the split (log2 units)
-    float mref = -INFINITY;  // exp reference (log2 units)
-    float l = 0.f;           // row sum relative to mref
-    int kc = 0;              // kept blocks
+    float sl2[G], m2[G], mref[G], l[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      sl2[g] = sh.sl2[g];
+      m2[g] = -INFINITY;
+      mref[g] = -INFINITY;
+      l[g] = 0.f;
+    }
+    int kc = 0;
     uint32_t word = 0;
     bool ok = true;
     for (int j = 0; j < nb; ++j) {
@@ -493,30 +492,41 @@ __global__ void __launch_bounds__(NT, 1)
         break;
       }
       fence_after_sync();
-      const uint32_t sa = tmem + sb * BC;  // lanes 0-31: this warp's TMEM quarter
-      const int lim = a.L - (j0 + j) * BC;
-      if (lim < BC) mask_tail_tmem(sa, lim);
-      uint32_t x0[32], x1[32], x2[32], x3[32];
-      tmem_ld32(sa, x0);
-      tmem_ld32(sa + 32, x1);
-      tmem_ld32(sa + 64, x2);
-      tmem_ld32(sa + 96, x3);
-      tmem_wait_ld_regs(x0);
-      tmem_wait_ld_regs(x1);
-      tmem_wait_ld_regs(x2);
-      tmem_wait_ld_regs(x3);
-      // The scores are in registers: the S buffer can take block j + NS.
-      fence_before_sync();
+      uint32_t x[16];
+      tmem_ld16(lane_base + sb * NQ, x);
+      fence_before_sync();  // the scores are in registers: S^T buffer sb is free
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.s_free[sb]));
-      const float mt =
-          fmaxf(fmaxf(chunk_max(x0), chunk_max(x1)), fmaxf(chunk_max(x2), chunk_max(x3)));
-      const float pm2 = mt * sl2;
-      // With c < 0, "rowmax - m_new < c" is "rowmax - m_old < c" (a block
-      // that raises the max fails both).  Every head must vote skip.
-      const float diff = (mt == -INFINITY) ? -INFINITY : pm2 - m2;
-      const bool skip = __all_sync(0xffffffffu, !head || diff < c2);
-      if (lane == 0) {
+      const bool valid = (j0 + j) * BC + kidx < a.L;
+      float s[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        s[g] = valid ? __uint_as_float(x[g]) * sl2[g] : -INFINITY;
+        const float v = warp_max(s[g]);
+        if (lane == 0) sh.red[j & 1][warp][g] = v;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.red_full[j & 1]));
+      if (!mbar_wait_warp(smem_u32(&sh.red_full[j & 1]), (j >> 1) & 1, abort, a.err,
+                          kErrTimeout)) {
+        ok = false;
+        break;
+      }
+      // Block maxima per head; with c < 0, "rowmax - m_new < c" is "rowmax -
+      // m_old < c" (a block that raises the max fails both).  Every head must
+      // vote skip.
+      bool skip = true;
+      float mnew[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float bm = fmaxf(fmaxf(sh.red[j & 1][0][g], sh.red[j & 1][1][g]),
+                               fmaxf(sh.red[j & 1][2][g], sh.red[j & 1][3][g]));
+        const float diff = (bm == -INFINITY) ? -INFINITY : bm - m2[g];
+        skip = skip && (diff < c2);
+        mnew[g] = fmaxf(m2[g], bm);
+        m2[g] = mnew[g];  // the running max advances on every block
+      }
+      if (tid == 0) {
         // On a timeout the abort flag is raised and every later wait fails.
         if (j < NDEC || mbar_wait(smem_u32(&sh.dec_empty[j % NDEC]), ((j / NDEC) - 1) & 1,
                                   abort, a.err, kErrTimeout)) {
@@ -529,64 +539,63 @@ __global__ void __launch_bounds__(NT, 1)
           word = 0;
         }
       }
-      // The running max advances on every block (a skipped block leaves it unchanged).
-      const float mnew = fmaxf(m2, pm2);
-      m2 = mnew;
       if (skip) continue;
+      // Kept: exponent references (rescaled lazily, as in the other kernels),
+      // this key's P for every head, the per-thread row sums.
       bool rescale = false;
-      float alpha = 1.f;
-      if (mref == -INFINITY) {
-        mref = mnew;
-      } else if (mnew > mref + kRescaleLog2) {
-        alpha = ex2(mref - mnew);
-        mref = mnew;
-        rescale = true;
+      float alpha[G], p[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        alpha[g] = 1.f;
+        if (mref[g] == -INFINITY) {
+          mref[g] = mnew[g];
+        } else if (mnew[g] > mref[g] + kRescaleLog2) {
+          alpha[g] = ex2(mref[g] - mnew[g]);
+          mref[g] = mnew[g];
+          rescale = true;
+        }
+        p[g] = ex2(s[g] - mref[g]);
+        l[g] = l[g] * alpha[g] + p[g];
       }
-      const int pb = kc % NP;
-      // P buffer pb last fed the P.V of kept block kc - NP.
-      if (kc >= NP && !mbar_wait_warp(smem_u32(&sh.p_free[pb]), ((kc / NP) - 1) & 1, abort,
-                                      a.err, kErrTimeout)) {
+      const int pb = kc % NPT;
+      // P^T buffer pb last fed the O^T product of kept block kc - NPT.
+      if (kc >= NPT && !mbar_wait_warp(smem_u32(&sh.p_free[pb]), ((kc / NPT) - 1) & 1, abort,
+                                       a.err, kErrTimeout)) {
         ok = false;
         break;
       }
-      fence_after_sync();
-      const uint32_t pa = tmem + TMEM_P + pb * (BC / 2);
-      const uint64_t sl2x2 = f2(sl2, sl2), negref2 = f2(-mref, -mref);
-      uint64_t acc2[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
       {
-        uint32_t pk[32];
-        chunk_exp(x0, sl2x2, negref2, acc2, pk);
-        chunk_exp(x1, sl2x2, negref2, acc2, pk + 16);
-        tmem_st32(pa, pk);
-        chunk_exp(x2, sl2x2, negref2, acc2, pk);
-        chunk_exp(x3, sl2x2, negref2, acc2, pk + 16);
-        tmem_st32(pa + 32, pk);
+        // P^T[g][kidx] (fp16): box kidx / 64, row g, 16-byte chunk (kidx % 64) / 8
+        // at chunk position chunk ^ (g % 8).
+        const uint32_t box = base + SMEM_PT + (uint32_t)(pb * 2 + (kidx >> 6)) * PT_BOX;
+        const uint32_t kk = (uint32_t)(kidx & 63);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const uint32_t addr = box + (uint32_t)g * 128u + ((((kk >> 3) ^ (uint32_t)g)) << 4) +
+                                (kk & 7u) * 2u;
+          const unsigned short hv = __half_as_ushort(__float2half_rn(p[g]));
+          asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(hv) : "memory");
+        }
       }
-      tmem_wait_st();
-      float acc[4];
-      f2_split(acc2[0], acc[0], acc[1]);
-      f2_split(acc2[1], acc[2], acc[3]);
-      l = l * alpha + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
-      // O rescale of the heads' rows once the previous P.V has landed.
-      if (__any_sync(0xffffffffu, rescale) && kc >= 1) {
-        if (!mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort,
+      // O^T rescale (columns g of this warp's lanes) once the previous product
+      // has landed (its commit to the P^T buffer it read; the score warps may be
+      // several kept blocks ahead, so a two-slot completion ring could alias);
+      // the same decision in every thread.
+      if (rescale && kc >= 1) {
+        if (!mbar_wait_warp(smem_u32(&sh.p_free[(kc - 1) % NPT]), ((kc - 1) / NPT) & 1, abort,
                             a.err, kErrTimeout)) {
           ok = false;
           break;
         }
         fence_after_sync();
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          const uint32_t oa = tmem + TMEM_O + c * 32;
-          tmem_ld32(oa, o);
-          tmem_wait_ld_regs(o);
+        uint32_t o[16];
+        tmem_ld16(lane_base + TMEM_O, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(oa, o);
-        }
+        for (int g = 0; g < G; ++g) o[g] = __float_as_uint(__uint_as_float(o[g]) * alpha[g]);
+        tmem_st16(lane_base + TMEM_O, o);
         tmem_wait_st();
       }
+      fence_proxy_async_smem();  // P^T is visible to the tensor core
       fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[pb]));
@@ -594,31 +603,33 @@ __global__ void __launch_bounds__(NT, 1)
     }
 
     // ---- epilogue: O_s = v_scale * O / l and LSE_s = ref + ln l per head ----
-    if (lane == 0)
+    if (tid == 0)
       for (int w = ((nb - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
-    if (ok && kc > 0)
-      ok = mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort, a.err,
-                          kErrTimeout);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float v = l[g];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) sh.lsum[warp][g] = v;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&sh.l_full));
+    if (ok) ok = mbar_wait_warp(smem_u32(&sh.l_full), 0, abort, a.err, kErrTimeout);
+    if (ok && kc > 0)  // the last product has landed
+      ok = mbar_wait_warp(smem_u32(&sh.p_free[(kc - 1) % NPT]), ((kc - 1) / NPT) & 1, abort,
+                          a.err, kErrTimeout);
     if (ok) {
       fence_after_sync();
-      const float inv = __ldg(a.v_scale + zkv) * 256.f / l;  // values were widened times 2^-8
-      const size_t row = (size_t)(b * a.Hq + hk * G + lane) * a.n_splits + sp;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tmem + TMEM_O + c * 32, o);
-        tmem_wait_ld_regs(o);
-        if (head) {
-          float4 *dst = reinterpret_cast<float4 *>(a.o_part + row * D + c * 32);
+      uint32_t o[16];
+      tmem_ld16(lane_base + TMEM_O, o);  // thread = value dimension d = kidx
+      const float vs = __ldg(a.v_scale + zkv) * 256.f;  // values were widened times 2^-8
 #pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4)
-            dst[q4] = make_float4(__uint_as_float(o[4 * q4]) * inv,
-                                  __uint_as_float(o[4 * q4 + 1]) * inv,
-                                  __uint_as_float(o[4 * q4 + 2]) * inv,
-                                  __uint_as_float(o[4 * q4 + 3]) * inv);
-        }
+      for (int g = 0; g < G; ++g) {
+        const float lt = (sh.lsum[0][g] + sh.lsum[1][g]) + (sh.lsum[2][g] + sh.lsum[3][g]);
+        const size_t row = (size_t)(b * a.Hq + hk * G + g) * a.n_splits + sp;
+        a.o_part[row * D + kidx] = __uint_as_float(o[g]) * (vs / lt);
+        if (tid == 0) a.lse_part[row] = mref[g] * kLn2 + logf(lt);
       }
-      if (head) a.lse_part[row] = mref * kLn2 + logf(l);
     }
   }
 
@@ -640,11 +651,18 @@ cudaError_t launch_decode_fp8(const DecodeArgs &a, cudaStream_t s) {
   if (!make_map_u8_3d(&mk, a.k, D, a.k_row_stride, a.L, a.B * a.Hkv, BC) ||
       !make_map_u8_3d(&mv, a.v, D, a.v_row_stride, a.L, a.B * a.Hkv, BC))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_fp8_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
+  const int G = a.Hq / a.Hkv;
+  auto kernel = G == 1   ? decode_fp8_kernel<1>
+                : G == 2 ? decode_fp8_kernel<2>
+                : G == 4 ? decode_fp8_kernel<4>
+                : G == 8 ? decode_fp8_kernel<8>
+                         : nullptr;
+  if (!kernel) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_ALLOC);
   if (e != cudaSuccess) return e;
   const long units = (long)a.B * a.Hkv * a.n_splits;
-  decode_fp8_kernel<<<(unsigned)units, NT, SMEM_ALLOC, s>>>(mk, mv, a);
+  kernel<<<(unsigned)units, NT, SMEM_ALLOC, s>>>(mk, mv, a);
   return cudaGetLastError();
 }
 
