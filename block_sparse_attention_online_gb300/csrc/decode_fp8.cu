@@ -33,14 +33,16 @@
 //   warps 0-3   scores: thread = key 32w + lane of the block (TMEM lane);
 //               maxima, votes, decision, exponentials, P^T, row sums, O^T
 //               rescale, epilogue (thread = value dimension d);
-//   warp 4      TMA producer of the E4M3 key tiles (every block, 5 stages);
+//   warp 4      TMA producer of the E4M3 key tiles (every block, 7 stages);
 //   warp 5      S^T issuer (allocates TMEM);
 //   warp 6      TMA producer of the E4M3 value tiles of kept blocks;
 //   warp 7      O^T issuer;
 //   warps 8-15  value converters (follow the decisions).
-// The decision ring holds 32 decisions and there are six P^T buffers, so the
-// score warps run ahead of the value loads and their widening by up to six
-// kept blocks; the value pipeline (load, widen, product) drains behind them.
+// The decision ring holds 32 decisions and there are three P^T buffers, so
+// the score warps run ahead of the value loads and their widening by up to
+// three kept blocks; the value pipeline (load, widen, product) drains behind
+// them.  Seven key stages (112 KB) keep enough bytes in flight to cover the
+// load latency under a full GPU's traffic (~2.8 us measured).
 // TMEM columns: S^T buffers [0,64) (16 each), O^T [64,80).
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -59,11 +61,11 @@ using namespace tc;
 constexpr int D = 128;    // head size (keys and values)
 constexpr int BC = 128;   // keys per block (MMA rows of S^T)
 constexpr int NQ = 16;    // MMA columns: query heads, padded
-constexpr int NKF = 5;    // E4M3 key stages
-constexpr int NVF = 3;    // E4M3 value stages
+constexpr int NKF = 7;    // E4M3 key stages (bytes in flight cover the load latency)
+constexpr int NVF = 2;    // E4M3 value stages
 constexpr int NVH = 2;    // fp16 value stages
 constexpr int NS = 4;     // TMEM S^T buffers
-constexpr int NPT = 6;    // P^T buffers
+constexpr int NPT = 3;    // P^T buffers
 constexpr int NDEC = 32;  // decision ring
 constexpr int NT = 16 * 32;
 constexpr int WARP_K = 4, WARP_QK = 5, WARP_V = 6, WARP_PV = 7, WARP_VC = 8;  // 0-3: scores
@@ -78,7 +80,7 @@ constexpr uint32_t SMEM_VF = SMEM_KF + NKF * F8_BYTES;
 constexpr uint32_t SMEM_VH = SMEM_VF + NVF * F8_BYTES;
 constexpr uint32_t SMEM_Q = SMEM_VH + NVH * H_BYTES;  // Q hi, then Q lo
 constexpr uint32_t SMEM_PT = SMEM_Q + 2 * QT_BYTES;   // NPT x two 64-key boxes
-constexpr uint32_t SMEM_TILES = SMEM_PT + NPT * 2 * PT_BOX;  // 220 KB
+constexpr uint32_t SMEM_TILES = SMEM_PT + NPT * 2 * PT_BOX;  // 224 KB
 constexpr uint32_t TMEM_COLS = 128;
 constexpr uint32_t TMEM_O = NS * NQ;  // 64
 constexpr float kLog2e = 1.4426950408889634f;
@@ -88,6 +90,8 @@ constexpr float kRescaleLog2 = 8.0f;  // exp reference may lag the max by 2^8
 constexpr uint32_t IDESC_QK = idesc_e4m3_f32(BC, NQ);
 constexpr uint32_t IDESC_PV = idesc_f16_f32(D, NQ, 0) | (1u << 15);
 static_assert(TMEM_O + NQ <= TMEM_COLS, "TMEM budget");
+static_assert(NS % 2 == 0, "block pairs read two adjacent S^T buffers");
+static_assert(NT >= NQ * 16, "16 threads per query row write the query pair");
 
 struct Shared {
   uint64_t kf_full[NKF], kf_empty[NKF];
@@ -96,10 +100,10 @@ struct Shared {
   uint64_t s_full[NS], s_free[NS];
   uint64_t p_full[NPT], p_free[NPT];
   uint64_t dec_full[NDEC], dec_empty[NDEC];
-  uint64_t red_full[2];  // the four score warps' partial maxima of a block are in
+  uint64_t red_full[2];  // the four score warps' partial maxima of a block pair are in
   uint64_t l_full;       // the four score warps' row sums are in
   int dec[NDEC];
-  float red[2][4][8];  // per block (double buffered): per score warp, per head max
+  float red[2][4][16];  // per block pair (double buffered): per score warp, per head max
   float lsum[4][8];    // epilogue: per score warp, per head row sum
   float sl2[NQ];       // per head: raw score -> log2 units
   uint32_t tmem_base;
@@ -190,63 +194,57 @@ __device__ __forceinline__ void widen_chunk(uint32_t src_tile, uint32_t dst_tile
   st_shared_v4(box + (((c0 + 1) ^ sw) << 4), h[4], h[5], h[6], h[7]);
 }
 
-// The query pair of head row r (r < G: query head hk*G + r) into the two
-// E4M3 query tiles (128-byte-swizzled rows of 128 codes); other rows zero.
-// Returns the row's exponent e (q 2^e = hi + lo, max |q| 2^e <= 256).
-__device__ __forceinline__ int write_query_pair(const DecodeArgs &a, int b, int hk, int G, int r,
-                                                uint32_t q_hi, uint32_t q_lo) {
-  const uint32_t sw = (uint32_t)(r & 7);
-  if (r >= G) {
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint32_t off = (uint32_t)r * 128u + (((uint32_t)c ^ sw) << 4);
-      st_shared_v4(q_hi + off, 0u, 0u, 0u, 0u);
-      st_shared_v4(q_lo + off, 0u, 0u, 0u, 0u);
-    }
-    return 0;
-  }
-  // bf16 pairs of the row (low element first), 8 per 16-byte load.
-  const uint4 *qr = reinterpret_cast<const uint4 *>((const __nv_bfloat16 *)a.q +
-                                                    (size_t)(b * a.Hq + hk * G + r) * D);
+// The query pair into the two E4M3 query tiles (16 rows of 128 codes,
+// 128-byte-swizzled), by threads 0-255: thread t takes row r = t / 16 (query
+// head hk*G + r, zero for r >= G) and its 16-byte chunk t % 16 of bf16
+// values, so the whole query is read in one round of coalesced loads.  Per
+// row: e = 8 - ceil(log2 max|q|) (the largest power of two with max|q| 2^e <=
+// 256), hi = E4M3(q 2^e), lo = E4M3(q 2^e - hi), both nearest even; sl2[r] =
+// the row's score scale (scale * key scale * log2 e * 2^-e).
+__device__ __forceinline__ void write_query_pair(const DecodeArgs &a, int b, int hk, int G, int zkv,
+                                                 int t, uint32_t q_hi, uint32_t q_lo,
+                                                 float *sl2) {
+  const int r = t >> 4, c16 = t & 15;
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (r < G)
+    v = __ldg(reinterpret_cast<const uint4 *>((const __nv_bfloat16 *)a.q +
+                                              (size_t)(b * a.Hq + hk * G + r) * D) + c16);
+  const uint32_t pr[4] = {v.x, v.y, v.z, v.w};  // bf16 pairs, low element first
   uint32_t amax_bits = 0;  // |bf16| bit patterns order like their values
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const uint4 v = __ldg(qr + i);
-    amax_bits = max(amax_bits, max(v.x & 0x7fffu, (v.x >> 16) & 0x7fffu));
-    amax_bits = max(amax_bits, max(v.y & 0x7fffu, (v.y >> 16) & 0x7fffu));
-    amax_bits = max(amax_bits, max(v.z & 0x7fffu, (v.z >> 16) & 0x7fffu));
-    amax_bits = max(amax_bits, max(v.w & 0x7fffu, (v.w >> 16) & 0x7fffu));
-  }
+  for (int i = 0; i < 4; ++i)
+    amax_bits = max(amax_bits, max(pr[i] & 0x7fffu, (pr[i] >> 16) & 0x7fffu));
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1)  // the 16 threads of the row
+    amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, o));
   const float amax = __uint_as_float(amax_bits << 16);
   int ex = 0;
   const float fr = frexpf(amax > 0.f ? amax : 1.f, &ex);  // amax = fr * 2^ex
   const int qexp = amax > 0.f ? 8 - (fr == 0.5f ? ex - 1 : ex) : 0;  // 8 - ceil(log2 amax)
-#pragma unroll 2
-  for (int c = 0; c < 8; ++c) {  // codes 16c .. 16c+15: two 16-byte loads of bf16
-    const uint4 v0 = __ldg(qr + 2 * c), v1 = __ldg(qr + 2 * c + 1);
-    const uint32_t pr[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    uint32_t hi[4], lo[4];
+  uint32_t hi[2], lo[2];
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      uint32_t wh = 0, wl = 0;
+  for (int w = 0; w < 2; ++w) {
+    uint32_t wh = 0, wl = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t pair = pr[2 * w + (i >> 1)];
-        const float q = __uint_as_float((i & 1) ? (pair & 0xffff0000u) : (pair << 16));
-        const float x = ldexpf(q, qexp);      // exact
-        const __nv_fp8_e4m3 h(x);             // nearest even
-        const __nv_fp8_e4m3 l(x - (float)h);  // x - h is exact
-        wh |= (uint32_t)h.__x << (8 * i);
-        wl |= (uint32_t)l.__x << (8 * i);
-      }
-      hi[w] = wh;
-      lo[w] = wl;
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t pair = pr[2 * w + (i >> 1)];
+      const float q = __uint_as_float((i & 1) ? (pair & 0xffff0000u) : (pair << 16));
+      const float x = ldexpf(q, qexp);      // exact
+      const __nv_fp8_e4m3 h(x);             // nearest even
+      const __nv_fp8_e4m3 l(x - (float)h);  // x - h is exact
+      wh |= (uint32_t)h.__x << (8 * i);
+      wl |= (uint32_t)l.__x << (8 * i);
     }
-    const uint32_t off = (uint32_t)r * 128u + (((uint32_t)c ^ sw) << 4);
-    st_shared_v4(q_hi + off, hi[0], hi[1], hi[2], hi[3]);
-    st_shared_v4(q_lo + off, lo[0], lo[1], lo[2], lo[3]);
+    hi[w] = wh;
+    lo[w] = wl;
   }
-  return qexp;
+  const uint32_t off = (uint32_t)r * 128u + ((((uint32_t)c16 >> 1) ^ (uint32_t)(r & 7)) << 4) +
+                       ((uint32_t)c16 & 1u) * 8u;
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(q_hi + off), "r"(hi[0]), "r"(hi[1])
+               : "memory");
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(q_lo + off), "r"(lo[0]), "r"(lo[1])
+               : "memory");
+  if (c16 == 0) sl2[r] = ldexpf(a.scale * __ldg(a.k_scale + zkv) * kLog2e, -qexp);
 }
 
 template <int G>
@@ -281,12 +279,10 @@ __global__ void __launch_bounds__(NT, 1)
     return;
   }
 
-  // The query pair (threads 0-15, one head row each, rows >= G zero) and each
-  // head's score scale; the P^T rows of the padding heads are zeroed once.
-  if (tid < NQ) {
-    const int e = write_query_pair(a, b, hk, G, tid, base + SMEM_Q, base + SMEM_Q + QT_BYTES);
-    sh.sl2[tid] = ldexpf(a.scale * __ldg(a.k_scale + zkv) * kLog2e, -e);
-  }
+  // The query pair and each head's score scale; the P^T rows of the padding
+  // heads are zeroed once.
+  if (tid < NQ * 16)
+    write_query_pair(a, b, hk, G, zkv, tid, base + SMEM_Q, base + SMEM_Q + QT_BYTES, sh.sl2);
   for (int idx = tid; idx < NPT * 2 * (NQ - 8) * 8; idx += NT) {  // rows 8..15, 16-byte chunks
     const int c = idx & 7, r = 8 + ((idx >> 3) & 7), box = idx >> 6;
     st_shared_v4(base + SMEM_PT + box * PT_BOX + r * 128 + c * 16, 0u, 0u, 0u, 0u);
@@ -485,63 +481,10 @@ __global__ void __launch_bounds__(NT, 1)
     int kc = 0;
     uint32_t word = 0;
     bool ok = true;
-    for (int j = 0; j < nb; ++j) {
-      const int sb = j % NS;
-      if (!mbar_wait_warp(smem_u32(&sh.s_full[sb]), (j / NS) & 1, abort, a.err, kErrTimeout)) {
-        ok = false;
-        break;
-      }
-      fence_after_sync();
-      uint32_t x[16];
-      tmem_ld16(lane_base + sb * NQ, x);
-      fence_before_sync();  // the scores are in registers: S^T buffer sb is free
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.s_free[sb]));
-      const bool valid = (j0 + j) * BC + kidx < a.L;
-      float s[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        s[g] = valid ? __uint_as_float(x[g]) * sl2[g] : -INFINITY;
-        const float v = warp_max(s[g]);
-        if (lane == 0) sh.red[j & 1][warp][g] = v;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.red_full[j & 1]));
-      if (!mbar_wait_warp(smem_u32(&sh.red_full[j & 1]), (j >> 1) & 1, abort, a.err,
-                          kErrTimeout)) {
-        ok = false;
-        break;
-      }
-      // Block maxima per head; with c < 0, "rowmax - m_new < c" is "rowmax -
-      // m_old < c" (a block that raises the max fails both).  Every head must
-      // vote skip.
-      bool skip = true;
-      float mnew[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float bm = fmaxf(fmaxf(sh.red[j & 1][0][g], sh.red[j & 1][1][g]),
-                               fmaxf(sh.red[j & 1][2][g], sh.red[j & 1][3][g]));
-        const float diff = (bm == -INFINITY) ? -INFINITY : bm - m2[g];
-        skip = skip && (diff < c2);
-        mnew[g] = fmaxf(m2[g], bm);
-        m2[g] = mnew[g];  // the running max advances on every block
-      }
-      if (tid == 0) {
-        // On a timeout the abort flag is raised and every later wait fails.
-        if (j < NDEC || mbar_wait(smem_u32(&sh.dec_empty[j % NDEC]), ((j / NDEC) - 1) & 1,
-                                  abort, a.err, kErrTimeout)) {
-          sh.dec[j % NDEC] = skip ? 0 : 1;
-          mbar_arrive(smem_u32(&sh.dec_full[j % NDEC]));
-        }
-        if (skip) word |= 1u << (j & 31);
-        if ((j & 31) == 31 || j == nb - 1) {
-          bits[j >> 5] = word;
-          word = 0;
-        }
-      }
-      if (skip) continue;
-      // Kept: exponent references (rescaled lazily, as in the other kernels),
-      // this key's P for every head, the per-thread row sums.
+    // Kept block: exponent references (rescaled lazily, as in the other
+    // kernels), this key's P for every head into the next P^T buffer, the
+    // per-thread row sums, an O^T rescale when a reference moved.
+    auto kept = [&](const float (&s)[G], const float (&mnew)[G]) -> bool {
       bool rescale = false;
       float alpha[G], p[G];
 #pragma unroll
@@ -560,10 +503,8 @@ __global__ void __launch_bounds__(NT, 1)
       const int pb = kc % NPT;
       // P^T buffer pb last fed the O^T product of kept block kc - NPT.
       if (kc >= NPT && !mbar_wait_warp(smem_u32(&sh.p_free[pb]), ((kc / NPT) - 1) & 1, abort,
-                                       a.err, kErrTimeout)) {
-        ok = false;
-        break;
-      }
+                                       a.err, kErrTimeout))
+        return false;
       {
         // P^T[g][kidx] (fp16): box kidx / 64, row g, 16-byte chunk (kidx % 64) / 8
         // at chunk position chunk ^ (g % 8).
@@ -583,10 +524,8 @@ __global__ void __launch_bounds__(NT, 1)
       // the same decision in every thread.
       if (rescale && kc >= 1) {
         if (!mbar_wait_warp(smem_u32(&sh.p_free[(kc - 1) % NPT]), ((kc - 1) / NPT) & 1, abort,
-                            a.err, kErrTimeout)) {
-          ok = false;
-          break;
-        }
+                            a.err, kErrTimeout))
+          return false;
         fence_after_sync();
         uint32_t o[16];
         tmem_ld16(lane_base + TMEM_O, o);
@@ -600,6 +539,95 @@ __global__ void __launch_bounds__(NT, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[pb]));
       ++kc;
+      return true;
+    };
+    // Decision of block jj (thread 0): published to the value pipeline; bitmap.
+    auto publish = [&](int jj, bool skip) {
+      // On a timeout the abort flag is raised and every later wait fails.
+      if (jj < NDEC || mbar_wait(smem_u32(&sh.dec_empty[jj % NDEC]), ((jj / NDEC) - 1) & 1,
+                                 abort, a.err, kErrTimeout)) {
+        sh.dec[jj % NDEC] = skip ? 0 : 1;
+        mbar_arrive(smem_u32(&sh.dec_full[jj % NDEC]));
+      }
+      if (skip) word |= 1u << (jj & 31);
+      if ((jj & 31) == 31 || jj == nb - 1) {
+        bits[jj >> 5] = word;
+        word = 0;
+      }
+    };
+    // Blocks in pairs: both S^T buffers read at once (j even, so they are
+    // adjacent), both blocks' partial maxima exchanged in one round.
+    for (int j = 0; j < nb; j += 2) {
+      const bool two = j + 1 < nb;
+      const int sb = j % NS;
+      const int q = j >> 1;  // pair index
+      if (!mbar_wait_warp(smem_u32(&sh.s_full[sb]), (j / NS) & 1, abort, a.err, kErrTimeout) ||
+          (two && !mbar_wait_warp(smem_u32(&sh.s_full[sb + 1]), ((j + 1) / NS) & 1, abort, a.err,
+                                  kErrTimeout))) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      uint32_t x[32];
+      tmem_ld32(lane_base + sb * NQ, x);  // block j in columns [0,16), j + 1 in [16,32)
+      tmem_wait_ld_regs(x);
+      fence_before_sync();  // the scores are in registers: the S^T buffers are free
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&sh.s_free[sb]));
+        if (two) mbar_arrive(smem_u32(&sh.s_free[sb + 1]));
+      }
+      const bool v0 = (j0 + j) * BC + kidx < a.L;
+      const bool v1 = two && (j0 + j + 1) * BC + kidx < a.L;
+      float s0[G], s1[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        s0[g] = v0 ? __uint_as_float(x[g]) * sl2[g] : -INFINITY;
+        s1[g] = v1 ? __uint_as_float(x[16 + g]) * sl2[g] : -INFINITY;
+        const float m0 = warp_max(s0[g]), m1 = warp_max(s1[g]);
+        if (lane == 0) {
+          sh.red[q & 1][warp][g] = m0;
+          sh.red[q & 1][warp][8 + g] = m1;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.red_full[q & 1]));
+      if (!mbar_wait_warp(smem_u32(&sh.red_full[q & 1]), (q >> 1) & 1, abort, a.err,
+                          kErrTimeout)) {
+        ok = false;
+        break;
+      }
+      // Block maxima per head; with c < 0, "rowmax - m_new < c" is "rowmax -
+      // m_old < c" (a block that raises the max fails both).  Every head must
+      // vote skip.  Block j + 1 is tested against the max after block j.
+      bool skip0 = true, skip1 = true;
+      float mn0[G], mn1[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float b0 = fmaxf(fmaxf(sh.red[q & 1][0][g], sh.red[q & 1][1][g]),
+                               fmaxf(sh.red[q & 1][2][g], sh.red[q & 1][3][g]));
+        const float d0 = (b0 == -INFINITY) ? -INFINITY : b0 - m2[g];
+        skip0 = skip0 && (d0 < c2);
+        mn0[g] = fmaxf(m2[g], b0);
+        const float b1 = fmaxf(fmaxf(sh.red[q & 1][0][8 + g], sh.red[q & 1][1][8 + g]),
+                               fmaxf(sh.red[q & 1][2][8 + g], sh.red[q & 1][3][8 + g]));
+        const float d1 = (b1 == -INFINITY) ? -INFINITY : b1 - mn0[g];
+        skip1 = skip1 && (d1 < c2);
+        mn1[g] = fmaxf(mn0[g], b1);
+        m2[g] = two ? mn1[g] : mn0[g];  // the running max advances on every block
+      }
+      if (tid == 0) {
+        publish(j, skip0);
+        if (two) publish(j + 1, skip1);
+      }
+      if (!skip0 && !kept(s0, mn0)) {
+        ok = false;
+        break;
+      }
+      if (two && !skip1 && !kept(s1, mn1)) {
+        ok = false;
+        break;
+      }
     }
 
     // ---- epilogue: O_s = v_scale * O / l and LSE_s = ref + ln l per head ----
