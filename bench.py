@@ -47,8 +47,8 @@ CSRC = os.path.join(ROOT, "block_sparse_attention_online_gb300", "csrc")
 NCU_TRAFFIC = {
     "prefill_tc_kernel": {
         "file": "prefill_tc.cu",
-        "sha256": "de67a4dad17928c67bc3c2254eedb58c7682d897b6452eb16e8dee353e4ec812",
-        "bytes": 241140736 + 82635008},
+        "sha256": "565262cdacc29a5c12f5ba9a6da792ccebf73aea9608800dd853200960eba536",
+        "bytes": 240405760 + 82815744},
     "decode_tc_kernel": {
         "file": "decode.cu",
         "sha256": "ff34ba73cd4d7a696421321d8216e9dfb410f7de5c3dc96dfc0ac0f5ea45e540",
