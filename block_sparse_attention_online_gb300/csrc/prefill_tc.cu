@@ -12,7 +12,7 @@
 // MMA, so it never touches shared memory.
 //
 // One CTA per (batch, query head, query tile), longest causal tiles first.
-// Warp roles (384 threads):
+// Warp roles (416 threads):
 //   warps 0-3  deciders: warp w owns query rows 32w..32w+31 (TMEM lane
 //              quarter w) over all 128 key columns.  Per block: the row max
 //              of S_j, the row vote against the running max before the
@@ -26,13 +26,14 @@
 //              the block's S buffer), the row sum, and an O rescale in TMEM
 //              when the exp reference moves by > 2^8;
 //   warp 8     TMA producer of Q (once) and K_j (every block);
-//   warp 9     Q.K^T issuer: S_j = Q K_j^T up to three blocks ahead (also
-//              allocates TMEM);
+//   warps 9, 12 Q.K^T issuers (even / odd traversed blocks): S_j = Q K_j^T
+//              up to three blocks ahead (warp 9 also allocates TMEM);
 //   warp 10    TMA producer of V_j, for kept blocks only, as soon as the
 //              block's decision is known;
 //   warp 11    P.V issuer: O += P_j V_j (P from TMEM) for kept blocks; the
-//              commit of that product frees the S buffer of a kept block.
-// Two issuing threads keep one product chain from waiting on the other's
+//              commit of that product frees the S buffer of a kept block
+//              (the decision frees that of a skipped block).
+// Separate issuing threads keep one product chain from waiting on another's
 // barriers: a tcgen05.mma issue is accepted at about the rate the tensor core
 // retires it, so a single issuer serialises every wait with every product.
 // TMEM columns: three S buffers [0,384), O [384,512).
@@ -61,8 +62,14 @@ constexpr int NS = 3;         // TMEM S buffers
 constexpr int NDEC = 4;       // decision ring
 constexpr int NQ = 4;     // decider warps (0-3) and exponential warps (4-7): one per TMEM lane quarter
 constexpr int NSOFT = 2 * NQ;
-constexpr int NTHREADS = (NSOFT + 4) * 32;
-constexpr int WARP_K = NSOFT, WARP_MMA = NSOFT + 1, WARP_V = NSOFT + 2, WARP_PV = NSOFT + 3;
+constexpr int kDeciderBarrier = 1;  // named barrier of the four decider warps
+// Two Q.K^T issuers (even and odd blocks): a thread that issues tcgen05.mma
+// is held until the tensor pipe takes each instruction, so one issuer's
+// barrier waits between blocks leave the pipe idle; with two, one waits while
+// the other issues.
+constexpr int NTHREADS = (NSOFT + 5) * 32;
+constexpr int WARP_K = NSOFT, WARP_MMA = NSOFT + 1, WARP_V = NSOFT + 2, WARP_PV = NSOFT + 3,
+              WARP_MMA2 = NSOFT + 4;
 constexpr uint32_t TILE_BYTES = BM * D * 2;      // 32 KB: one 128 x 128 bf16 tile
 constexpr uint32_t HALF_BYTES = TILE_BYTES / 2;  // one 64-column swizzled box
 constexpr uint32_t SMEM_Q = 0;
@@ -99,10 +106,8 @@ struct Shared {
   uint64_t pv_done[2];
   uint64_t dec_full[NDEC];
   uint64_t dec_read[NDEC];  // the V producer, the P.V issuer and the exponential warps read slot j % NDEC
-  uint64_t vote_full[2];
   uint64_t l_full;
   int dec[NDEC];
-  unsigned keepw[3];  // ring: bit w set when decider warp w votes "keep" for the block
   float wstat[2][NQ];  // statistics mode: per decider warp, max over its rows of rowmax - m_new
   // [S buffer][row] running max after the buffer's block (log2 units), from
   // the deciders to the exponential warps.
@@ -396,15 +401,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&sh.s_full[i]), 1);
-      mbar_init(smem_u32(&sh.s_free[i]), 1);  // the P.V commit of a kept block
+      // once per block: the decision of a skipped block, the P.V commit of a kept one
+      mbar_init(smem_u32(&sh.s_free[i]), 1);
       mbar_init(smem_u32(&sh.p_full[i]), NQ);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh.pv_done[i]), 1);
-      mbar_init(smem_u32(&sh.vote_full[i]), NQ);
     }
     mbar_init(smem_u32(&sh.l_full), NQ);
-    sh.keepw[0] = sh.keepw[1] = sh.keepw[2] = 0u;
     for (int i = 0; i < NDEC; ++i) {
       mbar_init(smem_u32(&sh.dec_full[i]), 1);
       mbar_init(smem_u32(&sh.dec_read[i]), 2 + NQ);
@@ -529,43 +533,40 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_wait_drain(smem_u32(&sh.v_full[s]), (last / NV) & 1);
       }
     }
-  } else if (warp == WARP_MMA) {
-    // -------------------------------------------------------- Q.K^T issuer --
-    if (lane == 0) {
-      bool ok = mbar_wait(smem_u32(&sh.q_full), 0, abort, a.err, kErrTimeout);
+  } else if (warp == WARP_MMA || warp == WARP_MMA2) {
+    // ------------------------------------------- Q.K^T issuers (c even / odd) --
+    // The whole warp waits (a warp-wide poll resolves faster than one lane's);
+    // lane 0 issues.
+    {
+      const int mine = warp == WARP_MMA ? 0 : 1;
+      bool ok = mbar_wait_warp(smem_u32(&sh.q_full), 0, abort, a.err, kErrTimeout);
       fence_after_sync();
       const uint64_t qdesc = kmajor_base(base + SMEM_Q);
-      int pv_into[NS] = {0, 0, 0};  // P.V products issued into each S buffer
       int cc = 0;
       for (int j = 0; ok && j < nblk; ++j) {
         if constexpr (SET) {
           if (!in_set(j)) continue;
         }
         const int c = SET ? cc++ : j;
+        if ((c & 1) != mine) continue;
         const int s = c % NK, sb = c % NS;
-        if (!mbar_wait(smem_u32(&sh.k_full[s]), (c / NK) & 1, abort, a.err, kErrTimeout)) break;
-        if (c >= NS) {
-          // S buffer sb last held block j - NS: free once its scores were read
-          // (a skipped block: its decision exists) or its P.V completed (kept).
-          const int cp = c - NS;
-          if (!mbar_wait(smem_u32(&sh.dec_full[cp % NDEC]), (cp / NDEC) & 1, abort, a.err,
-                         kErrTimeout))
-            break;
-          if (sh.dec[cp % NDEC]) {
-            ++pv_into[sb];
-            if (!mbar_wait(smem_u32(&sh.s_free[sb]), (pv_into[sb] - 1) & 1, abort, a.err,
-                           kErrTimeout))
-              break;
-          }
-        }
+        if (!mbar_wait_warp(smem_u32(&sh.k_full[s]), (c / NK) & 1, abort, a.err, kErrTimeout)) break;
+        // S buffer sb last held block c - NS: free once that block was
+        // decided (skipped) or its P.V completed (kept); one phase per block.
+        if (c >= NS &&
+            !mbar_wait_warp(smem_u32(&sh.s_free[sb]), ((c / NS) - 1) & 1, abort, a.err, kErrTimeout))
+          break;
         fence_after_sync();
-        const uint64_t kd = kmajor_base(base + SMEM_K + s * TILE_BYTES);
-        const uint32_t d_s = tmem + sb * BN;
+        if (lane == 0) {
+          const uint64_t kd = kmajor_base(base + SMEM_K + s * TILE_BYTES);
+          const uint32_t d_s = tmem + sb * BN;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ss(d_s, qdesc + kmajor_step(kk), kd + kmajor_step(kk), IDESC_QK, kk > 0);
-        mma_commit(smem_u32(&sh.s_full[sb]));
-        mma_commit(smem_u32(&sh.k_empty[s]));
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ss(d_s, qdesc + kmajor_step(kk), kd + kmajor_step(kk), IDESC_QK, kk > 0);
+          mma_commit(smem_u32(&sh.s_full[sb]));
+          mma_commit(smem_u32(&sh.k_empty[s]));
+        }
+        __syncwarp();
       }
     }
   } else if (warp == WARP_PV) {
@@ -637,53 +638,48 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           if (!in_set(j)) continue;
         }
         const int c = SET ? cc++ : j;
-        const int sbn = sb == NS - 1 ? 0 : sb + 1;
-        // Slot sbn was last read after the barrier of block j-2, before every
-        // decider arrived at the barrier of block j-1.
-        if (tid == 0) sh.keepw[sbn] = 0u;
-        if (!mbar_wait_warp(smem_u32(&sh.s_full[sb]), (c / NS) & 1, abort, a.err, kErrTimeout)) {
-          ok = false;
-          break;
-        }
-        fence_after_sync();
-        const uint32_t sa = lane_base + sb * BN;
-        if (needs_mask(j)) mask_block_tmem(sa, j * BN, row, a.causal, T);
-        uint32_t x0[32], x1[32], x2[32], x3[32];
-        tmem_ld32(sa, x0);
-        tmem_ld32(sa + 32, x1);
-        tmem_ld32(sa + 64, x2);
-        tmem_ld32(sa + 96, x3);
-        tmem_wait_ld_regs(x0);
-        tmem_wait_ld_regs(x1);
-        tmem_wait_ld_regs(x2);
-        tmem_wait_ld_regs(x3);
-        const float mt =
-            fmaxf(fmaxf(chunk_max(x0), chunk_max(x1)), fmaxf(chunk_max(x2), chunk_max(x3)));
-        const float pm2 = mt * sl2;
-        // With c < 0, "rowmax - m_new < c" is "rowmax - m_old < c" (a block
-        // that raises the max fails both).
-        const float diff = (mt == -INFINITY) ? -INFINITY : pm2 - m2;
-        const unsigned all = __all_sync(0xffffffffu, !valid || (diff < c2));
-        const float mnew = fmaxf(m2, pm2);
-        sh.mdec[sb][r] = mnew;
-        if (lane == 0 && !all) atomicOr(&sh.keepw[sb], 1u << warp);
-        if constexpr (STATS) {
-          // rowmax - m_new = min(rowmax - m_old, 0) (log2 units) over valid rows.
-          float st = (valid && mt != -INFINITY) ? fminf(diff, 0.f) : -INFINITY;
+        // Once a wait has failed (the abort flag is up and every later wait
+        // fails at once) the loop still runs to its end, so that the four
+        // warps meet the vote barrier equally often.
+        if (ok) ok = mbar_wait_warp(smem_u32(&sh.s_full[sb]), (c / NS) & 1, abort, a.err, kErrTimeout);
+        bool keep_vote = false;  // warp-uniform: some row of this warp keeps the block
+        float mnew = m2;
+        if (ok) {
+          fence_after_sync();
+          const uint32_t sa = lane_base + sb * BN;
+          if (needs_mask(j)) mask_block_tmem(sa, j * BN, row, a.causal, T);
+          uint32_t x0[32], x1[32], x2[32], x3[32];
+          tmem_ld32(sa, x0);
+          tmem_ld32(sa + 32, x1);
+          tmem_ld32(sa + 64, x2);
+          tmem_ld32(sa + 96, x3);
+          tmem_wait_ld_regs(x0);
+          tmem_wait_ld_regs(x1);
+          tmem_wait_ld_regs(x2);
+          tmem_wait_ld_regs(x3);
+          const float mt =
+              fmaxf(fmaxf(chunk_max(x0), chunk_max(x1)), fmaxf(chunk_max(x2), chunk_max(x3)));
+          const float pm2 = mt * sl2;
+          // With c < 0, "rowmax - m_new < c" is "rowmax - m_old < c" (a block
+          // that raises the max fails both).
+          const float diff = (mt == -INFINITY) ? -INFINITY : pm2 - m2;
+          keep_vote = !__all_sync(0xffffffffu, !valid || (diff < c2));
+          mnew = fmaxf(m2, pm2);
+          sh.mdec[sb][r] = mnew;
+          if constexpr (STATS) {
+            // rowmax - m_new = min(rowmax - m_old, 0) (log2 units) over valid rows.
+            float st = (valid && mt != -INFINITY) ? fminf(diff, 0.f) : -INFINITY;
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1) st = fmaxf(st, __shfl_xor_sync(0xffffffffu, st, o));
-          if (lane == 0) sh.wstat[c & 1][warp] = st;
+            for (int o = 16; o > 0; o >>= 1) st = fmaxf(st, __shfl_xor_sync(0xffffffffu, st, o));
+            if (lane == 0) sh.wstat[c & 1][warp] = st;
+          }
+          fence_before_sync();  // this warp's reads of S_j are complete
         }
-        fence_before_sync();  // this warp's reads of S_j are complete
-        __syncwarp();
-        const int vb = c & 1;
-        if (lane == 0) mbar_arrive(smem_u32(&sh.vote_full[vb]));
-        if (!mbar_wait_warp(smem_u32(&sh.vote_full[vb]), (c >> 1) & 1, abort, a.err,
-                            kErrTimeout)) {
-          ok = false;
-          break;
-        }
-        const bool skip = STATS || sh.keepw[sb] == 0u;
+        // The block is kept if any of the four warps votes keep: one
+        // reduction on the deciders' named barrier.
+        const bool any_keep = bar_red_or(kDeciderBarrier, NQ * 32, keep_vote);
+        if (!ok) continue;
+        const bool skip = STATS || !any_keep;
         m2 = mnew;
         if (STATS && tid == 0) {
           const float st = fmaxf(fmaxf(sh.wstat[c & 1][0], sh.wstat[c & 1][1]),
@@ -691,15 +687,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           a.margin[((size_t)bh * a.n_t + t) * a.n_b + j] = st * kLn2;
         }
         if (tid == 0) {
-          // (A skipped block's S buffer is reused by the Q.K^T issuer as soon
-          // as it reads this decision.)  The slot's previous decision (block
-          // j - NDEC) must have been read by all its readers; on a timeout the
-          // abort flag is raised and every later wait fails.
+          // The slot's previous decision (block j - NDEC) must have been read
+          // by all its readers; on a timeout the abort flag is raised and
+          // every later wait fails.
           if (c < NDEC || mbar_wait(smem_u32(&sh.dec_read[c % NDEC]), ((c / NDEC) - 1) & 1,
                                     abort, a.err, kErrTimeout)) {
             sh.dec[c % NDEC] = skip ? 0 : 1;
             mbar_arrive(smem_u32(&sh.dec_full[c % NDEC]));
           }
+          // A skipped block's S buffer is free: every decider has read it
+          // (the vote barrier above) and nothing else will.
+          if (skip) mbar_arrive(smem_u32(&sh.s_free[sb]));
           if constexpr (SET) {
             // Words before this block's are complete (untraversed blocks read 0).
             for (; wcur < (j >> 5); ++wcur) {
@@ -713,7 +711,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             word = 0;
           }
         }
-        sb = sbn;
+        sb = sb == NS - 1 ? 0 : sb + 1;
       }
       if (tid == 0) {
         if constexpr (SET) {

@@ -75,6 +75,23 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, err, code));
 }
 
+// OR of `pred` over the `nthreads` threads (whole, converged warps) that use
+// named barrier `id` (1-15; 0 is __syncthreads); a barrier with the memory
+// ordering of bar.sync.  Every participating warp must reach it equally
+// often: no wait of its own, so callers keep their loops in step.
+__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.cta.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+      : "memory");
+  return out != 0;
+}
+
 // Bounded wait that ignores the abort flag: used to drain copies in flight
 // before a CTA exits.  Returns false if the phase did not complete in time.
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
