@@ -686,10 +686,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                                  fmaxf(sh.wstat[c & 1][2], sh.wstat[c & 1][3]));
           a.margin[((size_t)bh * a.n_t + t) * a.n_b + j] = st * kLn2;
         }
-        if (tid == 0) {
-          // The slot's previous decision (block j - NDEC) must have been read
-          // by all its readers; on a timeout the abort flag is raised and
-          // every later wait fails.
+        if (lane == 0 && warp == (c & (NQ - 1))) {
+          // Lane 0 of decider warp c % 4 publishes (the next vote barrier
+          // keeps the publications in block order).  The slot's previous
+          // decision (block c - NDEC) must have been read by all its readers;
+          // on a timeout the abort flag is raised and every later wait fails.
           if (c < NDEC || mbar_wait(smem_u32(&sh.dec_read[c % NDEC]), ((c / NDEC) - 1) & 1,
                                     abort, a.err, kErrTimeout)) {
             sh.dec[c % NDEC] = skip ? 0 : 1;
@@ -698,6 +699,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // A skipped block's S buffer is free: every decider has read it
           // (the vote barrier above) and nothing else will.
           if (skip) mbar_arrive(smem_u32(&sh.s_free[sb]));
+        }
+        if (tid == 0) {
           if constexpr (SET) {
             // Words before this block's are complete (untraversed blocks read 0).
             for (; wcur < (j >> 5); ++wcur) {
