@@ -38,6 +38,7 @@ METRIC = "skip-softmax attn: prefill dense-equiv TFLOP/s, decode tok/s & GB/s @~
 PREFILL = W.GQA_PREFILL_16K
 DECODE = W.GQA_DECODE_32K
 MLA = W.MLA_DECODE_16K
+LONG = W.GQA_PREFILL_64K
 TARGET = "0.7"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 CSRC = os.path.join(ROOT, "block_sparse_attention_online_gb300", "csrc")
@@ -47,8 +48,8 @@ CSRC = os.path.join(ROOT, "block_sparse_attention_online_gb300", "csrc")
 NCU_TRAFFIC = {
     "prefill_tc_kernel": {
         "file": "prefill_tc.cu",
-        "sha256": "565262cdacc29a5c12f5ba9a6da792ccebf73aea9608800dd853200960eba536",
-        "bytes": 240405760 + 82815744},
+        "sha256": "8fc65664af79915ab9ddef22824ce0a6a708f25342b9b4f8d1cbcd5c0c602ebe",
+        "bytes": 234921728 + 82440960},
     "decode_tc_kernel": {
         "file": "decode.cu",
         "sha256": "ff34ba73cd4d7a696421321d8216e9dfb410f7de5c3dc96dfc0ac0f5ea45e540",
@@ -265,6 +266,7 @@ def run_gpu(args, rank, world):
         "head_sparsity": float(bs.unpack_bits(hbits, -(-n_b // D.n_splits)).float().mean())}
 
     msweep = mla_sweep(args, bs, dev, stream, flush, lam)
+    lsweep = long_prefill_sweep(args, bs, dev, stream, flush, lam, pk)
     calib = calibration(args, bs, dev, stream, flush, dq, dk_, dv_, dqd, dkd, lp, ld, pbits)
     blocks = block_set_sweep(args, bs, dev, stream, flush, dq, dk_, dv_, lp, po, plse, pbits)
     santa = santa_sweep(args, bs, dev, stream, flush)
@@ -329,13 +331,15 @@ def run_gpu(args, rank, world):
                     "sparsity": round(s70["sparsity"], 4),
                     "dense_equiv_tflops": round(value / world, 2),
                     "executed_tflops": round(executed_tflops, 2),
-                    "sweep": {t: {kk: (round(vv, 5) if isinstance(vv, float) else vv)
+                    "sweep": {t: {kk: (round(vv, 5) if isinstance(vv, float) and kk != "lambda"
+                                       else vv)
                                   for kk, vv in s.items()} for t, s in sweep.items()}},
         "decode": {"ms": round(d_avg, 4), "ms_combine": round(c_avg, 4),
                    "lambda": ld[TARGET], "sparsity": round(dec["sparsity"], 4),
                    "tok_per_s": round(world * D.B / ((d_avg + c_avg) / 1e3), 1),
                    "gbs": round(dec_gbs, 1), "hbm_frac": round(dec_gbs / peak_hbm, 4),
-                   "sweep": {t: {kk: (round(vv, 5) if isinstance(vv, float) else vv)
+                   "sweep": {t: {kk: (round(vv, 5) if isinstance(vv, float) and kk != "lambda"
+                                      else vv)
                                  for kk, vv in s.items()} for t, s in dsweep.items()}},
         "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel",
                      "achieved": round(executed_tflops, 2), "peak": peak_tf,
@@ -352,6 +356,7 @@ def run_gpu(args, rank, world):
                             "traffic": ncu_traffic("decode_tc_kernel"),
                             "algorithmic_bytes": dec["bytes"]},
         "mla_decode": msweep,
+        "long_prefill": lsweep,
         "calibration": calib,
         "block_set": blocks,
         "santa_decode": santa,
@@ -402,6 +407,42 @@ def mla_sweep(args, bs, dev, stream, flush, lam):
     out["max"]["speedup_vs_lambda0"] = round(out["0.0"]["ms"] / out["max"]["ms"], 4)
     out["workload"] = (f"B{M.B} Hq{M.Hq} latent dk{M.dk} dv{M.dv} L{M.L} Bc{M.Bc} "
                        f"splits{M.n_splits}; 'max' = largest sparsity any lambda < 1 reaches")
+    return out
+
+
+def long_prefill_sweep(args, bs, dev, stream, flush, lam, pk):
+    """Long causal GQA prefill (B=1, 32/8 heads, d=128, T=65536, 1 % salient
+    keys plus the local band) at lambda = 0 and the 50/70/85 % thresholds."""
+    C = LONG
+    q, k, v = W.prefill_inputs(C)
+    dq, dk_, dv_ = q.to(dev), k.to(dev), v.to(dev)
+    del q, k, v
+    o = torch.empty(C.B, C.Hq, C.T, C.d, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(C.B, C.Hq, C.T, dtype=torch.float32, device=dev)
+    bits = torch.empty(bs.prefill_bitmap_shape(C.B, C.Hq, C.T, C.Br, C.Bc), dtype=torch.int32,
+                       device=dev)
+    pairs = traversed_pairs(C)
+    dense, per_pair = prefill_flops(C)
+    peak_tf = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    out = {"workload": f"{C.name}: B{C.B} Hq{C.Hq} Hkv{C.Hkv} d{C.d} T{C.T} causal "
+                       f"Br{C.Br} Bc{C.Bc}; {C.salient_frac:.0%} salient keys, band "
+                       f"+{C.band_a:g}*sqrt(d) on each tile's 256 nearest keys",
+           "dense_equiv_flops": dense}
+    for t in ("0.0", "0.5", "0.7", "0.85"):
+        lmb = lam[C.name][t]["lambda"]
+        durs = timed_launches(
+            lambda: bs.attn_skip_prefill(dq, dk_, dv_, lmb, C.Br, C.Bc, True,
+                                         out=(o, lse, bits)),
+            args.warmup, args.steps, flush, stream)
+        skipped = int(bs.unpack_bits(bits, C.n_b).sum())
+        executed = per_pair * (2 * pairs - skipped)
+        ms = statistics.mean(durs)
+        out[t] = {"lambda": lmb, "sparsity": round(skipped / pairs, 4), "ms": round(ms, 4),
+                  "dense_equiv_tflops": round(dense / ms / 1e9, 2),
+                  "executed_tflops": round(executed / ms / 1e9, 2),
+                  "executed_frac_of_peak": round(executed / ms / 1e9 / peak_tf, 4)}
+    for t in ("0.5", "0.7", "0.85"):
+        out[t]["speedup_vs_lambda0"] = round(out["0.0"]["ms"] / out[t]["ms"], 4)
     return out
 
 
