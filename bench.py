@@ -52,8 +52,8 @@ NCU_TRAFFIC = {
         "bytes": 234921728 + 82440960},
     "decode_tc_kernel": {
         "file": "decode.cu",
-        "sha256": "ff34ba73cd4d7a696421321d8216e9dfb410f7de5c3dc96dfc0ac0f5ea45e540",
-        "bytes": 1396185600 + 3996928},
+        "sha256": "67c9de81d8f8ee7ddce7a6299cee4da7e507f86994a81d430c15461053d8a9e0",
+        "bytes": 1396106752 + 4154112},
 }
 
 
@@ -830,7 +830,8 @@ def run_reference(args):
 def run_profile_case(args):
     """Warm-up launches then one launch of a single kernel at the ~70 %
     threshold, for an ncu capture (prefill: the T=16384 workload, inputs 201 MB;
-    decode: the B=16, L=32768 workload, 2.1 GB)."""
+    decode: the B=16, L=32768 workload, 2.1 GB; mla: the absorbed-MLA decode,
+    B=32, L=16384, 604 MB of latent rows, at lambda = 0)."""
     from block_sparse_attention_online_gb300 import binding as bs
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -839,6 +840,13 @@ def run_profile_case(args):
         q, k, v = (x.to(dev) for x in W.prefill_inputs(PREFILL))
         lmb = lam[PREFILL.name][TARGET]["lambda"]
         fn = lambda: bs.attn_skip_prefill(q, k, v, lmb, PREFILL.Br, PREFILL.Bc, True)  # noqa: E731
+    elif args.profile == "mla":
+        q, k, _ = (x.to(dev) if x is not None else None for x in W.decode_inputs(MLA))
+        lmb = lam[MLA.name]["0.0"]["lambda"]
+
+        def fn():
+            op, lp, _ = bs.attn_skip_decode(q, k, None, lmb, MLA.Bc, MLA.n_splits, dv=MLA.dv)
+            bs.attn_skip_decode_combine(op, lp)
     elif args.profile == "fp8":
         C = W.GQA_DECODE_FP8_32K
         q, k8, v8, ks, vs = (x.to(dev) for x in W.decode_inputs_fp8(C))
@@ -870,7 +878,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--calibration-sweep", action="store_true",
                     help="also fit the threshold model over prefill lengths 4K-64K")
-    ap.add_argument("--profile", choices=("prefill", "decode", "fp8"),
+    ap.add_argument("--profile", choices=("prefill", "decode", "fp8", "mla"),
                     help="only warm up and launch one kernel (for ncu captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
