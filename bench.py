@@ -313,6 +313,8 @@ def run_gpu(args, rank, world):
 
     # ---- end to end: pinned host buffers, copies inside the timed region --
     e2e = end_to_end(args, bs, dev, stream, q, k, v, lp[TARGET])
+    # Any bounded wait that gave up anywhere in the run raises here.
+    bs.attn_skip_last_device_error()
 
     peak_tf = pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
     peak_hbm = pk.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])
@@ -363,6 +365,7 @@ def run_gpu(args, rank, world):
         "varlen_prefill": varlen,
         "fp8_decode": fp8,
         "e2e": e2e,
+        "device_errors": "none (device error word read after the run)",
         "gpu_launches": 3 * args.steps,  # prefill, decode, merge per timed step
         "clocks": clk.summary(),
     }

@@ -56,10 +56,18 @@ using namespace tc;
 constexpr int D = 128;        // head size of keys and values
 constexpr int BM = 128;       // query rows per tile
 constexpr int BN = 128;       // keys per block
-constexpr int NK = 3;         // K stages
-constexpr int NV = 3;         // V stages
+constexpr int NK = 4;         // K stages
+constexpr int NV = 2;         // V stages
 constexpr int NS = 3;         // TMEM S buffers
 constexpr int NDEC = 4;       // decision ring
+// Blocks whose S buffers go back to one issuer's s_free set: b % NS and the
+// issuer parity (b + NS) & 1 repeat every kFreePeriod blocks.
+constexpr int kFreePeriod = (NS % 2) ? 2 * NS : NS;
+// The two Q.K^T issuers take alternate blocks; with an even K stage count
+// every stage belongs to one issuer, whose waits on its k_full phases then
+// come in load order (with an odd count, a wait could find the stage's
+// previous load, the other issuer's block, still in flight and pass early).
+static_assert(NK % 2 == 0, "K stages: an even count (one issuer per stage)");
 constexpr int NQ = 4;     // decider warps (0-3) and exponential warps (4-7): one per TMEM lane quarter
 constexpr int NSOFT = 2 * NQ;
 constexpr int kDeciderBarrier = 1;  // named barrier of the four decider warps
@@ -96,14 +104,28 @@ struct Shared {
   uint64_t q_full;
   uint64_t k_full[NK], k_empty[NK];
   uint64_t v_full[NV], v_empty[NV];
-  uint64_t s_full[NS], s_free[NS];
+  uint64_t s_full[NS];
+  // S buffer of block b free again (its decision if skipped, its P.V commit if
+  // kept), for the issuer of block b + NS, one barrier set per issuer.  Block
+  // b + NS is the other issuer's (NS is odd), so with one shared set an
+  // issuer could wait for the phase of block b while the phase of block
+  // b - NS (the other issuer's business) was still pending, and a parity wait
+  // would pass at once.  Per issuer the phases follow that issuer's own order.
+  uint64_t s_free[2][NS];
   // P of kept block kc ready, slot kc % NS.  Kept blocks whose P exists but
   // whose P.V has not completed each hold an S buffer, so at most NS are
   // outstanding and a slot is never re-armed before its phase was consumed
   // (with fewer slots than S buffers the exponential warps could complete a
   // slot's next phase first when a value load is slow).
   uint64_t p_full[NS];
-  uint64_t pv_done[2];
+  // P.V of kept block kc complete, slot kc % NS.  Up to NS kept blocks can
+  // have a P.V in flight (each holds its S buffer), so with NS slots each slot
+  // has at most one phase pending and a wait on it has one meaning; a commit
+  // also covers every earlier product of the issuing thread.  (With two slots
+  // the end-of-tile wait could see an older pending phase of the other
+  // parity, pass early, and let the epilogue read O before the last products
+  // landed.)
+  uint64_t pv_done[NS];
   uint64_t dec_full[NDEC];
   uint64_t dec_read[NDEC];  // the V producer, the P.V issuer and the exponential warps read slot j % NDEC
   uint64_t l_full;
@@ -402,10 +424,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&sh.s_full[i]), 1);
       // once per block: the decision of a skipped block, the P.V commit of a kept one
-      mbar_init(smem_u32(&sh.s_free[i]), 1);
+      mbar_init(smem_u32(&sh.s_free[0][i]), 1);
+      mbar_init(smem_u32(&sh.s_free[1][i]), 1);
       mbar_init(smem_u32(&sh.p_full[i]), NQ);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&sh.pv_done[i]), 1);
     }
     mbar_init(smem_u32(&sh.l_full), NQ);
@@ -552,9 +575,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int s = c % NK, sb = c % NS;
         if (!mbar_wait_warp(smem_u32(&sh.k_full[s]), (c / NK) & 1, abort, a.err, kErrTimeout)) break;
         // S buffer sb last held block c - NS: free once that block was
-        // decided (skipped) or its P.V completed (kept); one phase per block.
-        if (c >= NS &&
-            !mbar_wait_warp(smem_u32(&sh.s_free[sb]), ((c / NS) - 1) & 1, abort, a.err, kErrTimeout))
+        // decided (skipped) or its P.V completed (kept); in this issuer's set
+        // one phase per such block, in this issuer's order.
+        if (c >= NS && !mbar_wait_warp(smem_u32(&sh.s_free[c & 1][sb]),
+                                       ((c - NS) / kFreePeriod) & 1, abort, a.err, kErrTimeout))
           break;
         fence_after_sync();
         if (lane == 0) {
@@ -584,7 +608,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int keep = sh.dec[i % NDEC];
         mbar_arrive(smem_u32(&sh.dec_read[i % NDEC]));
         if (!keep) continue;
-        const int pb = kc & 1, vs = vi % NV;
+        const int pb = kc % NS, vs = vi % NV;
         if (!mbar_wait(smem_u32(&sh.p_full[kc % NS]), (kc / NS) & 1, abort, a.err, kErrTimeout))
           break;
         if (!mbar_wait(smem_u32(&sh.v_full[vs]), (vi / NV) & 1, abort, a.err, kErrTimeout))
@@ -599,7 +623,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_bf16_ts(d_o, pt + kk * 8, vd + vmajor_step(kk), IDESC_PV, kk > 0 ? 1u : acc0);
         mma_commit(smem_u32(&sh.v_empty[vs]));
-        mma_commit(smem_u32(&sh.s_free[i % NS]));
+        mma_commit(smem_u32(&sh.s_free[(i + NS) & 1][i % NS]));
         mma_commit(smem_u32(&sh.pv_done[pb]));
         ++kc;
         ++vi;
@@ -698,7 +722,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           // A skipped block's S buffer is free: every decider has read it
           // (the vote barrier above) and nothing else will.
-          if (skip) mbar_arrive(smem_u32(&sh.s_free[sb]));
+          if (skip) mbar_arrive(smem_u32(&sh.s_free[(c + NS) & 1][sb]));
         }
         if (tid == 0) {
           if constexpr (SET) {
@@ -784,7 +808,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // O rescale of this warp's rows (warp-wide if any row needs it), after
         // the previous P.V landed.
         if (__any_sync(0xffffffffu, rescale) && kc >= 1) {
-          if (!mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort,
+          if (!mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) % NS]), ((kc - 1) / NS) & 1, abort,
                               a.err, kErrTimeout)) {
             ok = false;
             break;
@@ -808,7 +832,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         ++kc;
       }
       if (ok && kc > 0) {
-        ok = mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) & 1]), ((kc - 1) >> 1) & 1, abort,
+        ok = mbar_wait_warp(smem_u32(&sh.pv_done[(kc - 1) % NS]), ((kc - 1) / NS) & 1, abort,
                             a.err, kErrTimeout);
       }
       sh.lfin[r] = l;
