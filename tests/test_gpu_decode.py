@@ -70,6 +70,17 @@ def test_decode_split_counts_and_empty_splits(n_splits):
     check_decode(cfg, q, k, v, 1e-10, n_splits)
 
 
+@pytest.mark.parametrize("L", [1, 127, 129])
+@pytest.mark.parametrize("n_splits", [1, 4])
+def test_decode_shortest_caches(L, n_splits):
+    """A cache of one key, one ragged block, and one key past a block; with
+    four splits some splits own no block (LSE -inf, O 0, merged away)."""
+    cfg = W.GQA_DECODE_32K.with_(B=3, L=L, seed=66)
+    q, k, v = W.decode_inputs(cfg)
+    for lam in (0.0, 0.5):
+        check_decode(cfg, q, k, v, lam, n_splits)
+
+
 @pytest.mark.parametrize("lam", [1e-3, 1e-2, 0.2, 0.999])
 def test_decode_temperate_mixtures(lam):
     cfg = W.temperate(W.GQA_DECODE_32K.with_(B=2, L=4096, seed=33))

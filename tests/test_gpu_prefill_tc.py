@@ -65,6 +65,21 @@ def test_prefill_tc_temperate_mixtures(lam):
     check_prefill(cfg, q, k, v, lam)
 
 
+@pytest.mark.parametrize("Hq,Hkv", [(3, 3), (8, 1)])
+@pytest.mark.parametrize("T", [1, 77, 1000])
+def test_prefill_tc_group_sizes_and_short_sequences(Hq, Hkv, T):
+    """One query head per KV head (MHA) and eight; a single key, a single
+    partial tile, and several tiles with a ragged tail; planted inputs at a
+    small threshold and temperate ones close to lambda = 1 (as many blocks
+    left out as the rule allows)."""
+    cfg = W.GQA_PREFILL_16K.with_(T=T, Hq=Hq, Hkv=Hkv, B=2, seed=55)
+    q, k, v = W.prefill_inputs(cfg)
+    check_prefill(cfg, q, k, v, 1e-6)
+    tcfg = W.temperate(cfg)
+    q, k, v = W.prefill_inputs(tcfg)
+    check_prefill(tcfg, q, k, v, 0.999)
+
+
 def test_prefill_tc_rescale_path():
     """Scores whose running max keeps rising (keys drift along the query
     direction), so the exp reference moves by more than 2^8 many times."""
