@@ -715,14 +715,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // keeps the publications in block order).  The slot's previous
           // decision (block c - NDEC) must have been read by all its readers;
           // on a timeout the abort flag is raised and every later wait fails.
+          // A skipped block's S buffer is free: every decider has read it
+          // (the vote barrier above) and nothing else will.  Released first:
+          // the next Q.K^T into this buffer waits for it.
+          if (skip) mbar_arrive(smem_u32(&sh.s_free[(c + NS) & 1][sb]));
           if (c < NDEC || mbar_wait(smem_u32(&sh.dec_read[c % NDEC]), ((c / NDEC) - 1) & 1,
                                     abort, a.err, kErrTimeout)) {
             sh.dec[c % NDEC] = skip ? 0 : 1;
             mbar_arrive(smem_u32(&sh.dec_full[c % NDEC]));
           }
-          // A skipped block's S buffer is free: every decider has read it
-          // (the vote barrier above) and nothing else will.
-          if (skip) mbar_arrive(smem_u32(&sh.s_free[(c + NS) & 1][sb]));
         }
         if (tid == 0) {
           if constexpr (SET) {
