@@ -13,7 +13,9 @@
 // 128 keys are the MMA rows and the G <= 8 query heads sharing the KV head
 // the columns (N = 16, padded):
 //   S^T = K_j Q^T   kind::f8f6f4, A = the E4M3 key tile straight from TMA,
-//                   B = the query as an exact E4M3 pair (below), 8 k-steps;
+//                   B = the query as an exact E4M3 pair (below) stacked as
+//                   32 rows (hi heads, then lo heads), 4 k-steps; the score
+//                   threads add the two parts;
 //   O^T += V_j^T P^T  kind::f16, A = the fp16 value tile (MN-major: d is the
 //                   contiguous dimension), B = P^T (fp16, heads x keys).
 // So every thread of the four score warps owns one key of the block and its G
@@ -43,7 +45,8 @@
 // three kept blocks; the value pipeline (load, widen, product) drains behind
 // them.  Seven key stages (112 KB) keep enough bytes in flight to cover the
 // load latency under a full GPU's traffic (~2.8 us measured).
-// TMEM columns: S^T buffers [0,64) (16 each), O^T [64,80).
+// TMEM columns: S^T buffers [0,128) (32 each: the hi part, then the lo part), O^T
+// [128,144).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -81,13 +84,16 @@ constexpr uint32_t SMEM_VH = SMEM_VF + NVF * F8_BYTES;
 constexpr uint32_t SMEM_Q = SMEM_VH + NVH * H_BYTES;  // Q hi, then Q lo
 constexpr uint32_t SMEM_PT = SMEM_Q + 2 * QT_BYTES;   // NPT x two 64-key boxes
 constexpr uint32_t SMEM_TILES = SMEM_PT + NPT * 2 * PT_BOX;  // 224 KB
-constexpr uint32_t TMEM_COLS = 128;
-constexpr uint32_t TMEM_O = NS * NQ;  // 64
+// An S^T buffer holds K Q_hi^T in its first NQ columns and K Q_lo^T in the
+// next NQ: one N = 2 NQ product per k-step instead of one per part.
+constexpr int NSC = 2 * NQ;
+constexpr uint32_t TMEM_COLS = 256;
+constexpr uint32_t TMEM_O = NS * NSC;  // 128
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // exp reference may lag the max by 2^8
 // S^T: E4M3 x E4M3, both K-major.  O^T: fp16, A (V^T) MN-major, B (P^T) K-major.
-constexpr uint32_t IDESC_QK = idesc_e4m3_f32(BC, NQ);
+constexpr uint32_t IDESC_QK = idesc_e4m3_f32(BC, NSC);
 constexpr uint32_t IDESC_PV = idesc_f16_f32(D, NQ, 0) | (1u << 15);
 static_assert(TMEM_O + NQ <= TMEM_COLS, "TMEM budget");
 static_assert(NS % 2 == 0, "block pairs read two adjacent S^T buffers");
@@ -414,7 +420,9 @@ __global__ void __launch_bounds__(NT, 1)
   } else if (warp == WARP_QK) {
     // --------------------------------------------------------- S^T issuer --
     if (lane == 0) {
-      const uint64_t qhi = kmajor_base(base + SMEM_Q), qlo = kmajor_base(base + SMEM_Q + QT_BYTES);
+      // The query pair as one 32-row operand: hi in rows 0-15, lo in rows 16-31
+      // (the two 2 KB tiles are adjacent, 8-row groups 1 KB apart).
+      const uint64_t qd = kmajor_base(base + SMEM_Q);
       for (int j = 0; j < nb; ++j) {
         const int f = j % NKF, sb = j % NS;
         if (!mbar_wait(smem_u32(&sh.kf_full[f]), (j / NKF) & 1, abort, a.err, kErrTimeout))
@@ -425,11 +433,12 @@ __global__ void __launch_bounds__(NT, 1)
           break;
         fence_after_sync();
         const uint64_t kd = kmajor_base(base + SMEM_KF + f * F8_BYTES);
-        // S^T = K (hi)^T + K (lo)^T: four k-steps of 32 codes for each part.
+        // [K hi^T | K lo^T]: four k-steps of 32 codes; the score threads add
+        // the two parts.
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_f8f6f4_ss(tmem + sb * NQ, kd + ((uint64_t)(kk & 3) * 2),
-                        (kk < 4 ? qhi : qlo) + ((uint64_t)(kk & 3) * 2), IDESC_QK, kk > 0);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f8f6f4_ss(tmem + sb * NSC, kd + ((uint64_t)kk * 2), qd + ((uint64_t)kk * 2),
+                        IDESC_QK, kk > 0);
         mma_commit(smem_u32(&sh.s_full[sb]));
         mma_commit(smem_u32(&sh.kf_empty[f]));
       }
@@ -568,9 +577,11 @@ __global__ void __launch_bounds__(NT, 1)
         break;
       }
       fence_after_sync();
-      uint32_t x[32];
-      tmem_ld32(lane_base + sb * NQ, x);  // block j in columns [0,16), j + 1 in [16,32)
+      uint32_t x[32], y[32];
+      tmem_ld32(lane_base + sb * NSC, x);        // block j: hi part [0,16), lo part [16,32)
+      tmem_ld32(lane_base + (sb + 1) * NSC, y);  // block j + 1 (unused when there is none)
       tmem_wait_ld_regs(x);
+      tmem_wait_ld_regs(y);
       fence_before_sync();  // the scores are in registers: the S^T buffers are free
       __syncwarp();
       if (lane == 0) {
@@ -582,8 +593,8 @@ __global__ void __launch_bounds__(NT, 1)
       float s0[G], s1[G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        s0[g] = v0 ? __uint_as_float(x[g]) * sl2[g] : -INFINITY;
-        s1[g] = v1 ? __uint_as_float(x[16 + g]) * sl2[g] : -INFINITY;
+        s0[g] = v0 ? (__uint_as_float(x[g]) + __uint_as_float(x[16 + g])) * sl2[g] : -INFINITY;
+        s1[g] = v1 ? (__uint_as_float(y[g]) + __uint_as_float(y[16 + g])) * sl2[g] : -INFINITY;
         const float m0 = warp_max(s0[g]), m1 = warp_max(s1[g]);
         if (lane == 0) {
           sh.red[q & 1][warp][g] = m0;
