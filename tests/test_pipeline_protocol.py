@@ -81,8 +81,8 @@ def simulate(nblk, keep, rescale, seed, NK=4, NV=2, NS=3, NDEC=4, split_free=Tru
     sbuf = [None] * NS      # block whose scores / P an S buffer holds
     dec = [None] * NDEC
     pv_done_count = [0]
-    pipe = []               # in-order tensor pipe: (label, callbacks on completion)
-    tma = []                # TMA loads in flight: (callback)
+    pipe = []               # in-order tensor pipe: completion callbacks of issued products
+    tma = []                # TMA loads in flight: their landing callbacks
 
     def wait(name, phase):
         b = B[name]
