@@ -361,6 +361,65 @@ def decode_inputs_fp8(cfg: DecodeConfig, pow2_scales: bool = True):
 GQA_DECODE_FP8_32K = GQA_DECODE_32K.with_(name="gqa_decode_fp8_B16_L32768", seed=1241)
 
 
+# Magnitudes of the E2M1 (FP4) codes 0..7; bit 3 is the sign.
+E2M1_GRID = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def _e2m1_codes(y: torch.Tensor) -> torch.Tensor:
+    """E2M1 codes of y (saturating at 6), rounded to nearest, ties to the even
+    code (mantissa bit 0)."""
+    grid = torch.tensor(E2M1_GRID, dtype=torch.float32)
+    a = y.abs().clamp(max=6.0).contiguous()
+    lo = (torch.searchsorted(grid, a, right=True) - 1).clamp(0, 7)
+    hi = (lo + 1).clamp(max=7)
+    dlo, dhi = a - grid[lo], grid[hi] - a
+    up = (hi != lo) & ((dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0)))
+    idx = torch.where(up, hi, lo)
+    sign = ((y < 0) & (idx > 0)).to(torch.int64) << 3
+    return (idx | sign).to(torch.uint8)
+
+
+def decode_inputs_nvfp4(cfg: DecodeConfig):
+    """The decode draws with an NVFP4 key/value cache: returns ``(q, k4, v4,
+    k_bs, v_bs, k_scale, v_scale)`` with q bf16 ``[B, Hq, dk]``; k4, v4 uint8
+    ``[B, Hkv, L, d/2]`` holding two E2M1 codes per byte (element 2i in the
+    low nibble); k_bs, v_bs uint8 E4M3 codes ``[B, Hkv, L, d/16]``, one scale
+    per 16 consecutive elements of a row; k_scale, v_scale fp32 ``[B, Hkv]``.
+    A row element is ``scale * E4M3(block scale) * E2M1(code)``.  Each
+    (sequence, KV head) slice of the bf16 draws gets scale = amax / (6 * 448),
+    each 16-element block the E4M3 code of (its amax / 6) / scale rounded up
+    (no element exceeds the E2M1 range), each element the E2M1 code of
+    x / (block scale * scale)."""
+    q, k, v = decode_inputs(cfg)
+
+    def quant(x):
+        xf = x.float()
+        B_, H_, L_, d_ = xf.shape
+        blk = xf.reshape(B_, H_, L_, d_ // 16, 16)
+        sc = (xf.abs().amax(dim=(2, 3)).clamp_min(1e-30) / (6.0 * 448.0))[:, :, None, None]
+        want = (blk.abs().amax(-1) / 6.0) / sc  # in [0, 448]
+        code = want.to(torch.float8_e4m3fn).view(torch.uint8)
+        # rounded up to the next E4M3 value, so that no element exceeds 6
+        up = code.view(torch.float8_e4m3fn).float() < want
+        code = torch.where(up, (code + 1).clamp(max=0x7E), code)
+        bs8 = code.view(torch.float8_e4m3fn)
+        den = (bs8.float() * sc)[..., None]
+        y = torch.where(den > 0, blk / den.clamp_min(1e-38), torch.zeros_like(blk))
+        codes = _e2m1_codes(y).reshape(B_, H_, L_, d_)
+        packed = codes[..., 0::2] | (codes[..., 1::2] << 4)
+        return (packed.contiguous(), bs8.view(torch.uint8).contiguous(),
+                sc[:, :, 0, 0].contiguous())
+
+    k4, kbs, ks = quant(k)
+    v4, vbs, vs = quant(v)
+    return q, k4, v4, kbs, vbs, ks, vs
+
+
+# The GQA decode shape with an NVFP4 key/value cache (E2M1 codes, one E4M3
+# scale per 16 elements, one fp32 scale per (sequence, KV head)).
+GQA_DECODE_NVFP4_32K = GQA_DECODE_32K.with_(name="gqa_decode_nvfp4_B16_L32768", seed=1243)
+
+
 def santa_offsets(cfg: DecodeConfig, n_samples: int, mode: str, seed: int = 0) -> torch.Tensor:
     """Uniform draws in [0, 1) for the sampled decode (fp32, one generator per
     (sequence, query head)): ``[B, Hq]`` for the systematic sampler (one

@@ -27,6 +27,13 @@ Parity status of each function (what pins it, in ``tests/test_oracle.py``):
   ``fp8_query`` returns a bf16 row unchanged when no element is below 2^-9 of
   the row's largest, never moves an element by more than 2^-10 / sigma, and
   picks the largest sigma with max|q| sigma <= 256.
+* ``decode_nvfp4`` / ``nvfp4_rows`` / ``e2m1_decode``: the E2M1 decoding
+  equals the FP4 value table of the OCP Microscaling formats specification
+  over all 16 codes; rows dequantised from the seeded generator lie within
+  half an E2M1 step of the drawn values (which pins the nibble order and the
+  block-scale indexing against the generator's independent packing); at
+  lambda = 0 and with thresholds the output equals brute-force fp64 attention
+  over rows decoded from that table, with non-power-of-two scales.
 * ``prefill_varlen``: each packed sequence at lambda = 0 equals torch's fp64
   SDPA on that sequence alone; with thresholds, each sequence's output is the
   softmax over its own kept tokens, a larger lambda skips a superset of
@@ -280,6 +287,71 @@ def decode_fp8(q, k8, v8, k_scale, v_scale, scale, lam, Bc, n_splits, units=None
     v8 = torch.as_tensor(np.ascontiguousarray(v8, dtype=np.uint8))
     kf = k8.view(torch.float8_e4m3fn).float().numpy()
     vf = v8.view(torch.float8_e4m3fn).float().numpy()
+    _, Hkv, L, _ = kf.shape
+    dv = vf.shape[3]
+    ks = np.asarray(k_scale, dtype=np.float32).reshape(B, Hkv)
+    vs = np.asarray(v_scale, dtype=np.float32).reshape(B, Hkv)
+    G = Hq // Hkv
+    n_b = -(-L // Bc)
+    bps = -(-n_b // n_splits)
+    o_part = np.zeros((B, Hq, n_splits, dv))
+    lse_part = np.full((B, Hq, n_splits), np.nan)
+    skip = np.zeros((B, Hkv, n_splits, bps), dtype=np.uint8)
+    margin = np.full((B, Hkv, n_splits, bps), np.nan)
+    want = None if units is None else set(int(x) // n_splits for x in np.asarray(units).ravel())
+    for b in range(B):
+        for h in range(Hkv):
+            if want is not None and (b * Hkv + h) not in want:
+                continue
+            fs = None if force_skip is None else np.asarray(force_skip)[b:b + 1, h:h + 1]
+            r = decode(q[b:b + 1, h * G:(h + 1) * G], kf[b:b + 1, h:h + 1], vf[b:b + 1, h:h + 1],
+                       float(scale) * float(ks[b, h]), lam, Bc, n_splits, force_skip=fs)
+            o_part[b, h * G:(h + 1) * G] = r["o_part"][0] * float(vs[b, h])
+            lse_part[b, h * G:(h + 1) * G] = r["lse_part"][0]
+            skip[b, h] = r["skip"][0, 0]
+            margin[b, h] = r["margin"][0, 0]
+    return {"o_part": o_part, "lse_part": lse_part, "skip": skip, "margin": margin}
+
+
+def e2m1_decode(codes):
+    """Values of E2M1 (FP4) codes: bit 3 the sign, bits 2-1 the exponent (bias
+    1), bit 0 the mantissa; exponent 0 is subnormal (0 or 0.5)."""
+    c = np.asarray(codes).astype(np.int64)
+    sgn = np.where(c & 8, -1.0, 1.0)
+    e, m = (c >> 1) & 3, c & 1
+    mag = np.where(e == 0, 0.5 * m, np.exp2(e - 1.0) * (1.0 + 0.5 * m))
+    return sgn * mag
+
+
+def nvfp4_rows(x4, bs8):
+    """Rows of an NVFP4 cache without its per-(sequence, head) scale: the two
+    E2M1 codes of each byte of ``x4`` [..., d/2] (element 2i in the low
+    nibble) times the E4M3 scale ``bs8`` [..., d/16] of their 16-element
+    block; exact in fp32 (two by four significant bits)."""
+    import torch
+    x4 = np.ascontiguousarray(x4, dtype=np.uint8)
+    codes = np.empty(x4.shape[:-1] + (2 * x4.shape[-1],), dtype=np.uint8)
+    codes[..., 0::2] = x4 & 0xF
+    codes[..., 1::2] = x4 >> 4
+    bs = torch.as_tensor(np.ascontiguousarray(bs8, dtype=np.uint8)).view(
+        torch.float8_e4m3fn).double().numpy()
+    return (e2m1_decode(codes) * np.repeat(bs, 16, axis=-1)).astype(np.float32)
+
+
+def decode_nvfp4(q, k4, v4, k_bs, v_bs, k_scale, v_scale, scale, lam, Bc, n_splits,
+                 units=None, force_skip=None):
+    """Split-KV thresholded decode over an NVFP4 key/value cache, fp64.
+
+    Reading (the pages name NVFP4 models but define no cache format): a row
+    element is ``s * E4M3(block scale) * E2M1(code)`` with one fp32 ``s`` per
+    (sequence, KV head) and one E4M3 block scale per 16 consecutive elements
+    (:func:`nvfp4_rows`).  As for the FP8 cache, the key scale ``s`` is folded
+    into the score scale and the value scale multiplies the split outputs; the
+    query is used as given (bf16).  Each (b, h) slice then runs
+    :func:`decode`.  ``units`` / ``force_skip`` as for :func:`decode`."""
+    q = _f32(q)
+    B, Hq, dk = q.shape
+    kf, vf = nvfp4_rows(k4, k_bs), nvfp4_rows(v4, v_bs)
     _, Hkv, L, _ = kf.shape
     dv = vf.shape[3]
     ks = np.asarray(k_scale, dtype=np.float32).reshape(B, Hkv)
