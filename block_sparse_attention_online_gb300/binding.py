@@ -18,7 +18,7 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build",
                          "libattn_skip.so")
 _lib = None
 
-ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT = range(5)
+ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT, ATTN_EINTERNAL = range(6)
 ATTN_BF16, ATTN_F32 = 0, 1
 
 #: Every symbol include/attn_skip.h declares.
@@ -470,6 +470,11 @@ def attn_skip_santa_decode(q, k, v, n_samples, mode, u, n_tiles=16, scale=0.0,
     return (o, idx) if with_idx else o
 
 
+# Sizes of the library's built-in sampled-decode scratch, in floats.
+NOALLOC_SCORE_FLOATS = 4 << 20
+NOALLOC_STAT_FLOATS = 64 << 10
+
+
 def attn_skip_santa_decode_noalloc(q, k, v, n_samples, mode, u, o, idx=None, n_tiles=16,
                                    scale=0.0, stream=None):
     """attn_skip_santa_decode with both workspaces in the library's own
@@ -492,10 +497,12 @@ def attn_skip_santa_decode_noalloc(q, k, v, n_samples, mode, u, o, idx=None, n_t
         _ptr(q), _ptr(k), _ptr(v), _dtype_code(q), B, Hq, Hkv, L, dk, dv, kstride, vstride,
         float(scale), int(n_samples), SANTA_MODES[mode], _ptr(u), int(n_tiles), _dtype_code(o),
         _ptr(o), None if idx is None else _ptr(idx), _stream(stream, q.device))
-    if st == ATTN_EINVAL:
+    over = (B * Hq * (-(-L // 128)) * 128 > NOALLOC_SCORE_FLOATS
+            or B * Hq * int(n_tiles) * 2 > NOALLOC_STAT_FLOATS)
+    if st == ATTN_EINVAL and over:
         raise AttnSkipError("attn_skip_santa_decode_noalloc (the built-in scratch holds "
-                            "B*Hq*ceil(L/128)*128 <= 4194304 score floats and "
-                            "B*Hq*n_tiles*2 <= 65536 statistics floats)", st)
+                            f"B*Hq*ceil(L/128)*128 <= {NOALLOC_SCORE_FLOATS} score floats and "
+                            f"B*Hq*n_tiles*2 <= {NOALLOC_STAT_FLOATS} statistics floats)", st)
     _check("attn_skip_santa_decode_noalloc", st)
     return o
 

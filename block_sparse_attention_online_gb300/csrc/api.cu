@@ -14,21 +14,15 @@ namespace {
 // One error word per device (a kernel that gives up a bounded wait ORs a bit in).
 __device__ unsigned g_error_word;
 
-constexpr int kMaxDevices = 64;
-unsigned *g_err_ptr[kMaxDevices];
-
+// Device address of g_error_word in the context current on this thread,
+// looked up on every call (a host-side table read once the module is loaded):
+// a cached address would go stale after cudaDeviceReset or when another
+// context is made current on the same device.
 cudaError_t error_word(unsigned **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void *p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_error_word);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!g_err_ptr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_error_word);
-    if (e != cudaSuccess) return e;
-    g_err_ptr[dev] = (unsigned *)p;
-  }
-  *out = g_err_ptr[dev];
+  *out = (unsigned *)p;
   return cudaSuccess;
 }
 
@@ -379,6 +373,7 @@ extern "C" attn_status attn_skip_last_device_error(void *stream) {
     if (e != cudaSuccess) return from_cuda(e);
     return (word & kErrTimeout)  ? ATTN_ETIMEOUT
            : (word & kErrBadArg) ? ATTN_EINVAL
+           : (word & kErrLayout) ? ATTN_EINTERNAL
                                  : ATTN_ECUDA;
   }
   return ATTN_OK;
@@ -474,6 +469,7 @@ extern "C" const char *attn_skip_status_string(attn_status s) {
     case ATTN_EUNSUPPORTED: return "unsupported combination (no kernel built for it)";
     case ATTN_ECUDA: return "CUDA error";
     case ATTN_ETIMEOUT: return "device-side bounded wait timed out";
+    case ATTN_EINTERNAL: return "kernel shared-memory layout misaligned (internal error)";
   }
   return "unknown status";
 }

@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t base = smem_u32(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (base & 1023u) {  // the swizzled layouts need a 1024-byte aligned base
-    if (tid == 0) atomicOr(a.err, kErrTimeout);
+    if (tid == 0) atomicOr(a.err, kErrLayout);
     return;
   }
   const int G = a.Hq / a.Hkv;

@@ -10,6 +10,7 @@ namespace attn_skip {
 enum : unsigned {
   kErrTimeout = 1u,  // a bounded mbarrier / flag wait gave up
   kErrBadArg = 2u,   // a device-side argument (a varlen length or threshold) was out of range
+  kErrLayout = 4u,   // the dynamic shared-memory base was not 1024-byte aligned
 };
 
 struct PrefillArgs {

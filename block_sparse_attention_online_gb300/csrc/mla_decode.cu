@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t base = smem_u32(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (base & 1023u) {
-    if (tid == 0) atomicOr(a.err, kErrTimeout);
+    if (tid == 0) atomicOr(a.err, kErrLayout);
     return;
   }
   const int half = blockIdx.x & 1;

@@ -12,12 +12,15 @@
 //
 // The array is a file-scope __device__ variable: every GPU on which the
 // library is loaded holds it (16.25 MiB) until the process exits.  In host
-// code its name is only a host-side stand-in, never a device address, so the
-// device address is looked up once per device with cudaGetSymbolAddress and
-// passed to the kernels.
+// code its name is only a host-side stand-in, never a device address, so each
+// call looks up the device address with cudaGetSymbolAddress, for the context
+// current on the calling thread, and passes it to the kernels.  The look-up is
+// a host-side table read once the library's device code is loaded in that
+// context; the first call in a context may load it.  No address is cached
+// across calls: after cudaDeviceReset, or with another context made current
+// on the same device, the array lives at a new address (or in another module
+// instance), and a cached one would point at memory that is gone.
 #include <cuda_runtime.h>
-
-#include <atomic>
 
 #include "attn_skip.h"
 
@@ -25,27 +28,14 @@ namespace {
 
 constexpr size_t kScoreFloats = size_t(4) << 20;  // score stash: 4,194,304 floats
 constexpr size_t kStatFloats = size_t(64) << 10;  // tile statistics: 65,536 floats
-constexpr int kMaxDevices = 64;
-
 static __device__ __align__(256) float g_santa_scratch[kScoreFloats + kStatFloats];
 
-// Device address of g_santa_scratch on each device, looked up on first use.
-std::atomic<float *> g_scratch_addr[kMaxDevices];
-
+// Device address of g_santa_scratch in the context current on this thread.
 cudaError_t scratch_address(float **out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void *sym = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&sym, g_santa_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  float *p = g_scratch_addr[dev].load(std::memory_order_acquire);
-  if (!p) {
-    void *sym = nullptr;
-    e = cudaGetSymbolAddress(&sym, g_santa_scratch);  // device `dev` is current here
-    if (e != cudaSuccess) return e;
-    p = static_cast<float *>(sym);
-    g_scratch_addr[dev].store(p, std::memory_order_release);
-  }
-  *out = p;
+  *out = static_cast<float *>(sym);
   return cudaSuccess;
 }
 

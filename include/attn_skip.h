@@ -36,7 +36,9 @@
  * multiple of Hkv, lambda outside [0,1) or NaN, or a misaligned pointer;
  * ATTN_EUNSUPPORTED for a valid combination this build has no kernel for;
  * ATTN_ECUDA for a launch or CUDA runtime error (the CUDA error is cleared);
- * ATTN_ETIMEOUT when a device-side bounded wait gave up (reported by
+ * ATTN_ETIMEOUT when a device-side bounded wait gave up, ATTN_EINTERNAL when a
+ * kernel found its dynamic shared memory placed off the 1024-byte boundary its
+ * swizzled tiles need and returned without work (both reported by
  * attn_skip_last_device_error).
  */
 #ifndef ATTN_SKIP_H
@@ -54,7 +56,8 @@ typedef enum {
   ATTN_EINVAL = 1,
   ATTN_EUNSUPPORTED = 2,
   ATTN_ECUDA = 3,
-  ATTN_ETIMEOUT = 4
+  ATTN_ETIMEOUT = 4,
+  ATTN_EINTERNAL = 5
 } attn_status;
 
 typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
@@ -390,10 +393,12 @@ attn_status attn_skip_santa_decode(const void *q, const void *k, const void *v, 
  * returns ATTN_EINVAL before any CUDA call.  The other checks are those of
  * attn_skip_santa_decode.
  *
- * Set-up: the first call on a device (the device current on the calling
- * thread; `stream` must belong to it) looks up the array's device address
- * with cudaGetSymbolAddress, which can load the library's device code; make
- * that first call before any stream capture.  ATTN_ECUDA if the look-up
+ * Set-up: every call looks up the array's device address with
+ * cudaGetSymbolAddress in the context current on the calling thread (`stream`
+ * must belong to its device); no address is kept between calls, so a
+ * cudaDeviceReset or another context on the same device is followed
+ * correctly.  The first call in a context can load the library's device code;
+ * make that first call before any stream capture.  ATTN_ECUDA if the look-up
  * fails.
  *
  * Sharing: every call on a device uses the same array, which keeps the last
@@ -424,7 +429,8 @@ attn_status attn_skip_selftest_wait_timeout(void *stream);
  * Synchronises `stream`, then reads and clears the current device's error
  * word: ATTN_ETIMEOUT if a kernel gave up a bounded wait since the last read,
  * ATTN_EINVAL if a kernel found a device-side argument out of range (the
- * varlen lengths and thresholds), ATTN_ECUDA on a CUDA error, else ATTN_OK.
+ * varlen lengths and thresholds), ATTN_EINTERNAL if a kernel found its shared
+ * memory misaligned, ATTN_ECUDA on a CUDA error, else ATTN_OK.
  */
 attn_status attn_skip_last_device_error(void *stream);
 

@@ -68,14 +68,24 @@ def test_noalloc_matches_the_workspace_entry_point_on_calls_in_a_row():
         del q, k, v, u, o, idx
     torch.cuda.synchronize()
 
+    calls = 0
     for name, (cfg, S, mode, n_tiles, seed) in (("a", case_a), ("b", case_b), ("a", case_a)):
         q, k, v, u = _inputs(cfg, S, mode, seed)
+        torch.cuda.synchronize()
         o = torch.full((cfg.B, cfg.Hq, 128), float("nan"), device="cuda")
         idx = torch.full((cfg.B, cfg.Hq, S), -1, dtype=torch.int32, device="cuda")
         before = torch.cuda.memory_allocated()
+        free_before = torch.cuda.mem_get_info()[0]
         bs.attn_skip_santa_decode_noalloc(q, k, v, S, mode, u, o, idx, n_tiles=n_tiles)
         bs.attn_skip_last_device_error()
+        # torch's counter sees its own caching allocator; the driver's free
+        # bytes also see a cudaMalloc made inside the library.  The first call
+        # may load the library's device code (the scratch array included), so
+        # the driver figure is compared from the second call on.
         assert torch.cuda.memory_allocated() == before
+        if calls:
+            assert torch.cuda.mem_get_info()[0] == free_before
+        calls += 1
         o_ref, idx_ref, vmax = want[name]
         assert torch.equal(idx.cpu(), idx_ref)
         err = (o.cpu().double() - o_ref.double()).abs().max().item()
@@ -90,3 +100,9 @@ def test_noalloc_binding_reports_the_limit():
     o = torch.empty(cfg.B, cfg.Hq, 128, device="cuda")
     with pytest.raises(bs.AttnSkipError, match="scratch"):
         bs.attn_skip_santa_decode_noalloc(q, k, v, 32, "sys", u, o, n_tiles=4200)
+    # within the limits, an invalid argument of the sampled decode itself is
+    # not reported as the scratch limit
+    k3 = torch.zeros(cfg.B, 3, cfg.L, 128, dtype=k.dtype, device="cuda")  # 8 % 3 != 0
+    with pytest.raises(bs.AttnSkipError) as e:
+        bs.attn_skip_santa_decode_noalloc(q, k3, k3, 32, "sys", u, o, n_tiles=4)
+    assert e.value.status == bs.ATTN_EINVAL and "scratch" not in str(e.value)
