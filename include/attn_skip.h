@@ -230,8 +230,13 @@ attn_status attn_skip_decode_per_head(const void *q, const void *k, const void *
  * format; halving the cache bytes halves the time of this bandwidth-bound
  * loop.
  *
- *  q          [B, Hq, dk] bf16 (device); widened to fp16 for the products,
- *             exact for |q| < 65504 (larger values overflow)
+ *  q          [B, Hq, dk] bf16 (device).  The products are E4M3 x E4M3, so
+ *             each query head enters as the pair hi + lo of E4M3 values of
+ *             q * 2^e (2^e the largest power of two with max|q| 2^e <= 256),
+ *             both rounded to nearest even: exact for every element within
+ *             about 2^-10 of the head's largest, and otherwise off by at most
+ *             2^-10 / 2^e, which moves a score by at most
+ *             scale * k_scale * 2^-10 / 2^e * sum_d |E4M3(k_d)|
  *  k, v       [B, Hkv, L, d] uint8 E4M3 codes (device), row strides in bytes
  *             (multiples of 16); no NaN codes
  *  k_scale, v_scale [B, Hkv] fp32 (device)

@@ -21,12 +21,10 @@ Parity status of each function (what pins it, in ``tests/test_oracle.py``):
 * ``combine``: lambda = 0 merged decode equals dense single-pass attention;
   one split is the identity.
 * ``decode_fp8``: the E4M3 decoding it relies on equals an independent
-  bit-level decoder over all 256 codes; at lambda = 0 the merged output equals
-  a brute-force fp64 softmax over the scaled decoded rows (key scale in the
-  scores, value scale on the output), for scales that are not powers of two.
-  ``fp8_query`` returns a bf16 row unchanged when no element is below 2^-9 of
-  the row's largest, never moves an element by more than 2^-10 / sigma, and
-  picks the largest sigma with max|q| sigma <= 256.
+  bit-level decoder over all 256 codes; at lambda = 0 and with thresholds the
+  merged output equals a brute-force fp64 softmax of the given query against
+  the scaled decoded rows (key scale in the scores, value scale on the
+  output), for scales that are not powers of two.
 * ``decode_nvfp4`` / ``nvfp4_rows`` / ``e2m1_decode``: the E2M1 decoding
   equals the FP4 value table of the OCP Microscaling formats specification
   over all 16 codes; rows dequantised from the seeded generator lie within
@@ -243,29 +241,6 @@ def decode(q, k, v, scale, lam, Bc, n_splits, dv=None, units=None, force_skip=No
     return {"o_part": o_part, "lse_part": lse_part, "skip": skip, "margin": margin}
 
 
-def fp8_query(q):
-    """The query an E4M3 key cache is multiplied with: per query head, the
-    row times sigma = 2^e, the largest power of two with max|q| * sigma <=
-    256, is written as the sum of an E4M3 value and an E4M3 remainder
-    (round to nearest even each), and divided by sigma again:
-    q_eff = (hi + lo) / sigma.  For a bf16 row this is the row itself, except
-    for elements whose remainder falls below the E4M3 normal range (smaller
-    than about 2^-10 of the row's largest), which move by at most
-    2^-10 / sigma.  Returns ``(q_eff, e)`` (fp32 [..., dk], int [...])."""
-    import torch
-    qf = _f32(q).astype(np.float64)
-    amax = np.abs(qf).max(axis=-1)
-    frac, ex = np.frexp(np.where(amax > 0, amax, 1.0))  # amax = frac * 2^ex, frac in [0.5, 1)
-    e = 8 - np.where(frac == 0.5, ex - 1, ex)           # 8 - ceil(log2(amax))
-    e = np.where(amax > 0, e, 0).astype(np.int64)
-    x = qf * np.exp2(e)[..., None]                      # exact
-    def e4m3(y):
-        return torch.from_numpy(y.astype(np.float32)).to(torch.float8_e4m3fn).double().numpy()
-    hi = e4m3(x)
-    lo = e4m3(x - hi)
-    return ((hi + lo) * np.exp2(-e)[..., None]).astype(np.float32), e
-
-
 def decode_fp8(q, k8, v8, k_scale, v_scale, scale, lam, Bc, n_splits, units=None,
                force_skip=None):
     """Split-KV thresholded decode over an FP8 (E4M3) key/value cache, fp64.
@@ -276,12 +251,12 @@ def decode_fp8(q, k8, v8, k_scale, v_scale, scale, lam, Bc, n_splits, units=None
     ``k_scale[b,h] * decode(k8)`` and ``v_scale[b,h] * decode(v8)``.  The
     scale of a key row multiplies its scores, so it is folded into the score
     scale (``scale * k_scale``, exact in double); the value scale multiplies
-    the split outputs.  The query is the one :func:`fp8_query` gives (the
-    scores of an E4M3 cache are products of E4M3 values).  Each (b, h) slice
+    the split outputs.  The query is used as given (bf16, widened exactly):
+    the dequantised cache rows meet the caller's query.  Each (b, h) slice
     then runs :func:`decode` on the decoded codes, which are exact in fp32.
     ``units`` / ``force_skip`` as for :func:`decode`.  Returns the same dict."""
     import torch
-    q = fp8_query(q)[0]
+    q = _f32(q)
     B, Hq, dk = q.shape
     k8 = torch.as_tensor(np.ascontiguousarray(k8, dtype=np.uint8))
     v8 = torch.as_tensor(np.ascontiguousarray(v8, dtype=np.uint8))

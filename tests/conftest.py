@@ -21,3 +21,25 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print the skip-bit flips of every GPU/oracle bitmap comparison: blocks
+    whose bit differs, out of the blocks whose oracle statistic lies in the
+    margin band around ln(lambda), out of the traversed blocks."""
+    try:
+        from tests.parity import FLIP_LOG
+    except Exception:
+        return
+    if not FLIP_LOG:
+        return
+    tr = terminalreporter
+    tr.section("skip-bit flips inside the margin band")
+    flips = sum(f for _, f, _, _ in FLIP_LOG)
+    near = sum(n for _, _, n, _ in FLIP_LOG)
+    trav = sum(t for _, _, _, t in FLIP_LOG)
+    tr.write_line(f"{len(FLIP_LOG)} comparisons: {flips} flips, {near} blocks in the band, "
+                  f"{trav} traversed blocks")
+    for label, f, n, t in FLIP_LOG:
+        if f or n:
+            tr.write_line(f"  {label}: {f} flips / {n} in band / {t} traversed")

@@ -20,20 +20,72 @@ TOL = {
 }
 
 
+# Every compare_bits call appends (label, flips, blocks in the band, traversed
+# blocks); the session's terminal summary prints them (tests/conftest.py).
+FLIP_LOG = []
+
+
 def compare_bits(gpu_skip: np.ndarray, ora_skip: np.ndarray, ora_margin: np.ndarray,
-                 lam: float):
-    """gpu_skip/ora_skip/ora_margin share a shape; returns (n_bad, flips_mask)."""
+                 lam: float, extra_band=0.0, label: str = ""):
+    """gpu_skip/ora_skip/ora_margin share a shape; returns (n_bad, flips_mask).
+
+    A traversed block is in the band when its oracle statistic lies within
+    MARGIN_BAND + ``extra_band`` of ln(lambda) (``extra_band`` a scalar or an
+    array of the same shape, for a kernel whose scores differ from the
+    oracle's by a derived amount); only there may the bits differ.  Flips are
+    counted, checked against the number of blocks in the band, and logged."""
     gpu_skip = gpu_skip.astype(bool)
     ora = ora_skip.astype(bool)
     trav = np.isfinite(ora_margin)
     ln_lam = math.log(lam) if lam > 0 else -math.inf
     if math.isfinite(ln_lam):
-        near = trav & (np.abs(np.nan_to_num(ora_margin, nan=0.0) - ln_lam) < MARGIN_BAND)
+        band = MARGIN_BAND + np.asarray(extra_band, dtype=np.float64)
+        near = trav & (np.abs(np.nan_to_num(ora_margin, nan=0.0) - ln_lam) < band)
     else:
         near = np.zeros_like(trav)
     diff = gpu_skip != ora
     bad = (diff & ~near) | (gpu_skip & ~trav)
-    return int(bad.sum()), diff & near
+    flips = diff & near
+    assert flips.sum() <= near.sum()
+    FLIP_LOG.append((label or f"lambda={lam:.6g}", int(flips.sum()), int(near.sum()),
+                     int(trav.sum())))
+    return int(bad.sum()), flips
+
+
+def fp8_query_pair_band(q, k8, k_scale, scale: float, Bc: int, n_splits: int, G: int):
+    """Extra bit band of the E4M3-cache decode kernel, per (b, KV head, split).
+
+    The kernel multiplies the E4M3 key codes with the query written as the
+    exact pair hi + lo of E4M3 values after a per-head power-of-two scale
+    sigma = 2^e, the largest with max|q| sigma <= 256 (an E4M3 x E4M3 product
+    needs both operands in E4M3).  For a bf16 element x = q sigma the remainder
+    x - hi has at most four significant bits, so lo is exact unless it falls
+    below E4M3's subnormal step 2^-9, where rounding moves x by at most 2^-10:
+    each query element moves by at most 2^-10 / sigma.  A score of key c then
+    moves by at most eps_c = scale * k_scale * 2^-10 / sigma * sum_d |code_cd|
+    (code values decoded from E4M3), and a block statistic max_r(rowmax_r -
+    m_new_r) by at most twice the largest eps over the split's keys and the
+    group's heads.  Returns that bound, shape [B, Hkv, n_splits, 1]."""
+    import torch
+    qf = q.detach().to("cpu", torch.float64).numpy()
+    B, Hq, _ = qf.shape
+    amax = np.abs(qf).max(axis=-1)
+    frac, ex = np.frexp(np.where(amax > 0, amax, 1.0))
+    e = np.where(amax > 0, 8 - np.where(frac == 0.5, ex - 1, ex), 0)
+    qstep = (2.0 ** -10) * np.exp2(-e.astype(np.float64))          # [B, Hq]
+    Hkv = Hq // G
+    qstep = qstep.reshape(B, Hkv, G).max(axis=-1)                   # [B, Hkv]
+    kd = torch.as_tensor(np.ascontiguousarray(k8, dtype=np.uint8)).view(
+        torch.float8_e4m3fn).double().abs().sum(-1).numpy()          # [B, Hkv, L]
+    L = kd.shape[-1]
+    n_b = -(-L // Bc)
+    out = np.zeros((B, Hkv, n_splits, 1))
+    for s in range(n_splits):
+        b0, b1 = (s * n_b) // n_splits, ((s + 1) * n_b) // n_splits
+        if b1 > b0:
+            seg = kd[:, :, b0 * Bc:min(b1 * Bc, L)].max(axis=-1)
+            out[:, :, s, 0] = 2.0 * scale * np.asarray(k_scale, dtype=np.float64) * qstep * seg
+    return out
 
 
 def rel_l2(a, b):

@@ -1,6 +1,7 @@
 """Split-KV decode over an FP8 (E4M3) key/value cache on the GPU against the
-fp64 oracle (bits exact outside the margin band, partials within the bf16
-tolerances), and the merged output."""
+fp64 oracle, which takes the query as given (bits exact outside the margin
+band widened by the kernel's derived query-pair bound, partials and merged
+output within the bf16 tolerances)."""
 import json
 import os
 
@@ -11,7 +12,7 @@ import torch
 import oracle
 from block_sparse_attention_online_gb300 import binding as bs
 from block_sparse_attention_online_gb300 import workloads as W
-from tests.parity import check_outputs, compare_bits
+from tests.parity import check_outputs, compare_bits, fp8_query_pair_band
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -37,7 +38,10 @@ def check_fp8(cfg, q, k8, v8, ks, vs, lam, n_splits, units=None):
         sel[:] = False
         for u in np.asarray(units).ravel():
             sel.reshape(-1)[int(u) // n_splits] = True
-    n_bad, flips = compare_bits(skip[sel], r["skip"][sel], r["margin"][sel], lam)
+    band = np.broadcast_to(fp8_query_pair_band(q, k8.numpy(), ks.numpy(), cfg.scale, cfg.Bc,
+                                               n_splits, cfg.G), skip.shape)
+    n_bad, flips = compare_bits(skip[sel], r["skip"][sel], r["margin"][sel], lam,
+                                extra_band=band[sel], label=f"fp8 decode L={cfg.L} lambda={lam:.4g}")
     assert n_bad == 0, f"{n_bad} skip bits differ outside the margin band"
     if flips.any():
         forced = r["skip"].copy()

@@ -59,13 +59,13 @@ def _small(seed=31, L=1000, B=2, Hq=8, Hkv=2, d=32, temperate=True):
 
 
 def _brute(cfg, q, k8, v8, ks, vs):
-    """Scaled fp64 scores [B,Hq,L] and dequantised values [B,Hq,L,d]; the
-    query is the E4M3 hi + lo form (pinned by the fp8_query tests below)."""
+    """Scaled fp64 scores [B,Hq,L] of the given query against rows
+    dequantised here (bit-level decoder times the scale), and the
+    dequantised values [B,Hq,L,d]."""
     kd = decoded(k8) * ks.astype(np.float64)[:, :, None, None]
     vd = decoded(v8) * vs.astype(np.float64)[:, :, None, None]
     kd, vd = np.repeat(kd, cfg.G, axis=1), np.repeat(vd, cfg.G, axis=1)
-    qe = oracle.fp8_query(q)[0].astype(np.float64)
-    s = cfg.scale * np.einsum("bhd,bhcd->bhc", qe, kd)
+    s = cfg.scale * np.einsum("bhd,bhcd->bhc", q.double().numpy(), kd)
     return s, vd
 
 
@@ -117,29 +117,3 @@ def test_fp8_generator_quantises_within_half_a_step():
         assert (lg == np.round(lg)).all()
         amax = np.abs(decoded(x8.numpy())).max(axis=(2, 3))
         assert (amax >= 224).all() and (amax <= 448).all()
-
-
-def test_fp8_query_is_exact_for_bf16_rows_without_tiny_elements():
-    g = np.random.default_rng(5)
-    x = g.standard_normal((64, 128)) * np.exp2(g.integers(-20, 20, size=(64, 1)))
-    # keep every element within 2^-8 of its row's largest (in magnitude)
-    amax = np.abs(x).max(axis=1, keepdims=True)
-    x = np.where(np.abs(x) < amax * 2.0 ** -8, np.sign(x + 1e-300) * amax * 2.0 ** -8, x)
-    q = torch.from_numpy(x).to(torch.bfloat16)
-    qe, e = oracle.fp8_query(q)
-    assert (qe == q.float().numpy()).all()
-    # sigma: the largest power of two with max|q| sigma <= 256
-    m = np.abs(q.float().numpy()).max(axis=1)
-    assert (m * np.exp2(e) <= 256).all() and (m * np.exp2(e + 1) > 256).all()
-
-
-def test_fp8_query_moves_tiny_elements_by_at_most_half_a_subnormal_step():
-    g = np.random.default_rng(6)
-    x = g.standard_normal((64, 128)) * np.exp2(g.uniform(-12, 0, size=(64, 128)))
-    q = torch.from_numpy(x).to(torch.bfloat16)
-    qe, e = oracle.fp8_query(q)
-    d = np.abs(qe.astype(np.float64) - q.double().numpy())
-    assert (d <= 2.0 ** -10 * np.exp2(-e)[:, None] * (1 + 1e-12)).all()
-    assert d.max() > 0  # some element did move: the case is exercised
-    z = oracle.fp8_query(torch.zeros(2, 128, dtype=torch.bfloat16))
-    assert (z[0] == 0).all() and (z[1] == 0).all()
