@@ -23,7 +23,7 @@ ATTN_BF16, ATTN_F32 = 0, 1
 
 #: Every symbol include/attn_skip.h declares.
 EXPORTED = ("attn_skip_prefill", "attn_skip_prefill_blocks", "attn_skip_prefill_varlen",
-            "attn_skip_decode", "attn_skip_decode_fp8",
+            "attn_skip_decode", "attn_skip_decode_fp8", "attn_skip_decode_nvfp4",
             "attn_skip_decode_per_head", "attn_skip_decode_combine",
             "attn_skip_prefill_margins", "attn_skip_decode_margins", "attn_skip_sparsity_at",
             "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
@@ -63,6 +63,8 @@ def load() -> ctypes.CDLL:
                                              P, P, P, P]
     lib.attn_skip_decode_fp8.argtypes = [P, P, P, P, P, i, i, i, i, i, i, i64, i64, f, d, i, i,
                                          P, P, P, P]
+    lib.attn_skip_decode_nvfp4.argtypes = [P, P, P, P, P, P, P, i, i, i, i, i, i, i64, i64, f,
+                                           d, i, i, P, P, P, P]
     lib.attn_skip_decode.argtypes = [P, P, P, i, i, i, i, i, i, i, i64, i64, f, d, i, i, P, P, P,
                                      P]
     lib.attn_skip_decode_combine.argtypes = [P, P, i, i, i, i, i, P, P, P]
@@ -86,7 +88,7 @@ def load() -> ctypes.CDLL:
     lib.attn_skip_status_string.argtypes = [i]
     lib.attn_skip_status_string.restype = ctypes.c_char_p
     for fn in ("attn_skip_prefill", "attn_skip_prefill_blocks", "attn_skip_prefill_varlen",
-               "attn_skip_decode", "attn_skip_decode_fp8",
+               "attn_skip_decode", "attn_skip_decode_fp8", "attn_skip_decode_nvfp4",
                "attn_skip_decode_per_head", "attn_skip_decode_combine",
                "attn_skip_prefill_margins", "attn_skip_decode_margins",
                "attn_skip_lambda_for_sparsity", "attn_skip_fit_lambda_model",
@@ -319,6 +321,40 @@ def attn_skip_decode_fp8(q, k8, v8, k_scale, v_scale, lam, Bc=128, n_splits=8, s
                                      float(scale), float(lam), Bc, n_splits, _ptr(o), _ptr(lse),
                                      _ptr(bits), _stream(stream, q.device))
     _check("attn_skip_decode_fp8", st)
+    return o, lse, bits
+
+
+def attn_skip_decode_nvfp4(q, k4, v4, k_bs, v_bs, k_scale, v_scale, lam, Bc=128, n_splits=8,
+                           scale=0.0, out=None, stream=None):
+    """Decode over an NVFP4 cache: q [B,Hq,128] bf16; k4/v4 [B,Hkv,L,64] uint8
+    (two E2M1 codes per byte, element 2i in the low nibble); k_bs/v_bs
+    [B,Hkv,L,8] uint8 E4M3 block scales; k_scale/v_scale [B,Hkv] fp32; all on
+    one device.  Returns fp32 ``(o_part, lse_part, skip_bits)`` like
+    :func:`attn_skip_decode`."""
+    _cuda_contig(q, k4, v4, k_bs, v_bs, k_scale, v_scale)
+    for t in (k4, v4, k_bs, v_bs):
+        if t.dtype != torch.uint8:
+            raise TypeError("codes and block scales must be uint8")
+    if k_scale.dtype != torch.float32 or v_scale.dtype != torch.float32:
+        raise TypeError("scales must be float32")
+    B, Hq, dk = q.shape
+    _, Hkv, L, half = v4.shape
+    dv = 2 * half
+    if k_bs.shape != (B, Hkv, L, dk // 16) or v_bs.shape != (B, Hkv, L, dv // 16):
+        raise ValueError("block scales must be [B, Hkv, L, d/16]")
+    if out is None:
+        o = torch.empty(B, Hq, n_splits, dv, dtype=torch.float32, device=q.device)
+        lse = torch.empty(B, Hq, n_splits, dtype=torch.float32, device=q.device)
+        bits = torch.empty(decode_bitmap_shape(B, Hkv, L, Bc, n_splits), dtype=torch.int32,
+                           device=q.device)
+    else:
+        o, lse, bits = out
+    st = load().attn_skip_decode_nvfp4(_ptr(q), _ptr(k4), _ptr(v4), _ptr(k_bs), _ptr(v_bs),
+                                       _ptr(k_scale), _ptr(v_scale), B, Hq, Hkv, L, dk, dv,
+                                       k4.shape[3], v4.shape[3], float(scale), float(lam), Bc,
+                                       n_splits, _ptr(o), _ptr(lse), _ptr(bits),
+                                       _stream(stream, q.device))
+    _check("attn_skip_decode_nvfp4", st)
     return o, lse, bits
 
 

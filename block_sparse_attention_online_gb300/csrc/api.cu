@@ -288,6 +288,49 @@ extern "C" attn_status attn_skip_decode_fp8(const void *q, const void *k, const 
   return from_cuda(launch_decode_fp8(a, (cudaStream_t)stream));
 }
 
+extern "C" attn_status attn_skip_decode_nvfp4(const void *q, const void *k4, const void *v4,
+                                              const uint8_t *k_bs, const uint8_t *v_bs,
+                                              const float *k_scale, const float *v_scale, int B,
+                                              int Hq, int Hkv, int L, int dk, int dv,
+                                              int64_t k_row_stride, int64_t v_row_stride,
+                                              float scale, double lambda, int Bc, int n_splits,
+                                              float *o_part, float *lse_part,
+                                              uint32_t *skip_bits, void *stream) {
+  if (!q || !k4 || !v4 || !k_bs || !v_bs || !k_scale || !v_scale || !o_part || !lse_part ||
+      !skip_bits)
+    return ATTN_EINVAL;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || L <= 0 || dk <= 0 || dv <= 0 || Bc <= 0 || n_splits <= 0)
+    return ATTN_EINVAL;
+  if (Hq % Hkv != 0 || !lambda_ok(lambda) || !(scale == scale)) return ATTN_EINVAL;
+  if ((dk % 16) || (dv % 16) || k_row_stride < dk / 2 || v_row_stride < dv / 2)
+    return ATTN_EINVAL;
+  if (!aligned16(q) || !aligned16(k4) || !aligned16(v4) || !aligned16(k_bs) ||
+      !aligned16(v_bs) || !aligned16(o_part) || !aligned16(lse_part) || !aligned16(skip_bits) ||
+      ((uintptr_t)k_scale & 3u) || ((uintptr_t)v_scale & 3u))
+    return ATTN_EINVAL;
+  const int G = Hq / Hkv;
+  if (dk != 128 || dv != 128 || Bc != 128 || !(G == 1 || G == 2 || G == 4 || G == 8) ||
+      (k_row_stride % 16) || (v_row_stride % 16))
+    return ATTN_EUNSUPPORTED;
+  const long n_b = (L + (long)Bc - 1) / Bc;
+  if ((long)B * Hkv * n_splits > 0x7fffffffL || (long)B * Hkv * L > 0x7fffffffL)
+    return ATTN_EUNSUPPORTED;
+  DecodeArgs a{};
+  a.q = q; a.k = k4; a.v = v4; a.k_bs = k_bs; a.v_bs = v_bs;
+  a.k_scale = k_scale; a.v_scale = v_scale;
+  a.o_part = o_part; a.lse_part = lse_part; a.bits = skip_bits;
+  a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.L = L; a.dk = dk; a.dv = dv; a.Bc = Bc;
+  a.n_splits = n_splits; a.k_row_stride = k_row_stride; a.v_row_stride = v_row_stride;
+  a.n_b = (int)n_b;
+  a.bps = (int)((n_b + n_splits - 1) / n_splits);
+  a.words = (a.bps + 31) / 32;
+  a.scale = scale > 0.f ? scale : (float)(1.0 / sqrt((double)dk));
+  a.ln_lambda = ln_lambda(lambda);
+  cudaError_t e = error_word(&a.err);
+  if (e != cudaSuccess) return from_cuda(e);
+  return from_cuda(launch_decode_nvfp4(a, (cudaStream_t)stream));
+}
+
 extern "C" attn_status attn_skip_decode_combine(const float *o_part, const float *lse_part, int B,
                                                 int Hq, int n_splits, int dv, attn_dtype out_dt,
                                                 void *o, float *lse, void *stream) {

@@ -61,6 +61,9 @@ struct DecodeArgs {
   // FP8 (E4M3) cache: k and v hold codes; one fp32 scale per (b, KV head)
   // for keys (multiplies the scores) and values (multiplies the outputs).
   const float *k_scale, *v_scale;
+  // NVFP4 cache: k and v hold packed E2M1 codes [.., L, d/2], k_bs and v_bs
+  // the E4M3 block scales [B,Hkv,L,d/16] (one per 16 elements of a row).
+  const uint8_t *k_bs, *v_bs;
 };
 
 // Sampled decode output (SANTA estimator).
@@ -91,6 +94,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_decode_fp8(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_decode_nvfp4(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 cudaError_t launch_selftest_wait(unsigned *err, cudaStream_t s);
 cudaError_t launch_santa_decode(const SantaArgs &a, cudaStream_t s);

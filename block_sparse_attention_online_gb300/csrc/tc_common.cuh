@@ -406,12 +406,13 @@ inline bool make_map_bf16_3d(CUtensorMap *m, const void *ptr, int cols, int64_t 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D map over a byte tensor [outer][rows][cols] (E4M3 codes) whose rows are
-// row_bytes apart and whose outer slices are rows * row_bytes apart; box =
-// `cols` bytes x box_rows rows x 1, 128-byte swizzle; rows past `rows` read
-// as zero.
+// 3-D map over a byte tensor [outer][rows][cols] (E4M3 or packed E2M1 codes)
+// whose rows are row_bytes apart and whose outer slices are rows * row_bytes
+// apart; box = `cols` bytes x box_rows rows x 1, 128-byte swizzle (or the
+// given one; `cols` at most the swizzle span); rows past `rows` read as zero.
 inline bool make_map_u8_3d(CUtensorMap *m, const void *ptr, int cols, int64_t row_bytes,
-                           int rows, int outer, int box_rows) {
+                           int rows, int outer, int box_rows,
+                           CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)outer};
@@ -419,7 +420,7 @@ inline bool make_map_u8_3d(CUtensorMap *m, const void *ptr, int cols, int64_t ro
   const cuuint32_t box[3] = {(cuuint32_t)cols, (cuuint32_t)box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -211,14 +211,6 @@ attn_status attn_skip_decode_per_head(const void *q, const void *k, const void *
                                       float *lse_part, uint32_t *skip_bits, void *stream);
 
 /*
- * Merge of decode split partials by log-sum-exp (FlashDecoding):
- * LSE = ln sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) * O_s.
- * Splits with LSE_s = -inf weigh zero.
- *
- *  o_part [B, Hq, n_splits, dv] fp32,  lse_part [B, Hq, n_splits] fp32
- *  o      [B, Hq, dv] (out_dt),       lse      [B, Hq] fp32
- */
-/*
  * Split-KV decode with block skipping over an FP8 (E4M3) key/value cache.
  *
  * Defines: the loop of attn_skip_decode (section "Decode 内核：砍带宽": decide
@@ -253,6 +245,53 @@ attn_status attn_skip_decode_fp8(const void *q, const void *k, const void *v, co
                                  double lambda, int Bc, int n_splits, float *o_part,
                                  float *lse_part, uint32_t *skip_bits, void *stream);
 
+/*
+ * Split-KV decode with block skipping over an NVFP4 key/value cache.
+ *
+ * Defines: the loop of attn_skip_decode (section "Decode 内核：砍带宽") over a
+ * cache in the NVFP4 layout (the BLASST page evaluates NVFP4-quantised models,
+ * section "更大模型、MLA 与组合性", and fixes no format): per row, E2M1 codes
+ * (OCP MX FP4: +-{0, 0.5, 1, 1.5, 2, 3, 4, 6}) two per byte, element 2i in
+ * the low nibble; one E4M3 block scale per 16 consecutive elements; one fp32
+ * scale per (sequence, KV head) for keys and one for values:
+ * row element = scale[b,h] * E4M3(block scale) * E2M1(code).  The key scale
+ * is folded into the score scale, the value scale multiplies the outputs.
+ *
+ *  q          [B, Hq, dk] bf16 (device).  The key products are fp16 x fp16,
+ *             so each query head enters as fp16(q * 2^e), 2^e the largest
+ *             power of two with max|q| 2^e <= 2^15: exact for every element
+ *             not below about 2^-31 of the head's largest, and otherwise off
+ *             by at most 2^-25 / 2^e
+ *  k4, v4     [B, Hkv, L, d/2] uint8 packed E2M1 codes (device), row strides
+ *             in bytes (multiples of 16, at least d/2)
+ *  k_bs, v_bs [B, Hkv, L, d/16] uint8 E4M3 block scales (device, dense)
+ *  k_scale, v_scale [B, Hkv] fp32 (device)
+ *  outputs, bitmap layout, merge, lambda, scale: as attn_skip_decode
+ *  (o_part already multiplied by v_scale; attn_skip_decode_combine merges)
+ *
+ * Codes and block scales are widened exactly to fp16 on the chip (an E2M1
+ * value times an E4M3 scale is an fp16 normal number); P is rounded to fp16
+ * for the P.V product, accumulation in fp32.  No NaN block-scale codes.
+ * Kernels built: dk = dv = 128, Bc = 128, Hq/Hkv in {1, 2, 4, 8}.  EINVAL
+ * as for attn_skip_decode_fp8 (also for a null or misaligned block-scale
+ * pointer).
+ */
+attn_status attn_skip_decode_nvfp4(const void *q, const void *k4, const void *v4,
+                                   const uint8_t *k_bs, const uint8_t *v_bs,
+                                   const float *k_scale, const float *v_scale, int B, int Hq,
+                                   int Hkv, int L, int dk, int dv, int64_t k_row_stride,
+                                   int64_t v_row_stride, float scale, double lambda, int Bc,
+                                   int n_splits, float *o_part, float *lse_part,
+                                   uint32_t *skip_bits, void *stream);
+
+/*
+ * Merge of decode split partials by log-sum-exp (FlashDecoding):
+ * LSE = ln sum_s exp(LSE_s),  O = sum_s exp(LSE_s - LSE) * O_s.
+ * Splits with LSE_s = -inf weigh zero.
+ *
+ *  o_part [B, Hq, n_splits, dv] fp32,  lse_part [B, Hq, n_splits] fp32
+ *  o      [B, Hq, dv] (out_dt),       lse      [B, Hq] fp32
+ */
 attn_status attn_skip_decode_combine(const float *o_part, const float *lse_part, int B, int Hq,
                                      int n_splits, int dv, attn_dtype out_dt, void *o,
                                      float *lse, void *stream);

@@ -31,6 +31,7 @@ from block_sparse_attention_online_gb300 import workloads as W  # noqa: E402
 
 OUT = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lambdas.json")
 FP8 = {W.GQA_DECODE_FP8_32K.name: W.GQA_DECODE_FP8_32K}  # E4M3 cache workloads
+NVFP4 = {W.GQA_DECODE_NVFP4_32K.name: W.GQA_DECODE_NVFP4_32K}  # NVFP4 cache workloads
 TARGETS = (0.5, 0.7, 0.85)
 
 
@@ -43,6 +44,12 @@ def statistics(cfg):
         r = oracle.prefill(q, k, v, cfg.scale, 0.0, cfg.Br, cfg.Bc, cfg.causal, units=units)
         m = r["margin"].reshape(-1, cfg.n_b)[units]
         sample = f"query heads {[hk * cfg.G for hk in kv_heads]}, all {cfg.n_t} tiles"
+    elif cfg.name in NVFP4:
+        q, k4, v4, kbs, vbs, ks, vs = W.decode_inputs_nvfp4(cfg)
+        r = oracle.decode_nvfp4(q, k4, v4, kbs, vbs, ks, vs, cfg.scale, 0.0, cfg.Bc,
+                                cfg.n_splits)
+        m = r["margin"]
+        sample = "all (sequence, KV head, split) units"
     elif cfg.name in FP8:
         q, k8, v8, ks, vs = W.decode_inputs_fp8(cfg)
         r = oracle.decode_fp8(q, k8, v8, ks, vs, cfg.scale, 0.0, cfg.Bc, cfg.n_splits)
@@ -63,7 +70,7 @@ def main(names):
         with open(OUT) as f:
             data = json.load(f)
     for name in names:
-        cfg = W.CONFIGS[name] if name in W.CONFIGS else FP8[name]
+        cfg = W.CONFIGS[name] if name in W.CONFIGS else {**FP8, **NVFP4}[name]
         t0 = time.time()
         m, sample = statistics(cfg)
         entry = {"pairs": int(m.size), "sample": sample, "0.0": {"lambda": 0.0, "sparsity": 0.0}}
@@ -92,4 +99,4 @@ def main(names):
 
 
 if __name__ == "__main__":
-    main(sys.argv[1:] or [c for c in W.CONFIGS] + list(FP8))
+    main(sys.argv[1:] or [c for c in W.CONFIGS] + list(FP8) + list(NVFP4))

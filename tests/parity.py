@@ -52,40 +52,88 @@ def compare_bits(gpu_skip: np.ndarray, ora_skip: np.ndarray, ora_margin: np.ndar
     return int(bad.sum()), flips
 
 
+def _split_band(eps, Bc, n_splits):
+    """From per-(b, query head, key) score deviations eps [B, Hkv, G, L]: twice
+    the largest over the split's keys and the group's heads, per (b, KV head,
+    split); shape [B, Hkv, n_splits, 1]."""
+    eps = eps.max(axis=2)
+    B, Hkv, L = eps.shape
+    n_b = -(-L // Bc)
+    out = np.zeros((B, Hkv, n_splits, 1))
+    for s in range(n_splits):
+        b0, b1 = (s * n_b) // n_splits, ((s + 1) * n_b) // n_splits
+        if b1 > b0:
+            out[:, :, s, 0] = 2.0 * eps[:, :, b0 * Bc:min(b1 * Bc, L)].max(axis=-1)
+    return out
+
+
+def _pow2_exponent(q, top):
+    """Per head: e = top - ceil(log2 max|q|) (0 for a zero row)."""
+    import torch
+    qf = q.detach().to("cpu", torch.float64).numpy()
+    amax = np.abs(qf).max(axis=-1)
+    frac, ex = np.frexp(np.where(amax > 0, amax, 1.0))
+    return np.where(amax > 0, top - np.where(frac == 0.5, ex - 1, ex), 0).astype(np.float64)
+
+
 def fp8_query_pair_band(q, k8, k_scale, scale: float, Bc: int, n_splits: int, G: int):
     """Extra bit band of the E4M3-cache decode kernel, per (b, KV head, split).
 
     The kernel multiplies the E4M3 key codes with the query written as the
     exact pair hi + lo of E4M3 values after a per-head power-of-two scale
     sigma = 2^e, the largest with max|q| sigma <= 256 (an E4M3 x E4M3 product
-    needs both operands in E4M3).  For a bf16 element x = q sigma the remainder
-    x - hi has at most four significant bits, so lo is exact unless it falls
-    below E4M3's subnormal step 2^-9, where rounding moves x by at most 2^-10:
-    each query element moves by at most 2^-10 / sigma.  A score of key c then
-    moves by at most eps_c = scale * k_scale * 2^-10 / sigma * sum_d |code_cd|
-    (code values decoded from E4M3), and a block statistic max_r(rowmax_r -
-    m_new_r) by at most twice the largest eps over the split's keys and the
-    group's heads.  Returns that bound, shape [B, Hkv, n_splits, 1]."""
+    needs both operands in E4M3).  For a bf16 element x = q sigma with |x| >=
+    2^-6 the remainder x - hi is a multiple of x's last place with at most four
+    significant bits, exact in E4M3 when |x| >= 2^-2 (its last place is then
+    at least E4M3's subnormal step 2^-9); below 2^-2 rounding lo to that step
+    moves x by at most 2^-10.  So query element d of head h moves by at most
+    2^-10 / sigma_h, and only if |q_hd sigma_h| < 2^-2.  A score of key c then
+    moves by at most eps_hc = scale * k_scale * 2^-10 / sigma_h * (sum of
+    |code_cd| over those d), and a block statistic max_r(rowmax_r - m_new_r)
+    by at most twice the largest eps over the split's keys and the group's
+    heads.  Returns that bound, shape [B, Hkv, n_splits, 1]."""
     import torch
+    e = _pow2_exponent(q, 8)                                          # [B, Hq]
     qf = q.detach().to("cpu", torch.float64).numpy()
-    B, Hq, _ = qf.shape
-    amax = np.abs(qf).max(axis=-1)
-    frac, ex = np.frexp(np.where(amax > 0, amax, 1.0))
-    e = np.where(amax > 0, 8 - np.where(frac == 0.5, ex - 1, ex), 0)
-    qstep = (2.0 ** -10) * np.exp2(-e.astype(np.float64))          # [B, Hq]
-    Hkv = Hq // G
-    qstep = qstep.reshape(B, Hkv, G).max(axis=-1)                   # [B, Hkv]
+    moved = (np.abs(qf) * np.exp2(e)[..., None] < 0.25).astype(np.float32)  # [B, Hq, dk]
     kd = torch.as_tensor(np.ascontiguousarray(k8, dtype=np.uint8)).view(
-        torch.float8_e4m3fn).double().abs().sum(-1).numpy()          # [B, Hkv, L]
-    L = kd.shape[-1]
-    n_b = -(-L // Bc)
-    out = np.zeros((B, Hkv, n_splits, 1))
-    for s in range(n_splits):
-        b0, b1 = (s * n_b) // n_splits, ((s + 1) * n_b) // n_splits
-        if b1 > b0:
-            seg = kd[:, :, b0 * Bc:min(b1 * Bc, L)].max(axis=-1)
-            out[:, :, s, 0] = 2.0 * scale * np.asarray(k_scale, dtype=np.float64) * qstep * seg
-    return out
+        torch.float8_e4m3fn).float().abs()                            # [B, Hkv, L, dk]
+    B, Hq, dk = moved.shape
+    Hkv = Hq // G
+    m = torch.from_numpy(moved.reshape(B, Hkv, G, dk))
+    ksum = torch.einsum("bhgd,bhld->bhgl", m, kd).double().numpy()    # [B, Hkv, G, L]
+    coef = (scale * np.asarray(k_scale, dtype=np.float64)[:, :, None]
+            * (2.0 ** -10) * np.exp2(-e).reshape(B, Hkv, G))
+    return _split_band(coef[..., None] * ksum, Bc, n_splits)
+
+
+# E2M1 magnitudes by the code's low three bits (OCP MX FP4).
+_E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def nvfp4_query_band(q, k4, k_bs, k_scale, scale: float, Bc: int, n_splits: int, G: int):
+    """Extra bit band of the NVFP4-cache decode kernel, per (b, KV head, split).
+
+    The kernel's key products are fp16 x fp16: each query head enters as
+    fp16(q sigma), sigma = 2^e the largest power of two with max|q| sigma <=
+    2^15.  A bf16 element keeps its eight significant bits in fp16 unless
+    |q sigma| < 2^-17, where fp16's subnormal step 2^-24 rounds it by at most
+    2^-25: each query element moves by at most 2^-25 / sigma.  The widened keys
+    are exact, so a score moves by at most scale * k_scale * 2^-25 / sigma *
+    sum_d |k_d| and a block statistic by twice the largest such amount over
+    the split's keys and the group's heads.  Returns [B, Hkv, n_splits, 1]."""
+    import torch
+    e = _pow2_exponent(q, 15)                                         # [B, Hq]
+    k4 = np.ascontiguousarray(k4, dtype=np.uint8)
+    mag = _E2M1[k4 & 7] + _E2M1[(k4 >> 4) & 7]                       # per byte: two elements
+    bs = torch.as_tensor(np.ascontiguousarray(k_bs, dtype=np.uint8)).view(
+        torch.float8_e4m3fn).double().abs().numpy()                   # [B, Hkv, L, d/16]
+    ksum = (mag.reshape(*mag.shape[:-1], bs.shape[-1], 8).sum(-1) * bs).sum(-1)  # [B, Hkv, L]
+    B, Hq = e.shape
+    Hkv = Hq // G
+    coef = (scale * np.asarray(k_scale, dtype=np.float64)[:, :, None]
+            * (2.0 ** -25) * np.exp2(-e).reshape(B, Hkv, G))
+    return _split_band(coef[..., None] * ksum[:, :, None, :], Bc, n_splits)
 
 
 def rel_l2(a, b):
