@@ -108,6 +108,19 @@ def decode_bytes(cfg, kept_blocks, total_blocks):
     return total_blocks * kv_block + kept_blocks * v_block + q + part
 
 
+MARGIN_BAND = 1e-3
+
+
+def margin_blocks(mu, lam):
+    """Traversed blocks whose statistic (from the kernel's statistics mode)
+    lies within MARGIN_BAND of ln(lambda): the blocks whose skip bit fp32 and
+    fp64 arithmetic may decide differently.  0 for lambda = 0."""
+    if lam <= 0:
+        return 0
+    m = mu[~torch.isnan(mu)].double()
+    return int(((m - math.log(lam)).abs() < MARGIN_BAND).sum())
+
+
 # ------------------------------------------------------------------ clocks --
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -223,6 +236,9 @@ def run_gpu(args, rank, world):
     dense, per_pair = prefill_flops(P)
     n_b = -(-D.L // D.Bc)
     d_blocks = D.B * D.Hkv * n_b
+    # each traversed block's statistic, for the margin-block counts
+    p_mu = bs.attn_skip_prefill_margins(dq, dk_, P.Br, P.Bc, True).cpu()
+    d_mu = bs.attn_skip_decode_margins(dqd, dkd, D.Bc, D.n_splits).cpu()
 
     # prefill sweep: lambda = 0 and the 50/70/85 % thresholds
     sweep = {}
@@ -233,7 +249,8 @@ def run_gpu(args, rank, world):
         kept = pairs - skipped
         executed = per_pair * (pairs + kept)
         ms = statistics.mean(durs)
-        sweep[t] = {"lambda": lmb, "sparsity": skipped / pairs, "ms": ms,
+        sweep[t] = {"lambda": lmb, "sparsity": skipped / pairs,
+                    "margin_blocks": margin_blocks(p_mu, lmb), "ms": ms,
                     "dense_equiv_tflops": dense / ms / 1e9,
                     "executed_tflops": executed / ms / 1e9, "executed_flops": executed}
     for t in sweep:
@@ -247,7 +264,8 @@ def run_gpu(args, rank, world):
         kept = d_blocks - skipped
         byts = decode_bytes(D, kept, d_blocks)
         ms, cms = statistics.mean(durs), statistics.mean(cdurs)
-        dsweep[t] = {"lambda": lmb, "sparsity": skipped / d_blocks, "ms_decode": ms,
+        dsweep[t] = {"lambda": lmb, "sparsity": skipped / d_blocks,
+                     "margin_blocks": margin_blocks(d_mu, lmb), "ms_decode": ms,
                      "ms_combine": cms, "tok_per_s": D.B / ((ms + cms) / 1e3),
                      "gbs": byts / ms / 1e6, "bytes": byts}
     for t in dsweep:
@@ -272,6 +290,7 @@ def run_gpu(args, rank, world):
     santa = santa_sweep(args, bs, dev, stream, flush)
     varlen = varlen_sweep(args, bs, dev, stream, flush)
     fp8 = fp8_decode_sweep(args, bs, dev, stream, flush, lam)
+    nvfp4 = nvfp4_decode_sweep(args, bs, dev, stream, flush, lam)
 
     # ---- the timed region: K steps of the whole hot path at ~70 % ---------
     fp, fd = prefill(lp[TARGET]), decode(ld[TARGET])
@@ -331,6 +350,7 @@ def run_gpu(args, rank, world):
                    "parallelism": f"replicas x{world}"},
         "prefill": {"ms": round(p_avg, 4), "lambda": lp[TARGET],
                     "sparsity": round(s70["sparsity"], 4),
+                    "margin_blocks": s70["margin_blocks"],
                     "dense_equiv_tflops": round(value / world, 2),
                     "executed_tflops": round(executed_tflops, 2),
                     "sweep": {t: {kk: (round(vv, 5) if isinstance(vv, float) and kk != "lambda"
@@ -338,6 +358,7 @@ def run_gpu(args, rank, world):
                                   for kk, vv in s.items()} for t, s in sweep.items()}},
         "decode": {"ms": round(d_avg, 4), "ms_combine": round(c_avg, 4),
                    "lambda": ld[TARGET], "sparsity": round(dec["sparsity"], 4),
+                   "margin_blocks": dec["margin_blocks"],
                    "tok_per_s": round(world * D.B / ((d_avg + c_avg) / 1e3), 1),
                    "gbs": round(dec_gbs, 1), "hbm_frac": round(dec_gbs / peak_hbm, 4),
                    "sweep": {t: {kk: (round(vv, 5) if isinstance(vv, float) and kk != "lambda"
@@ -364,6 +385,7 @@ def run_gpu(args, rank, world):
         "santa_decode": santa,
         "varlen_prefill": varlen,
         "fp8_decode": fp8,
+        "nvfp4_decode": nvfp4,
         "e2e": e2e,
         "device_errors": "none (device error word read after the run)",
         "gpu_launches": 3 * args.steps,  # prefill, decode, merge per timed step
@@ -388,6 +410,7 @@ def mla_sweep(args, bs, dev, stream, flush, lam):
     o = torch.empty(M.B, M.Hq, M.dv, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(M.B, M.Hq, dtype=torch.float32, device=dev)
     out = {}
+    mu = bs.attn_skip_decode_margins(dq, dk_, M.Bc, M.n_splits).cpu()
     for t in ("0.0", "max"):
         lmb = lam[M.name][t]["lambda"]
 
@@ -403,7 +426,8 @@ def mla_sweep(args, bs, dev, stream, flush, lam):
         qk = 2.0 * M.Hq * M.Bc * M.dk * units          # every block
         pv = 2.0 * M.Hq * M.Bc * M.dv * kept           # kept blocks
         byts = M.B * M.L * M.dk * 2 + M.B * M.Hq * M.dk * 2 + op.numel() * 4 + lp.numel() * 4
-        out[t] = {"lambda": lmb, "sparsity": round(skipped / units, 4), "ms": round(ms, 4),
+        out[t] = {"lambda": lmb, "sparsity": round(skipped / units, 4),
+                  "margin_blocks": margin_blocks(mu, lmb), "ms": round(ms, 4),
                   "tok_per_s": round(M.B / (ms / 1e3), 1), "gbs": round(byts / ms / 1e6, 1),
                   "algorithmic_tflops": round((qk + pv) / ms / 1e9, 2),
                   "tensor_tflops_executed": round((2 * qk + pv) / ms / 1e9, 2)}
@@ -431,6 +455,7 @@ def long_prefill_sweep(args, bs, dev, stream, flush, lam, pk):
                        f"Br{C.Br} Bc{C.Bc}; {C.salient_frac:.0%} salient keys, band "
                        f"+{C.band_a:g}*sqrt(d) on each tile's 256 nearest keys",
            "dense_equiv_flops": dense}
+    mu = bs.attn_skip_prefill_margins(dq, dk_, C.Br, C.Bc, True).cpu()
     for t in ("0.0", "0.5", "0.7", "0.85"):
         lmb = lam[C.name][t]["lambda"]
         durs = timed_launches(
@@ -440,7 +465,8 @@ def long_prefill_sweep(args, bs, dev, stream, flush, lam, pk):
         skipped = int(bs.unpack_bits(bits, C.n_b).sum())
         executed = per_pair * (2 * pairs - skipped)
         ms = statistics.mean(durs)
-        out[t] = {"lambda": lmb, "sparsity": round(skipped / pairs, 4), "ms": round(ms, 4),
+        out[t] = {"lambda": lmb, "sparsity": round(skipped / pairs, 4),
+                  "margin_blocks": margin_blocks(mu, lmb), "ms": round(ms, 4),
                   "dense_equiv_tflops": round(dense / ms / 1e9, 2),
                   "executed_tflops": round(executed / ms / 1e9, 2),
                   "executed_frac_of_peak": round(executed / ms / 1e9 / peak_tf, 4)}
@@ -538,6 +564,46 @@ def fp8_decode_sweep(args, bs, dev, stream, flush, lam):
         skipped = int(bs.unpack_bits(bits, -(-n_b // C.n_splits)).sum())
         kept = blocks - skipped
         byts = (blocks + kept) * C.Bc * C.dk + C.B * C.Hq * C.dk * 2 + op.numel() * 4 * 2
+        ms, cms = statistics.mean(durs), statistics.mean(cdurs)
+        out[t] = {"lambda": lmb, "sparsity": round(skipped / blocks, 4), "ms_decode": round(ms, 4),
+                  "ms_combine": round(cms, 4), "tok_per_s": round(C.B / ((ms + cms) / 1e3), 1),
+                  "gbs": round(byts / ms / 1e6, 1), "bytes": byts}
+    out[TARGET]["speedup_vs_lambda0"] = round(
+        (out["0.0"]["ms_decode"] + out["0.0"]["ms_combine"])
+        / (out[TARGET]["ms_decode"] + out[TARGET]["ms_combine"]), 4)
+    return out
+
+
+def nvfp4_decode_sweep(args, bs, dev, stream, flush, lam):
+    """Decode over an NVFP4 key/value cache, the GQA decode shape (B=16,
+    32/8 heads, L=32768, 8 splits), at lambda = 0 and the oracle's ~70 %
+    threshold, decode + merge; bytes = key codes and block scales + kept
+    value codes and block scales + Q + partials."""
+    C = W.GQA_DECODE_NVFP4_32K
+    inputs = [x.to(dev) for x in W.decode_inputs_nvfp4(C)]
+    n_b = -(-C.L // C.Bc)
+    blocks = C.B * C.Hkv * n_b
+    op = torch.empty(C.B, C.Hq, C.n_splits, C.dv, dtype=torch.float32, device=dev)
+    lpart = torch.empty(C.B, C.Hq, C.n_splits, dtype=torch.float32, device=dev)
+    bits = torch.empty(bs.decode_bitmap_shape(C.B, C.Hkv, C.L, C.Bc, C.n_splits),
+                       dtype=torch.int32, device=dev)
+    o = torch.empty(C.B, C.Hq, C.dv, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(C.B, C.Hq, dtype=torch.float32, device=dev)
+    block_bytes = C.Bc * (C.dk // 2 + C.dk // 16)  # codes + block scales
+    out = {"workload": f"{C.name}: B{C.B} Hq{C.Hq} Hkv{C.Hkv} d{C.dk} L{C.L} Bc{C.Bc} "
+                       f"splits{C.n_splits}, E2M1 codes, E4M3 scale per 16 elements, "
+                       f"fp32 scale per (sequence, KV head)"}
+    for t in ("0.0", TARGET):
+        lmb = lam[C.name][t]["lambda"]
+        durs = timed_launches(
+            lambda: bs.attn_skip_decode_nvfp4(*inputs, lmb, C.Bc, C.n_splits,
+                                              out=(op, lpart, bits)),
+            args.warmup, args.steps, flush, stream)
+        cdurs = timed_launches(lambda: bs.attn_skip_decode_combine(op, lpart, out=(o, lse)),
+                               args.warmup, args.steps, flush, stream)
+        skipped = int(bs.unpack_bits(bits, -(-n_b // C.n_splits)).sum())
+        kept = blocks - skipped
+        byts = (blocks + kept) * block_bytes + C.B * C.Hq * C.dk * 2 + op.numel() * 4 * 2
         ms, cms = statistics.mean(durs), statistics.mean(cdurs)
         out[t] = {"lambda": lmb, "sparsity": round(skipped / blocks, 4), "ms_decode": round(ms, 4),
                   "ms_combine": round(cms, 4), "tok_per_s": round(C.B / ((ms + cms) / 1e3), 1),
@@ -850,6 +916,14 @@ def run_profile_case(args):
         def fn():
             op, lp, _ = bs.attn_skip_decode(q, k, None, lmb, MLA.Bc, MLA.n_splits, dv=MLA.dv)
             bs.attn_skip_decode_combine(op, lp)
+    elif args.profile == "nvfp4":
+        C = W.GQA_DECODE_NVFP4_32K
+        inputs = [x.to(dev) for x in W.decode_inputs_nvfp4(C)]
+        lmb = lam[C.name][TARGET]["lambda"]
+
+        def fn():
+            op, lp, _ = bs.attn_skip_decode_nvfp4(*inputs, lmb, C.Bc, C.n_splits)
+            bs.attn_skip_decode_combine(op, lp)
     elif args.profile == "fp8":
         C = W.GQA_DECODE_FP8_32K
         q, k8, v8, ks, vs = (x.to(dev) for x in W.decode_inputs_fp8(C))
@@ -872,7 +946,30 @@ def run_profile_case(args):
     print(json.dumps({"profile": args.profile, "launches": args.warmup + 1}))
 
 
+def launch_plan(gpus, env, argv):
+    """How to honour --gpus: ("run", world) when the process group matches it
+    (torchrun's WORLD_SIZE, or one process for --gpus 1); ("relaunch", cmd)
+    to start one process per GPU under torch.distributed.run when --gpus N > 1
+    is given outside torchrun; ("error", why) when torchrun's world size and
+    --gpus disagree."""
+    if gpus < 1:
+        return "error", f"--gpus must be at least 1 (got {gpus})"
+    if "WORLD_SIZE" in env:
+        world = int(env["WORLD_SIZE"])
+        if world != gpus:
+            return "error", f"--gpus {gpus} but WORLD_SIZE={world}"
+        return "run", world
+    if gpus == 1:
+        return "run", 1
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={gpus}", "--master-addr", "127.0.0.1",
+           "--master-port", env.get("MASTER_PORT", "29531"), os.path.abspath(__file__),
+           *argv]
+    return "relaunch", cmd
+
+
 def main(argv=None):
+    argv = list(sys.argv[1:] if argv is None else argv)
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -881,12 +978,18 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--calibration-sweep", action="store_true",
                     help="also fit the threshold model over prefill lengths 4K-64K")
-    ap.add_argument("--profile", choices=("prefill", "decode", "fp8", "mla"),
+    ap.add_argument("--profile", choices=("prefill", "decode", "fp8", "nvfp4", "mla"),
                     help="only warm up and launch one kernel (for ncu captures)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    world = int(os.environ.get("WORLD_SIZE", "1"))
+    plan, what = launch_plan(args.gpus, os.environ, argv)
+    if plan == "error":
+        ap.error(what)
+    if plan == "relaunch":
+        sys.stdout.flush()
+        os.execv(what[0], what)
+    world = what
     rank = int(os.environ.get("RANK", "0"))
     if world > 1:
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")

@@ -11,6 +11,8 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long CPU-only oracle runs")
+    config.addinivalue_line("markers", "fullsize: GPU parity over a whole benchmark launch "
+                            "(minutes of oracle time; still part of -m gpu)")
 
 
 def pytest_collection_modifyitems(config, items):

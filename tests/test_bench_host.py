@@ -77,3 +77,19 @@ def test_work_model():
 def test_rejects_too_few_warmups():
     with pytest.raises(SystemExit):
         bench.main(["--warmup", "2"])
+
+
+def test_gpus_flag_drives_the_world_size():
+    """--gpus N outside torchrun relaunches one process per GPU under
+    torch.distributed.run; inside torchrun it must match WORLD_SIZE."""
+    assert bench.launch_plan(1, {}, []) == ("run", 1)
+    assert bench.launch_plan(4, {"WORLD_SIZE": "4"}, []) == ("run", 4)
+    plan, why = bench.launch_plan(8, {"WORLD_SIZE": "2"}, [])
+    assert plan == "error" and "WORLD_SIZE=2" in why
+    assert bench.launch_plan(0, {}, [])[0] == "error"
+    plan, cmd = bench.launch_plan(2, {}, ["--gpus", "2", "--steps", "3"])
+    assert plan == "relaunch"
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert "--nproc-per-node=2" in cmd and "127.0.0.1" in cmd
+    assert cmd[-4:] == ["--gpus", "2", "--steps", "3"]
+    assert cmd[-5].endswith("bench.py")

@@ -27,8 +27,10 @@ def run_prefill(q, k, v, lam, causal=True):
     return o.float().cpu().numpy(), lse.cpu().numpy(), bits
 
 
-def check_prefill(cfg, q, k, v, lam, units=None, causal=True):
-    """Compare all tiles (units=None) or the given (b,h,t) units."""
+def check_prefill(cfg, q, k, v, lam, units=None, causal=True, label=""):
+    """Compare all tiles (units=None) or the given (b,h,t) units.  Tiles where
+    a bit flipped inside the margin band are compared against the oracle
+    re-run on those tiles alone with the GPU's decisions."""
     o, lse, bits = run_prefill(q, k, v, lam, causal)
     skip = bs.unpack_bits(bits, cfg.n_b).numpy()
     r = oracle.prefill(q, k, v, cfg.scale, lam, 128, 128, causal, units=units)
@@ -37,17 +39,37 @@ def check_prefill(cfg, q, k, v, lam, units=None, causal=True):
         sel[:] = True
     else:
         sel.reshape(-1)[np.asarray(units)] = True
-    n_bad, flips = compare_bits(skip[sel], r["skip"][sel], r["margin"][sel], lam)
+    n_bad, flips = compare_bits(skip[sel], r["skip"][sel], r["margin"][sel], lam,
+                                label=label or f"prefill T={cfg.T} lambda={lam:.4g}")
     assert n_bad == 0, f"{n_bad} skip bits differ outside the margin band"
     if flips.any():
+        fl = np.zeros(sel.shape, dtype=bool)
+        fl[sel] = flips.any(axis=-1)
+        fu = np.flatnonzero(fl)
         forced = np.zeros_like(r["skip"])
-        forced[sel] = skip[sel]
-        r = oracle.prefill(q, k, v, cfg.scale, lam, 128, 128, causal, units=units,
-                           force_skip=forced)
+        forced[fl] = skip[fl]
+        rf = oracle.prefill(q, k, v, cfg.scale, lam, 128, 128, causal, units=fu,
+                            force_skip=forced)
+        frows = np.repeat(fl, 128, axis=2)[:, :, :cfg.T]
+        r["o"][frows] = rf["o"][frows]
+        r["lse"][frows] = rf["lse"][frows]
     rows = np.repeat(sel, 128, axis=2)[:, :, :cfg.T]
     check_outputs(o[rows], r["o"][rows], lse[rows], r["lse"][rows], "bf16", "prefill")
     trav = np.isfinite(r["margin"][sel])
+    LAST_LAUNCH["skip"] = skip
     return float(skip[sel][trav].mean()), int(flips.sum())
+
+
+# The GPU bitmap of the last check_prefill launch (every head and tile).
+LAST_LAUNCH = {}
+
+
+def launch_sparsity(cfg, skip):
+    """Skipped / traversed (tile, block) pairs of a whole causal launch."""
+    t = np.arange(cfg.n_t)[:, None]
+    j = np.arange(cfg.n_b)[None, :]
+    trav = j <= np.minimum(cfg.T - 1, (t + 1) * cfg.Br - 1) // cfg.Bc
+    return float(skip[:, :, trav].mean())
 
 
 @pytest.mark.parametrize("T", [128, 640, 1000])
@@ -103,30 +125,56 @@ def test_prefill_tc_noncausal_ragged():
         check_prefill(cfg, q, k, v, lam, causal=False)
 
 
-def _sample_units(cfg, n_heads, seed):
-    rng = np.random.default_rng(seed)
-    heads = rng.choice(cfg.Hq, n_heads, replace=False)
-    tiles = [0, 1, cfg.n_t // 2, cfg.n_t - 2, cfg.n_t - 1]
-    return sorted({int(h) * cfg.n_t + t for h in heads for t in tiles})
+_INPUTS = {}
 
 
-@pytest.mark.parametrize("target", ["0.0", "0.7"])
-def test_prefill_tc_full_size_16k(target):
-    """B=1, 32/8 heads, T=16384 (the benchmark's launch), sampled tiles."""
+def _inputs(cfg):
+    if cfg.name not in _INPUTS:
+        _INPUTS.clear()
+        _INPUTS[cfg.name] = W.prefill_inputs(cfg)
+    return _INPUTS[cfg.name]
+
+
+@pytest.mark.fullsize
+@pytest.mark.parametrize("target", ["0.0", "0.5", "0.7", "0.85"])
+def test_prefill_tc_full_size_16k_every_tile(target):
+    """B=1, 32/8 heads, T=16384 (the benchmark's launch): all 32 x 128
+    (head, tile) units against the oracle at lambda = 0 and the oracle's
+    ~50/70/85 % thresholds; the sparsity of the launch against the oracle's
+    stored figure for its sampled heads."""
     cfg = W.GQA_PREFILL_16K
-    q, k, v = W.prefill_inputs(cfg)
+    q, k, v = _inputs(cfg)
     lam = 0.0 if target == "0.0" else _lambda(cfg.name, target)
-    sparsity, flips = check_prefill(cfg, q, k, v, lam, units=_sample_units(cfg, 3, 7))
-    if target == "0.7":  # the sample is dominated by short early tiles; the whole
-        assert sparsity > 0.3, sparsity  # workload's sparsity is read from the bench bitmap
+    sparsity, flips = check_prefill(cfg, q, k, v, lam,
+                                    label=f"prefill T=16384 every tile, target {target}")
+    if target != "0.0":  # the threshold was placed on three heads' statistics
+        assert abs(sparsity - float(target)) < 0.03, sparsity
+        assert abs(sparsity - launch_sparsity(cfg, LAST_LAUNCH["skip"])) < 1e-9
 
 
-def test_prefill_tc_full_size_64k_sampled():
+def _long_units(cfg, n_heads=4, seed=64):
+    """A seeded subset of query heads (one per KV head pair), all their tiles."""
+    rng = np.random.default_rng(seed)
+    heads = sorted(int(x) for x in rng.choice(cfg.Hq, n_heads, replace=False))
+    return heads, [h * cfg.n_t + t for h in heads for t in range(cfg.n_t)]
+
+
+@pytest.mark.fullsize
+@pytest.mark.parametrize("target", ["0.0", "0.5", "0.7", "0.85"])
+def test_prefill_tc_full_size_64k_four_heads(target):
+    """B=1, 32/8 heads, T=65536 with the local band, the whole launch on the
+    GPU; four seeded query heads, all 512 tiles each, against the oracle at
+    lambda = 0 and the ~50/70/85 % thresholds."""
     cfg = W.GQA_PREFILL_64K
-    q, k, v = W.prefill_inputs(cfg)
-    lam = _lambda(cfg.name, "0.7")
-    units = [cfg.n_t - 1, cfg.n_t // 2, 5 * cfg.n_t + cfg.n_t - 1]
-    check_prefill(cfg, q, k, v, lam, units=units)
+    q, k, v = _inputs(cfg)
+    lam = 0.0 if target == "0.0" else _lambda(cfg.name, target)
+    heads, units = _long_units(cfg)
+    sparsity, flips = check_prefill(cfg, q, k, v, lam, units=units,
+                                    label=f"prefill T=65536 heads {heads}, target {target}")
+    if target != "0.0":  # the threshold was placed on three other heads' statistics
+        assert sparsity > 0.3, sparsity
+        whole = launch_sparsity(cfg, LAST_LAUNCH["skip"])
+        assert abs(whole - float(target)) < 0.03, whole
 
 
 @pytest.mark.parametrize("target", ["0.0", "0.7"])
