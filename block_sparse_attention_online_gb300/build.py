@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libattn_skip.so")
 SOURCES = ["api.cu", "prefill_f32.cu", "prefill_tc.cu", "decode.cu", "mla_decode.cu",
            "combine.cu", "selftest.cu", "santa.cu", "santa_noalloc.cu", "decode_fp8.cu",
-           "decode_nvfp4.cu"]
+           "decode_nvfp4.cu", "mla_cluster.cu"]
 HEADERS = [os.path.join(ROOT, "include", "attn_skip.h")] + [
     os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

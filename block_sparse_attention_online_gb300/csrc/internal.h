@@ -93,6 +93,8 @@ cudaError_t launch_prefill_f32(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 cudaError_t launch_decode_bf16(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s);
+cudaError_t launch_mla_cluster(const DecodeArgs &a, cudaStream_t s);
+int mla_cluster_max_bps();
 cudaError_t launch_decode_fp8(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_decode_nvfp4(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);

@@ -469,6 +469,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }  // namespace
 
 cudaError_t launch_mla_decode(const DecodeArgs &a, cudaStream_t s) {
+  // The three-CTA cluster kernel (mla_cluster.cu) computes Q.K^T once per key;
+  // this two-CTA kernel serves the statistics mode and splits longer than the
+  // cluster kernel's decision array.
+  if (!a.stats_only && a.bps <= mla_cluster_max_bps()) return launch_mla_cluster(a, s);
   CUtensorMap mq, mkv;
   // [B, rows, 576] bf16, boxes of 64 columns x (H or BN) rows, 128-byte swizzle.
   if (!make_map_bf16_3d(&mq, a.q, DK, DK, H, a.B, H) ||

@@ -46,3 +46,12 @@ def test_mla_full_size(target):
         with open(os.path.join(GOLDEN, "lambdas.json")) as f:
             expect = json.load(f)[cfg.name]["max"]["sparsity"]
         assert abs(sparsity - expect) < 0.01, (sparsity, expect)
+
+
+def test_mla_long_split_uses_the_two_cta_kernel():
+    """A split of more than 2048 blocks (one split over 131,136 keys) runs the
+    two-CTA kernel the cluster kernel hands over to; the same oracle checks it."""
+    cfg = W.MLA_DECODE_16K.with_(B=1, L=2049 * 64 + 40, n_splits=1, seed=63)
+    q, k, _ = W.decode_inputs(cfg)
+    for lam in (0.0, 1e-9):
+        check_decode(cfg, q, k, None, lam, 1)
