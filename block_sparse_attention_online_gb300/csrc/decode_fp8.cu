@@ -64,12 +64,12 @@ using namespace tc;
 constexpr int D = 128;    // head size (keys and values)
 constexpr int BC = 128;   // keys per block (MMA rows of S^T)
 constexpr int NQ = 16;    // MMA columns: query heads, padded
-constexpr int NKF = 7;    // E4M3 key stages (bytes in flight cover the load latency)
+constexpr int NKP = 3;    // E4M3 key stages of two blocks each (one barrier per pair)
 constexpr int NVF = 2;    // E4M3 value stages
 constexpr int NVH = 2;    // fp16 value stages
-constexpr int NS = 4;     // TMEM S^T buffers
+constexpr int NS = 4;     // TMEM S^T buffers (two pairs)
 constexpr int NPT = 3;    // P^T buffers
-constexpr int NDEC = 32;  // decision ring
+constexpr int NDP = 16;   // decision ring, in block pairs
 constexpr int NT = 16 * 32;
 constexpr int WARP_K = 4, WARP_QK = 5, WARP_V = 6, WARP_PV = 7, WARP_VC = 8;  // 0-3: scores
 constexpr int NVC = 8 * 32;                                                 // converter threads
@@ -79,7 +79,7 @@ constexpr uint32_t HALF_BYTES = H_BYTES / 2;  // one 64-column swizzled box
 constexpr uint32_t QT_BYTES = NQ * 128;       // 2 KB: 16 rows x 128 codes
 constexpr uint32_t PT_BOX = NQ * 128;         // 2 KB: 16 heads x 64 fp16 keys
 constexpr uint32_t SMEM_KF = 0;
-constexpr uint32_t SMEM_VF = SMEM_KF + NKF * F8_BYTES;
+constexpr uint32_t SMEM_VF = SMEM_KF + NKP * 2 * F8_BYTES;
 constexpr uint32_t SMEM_VH = SMEM_VF + NVF * F8_BYTES;
 constexpr uint32_t SMEM_Q = SMEM_VH + NVH * H_BYTES;  // Q hi, then Q lo
 constexpr uint32_t SMEM_PT = SMEM_Q + 2 * QT_BYTES;   // NPT x two 64-key boxes
@@ -96,19 +96,19 @@ constexpr float kRescaleLog2 = 8.0f;  // exp reference may lag the max by 2^8
 constexpr uint32_t IDESC_QK = idesc_e4m3_f32(BC, NSC);
 constexpr uint32_t IDESC_PV = idesc_f16_f32(D, NQ, 0) | (1u << 15);
 static_assert(TMEM_O + NQ <= TMEM_COLS, "TMEM budget");
-static_assert(NS % 2 == 0, "block pairs read two adjacent S^T buffers");
+static_assert(NS == 4, "two pair buffers of two adjacent S^T buffers");
 static_assert(NT >= NQ * 16, "16 threads per query row write the query pair");
 
 struct Shared {
-  uint64_t kf_full[NKF], kf_empty[NKF];
+  uint64_t kf_full[NKP], kf_empty[NKP];
   uint64_t vf_full[NVF], vf_empty[NVF];
   uint64_t vh_full[NVH], vh_empty[NVH];
-  uint64_t s_full[NS], s_free[NS];
+  uint64_t s_full[2], s_free[2];  // per pair buffer
   uint64_t p_full[NPT], p_free[NPT];
-  uint64_t dec_full[NDEC], dec_empty[NDEC];
+  uint64_t dec_full[NDP], dec_empty[NDP];
   uint64_t red_full[2];  // the four score warps' partial maxima of a block pair are in
   uint64_t l_full;       // the four score warps' row sums are in
-  int dec[NDEC];
+  int dec[NDP][2];
   float red[2][4][16];  // per block pair (double buffered): per score warp, per head max
   float lsum[4][8];    // epilogue: per score warp, per head row sum
   float sl2[NQ];       // per head: raw score -> log2 units
@@ -301,9 +301,9 @@ __global__ void __launch_bounds__(NT, 1)
   }
   fence_proxy_async_smem();  // visible to the tensor core
   if (tid == 0) {
-    for (int i = 0; i < NKF; ++i) {
+    for (int i = 0; i < NKP; ++i) {
       mbar_init(smem_u32(&sh.kf_full[i]), 1);
-      mbar_init(smem_u32(&sh.kf_empty[i]), 1);  // the S^T commit
+      mbar_init(smem_u32(&sh.kf_empty[i]), 1);  // the S^T commit of the pair
     }
     for (int i = 0; i < NVF; ++i) {
       mbar_init(smem_u32(&sh.vf_full[i]), 1);
@@ -313,7 +313,7 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(smem_u32(&sh.vh_full[i]), 8);
       mbar_init(smem_u32(&sh.vh_empty[i]), 1);  // the O^T commit
     }
-    for (int i = 0; i < NS; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh.s_full[i]), 1);
       mbar_init(smem_u32(&sh.s_free[i]), 4);  // the four score warps
     }
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(smem_u32(&sh.p_full[i]), 4);  // the four score warps
       mbar_init(smem_u32(&sh.p_free[i]), 1);  // the O^T commit
     }
-    for (int i = 0; i < NDEC; ++i) {
+    for (int i = 0; i < NDP; ++i) {
       mbar_init(smem_u32(&sh.dec_full[i]), 1);
       // readers: the value producer, the O^T issuer, the eight value converters
       mbar_init(smem_u32(&sh.dec_empty[i]), 10);
@@ -343,20 +343,24 @@ __global__ void __launch_bounds__(NT, 1)
     if (lane == 0) {
       prefetch_tmap(&tm_k);
       const uint64_t pol = policy_evict_first();  // the cache is streamed once
+      // Blocks in pairs: one stage (two tiles) and one barrier per pair.
+      const int npair = (nb + 1) / 2;
       int issued = 0;
-      for (int j = 0; j < nb && !*abort; ++j) {
-        const int f = j % NKF;
-        if (j >= NKF &&
-            !mbar_wait(smem_u32(&sh.kf_empty[f]), ((j / NKF) - 1) & 1, abort, a.err, kErrTimeout))
+      for (int q = 0; q < npair && !*abort; ++q) {
+        const int f = q % NKP;
+        const int n = 2 * q + 1 < nb ? 2 : 1;
+        if (q >= NKP &&
+            !mbar_wait(smem_u32(&sh.kf_empty[f]), ((q / NKP) - 1) & 1, abort, a.err, kErrTimeout))
           break;
-        mbar_expect_tx(smem_u32(&sh.kf_full[f]), F8_BYTES);
-        tma_load_3d(base + SMEM_KF + f * F8_BYTES, &tm_k, smem_u32(&sh.kf_full[f]), 0,
-                    (j0 + j) * BC, zkv, pol);
+        mbar_expect_tx(smem_u32(&sh.kf_full[f]), n * F8_BYTES);
+        for (int t = 0; t < n; ++t)
+          tma_load_3d(base + SMEM_KF + (2 * f + t) * F8_BYTES, &tm_k, smem_u32(&sh.kf_full[f]), 0,
+                      (j0 + 2 * q + t) * BC, zkv, pol);
         ++issued;
       }
-      for (int f = 0; f < NKF && f < issued; ++f) {
-        const int last = f + ((issued - 1 - f) / NKF) * NKF;
-        mbar_wait_drain(smem_u32(&sh.kf_full[f]), (last / NKF) & 1);
+      for (int f = 0; f < NKP && f < issued; ++f) {
+        const int last = f + ((issued - 1 - f) / NKP) * NKP;
+        mbar_wait_drain(smem_u32(&sh.kf_full[f]), (last / NKP) & 1);
       }
     }
   } else if (warp == WARP_V) {
@@ -366,11 +370,12 @@ __global__ void __launch_bounds__(NT, 1)
       const uint64_t pol = policy_evict_first();
       int vi = 0;
       for (int j = 0; j < nb && !*abort; ++j) {
-        if (!mbar_wait(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
-                       kErrTimeout))
+        const int q = j >> 1, ds = q % NDP;
+        if (!(j & 1) && !mbar_wait(smem_u32(&sh.dec_full[ds]), (q / NDP) & 1, abort, a.err,
+                                   kErrTimeout))
           break;
-        const int keep = sh.dec[j % NDEC];
-        mbar_arrive(smem_u32(&sh.dec_empty[j % NDEC]));
+        const int keep = sh.dec[ds][j & 1];
+        if ((j & 1) || j == nb - 1) mbar_arrive(smem_u32(&sh.dec_empty[ds]));  // pair read
         if (!keep) continue;
         const int f = vi % NVF;
         if (vi >= NVF &&
@@ -393,12 +398,13 @@ __global__ void __launch_bounds__(NT, 1)
     const int t0 = (warp - WARP_VC) * 32 + lane;
     int vi = 0;
     for (int j = 0; j < nb; ++j) {
-      if (!mbar_wait_warp(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
-                          kErrTimeout))
+      const int q = j >> 1, ds = q % NDP;
+      if (!(j & 1) && !mbar_wait_warp(smem_u32(&sh.dec_full[ds]), (q / NDP) & 1, abort, a.err,
+                                      kErrTimeout))
         break;
-      const int keep = sh.dec[j % NDEC];
+      const int keep = sh.dec[ds][j & 1];
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.dec_empty[j % NDEC]));
+      if (lane == 0 && ((j & 1) || j == nb - 1)) mbar_arrive(smem_u32(&sh.dec_empty[ds]));
       if (!keep) continue;
       const int f = vi % NVF, hs = vi % NVH;
       if (!mbar_wait_warp(smem_u32(&sh.vf_full[f]), (vi / NVF) & 1, abort, a.err, kErrTimeout))
@@ -423,23 +429,30 @@ __global__ void __launch_bounds__(NT, 1)
       // The query pair as one 32-row operand: hi in rows 0-15, lo in rows 16-31
       // (the two 2 KB tiles are adjacent, 8-row groups 1 KB apart).
       const uint64_t qd = kmajor_base(base + SMEM_Q);
-      for (int j = 0; j < nb; ++j) {
-        const int f = j % NKF, sb = j % NS;
-        if (!mbar_wait(smem_u32(&sh.kf_full[f]), (j / NKF) & 1, abort, a.err, kErrTimeout))
+      // Blocks in pairs: one key barrier, one S^T buffer barrier and two
+      // commits per pair (a barrier wait between products costs about as
+      // much as a product).
+      const int npair = (nb + 1) / 2;
+      for (int q = 0; q < npair; ++q) {
+        const int f = q % NKP, pb = q & 1;
+        const int n = 2 * q + 1 < nb ? 2 : 1;
+        if (!mbar_wait(smem_u32(&sh.kf_full[f]), (q / NKP) & 1, abort, a.err, kErrTimeout))
           break;
-        // S^T buffer sb is free once the score warps have read block j - NS.
-        if (j >= NS && !mbar_wait(smem_u32(&sh.s_free[sb]), ((j / NS) - 1) & 1, abort, a.err,
-                                  kErrTimeout))
+        // Pair buffer pb is free once the score warps have read pair q - 2.
+        if (q >= 2 && !mbar_wait(smem_u32(&sh.s_free[pb]), ((q >> 1) - 1) & 1, abort, a.err,
+                                 kErrTimeout))
           break;
         fence_after_sync();
-        const uint64_t kd = kmajor_base(base + SMEM_KF + f * F8_BYTES);
-        // [K hi^T | K lo^T]: four k-steps of 32 codes; the score threads add
-        // the two parts.
+        for (int t = 0; t < n; ++t) {
+          const uint64_t kd = kmajor_base(base + SMEM_KF + (2 * f + t) * F8_BYTES);
+          // [K hi^T | K lo^T]: four k-steps of 32 codes; the score threads add
+          // the two parts.
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_f8f6f4_ss(tmem + sb * NSC, kd + ((uint64_t)kk * 2), qd + ((uint64_t)kk * 2),
-                        IDESC_QK, kk > 0);
-        mma_commit(smem_u32(&sh.s_full[sb]));
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f8f6f4_ss(tmem + (2 * pb + t) * NSC, kd + ((uint64_t)kk * 2), qd + ((uint64_t)kk * 2),
+                          IDESC_QK, kk > 0);
+        }
+        mma_commit(smem_u32(&sh.s_full[pb]));
         mma_commit(smem_u32(&sh.kf_empty[f]));
       }
     }
@@ -448,11 +461,12 @@ __global__ void __launch_bounds__(NT, 1)
     if (lane == 0) {
       int kc = 0;
       for (int j = 0; j < nb && !*abort; ++j) {
-        if (!mbar_wait(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
-                       kErrTimeout))
+        const int q = j >> 1, ds = q % NDP;
+        if (!(j & 1) && !mbar_wait(smem_u32(&sh.dec_full[ds]), (q / NDP) & 1, abort, a.err,
+                                   kErrTimeout))
           break;
-        const int keep = sh.dec[j % NDEC];
-        mbar_arrive(smem_u32(&sh.dec_empty[j % NDEC]));
+        const int keep = sh.dec[ds][j & 1];
+        if ((j & 1) || j == nb - 1) mbar_arrive(smem_u32(&sh.dec_empty[ds]));  // pair read
         if (!keep) continue;
         const int pb = kc % NPT, hs = kc % NVH;
         if (!mbar_wait(smem_u32(&sh.p_full[pb]), (kc / NPT) & 1, abort, a.err, kErrTimeout) ||
@@ -550,29 +564,33 @@ __global__ void __launch_bounds__(NT, 1)
       ++kc;
       return true;
     };
-    // Decision of block jj (thread 0): published to the value pipeline; bitmap.
-    auto publish = [&](int jj, bool skip) {
+    // Decisions of pair q (thread 0): published to the value pipeline together
+    // (one barrier per pair); bitmap.
+    auto publish = [&](int q, bool skip0, bool skip1, bool two) {
+      const int ds = q % NDP;
       // On a timeout the abort flag is raised and every later wait fails.
-      if (jj < NDEC || mbar_wait(smem_u32(&sh.dec_empty[jj % NDEC]), ((jj / NDEC) - 1) & 1,
-                                 abort, a.err, kErrTimeout)) {
-        sh.dec[jj % NDEC] = skip ? 0 : 1;
-        mbar_arrive(smem_u32(&sh.dec_full[jj % NDEC]));
+      if (q < NDP || mbar_wait(smem_u32(&sh.dec_empty[ds]), ((q / NDP) - 1) & 1, abort, a.err,
+                               kErrTimeout)) {
+        sh.dec[ds][0] = skip0 ? 0 : 1;
+        sh.dec[ds][1] = skip1 ? 0 : 1;
+        mbar_arrive(smem_u32(&sh.dec_full[ds]));
       }
-      if (skip) word |= 1u << (jj & 31);
-      if ((jj & 31) == 31 || jj == nb - 1) {
-        bits[jj >> 5] = word;
-        word = 0;
+      for (int t = 0; t < (two ? 2 : 1); ++t) {
+        const int jj = 2 * q + t;
+        if (t ? skip1 : skip0) word |= 1u << (jj & 31);
+        if ((jj & 31) == 31 || jj == nb - 1) {
+          bits[jj >> 5] = word;
+          word = 0;
+        }
       }
     };
     // Blocks in pairs: both S^T buffers read at once (j even, so they are
     // adjacent), both blocks' partial maxima exchanged in one round.
     for (int j = 0; j < nb; j += 2) {
       const bool two = j + 1 < nb;
-      const int sb = j % NS;
       const int q = j >> 1;  // pair index
-      if (!mbar_wait_warp(smem_u32(&sh.s_full[sb]), (j / NS) & 1, abort, a.err, kErrTimeout) ||
-          (two && !mbar_wait_warp(smem_u32(&sh.s_full[sb + 1]), ((j + 1) / NS) & 1, abort, a.err,
-                                  kErrTimeout))) {
+      const int pb = q & 1, sb = 2 * pb;
+      if (!mbar_wait_warp(smem_u32(&sh.s_full[pb]), (q >> 1) & 1, abort, a.err, kErrTimeout)) {
         ok = false;
         break;
       }
@@ -584,10 +602,7 @@ __global__ void __launch_bounds__(NT, 1)
       tmem_wait_ld_regs(y);
       fence_before_sync();  // the scores are in registers: the S^T buffers are free
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&sh.s_free[sb]));
-        if (two) mbar_arrive(smem_u32(&sh.s_free[sb + 1]));
-      }
+      if (lane == 0) mbar_arrive(smem_u32(&sh.s_free[pb]));
       const bool v0 = (j0 + j) * BC + kidx < a.L;
       const bool v1 = two && (j0 + j + 1) * BC + kidx < a.L;
       float s0[G], s1[G];
@@ -627,10 +642,7 @@ __global__ void __launch_bounds__(NT, 1)
         mn1[g] = fmaxf(mn0[g], b1);
         m2[g] = two ? mn1[g] : mn0[g];  // the running max advances on every block
       }
-      if (tid == 0) {
-        publish(j, skip0);
-        if (two) publish(j + 1, skip1);
-      }
+      if (tid == 0) publish(q, skip0, skip1, two);
       if (!skip0 && !kept(s0, mn0)) {
         ok = false;
         break;

@@ -2,13 +2,15 @@
 (CPU, a model of the protocol, not of the arithmetic); the barrier model and
 the checks are those of the prefill protocol test.
 
-Roles of one CTA: the K producer (E4M3 key tiles), the S^T issuer, the score
-warps (blocks in pairs: both S^T buffers read and freed, both decisions
-published, then P^T of each kept block), the V producer (E4M3 value tiles of
-kept blocks), the converter warps (E4M3 -> fp16 value tiles) and the O^T
-issuer.  Decisions go through a ring read by the V producer, the converters
-and the O^T issuer; the P^T buffers are released by the O^T commits, which
-also serve the O^T rescale and the end-of-split waits.
+Roles of one CTA: the K producer (E4M3 key tiles, two blocks per stage and
+barrier), the S^T issuer (one pair per key barrier, one S^T pair buffer of two
+adjacent buffers per barrier), the score warps (blocks in pairs: the pair
+buffer read and freed, both decisions published under one ring barrier, then
+P^T of each kept block), the V producer (E4M3 value tiles of kept blocks), the
+converter warps (E4M3 -> fp16 value tiles) and the O^T issuer.  Decisions go
+through a ring of block pairs read by the V producer, the converters and the
+O^T issuer (each reads a pair's slot once); the P^T buffers are released by
+the O^T commits, which also serve the O^T rescale and the end-of-split waits.
 """
 import random
 
@@ -17,7 +19,7 @@ import pytest
 from tests.test_pipeline_protocol import Bar, ProtocolError
 
 
-def simulate_fp8(nb, keep, rescale, seed, NKF=7, NVF=2, NVH=2, NS=4, NPT=3, NDEC=32,
+def simulate_fp8(nb, keep, rescale, seed, NKP=3, NVF=2, NVH=2, NPT=3, NDP=16,
                  wait_ring_slot=True):
     rng = random.Random(seed)
     B = {}
@@ -25,25 +27,26 @@ def simulate_fp8(nb, keep, rescale, seed, NKF=7, NVF=2, NVH=2, NS=4, NPT=3, NDEC
     def bar(name, count=1):
         B[name] = Bar(name, count)
 
-    for i in range(NKF):
+    for i in range(NKP):
         bar(("kf_full", i)), bar(("kf_empty", i))
     for i in range(NVF):
         bar(("vf_full", i)), bar(("vf_empty", i))
     for i in range(NVH):
         bar(("vh_full", i)), bar(("vh_empty", i))
-    for i in range(NS):
+    for i in range(2):  # pair buffers
         bar(("s_full", i)), bar(("s_free", i))
     for i in range(NPT):
         bar(("p_full", i)), bar(("p_free", i))
-    for i in range(NDEC):
+    for i in range(NDP):
         bar(("dec_full", i)), bar(("dec_empty", i), 3)  # V producer, converters, O^T issuer
 
-    kf = [None] * NKF
+    npair = (nb + 1) // 2
+    kf = [None] * NKP
     vf = [None] * NVF
     vh = [None] * NVH
-    sbuf = [None] * NS
+    sbuf = [None] * 2
     pt = [None] * NPT
-    dec = [None] * NDEC
+    dec = [None] * NDP
     pv_count = [0]
     pipe, tma = [], []
 
@@ -62,32 +65,37 @@ def simulate_fp8(nb, keep, rescale, seed, NKF=7, NVF=2, NVH=2, NS=4, NPT=3, NDEC
             raise ProtocolError(msg)
 
     def kprod():
-        for j in range(nb):
-            f = j % NKF
-            if j >= NKF:
-                yield ("wait", ("kf_empty", f), j // NKF - 1)
+        for q in range(npair):
+            f = q % NKP
+            n = 2 if 2 * q + 1 < nb else 1
+            if q >= NKP:
+                yield ("wait", ("kf_empty", f), q // NKP - 1)
             kf[f] = None
-            B[("kf_full", f)].arrive(tx=1)
+            B[("kf_full", f)].arrive(tx=n)
+            got = []
 
-            def land(f=f, j=j):
-                kf[f] = j
+            def land(f=f, q=q, got=got, n=n):  # one tile of the pair; the stage holds
+                got.append(1)                   # the pair once both have landed
+                if len(got) == n:
+                    kf[f] = q
                 B[("kf_full", f)].complete_tx(1)
-            tma.append(land)
+            for _ in range(n):
+                tma.append(land)
             yield None
 
     def qk():
-        for j in range(nb):
-            f, sb = j % NKF, j % NS
-            yield ("wait", ("kf_full", f), j // NKF)
-            if j >= NS:
-                yield ("wait", ("s_free", sb), j // NS - 1)
-            expect(kf[f] == j, f"S^T of block {j} reads key stage {f} holding {kf[f]}")
-            expect(sbuf[sb] is None, f"S^T of block {j} overwrites buffer {sb} holding {sbuf[sb]}")
-            sbuf[sb] = ("writing", j)
+        for q in range(npair):
+            f, pb = q % NKP, q % 2
+            yield ("wait", ("kf_full", f), q // NKP)
+            if q >= 2:
+                yield ("wait", ("s_free", pb), q // 2 - 1)
+            expect(kf[f] == q, f"S^T of pair {q} reads key stage {f} holding {kf[f]}")
+            expect(sbuf[pb] is None, f"S^T of pair {q} overwrites buffer {pb} holding {sbuf[pb]}")
+            sbuf[pb] = ("writing", q)
 
-            def done(j=j, f=f, sb=sb):
-                sbuf[sb] = j
-                B[("s_full", sb)].arrive()
+            def done(q=q, f=f, pb=pb):
+                sbuf[pb] = q
+                B[("s_full", pb)].arrive()
                 B[("kf_empty", f)].arrive()
             pipe.append(done)
             yield None
@@ -97,20 +105,17 @@ def simulate_fp8(nb, keep, rescale, seed, NKF=7, NVF=2, NVH=2, NS=4, NPT=3, NDEC
         for j in range(0, nb, 2):
             two = j + 1 < nb
             blocks = [j, j + 1] if two else [j]
-            for b in blocks:
-                yield ("wait", ("s_full", b % NS), b // NS)
-            for b in blocks:
-                expect(sbuf[b % NS] == b, f"score warps read buffer {b % NS} for block {b}: "
-                                          f"{sbuf[b % NS]}")
-            for b in blocks:
-                sbuf[b % NS] = None
-                B[("s_free", b % NS)].arrive()
-            for b in blocks:  # publication by thread 0
-                if b >= NDEC and wait_ring_slot:
-                    yield ("wait", ("dec_empty", b % NDEC), b // NDEC - 1)
-                dec[b % NDEC] = (b, keep[b])
-                B[("dec_full", b % NDEC)].arrive()
-                yield None
+            q, pb = j // 2, (j // 2) % 2
+            yield ("wait", ("s_full", pb), q // 2)
+            expect(sbuf[pb] == q, f"score warps read pair buffer {pb} for pair {q}: {sbuf[pb]}")
+            sbuf[pb] = None
+            B[("s_free", pb)].arrive()
+            # publication of the pair by thread 0
+            if q >= NDP and wait_ring_slot:
+                yield ("wait", ("dec_empty", q % NDP), q // NDP - 1)
+            dec[q % NDP] = (q, [keep[b] for b in blocks])
+            B[("dec_full", q % NDP)].arrive()
+            yield None
             for b in blocks:
                 if not keep[b]:
                     continue
@@ -130,15 +135,22 @@ def simulate_fp8(nb, keep, rescale, seed, NKF=7, NVF=2, NVH=2, NS=4, NPT=3, NDEC
             expect(pv_count[0] == kc, f"epilogue reads O^T with {pv_count[0]} of {kc} products")
 
     def read_dec(j):
-        d = dec[j % NDEC]
-        expect(d is not None and d[0] == j, f"decision slot {j % NDEC} holds {d}, not block {j}")
-        B[("dec_empty", j % NDEC)].arrive()
-        return d[1]
+        q = j // 2
+        d = dec[q % NDP]
+        expect(d is not None and d[0] == q, f"decision slot {q % NDP} holds {d}, not pair {q}")
+        keep_j = d[1][j % 2]
+        if j % 2 == 1 or j == nb - 1:  # the pair's slot is read
+            B[("dec_empty", q % NDP)].arrive()
+        return keep_j
+
+    def wait_dec(j):  # the readers wait once per pair, at its first block
+        return [("wait", ("dec_full", (j // 2) % NDP), (j // 2) // NDP)] if j % 2 == 0 else []
 
     def vprod():
         vi = 0
         for j in range(nb):
-            yield ("wait", ("dec_full", j % NDEC), j // NDEC)
+            for w in wait_dec(j):
+                yield w
             if not read_dec(j):
                 continue
             f = vi % NVF
@@ -157,7 +169,8 @@ def simulate_fp8(nb, keep, rescale, seed, NKF=7, NVF=2, NVH=2, NS=4, NPT=3, NDEC
     def converters():
         vi = 0
         for j in range(nb):
-            yield ("wait", ("dec_full", j % NDEC), j // NDEC)
+            for w in wait_dec(j):
+                yield w
             if not read_dec(j):
                 continue
             f, hs = vi % NVF, vi % NVH
@@ -175,7 +188,8 @@ def simulate_fp8(nb, keep, rescale, seed, NKF=7, NVF=2, NVH=2, NS=4, NPT=3, NDEC
     def ot():
         kc = 0
         for j in range(nb):
-            yield ("wait", ("dec_full", j % NDEC), j // NDEC)
+            for w in wait_dec(j):
+                yield w
             if not read_dec(j):
                 continue
             pb, hs = kc % NPT, kc % NVH
@@ -231,12 +245,16 @@ def test_fp8_decode_protocol_has_no_parity_race_or_deadlock():
 
 
 def test_fp8_decode_protocol_with_a_short_decision_ring():
-    """The ring bound exercised: 4 decision slots instead of 32."""
-    _run_many(300, NDEC=4)
+    """The ring bound exercised: 2 pair slots instead of 16."""
+    _run_many(300, NDP=2)
+
+
+def test_fp8_decode_protocol_with_one_key_stage():
+    _run_many(200, NKP=1)
 
 
 def test_model_catches_a_decision_published_over_an_unread_slot():
     """Self-check of the model: publishing without waiting for the slot's
-    previous decision to be read by all three readers must be reported."""
+    previous pair to be read by all three readers must be reported."""
     with pytest.raises(ProtocolError):
-        _run_many(300, NDEC=4, wait_ring_slot=False)
+        _run_many(300, NDP=2, wait_ring_slot=False)
