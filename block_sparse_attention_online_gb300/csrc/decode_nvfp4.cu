@@ -56,13 +56,13 @@ using namespace tc;
 constexpr int D = 128;    // head size (keys and values)
 constexpr int BC = 128;   // keys per block (MMA rows of S^T)
 constexpr int NQ = 16;    // MMA columns: query heads, padded
-constexpr int NKF = 12;   // key code stages in shared memory
-constexpr int NKT = 4;    // widened key tiles in TMEM
+constexpr int NKF = 12;   // key code stages in shared memory (NKF / 2 block pairs)
+constexpr int NKT = 4;    // widened key tiles in TMEM (NKT / 2 block pairs)
 constexpr int NVF = 3;    // value code stages
 constexpr int NVH = 2;    // widened (fp16) value tiles
 constexpr int NS = 4;     // TMEM S^T buffers
 constexpr int NPT = 3;    // P^T buffers
-constexpr int NDEC = 32;  // decision ring
+constexpr int NDP = 16;   // decision ring, in block pairs
 constexpr int NT = 16 * 32;
 constexpr int WARP_K = 4, WARP_QK = 5, WARP_V = 6, WARP_PV = 7, WARP_KW = 8, WARP_VW = 12;
 constexpr int NVW = 4 * 32;                  // value widener threads
@@ -93,23 +93,23 @@ constexpr float kRescaleLog2 = 8.0f;  // exp reference may lag the max by 2^8
 constexpr uint32_t IDESC_QK = idesc_f16_f32(BC, NQ, 0);
 constexpr uint32_t IDESC_PV = idesc_f16_f32(D, NQ, 0) | (1u << 15);
 static_assert(TMEM_O + NQ <= TMEM_COLS, "TMEM budget");
-static_assert(NS % 2 == 0, "block pairs read two adjacent S^T buffers");
+static_assert(NS == 4 && NKF % 2 == 0 && NKT % 2 == 0, "stages and buffers in block pairs");
 static_assert(NT >= NQ * 16, "16 threads per query row write the query");
 static_assert(SMEM_KC % 1024 == 0 && SMEM_VC % 1024 == 0 && SMEM_VH % 1024 == 0 &&
                   SMEM_Q % 1024 == 0 && SMEM_PT % 1024 == 0,
               "swizzled tiles on 1024-byte boundaries");
 
 struct Shared {
-  uint64_t kc_full[NKF], kc_empty[NKF];
-  uint64_t kt_full[NKT], kt_empty[NKT];
+  uint64_t kc_full[NKF / 2], kc_empty[NKF / 2];  // per pair stage
+  uint64_t kt_full[NKT / 2], kt_empty[NKT / 2];  // per pair of TMEM tiles
   uint64_t vc_full[NVF], vc_empty[NVF];
   uint64_t vh_full[NVH], vh_empty[NVH];
-  uint64_t s_full[NS], s_free[NS];
+  uint64_t s_full[2], s_free[2];  // per pair buffer
   uint64_t p_full[NPT], p_free[NPT];
-  uint64_t dec_full[NDEC], dec_empty[NDEC];
+  uint64_t dec_full[NDP], dec_empty[NDP];
   uint64_t red_full[2];  // the four score warps' partial maxima of a block pair are in
   uint64_t l_full;       // the four score warps' row sums are in
-  int dec[NDEC];
+  int dec[NDP][2];
   float red[2][4][16];  // per block pair (double buffered): per score warp, per head max
   float lsum[4][8];     // epilogue: per score warp, per head row sum
   float sl2[NQ];        // per head: raw score -> log2 units
@@ -281,10 +281,10 @@ __device__ __forceinline__ void write_query(const DecodeArgs &a, int b, int hk, 
 
 // The scale rows of block `row0` .. row0 + 127 of (b, KV head) slice `zkv`
 // into the 1 KB stage at `dst`, by the 32 lanes of a producer warp (rows
-// lane, lane + 32, lane + 64, lane + 96; rows past L read as zero), then
-// each lane's arrival on `bar` once its copies have landed.
+// lane, lane + 32, lane + 64, lane + 96; rows past L read as zero). The
+// caller adds each lane's arrival on the stage barrier (cp_async_arrive).
 __device__ __forceinline__ void load_scales(uint32_t dst, const uint8_t *sc, int zkv, int row0,
-                                            int L, int lane, uint32_t bar) {
+                                            int L, int lane) {
   const uint8_t *slice = sc + (size_t)zkv * L * SC_ROW;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -294,7 +294,6 @@ __device__ __forceinline__ void load_scales(uint32_t dst, const uint8_t *sc, int
     cp_async8(dst + (uint32_t)r * SC_ROW, slice + (size_t)(in ? row : L - 1) * SC_ROW,
               in ? 8u : 0u);
   }
-  cp_async_arrive(bar);
 }
 
 template <int G>
@@ -338,13 +337,13 @@ __global__ void __launch_bounds__(NT, 1)
   }
   fence_proxy_async_smem();  // visible to the tensor core
   if (tid == 0) {
-    for (int i = 0; i < NKF; ++i) {
+    for (int i = 0; i < NKF / 2; ++i) {
       mbar_init(smem_u32(&sh.kc_full[i]), 1 + 32);  // TMA arrival + 32 cp.async lanes
       mbar_init(smem_u32(&sh.kc_empty[i]), 4);      // the four key wideners
     }
-    for (int i = 0; i < NKT; ++i) {
+    for (int i = 0; i < NKT / 2; ++i) {
       mbar_init(smem_u32(&sh.kt_full[i]), 4);  // the four key wideners
-      mbar_init(smem_u32(&sh.kt_empty[i]), 1);  // the S^T commit
+      mbar_init(smem_u32(&sh.kt_empty[i]), 1);  // the S^T commit of the pair
     }
     for (int i = 0; i < NVF; ++i) {
       mbar_init(smem_u32(&sh.vc_full[i]), 1 + 32);
@@ -354,7 +353,7 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(smem_u32(&sh.vh_full[i]), 4);
       mbar_init(smem_u32(&sh.vh_empty[i]), 1);  // the O^T commit
     }
-    for (int i = 0; i < NS; ++i) {
+    for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh.s_full[i]), 1);
       mbar_init(smem_u32(&sh.s_free[i]), 4);  // the four score warps
     }
@@ -362,7 +361,7 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(smem_u32(&sh.p_full[i]), 4);  // the four score warps
       mbar_init(smem_u32(&sh.p_free[i]), 1);  // the O^T commit
     }
-    for (int i = 0; i < NDEC; ++i) {
+    for (int i = 0; i < NDP; ++i) {
       mbar_init(smem_u32(&sh.dec_full[i]), 1);
       // readers: the value producer, the O^T issuer, the four value wideners
       mbar_init(smem_u32(&sh.dec_empty[i]), 6);
@@ -383,25 +382,32 @@ __global__ void __launch_bounds__(NT, 1)
     // ------------------------------------------------------ key producer --
     if (lane == 0) prefetch_tmap(&tm_k);
     const uint64_t pol = policy_evict_first();  // the cache is streamed once
+    // Blocks in pairs: stage f holds two blocks' codes and scales under one
+    // barrier.
+    const int npair = (nb + 1) / 2;
     int issued = 0;
-    for (int j = 0; j < nb; ++j) {
+    for (int q = 0; q < npair; ++q) {
       if (__any_sync(0xffffffffu, *abort)) break;  // one outcome for the warp
-      const int f = j % NKF;
-      if (j >= NKF && !mbar_wait_warp(smem_u32(&sh.kc_empty[f]), ((j / NKF) - 1) & 1, abort,
-                                      a.err, kErrTimeout))
+      const int f = q % (NKF / 2);
+      const int n = 2 * q + 1 < nb ? 2 : 1;
+      if (q >= NKF / 2 && !mbar_wait_warp(smem_u32(&sh.kc_empty[f]), ((q / (NKF / 2)) - 1) & 1,
+                                          abort, a.err, kErrTimeout))
         break;
       if (lane == 0) {
-        mbar_expect_tx(smem_u32(&sh.kc_full[f]), CODE_BYTES);
-        tma_load_3d(base + SMEM_KC + f * CODE_BYTES, &tm_k, smem_u32(&sh.kc_full[f]), 0,
-                    (j0 + j) * BC, zkv, pol);
+        mbar_expect_tx(smem_u32(&sh.kc_full[f]), n * CODE_BYTES);
+        for (int t = 0; t < n; ++t)
+          tma_load_3d(base + SMEM_KC + (2 * f + t) * CODE_BYTES, &tm_k, smem_u32(&sh.kc_full[f]),
+                      0, (j0 + 2 * q + t) * BC, zkv, pol);
       }
-      load_scales(base + SMEM_KS + f * SC_BYTES, a.k_bs, zkv, (j0 + j) * BC, a.L, lane,
-                  smem_u32(&sh.kc_full[f]));
+      for (int t = 0; t < n; ++t)
+        load_scales(base + SMEM_KS + (2 * f + t) * SC_BYTES, a.k_bs, zkv, (j0 + 2 * q + t) * BC,
+                    a.L, lane);
+      cp_async_arrive(smem_u32(&sh.kc_full[f]));
       ++issued;
     }
-    for (int f = 0; f < NKF && f < issued; ++f) {  // drain the copies in flight
-      const int last = f + ((issued - 1 - f) / NKF) * NKF;
-      mbar_wait_drain(smem_u32(&sh.kc_full[f]), (last / NKF) & 1);
+    for (int f = 0; f < NKF / 2 && f < issued; ++f) {  // drain the copies in flight
+      const int last = f + ((issued - 1 - f) / (NKF / 2)) * (NKF / 2);
+      mbar_wait_drain(smem_u32(&sh.kc_full[f]), (last / (NKF / 2)) & 1);
     }
   } else if (warp == WARP_V) {
     // ---------------------------------------------------- value producer --
@@ -410,12 +416,13 @@ __global__ void __launch_bounds__(NT, 1)
     int vi = 0;
     for (int j = 0; j < nb; ++j) {
       if (__any_sync(0xffffffffu, *abort)) break;  // one outcome for the warp
-      if (!mbar_wait_warp(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
-                          kErrTimeout))
+      const int q = j >> 1, ds = q % NDP;
+      if (!(j & 1) && !mbar_wait_warp(smem_u32(&sh.dec_full[ds]), (q / NDP) & 1, abort, a.err,
+                                      kErrTimeout))
         break;
-      const int keep = sh.dec[j % NDEC];
+      const int keep = sh.dec[ds][j & 1];
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.dec_empty[j % NDEC]));
+      if (lane == 0 && ((j & 1) || j == nb - 1)) mbar_arrive(smem_u32(&sh.dec_empty[ds]));
       if (!keep) continue;
       const int f = vi % NVF;
       if (vi >= NVF && !mbar_wait_warp(smem_u32(&sh.vc_empty[f]), ((vi / NVF) - 1) & 1, abort,
@@ -426,8 +433,8 @@ __global__ void __launch_bounds__(NT, 1)
         tma_load_3d(base + SMEM_VC + f * CODE_BYTES, &tm_v, smem_u32(&sh.vc_full[f]), 0,
                     (j0 + j) * BC, zkv, pol);
       }
-      load_scales(base + SMEM_VS + f * SC_BYTES, a.v_bs, zkv, (j0 + j) * BC, a.L, lane,
-                  smem_u32(&sh.vc_full[f]));
+      load_scales(base + SMEM_VS + f * SC_BYTES, a.v_bs, zkv, (j0 + j) * BC, a.L, lane);
+      cp_async_arrive(smem_u32(&sh.vc_full[f]));
       ++vi;
     }
     for (int f = 0; f < NVF && f < vi; ++f) {
@@ -440,38 +447,43 @@ __global__ void __launch_bounds__(NT, 1)
     // and 8 block scales -> 64 columns of fp16 pairs (element 2i low).
     const int r = (warp - WARP_KW) * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    for (int j = 0; j < nb; ++j) {
-      const int f = j % NKF, kt = j % NKT;
-      if (!mbar_wait_warp(smem_u32(&sh.kc_full[f]), (j / NKF) & 1, abort, a.err, kErrTimeout))
+    const int npair = (nb + 1) / 2;
+    for (int q = 0; q < npair; ++q) {
+      const int f = q % (NKF / 2), kp = q % (NKT / 2);
+      const int n = 2 * q + 1 < nb ? 2 : 1;
+      if (!mbar_wait_warp(smem_u32(&sh.kc_full[f]), (q / (NKF / 2)) & 1, abort, a.err,
+                          kErrTimeout))
         break;
-      // TMEM tile kt last fed the S^T product of block j - NKT.
-      if (j >= NKT && !mbar_wait_warp(smem_u32(&sh.kt_empty[kt]), ((j / NKT) - 1) & 1, abort,
-                                      a.err, kErrTimeout))
+      // TMEM tiles of pair kp last fed the S^T products of pair q - NKT / 2.
+      if (q >= NKT / 2 && !mbar_wait_warp(smem_u32(&sh.kt_empty[kp]), ((q / (NKT / 2)) - 1) & 1,
+                                          abort, a.err, kErrTimeout))
         break;
       fence_after_sync();
-      const uint32_t codes = base + SMEM_KC + f * CODE_BYTES;
-      uint32_t slo, shi;
-      asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
-                   : "=r"(slo), "=r"(shi)
-                   : "r"(base + SMEM_KS + f * SC_BYTES + (uint32_t)r * SC_ROW));
+      for (int t = 0; t < n; ++t) {
+        const uint32_t codes = base + SMEM_KC + (2 * f + t) * CODE_BYTES;
+        uint32_t slo, shi;
+        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
+                     : "=r"(slo), "=r"(shi)
+                     : "r"(base + SMEM_KS + (2 * f + t) * SC_BYTES + (uint32_t)r * SC_ROW));
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {  // elements 64 half .. + 63: columns 32 half ..
-        const uint4 x0 = ld_code_chunk(codes, r, 2 * half);
-        const uint4 x1 = ld_code_chunk(codes, r, 2 * half + 1);
-        const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-        uint32_t h[32];
+        for (int half = 0; half < 2; ++half) {  // elements 64 half .. + 63: columns 32 half ..
+          const uint4 x0 = ld_code_chunk(codes, r, 2 * half);
+          const uint4 x1 = ld_code_chunk(codes, r, 2 * half + 1);
+          const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          uint32_t h[32];
 #pragma unroll
-        for (int q = 0; q < 8; ++q)  // word q: elements 8q..8q+7 of the half, block 4 half + q/2
-          e2m1x8_scaled(w[q], e4m3_scale2(slo, shi, 4 * half + (q >> 1)),
-                        *reinterpret_cast<uint32_t(*)[4]>(&h[4 * q]));
-        tmem_st32(lane_addr + TMEM_K + (uint32_t)kt * 64u + (uint32_t)half * 32u, h);
+          for (int qw = 0; qw < 8; ++qw)  // word qw: elements 8qw..8qw+7, block 4 half + qw/2
+            e2m1x8_scaled(w[qw], e4m3_scale2(slo, shi, 4 * half + (qw >> 1)),
+                          *reinterpret_cast<uint32_t(*)[4]>(&h[4 * qw]));
+          tmem_st32(lane_addr + TMEM_K + (uint32_t)(2 * kp + t) * 64u + (uint32_t)half * 32u, h);
+        }
       }
       tmem_wait_st();
       fence_before_sync();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(smem_u32(&sh.kc_empty[f]));
-        mbar_arrive(smem_u32(&sh.kt_full[kt]));
+        mbar_arrive(smem_u32(&sh.kt_full[kp]));
       }
     }
   } else if (warp >= WARP_VW) {
@@ -481,12 +493,13 @@ __global__ void __launch_bounds__(NT, 1)
     const int t0 = (warp - WARP_VW) * 32 + lane;
     int vi = 0;
     for (int j = 0; j < nb; ++j) {
-      if (!mbar_wait_warp(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
-                          kErrTimeout))
+      const int q = j >> 1, ds = q % NDP;
+      if (!(j & 1) && !mbar_wait_warp(smem_u32(&sh.dec_full[ds]), (q / NDP) & 1, abort, a.err,
+                                      kErrTimeout))
         break;
-      const int keep = sh.dec[j % NDEC];
+      const int keep = sh.dec[ds][j & 1];
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.dec_empty[j % NDEC]));
+      if (lane == 0 && ((j & 1) || j == nb - 1)) mbar_arrive(smem_u32(&sh.dec_empty[ds]));
       if (!keep) continue;
       const int f = vi % NVF, hs = vi % NVH;
       if (!mbar_wait_warp(smem_u32(&sh.vc_full[f]), (vi / NVF) & 1, abort, a.err, kErrTimeout))
@@ -510,21 +523,28 @@ __global__ void __launch_bounds__(NT, 1)
     // --------------------------------------------------------- S^T issuer --
     if (lane == 0) {
       const uint64_t qd = kmajor_base(base + SMEM_Q);
-      for (int j = 0; j < nb; ++j) {
-        const int kt = j % NKT, sb = j % NS;
-        if (!mbar_wait(smem_u32(&sh.kt_full[kt]), (j / NKT) & 1, abort, a.err, kErrTimeout))
-          break;
-        // S^T buffer sb is free once the score warps have read block j - NS.
-        if (j >= NS && !mbar_wait(smem_u32(&sh.s_free[sb]), ((j / NS) - 1) & 1, abort, a.err,
-                                  kErrTimeout))
+      // Blocks in pairs: one TMEM-tile barrier, one S^T buffer barrier and
+      // two commits per pair (a barrier wait between products costs about as
+      // much as a product).
+      const int npair = (nb + 1) / 2;
+      for (int q = 0; q < npair; ++q) {
+        const int kp = q % (NKT / 2), pb = q & 1;
+        const int n = 2 * q + 1 < nb ? 2 : 1;
+        if (!mbar_wait(smem_u32(&sh.kt_full[kp]), (q / (NKT / 2)) & 1, abort, a.err,
+                       kErrTimeout) ||
+            // pair buffer pb is free once the score warps have read pair q - 2
+            (q >= 2 && !mbar_wait(smem_u32(&sh.s_free[pb]), ((q >> 1) - 1) & 1, abort, a.err,
+                                  kErrTimeout)))
           break;
         fence_after_sync();
+        for (int t = 0; t < n; ++t) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-          mma_bf16_ts(tmem + TMEM_S + sb * NQ, tmem + TMEM_K + kt * 64 + kk * 8, qd + box_step(kk),
-                      IDESC_QK, kk > 0);
-        mma_commit(smem_u32(&sh.s_full[sb]));
-        mma_commit(smem_u32(&sh.kt_empty[kt]));
+          for (int kk = 0; kk < D / 16; ++kk)
+            mma_bf16_ts(tmem + TMEM_S + (2 * pb + t) * NQ, tmem + TMEM_K + (2 * kp + t) * 64 + kk * 8,
+                        qd + box_step(kk), IDESC_QK, kk > 0);
+        }
+        mma_commit(smem_u32(&sh.s_full[pb]));
+        mma_commit(smem_u32(&sh.kt_empty[kp]));
       }
     }
   } else if (warp == WARP_PV) {
@@ -532,11 +552,12 @@ __global__ void __launch_bounds__(NT, 1)
     if (lane == 0) {
       int kc = 0;
       for (int j = 0; j < nb && !*abort; ++j) {
-        if (!mbar_wait(smem_u32(&sh.dec_full[j % NDEC]), (j / NDEC) & 1, abort, a.err,
-                       kErrTimeout))
+        const int q = j >> 1, ds = q % NDP;
+        if (!(j & 1) && !mbar_wait(smem_u32(&sh.dec_full[ds]), (q / NDP) & 1, abort, a.err,
+                                   kErrTimeout))
           break;
-        const int keep = sh.dec[j % NDEC];
-        mbar_arrive(smem_u32(&sh.dec_empty[j % NDEC]));
+        const int keep = sh.dec[ds][j & 1];
+        if ((j & 1) || j == nb - 1) mbar_arrive(smem_u32(&sh.dec_empty[ds]));  // pair read
         if (!keep) continue;
         const int pb = kc % NPT, hs = kc % NVH;
         if (!mbar_wait(smem_u32(&sh.p_full[pb]), (kc / NPT) & 1, abort, a.err, kErrTimeout) ||
@@ -632,29 +653,33 @@ __global__ void __launch_bounds__(NT, 1)
       ++kc;
       return true;
     };
-    // Decision of block jj (thread 0): published to the value pipeline; bitmap.
-    auto publish = [&](int jj, bool skip) {
+    // Decisions of pair q (thread 0): published to the value pipeline together
+    // (one barrier per pair); bitmap.
+    auto publish = [&](int q, bool skip0, bool skip1, bool two) {
+      const int ds = q % NDP;
       // On a timeout the abort flag is raised and every later wait fails.
-      if (jj < NDEC || mbar_wait(smem_u32(&sh.dec_empty[jj % NDEC]), ((jj / NDEC) - 1) & 1,
-                                 abort, a.err, kErrTimeout)) {
-        sh.dec[jj % NDEC] = skip ? 0 : 1;
-        mbar_arrive(smem_u32(&sh.dec_full[jj % NDEC]));
+      if (q < NDP || mbar_wait(smem_u32(&sh.dec_empty[ds]), ((q / NDP) - 1) & 1, abort, a.err,
+                               kErrTimeout)) {
+        sh.dec[ds][0] = skip0 ? 0 : 1;
+        sh.dec[ds][1] = skip1 ? 0 : 1;
+        mbar_arrive(smem_u32(&sh.dec_full[ds]));
       }
-      if (skip) word |= 1u << (jj & 31);
-      if ((jj & 31) == 31 || jj == nb - 1) {
-        bits[jj >> 5] = word;
-        word = 0;
+      for (int t = 0; t < (two ? 2 : 1); ++t) {
+        const int jj = 2 * q + t;
+        if (t ? skip1 : skip0) word |= 1u << (jj & 31);
+        if ((jj & 31) == 31 || jj == nb - 1) {
+          bits[jj >> 5] = word;
+          word = 0;
+        }
       }
     };
     // Blocks in pairs: both S^T buffers read at once (j even, so they are
     // adjacent), both blocks' partial maxima exchanged in one round.
     for (int j = 0; j < nb; j += 2) {
       const bool two = j + 1 < nb;
-      const int sb = j % NS;
       const int q = j >> 1;  // pair index
-      if (!mbar_wait_warp(smem_u32(&sh.s_full[sb]), (j / NS) & 1, abort, a.err, kErrTimeout) ||
-          (two && !mbar_wait_warp(smem_u32(&sh.s_full[sb + 1]), ((j + 1) / NS) & 1, abort, a.err,
-                                  kErrTimeout))) {
+      const int pb = q & 1, sb = 2 * pb;
+      if (!mbar_wait_warp(smem_u32(&sh.s_full[pb]), (q >> 1) & 1, abort, a.err, kErrTimeout)) {
         ok = false;
         break;
       }
@@ -664,10 +689,7 @@ __global__ void __launch_bounds__(NT, 1)
       tmem_wait_ld_regs(x);
       fence_before_sync();  // the scores are in registers: the S^T buffers are free
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&sh.s_free[sb]));
-        if (two) mbar_arrive(smem_u32(&sh.s_free[sb + 1]));
-      }
+      if (lane == 0) mbar_arrive(smem_u32(&sh.s_free[pb]));
       const bool v0 = (j0 + j) * BC + kidx < a.L;
       const bool v1 = two && (j0 + j + 1) * BC + kidx < a.L;
       float s0[G], s1[G];
@@ -707,10 +729,7 @@ __global__ void __launch_bounds__(NT, 1)
         mn1[g] = fmaxf(mn0[g], b1);
         m2[g] = two ? mn1[g] : mn0[g];  // the running max advances on every block
       }
-      if (tid == 0) {
-        publish(j, skip0);
-        if (two) publish(j + 1, skip1);
-      }
+      if (tid == 0) publish(q, skip0, skip1, two);
       if (!skip0 && !kept(s0, mn0)) {
         ok = false;
         break;
