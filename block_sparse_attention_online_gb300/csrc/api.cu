@@ -385,7 +385,7 @@ extern "C" attn_status attn_skip_santa_decode(const void *q, const void *k, cons
   if (n_samples > 2048 || n_tiles > 1024 || bps > 16 || (long)B * Hkv * n_tiles > 0x7fffffffL ||
       (long)B * Hq > 0x7fffffffL)
     return ATTN_EUNSUPPORTED;
-  if (santa_sample_smem_bytes(n_tiles, n_samples, (int)bps) > 200 * 1024) return ATTN_EUNSUPPORTED;
+  if (santa_sample_smem_bytes(n_tiles, n_samples) > 200 * 1024) return ATTN_EUNSUPPORTED;
   SantaArgs a{};
   a.q = q; a.k = k; a.v = v; a.u = u; a.scores = scores; a.tile_stats = tile_stats;
   a.o = o; a.idx = idx;

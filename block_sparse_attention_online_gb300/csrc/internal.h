@@ -100,6 +100,6 @@ cudaError_t launch_decode_nvfp4(const DecodeArgs &a, cudaStream_t s);
 cudaError_t launch_combine(const CombineArgs &a, cudaStream_t s);
 cudaError_t launch_selftest_wait(unsigned *err, cudaStream_t s);
 cudaError_t launch_santa_decode(const SantaArgs &a, cudaStream_t s);
-size_t santa_sample_smem_bytes(int n_tiles, int S, int bps);
+size_t santa_sample_smem_bytes(int n_tiles, int S);
 
 }  // namespace attn_skip

@@ -290,24 +290,77 @@ __device__ __forceinline__ int first_above(int n, float r, bool strict, F at) {
 //   P[n_tiles + 1]        CDF at the tile boundaries (unnormalised)
 //   rr[S], tile_of[S]     each sample's tile and its offset inside the tile
 //   idx_s[S]              sample indices
-//   cdf[NW2][32 (c+1) + 64]  per warp: running sums of a tile (lane chunk l
-//                         at l (c + 1)), chunk starts and ends
+//   cdf[NW2][64]          per warp: the chunk starts and ends of a tile
 //   red[NW2][D]           per-warp partial sums of the gathered rows
-__host__ __device__ inline size_t sample_smem_floats(int n_tiles, int S, int c) {
-  return (size_t)(n_tiles + 1) + 3 * (size_t)S + (size_t)NW2 * (32 * (c + 1) + 64) +
-         (size_t)NW2 * D;
+// A few KB: several CTAs share an SM, so the (sequence, head) CTAs run in
+// one wave.
+__host__ __device__ inline size_t sample_smem_floats(int n_tiles, int S) {
+  return (size_t)(n_tiles + 1) + 3 * (size_t)S + (size_t)NW2 * 64 + (size_t)NW2 * D;
 }
 
-__global__ void __launch_bounds__(NT2) santa_sample_kernel(const SantaArgs a) {
+// Running sum of exp2(x - M) over the keys of one lane chunk (consecutive
+// stash entries, a multiple of 4), added in key order.  The chunk totals and
+// the per-sample search below take the same sums in the same order, so a
+// sample's key follows the chunk ends exactly.
+constexpr int kChunkLoads = 4;  // float4 loads in flight per lane (16 keys)
+
+__device__ __forceinline__ float chunk_total(const float *src, int cl, float M) {
+  float run = 0.f;
+  for (int i0 = 0; i0 < cl; i0 += 4 * kChunkLoads) {
+    float4 x[kChunkLoads];
+#pragma unroll
+    for (int q = 0; q < kChunkLoads; ++q)
+      if (i0 + 4 * q < cl) x[q] = __ldg(reinterpret_cast<const float4 *>(src + i0 + 4 * q));
+#pragma unroll
+    for (int q = 0; q < kChunkLoads; ++q) {
+      if (i0 + 4 * q < cl) {
+        run += ex2(x[q].x - M);
+        run += ex2(x[q].y - M);
+        run += ex2(x[q].z - M);
+        run += ex2(x[q].w - M);
+      }
+    }
+  }
+  return run;
+}
+
+// First key i of the chunk whose running sum, offset by `pl`, exceeds `r`
+// (strict) or reaches it; cl when none.  Straight-line: the sums run to the
+// end of each group of loads and the first hit is kept.
+__device__ __forceinline__ int chunk_first_above(const float *src, int cl, float M, float pl,
+                                                 float r, bool strict) {
+  float run = 0.f;
+  int found = cl;
+  for (int i0 = 0; i0 < cl && found == cl; i0 += 4 * kChunkLoads) {
+    float4 x[kChunkLoads];
+#pragma unroll
+    for (int q = 0; q < kChunkLoads; ++q)
+      if (i0 + 4 * q < cl) x[q] = __ldg(reinterpret_cast<const float4 *>(src + i0 + 4 * q));
+#pragma unroll
+    for (int q = 0; q < kChunkLoads; ++q) {
+      if (i0 + 4 * q < cl) {
+        const float e[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          run += ex2(e[u] - M);
+          const float v = pl + run;
+          if (found == cl && (strict ? (v > r) : (v >= r))) found = i0 + 4 * q + u;
+        }
+      }
+    }
+  }
+  return found;
+}
+
+__global__ void __launch_bounds__(NT2, 4) santa_sample_kernel(const SantaArgs a) {
   extern __shared__ float sm[];
   const int T = a.n_tiles, S = a.S;
-  const int c = a.bps * (BC / 32);  // keys per lane chunk of the longest tile
   float *P = sm;
   float *rr = P + T + 1;
   int *tile_of = reinterpret_cast<int *>(rr + S);
   int *idx_s = tile_of + S;
   float *cdf_all = reinterpret_cast<float *>(idx_s + S);
-  float *red = cdf_all + (size_t)NW2 * (32 * (c + 1) + 64);
+  float *red = cdf_all + (size_t)NW2 * 64;
   __shared__ float sh_M, sh_Z;
   __shared__ int sh_tlast;
 
@@ -377,11 +430,13 @@ __global__ void __launch_bounds__(NT2) santa_sample_kernel(const SantaArgs a) {
   }
   __syncthreads();
 
-  // ---- 3. per tile holding samples: running sums and each sample's key -----
+  // ---- 3. per tile holding samples: chunk sums and each sample's key ------
+  // Lane l of the tile's warp owns a chunk of cl consecutive keys: the chunk
+  // totals and their prefix over the lanes locate a sample's chunk; the
+  // sample's lane then walks that chunk's running sum to its key.
   {
-    float *cw = cdf_all + (size_t)warp * (32 * (c + 1) + 64);
-    float *pre = cw + 32 * (c + 1);  // chunk starts
-    float *ends = pre + 32;          // chunk ends
+    float *pre = cdf_all + (size_t)warp * 64;  // chunk starts
+    float *ends = pre + 32;                    // chunk ends
     const size_t row = (size_t)a.n_b * BC;
     for (int t = warp; t < T; t += NW2) {
       const int mlo = first_above(S, (float)t, false, [&](int i) { return (float)tile_of[i]; });
@@ -391,20 +446,8 @@ __global__ void __launch_bounds__(NT2) santa_sample_kernel(const SantaArgs a) {
       const int k0 = jb0 * BC;
       const int cl = (jb1 - jb0) * (BC / 32);  // keys per lane in this tile (multiple of 4)
       if (cl == 0) continue;  // a tile with no key gets no sample unless the weights are NaN
-      const float *src = a.scores + (size_t)bh * row + k0 + (size_t)lane * cl;
-      float *mine = cw + lane * (c + 1);
-      float run = 0.f;
-      for (int i = 0; i < cl; i += 4) {
-        const float4 x4 = __ldg(reinterpret_cast<const float4 *>(src + i));
-        run += ex2(x4.x - M);
-        mine[i] = run;
-        run += ex2(x4.y - M);
-        mine[i + 1] = run;
-        run += ex2(x4.z - M);
-        mine[i + 2] = run;
-        run += ex2(x4.w - M);
-        mine[i + 3] = run;
-      }
+      const float *tile_src = a.scores + (size_t)bh * row + k0;
+      const float run = chunk_total(tile_src + (size_t)lane * cl, cl, M);
       float incl = run;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -429,9 +472,7 @@ __global__ void __launch_bounds__(NT2) santa_sample_kernel(const SantaArgs a) {
           l = first_above(32, r, false, [&](int i) { return ends[i]; });
           if (l == 32) l = 31;
         }
-        const float pl = pre[l];
-        const float *ch = cw + l * (c + 1);
-        int ii = first_above(cl, r, strict, [&](int i) { return pl + ch[i]; });
+        int ii = chunk_first_above(tile_src + (size_t)l * cl, cl, M, pre[l], r, strict);
         if (ii >= cl) ii = cl - 1;
         idx_s[m] = max(0, min(k0 + l * cl + ii, a.L - 1));
       }
@@ -442,17 +483,28 @@ __global__ void __launch_bounds__(NT2) santa_sample_kernel(const SantaArgs a) {
 
   // ---- 4. gather the sampled value rows ---------------------------------------
   const __nv_bfloat16 *vb = (const __nv_bfloat16 *)a.v + (size_t)(b * a.Hkv + hk) * a.L * D;
+  // Up to kGather rows in flight per warp; added in sample order.
+  constexpr int kGather = 8;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-  for (int m = warp; m < S; m += NW2) {
-    const int J = idx_s[m];
-    const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(vb + (size_t)J * D + lane * 4));
-    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
-    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
-    acc[0] += lo.x;
-    acc[1] += lo.y;
-    acc[2] += hi.x;
-    acc[3] += hi.y;
+  for (int m0 = warp; m0 < S; m0 += NW2 * kGather) {
+    uint2 raw[kGather];
+#pragma unroll
+    for (int q = 0; q < kGather; ++q) {
+      const int m = m0 + q * NW2;
+      if (m < S)
+        raw[q] = __ldg(reinterpret_cast<const uint2 *>(vb + (size_t)idx_s[m] * D + lane * 4));
+    }
+#pragma unroll
+    for (int q = 0; q < kGather; ++q) {
+      if (m0 + q * NW2 < S) {
+        const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw[q].x));
+        const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw[q].y));
+        acc[0] += lo.x;
+        acc[1] += lo.y;
+        acc[2] += hi.x;
+        acc[3] += hi.y;
+      }
+    }
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) red[warp * D + lane * 4 + i] = acc[i];
@@ -473,8 +525,8 @@ __global__ void __launch_bounds__(NT2) santa_sample_kernel(const SantaArgs a) {
 
 }  // namespace
 
-size_t santa_sample_smem_bytes(int n_tiles, int S, int bps) {
-  return sample_smem_floats(n_tiles, S, bps * (BC / 32)) * sizeof(float);
+size_t santa_sample_smem_bytes(int n_tiles, int S) {
+  return sample_smem_floats(n_tiles, S) * sizeof(float);
 }
 
 cudaError_t launch_santa_decode(const SantaArgs &a, cudaStream_t s) {
@@ -495,7 +547,7 @@ cudaError_t launch_santa_decode(const SantaArgs &a, cudaStream_t s) {
   k1<<<(unsigned)units, NT1, SMEM1, s>>>(mk, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t smem2 = santa_sample_smem_bytes(a.n_tiles, a.S, a.bps);
+  const size_t smem2 = santa_sample_smem_bytes(a.n_tiles, a.S);
   e = cudaFuncSetAttribute(santa_sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem2);
   if (e != cudaSuccess) return e;
