@@ -35,7 +35,8 @@
 //   warps 0-3   scores: thread = key 32w + lane of the block (TMEM lane);
 //               maxima, votes, decision, exponentials, P^T, row sums, O^T
 //               rescale, epilogue (thread = value dimension d);
-//   warp 4      TMA producer of the E4M3 key tiles (every block, 7 stages);
+//   warp 4      TMA producer of the E4M3 key tiles (every block; three stages
+//               of two tiles);
 //   warp 5      S^T issuer (allocates TMEM);
 //   warp 6      TMA producer of the E4M3 value tiles of kept blocks;
 //   warp 7      O^T issuer;
@@ -43,8 +44,10 @@
 // The decision ring holds 32 decisions and there are three P^T buffers, so
 // the score warps run ahead of the value loads and their widening by up to
 // three kept blocks; the value pipeline (load, widen, product) drains behind
-// them.  Seven key stages (112 KB) keep enough bytes in flight to cover the
-// load latency under a full GPU's traffic (~2.8 us measured).
+// them.  Six key tiles (96 KB) keep enough bytes in flight to cover the load
+// latency under a full GPU's traffic (~2.8 us measured); three E4M3 value
+// stages give a kept block's value load the same lead when most blocks are
+// kept.
 // TMEM columns: S^T buffers [0,128) (32 each: the hi part, then the lo part), O^T
 // [128,144).
 #include <cuda.h>
@@ -65,7 +68,7 @@ constexpr int D = 128;    // head size (keys and values)
 constexpr int BC = 128;   // keys per block (MMA rows of S^T)
 constexpr int NQ = 16;    // MMA columns: query heads, padded
 constexpr int NKP = 3;    // E4M3 key stages of two blocks each (one barrier per pair)
-constexpr int NVF = 2;    // E4M3 value stages
+constexpr int NVF = 3;    // E4M3 value stages
 constexpr int NVH = 2;    // fp16 value stages
 constexpr int NS = 4;     // TMEM S^T buffers (two pairs)
 constexpr int NPT = 3;    // P^T buffers
