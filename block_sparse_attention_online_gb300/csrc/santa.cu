@@ -291,20 +291,26 @@ __device__ __forceinline__ int first_above(int n, float r, bool strict, F at) {
 //   rr[S], tile_of[S]     each sample's tile and its offset inside the tile
 //   idx_s[S]              sample indices
 //   cdf[NW2][64]          per warp: the chunk starts and ends of a tile
+//   grp[NW2][32][4]       per warp and lane: running sums at the 16-key group ends
 //   red[NW2][D]           per-warp partial sums of the gathered rows
 // A few KB: several CTAs share an SM, so the (sequence, head) CTAs run in
 // one wave.
 __host__ __device__ inline size_t sample_smem_floats(int n_tiles, int S) {
-  return (size_t)(n_tiles + 1) + 3 * (size_t)S + (size_t)NW2 * 64 + (size_t)NW2 * D;
+  return (size_t)(n_tiles + 1) + 3 * (size_t)S + (size_t)NW2 * 64 + (size_t)NW2 * 32 * 4 +
+         (size_t)NW2 * D;
 }
 
 // Running sum of exp2(x - M) over the keys of one lane chunk (consecutive
-// stash entries, a multiple of 4), added in key order.  The chunk totals and
-// the per-sample search below take the same sums in the same order, so a
-// sample's key follows the chunk ends exactly.
-constexpr int kChunkLoads = 4;  // float4 loads in flight per lane (16 keys)
+// stash entries, a multiple of 4, at most kMaxChunk), added in key order;
+// the sum after every group of kGroup keys goes to grp[0..].  The search
+// below resumes from those group sums and adds the same terms in the same
+// order, so a sample's key follows the chunk and group ends exactly.
+constexpr int kGroup = 16;                      // keys per group (4 float4 loads)
+constexpr int kMaxChunk = 64;                   // keys per lane chunk at most (16 blocks a tile)
+constexpr int kGroups = kMaxChunk / kGroup;     // group sums per lane
+constexpr int kChunkLoads = 4;                  // float4 loads in flight per lane (16 keys)
 
-__device__ __forceinline__ float chunk_total(const float *src, int cl, float M) {
+__device__ __forceinline__ float chunk_total(const float *src, int cl, float M, float *grp) {
   float run = 0.f;
   for (int i0 = 0; i0 < cl; i0 += 4 * kChunkLoads) {
     float4 x[kChunkLoads];
@@ -318,6 +324,8 @@ __device__ __forceinline__ float chunk_total(const float *src, int cl, float M) 
         run += ex2(x[q].y - M);
         run += ex2(x[q].z - M);
         run += ex2(x[q].w - M);
+        if (((i0 + 4 * q + 4) % kGroup) == 0 || i0 + 4 * q + 4 == cl)
+          grp[(i0 + 4 * q) / kGroup] = run;
       }
     }
   }
@@ -325,27 +333,30 @@ __device__ __forceinline__ float chunk_total(const float *src, int cl, float M) 
 }
 
 // First key i of the chunk whose running sum, offset by `pl`, exceeds `r`
-// (strict) or reaches it; cl when none.  Straight-line: the sums run to the
-// end of each group of loads and the first hit is kept.
+// (strict) or reaches it; cl when none.  The group sums `grp` of the chunk
+// pick the group; only its (at most kGroup) keys are read again.
 __device__ __forceinline__ int chunk_first_above(const float *src, int cl, float M, float pl,
-                                                 float r, bool strict) {
-  float run = 0.f;
+                                                 float r, bool strict, const float *grp) {
+  const int ng = (cl + kGroup - 1) / kGroup;
+  int g = 0;
+  while (g < ng && !(strict ? (pl + grp[g] > r) : (pl + grp[g] >= r))) ++g;
+  if (g == ng) return cl;
+  const int i0 = g * kGroup;
+  float run = g > 0 ? grp[g - 1] : 0.f;
+  float4 x[kGroup / 4];
+#pragma unroll
+  for (int q = 0; q < kGroup / 4; ++q)
+    if (i0 + 4 * q < cl) x[q] = __ldg(reinterpret_cast<const float4 *>(src + i0 + 4 * q));
   int found = cl;
-  for (int i0 = 0; i0 < cl && found == cl; i0 += 4 * kChunkLoads) {
-    float4 x[kChunkLoads];
 #pragma unroll
-    for (int q = 0; q < kChunkLoads; ++q)
-      if (i0 + 4 * q < cl) x[q] = __ldg(reinterpret_cast<const float4 *>(src + i0 + 4 * q));
+  for (int q = 0; q < kGroup / 4; ++q) {
+    if (i0 + 4 * q < cl) {
+      const float e[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
 #pragma unroll
-    for (int q = 0; q < kChunkLoads; ++q) {
-      if (i0 + 4 * q < cl) {
-        const float e[4] = {x[q].x, x[q].y, x[q].z, x[q].w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          run += ex2(e[u] - M);
-          const float v = pl + run;
-          if (found == cl && (strict ? (v > r) : (v >= r))) found = i0 + 4 * q + u;
-        }
+      for (int u = 0; u < 4; ++u) {
+        run += ex2(e[u] - M);
+        const float v = pl + run;
+        if (found == cl && (strict ? (v > r) : (v >= r))) found = i0 + 4 * q + u;
       }
     }
   }
@@ -360,7 +371,8 @@ __global__ void __launch_bounds__(NT2, 4) santa_sample_kernel(const SantaArgs a)
   int *tile_of = reinterpret_cast<int *>(rr + S);
   int *idx_s = tile_of + S;
   float *cdf_all = reinterpret_cast<float *>(idx_s + S);
-  float *red = cdf_all + (size_t)NW2 * 64;
+  float *grp_all = cdf_all + (size_t)NW2 * 64;
+  float *red = grp_all + (size_t)NW2 * 32 * kGroups;
   __shared__ float sh_M, sh_Z;
   __shared__ int sh_tlast;
 
@@ -437,6 +449,7 @@ __global__ void __launch_bounds__(NT2, 4) santa_sample_kernel(const SantaArgs a)
   {
     float *pre = cdf_all + (size_t)warp * 64;  // chunk starts
     float *ends = pre + 32;                    // chunk ends
+    float *grp = grp_all + (size_t)warp * 32 * kGroups;  // [lane][group] running sums
     const size_t row = (size_t)a.n_b * BC;
     for (int t = warp; t < T; t += NW2) {
       const int mlo = first_above(S, (float)t, false, [&](int i) { return (float)tile_of[i]; });
@@ -447,7 +460,7 @@ __global__ void __launch_bounds__(NT2, 4) santa_sample_kernel(const SantaArgs a)
       const int cl = (jb1 - jb0) * (BC / 32);  // keys per lane in this tile (multiple of 4)
       if (cl == 0) continue;  // a tile with no key gets no sample unless the weights are NaN
       const float *tile_src = a.scores + (size_t)bh * row + k0;
-      const float run = chunk_total(tile_src + (size_t)lane * cl, cl, M);
+      const float run = chunk_total(tile_src + (size_t)lane * cl, cl, M, grp + lane * kGroups);
       float incl = run;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -472,7 +485,8 @@ __global__ void __launch_bounds__(NT2, 4) santa_sample_kernel(const SantaArgs a)
           l = first_above(32, r, false, [&](int i) { return ends[i]; });
           if (l == 32) l = 31;
         }
-        int ii = chunk_first_above(tile_src + (size_t)l * cl, cl, M, pre[l], r, strict);
+        int ii = chunk_first_above(tile_src + (size_t)l * cl, cl, M, pre[l], r, strict,
+                                   grp + l * kGroups);
         if (ii >= cl) ii = cl - 1;
         idx_s[m] = max(0, min(k0 + l * cl + ii, a.L - 1));
       }
