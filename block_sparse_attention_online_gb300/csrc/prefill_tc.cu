@@ -60,14 +60,17 @@ constexpr int NK = 4;         // K stages
 constexpr int NV = 2;         // V stages
 constexpr int NS = 3;         // TMEM S buffers
 constexpr int NDEC = 4;       // decision ring
-// Blocks whose S buffers go back to one issuer's s_free set: b % NS and the
-// issuer parity (b + NS) & 1 repeat every kFreePeriod blocks.
-constexpr int kFreePeriod = (NS % 2) ? 2 * NS : NS;
-// The two Q.K^T issuers take alternate blocks; with an even K stage count
-// every stage belongs to one issuer, whose waits on its k_full phases then
-// come in load order (with an odd count, a wait could find the stage's
-// previous load, the other issuer's block, still in flight and pass early).
-static_assert(NK % 2 == 0, "K stages: an even count (one issuer per stage)");
+// Block c may be issued once one barrier, slot c % NK of the "ready" ring,
+// has completed: its key tile has landed (the producer's arrival with the
+// byte count) and its S buffer is free (the decision of block c - NS if that
+// block was skipped, its P.V commit if kept; the first NS blocks' buffers are
+// free from the start).  One wait per block: a wait or a memory operation of
+// the issuing thread between two product batches stalls the tensor pipe for
+// about 100-250 cycles.  The two Q.K^T issuers take alternate blocks, so with
+// an even ring every slot belongs to one issuer and its phases come in that
+// issuer's order; a slot's next "free" arrival (block c + NK's, made at block
+// c + NK - NS's decision) cannot come before block c was issued, as NK > NS.
+static_assert(NK % 2 == 0 && NK > NS, "ready ring: even, and longer than the S buffer ring");
 constexpr int NQ = 4;     // decider warps (0-3) and exponential warps (4-7): one per TMEM lane quarter
 constexpr int NSOFT = 2 * NQ;
 constexpr int kDeciderBarrier = 1;  // named barrier of the four decider warps
@@ -102,16 +105,9 @@ struct VarTile {
 
 struct Shared {
   uint64_t q_full;
-  uint64_t k_full[NK], k_empty[NK];
+  uint64_t ready[NK];    // slot c % NK: block c's key tile landed and its S buffer free
+  uint64_t qk_done[NK];  // slot c % NK: block c's Q.K^T complete (scores in, key stage free)
   uint64_t v_full[NV], v_empty[NV];
-  uint64_t s_full[NS];
-  // S buffer of block b free again (its decision if skipped, its P.V commit if
-  // kept), for the issuer of block b + NS, one barrier set per issuer.  Block
-  // b + NS is the other issuer's (NS is odd), so with one shared set an
-  // issuer could wait for the phase of block b while the phase of block
-  // b - NS (the other issuer's business) was still pending, and a parity wait
-  // would pass at once.  Per issuer the phases follow that issuer's own order.
-  uint64_t s_free[2][NS];
   // P of kept block kc ready, slot kc % NS.  Kept blocks whose P exists but
   // whose P.V has not completed each hold an S buffer, so at most NS are
   // outstanding and a slot is never re-armed before its phase was consumed
@@ -414,20 +410,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   if (tid == 0) {
     mbar_init(smem_u32(&sh.q_full), 1);
     for (int i = 0; i < NK; ++i) {
-      mbar_init(smem_u32(&sh.k_full[i]), 1);
-      mbar_init(smem_u32(&sh.k_empty[i]), 1);
+      mbar_init(smem_u32(&sh.ready[i]), 2);  // the key tile (arrival + bytes), the S buffer
+      mbar_init(smem_u32(&sh.qk_done[i]), 1);
     }
+    for (int i = 0; i < NS; ++i) mbar_arrive(smem_u32(&sh.ready[i]));  // buffers free at first
     for (int i = 0; i < NV; ++i) {
       mbar_init(smem_u32(&sh.v_full[i]), 1);
       mbar_init(smem_u32(&sh.v_empty[i]), 1);
     }
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(smem_u32(&sh.s_full[i]), 1);
-      // once per block: the decision of a skipped block, the P.V commit of a kept one
-      mbar_init(smem_u32(&sh.s_free[0][i]), 1);
-      mbar_init(smem_u32(&sh.s_free[1][i]), 1);
-      mbar_init(smem_u32(&sh.p_full[i]), NQ);
-    }
+    for (int i = 0; i < NS; ++i) mbar_init(smem_u32(&sh.p_full[i]), NQ);
     for (int i = 0; i < NS; ++i) {
       mbar_init(smem_u32(&sh.pv_done[i]), 1);
     }
@@ -505,22 +496,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const int c = SET ? cc++ : j;
         const int s = c % NK;
+        // Stage s last held block c - NK, whose Q.K^T has completed.
         if (c >= NK &&
-            !mbar_wait(smem_u32(&sh.k_empty[s]), ((c / NK) - 1) & 1, abort, a.err, kErrTimeout))
+            !mbar_wait(smem_u32(&sh.qk_done[s]), ((c / NK) - 1) & 1, abort, a.err, kErrTimeout))
           break;
         const uint32_t dst = base + SMEM_K + s * TILE_BYTES;
-        mbar_expect_tx(smem_u32(&sh.k_full[s]), TILE_BYTES);
-        tma_load_3d(dst, &tm_k, smem_u32(&sh.k_full[s]), 0, kv_y(j), kv_z(j), keep_l2);
-        tma_load_3d(dst + HALF_BYTES, &tm_k, smem_u32(&sh.k_full[s]), 64, kv_y(j), kv_z(j),
+        mbar_expect_tx(smem_u32(&sh.ready[s]), TILE_BYTES);
+        tma_load_3d(dst, &tm_k, smem_u32(&sh.ready[s]), 0, kv_y(j), kv_z(j), keep_l2);
+        tma_load_3d(dst + HALF_BYTES, &tm_k, smem_u32(&sh.ready[s]), 64, kv_y(j), kv_z(j),
                     keep_l2);
         ++ki;
       }
       // Drain: the last load issued into each slot has landed before exit
-      // (earlier loads of a slot were consumed before the slot was reused).
+      // (earlier loads of a slot were consumed before the slot was reused;
+      // the slot's phase also waits for its S buffer, freed by every decided
+      // block, so this wait is only long after a failed wait elsewhere).
       mbar_wait_drain(smem_u32(&sh.q_full), 0);
       for (int s = 0; s < NK && s < ki; ++s) {
         const int last = s + ((ki - 1 - s) / NK) * NK;
-        mbar_wait_drain(smem_u32(&sh.k_full[s]), (last / NK) & 1);
+        mbar_wait_drain(smem_u32(&sh.ready[s]), (last / NK) & 1);
       }
     }
   } else if (warp == WARP_V) {
@@ -573,13 +567,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int c = SET ? cc++ : j;
         if ((c & 1) != mine) continue;
         const int s = c % NK, sb = c % NS;
-        if (!mbar_wait_warp(smem_u32(&sh.k_full[s]), (c / NK) & 1, abort, a.err, kErrTimeout)) break;
-        // S buffer sb last held block c - NS: free once that block was
-        // decided (skipped) or its P.V completed (kept); in this issuer's set
-        // one phase per such block, in this issuer's order.
-        if (c >= NS && !mbar_wait_warp(smem_u32(&sh.s_free[c & 1][sb]),
-                                       ((c - NS) / kFreePeriod) & 1, abort, a.err, kErrTimeout))
-          break;
+        // Key tile landed and S buffer sb (last: block c - NS) free.
+        if (!mbar_wait_warp(smem_u32(&sh.ready[s]), (c / NK) & 1, abort, a.err, kErrTimeout)) break;
         fence_after_sync();
         if (lane == 0) {
           const uint64_t kd = kmajor_base(base + SMEM_K + s * TILE_BYTES);
@@ -587,8 +576,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk)
             mma_bf16_ss(d_s, qdesc + kmajor_step(kk), kd + kmajor_step(kk), IDESC_QK, kk > 0);
-          mma_commit(smem_u32(&sh.s_full[sb]));
-          mma_commit(smem_u32(&sh.k_empty[s]));
+          mma_commit(smem_u32(&sh.qk_done[s]));
         }
         __syncwarp();
       }
@@ -623,7 +611,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_bf16_ts(d_o, pt + kk * 8, vd + vmajor_step(kk), IDESC_PV, kk > 0 ? 1u : acc0);
         mma_commit(smem_u32(&sh.v_empty[vs]));
-        mma_commit(smem_u32(&sh.s_free[(i + NS) & 1][i % NS]));
+        mma_commit(smem_u32(&sh.ready[(i + NS) % NK]));  // S buffer free for block i + NS
         mma_commit(smem_u32(&sh.pv_done[pb]));
         ++kc;
         ++vi;
@@ -665,7 +653,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // Once a wait has failed (the abort flag is up and every later wait
         // fails at once) the loop still runs to its end, so that the four
         // warps meet the vote barrier equally often.
-        if (ok) ok = mbar_wait_warp(smem_u32(&sh.s_full[sb]), (c / NS) & 1, abort, a.err, kErrTimeout);
+        if (ok) ok = mbar_wait_warp(smem_u32(&sh.qk_done[c % NK]), (c / NK) & 1, abort, a.err, kErrTimeout);
         bool keep_vote = false;  // warp-uniform: some row of this warp keeps the block
         float mnew = m2;
         if (ok) {
@@ -718,7 +706,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // A skipped block's S buffer is free: every decider has read it
           // (the vote barrier above) and nothing else will.  Released first:
           // the next Q.K^T into this buffer waits for it.
-          if (skip) mbar_arrive(smem_u32(&sh.s_free[(c + NS) & 1][sb]));
+          if (skip) mbar_arrive(smem_u32(&sh.ready[(c + NS) % NK]));
           if (c < NDEC || mbar_wait(smem_u32(&sh.dec_read[c % NDEC]), ((c / NDEC) - 1) & 1,
                                     abort, a.err, kErrTimeout)) {
             sh.dec[c % NDEC] = skip ? 0 : 1;

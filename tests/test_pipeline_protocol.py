@@ -43,9 +43,15 @@ class ProtocolError(AssertionError):
     pass
 
 
-def simulate(nblk, keep, rescale, seed, NK=4, NV=2, NS=3, NDEC=4, split_free=True,
-             pv_slots=None):
-    """Run one CTA's protocol once; raises ProtocolError on any violation."""
+def simulate(nblk, keep, rescale, seed, NK=4, NV=2, NS=3, NDEC=4, pv_slots=None):
+    """Run one CTA's protocol once; raises ProtocolError on any violation.
+
+    Block c is issued after one wait, on slot c % NK of the "ready" ring (two
+    arrivals: the key producer's, with the tile's bytes, and the S buffer's
+    release by block c - NS: its decision if skipped, its P.V commit if kept;
+    the first NS slots get the release at set-up).  Slot c % NK of "qk_done"
+    is block c's Q.K^T commit: the deciders' scores and the key stage's
+    release in one."""
     rng = random.Random(seed)
     pv_slots = NS if pv_slots is None else pv_slots
     B = {}
@@ -55,26 +61,21 @@ def simulate(nblk, keep, rescale, seed, NK=4, NV=2, NS=3, NDEC=4, split_free=Tru
 
     bar("q_full")
     for i in range(NK):
-        bar(("k_full", i)), bar(("k_empty", i))
+        bar(("ready", i), 2), bar(("qk_done", i))
+    for i in range(NS):
+        B[("ready", i % NK)].arrive()  # S buffers free at set-up
     for i in range(NV):
         bar(("v_full", i)), bar(("v_empty", i))
     for i in range(NS):
-        bar(("s_full", i)), bar(("p_full", i))
-        for p in range(2 if split_free else 1):
-            bar(("s_free", p, i))
+        bar(("p_full", i))
     for i in range(pv_slots):
         bar(("pv_done", i))
     for i in range(NDEC):
         bar(("dec_full", i)), bar(("dec_read", i), 3)  # V producer, P.V issuer, exponential warps
     bar("l_full")
 
-    period = (2 * NS) if NS % 2 else NS
-
-    def free_bar(b):  # the "S buffer free" barrier the next user of block b's buffer waits on
-        return ("s_free", (b + NS) & 1, b % NS) if split_free else ("s_free", 0, b % NS)
-
-    def free_phase(c):  # phase the issuer of block c >= NS waits for
-        return (c - NS) // period if split_free else c // NS - 1
+    def free_bar(b):  # the slot that block b's S buffer release goes to: block b + NS's
+        return ("ready", (b + NS) % NK)
 
     kstage = [None] * NK    # block whose keys a K stage holds (None: loading / empty)
     vstage = [None] * NV
@@ -106,13 +107,13 @@ def simulate(nblk, keep, rescale, seed, NK=4, NV=2, NS=3, NDEC=4, split_free=Tru
         for c in range(nblk):
             s = c % NK
             if c >= NK:
-                yield ("wait", ("k_empty", s), c // NK - 1)
+                yield ("wait", ("qk_done", s), c // NK - 1)
             kstage[s] = None
-            B[("k_full", s)].arrive(tx=1)
+            B[("ready", s)].arrive(tx=1)
 
             def land(s=s, c=c):
                 kstage[s] = c
-                B[("k_full", s)].complete_tx(1)
+                B[("ready", s)].complete_tx(1)
             tma.append(land)
             yield None
 
@@ -120,9 +121,7 @@ def simulate(nblk, keep, rescale, seed, NK=4, NV=2, NS=3, NDEC=4, split_free=Tru
         yield ("wait", "q_full", 0)
         for c in range(par, nblk, 2):
             s, sb = c % NK, c % NS
-            yield ("wait", ("k_full", s), c // NK)
-            if c >= NS:
-                yield ("wait", free_bar(c - NS), free_phase(c))
+            yield ("wait", ("ready", s), c // NK)
             expect(kstage[s] == c, f"Q.K^T of block {c} reads K stage {s} holding {kstage[s]}")
             expect(sbuf[sb] is None, f"Q.K^T of block {c} overwrites S buffer {sb} "
                                      f"still holding block {sbuf[sb]}")
@@ -130,15 +129,14 @@ def simulate(nblk, keep, rescale, seed, NK=4, NV=2, NS=3, NDEC=4, split_free=Tru
 
             def done(c=c, s=s, sb=sb):
                 sbuf[sb] = c
-                B[("s_full", sb)].arrive()
-                B[("k_empty", s)].arrive()
+                B[("qk_done", s)].arrive()
             pipe.append(done)
             yield None
 
     def deciders():
         for c in range(nblk):
             sb = c % NS
-            yield ("wait", ("s_full", sb), c // NS)
+            yield ("wait", ("qk_done", c % NK), c // NK)
             expect(sbuf[sb] == c, f"deciders read S buffer {sb} for block {c}: {sbuf[sb]}")
             k = keep[c]
             if not k:
@@ -256,20 +254,22 @@ def _run_many(n_runs, nblk=14, **kw):
         simulate(nblk, keep, rescale, seed=run, **kw)
 
 
-@pytest.mark.parametrize("NK,NV", [(4, 2), (2, 4)])
+@pytest.mark.parametrize("NK,NV", [(4, 2), (6, 2), (8, 2)])
 def test_prefill_protocol_has_no_parity_race_or_deadlock(NK, NV):
-    """The shipped protocol (per-issuer "S buffer free" barriers, one P.V
-    completion slot per S buffer, an even K stage count) under random
-    interleavings, keep patterns and rescales."""
+    """The shipped protocol (one "ready" wait per block on an even ring longer
+    than the S buffer ring, one Q.K^T commit per block, one P.V completion
+    slot per S buffer) under random interleavings, keep patterns and
+    rescales."""
     _run_many(400, NK=NK, NV=NV)
 
 
-def test_model_catches_the_shared_free_barriers():
-    """Self-check of the model: one shared set of "S buffer free" barriers for
-    both Q.K^T issuers with 4 K stages lets an issuer's parity wait pass on the
-    other issuer's pending phase; the model must report it."""
+def test_model_catches_a_ready_ring_as_short_as_the_s_buffers():
+    """Self-check of the model: with a ready ring of 3 slots and 3 S buffers,
+    the release of block c's buffer (meant for block c + 3, the same slot)
+    can reach the slot while block c's own phase is still pending, and an
+    issuer's parity wait passes on it; the model must report it."""
     with pytest.raises(ProtocolError):
-        _run_many(400, NK=4, NV=2, split_free=False)
+        _run_many(400, nblk=20, NK=3, NV=2)
 
 
 def test_model_catches_two_pv_completion_slots():
@@ -277,12 +277,3 @@ def test_model_catches_two_pv_completion_slots():
     let the end-of-tile wait pass while products are still in flight."""
     with pytest.raises(ProtocolError):
         _run_many(400, NK=4, NV=2, pv_slots=2)
-
-
-def test_model_catches_an_odd_key_stage_count():
-    """Self-check of the model: with 3 K stages a stage serves both issuers in
-    turn; if an earlier key load lands late (TMA loads complete in any order)
-    an issuer's k_full wait can pass on the stage's virtual phase before its
-    first load landed."""
-    with pytest.raises(ProtocolError):
-        _run_many(400, NK=3, NV=3)
