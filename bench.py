@@ -48,8 +48,8 @@ CSRC = os.path.join(ROOT, "block_sparse_attention_online_gb300", "csrc")
 NCU_TRAFFIC = {
     "prefill_tc_kernel": {
         "file": "prefill_tc.cu",
-        "sha256": "0cf2a696cb1e5f8b42ef8ccf759c2abc68294d694a478262f4bceb24b94948f5",
-        "bytes": 233965568 + 82188288},
+        "sha256": "4d67b0e4355f331411c6447e7cac27300dcbaed8fb3347e5a882533b79c5d778",
+        "bytes": 235137280 + 82245632},
     "decode_tc_kernel": {
         "file": "decode.cu",
         "sha256": "67c9de81d8f8ee7ddce7a6299cee4da7e507f86994a81d430c15461053d8a9e0",
