@@ -22,7 +22,8 @@ ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ECUDA, ATTN_ETIMEOUT, ATTN_EINTERN
 ATTN_BF16, ATTN_F32 = 0, 1
 
 #: Every symbol include/attn_skip.h declares.
-EXPORTED = ("attn_skip_prefill", "attn_skip_prefill_blocks", "attn_skip_prefill_varlen",
+EXPORTED = ("attn_skip_prefill", "attn_skip_prefill_from_host", "attn_skip_prefill_blocks",
+            "attn_skip_prefill_varlen",
             "attn_skip_decode", "attn_skip_decode_fp8", "attn_skip_decode_nvfp4",
             "attn_skip_decode_per_head", "attn_skip_decode_combine",
             "attn_skip_prefill_margins", "attn_skip_decode_margins", "attn_skip_sparsity_at",
@@ -57,6 +58,8 @@ def load() -> ctypes.CDLL:
     lib = ctypes.CDLL(_LIB_PATH)
     P, i, f, d, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_int64
     lib.attn_skip_prefill.argtypes = [P, P, P, i, i, i, i, i, i, i, f, d, i, i, i, P, P, P, P]
+    lib.attn_skip_prefill_from_host.argtypes = [P, P, P, P, P, P, i, i, i, i, i, i, i, f, d, i, i,
+                                                i, P, P, P, P, P, i, P, P, P]
     lib.attn_skip_prefill_blocks.argtypes = [P, P, P, i, i, i, i, i, i, i, f, d, i, i, i, P, P, P,
                                              P, P]
     lib.attn_skip_prefill_varlen.argtypes = [P, P, P, i, i, P, i, i, i, i, i, i, f, P, i, i, i,
@@ -170,6 +173,36 @@ def attn_skip_prefill(q, k, v, lam, Br=128, Bc=128, causal=True, scale=0.0, out=
                                   _ptr(o), _ptr(lse), _ptr(bits), _stream(stream, q.device))
     _check("attn_skip_prefill", st)
     return o, lse, bits
+
+
+def attn_skip_prefill_from_host(q, k, v, lam, dev, out_host, Br=128, Bc=128, causal=True,
+                                scale=0.0, n_groups=0, stream=None, copy_streams=(None, None)):
+    """The prefill with host-resident inputs and outputs, the copies overlapped
+    with the computation over groups of KV heads.
+
+    ``q, k, v`` are CPU tensors (pinned for asynchronous copies) in the
+    layouts of :func:`attn_skip_prefill`; ``dev`` holds the device tensors
+    ``(q_dev, k_dev, v_dev, o_dev, lse_dev, skip_bits)``; ``out_host`` the CPU
+    tensors ``(o, lse)`` written once ``stream`` has reached the end of the
+    call.  ``copy_streams`` are the CUDA streams of the copies in and out
+    (None: ``stream``).  Returns ``out_host``."""
+    for x in (q, k, v, *out_host):
+        if x.is_cuda or not x.is_contiguous():
+            raise ValueError("host tensors must be contiguous CPU tensors")
+    qd, kd, vd, od, ld, bd = dev
+    _cuda_contig(qd, kd, vd, od, ld, bd)
+    B, Hq, T, dk = q.shape
+    Hkv, dv = k.shape[1], v.shape[3]
+    o, lse = out_host
+    cs = tuple(None if c is None else _stream(c, qd.device) for c in copy_streams)
+    st = load().attn_skip_prefill_from_host(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()), ctypes.c_void_p(v.data_ptr()),
+        _ptr(qd), _ptr(kd), _ptr(vd), _dtype_code(q), B, Hq, Hkv, T, dk, dv, float(scale),
+        float(lam), Br, Bc, int(bool(causal)), _ptr(od), _ptr(ld), _ptr(bd),
+        ctypes.c_void_p(o.data_ptr()), ctypes.c_void_p(lse.data_ptr()), int(n_groups),
+        _stream(stream, qd.device), cs[0], cs[1])
+    _check("attn_skip_prefill_from_host", st)
+    return out_host
 
 
 def pack_block_set(allow: torch.Tensor) -> torch.Tensor:

@@ -96,6 +96,44 @@ attn_status attn_skip_prefill(const void *q, const void *k, const void *v, attn_
                               uint32_t *skip_bits, void *stream);
 
 /*
+ * The same prefill with its inputs and outputs in host memory: Q, K, V are
+ * copied in and O, LSE copied back, overlapped with the computation.  The
+ * B * Hkv KV heads (flattened, batch-major) are split into n_groups
+ * contiguous groups; group g's copies in run on copy_in_stream while group
+ * g - 1 is computed on `stream` and group g - 2's results are copied back on
+ * copy_out_stream (each group is attn_skip_prefill on its own query heads and
+ * KV heads, so the results are bit-identical to one attn_skip_prefill call).
+ *
+ * Defines: as attn_skip_prefill; the pipelining is not on the pages (it moves
+ * data to and from the device, not any step of the method).
+ *
+ *  q_host, k_host, v_host  host, the layouts of q, k, v of attn_skip_prefill;
+ *                          page-locked memory lets the copies run
+ *                          asynchronously (pageable memory still works, the
+ *                          copies then stall the host)
+ *  q_dev, k_dev, v_dev     device staging of the same shapes, written
+ *  o_dev, lse_dev, skip_bits  device outputs as for attn_skip_prefill
+ *  o_host, lse_host        host outputs, same layouts as o, lse; written when
+ *                          `stream` has reached the end of the call's work
+ *  n_groups                1 .. B*Hkv (0 picks min(8, B*Hkv))
+ *  stream                  computation; the call's work (copies included) is
+ *                          complete when `stream` reaches the point of the call
+ *  copy_in_stream, copy_out_stream  streams of the two copy directions; NULL
+ *                          uses `stream` (no overlap in that direction).
+ * Every pointer is caller-owned.  The call creates 2 * n_groups + 1 CUDA
+ * events and releases them before it returns (their last records complete
+ * later, as CUDA allows).  Errors: those of attn_skip_prefill, EINVAL for a
+ * null host or staging pointer or n_groups out of range; argument errors are
+ * found before anything is enqueued.
+ */
+attn_status attn_skip_prefill_from_host(
+    const void *q_host, const void *k_host, const void *v_host, void *q_dev, void *k_dev,
+    void *v_dev, attn_dtype dt, int B, int Hq, int Hkv, int T, int dk, int dv, float scale,
+    double lambda, int Br, int Bc, int causal, void *o_dev, float *lse_dev, uint32_t *skip_bits,
+    void *o_host, float *lse_host, int n_groups, void *stream, void *copy_in_stream,
+    void *copy_out_stream);
+
+/*
  * Prefill restricted to an explicit block set per query tile, composed with
  * the threshold test: the consumer side of a block-selection stage such as the
  * SparDA page's InfLLM-V2 access set B_init u B_local u B_topk (section 2.1).

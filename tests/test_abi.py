@@ -57,6 +57,29 @@ def test_prefill_rejects_invalid_arguments(lib, kw):
     assert _prefill(lib, **kw) == bs.ATTN_EINVAL
 
 
+def _prefill_host(lib, **kw):
+    a = dict(qh=FAKE, kh=FAKE, vh=FAKE, qd=FAKE, kd=FAKE, vd=FAKE, dt=0, B=1, Hq=4, Hkv=2, T=256,
+             dk=128, dv=128, scale=0.0, lam=0.01, Br=128, Bc=128, causal=1, o=FAKE, lse=FAKE,
+             bits=FAKE, oh=FAKE, lh=FAKE, n_groups=2, stream=None, si=None, so=None)
+    a.update(kw)
+    return lib.attn_skip_prefill_from_host(*a.values())
+
+
+@pytest.mark.parametrize("kw", [
+    dict(qh=None), dict(vh=None), dict(oh=None), dict(lh=None), dict(qd=None), dict(o=None),
+    dict(bits=None), dict(n_groups=-1), dict(n_groups=3), dict(Hq=3), dict(lam=1.0),
+    dict(kd=ctypes.c_void_p(0x10004)),
+])
+def test_prefill_from_host_rejects_invalid_arguments(lib, kw):
+    """Argument errors are found before any copy or event (n_groups must lie
+    in 1 .. B * Hkv; here B * Hkv = 2)."""
+    assert _prefill_host(lib, **kw) == bs.ATTN_EINVAL
+
+
+def test_prefill_from_host_unsupported_shape(lib):
+    assert _prefill_host(lib, dk=64, dv=64) == bs.ATTN_EUNSUPPORTED
+
+
 def _decode(lib, **kw):
     a = dict(q=FAKE, k=FAKE, v=FAKE, dt=0, B=2, Hq=8, Hkv=2, L=1024, dk=128, dv=128, ks=128,
              vs=128, scale=0.0, lam=0.01, Bc=128, n=4, op=FAKE, lp=FAKE, bits=FAKE, stream=None)
