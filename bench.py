@@ -494,7 +494,7 @@ def santa_sweep(args, bs, dev, stream, flush):
     k_bytes = C.B * C.Hkv * C.L * C.dk * 2
     out = {"workload": f"{C.name}: B{C.B} Hq{C.Hq} Hkv{C.Hkv} d{C.dk} L{C.L}, sink 1.2, "
                        f"salient 0.6; S={S} samples per head, {n_tiles} key tiles"}
-    for mode in ("sys", "strat"):
+    for mode in ("sys", "strat", "iid"):
         u = W.santa_offsets(C, S, mode).to(dev)
 
         def step():

@@ -490,7 +490,7 @@ extern "C" attn_status attn_skip_santa_decode(const void *q, const void *k, cons
   const long n_b = (L + 127L) / 128;
   const long bps = (n_b + n_tiles - 1) / n_tiles;
   if (dt != ATTN_BF16 || dk != 128 || dv != 128 || k_row_stride != 128 || v_row_stride != 128 ||
-      !(G == 1 || G == 2 || G == 4 || G == 8) || mode == ATTN_SANTA_IID)
+      !(G == 1 || G == 2 || G == 4 || G == 8))
     return ATTN_EUNSUPPORTED;
   if (n_samples > 2048 || n_tiles > 1024 || bps > 16 || (long)B * Hkv * n_tiles > 0x7fffffffL ||
       (long)B * Hq > 0x7fffffffL)

@@ -293,11 +293,18 @@ __device__ __forceinline__ int first_above(int n, float r, bool strict, F at) {
 //   cdf[NW2][64]          per warp: the chunk starts and ends of a tile
 //   grp[NW2][32][4]       per warp and lane: running sums at the 16-key group ends
 //   red[NW2][D]           per-warp partial sums of the gathered rows
+//   su[S2], sp[S2]        i.i.d. sampler: the draws sorted ascending and their
+//                         sample numbers (S2 = S rounded up to a power of two)
 // A few KB: several CTAs share an SM, so the (sequence, head) CTAs run in
 // one wave.
+__host__ __device__ inline int pow2_ceil(int S) {
+  int p = 1;
+  while (p < S) p <<= 1;
+  return p;
+}
 __host__ __device__ inline size_t sample_smem_floats(int n_tiles, int S) {
   return (size_t)(n_tiles + 1) + 3 * (size_t)S + (size_t)NW2 * 64 + (size_t)NW2 * 32 * 4 +
-         (size_t)NW2 * D;
+         (size_t)NW2 * D + 2 * (size_t)pow2_ceil(S);
 }
 
 // Running sum of exp2(x - M) over the keys of one lane chunk (consecutive
@@ -373,6 +380,8 @@ __global__ void __launch_bounds__(NT2, 4) santa_sample_kernel(const SantaArgs a)
   float *cdf_all = reinterpret_cast<float *>(idx_s + S);
   float *grp_all = cdf_all + (size_t)NW2 * 64;
   float *red = grp_all + (size_t)NW2 * 32 * kGroups;
+  float *su = red + (size_t)NW2 * D;
+  int *sp = reinterpret_cast<int *>(su + pow2_ceil(S));
   __shared__ float sh_M, sh_Z;
   __shared__ int sh_tlast;
 
@@ -425,10 +434,44 @@ __global__ void __launch_bounds__(NT2, 4) santa_sample_kernel(const SantaArgs a)
   const int tlast = sh_tlast;
 
   // ---- 2. the tile of each threshold: largest t with P[t] <= T_m Z ----------
+  // The steps below want the thresholds in ascending order (a tile's samples
+  // are a contiguous range): the systematic and stratified thresholds come in
+  // order; the i.i.d. draws are sorted first (bitonic, with their sample
+  // numbers, so that each index is reported at its own sample).
+  const bool iid = a.mode == kSantaIid;
+  if (iid) {
+    const int S2 = pow2_ceil(S);
+    for (int i = tid; i < S2; i += NT2) {
+      su[i] = i < S ? a.u[(size_t)bh * S + i] : INFINITY;
+      sp[i] = i;
+    }
+    __syncthreads();
+    for (int k2 = 2; k2 <= S2; k2 <<= 1) {
+      for (int j2 = k2 >> 1; j2 > 0; j2 >>= 1) {
+        for (int i = tid; i < S2; i += NT2) {
+          const int o = i ^ j2;
+          if (o > i && ((su[i] > su[o]) == ((i & k2) == 0))) {
+            const float tu = su[i];
+            su[i] = su[o];
+            su[o] = tu;
+            const int tp = sp[i];
+            sp[i] = sp[o];
+            sp[o] = tp;
+          }
+        }
+        __syncthreads();
+      }
+    }
+  }
   const float invS = 1.f / (float)S;
   for (int m = tid; m < S; m += NT2) {
-    const float um = a.mode == kSantaSys ? a.u[bh] : a.u[(size_t)bh * S + m];
-    const float R = ((float)m + um) * invS * Z;
+    float R;
+    if (iid) {
+      R = su[m] * Z;
+    } else {
+      const float um = a.mode == kSantaSys ? a.u[bh] : a.u[(size_t)bh * S + m];
+      R = ((float)m + um) * invS * Z;
+    }
     int lo = 0, hi = T - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -534,7 +577,7 @@ __global__ void __launch_bounds__(NT2, 4) santa_sample_kernel(const SantaArgs a)
       reinterpret_cast<float *>(a.o)[(size_t)bh * D + tid] = s;
   }
   if (a.idx)
-    for (int m = tid; m < S; m += NT2) a.idx[(size_t)bh * S + m] = idx_s[m];
+    for (int m = tid; m < S; m += NT2) a.idx[(size_t)bh * S + (iid ? sp[m] : m)] = idx_s[m];
 }
 
 }  // namespace

@@ -412,8 +412,8 @@ double attn_skip_lambda_for_target(double alpha, double beta, double sparsity, d
  *   ATTN_SANTA_SYS:    T_m = (m + u[b,h]) / S     (the page's offset U ~
  *                      Unif[0, 1/S) is u / S; one draw per head)
  *   ATTN_SANTA_STRAT:  T_m = (m + u[b,h,m]) / S  (one draw per stratum)
- *   ATTN_SANTA_IID:    T_m = u[b,h,m]            (declared for completeness;
- *                      no kernel: ATTN_EUNSUPPORTED)
+ *   ATTN_SANTA_IID:    T_m = u[b,h,m]            (independent draws; sorted on
+ *                      the device, idx[b,h,m] is still the index of draw m)
  * The caller draws u (uniform in [0, 1)); a value outside [0, 1) still yields
  * an in-range key index, but not the estimator.
  *
@@ -429,7 +429,7 @@ double attn_skip_lambda_for_target(double alpha, double beta, double sparsity, d
  *
  *  q           [B, Hq, dk]              bf16 (device)
  *  k, v        [B, Hkv, L, 128]         bf16 (device), row strides 128
- *  u           [B, Hq] (SYS) or [B, Hq, S] (STRAT) fp32 (device)
+ *  u           [B, Hq] (SYS) or [B, Hq, S] (STRAT, IID) fp32 (device)
  *  scores      [B, Hq, n_b * 128] fp32  (device, caller-owned workspace;
  *              keys past L hold -inf)
  *  tile_stats  [B, Hq, n_tiles, 2] fp32 (device, caller-owned workspace)

@@ -191,7 +191,7 @@ def test_santa_rejects_invalid_arguments(lib, kw):
 
 
 @pytest.mark.parametrize("kw", [
-    dict(mode=0), dict(dk=64, ks=64), dict(dt=1), dict(S=4096), dict(L=32768, T=8),
+    dict(dk=64, ks=64), dict(dt=1), dict(S=4096), dict(L=32768, T=8),
     dict(Hq=6, Hkv=2), dict(T=2000),
 ])
 def test_santa_unsupported_shapes(lib, kw):

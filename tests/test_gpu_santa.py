@@ -41,6 +41,8 @@ def thresholds(u, S, mode):
     m = np.arange(S)
     if mode == "sys":
         return (m[None, None, :] + u[:, :, None]) / S
+    if mode == "iid":
+        return u
     return (m[None, None, :] + u) / S
 
 
@@ -79,7 +81,7 @@ def check_santa(cfg, q, k, v, S, mode, u, n_tiles):
 
 
 @pytest.mark.parametrize("G", [1, 2, 4, 8])
-@pytest.mark.parametrize("mode", ["sys", "strat"])
+@pytest.mark.parametrize("mode", ["sys", "strat", "iid"])
 def test_santa_small(G, mode):
     cfg = W.SANTA_DECODE_32K.with_(B=2, Hq=2 * G, Hkv=2, L=2048, seed=41)
     q, k, v = W.decode_inputs(cfg)
@@ -95,7 +97,7 @@ def test_santa_ragged_lengths_and_empty_tiles(L, n_tiles):
     with no block (n_tiles > number of blocks)."""
     cfg = W.SANTA_DECODE_32K.with_(B=2, Hq=8, Hkv=2, L=L, seed=42)
     q, k, v = W.decode_inputs(cfg)
-    for mode in ("sys", "strat"):
+    for mode in ("sys", "strat", "iid"):
         u = W.santa_offsets(cfg, 64, mode, seed=L)
         check_santa(cfg, q, k, v, 64, mode, u, n_tiles)
 
@@ -104,7 +106,7 @@ def test_santa_flat_attention():
     """Flatter attention still: the samples spread over many keys and tiles."""
     cfg = W.SANTA_DECODE_32K.with_(B=2, L=8192, sink_a=0.5, salient_a=0.3, seed=43)
     q, k, v = W.decode_inputs(cfg)
-    for mode in ("sys", "strat"):
+    for mode in ("sys", "strat", "iid"):
         u = W.santa_offsets(cfg, 256, mode, seed=1)
         check_santa(cfg, q, k, v, 256, mode, u, 8)
 
@@ -136,7 +138,7 @@ def test_santa_sink_dominated():
     check_santa(cfg, q, k, v, 128, "sys", u, 16)
 
 
-@pytest.mark.parametrize("mode", ["sys", "strat"])
+@pytest.mark.parametrize("mode", ["sys", "strat", "iid"])
 def test_santa_full_size(mode):
     """B=16, 32/8 heads, L=32768, S=128 samples, 16 key tiles, spread
     attention: the configuration the benchmark times."""
