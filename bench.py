@@ -433,6 +433,39 @@ def mla_sweep(args, bs, dev, stream, flush, lam):
                   # executed products are the algorithmic ones
                   "algorithmic_tflops": round((qk + pv) / ms / 1e9, 2)}
     out["max"]["speedup_vs_lambda0"] = round(out["0.0"]["ms"] / out["max"]["ms"], 4)
+    # Per-head decisions: lambda bisected (on the kernel's own bitmaps) for ~70 %
+    # of the (head, block) pairs skipped; a block's values are still read when
+    # any head keeps it.
+    hbits = torch.empty(bs.decode_bitmap_shape(M.B, M.Hq, M.L, M.Bc, M.n_splits),
+                        dtype=torch.int32, device=dev)
+    bps = -(-n_b // M.n_splits)
+
+    def head_sparsity(lmb):
+        bs.attn_skip_decode_per_head(dq, dk_, None, lmb, M.Bc, M.n_splits, dv=M.dv,
+                                     out=(op, lp, hbits))
+        return float(bs.unpack_bits(hbits, bps).float().mean()) * (bps * M.n_splits) / n_b
+
+    lo, hi = math.log(1e-8), math.log(0.999)
+    for _ in range(14):
+        mid = 0.5 * (lo + hi)
+        if head_sparsity(math.exp(mid)) < float(TARGET):
+            lo = mid
+        else:
+            hi = mid
+    lmb = math.exp(hi)
+    hs = head_sparsity(lmb)
+    hb = bs.unpack_bits(hbits, bps).bool()
+    all_skip = int(hb.all(dim=1).sum())  # blocks every head skipped
+
+    def step_ph():
+        bs.attn_skip_decode_per_head(dq, dk_, None, lmb, M.Bc, M.n_splits, dv=M.dv,
+                                     out=(op, lp, hbits))
+        bs.attn_skip_decode_combine(op, lp, out=(o, lse))
+
+    ms = statistics.mean(timed_launches(step_ph, args.warmup, args.steps, flush, stream))
+    out["per_head"] = {"lambda": lmb, "head_sparsity": round(hs, 4),
+                       "block_sparsity": round(all_skip / units, 4), "ms": round(ms, 4),
+                       "speedup_vs_lambda0": round(out["0.0"]["ms"] / ms, 4)}
     out["workload"] = (f"B{M.B} Hq{M.Hq} latent dk{M.dk} dv{M.dv} L{M.L} Bc{M.Bc} "
                        f"splits{M.n_splits}; 'max' = largest sparsity any lambda < 1 reaches")
     return out

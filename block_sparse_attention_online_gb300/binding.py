@@ -307,14 +307,21 @@ def attn_skip_decode(q, k, v, lam, Bc=128, n_splits=8, dv=None, scale=0.0, out=N
     return o_part, lse_part, bits
 
 
-def attn_skip_decode_per_head(q, k, v, lam, Bc=128, n_splits=8, scale=0.0, out=None,
+def attn_skip_decode_per_head(q, k, v, lam, Bc=128, n_splits=8, dv=None, scale=0.0, out=None,
                               stream=None):
-    """Decode with per-head decisions (GQA shape): returns fp32 ``(o_part,
-    lse_part, skip_bits)`` with bits per query head [B,Hq,S,words]."""
-    _cuda_contig(q, k, v)
+    """Decode with per-head decisions (GQA shape, or MLA with ``v=None`` and
+    ``dv``): returns fp32 ``(o_part, lse_part, skip_bits)`` with bits per
+    query head [B,Hq,S,words]."""
+    _cuda_contig(q, k)
     B, Hq, dk = q.shape
     _, Hkv, L, kstride = k.shape
-    dv, vstride = v.shape[3], v.shape[3]
+    if v is None:
+        v, vstride = k, kstride
+        if dv is None:
+            raise ValueError("dv is required when values alias the keys")
+    else:
+        _cuda_contig(v)
+        dv, vstride = v.shape[3], v.shape[3]
     if out is None:
         o_part = torch.empty(B, Hq, n_splits, dv, dtype=torch.float32, device=q.device)
         lse_part = torch.empty(B, Hq, n_splits, dtype=torch.float32, device=q.device)

@@ -112,9 +112,13 @@ attn_status decode_common(DecodeArgs &a, const void *q, const void *k, const voi
       v_row_stride == 128 && (G == 1 || G == 2 || G == 4 || G == 8))
     return from_cuda(launch_decode_bf16(a, s));
   // Absorbed MLA: one latent head of 576 columns, values = its first 512 columns.
+  // Per-head decisions run in the cluster kernel (splits of up to its block
+  // count).
   if (dt == ATTN_BF16 && dk == 576 && dv == 512 && v == k && k_row_stride == 576 &&
-      v_row_stride == 576 && Bc == 64 && Hkv == 1 && Hq == 128 && !a.per_head)
+      v_row_stride == 576 && Bc == 64 && Hkv == 1 && Hq == 128) {
+    if (a.per_head && (a.stats_only || a.bps > mla_cluster_max_bps())) return ATTN_EUNSUPPORTED;
     return from_cuda(launch_mla_decode(a, s));
+  }
   return ATTN_EUNSUPPORTED;
 }
 

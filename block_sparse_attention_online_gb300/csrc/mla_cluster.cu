@@ -280,11 +280,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     return;
   }
 
+  // Bitmap rows: one per (sequence, split), or per (sequence, head, split)
+  // with per-head decisions.
+  const bool ph = a.per_head != 0;
   uint32_t *bits = a.bits + (size_t)us * a.words;
   if (nb == 0) {  // empty split: no key, zero weight in the merge; no hand-off
     if (scorer) {
       if (tid < H) a.lse_part[(size_t)(b * a.Hq + tid) * a.n_splits + sp] = -INFINITY;
-      for (int w = tid; w < a.words; w += NTHREADS) bits[w] = 0u;
+      if (ph) {
+        for (int w = tid; w < H * a.words; w += NTHREADS)
+          a.bits[((size_t)(b * a.Hq + w / a.words) * a.n_splits + sp) * a.words + w % a.words] = 0u;
+      } else {
+        for (int w = tid; w < a.words; w += NTHREADS) bits[w] = 0u;
+      }
     } else {
       for (int idx = tid; idx < H * DVH; idx += NTHREADS) {
         const size_t row = (size_t)(b * a.Hq + idx / DVH) * a.n_splits + sp;
@@ -428,6 +436,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       float m2 = -INFINITY, mref = -INFINITY, l = 0.f;
       int kc = 0;
       uint32_t word = 0;
+      // Per-head decisions: this head's own bitmap row and word.
+      uint32_t *hbits = a.bits + ((size_t)(b * a.Hq + r) * a.n_splits + sp) * a.words;
+      uint32_t hword = 0;
       // Once a wait has failed (the abort flag is up and every later wait
       // fails at once) the loops still run to their end, so that the four
       // warps meet the vote barrier equally often.
@@ -468,8 +479,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const float mt2 = mt * sl2;
           const float mnew = fmaxf(m2, mt2);
           const float diff = (mt == -INFINITY) ? -INFINITY : mt2 - m2;  // Eq. 5 (reading 2)
-          // The block is kept if any head votes keep (one reduction of the four warps).
-          const bool keep = bar_red_or(kVoteBarrier, H, ok && !(diff < c2));
+          // The block is kept if any head votes keep (one reduction of the four
+          // warps); with per-head decisions a head that votes skip takes no
+          // part in the block (P row 0, no row sum, no rescale), and the block
+          // is still skipped as a whole (no value load, no P.V) only if every
+          // head votes skip.
+          const bool vote = ok && !(diff < c2);
+          const bool keep = bar_red_or(kVoteBarrier, H, vote);
           // One outcome for the four warps: the kept path below has a barrier
           // of its own that all of them must reach.
           if (bar_red_or(kFailBarrier, H, !ok)) ok = false;
@@ -479,19 +495,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             // Publish the decision to both value CTAs (one word each).
             for (int t = 0; t < 2; ++t)
               st_remote_relaxed_u32(remote(base + SMEM_DEC + 4u * (uint32_t)j, rk[t]), keep ? 2u : 1u);
-            if (!keep) word |= 1u << (j & 31);
+            if (!ph) {
+              if (!keep) word |= 1u << (j & 31);
+              if ((j & 31) == 31 || j == nb - 1) {
+                bits[j >> 5] = word;
+                word = 0;
+              }
+            }
+          }
+          if (ph) {
+            if (!vote) hword |= 1u << (j & 31);
             if ((j & 31) == 31 || j == nb - 1) {
-              bits[j >> 5] = word;
-              word = 0;
+              hbits[j >> 5] = hword;
+              hword = 0;
             }
           }
           if (!keep) continue;
+          const bool mine = !ph || vote;  // this head takes part in the block
           float alpha = 1.f;
-          if (mref == -INFINITY) {
-            mref = mnew;
-          } else if (mnew > mref + kRescaleLog2) {
-            alpha = ex2(mref - mnew);
-            mref = mnew;
+          if (mine) {
+            if (mref == -INFINITY) {
+              mref = mnew;
+            } else if (mnew > mref + kRescaleLog2) {
+              alpha = ex2(mref - mnew);
+              mref = mnew;
+            }
           }
           const uint64_t sl2x2 = f2(sl2, sl2), negref2 = f2(-mref, -mref);
           uint64_t acc2 = f2(0.f, 0.f);
@@ -518,7 +546,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           }
           float s0, s1;
           f2_split(acc2, s0, s1);
-          l = l * alpha + (s0 + s1);
+          if (mine) {
+            l = l * alpha + (s0 + s1);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) pk[e] = 0u;
+          }
           const int ps = kc % NPS;
           const uint32_t stage = base + SMEM_STAGE;
           // The staging buffer last fed the copies of kept block kc - 1: their
@@ -552,8 +585,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
       // ---- epilogue: LSE here, the final row sums to the value CTAs ------
-      if (tid == 0)
+      if (ph) {
+        for (int w = ((nb - 1) >> 5) + 1; w < a.words; ++w) hbits[w] = 0u;
+      } else if (tid == 0) {
         for (int w = ((nb - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
+      }
       if (ok) {
         a.lse_part[(size_t)(b * a.Hq + r) * a.n_splits + sp] = mref * kLn2 + logf(l);
         asm volatile("st.shared.f32 [%0], %1;" ::"r"(base + SMEM_FIN + (uint32_t)r * 4u), "f"(l)

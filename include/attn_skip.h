@@ -239,8 +239,11 @@ attn_status attn_skip_decode(const void *q, const void *k, const void *v, attn_d
  *  other arguments and outputs as for attn_skip_decode.
  *
  * Kernels built: the GQA shape of attn_skip_decode (dt = ATTN_BF16, dk = dv =
- * 128, Bc = 128, G in {1, 2, 4, 8}, row strides 128); anything else returns
- * ATTN_EUNSUPPORTED.
+ * 128, Bc = 128, G in {1, 2, 4, 8}, row strides 128) and its absorbed-MLA
+ * shape (128 heads over one 576-column latent row, v == k, dv = 512, Bc = 64)
+ * for splits of at most 2048 blocks; anything else returns ATTN_EUNSUPPORTED.
+ * With MLA's 128 heads on one latent head, per-head decisions reach sparsity
+ * that the group AND (a block skipped only when all 128 agree) cannot.
  */
 attn_status attn_skip_decode_per_head(const void *q, const void *k, const void *v, attn_dtype dt,
                                       int B, int Hq, int Hkv, int L, int dk, int dv,

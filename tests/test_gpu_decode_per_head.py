@@ -91,3 +91,53 @@ def test_per_head_full_size_sampled_and_group_is_and_of_heads():
     hb = hb.reshape(cfg.B, cfg.Hkv, cfg.G, cfg.n_splits, bps)
     np.testing.assert_array_equal(hb.all(axis=2), gb)
     assert hb.mean() > gb.mean()  # heads that would keep a block alone are rarer
+
+
+def check_mla_per_head(cfg, q, k, lam):
+    """Absorbed MLA (128 heads on one latent row, values = its first 512
+    columns) with per-head decisions, against the oracle's per-head decode."""
+    dev = torch.device("cuda")
+    op, lp, bits = bs.attn_skip_decode_per_head(q.to(dev), k.to(dev), None, lam, cfg.Bc,
+                                                cfg.n_splits, dv=cfg.dv)
+    bs.attn_skip_last_device_error()
+    n_b = -(-cfg.L // cfg.Bc)
+    bps = -(-n_b // cfg.n_splits)
+    skip = bs.unpack_bits(bits, bps).numpy()
+    r = oracle.decode(q, k, None, cfg.scale, lam, cfg.Bc, cfg.n_splits, dv=cfg.dv,
+                      per_head=True)
+    n_bad, flips = compare_bits(skip, r["skip"], r["margin"], lam, label="mla per-head")
+    assert n_bad == 0, f"{n_bad} per-head skip bits differ outside the margin band"
+    if flips.any():
+        r = oracle.decode(q, k, None, cfg.scale, lam, cfg.Bc, cfg.n_splits, dv=cfg.dv,
+                          per_head=True, force_skip=skip)
+    ne = np.isfinite(r["lse_part"])
+    check_outputs(op.cpu().numpy()[ne], r["o_part"][ne], lp.cpu().numpy()[ne],
+                  r["lse_part"][ne], "bf16", "mla o_part")
+    trav = np.isfinite(r["margin"])
+    return float(skip[trav].mean())
+
+
+@pytest.mark.parametrize("lam", [0.0, 1e-3, 0.05])
+def test_mla_per_head(lam):
+    """Per-head decisions on the MLA shape: ragged last block, 4 splits; the
+    per-head sparsity exceeds the group AND's on the same inputs."""
+    cfg = W.temperate(W.MLA_DECODE_16K.with_(B=2, L=3000, n_splits=4, seed=171))
+    q, k, _ = W.decode_inputs(cfg)
+    sp = check_mla_per_head(cfg, q, k, lam)
+    if lam > 0:
+        dev = torch.device("cuda")
+        _, _, gbits = bs.attn_skip_decode(q.to(dev), k.to(dev), None, lam, cfg.Bc, cfg.n_splits,
+                                          dv=cfg.dv)
+        n_b = -(-cfg.L // cfg.Bc)
+        bps = -(-n_b // cfg.n_splits)
+        gskip = bs.unpack_bits(gbits, bps).numpy()
+        r = oracle.decode(q, k, None, cfg.scale, lam, cfg.Bc, cfg.n_splits, dv=cfg.dv)
+        gsp = float(gskip[np.isfinite(r["margin"])].mean())
+        assert sp >= gsp
+
+
+def test_mla_per_head_empty_splits():
+    """More splits than blocks: empty splits give LSE -inf and zero bitmap rows."""
+    cfg = W.temperate(W.MLA_DECODE_16K.with_(B=1, L=300, n_splits=8, seed=172))
+    q, k, _ = W.decode_inputs(cfg)
+    check_mla_per_head(cfg, q, k, 1e-3)
