@@ -757,22 +757,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (ok) {
         fence_after_sync();
         const float inv = 1.f / sh.fin_l[r];
-        const size_t row = (size_t)(b * a.Hq + r) * a.n_splits + sp;
-        float *orow = a.o_part + row * DV + half * DVH;
+        // O_h / l, 32 columns at a time: each thread's row goes through a 4 KB
+        // staging area of its warp (in the value tiles, idle now that every
+        // product has completed; 16-byte chunk q of row i at chunk position
+        // q ^ (i % 8)), then each row's 128 bytes leave as one coalesced
+        // segment (8 lanes per row, 4 rows per store).
+        const uint32_t stg = base + SMEM_V + (uint32_t)warp * 4096u;
+        const int rr = lane >> 3, qq = lane & 7;  // read side: row of 4, chunk
 #pragma unroll 1
         for (int cc = 0; cc < DVH / 32; ++cc) {
           uint32_t o[32];
           tmem_ld32(lane_base + TMEM_O + cc * 32, o);
           tmem_wait_ld_regs(o);
 #pragma unroll
-          for (int q = 0; q < 8; ++q) {
+          for (int q = 0; q < 8; ++q)
+            st_shared_v4(stg + (uint32_t)lane * 128u + (uint32_t)((q ^ (lane & 7)) << 4),
+                         __float_as_uint(__uint_as_float(o[4 * q]) * inv),
+                         __float_as_uint(__uint_as_float(o[4 * q + 1]) * inv),
+                         __float_as_uint(__uint_as_float(o[4 * q + 2]) * inv),
+                         __float_as_uint(__uint_as_float(o[4 * q + 3]) * inv));
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int ro = 4 * i + rr;  // row within the warp
             float4 v;
-            v.x = __uint_as_float(o[4 * q]) * inv;
-            v.y = __uint_as_float(o[4 * q + 1]) * inv;
-            v.z = __uint_as_float(o[4 * q + 2]) * inv;
-            v.w = __uint_as_float(o[4 * q + 3]) * inv;
-            *reinterpret_cast<float4 *>(orow + cc * 32 + 4 * q) = v;
+            asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                         : "r"(stg + (uint32_t)ro * 128u + (uint32_t)((qq ^ (ro & 7)) << 4)));
+            const size_t row = (size_t)(b * a.Hq + warp * 32 + ro) * a.n_splits + sp;
+            *reinterpret_cast<float4 *>(a.o_part + row * DV + half * DVH + cc * 32 + 4 * qq) = v;
           }
+          __syncwarp();
         }
       }
     }
