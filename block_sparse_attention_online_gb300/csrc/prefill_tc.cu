@@ -387,6 +387,30 @@ __device__ __noinline__ void varlen_locate(const PrefillArgs &a, int i, int grid
   }
 }
 
+// The tile of CTA u: (sequence b, query head h, tile index t) and what
+// follows from it.  Fixed length: longest causal tiles first, CTAs ordered by
+// decreasing tile index; varlen: the located tile vt.
+struct Tile {
+  int t, h, b, T, off, row0, nblk;
+  float ln_lam;
+};
+
+template <bool VARLEN>
+__device__ __forceinline__ Tile tile_of(const PrefillArgs &a, const VarTile &vt, int u) {
+  const int BH = a.B * a.Hq;
+  Tile x;
+  x.t = VARLEN ? vt.t : a.n_t - 1 - u / BH;
+  x.h = VARLEN ? u % a.Hq : (u % BH) % a.Hq;
+  x.b = VARLEN ? vt.s : (u % BH) / a.Hq;
+  x.T = VARLEN ? vt.len : a.T;
+  x.off = VARLEN ? vt.c0 : 0;
+  x.ln_lam = VARLEN ? vt.ln_lam : a.ln_lambda;
+  x.row0 = x.t * BM;
+  const int last_row = min(x.T, x.row0 + BM) - 1;
+  x.nblk = a.causal ? last_row / BN + 1 : (VARLEN ? (x.T + BN - 1) / BN : a.n_b);
+  return x;
+}
+
 // STATS: the statistics mode; SET: an explicit block set per tile (blocks
 // outside it are not traversed); VARLEN: a batch of sequences of different
 // lengths packed token-major, each with its own threshold.  Each is compiled
@@ -407,7 +431,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     return;
   }
 
-  if (tid == 0) {
+  // Set-up.  The key producer's lane initialises the barriers; for a fixed
+  // length batch (whose tile follows from the block index) it then issues Q
+  // and the first NK traversed key tiles at once, so that they are in flight
+  // during the rest of the set-up (the tensor-map descriptors are prefetched
+  // first thing).  It resumes after the CTA barrier at block p_j, load p_c.
+  const uint64_t keep_l2 = policy_evict_last();    // K and V are re-read by other tiles/heads
+  const uint64_t stream_l2 = policy_evict_first();  // Q is read once
+  int p_j = 0, p_c = 0;
+  if (warp == WARP_V && lane == 0) prefetch_tmap(&tm_v);
+  if (warp == WARP_K && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
     mbar_init(smem_u32(&sh.q_full), 1);
     for (int i = 0; i < NK; ++i) {
       mbar_init(smem_u32(&sh.ready[i]), 2);  // the key tile (arrival + bytes), the S buffer
@@ -429,6 +464,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
     sh.abort = 0;
     fence_mbar_init();
+    fence_proxy_async_smem();  // the initialised barriers, seen by this thread's TMA loads
+    if constexpr (!VARLEN) {
+      const Tile x = tile_of<false>(a, VarTile{}, (int)blockIdx.x);
+      const int zq = x.b * a.Hq + x.h, zkv = x.b * a.Hkv + x.h / (a.Hq / a.Hkv);
+      const uint32_t *sw = SET ? a.block_set + ((size_t)zq * a.n_t + x.t) * a.words : nullptr;
+      mbar_expect_tx(smem_u32(&sh.q_full), TILE_BYTES);
+      tma_load_3d(base + SMEM_Q, &tm_q, smem_u32(&sh.q_full), 0, x.row0, zq, stream_l2);
+      tma_load_3d(base + SMEM_Q + HALF_BYTES, &tm_q, smem_u32(&sh.q_full), 64, x.row0, zq,
+                  stream_l2);
+      for (; p_j < x.nblk && p_c < NK; ++p_j) {
+        if constexpr (SET) {
+          if (((__ldg(sw + (p_j >> 5)) >> (p_j & 31)) & 1u) == 0u) continue;
+        }
+        const uint32_t dst = base + SMEM_K + p_c * TILE_BYTES;
+        mbar_expect_tx(smem_u32(&sh.ready[p_c]), TILE_BYTES);
+        tma_load_3d(dst, &tm_k, smem_u32(&sh.ready[p_c]), 0, p_j * BN, zkv, keep_l2);
+        tma_load_3d(dst + HALF_BYTES, &tm_k, smem_u32(&sh.ready[p_c]), 64, p_j * BN, zkv,
+                    keep_l2);
+        ++p_c;
+      }
+    }
   }
   if (warp == WARP_MMA) tmem_alloc(smem_u32(&sh.tmem_base), TMEM_COLS);
   // Varlen: the V-producer warp locates this CTA's tile while the barriers and
@@ -451,19 +507,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   VarTile vt{};
   if constexpr (VARLEN) vt = sh.vt;
   const bool has_tile = !VARLEN || vt.s >= 0;  // varlen: a CTA past the last tile has none
-  // Longest causal tiles first: blocks are ordered by decreasing tile index.
-  const int BH = a.B * a.Hq;
-  const int t = VARLEN ? vt.t : a.n_t - 1 - (int)(blockIdx.x / BH);
-  const int h = VARLEN ? (int)(blockIdx.x % a.Hq) : (int)(blockIdx.x % BH) % a.Hq;
-  const int b = VARLEN ? vt.s : (int)(blockIdx.x % BH) / a.Hq;
+  const Tile tile = tile_of<VARLEN>(a, vt, (int)blockIdx.x);
+  const int t = tile.t, h = tile.h, b = tile.b;
   const int bh = b * a.Hq + h;
   const int hk = h / (a.Hq / a.Hkv);
-  const int T = VARLEN ? vt.len : a.T;
-  const int off = VARLEN ? vt.c0 : 0;
-  const float ln_lam = VARLEN ? vt.ln_lam : a.ln_lambda;
-  const int row0 = t * BM;
-  const int last_row = min(T, row0 + BM) - 1;
-  const int nblk = a.causal ? last_row / BN + 1 : (VARLEN ? (T + BN - 1) / BN : a.n_b);
+  const int T = tile.T, off = tile.off;
+  const float ln_lam = tile.ln_lam;
+  const int row0 = tile.row0, nblk = tile.nblk;
   volatile int *abort = &sh.abort;
   const int zq = b * a.Hq + h, zkv = b * a.Hkv + hk;
   // TMA coordinates (column, y, z) of query rows / key block j: [heads, T, 128]
@@ -481,16 +531,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == WARP_K) {
     // -------------------------------------------------------- Q/K producer --
     if (lane == 0) {
-      prefetch_tmap(&tm_q);
-      prefetch_tmap(&tm_k);
-      const uint64_t keep_l2 = policy_evict_last();    // K is re-read by other tiles/heads
-      const uint64_t stream_l2 = policy_evict_first();  // Q is read once
-      mbar_expect_tx(smem_u32(&sh.q_full), TILE_BYTES);
-      tma_load_3d(base + SMEM_Q, &tm_q, smem_u32(&sh.q_full), 0, q_y, q_z, stream_l2);
-      tma_load_3d(base + SMEM_Q + HALF_BYTES, &tm_q, smem_u32(&sh.q_full), 64, q_y, q_z,
-                  stream_l2);
-      int ki = 0, cc = 0;
-      for (int j = 0; j < nblk && !*abort; ++j) {
+      if constexpr (VARLEN) {  // the tile is known only now
+        mbar_expect_tx(smem_u32(&sh.q_full), TILE_BYTES);
+        tma_load_3d(base + SMEM_Q, &tm_q, smem_u32(&sh.q_full), 0, q_y, q_z, stream_l2);
+        tma_load_3d(base + SMEM_Q + HALF_BYTES, &tm_q, smem_u32(&sh.q_full), 64, q_y, q_z,
+                    stream_l2);
+      }
+      int ki = p_c, cc = p_c;
+      for (int j = p_j; j < nblk && !*abort; ++j) {
         if constexpr (SET) {
           if (!in_set(j)) continue;
         }
@@ -520,8 +568,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == WARP_V) {
     // ---------------------------------------------------------- V producer --
     if (lane == 0) {
-      prefetch_tmap(&tm_v);
-      const uint64_t keep_l2 = policy_evict_last();
       int vi = 0, cc = 0;
       for (int j = 0; j < nblk && !*abort; ++j) {
         if constexpr (SET) {

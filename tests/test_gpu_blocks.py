@@ -131,3 +131,21 @@ def test_blocks_full_size_infllm_like_set():
     allow = infllm_set(cfg.B, cfg.Hq, cfg.n_t, cfg.n_b, 8, seed=105)
     units = sorted({h * cfg.n_t + t for h in (2, 29) for t in (0, 1, 2, 70, cfg.n_t - 1)})
     check_blocks(cfg, q, k, v, _lambda(cfg.name, "0.7"), allow, "bf16", units=units)
+
+
+def test_blocks_tc_many_tiles_per_cta():
+    """1024 (b, h, t) tiles, several waves of CTAs per SM: random sets with a
+    fifth of the tiles empty (their CTAs issue no key load), sampled tiles
+    against the oracle, and every empty tile's rows O = 0, LSE = -inf."""
+    cfg = W.temperate(W.GQA_PREFILL_16K.with_(B=2, Hq=32, Hkv=8, T=2048, seed=106))
+    q, k, v = W.prefill_inputs(cfg)
+    allow = random_set(cfg.B, cfg.Hq, cfg.n_t, cfg.n_b, 0.3, seed=106)
+    g = np.random.default_rng(107)
+    empty = g.random((cfg.B, cfg.Hq, cfg.n_t)) < 0.2
+    allow[empty] = False
+    units = sorted(int(u) for u in g.choice(cfg.B * cfg.Hq * cfg.n_t, 48, replace=False))
+    for lam in (0.0, 1e-3):
+        check_blocks(cfg, q, k, v, lam, allow, "bf16", units=units)
+    o, lse, _ = run_blocks(q, k, v, 1e-3, allow, 128, 128)
+    rows = np.repeat(empty, 128, axis=2)[:, :, :cfg.T]
+    assert (o[rows] == 0).all() and np.isneginf(lse[rows]).all()
