@@ -1,5 +1,5 @@
 // Split-KV decode with softmax-threshold block skipping over an NVFP4
-// key/value cache (d = 128, Bc = 128), on the tensor cores.
+// key/value cache (d = 128, Bc = 128), on warp-level tensor-core products.
 //
 // Method: the BLASST page, sections "BLASST 的判定准则" (Eq. 5) and "Decode 内核：
 // 砍带宽": the scores of a block decide whether its values are read at all.
@@ -10,36 +10,47 @@
 // head scale * E4M3(block scale) * E2M1(code).  A 128-key block is 8 KB of
 // codes and 1 KB of block scales: a quarter of the bf16 cache's bytes.
 //
-// The block scales vary along the contracted dimension, so no E2M1 product
-// can take them; both caches are widened, exactly, to fp16 on the chip: an
-// E2M1 value has two significant bits and an E4M3 scale four, so their
-// product (|x| in [2^-10, 2688]) is an fp16 normal number.  Keys go straight
-// into TMEM (no shared-memory round trip), values into a shared-memory tile.
-//
-// Transposed products, one CTA per (sequence, KV head, split):
-//   S^T = K_j Q^T     kind::f16, A = the widened key tile read from TMEM
-//                     (the block's 128 keys are the MMA rows, lane = key),
+// A decode block is a batched matrix-vector product (G <= 8 query heads
+// against 128 keys) and HBM bound.  A tcgen05 product has 128 rows and takes
+// about as long to issue whatever its width, so with G heads most of it is
+// padding and the issue rate, not HBM, would set the pace.  Here every
+// product is a warp-level m16n8k16 one (fp16 operands, fp32 accumulation)
+// with its operands in registers:
+//   S = K_j Q^T       A = 16 keys x 16 elements, widened from the codes in
+//                     registers (cvt.e2m1x2 times the E4M3 block scale: an
+//                     E2M1 value has two significant bits and an E4M3 scale
+//                     four, so the product is an exact fp16 normal number);
 //                     B = the query as fp16 after a power-of-two per-head
 //                     scale 2^e (max|q| 2^e <= 2^15), exact for every bf16
 //                     element not below ~2^-31 of the head's largest;
-//   O^T += V_j^T P^T  kind::f16, A = the widened value tile (MN-major),
-//                     B = P^T (fp16, heads x keys).
-// Every thread of the four score warps owns one key of the block and its G
-// scores, as in the E4M3-cache kernel.
+//                     C = 16 keys x 8 heads (heads past G are zero columns);
+//   O^T += V_j^T P^T  A = 16 value dimensions x 16 keys from a widened fp16
+//                     value tile (ldmatrix.trans), B = P^T (keys x heads,
+//                     fp16) from shared memory, C = O^T held in registers.
+// The contracted dimension of S is taken in a permuted order, the same for A
+// and B (a dot product does not depend on the order of its terms): lane
+// (g, q) = (lane / 4, lane % 4) holds elements 32q .. 32q + 31 of its key
+// rows and of query head g, so one 16-byte load of a code row serves all
+// eight k-steps of a block; in k-step kk, columns 2q, 2q + 1 are elements
+// 32q + 4kk + {0, 1} (code byte 16q + 2kk) and columns 2q + 8, 2q + 9 are
+// elements 32q + 4kk + {2, 3} (the next byte).
 //
-// Warp roles (512 threads):
-//   warps 0-3   scores: thread = key 32w + lane; maxima, votes, decision,
-//               exponentials, P^T, row sums, O^T rescale, epilogue;
-//   warp 4      key producer: TMA of the code tile (64-byte swizzle), the
-//               block scales by cp.async from all 32 lanes;
-//   warp 5      S^T issuer (allocates TMEM);
-//   warp 6      value producer (kept blocks only), as warp 4;
-//   warp 7      O^T issuer;
-//   warps 8-11  key wideners: warp 8 + q owns TMEM lane quarter q, thread =
-//               key row; codes and scales -> 64 columns of fp16 pairs;
-//   warps 12-15 value wideners (follow the decisions).
-// TMEM columns: widened key tiles [0,256) (64 each), S^T buffers [256,320)
-// (16 each), O^T [320,336).
+// One CTA per (sequence, KV head, split).  Warp roles (320 threads):
+//   warps 0-3  scores: warp w owns keys 32w .. 32w + 31 of every block (two
+//              16-key products per k-step); block maxima per head, the
+//              decision (every head votes skip), exponentials, P^T, row sums;
+//   warps 4-7  values: warp 4 + w owns value dimensions 32w .. 32w + 31 (two
+//              16-row products per k-step) of O^T; it widens those columns
+//              of every kept value tile into its own part of one fp16 tile,
+//              then runs its products; rescales and the epilogue;
+//   warp 8     key producer: TMA of the code tile, block scales by cp.async
+//              from its 32 lanes (zero past L);
+//   warp 9     value producer, kept blocks only.
+// Two CTAs share an SM (104 KB of shared memory, <= 102 registers a thread),
+// so one CTA's per-block latencies (loads, product chains, the score warps'
+// exchange) overlap the other's.  Every wait inside the loops is a bounded
+// mbarrier wait (no CTA-wide or named barrier), so a failed wait ends every
+// role's loop with an error status instead of a hang.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -54,128 +65,74 @@ namespace {
 using namespace tc;
 
 constexpr int D = 128;    // head size (keys and values)
-constexpr int BC = 128;   // keys per block (MMA rows of S^T)
-constexpr int NQ = 16;    // MMA columns: query heads, padded
-constexpr int NKF = 12;   // key code stages in shared memory (NKF / 2 block pairs)
-constexpr int NKT = 4;    // widened key tiles in TMEM (NKT / 2 block pairs)
-constexpr int NVF = 3;    // value code stages
-constexpr int NVH = 2;    // widened (fp16) value tiles
-constexpr int NS = 4;     // TMEM S^T buffers
-constexpr int NPT = 3;    // P^T buffers
-constexpr int NDP = 16;   // decision ring, in block pairs
-constexpr int NT = 16 * 32;
-constexpr int WARP_K = 4, WARP_QK = 5, WARP_V = 6, WARP_PV = 7, WARP_KW = 8, WARP_VW = 12;
-constexpr int NVW = 4 * 32;                  // value widener threads
-constexpr uint32_t CODE_ROW = D / 2;         // 64 bytes of codes per row
-constexpr uint32_t SC_ROW = D / 16;          // 8 block scales per row
+constexpr int BC = 128;   // keys per block
+constexpr int NKF = 5;    // key stages (codes + block scales)
+constexpr int NVF = 2;    // value code stages
+constexpr int NP = 4;     // P^T buffers
+constexpr int NDEC = 16;  // decision ring
+constexpr int NSW = 4;    // score warps
+constexpr int NVW = 4;    // value warps
+constexpr int WARP_VAL = NSW, WARP_K = NSW + NVW, WARP_V = WARP_K + 1;
+constexpr int NT = (WARP_V + 1) * 32;
+constexpr uint32_t CODE_ROW = D / 2;            // 64 bytes of codes per row
+constexpr uint32_t SC_ROW = D / 16;             // 8 block scales per row
 constexpr uint32_t CODE_BYTES = BC * CODE_ROW;  // 8 KB
 constexpr uint32_t SC_BYTES = BC * SC_ROW;      // 1 KB
 constexpr uint32_t H_BYTES = BC * D * 2;        // 32 KB: 128 keys x 128 fp16
-constexpr uint32_t HALF_BYTES = H_BYTES / 2;    // one 64-column swizzled box
-constexpr uint32_t QBOX = NQ * 128;             // 2 KB: 16 heads x 64 fp16
+constexpr uint32_t HALF_BYTES = H_BYTES / 2;    // one 64-column box
+// P^T buffer: 8 head rows of 128 fp16 keys, rows 272 bytes apart so that the
+// eight rows of a fragment load fall in different banks.
+constexpr uint32_t P_ROW = BC * 2 + 16;
+constexpr uint32_t P_BYTES = 8 * P_ROW;
 constexpr uint32_t SMEM_KC = 0;
 constexpr uint32_t SMEM_VC = SMEM_KC + NKF * CODE_BYTES;
 constexpr uint32_t SMEM_VH = SMEM_VC + NVF * CODE_BYTES;
-constexpr uint32_t SMEM_KS = SMEM_VH + NVH * H_BYTES;
+constexpr uint32_t SMEM_KS = SMEM_VH + H_BYTES;
 constexpr uint32_t SMEM_VS = SMEM_KS + NKF * SC_BYTES;
-constexpr uint32_t SMEM_Q = SMEM_VS + NVF * SC_BYTES;  // two boxes
-constexpr uint32_t SMEM_PT = SMEM_Q + 2 * QBOX;        // NPT x two 64-key boxes
-constexpr uint32_t SMEM_TILES = SMEM_PT + NPT * 2 * QBOX;
-constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_K = 0;                 // NKT x 64 columns
-constexpr uint32_t TMEM_S = TMEM_K + NKT * 64; // NS x NQ columns
-constexpr uint32_t TMEM_O = TMEM_S + NS * NQ;
+constexpr uint32_t SMEM_P = SMEM_VS + NVF * SC_BYTES;
+constexpr uint32_t SMEM_TILES = SMEM_P + NP * P_BYTES;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleLog2 = 8.0f;  // exp reference may lag the max by 2^8
-// S^T: fp16, A (keys) from TMEM, B (query) K-major.  O^T: fp16, A (V^T)
-// MN-major, B (P^T) K-major.
-constexpr uint32_t IDESC_QK = idesc_f16_f32(BC, NQ, 0);
-constexpr uint32_t IDESC_PV = idesc_f16_f32(D, NQ, 0) | (1u << 15);
-static_assert(TMEM_O + NQ <= TMEM_COLS, "TMEM budget");
-static_assert(NS == 4 && NKF % 2 == 0 && NKT % 2 == 0, "stages and buffers in block pairs");
-static_assert(NT >= NQ * 16, "16 threads per query row write the query");
-static_assert(SMEM_KC % 1024 == 0 && SMEM_VC % 1024 == 0 && SMEM_VH % 1024 == 0 &&
-                  SMEM_Q % 1024 == 0 && SMEM_PT % 1024 == 0,
-              "swizzled tiles on 1024-byte boundaries");
+static_assert(SMEM_VC % 1024 == 0 && SMEM_VH % 1024 == 0 && SMEM_P % 16 == 0,
+              "swizzled TMA destinations and value tiles on 1024-byte boundaries");
 
 struct Shared {
-  uint64_t kc_full[NKF / 2], kc_empty[NKF / 2];  // per pair stage
-  uint64_t kt_full[NKT / 2], kt_empty[NKT / 2];  // per pair of TMEM tiles
+  uint64_t kc_full[NKF], kc_empty[NKF];
   uint64_t vc_full[NVF], vc_empty[NVF];
-  uint64_t vh_full[NVH], vh_empty[NVH];
-  uint64_t s_full[2], s_free[2];  // per pair buffer
-  uint64_t p_full[NPT], p_free[NPT];
-  uint64_t dec_full[NDP], dec_empty[NDP];
-  uint64_t red_full[2];  // the four score warps' partial maxima of a block pair are in
-  uint64_t l_full;       // the four score warps' row sums are in
-  int dec[NDP][2];
-  float red[2][4][16];  // per block pair (double buffered): per score warp, per head max
-  float lsum[4][8];     // epilogue: per score warp, per head row sum
-  float sl2[NQ];        // per head: raw score -> log2 units
-  uint32_t tmem_base;
+  uint64_t p_full[NP], p_free[NP];
+  uint64_t dec_full[NDEC], dec_empty[NDEC];
+  uint64_t red_full[2];  // the score warps' partial maxima of a block are in
+  uint64_t l_full;       // the score warps' row sums are in
+  int dec[NDEC];
+  float red[2][NSW][8];  // per block (double buffered): per score warp, per head max
+  float alpha[NP][8];    // per P^T buffer: the heads' O^T rescale factors
+  float lsum[NSW][8];    // epilogue: per score warp, per head row sum
   int abort;
 };
 constexpr uint32_t SMEM_ALLOC = SMEM_TILES + ((sizeof(Shared) + 127) / 128) * 128;
-static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory budget");
+static_assert(2 * SMEM_ALLOC <= 226 * 1024, "shared memory budget: two CTAs per SM");
 
-// K-major fp16 operand with 128-byte rows of 64 elements (the query, P^T):
-// two 128-byte-swizzled boxes of 16 rows, 8-row groups 1024 bytes apart;
-// k-step kk (16 elements) is box kk / 4 at 32-byte step kk % 4.
-__device__ __forceinline__ uint64_t kmajor_base(uint32_t tile) {
-  return smem_desc_sw128(tile, 16u, 1024u);
-}
-__device__ __forceinline__ constexpr uint64_t box_step(int kk) {
-  return (uint64_t)(((uint32_t)(kk >> 2) * QBOX + (uint32_t)(kk & 3) * 32u) >> 4);
-}
-// fp16 value tile (rows are keys, two 128-byte-swizzled boxes of 64 d values)
-// as the MN-major A operand V^T: the second 64-d half 16 KB further (LBO),
-// 8-key groups 1024 bytes apart (SBO); k-step kk (16 keys) 2048 bytes further.
-__device__ __forceinline__ uint64_t vmajor_base(uint32_t tile) {
-  return smem_desc_sw128(tile, HALF_BYTES, 1024u);
-}
-__device__ __forceinline__ constexpr uint64_t vmajor_step(int kk) {
-  return (uint64_t)(((uint32_t)kk * 2048u) >> 4);
-}
-
-__device__ __forceinline__ float warp_max(float v) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-  return r;
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+// D += A B for one m16n8k16 product (fp16 operands, fp32 accumulators).
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15}, [%16];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// 8-byte copy global -> shared through the L1-bypassing path; src_bytes = 0
-// writes zeros and reads nothing.  Both addresses 8-byte aligned.
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src, uint32_t src_bytes) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
-               : "memory");
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
 }
-// Arrive on `bar` once this thread's earlier cp.async copies have landed
-// (the arrival is one of the barrier's expected arrivals).
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr));
 }
 
 // Four E2M1 pairs (the bytes of w, element 2i in the low nibble) -> four fp16
@@ -195,16 +152,17 @@ __device__ __forceinline__ void e2m1x8_scaled(uint32_t w, uint32_t s2, uint32_t 
       : "r"(w), "r"(s2));
 }
 
-// E4M3 block scale (byte `i` of the pair (lo, hi)) -> the fp16 pair (s, s).
-__device__ __forceinline__ uint32_t e4m3_scale2(uint32_t lo, uint32_t hi, int i) {
-  const uint32_t byte = ((i < 4 ? lo : hi) >> (8 * (i & 3))) & 0xffu;
+// Two E4M3 block scales (the low two bytes of v: scale 0, scale 1) -> the
+// fp16 pairs (s0, s0) and (s1, s1).
+__device__ __forceinline__ void e4m3_scale_pairs(uint32_t v, uint32_t &s00, uint32_t &s11) {
   uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((unsigned short)(byte | (byte << 8))));
-  return r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((unsigned short)(v & 0xffffu)));
+  s00 = __byte_perm(r, r, 0x1010);
+  s11 = __byte_perm(r, r, 0x3232);
 }
 
-// Code chunk c (bytes 16c..16c+15: elements 32c..32c+31) of row r of a code
-// tile (64-byte rows, 64-byte swizzle: chunk c at chunk position
+// Code chunk c (bytes 16c..16c+15: elements 32c..32c+31) of row r of a value
+// code tile (64-byte rows, 64-byte swizzle: chunk c at chunk position
 // c ^ ((r / 2) % 4)).
 __device__ __forceinline__ uint4 ld_code_chunk(uint32_t tile, int r, int c) {
   uint4 x;
@@ -217,8 +175,8 @@ __device__ __forceinline__ uint4 ld_code_chunk(uint32_t tile, int r, int c) {
 
 // Widen value chunk t of a kept block: row r = t / 4, code chunk c = t % 4
 // (32 elements, block scales 2c and 2c + 1) -> 64 bytes of the fp16 tile
-// (box c / 2, 16-byte chunks 4 (c % 2) .. + 3 of the row, at chunk position
-// chunk ^ (r % 8)).
+// (box c / 2 of two 64-column boxes of 128-byte rows; 16-byte chunks
+// 4 (c % 2) .. + 3 of the row, at chunk position chunk ^ (r % 8)).
 __device__ __forceinline__ void widen_value_chunk(uint32_t codes, uint32_t scales,
                                                   uint32_t dst_tile, int t) {
   const int r = t >> 2, c = t & 3;
@@ -227,8 +185,8 @@ __device__ __forceinline__ void widen_value_chunk(uint32_t codes, uint32_t scale
   asm volatile("ld.shared.u16 %0, [%1];"
                : "=r"(sc)
                : "r"(scales + (uint32_t)r * SC_ROW + 2u * (uint32_t)c));
-  const uint32_t s0 = e4m3_scale2(sc & 0xffu, 0u, 0);
-  const uint32_t s1 = e4m3_scale2((sc >> 8) & 0xffu, 0u, 0);
+  uint32_t s0, s1;
+  e4m3_scale_pairs(sc, s0, s1);
   uint32_t h[16];
   e2m1x8_scaled(x.x, s0, *reinterpret_cast<uint32_t(*)[4]>(&h[0]));
   e2m1x8_scaled(x.y, s0, *reinterpret_cast<uint32_t(*)[4]>(&h[4]));
@@ -243,45 +201,22 @@ __device__ __forceinline__ void widen_value_chunk(uint32_t codes, uint32_t scale
                  h[4 * i + 3]);
 }
 
-// The query as fp16 into the two query boxes (16 rows of 64 fp16, 128-byte
-// swizzled), by threads 0-255: thread t takes row r = t / 16 (query head
-// hk*G + r, zero for r >= G) and its 16-byte chunk t % 16 of bf16 values.
-// Per row: e = 15 - ceil(log2 max|q|) (the largest power of two with max|q|
-// 2^e <= 2^15), the row times 2^e rounded to fp16; sl2[r] = the row's score
-// scale (scale * key scale * log2 e * 2^-e).
-__device__ __forceinline__ void write_query(const DecodeArgs &a, int b, int hk, int G, int zkv,
-                                            int t, uint32_t q_tile, float *sl2) {
-  const int r = t >> 4, c16 = t & 15;
-  uint4 v = make_uint4(0u, 0u, 0u, 0u);
-  if (r < G)
-    v = __ldg(reinterpret_cast<const uint4 *>((const __nv_bfloat16 *)a.q +
-                                              (size_t)(b * a.Hq + hk * G + r) * D) + c16);
-  const uint32_t pr[4] = {v.x, v.y, v.z, v.w};  // bf16 pairs, low element first
-  uint32_t amax_bits = 0;  // |bf16| bit patterns order like their values
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    amax_bits = max(amax_bits, max(pr[i] & 0x7fffu, (pr[i] >> 16) & 0x7fffu));
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1)  // the 16 threads of the row
-    amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, o));
-  const float amax = __uint_as_float(amax_bits << 16);
-  int ex = 0;
-  const float fr = frexpf(amax > 0.f ? amax : 1.f, &ex);  // amax = fr * 2^ex
-  const int qexp = amax > 0.f ? 15 - (fr == 0.5f ? ex - 1 : ex) : 0;  // 15 - ceil(log2 amax)
-  uint32_t h[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    h[i] = pack_f16x2(ldexpf(__uint_as_float(pr[i] << 16), qexp),
-                      ldexpf(__uint_as_float(pr[i] & 0xffff0000u), qexp));
-  const uint32_t box = q_tile + (uint32_t)(c16 >> 3) * QBOX;
-  st_shared_v4(box + (uint32_t)r * 128u + ((((uint32_t)c16 & 7u) ^ (uint32_t)(r & 7)) << 4), h[0],
-               h[1], h[2], h[3]);
-  if (c16 == 0) sl2[r] = ldexpf(a.scale * __ldg(a.k_scale + zkv) * kLog2e, -qexp);
+// 8-byte copy global -> shared through the L1-bypassing path; src_bytes = 0
+// writes zeros and reads nothing.  Both addresses 8-byte aligned.
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+// Arrive on `bar` once this thread's earlier cp.async copies have landed
+// (the arrival is one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // The scale rows of block `row0` .. row0 + 127 of (b, KV head) slice `zkv`
 // into the 1 KB stage at `dst`, by the 32 lanes of a producer warp (rows
-// lane, lane + 32, lane + 64, lane + 96; rows past L read as zero). The
+// lane, lane + 32, lane + 64, lane + 96; rows past L read as zero).  The
 // caller adds each lane's arrival on the stage barrier (cp_async_arrive).
 __device__ __forceinline__ void load_scales(uint32_t dst, const uint8_t *sc, int zkv, int row0,
                                             int L, int lane) {
@@ -297,13 +232,14 @@ __device__ __forceinline__ void load_scales(uint32_t dst, const uint8_t *sc, int
 }
 
 template <int G>
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(NT, 2)
     decode_nvfp4_kernel(const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Shared &sh = *reinterpret_cast<Shared *>(smem_raw + SMEM_TILES);
   const uint32_t base = smem_u32(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, q = lane & 3;  // fragment row group, thread in the group
   if (base & 1023u) {  // the swizzled layouts need a 1024-byte aligned base
     if (tid == 0) atomicOr(a.err, kErrLayout);
     return;
@@ -328,86 +264,62 @@ __global__ void __launch_bounds__(NT, 1)
     return;
   }
 
-  // The query and each head's score scale; the P^T rows of the padding heads
-  // are zeroed once.
-  if (tid < NQ * 16) write_query(a, b, hk, G, zkv, tid, base + SMEM_Q, sh.sl2);
-  for (int idx = tid; idx < NPT * 2 * (NQ - G) * 8; idx += NT) {  // rows G..15, 16-byte chunks
-    const int c = idx & 7, r = G + (idx >> 3) % (NQ - G), box = (idx >> 3) / (NQ - G);
-    st_shared_v4(base + SMEM_PT + box * QBOX + r * 128 + c * 16, 0u, 0u, 0u, 0u);
-  }
-  fence_proxy_async_smem();  // visible to the tensor core
-  if (tid == 0) {
-    for (int i = 0; i < NKF / 2; ++i) {
-      mbar_init(smem_u32(&sh.kc_full[i]), 1 + 32);  // TMA arrival + 32 cp.async lanes
-      mbar_init(smem_u32(&sh.kc_empty[i]), 4);      // the four key wideners
+  // The P^T rows of the heads past G stay zero (the products' padding columns).
+  if constexpr (G < 8) {
+    constexpr int kChunks = (int)(P_ROW / 16), kPad = (8 - G) * kChunks;
+    for (int idx = tid; idx < NP * kPad; idx += NT) {
+      const int buf = idx / kPad, r = G + (idx % kPad) / kChunks, c = (idx % kPad) % kChunks;
+      st_shared_v4(base + SMEM_P + buf * P_BYTES + r * P_ROW + c * 16, 0u, 0u, 0u, 0u);
     }
-    for (int i = 0; i < NKT / 2; ++i) {
-      mbar_init(smem_u32(&sh.kt_full[i]), 4);  // the four key wideners
-      mbar_init(smem_u32(&sh.kt_empty[i]), 1);  // the S^T commit of the pair
+  }
+  if (tid == 0) {
+    for (int i = 0; i < NKF; ++i) {
+      mbar_init(smem_u32(&sh.kc_full[i]), 1 + 32);  // TMA arrival + 32 cp.async lanes
+      mbar_init(smem_u32(&sh.kc_empty[i]), NSW);
     }
     for (int i = 0; i < NVF; ++i) {
       mbar_init(smem_u32(&sh.vc_full[i]), 1 + 32);
-      mbar_init(smem_u32(&sh.vc_empty[i]), 4);  // the four value wideners
+      mbar_init(smem_u32(&sh.vc_empty[i]), NVW);
     }
-    for (int i = 0; i < NVH; ++i) {
-      mbar_init(smem_u32(&sh.vh_full[i]), 4);
-      mbar_init(smem_u32(&sh.vh_empty[i]), 1);  // the O^T commit
+    for (int i = 0; i < NP; ++i) {
+      mbar_init(smem_u32(&sh.p_full[i]), NSW);
+      mbar_init(smem_u32(&sh.p_free[i]), NVW);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&sh.s_full[i]), 1);
-      mbar_init(smem_u32(&sh.s_free[i]), 4);  // the four score warps
-    }
-    for (int i = 0; i < NPT; ++i) {
-      mbar_init(smem_u32(&sh.p_full[i]), 4);  // the four score warps
-      mbar_init(smem_u32(&sh.p_free[i]), 1);  // the O^T commit
-    }
-    for (int i = 0; i < NDP; ++i) {
+    for (int i = 0; i < NDEC; ++i) {
       mbar_init(smem_u32(&sh.dec_full[i]), 1);
-      // readers: the value producer, the O^T issuer, the four value wideners
-      mbar_init(smem_u32(&sh.dec_empty[i]), 6);
+      mbar_init(smem_u32(&sh.dec_empty[i]), 1 + NVW);  // the value producer, the value warps
     }
-    mbar_init(smem_u32(&sh.red_full[0]), 4);
-    mbar_init(smem_u32(&sh.red_full[1]), 4);
-    mbar_init(smem_u32(&sh.l_full), 4);
+    mbar_init(smem_u32(&sh.red_full[0]), NSW);
+    mbar_init(smem_u32(&sh.red_full[1]), NSW);
+    mbar_init(smem_u32(&sh.l_full), NSW);
     sh.abort = 0;
     fence_mbar_init();
   }
-  if (warp == WARP_QK) tmem_alloc(smem_u32(&sh.tmem_base), TMEM_COLS);
-  fence_before_sync();
   __syncthreads();
-  fence_after_sync();
-  const uint32_t tmem = sh.tmem_base;
 
   if (warp == WARP_K) {
     // ------------------------------------------------------ key producer --
     if (lane == 0) prefetch_tmap(&tm_k);
     const uint64_t pol = policy_evict_first();  // the cache is streamed once
-    // Blocks in pairs: stage f holds two blocks' codes and scales under one
-    // barrier.
-    const int npair = (nb + 1) / 2;
     int issued = 0;
-    for (int q = 0; q < npair; ++q) {
+    for (int j = 0; j < nb; ++j) {
       if (__any_sync(0xffffffffu, *abort)) break;  // one outcome for the warp
-      const int f = q % (NKF / 2);
-      const int n = 2 * q + 1 < nb ? 2 : 1;
-      if (q >= NKF / 2 && !mbar_wait_warp(smem_u32(&sh.kc_empty[f]), ((q / (NKF / 2)) - 1) & 1,
-                                          abort, a.err, kErrTimeout))
+      const int f = j % NKF;
+      if (j >= NKF && !mbar_wait_warp(smem_u32(&sh.kc_empty[f]), ((j / NKF) - 1) & 1, abort,
+                                      a.err, kErrTimeout))
         break;
       if (lane == 0) {
-        mbar_expect_tx(smem_u32(&sh.kc_full[f]), n * CODE_BYTES);
-        for (int t = 0; t < n; ++t)
-          tma_load_3d(base + SMEM_KC + (2 * f + t) * CODE_BYTES, &tm_k, smem_u32(&sh.kc_full[f]),
-                      0, (j0 + 2 * q + t) * BC, zkv, pol);
+        mbar_expect_tx(smem_u32(&sh.kc_full[f]), CODE_BYTES);
+        tma_load_3d(base + SMEM_KC + f * CODE_BYTES, &tm_k, smem_u32(&sh.kc_full[f]), 0,
+                    (j0 + j) * BC, zkv, pol);
       }
-      for (int t = 0; t < n; ++t)
-        load_scales(base + SMEM_KS + (2 * f + t) * SC_BYTES, a.k_bs, zkv, (j0 + 2 * q + t) * BC,
-                    a.L, lane);
+      load_scales(base + SMEM_KS + f * SC_BYTES, a.k_bs, zkv, (j0 + j) * BC, a.L, lane);
       cp_async_arrive(smem_u32(&sh.kc_full[f]));
       ++issued;
     }
-    for (int f = 0; f < NKF / 2 && f < issued; ++f) {  // drain the copies in flight
-      const int last = f + ((issued - 1 - f) / (NKF / 2)) * (NKF / 2);
-      mbar_wait_drain(smem_u32(&sh.kc_full[f]), (last / (NKF / 2)) & 1);
+    for (int f = 0; f < NKF && f < issued; ++f) {  // drain the copies in flight
+      const int last = f + ((issued - 1 - f) / NKF) * NKF;
+      mbar_wait_drain(smem_u32(&sh.kc_full[f]), (last / NKF) & 1);
     }
   } else if (warp == WARP_V) {
     // ---------------------------------------------------- value producer --
@@ -416,13 +328,12 @@ __global__ void __launch_bounds__(NT, 1)
     int vi = 0;
     for (int j = 0; j < nb; ++j) {
       if (__any_sync(0xffffffffu, *abort)) break;  // one outcome for the warp
-      const int q = j >> 1, ds = q % NDP;
-      if (!(j & 1) && !mbar_wait_warp(smem_u32(&sh.dec_full[ds]), (q / NDP) & 1, abort, a.err,
-                                      kErrTimeout))
+      const int ds = j % NDEC;
+      if (!mbar_wait_warp(smem_u32(&sh.dec_full[ds]), (j / NDEC) & 1, abort, a.err, kErrTimeout))
         break;
-      const int keep = sh.dec[ds][j & 1];
+      const int keep = sh.dec[ds];
       __syncwarp();
-      if (lane == 0 && ((j & 1) || j == nb - 1)) mbar_arrive(smem_u32(&sh.dec_empty[ds]));
+      if (lane == 0) mbar_arrive(smem_u32(&sh.dec_empty[ds]));
       if (!keep) continue;
       const int f = vi % NVF;
       if (vi >= NVF && !mbar_wait_warp(smem_u32(&sh.vc_empty[f]), ((vi / NVF) - 1) & 1, abort,
@@ -441,343 +352,355 @@ __global__ void __launch_bounds__(NT, 1)
       const int last = f + ((vi - 1 - f) / NVF) * NVF;
       mbar_wait_drain(smem_u32(&sh.vc_full[f]), (last / NVF) & 1);
     }
-  } else if (warp >= WARP_KW && warp < WARP_VW) {
-    // ------------------------------------------------------ key wideners --
-    // Thread = key row r of the block = TMEM lane r: its 64 bytes of codes
-    // and 8 block scales -> 64 columns of fp16 pairs (element 2i low).
-    const int r = (warp - WARP_KW) * 32 + lane;
-    const uint32_t lane_addr = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const int npair = (nb + 1) / 2;
-    for (int q = 0; q < npair; ++q) {
-      const int f = q % (NKF / 2), kp = q % (NKT / 2);
-      const int n = 2 * q + 1 < nb ? 2 : 1;
-      if (!mbar_wait_warp(smem_u32(&sh.kc_full[f]), (q / (NKF / 2)) & 1, abort, a.err,
-                          kErrTimeout))
-        break;
-      // TMEM tiles of pair kp last fed the S^T products of pair q - NKT / 2.
-      if (q >= NKT / 2 && !mbar_wait_warp(smem_u32(&sh.kt_empty[kp]), ((q / (NKT / 2)) - 1) & 1,
-                                          abort, a.err, kErrTimeout))
-        break;
-      fence_after_sync();
-      for (int t = 0; t < n; ++t) {
-        const uint32_t codes = base + SMEM_KC + (2 * f + t) * CODE_BYTES;
-        uint32_t slo, shi;
-        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
-                     : "=r"(slo), "=r"(shi)
-                     : "r"(base + SMEM_KS + (2 * f + t) * SC_BYTES + (uint32_t)r * SC_ROW));
+  } else if (warp >= WARP_VAL) {
+    // ------------------------------------------------------------- values --
+    // O^T rows (value dimensions) 32 vw + 16 mt + g and + 8, for mt = 0, 1;
+    // columns (heads) 2q, 2q + 1.
+    const int vw = warp - WARP_VAL;
+    float o[2][2][4];  // [mt][even / odd k-steps][fragment]
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {  // elements 64 half .. + 63: columns 32 half ..
-          const uint4 x0 = ld_code_chunk(codes, r, 2 * half);
-          const uint4 x1 = ld_code_chunk(codes, r, 2 * half + 1);
-          const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-          uint32_t h[32];
+    for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-          for (int qw = 0; qw < 8; ++qw)  // word qw: elements 8qw..8qw+7, block 4 half + qw/2
-            e2m1x8_scaled(w[qw], e4m3_scale2(slo, shi, 4 * half + (qw >> 1)),
-                          *reinterpret_cast<uint32_t(*)[4]>(&h[4 * qw]));
-          tmem_st32(lane_addr + TMEM_K + (uint32_t)(2 * kp + t) * 64u + (uint32_t)half * 32u, h);
-        }
-      }
-      tmem_wait_st();
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&sh.kc_empty[f]));
-        mbar_arrive(smem_u32(&sh.kt_full[kp]));
-      }
-    }
-  } else if (warp >= WARP_VW) {
-    // ---------------------------------------------------- value wideners --
-    // Follow the decisions; chunks t, t + 128, ... (row = chunk / 4) of every
-    // kept value tile.
-    const int t0 = (warp - WARP_VW) * 32 + lane;
-    int vi = 0;
-    for (int j = 0; j < nb; ++j) {
-      const int q = j >> 1, ds = q % NDP;
-      if (!(j & 1) && !mbar_wait_warp(smem_u32(&sh.dec_full[ds]), (q / NDP) & 1, abort, a.err,
-                                      kErrTimeout))
-        break;
-      const int keep = sh.dec[ds][j & 1];
-      __syncwarp();
-      if (lane == 0 && ((j & 1) || j == nb - 1)) mbar_arrive(smem_u32(&sh.dec_empty[ds]));
-      if (!keep) continue;
-      const int f = vi % NVF, hs = vi % NVH;
-      if (!mbar_wait_warp(smem_u32(&sh.vc_full[f]), (vi / NVF) & 1, abort, a.err, kErrTimeout))
-        break;
-      if (vi >= NVH && !mbar_wait_warp(smem_u32(&sh.vh_empty[hs]), ((vi / NVH) - 1) & 1, abort,
-                                       a.err, kErrTimeout))
-        break;
-#pragma unroll 2
-      for (int t = t0; t < BC * 4; t += NVW)
-        widen_value_chunk(base + SMEM_VC + f * CODE_BYTES, base + SMEM_VS + f * SC_BYTES,
-                          base + SMEM_VH + hs * H_BYTES, t);
-      fence_proxy_async_smem();  // the fp16 rows are visible to the tensor core
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(smem_u32(&sh.vc_empty[f]));
-        mbar_arrive(smem_u32(&sh.vh_full[hs]));
-      }
-      ++vi;
-    }
-  } else if (warp == WARP_QK) {
-    // --------------------------------------------------------- S^T issuer --
-    if (lane == 0) {
-      const uint64_t qd = kmajor_base(base + SMEM_Q);
-      // Blocks in pairs: one TMEM-tile barrier, one S^T buffer barrier and
-      // two commits per pair (a barrier wait between products costs about as
-      // much as a product).
-      const int npair = (nb + 1) / 2;
-      for (int q = 0; q < npair; ++q) {
-        const int kp = q % (NKT / 2), pb = q & 1;
-        const int n = 2 * q + 1 < nb ? 2 : 1;
-        if (!mbar_wait(smem_u32(&sh.kt_full[kp]), (q / (NKT / 2)) & 1, abort, a.err,
-                       kErrTimeout) ||
-            // pair buffer pb is free once the score warps have read pair q - 2
-            (q >= 2 && !mbar_wait(smem_u32(&sh.s_free[pb]), ((q >> 1) - 1) & 1, abort, a.err,
-                                  kErrTimeout)))
-          break;
-        fence_after_sync();
-        for (int t = 0; t < n; ++t) {
+      for (int e = 0; e < 2; ++e)
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk)
-            mma_bf16_ts(tmem + TMEM_S + (2 * pb + t) * NQ, tmem + TMEM_K + (2 * kp + t) * 64 + kk * 8,
-                        qd + box_step(kk), IDESC_QK, kk > 0);
-        }
-        mma_commit(smem_u32(&sh.s_full[pb]));
-        mma_commit(smem_u32(&sh.kt_empty[kp]));
-      }
-    }
-  } else if (warp == WARP_PV) {
-    // --------------------------------------------------------- O^T issuer --
-    if (lane == 0) {
-      int kc = 0;
-      for (int j = 0; j < nb && !*abort; ++j) {
-        const int q = j >> 1, ds = q % NDP;
-        if (!(j & 1) && !mbar_wait(smem_u32(&sh.dec_full[ds]), (q / NDP) & 1, abort, a.err,
-                                   kErrTimeout))
-          break;
-        const int keep = sh.dec[ds][j & 1];
-        if ((j & 1) || j == nb - 1) mbar_arrive(smem_u32(&sh.dec_empty[ds]));  // pair read
-        if (!keep) continue;
-        const int pb = kc % NPT, hs = kc % NVH;
-        if (!mbar_wait(smem_u32(&sh.p_full[pb]), (kc / NPT) & 1, abort, a.err, kErrTimeout) ||
-            !mbar_wait(smem_u32(&sh.vh_full[hs]), (kc / NVH) & 1, abort, a.err, kErrTimeout))
-          break;
-        fence_after_sync();
-        const uint64_t vd = vmajor_base(base + SMEM_VH + hs * H_BYTES);
-        const uint64_t pd = kmajor_base(base + SMEM_PT + pb * 2 * QBOX);
+        for (int i = 0; i < 4; ++i) o[mt][e][i] = 0.f;
+    // ldmatrix row addresses: lane l gives row l % 8 of matrix l / 8, whose
+    // keys are 8 further for matrices 2 and 3 and whose value dimensions are 8
+    // further for matrices 1 and 3 (the A fragment's four registers).
+    const int lm = lane >> 3, li = lane & 7;
+    const int key_off = (lm >> 1) * 8 + li;  // key within the 16-key k-step
+    uint32_t a_box[2], a_chunk[2];           // per mt: box and 16-byte chunk of the dimensions
 #pragma unroll
-        for (int kk = 0; kk < BC / 16; ++kk)
-          mma_bf16_ss(tmem + TMEM_O, vd + vmajor_step(kk), pd + box_step(kk), IDESC_PV,
-                      (kc > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(smem_u32(&sh.vh_empty[hs]));
-        mma_commit(smem_u32(&sh.p_free[pb]));
-        ++kc;
-      }
+    for (int mt = 0; mt < 2; ++mt) {
+      const int d0 = vw * 32 + mt * 16 + (lm & 1) * 8;
+      a_box[mt] = (uint32_t)(d0 >> 6) * HALF_BYTES;
+      a_chunk[mt] = (uint32_t)((d0 & 63) >> 3);
     }
-  } else {
-    // ------------------------------------------------------------- scores --
-    // Thread = key kidx of the block (TMEM lane of S^T); G scores per thread.
-    // Every thread computes the same maxima, decisions and references from
-    // the four warps' partial maxima, so the warps stay in step.
-    const int kidx = warp * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    uint32_t *bits = a.bits + (size_t)unit * a.words;
-    const float c2 = a.ln_lambda * kLog2e;  // ln(lambda), log2 units
-    float sl2[G], m2[G], mref[G], l[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      sl2[g] = sh.sl2[g];
-      m2[g] = -INFINITY;
-      mref[g] = -INFINITY;
-      l[g] = 0.f;
-    }
-    int kc = 0;
-    uint32_t word = 0;
+    const uint32_t tile = base + SMEM_VH;
     bool ok = true;
-    // Kept block: exponent references (rescaled lazily), this key's P for
-    // every head into the next P^T buffer, the per-thread row sums, an O^T
-    // rescale when a reference moved.
-    auto kept = [&](const float (&s)[G], const float (&mnew)[G]) -> bool {
-      bool rescale = false;
-      float alpha[G], p[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        alpha[g] = 1.f;
-        if (mref[g] == -INFINITY) {
-          mref[g] = mnew[g];
-        } else if (mnew[g] > mref[g] + kRescaleLog2) {
-          alpha[g] = ex2(mref[g] - mnew[g]);
-          mref[g] = mnew[g];
-          rescale = true;
-        }
-        p[g] = ex2(s[g] - mref[g]);
-        l[g] = l[g] * alpha[g] + p[g];
-      }
-      const int pb = kc % NPT;
-      // P^T buffer pb last fed the O^T product of kept block kc - NPT.
-      if (kc >= NPT && !mbar_wait_warp(smem_u32(&sh.p_free[pb]), ((kc / NPT) - 1) & 1, abort,
-                                       a.err, kErrTimeout))
-        return false;
-      {
-        // P^T[g][kidx] (fp16): box kidx / 64, row g, 16-byte chunk (kidx % 64) / 8
-        // at chunk position chunk ^ (g % 8).
-        const uint32_t box = base + SMEM_PT + (uint32_t)(pb * 2 + (kidx >> 6)) * QBOX;
-        const uint32_t kk = (uint32_t)(kidx & 63);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const uint32_t addr = box + (uint32_t)g * 128u + ((((kk >> 3) ^ (uint32_t)g)) << 4) +
-                                (kk & 7u) * 2u;
-          const unsigned short hv = __half_as_ushort(__float2half_rn(p[g]));
-          asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(hv) : "memory");
-        }
-      }
-      // O^T rescale once the previous product has landed (its commit to the
-      // P^T buffer it read); the same decision in every thread.
-      if (rescale && kc >= 1) {
-        if (!mbar_wait_warp(smem_u32(&sh.p_free[(kc - 1) % NPT]), ((kc - 1) / NPT) & 1, abort,
-                            a.err, kErrTimeout))
-          return false;
-        fence_after_sync();
-        uint32_t o[16];
-        tmem_ld16(lane_base + TMEM_O, o);
-#pragma unroll
-        for (int g = 0; g < G; ++g) o[g] = __float_as_uint(__uint_as_float(o[g]) * alpha[g]);
-        tmem_st16(lane_base + TMEM_O, o);
-        tmem_wait_st();
-      }
-      fence_proxy_async_smem();  // P^T is visible to the tensor core
-      fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[pb]));
-      ++kc;
-      return true;
-    };
-    // Decisions of pair q (thread 0): published to the value pipeline together
-    // (one barrier per pair); bitmap.
-    auto publish = [&](int q, bool skip0, bool skip1, bool two) {
-      const int ds = q % NDP;
-      // On a timeout the abort flag is raised and every later wait fails.
-      if (q < NDP || mbar_wait(smem_u32(&sh.dec_empty[ds]), ((q / NDP) - 1) & 1, abort, a.err,
-                               kErrTimeout)) {
-        sh.dec[ds][0] = skip0 ? 0 : 1;
-        sh.dec[ds][1] = skip1 ? 0 : 1;
-        mbar_arrive(smem_u32(&sh.dec_full[ds]));
-      }
-      for (int t = 0; t < (two ? 2 : 1); ++t) {
-        const int jj = 2 * q + t;
-        if (t ? skip1 : skip0) word |= 1u << (jj & 31);
-        if ((jj & 31) == 31 || jj == nb - 1) {
-          bits[jj >> 5] = word;
-          word = 0;
-        }
-      }
-    };
-    // Blocks in pairs: both S^T buffers read at once (j even, so they are
-    // adjacent), both blocks' partial maxima exchanged in one round.
-    for (int j = 0; j < nb; j += 2) {
-      const bool two = j + 1 < nb;
-      const int q = j >> 1;  // pair index
-      const int pb = q & 1, sb = 2 * pb;
-      if (!mbar_wait_warp(smem_u32(&sh.s_full[pb]), (q >> 1) & 1, abort, a.err, kErrTimeout)) {
-        ok = false;
-        break;
-      }
-      fence_after_sync();
-      uint32_t x[32];  // block j: columns [0,16); block j + 1: [16,32) (the adjacent buffer)
-      tmem_ld32(lane_base + TMEM_S + sb * NQ, x);
-      tmem_wait_ld_regs(x);
-      fence_before_sync();  // the scores are in registers: the S^T buffers are free
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.s_free[pb]));
-      const bool v0 = (j0 + j) * BC + kidx < a.L;
-      const bool v1 = two && (j0 + j + 1) * BC + kidx < a.L;
-      float s0[G], s1[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        s0[g] = v0 ? __uint_as_float(x[g]) * sl2[g] : -INFINITY;
-        s1[g] = v1 ? __uint_as_float(x[NQ + g]) * sl2[g] : -INFINITY;
-        const float m0 = warp_max(s0[g]), m1 = warp_max(s1[g]);
-        if (lane == 0) {
-          sh.red[q & 1][warp][g] = m0;
-          sh.red[q & 1][warp][8 + g] = m1;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.red_full[q & 1]));
-      if (!mbar_wait_warp(smem_u32(&sh.red_full[q & 1]), (q >> 1) & 1, abort, a.err,
+    int kc = 0;
+    for (int j = 0; j < nb; ++j) {
+      const int ds = j % NDEC;
+      if (!mbar_wait_warp(smem_u32(&sh.dec_full[ds]), (j / NDEC) & 1, abort, a.err,
                           kErrTimeout)) {
         ok = false;
         break;
       }
-      // Block maxima per head; with c < 0, "rowmax - m_new < c" is "rowmax -
-      // m_old < c" (a block that raises the max fails both).  Every head must
-      // vote skip.  Block j + 1 is tested against the max after block j.
-      bool skip0 = true, skip1 = true;
-      float mn0[G], mn1[G];
+      const int keep = sh.dec[ds];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.dec_empty[ds]));
+      if (!keep) continue;
+      const int f = kc % NVF, pb = kc % NP;
+      if (!mbar_wait_warp(smem_u32(&sh.vc_full[f]), (kc / NVF) & 1, abort, a.err, kErrTimeout)) {
+        ok = false;
+        break;
+      }
+      // This warp's value dimensions (code chunk vw) of all 128 keys into its
+      // own columns of the fp16 tile, which only it reads: the previous
+      // block's reads of them are done (its products have completed).
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float b0 = fmaxf(fmaxf(sh.red[q & 1][0][g], sh.red[q & 1][1][g]),
-                               fmaxf(sh.red[q & 1][2][g], sh.red[q & 1][3][g]));
-        const float d0 = (b0 == -INFINITY) ? -INFINITY : b0 - m2[g];
-        skip0 = skip0 && (d0 < c2);
-        mn0[g] = fmaxf(m2[g], b0);
-        const float b1 = fmaxf(fmaxf(sh.red[q & 1][0][8 + g], sh.red[q & 1][1][8 + g]),
-                               fmaxf(sh.red[q & 1][2][8 + g], sh.red[q & 1][3][8 + g]));
-        const float d1 = (b1 == -INFINITY) ? -INFINITY : b1 - mn0[g];
-        skip1 = skip1 && (d1 < c2);
-        mn1[g] = fmaxf(mn0[g], b1);
-        m2[g] = two ? mn1[g] : mn0[g];  // the running max advances on every block
-      }
-      if (tid == 0) publish(q, skip0, skip1, two);
-      if (!skip0 && !kept(s0, mn0)) {
+      for (int i = 0; i < 4; ++i)
+        widen_value_chunk(base + SMEM_VC + f * CODE_BYTES, base + SMEM_VS + f * SC_BYTES, tile,
+                          (lane + 32 * i) * 4 + vw);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.vc_empty[f]));  // the codes are read
+      if (!mbar_wait_warp(smem_u32(&sh.p_full[pb]), (kc / NP) & 1, abort, a.err, kErrTimeout)) {
         ok = false;
         break;
       }
-      if (two && !skip1 && !kept(s1, mn1)) {
-        ok = false;
-        break;
+      const float al0 = sh.alpha[pb][2 * q], al1 = sh.alpha[pb][2 * q + 1];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          o[mt][e][0] *= al0;
+          o[mt][e][1] *= al1;
+          o[mt][e][2] *= al0;
+          o[mt][e][3] *= al1;
+        }
+      const uint32_t pbuf = base + SMEM_P + pb * P_BYTES;
+#pragma unroll
+      for (int ks = 0; ks < BC / 16; ++ks) {
+        // B = P^T: keys 16ks + 2q, +1 (b0) and 16ks + 8 + 2q, +1 (b1) of head g
+        // (lanes 0-7 address the first 8 keys' rows, lanes 8-15 the next 8).
+        uint32_t b0, b1;
+        ldsm_x2(pbuf + (uint32_t)li * P_ROW + (uint32_t)(16 * ks + (lm & 1) * 8) * 2u, b0, b1);
+        const int key = 16 * ks + key_off;
+        const uint32_t row = tile + (uint32_t)key * 128u;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          uint32_t av[4];
+          ldsm_x4_trans(row + a_box[mt] + ((a_chunk[mt] ^ (uint32_t)(key & 7)) << 4), av);
+          mma16816(o[mt][ks & 1], av, b0, b1);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.p_free[pb]));  // P^T is read
+      ++kc;
+    }
+    // ---- epilogue: O_s = v_scale * O / l per head (the score warps' sums) ----
+    if (ok) ok = mbar_wait_warp(smem_u32(&sh.l_full), 0, abort, a.err, kErrTimeout);
+    if (ok) {
+      const float vs = __ldg(a.v_scale + zkv);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int h = 2 * q + c;
+        if (h < G) {
+          const float lt = (sh.lsum[0][h] + sh.lsum[1][h]) + (sh.lsum[2][h] + sh.lsum[3][h]);
+          const float sc = vs / lt;
+          float *orow = a.o_part + ((size_t)(b * a.Hq + hk * G + h) * a.n_splits + sp) * D;
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            const int d0 = vw * 32 + mt * 16 + g;
+            orow[d0] = (o[mt][0][c] + o[mt][1][c]) * sc;
+            orow[d0 + 8] = (o[mt][0][2 + c] + o[mt][1][2 + c]) * sc;
+          }
+        }
       }
     }
-
-    // ---- epilogue: O_s = v_scale * O / l and LSE_s = ref + ln l per head ----
+  } else {
+    // ------------------------------------------------------------- scores --
+    // Keys 32 warp + 16 mt + g and + 8 of each block, heads 2q, 2q + 1.
+    // The query fragments (B) of all eight k-steps: head g, elements
+    // 32q .. 32q + 31 as fp16 pairs after the head's power-of-two scale.
+    uint32_t qb[16];
+    float sl2h[2];  // raw score -> log2 units, heads 2q, 2q + 1
+    {
+      uint4 v[4] = {};
+      if (g < G) {
+        const uint4 *src = reinterpret_cast<const uint4 *>((const __nv_bfloat16 *)a.q +
+                                                           (size_t)(b * a.Hq + hk * G + g) * D) +
+                           4 * q;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = __ldg(src + i);
+      }
+      const uint32_t pr[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
+                               v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
+      uint32_t amax_bits = 0;  // |bf16| bit patterns order like their values
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        amax_bits = max(amax_bits, max(pr[i] & 0x7fffu, (pr[i] >> 16) & 0x7fffu));
+      // The four lanes of head g hold its 128 elements.
+      amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, 1));
+      amax_bits = max(amax_bits, __shfl_xor_sync(0xffffffffu, amax_bits, 2));
+      const float amax = __uint_as_float(amax_bits << 16);
+      int ex = 0;
+      const float fr = frexpf(amax > 0.f ? amax : 1.f, &ex);  // amax = fr * 2^ex
+      const int qexp = amax > 0.f ? 15 - (fr == 0.5f ? ex - 1 : ex) : 0;  // 15 - ceil(log2 amax)
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        qb[i] = pack_f16x2(ldexpf(__uint_as_float(pr[i] << 16), qexp),
+                           ldexpf(__uint_as_float(pr[i] & 0xffff0000u), qexp));
+      const float kscale = a.scale * __ldg(a.k_scale + zkv) * kLog2e;
+#pragma unroll
+      for (int c = 0; c < 2; ++c)  // head 2q + c: its exponent is in lanes 4 (2q + c) ..
+        sl2h[c] = ldexpf(kscale, -__shfl_sync(0xffffffffu, qexp, 4 * (2 * q + c)));
+    }
+    uint32_t *bits = a.bits + (size_t)unit * a.words;
+    const float c2 = a.ln_lambda * kLog2e;  // ln(lambda), log2 units
+    // Running max and exp reference of this thread's heads 2q, 2q + 1 (heads
+    // past G vote skip and are never used).
+    float m2[2] = {-INFINITY, -INFINITY}, mref[2] = {-INFINITY, -INFINITY};
+    bool hv[2];
+#pragma unroll
+    for (int c = 0; c < 2; ++c) hv[c] = 2 * q + c < G;
+    float lp[2] = {0.f, 0.f};  // this thread's part of the row sums, heads 2q, 2q + 1
+    int kc = 0;
+    uint32_t word = 0;
+    bool ok = true;
+    for (int j = 0; j < nb; ++j) {
+      const int f = j % NKF;
+      if (!mbar_wait_warp(smem_u32(&sh.kc_full[f]), (j / NKF) & 1, abort, a.err, kErrTimeout)) {
+        ok = false;
+        break;
+      }
+      // Rows r and r + 8 of each 16-key product: code bytes 16q .. 16q + 15
+      // (elements 32q .. 32q + 31) and their two block scales (2q, 2q + 1).
+      const uint32_t codes = base + SMEM_KC + f * CODE_BYTES;
+      const uint32_t scales = base + SMEM_KS + f * SC_BYTES;
+      uint4 cw[2][2];
+      uint32_t sw[2][2];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int r = warp * 32 + mt * 16 + hr * 8 + g;
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(cw[mt][hr].x), "=r"(cw[mt][hr].y), "=r"(cw[mt][hr].z),
+                         "=r"(cw[mt][hr].w)
+                       : "r"(codes + (uint32_t)r * CODE_ROW + 16u * (uint32_t)q));
+          asm volatile("ld.shared.u16 %0, [%1];"
+                       : "=r"(sw[mt][hr])
+                       : "r"(scales + (uint32_t)r * SC_ROW + 2u * (uint32_t)q));
+        }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.kc_empty[f]));  // the stage is in registers
+      // S, with two accumulators per product (even and odd k-steps) so that
+      // the chains of dependent products are half as long.
+      float acc[2][2][4];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[mt][e][i] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        uint32_t s0[2], s1[2];  // per row (r, r + 8): scale pairs of blocks 2q, 2q + 1
+        e4m3_scale_pairs(sw[mt][0], s0[0], s1[0]);
+        e4m3_scale_pairs(sw[mt][1], s0[1], s1[1]);
+        const uint32_t w0[4] = {cw[mt][0].x, cw[mt][0].y, cw[mt][0].z, cw[mt][0].w};
+        const uint32_t w1[4] = {cw[mt][1].x, cw[mt][1].y, cw[mt][1].z, cw[mt][1].w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          // Word m: k-steps 2m (bytes 0, 1) and 2m + 1 (bytes 2, 3); elements
+          // 32q + 8m .. + 7, block scale 2q for m < 2, 2q + 1 after.
+          uint32_t h0[4], h1[4];
+          e2m1x8_scaled(w0[m], m < 2 ? s0[0] : s1[0], h0);
+          e2m1x8_scaled(w1[m], m < 2 ? s0[1] : s1[1], h1);
+          const uint32_t a0[4] = {h0[0], h1[0], h0[1], h1[1]};
+          const uint32_t a1[4] = {h0[2], h1[2], h0[3], h1[3]};
+          mma16816(acc[mt][0], a0, qb[4 * m], qb[4 * m + 1]);
+          mma16816(acc[mt][1], a1, qb[4 * m + 2], qb[4 * m + 3]);
+        }
+      }
+      // Scores in log2 units (keys past L: -inf) and this thread's maxima
+      // over its four keys, heads 2q, 2q + 1.
+      float s[2][4];
+      float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int key = (j0 + j) * BC + warp * 32 + mt * 16 + (i >> 1) * 8 + g;
+          const float v = (acc[mt][0][i] + acc[mt][1][i]) * sl2h[i & 1];
+          s[mt][i] = key < a.L ? v : -INFINITY;
+          mx[i & 1] = fmaxf(mx[i & 1], s[mt][i]);
+        }
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
+        mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
+        mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
+      }
+      if (g == 0) {
+        sh.red[j & 1][warp][2 * q] = mx[0];
+        sh.red[j & 1][warp][2 * q + 1] = mx[1];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.red_full[j & 1]));
+      if (!mbar_wait_warp(smem_u32(&sh.red_full[j & 1]), (j >> 1) & 1, abort, a.err,
+                          kErrTimeout)) {
+        ok = false;
+        break;
+      }
+      // Block maxima of this thread's heads; with c < 0, "rowmax - m_new < c"
+      // is "rowmax - m_old < c" (a block that raises the max fails both).
+      // Every head must vote skip: the four lanes of a row group hold all
+      // eight heads, and every warp takes the same decision.
+      bool mine = true;
+      float mnew[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int h = 2 * q + c;
+        const float bm = fmaxf(fmaxf(sh.red[j & 1][0][h], sh.red[j & 1][1][h]),
+                               fmaxf(sh.red[j & 1][2][h], sh.red[j & 1][3][h]));
+        const float d = (bm == -INFINITY) ? -INFINITY : bm - m2[c];
+        mine = mine && (!hv[c] || d < c2);
+        mnew[c] = fmaxf(m2[c], bm);
+        m2[c] = mnew[c];  // the running max advances on every block
+      }
+      const bool skip = __all_sync(0xffffffffu, mine);
+      if (tid == 0) {
+        const int ds = j % NDEC;
+        // On a timeout the abort flag is raised and every later wait fails.
+        if (j < NDEC || mbar_wait(smem_u32(&sh.dec_empty[ds]), ((j / NDEC) - 1) & 1, abort, a.err,
+                                  kErrTimeout)) {
+          sh.dec[ds] = skip ? 0 : 1;
+          mbar_arrive(smem_u32(&sh.dec_full[ds]));
+        }
+        if (skip) word |= 1u << (j & 31);
+        if ((j & 31) == 31 || j == nb - 1) {
+          bits[j >> 5] = word;
+          word = 0;
+        }
+      }
+      if (skip) continue;
+      // Kept: exponent references (rescaled lazily; the factors go to the
+      // value warps with P^T), P^T of this thread's keys, row sums.
+      const int pb = kc % NP;
+      if (kc >= NP && !mbar_wait_warp(smem_u32(&sh.p_free[pb]), ((kc / NP) - 1) & 1, abort,
+                                       a.err, kErrTimeout)) {
+        ok = false;
+        break;
+      }
+      float alpha[2];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        alpha[c] = 1.f;
+        if (mref[c] == -INFINITY) {
+          mref[c] = mnew[c];
+        } else if (mnew[c] > mref[c] + kRescaleLog2) {
+          alpha[c] = ex2(mref[c] - mnew[c]);
+          mref[c] = mnew[c];
+        }
+        lp[c] *= alpha[c];
+      }
+      if (warp == 0 && g == 0) {  // heads 2q, 2q + 1 (1 past G)
+        sh.alpha[pb][2 * q] = hv[0] ? alpha[0] : 1.f;
+        sh.alpha[pb][2 * q + 1] = hv[1] ? alpha[1] : 1.f;
+      }
+      const uint32_t pbuf = base + SMEM_P + pb * P_BYTES;
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int c = i & 1, h = 2 * q + c;
+          if (h < G) {
+            const int key = warp * 32 + mt * 16 + (i >> 1) * 8 + g;
+            const float p = ex2(s[mt][i] - mref[c]);
+            lp[c] += p;
+            const unsigned short hv = __half_as_ushort(__float2half_rn(p));
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(pbuf + (uint32_t)h * P_ROW +
+                                                        (uint32_t)key * 2u),
+                         "h"(hv)
+                         : "memory");
+          }
+        }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[pb]));
+      ++kc;
+    }
+    // ---- epilogue: row sums per head to the value warps, LSE_s = ref + ln l ----
     if (tid == 0)
       for (int w = ((nb - 1) >> 5) + 1; w < a.words; ++w) bits[w] = 0u;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float v = l[g];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-      if (lane == 0) sh.lsum[warp][g] = v;
+    for (int c = 0; c < 2; ++c) {
+      lp[c] += __shfl_xor_sync(0xffffffffu, lp[c], 4);
+      lp[c] += __shfl_xor_sync(0xffffffffu, lp[c], 8);
+      lp[c] += __shfl_xor_sync(0xffffffffu, lp[c], 16);
+    }
+    if (g == 0) {
+      sh.lsum[warp][2 * q] = lp[0];
+      sh.lsum[warp][2 * q + 1] = lp[1];
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&sh.l_full));
     if (ok) ok = mbar_wait_warp(smem_u32(&sh.l_full), 0, abort, a.err, kErrTimeout);
-    if (ok && kc > 0)  // the last product has landed
-      ok = mbar_wait_warp(smem_u32(&sh.p_free[(kc - 1) % NPT]), ((kc - 1) / NPT) & 1, abort,
-                          a.err, kErrTimeout);
-    if (ok) {
-      fence_after_sync();
-      uint32_t o[16];
-      tmem_ld16(lane_base + TMEM_O, o);  // thread = value dimension d = kidx
-      const float vs = __ldg(a.v_scale + zkv);
+    if (ok && warp == 0 && g == 0) {
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float lt = (sh.lsum[0][g] + sh.lsum[1][g]) + (sh.lsum[2][g] + sh.lsum[3][g]);
-        const size_t row = (size_t)(b * a.Hq + hk * G + g) * a.n_splits + sp;
-        a.o_part[row * D + kidx] = __uint_as_float(o[g]) * (vs / lt);
-        if (tid == 0) a.lse_part[row] = mref[g] * kLn2 + logf(lt);
+      for (int c = 0; c < 2; ++c) {
+        const int h = 2 * q + c;
+        if (hv[c]) {
+          const float lt = (sh.lsum[0][h] + sh.lsum[1][h]) + (sh.lsum[2][h] + sh.lsum[3][h]);
+          a.lse_part[(size_t)(b * a.Hq + hk * G + h) * a.n_splits + sp] = mref[c] * kLn2 + logf(lt);
+        }
       }
     }
   }
 
   __syncwarp();
-  fence_before_sync();
   __syncthreads();
-  if (warp == WARP_QK) {
-    fence_after_sync();
-    tmem_dealloc(tmem, TMEM_COLS);
-  }
 }
 
 }  // namespace
@@ -785,9 +708,12 @@ __global__ void __launch_bounds__(NT, 1)
 cudaError_t launch_decode_nvfp4(const DecodeArgs &a, cudaStream_t s) {
   CUtensorMap mk, mv;
   // [B*Hkv, L, 64] bytes of E2M1 codes with the caller's row stride (bytes);
-  // boxes of 64 bytes x 128 keys, 64-byte swizzle; keys past L read as zero.
+  // boxes of 64 bytes x 128 keys, keys past L read as zero.  Key tiles land
+  // unswizzled (the score lanes' 16-byte loads at 16q of rows r, r + 1 of
+  // each eight-lane phase meet no bank twice); value tiles with the 64-byte
+  // swizzle (one widening thread per row chunk).
   if (!make_map_u8_3d(&mk, a.k, CODE_ROW, a.k_row_stride, a.L, a.B * a.Hkv, BC,
-                      CU_TENSOR_MAP_SWIZZLE_64B) ||
+                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
       !make_map_u8_3d(&mv, a.v, CODE_ROW, a.v_row_stride, a.L, a.B * a.Hkv, BC,
                       CU_TENSOR_MAP_SWIZZLE_64B))
     return cudaErrorInvalidValue;
