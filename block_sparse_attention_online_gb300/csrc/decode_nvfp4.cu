@@ -37,8 +37,9 @@
 //
 // One CTA per (sequence, KV head, split).  Warp roles (320 threads):
 //   warps 0-3  scores: warp w owns keys 32w .. 32w + 31 of every block (two
-//              16-key products per k-step); block maxima per head, the
-//              decision (every head votes skip), exponentials, P^T, row sums;
+//              16-key products per k-step); blocks in pairs: both blocks'
+//              products, one exchange of the four warps' maxima per head, both
+//              decisions (every head votes skip), exponentials, P^T, row sums;
 //   warps 4-7  values: warp 4 + w owns value dimensions 32w .. 32w + 31 (two
 //              16-row products per k-step) of O^T; it widens those columns
 //              of every kept value tile into its own part of one fp16 tile,
@@ -48,9 +49,10 @@
 //   warp 9     value producer, kept blocks only.
 // Two CTAs share an SM (104 KB of shared memory, <= 102 registers a thread),
 // so one CTA's per-block latencies (loads, product chains, the score warps'
-// exchange) overlap the other's.  Every wait inside the loops is a bounded
-// mbarrier wait (no CTA-wide or named barrier), so a failed wait ends every
-// role's loop with an error status instead of a hang.
+// exchange) overlap the other's.  Every other wait inside the loops is a
+// bounded mbarrier wait, so a failed wait ends the roles' loops with an
+// error status instead of a hang; the score warps' one named barrier is met
+// equally often by all four (their loop runs to its end).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -74,6 +76,7 @@ constexpr int NSW = 4;    // score warps
 constexpr int NVW = 4;    // value warps
 constexpr int WARP_VAL = NSW, WARP_K = NSW + NVW, WARP_V = WARP_K + 1;
 constexpr int NT = (WARP_V + 1) * 32;
+constexpr int kScoreBarrier = 1;  // named barrier of the four score warps
 constexpr uint32_t CODE_ROW = D / 2;            // 64 bytes of codes per row
 constexpr uint32_t SC_ROW = D / 16;             // 8 block scales per row
 constexpr uint32_t CODE_BYTES = BC * CODE_ROW;  // 8 KB
@@ -102,10 +105,9 @@ struct Shared {
   uint64_t vc_full[NVF], vc_empty[NVF];
   uint64_t p_full[NP], p_free[NP];
   uint64_t dec_full[NDEC], dec_empty[NDEC];
-  uint64_t red_full[2];  // the score warps' partial maxima of a block are in
   uint64_t l_full;       // the score warps' row sums are in
   int dec[NDEC];
-  float red[2][NSW][8];  // per block (double buffered): per score warp, per head max
+  float red[2][NSW][16];  // per block pair (double buffered): per score warp, block, head max
   float alpha[NP][8];    // per P^T buffer: the heads' O^T rescale factors
   float lsum[NSW][8];    // epilogue: per score warp, per head row sum
   int abort;
@@ -289,8 +291,6 @@ __global__ void __launch_bounds__(NT, 2)
       mbar_init(smem_u32(&sh.dec_full[i]), 1);
       mbar_init(smem_u32(&sh.dec_empty[i]), 1 + NVW);  // the value producer, the value warps
     }
-    mbar_init(smem_u32(&sh.red_full[0]), NSW);
-    mbar_init(smem_u32(&sh.red_full[1]), NSW);
     mbar_init(smem_u32(&sh.l_full), NSW);
     sh.abort = 0;
     fence_mbar_init();
@@ -508,168 +508,196 @@ __global__ void __launch_bounds__(NT, 2)
     int kc = 0;
     uint32_t word = 0;
     bool ok = true;
-    for (int j = 0; j < nb; ++j) {
-      const int f = j % NKF;
-      if (!mbar_wait_warp(smem_u32(&sh.kc_full[f]), (j / NKF) & 1, abort, a.err, kErrTimeout)) {
-        ok = false;
-        break;
-      }
-      // Rows r and r + 8 of each 16-key product: code bytes 16q .. 16q + 15
-      // (elements 32q .. 32q + 31) and their two block scales (2q, 2q + 1).
-      const uint32_t codes = base + SMEM_KC + f * CODE_BYTES;
-      const uint32_t scales = base + SMEM_KS + f * SC_BYTES;
-      uint4 cw[2][2];
-      uint32_t sw[2][2];
+    // Blocks in pairs: both blocks' products, then one exchange of the four
+    // warps' maxima and both decisions (block j + 1 is tested against the
+    // running max after block j).
+    for (int j = 0; j < nb; j += 2) {
+      const int np = j + 1 < nb ? 2 : 1;
+      const int pr = (j >> 1) & 1;  // exchange buffer of this pair
+      float s[2][2][4];             // [block][mt][fragment]: scores in log2 units, -inf past L
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
+      for (int t = 0; t < 2; ++t) {
 #pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int r = warp * 32 + mt * 16 + hr * 8 + g;
-          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(cw[mt][hr].x), "=r"(cw[mt][hr].y), "=r"(cw[mt][hr].z),
-                         "=r"(cw[mt][hr].w)
-                       : "r"(codes + (uint32_t)r * CODE_ROW + 16u * (uint32_t)q));
-          asm volatile("ld.shared.u16 %0, [%1];"
-                       : "=r"(sw[mt][hr])
-                       : "r"(scales + (uint32_t)r * SC_ROW + 2u * (uint32_t)q));
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) s[t][mt][i] = -INFINITY;
+        if ((t == 1 && np == 1) || !ok) break;
+        const int jj = j + t, f = jj % NKF;
+        if (!mbar_wait_warp(smem_u32(&sh.kc_full[f]), (jj / NKF) & 1, abort, a.err,
+                            kErrTimeout)) {
+          ok = false;
+          break;
         }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.kc_empty[f]));  // the stage is in registers
-      // S, with two accumulators per product (even and odd k-steps) so that
-      // the chains of dependent products are half as long.
-      float acc[2][2][4];
+        // Rows r and r + 8 of each 16-key product: code bytes 16q .. 16q + 15
+        // (elements 32q .. 32q + 31) and their two block scales (2q, 2q + 1).
+        const uint32_t codes = base + SMEM_KC + f * CODE_BYTES;
+        const uint32_t scales = base + SMEM_KS + f * SC_BYTES;
+        uint4 cw[2][2];
+        uint32_t sw[2][2];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int e = 0; e < 2; ++e)
+          for (int hr = 0; hr < 2; ++hr) {
+            const int r = warp * 32 + mt * 16 + hr * 8 + g;
+            asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(cw[mt][hr].x), "=r"(cw[mt][hr].y), "=r"(cw[mt][hr].z),
+                           "=r"(cw[mt][hr].w)
+                         : "r"(codes + (uint32_t)r * CODE_ROW + 16u * (uint32_t)q));
+            asm volatile("ld.shared.u16 %0, [%1];"
+                         : "=r"(sw[mt][hr])
+                         : "r"(scales + (uint32_t)r * SC_ROW + 2u * (uint32_t)q));
+          }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.kc_empty[f]));  // the stage is in registers
+        // S, with two accumulators per product (even and odd k-steps) so that
+        // the chains of dependent products are half as long.
+        float acc[2][2][4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) acc[mt][e][i] = 0.f;
+        for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        uint32_t s0[2], s1[2];  // per row (r, r + 8): scale pairs of blocks 2q, 2q + 1
-        e4m3_scale_pairs(sw[mt][0], s0[0], s1[0]);
-        e4m3_scale_pairs(sw[mt][1], s0[1], s1[1]);
-        const uint32_t w0[4] = {cw[mt][0].x, cw[mt][0].y, cw[mt][0].z, cw[mt][0].w};
-        const uint32_t w1[4] = {cw[mt][1].x, cw[mt][1].y, cw[mt][1].z, cw[mt][1].w};
+          for (int e = 0; e < 2; ++e)
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          // Word m: k-steps 2m (bytes 0, 1) and 2m + 1 (bytes 2, 3); elements
-          // 32q + 8m .. + 7, block scale 2q for m < 2, 2q + 1 after.
-          uint32_t h0[4], h1[4];
-          e2m1x8_scaled(w0[m], m < 2 ? s0[0] : s1[0], h0);
-          e2m1x8_scaled(w1[m], m < 2 ? s0[1] : s1[1], h1);
-          const uint32_t a0[4] = {h0[0], h1[0], h0[1], h1[1]};
-          const uint32_t a1[4] = {h0[2], h1[2], h0[3], h1[3]};
-          mma16816(acc[mt][0], a0, qb[4 * m], qb[4 * m + 1]);
-          mma16816(acc[mt][1], a1, qb[4 * m + 2], qb[4 * m + 3]);
+            for (int i = 0; i < 4; ++i) acc[mt][e][i] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          uint32_t s0[2], s1[2];  // per row (r, r + 8): scale pairs of blocks 2q, 2q + 1
+          e4m3_scale_pairs(sw[mt][0], s0[0], s1[0]);
+          e4m3_scale_pairs(sw[mt][1], s0[1], s1[1]);
+          const uint32_t w0[4] = {cw[mt][0].x, cw[mt][0].y, cw[mt][0].z, cw[mt][0].w};
+          const uint32_t w1[4] = {cw[mt][1].x, cw[mt][1].y, cw[mt][1].z, cw[mt][1].w};
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            // Word m: k-steps 2m (bytes 0, 1) and 2m + 1 (bytes 2, 3); elements
+            // 32q + 8m .. + 7, block scale 2q for m < 2, 2q + 1 after.
+            uint32_t h0[4], h1[4];
+            e2m1x8_scaled(w0[m], m < 2 ? s0[0] : s1[0], h0);
+            e2m1x8_scaled(w1[m], m < 2 ? s0[1] : s1[1], h1);
+            const uint32_t a0[4] = {h0[0], h1[0], h0[1], h1[1]};
+            const uint32_t a1[4] = {h0[2], h1[2], h0[3], h1[3]};
+            mma16816(acc[mt][0], a0, qb[4 * m], qb[4 * m + 1]);
+            mma16816(acc[mt][1], a1, qb[4 * m + 2], qb[4 * m + 3]);
+          }
         }
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int key = (j0 + jj) * BC + warp * 32 + mt * 16 + (i >> 1) * 8 + g;
+            const float v = (acc[mt][0][i] + acc[mt][1][i]) * sl2h[i & 1];
+            s[t][mt][i] = key < a.L ? v : -INFINITY;
+          }
       }
-      // Scores in log2 units (keys past L: -inf) and this thread's maxima
-      // over its four keys, heads 2q, 2q + 1.
-      float s[2][4];
-      float mx[2] = {-INFINITY, -INFINITY};
+      // This thread's maxima over its four keys of each block, heads 2q,
+      // 2q + 1, then over the warp's row groups; the four warps' exchange.
+      float mx[2][2];
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
+      for (int t = 0; t < 2; ++t)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int key = (j0 + j) * BC + warp * 32 + mt * 16 + (i >> 1) * 8 + g;
-          const float v = (acc[mt][0][i] + acc[mt][1][i]) * sl2h[i & 1];
-          s[mt][i] = key < a.L ? v : -INFINITY;
-          mx[i & 1] = fmaxf(mx[i & 1], s[mt][i]);
+        for (int c = 0; c < 2; ++c) {
+          float m = fmaxf(fmaxf(s[t][0][c], s[t][0][2 + c]), fmaxf(s[t][1][c], s[t][1][2 + c]));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+          m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+          mx[t][c] = m;
         }
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 4));
-        mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 8));
-        mx[c] = fmaxf(mx[c], __shfl_xor_sync(0xffffffffu, mx[c], 16));
-      }
       if (g == 0) {
-        sh.red[j & 1][warp][2 * q] = mx[0];
-        sh.red[j & 1][warp][2 * q + 1] = mx[1];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          sh.red[pr][warp][8 * t + 2 * q] = mx[t][0];
+          sh.red[pr][warp][8 * t + 2 * q + 1] = mx[t][1];
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.red_full[j & 1]));
-      if (!mbar_wait_warp(smem_u32(&sh.red_full[j & 1]), (j >> 1) & 1, abort, a.err,
-                          kErrTimeout)) {
-        ok = false;
-        break;
-      }
+      // The four score warps meet on a named barrier once per pair, whatever
+      // happened before: after a failed wait a warp skips the work but not
+      // the barrier, so none waits for ever.  (A warp writes buffer pr again
+      // two pairs later, after the next barrier, when every warp has read it.)
+      named_bar_sync(kScoreBarrier, NSW * 32);
+      if (!ok) continue;
       // Block maxima of this thread's heads; with c < 0, "rowmax - m_new < c"
       // is "rowmax - m_old < c" (a block that raises the max fails both).
       // Every head must vote skip: the four lanes of a row group hold all
-      // eight heads, and every warp takes the same decision.
-      bool mine = true;
-      float mnew[2];
+      // eight heads, and every warp takes the same decisions.
+      bool skip[2] = {true, true};
+      float mnew[2][2];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int h = 2 * q + c;
-        const float bm = fmaxf(fmaxf(sh.red[j & 1][0][h], sh.red[j & 1][1][h]),
-                               fmaxf(sh.red[j & 1][2][h], sh.red[j & 1][3][h]));
-        const float d = (bm == -INFINITY) ? -INFINITY : bm - m2[c];
-        mine = mine && (!hv[c] || d < c2);
-        mnew[c] = fmaxf(m2[c], bm);
-        m2[c] = mnew[c];  // the running max advances on every block
+      for (int t = 0; t < 2; ++t) {
+        bool mine = true;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int h = 8 * t + 2 * q + c;
+          const float bm = fmaxf(fmaxf(sh.red[pr][0][h], sh.red[pr][1][h]),
+                                 fmaxf(sh.red[pr][2][h], sh.red[pr][3][h]));
+          const float d = (bm == -INFINITY) ? -INFINITY : bm - m2[c];
+          mine = mine && (!hv[c] || d < c2);
+          mnew[t][c] = fmaxf(m2[c], bm);
+          if (t < np) m2[c] = mnew[t][c];  // the running max advances on every block
+        }
+        skip[t] = __all_sync(0xffffffffu, mine);
       }
-      const bool skip = __all_sync(0xffffffffu, mine);
       if (tid == 0) {
-        const int ds = j % NDEC;
-        // On a timeout the abort flag is raised and every later wait fails.
-        if (j < NDEC || mbar_wait(smem_u32(&sh.dec_empty[ds]), ((j / NDEC) - 1) & 1, abort, a.err,
-                                  kErrTimeout)) {
-          sh.dec[ds] = skip ? 0 : 1;
-          mbar_arrive(smem_u32(&sh.dec_full[ds]));
-        }
-        if (skip) word |= 1u << (j & 31);
-        if ((j & 31) == 31 || j == nb - 1) {
-          bits[j >> 5] = word;
-          word = 0;
-        }
-      }
-      if (skip) continue;
-      // Kept: exponent references (rescaled lazily; the factors go to the
-      // value warps with P^T), P^T of this thread's keys, row sums.
-      const int pb = kc % NP;
-      if (kc >= NP && !mbar_wait_warp(smem_u32(&sh.p_free[pb]), ((kc / NP) - 1) & 1, abort,
-                                       a.err, kErrTimeout)) {
-        ok = false;
-        break;
-      }
-      float alpha[2];
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        alpha[c] = 1.f;
-        if (mref[c] == -INFINITY) {
-          mref[c] = mnew[c];
-        } else if (mnew[c] > mref[c] + kRescaleLog2) {
-          alpha[c] = ex2(mref[c] - mnew[c]);
-          mref[c] = mnew[c];
-        }
-        lp[c] *= alpha[c];
-      }
-      if (warp == 0 && g == 0) {  // heads 2q, 2q + 1 (1 past G)
-        sh.alpha[pb][2 * q] = hv[0] ? alpha[0] : 1.f;
-        sh.alpha[pb][2 * q + 1] = hv[1] ? alpha[1] : 1.f;
-      }
-      const uint32_t pbuf = base + SMEM_P + pb * P_BYTES;
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int c = i & 1, h = 2 * q + c;
-          if (h < G) {
-            const int key = warp * 32 + mt * 16 + (i >> 1) * 8 + g;
-            const float p = ex2(s[mt][i] - mref[c]);
-            lp[c] += p;
-            const unsigned short hv = __half_as_ushort(__float2half_rn(p));
-            asm volatile("st.shared.u16 [%0], %1;" ::"r"(pbuf + (uint32_t)h * P_ROW +
-                                                        (uint32_t)key * 2u),
-                         "h"(hv)
-                         : "memory");
+        for (int t = 0; t < np; ++t) {
+          const int jj = j + t, ds = jj % NDEC;
+          // On a timeout the abort flag is raised and every later wait fails.
+          if (jj < NDEC || mbar_wait(smem_u32(&sh.dec_empty[ds]), ((jj / NDEC) - 1) & 1, abort,
+                                     a.err, kErrTimeout)) {
+            sh.dec[ds] = skip[t] ? 0 : 1;
+            mbar_arrive(smem_u32(&sh.dec_full[ds]));
+          }
+          if (skip[t]) word |= 1u << (jj & 31);
+          if ((jj & 31) == 31 || jj == nb - 1) {
+            bits[jj >> 5] = word;
+            word = 0;
           }
         }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[pb]));
-      ++kc;
+      }
+      // Kept blocks: exponent references (rescaled lazily; the factors go to
+      // the value warps with P^T), P^T of this thread's keys, row sums.
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (t >= np || skip[t] || !ok) continue;
+        const int pb = kc % NP;
+        if (kc >= NP && !mbar_wait_warp(smem_u32(&sh.p_free[pb]), ((kc / NP) - 1) & 1, abort,
+                                         a.err, kErrTimeout)) {
+          ok = false;
+          continue;
+        }
+        float alpha[2];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          alpha[c] = 1.f;
+          if (mref[c] == -INFINITY) {
+            mref[c] = mnew[t][c];
+          } else if (mnew[t][c] > mref[c] + kRescaleLog2) {
+            alpha[c] = ex2(mref[c] - mnew[t][c]);
+            mref[c] = mnew[t][c];
+          }
+          lp[c] *= alpha[c];
+        }
+        if (warp == 0 && g == 0) {  // heads 2q, 2q + 1 (1 past G)
+          sh.alpha[pb][2 * q] = hv[0] ? alpha[0] : 1.f;
+          sh.alpha[pb][2 * q + 1] = hv[1] ? alpha[1] : 1.f;
+        }
+        const uint32_t pbuf = base + SMEM_P + pb * P_BYTES;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int c = i & 1, h = 2 * q + c;
+            if (h < G) {
+              const int key = warp * 32 + mt * 16 + (i >> 1) * 8 + g;
+              const float p = ex2(s[t][mt][i] - mref[c]);
+              lp[c] += p;
+              const unsigned short hv16 = __half_as_ushort(__float2half_rn(p));
+              asm volatile("st.shared.u16 [%0], %1;" ::"r"(pbuf + (uint32_t)h * P_ROW +
+                                                          (uint32_t)key * 2u),
+                           "h"(hv16)
+                           : "memory");
+            }
+          }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&sh.p_full[pb]));
+        ++kc;
+      }
     }
     // ---- epilogue: row sums per head to the value warps, LSE_s = ref + ln l ----
     if (tid == 0)
