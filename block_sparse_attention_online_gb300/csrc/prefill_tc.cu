@@ -74,6 +74,7 @@ static_assert(NK % 2 == 0 && NK > NS, "ready ring: even, and longer than the S b
 constexpr int NQ = 4;     // decider warps (0-3) and exponential warps (4-7): one per TMEM lane quarter
 constexpr int NSOFT = 2 * NQ;
 constexpr int kDeciderBarrier = 1;  // named barrier of the four decider warps
+constexpr int kSetupBarrier = 2;    // varlen set-up: the key producer and the tile-locating warp
 // Two Q.K^T issuers (even and odd blocks): a thread that issues tcgen05.mma
 // is held until the tensor pipe takes each instruction, so one issuer's
 // barrier waits between blocks leave the pipe idle; with two, one waits while
@@ -431,11 +432,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     return;
   }
 
-  // Set-up.  The key producer's lane initialises the barriers; for a fixed
-  // length batch (whose tile follows from the block index) it then issues Q
-  // and the first NK traversed key tiles at once, so that they are in flight
-  // during the rest of the set-up (the tensor-map descriptors are prefetched
-  // first thing).  It resumes after the CTA barrier at block p_j, load p_c.
+  // Set-up.  The key producer's lane initialises the barriers and then issues
+  // Q and the first NK traversed key tiles at once, so that they are in
+  // flight during the rest of the set-up (the tensor-map descriptors are
+  // prefetched first thing); it resumes after the CTA barrier at block p_j,
+  // load p_c.  A fixed-length tile follows from the block index; a varlen
+  // CTA's tile is located by the V-producer warp meanwhile, and the two warps
+  // meet on a named barrier before the loads (once each, unconditionally).
   const uint64_t keep_l2 = policy_evict_last();    // K and V are re-read by other tiles/heads
   const uint64_t stream_l2 = policy_evict_first();  // Q is read once
   int p_j = 0, p_c = 0;
@@ -465,35 +468,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     sh.abort = 0;
     fence_mbar_init();
     fence_proxy_async_smem();  // the initialised barriers, seen by this thread's TMA loads
-    if constexpr (!VARLEN) {
-      const Tile x = tile_of<false>(a, VarTile{}, (int)blockIdx.x);
-      const int zq = x.b * a.Hq + x.h, zkv = x.b * a.Hkv + x.h / (a.Hq / a.Hkv);
-      const uint32_t *sw = SET ? a.block_set + ((size_t)zq * a.n_t + x.t) * a.words : nullptr;
-      mbar_expect_tx(smem_u32(&sh.q_full), TILE_BYTES);
-      tma_load_3d(base + SMEM_Q, &tm_q, smem_u32(&sh.q_full), 0, x.row0, zq, stream_l2);
-      tma_load_3d(base + SMEM_Q + HALF_BYTES, &tm_q, smem_u32(&sh.q_full), 64, x.row0, zq,
-                  stream_l2);
-      for (; p_j < x.nblk && p_c < NK; ++p_j) {
-        if constexpr (SET) {
-          if (((__ldg(sw + (p_j >> 5)) >> (p_j & 31)) & 1u) == 0u) continue;
-        }
-        const uint32_t dst = base + SMEM_K + p_c * TILE_BYTES;
-        mbar_expect_tx(smem_u32(&sh.ready[p_c]), TILE_BYTES);
-        tma_load_3d(dst, &tm_k, smem_u32(&sh.ready[p_c]), 0, p_j * BN, zkv, keep_l2);
-        tma_load_3d(dst + HALF_BYTES, &tm_k, smem_u32(&sh.ready[p_c]), 64, p_j * BN, zkv,
-                    keep_l2);
-        ++p_c;
-      }
-    }
   }
   if (warp == WARP_MMA) tmem_alloc(smem_u32(&sh.tmem_base), TMEM_COLS);
-  // Varlen: the V-producer warp locates this CTA's tile while the barriers and
-  // TMEM are set up.
   if constexpr (VARLEN) {
     if (warp == WARP_V) {
       const int i = (int)(blockIdx.x / a.Hq), h = (int)(blockIdx.x % a.Hq);
       if (a.B > 32 || !varlen_locate_small(a, i, h, lane, &sh.vt))
         varlen_locate(a, i, (int)(gridDim.x / a.Hq), h, lane, &sh.vt);
+    }
+    if (warp == WARP_V || warp == WARP_K) named_bar_sync(kSetupBarrier, 64);
+  }
+  if (warp == WARP_K && lane == 0 && (!VARLEN || sh.vt.s >= 0)) {
+    VarTile v0{};
+    if constexpr (VARLEN) v0 = sh.vt;
+    const Tile x = tile_of<VARLEN>(a, v0, (int)blockIdx.x);
+    const int hk0 = x.h / (a.Hq / a.Hkv);
+    const int zq = x.b * a.Hq + x.h, zkv = x.b * a.Hkv + hk0;
+    const int qy = VARLEN ? x.h : x.row0, qz = VARLEN ? x.off + x.row0 : zq;
+    const uint32_t *sw = SET ? a.block_set + ((size_t)zq * a.n_t + x.t) * a.words : nullptr;
+    mbar_expect_tx(smem_u32(&sh.q_full), TILE_BYTES);
+    tma_load_3d(base + SMEM_Q, &tm_q, smem_u32(&sh.q_full), 0, qy, qz, stream_l2);
+    tma_load_3d(base + SMEM_Q + HALF_BYTES, &tm_q, smem_u32(&sh.q_full), 64, qy, qz, stream_l2);
+    for (; p_j < x.nblk && p_c < NK; ++p_j) {
+      if constexpr (SET) {
+        if (((__ldg(sw + (p_j >> 5)) >> (p_j & 31)) & 1u) == 0u) continue;
+      }
+      const int ky = VARLEN ? hk0 : p_j * BN, kz = VARLEN ? x.off + p_j * BN : zkv;
+      const uint32_t dst = base + SMEM_K + p_c * TILE_BYTES;
+      mbar_expect_tx(smem_u32(&sh.ready[p_c]), TILE_BYTES);
+      tma_load_3d(dst, &tm_k, smem_u32(&sh.ready[p_c]), 0, ky, kz, keep_l2);
+      tma_load_3d(dst + HALF_BYTES, &tm_k, smem_u32(&sh.ready[p_c]), 64, ky, kz, keep_l2);
+      ++p_c;
     }
   }
   fence_before_sync();
@@ -515,11 +520,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const float ln_lam = tile.ln_lam;
   const int row0 = tile.row0, nblk = tile.nblk;
   volatile int *abort = &sh.abort;
-  const int zq = b * a.Hq + h, zkv = b * a.Hkv + hk;
-  // TMA coordinates (column, y, z) of query rows / key block j: [heads, T, 128]
-  // maps take (row, head); the token-major varlen maps [total, heads, 128]
-  // take (head, token).
-  const int q_y = VARLEN ? h : row0, q_z = VARLEN ? off + row0 : zq;
+  const int zkv = b * a.Hkv + hk;
+  // TMA coordinates (column, y, z) of key block j: [heads, T, 128] maps take
+  // (row, head); the token-major varlen maps [total, heads, 128] take (head,
+  // token).  (Q's, the same, are taken in the set-up.)
   auto kv_y = [&](int j) { return VARLEN ? hk : j * BN; };
   auto kv_z = [&](int j) { return VARLEN ? off + j * BN : zkv; };
   const uint32_t *set_words = SET ? a.block_set + ((size_t)bh * a.n_t + t) * a.words : nullptr;
@@ -531,12 +535,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   } else if (warp == WARP_K) {
     // -------------------------------------------------------- Q/K producer --
     if (lane == 0) {
-      if constexpr (VARLEN) {  // the tile is known only now
-        mbar_expect_tx(smem_u32(&sh.q_full), TILE_BYTES);
-        tma_load_3d(base + SMEM_Q, &tm_q, smem_u32(&sh.q_full), 0, q_y, q_z, stream_l2);
-        tma_load_3d(base + SMEM_Q + HALF_BYTES, &tm_q, smem_u32(&sh.q_full), 64, q_y, q_z,
-                    stream_l2);
-      }
       int ki = p_c, cc = p_c;
       for (int j = p_j; j < nblk && !*abort; ++j) {
         if constexpr (SET) {
