@@ -48,8 +48,8 @@ CSRC = os.path.join(ROOT, "block_sparse_attention_online_gb300", "csrc")
 NCU_TRAFFIC = {
     "prefill_tc_kernel": {
         "file": "prefill_tc.cu",
-        "sha256": "95590eba908696ec97d9459a69d2d6effd963a5aa5000cd604055b45ecc9dd53",
-        "bytes": 234835200 + 82129664},
+        "sha256": "860fc4c2ced66ea537075a7b808dfddaf5f8d87edf4acdfa1167f9d4e49a26b0",
+        "bytes": 234510848 + 82156544},
     "decode_tc_kernel": {
         "file": "decode.cu",
         "sha256": "67c9de81d8f8ee7ddce7a6299cee4da7e507f86994a81d430c15461053d8a9e0",
