@@ -47,7 +47,7 @@
 //   warp 8     key producer: TMA of the code tile, block scales by cp.async
 //              from its 32 lanes (zero past L);
 //   warp 9     value producer, kept blocks only.
-// Two CTAs share an SM (104 KB of shared memory, <= 102 registers a thread),
+// Two CTAs share an SM (105 KB of shared memory, <= 102 registers a thread),
 // so one CTA's per-block latencies (loads, product chains, the score warps'
 // exchange) overlap the other's.  Every other wait inside the loops is a
 // bounded mbarrier wait, so a failed wait ends the roles' loops with an
