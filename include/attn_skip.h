@@ -34,7 +34,7 @@
  *
  * Status codes: ATTN_EINVAL for a null pointer, a non-positive size, Hq not a
  * multiple of Hkv, lambda outside [0,1) or NaN, or a misaligned pointer;
- * ATTN_EUNSUPPORTED for a valid combination this build has no kernel for;
+ * ATTN_EUNSUPPORTED for a valid combination the library has no kernel for;
  * ATTN_ECUDA for a launch or CUDA runtime error (the CUDA error is cleared);
  * ATTN_ETIMEOUT when a device-side bounded wait gave up, ATTN_EINTERNAL when a
  * kernel found its dynamic shared memory placed off the 1024-byte boundary its
